@@ -1,0 +1,161 @@
+"""CPU oracle for batched speculative verification and the OPD loss.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, by ``__graft_entry__.smoke()``
+and by the CPU-baseline leg of ``bench.py``; the product path never imports it.
+
+The arithmetic lives in ``svw_oracle.c`` (plain C, binary64, sequential sums in
+vocabulary order); this module only compiles it with the host C compiler and
+marshals numpy arrays through ctypes.  See the header of ``svw_oracle.c`` for
+the passages each function follows and the readings taken where the pages are
+silent.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "svw_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+
+F32 = 0
+BF16 = 1
+
+FLAG_NEAR_ACCEPT = 1
+FLAG_NEAR_CDF = 2
+FLAG_DEGENERATE = 4
+FLAG_BAD = 8
+FLAG_NEAR_CLIP = 16
+
+_lib = None
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/_build/liboracle.so`` (no fast-math)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math",
+           "-ffp-contract=off", "-Wall", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            lib.oracle_philox4x32_10.argtypes = [P, P, P]
+            lib.oracle_philox4x32_10.restype = None
+            lib.oracle_uniform.argtypes = [ctypes.c_uint64, ctypes.c_uint32,
+                                           ctypes.c_uint32, ctypes.c_uint32]
+            lib.oracle_uniform.restype = ctypes.c_double
+            lib.oracle_spec_verify.argtypes = [
+                P, P, ctypes.c_int, ctypes.c_int64, ctypes.c_int32, P, P,
+                ctypes.c_double, ctypes.c_uint64, ctypes.c_int32, P, P, P, P, P]
+            lib.oracle_spec_verify.restype = ctypes.c_int
+            lib.oracle_opd_loss.argtypes = [
+                P, P, ctypes.c_int, ctypes.c_int64, ctypes.c_int32, P,
+                ctypes.c_int64, ctypes.c_int32, ctypes.c_double, ctypes.c_double,
+                ctypes.c_double, ctypes.c_double, P, P, P]
+            lib.oracle_opd_loss.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _logits(a):
+    """(array, dtype code): uint16 arrays are bf16 bit patterns, float32 is fp32."""
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return a, BF16
+    if a.dtype == np.float32:
+        return a, F32
+    raise TypeError(f"logits must be uint16 (bf16 bits) or float32, got {a.dtype}")
+
+
+def philox4x32_10(counter, key):
+    """Philox4x32-10 block: four 32-bit counter words, two key words -> 4 words."""
+    lib = _load()
+    c = np.ascontiguousarray(np.asarray(counter, dtype=np.uint32).reshape(4))
+    k = np.ascontiguousarray(np.asarray(key, dtype=np.uint32).reshape(2))
+    out = np.zeros(4, dtype=np.uint32)
+    lib.oracle_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def uniform(seed: int, i: int, j: int, s: int) -> float:
+    """U(seed, i, j, s): 24-bit uniform in [0, 1) from Philox word 0."""
+    return _load().oracle_uniform(seed, i, j, s)
+
+
+def spec_verify(target, draft, cu_draft, tokens, temperature, seed, max_len=32,
+                req_ids=None, want_thr=False):
+    """Verify a ragged batch.  Returns dict(accept_len, next_token, flags[, thr]).
+
+    target: [total_rows + N, V], draft: [total_rows, V] (uint16 bf16 bits or
+    float32); cu_draft: int32 [N + 1]; tokens: int32 [total_rows].
+    """
+    lib = _load()
+    t, dt = _logits(target)
+    d, dd = _logits(draft)
+    assert dt == dd, "target and draft must share a dtype"
+    V = t.shape[-1]
+    cu = np.ascontiguousarray(cu_draft, dtype=np.int32)
+    tok = np.ascontiguousarray(tokens, dtype=np.int32)
+    N = cu.shape[0] - 1
+    rid = None if req_ids is None else np.ascontiguousarray(req_ids, dtype=np.int32)
+    acc = np.zeros(N, dtype=np.int32)
+    nxt = np.zeros(N, dtype=np.int32)
+    flg = np.zeros(N, dtype=np.int32)
+    thr = np.full(max(1, tok.shape[0]), np.nan) if want_thr else None
+    rc = lib.oracle_spec_verify(_ptr(t), _ptr(d), dt, V, N, _ptr(cu), _ptr(tok),
+                                float(temperature), int(seed), int(max_len), _ptr(rid),
+                                _ptr(acc), _ptr(nxt), _ptr(flg), _ptr(thr))
+    if rc != 0:
+        raise MemoryError("oracle_spec_verify failed to allocate")
+    out = dict(accept_len=acc, next_token=nxt, flags=flg)
+    if want_thr:
+        out["thr"] = thr[: tok.shape[0]]
+    return out
+
+
+def opd_loss(target, draft, temperature=1.0, clip_c=1.0, lambda_ce=0.1, grad_scale=1.0,
+             cu_draft=None, has_bonus=False, want_grad=True):
+    """Clipped reverse-KL + lambda * CE per draft row and its gradient.
+
+    Returns dict(loss [R] f64, dlogits [R, V] f64 or None, flags [R]).
+    """
+    lib = _load()
+    t, dt = _logits(target)
+    d, dd = _logits(draft)
+    assert dt == dd, "target and draft must share a dtype"
+    R, V = d.shape
+    if has_bonus:
+        cu = np.ascontiguousarray(cu_draft, dtype=np.int32)
+        N = cu.shape[0] - 1
+    else:
+        cu, N = None, 0
+    loss = np.zeros(R, dtype=np.float64)
+    grad = np.zeros((R, V), dtype=np.float64) if want_grad else None
+    flg = np.zeros(R, dtype=np.int32)
+    rc = lib.oracle_opd_loss(_ptr(t), _ptr(d), dt, V, N, _ptr(cu), R, int(bool(has_bonus)),
+                             float(temperature), float(clip_c), float(lambda_ce),
+                             float(grad_scale), _ptr(loss), _ptr(grad), _ptr(flg))
+    if rc != 0:
+        raise MemoryError("oracle_opd_loss failed to allocate")
+    return dict(loss=loss, dlogits=grad, flags=flg)
