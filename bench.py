@@ -1,0 +1,415 @@
+"""Benchmark: the whole verification + OPD hot path on one batch per step.
+
+Workload (default "mix"): N = 256 requests, L_i ~ U{2,4,8,16} packed by CSR
+offsets, V = 151936, bf16 logits (log-Zipf target + Gaussian draft noise).
+One step = spec_verify at T = 0, 0.6 and 1.0 plus opd_loss (T = 1, c = 1,
+lambda = 0.1, forward + gradient) on the same batch: every step of the path.
+
+Metric: verified draft positions per second (3 x sum_i L_i per step) for the
+whole job; the achieved HBM bandwidth of the dominant kernel is reported in
+"roofline" against the measured copy bandwidth.  Inputs (1.2 GB + 1.2 GB of
+gradient output per step) are far larger than L2, so no flush is needed.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+
+--impl reference times the CPU oracle (fp64, single thread) on a bounded
+sample of the same workload and prints the same JSON line with
+"impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified draft positions/sec and achieved HBM GB/s vs GB300 peak (1 GPU)"
+UNIT = "positions/s"
+TEMPS = (0.0, 0.6, 1.0)
+OPD = dict(temperature=1.0, clip_c=1.0, lambda_ce=0.1)
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+
+
+def _args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=300)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["native", "reference"], default="native")
+    p.add_argument("--workload", choices=["mix"], default="mix")
+    p.add_argument("--e2e-steps", type=int, default=None)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def make_batch(rank: int):
+    import synth
+    # weak scaling: every rank verifies its own batch of the same shape
+    return synth.config(5, seed=1005 + 7919 * rank)
+
+
+def _src_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "serving_vocab_wide_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:12]
+
+
+KERNEL_SOURCES = {
+    "verify_main": ["verify.cu", "svw_device.cuh", "svw_internal.h"],
+    "opd_kernel": ["opd.cu", "svw_device.cuh", "svw_internal.h"],
+}
+
+
+def _profile_traffic(kernel: str, workload: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (same hash) and workload."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    want = _src_hash(KERNEL_SOURCES[kernel])
+    for line in open(PROFILE_TRAFFIC, encoding="utf-8"):
+        f = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
+        if f.get("kernel") == kernel and f.get("workload") == workload and f.get("src") == want:
+            try:
+                return float(f["dram_bytes_per_launch"])
+            except (KeyError, ValueError):
+                return None
+    return None
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def __exit__(self, *exc):
+        time.sleep(0.15)
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        if not getattr(self, "out", ""):
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# native arm
+# ---------------------------------------------------------------------------
+def run_native(args, ws, rank, local):
+    import torch
+    import serving_vocab_wide_gb300 as svw
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    svw.build()
+    svw.lib()
+    b = make_batch(rank)
+    N, R, V = b.N, b.total_rows, b.V
+    rows_t = R + N
+
+    def logits_host(a):
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+        return t.pin_memory()
+
+    h_t = logits_host(b.target)
+    h_d = logits_host(b.draft)
+    h_cu = torch.from_numpy(b.cu.astype(np.int32)).pin_memory()
+    h_tok = {T: torch.from_numpy(b.tokens[T].astype(np.int32)).pin_memory() for T in TEMPS}
+    t = h_t.to(dev)
+    d = h_d.to(dev)
+    cu = h_cu.to(dev)
+    tok = {T: h_tok[T].to(dev) for T in TEMPS}
+    ws_bytes = svw.verify_workspace_size(N, R, V, svw.SVW_BF16)
+    wsp = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    acc = {T: torch.empty(N, dtype=torch.int32, device=dev) for T in TEMPS}
+    nxt = {T: torch.empty(N, dtype=torch.int32, device=dev) for T in TEMPS}
+    loss = torch.empty(R, dtype=torch.float32, device=dev)
+    grad = torch.empty((R, V), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    calls = ["verify_T0", "verify_T0.6", "verify_T1", "opd"]
+
+    def step(ev=None):
+        for ci, T in enumerate(TEMPS):
+            if ev is not None:
+                ev[2 * ci].record(stream)
+            svw.spec_verify(t, d, cu, tok[T], T, 0, max_len=16, total_draft_rows=R,
+                            accept_len=acc[T], next_token=nxt[T], status=status,
+                            workspace=wsp, stream=stream)
+            if ev is not None:
+                ev[2 * ci + 1].record(stream)
+        if ev is not None:
+            ev[6].record(stream)
+        svw.opd_loss(t, d, cu_draft=cu, has_bonus=True, loss=loss, dlogits=grad,
+                     status=status, stream=stream, **OPD)
+        if ev is not None:
+            ev[7].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} after warm-up")
+
+    # ---- device-timed region: inputs resident in HBM ----
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(K)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for k in range(K):
+            step(evs[k])
+        e1.record(stream)
+        torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    elapsed_ms = e0.elapsed_time(e1)
+    if ws > 1:
+        tt = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    per_call = {c: [] for c in calls}
+    for k in range(K):
+        for ci, c in enumerate(calls):
+            per_call[c].append(evs[k][2 * ci].elapsed_time(evs[k][2 * ci + 1]))
+    avg_us = {c: 1000.0 * float(np.mean(v)) for c, v in per_call.items()}
+
+    # algorithmic bytes per call (each logit byte read once; OPD also writes dz once)
+    es = 2
+    alg = {"verify_T0": rows_t * V * es,
+           "verify_T0.6": (rows_t + R) * V * es,
+           "verify_T1": (rows_t + R) * V * es,
+           "opd": 2 * R * V * es + R * V * 4}
+    ms_per_step = elapsed_ms / K
+    positions_per_step = 3 * R
+    value = positions_per_step * ws / (elapsed_ms / K / 1000.0)
+    step_bytes = sum(alg.values())
+    peak, peak_kind = _peaks()
+    dom = max(calls, key=lambda c: avg_us[c])
+    dom_kernel = "opd_kernel" if dom == "opd" else "verify_main"
+    achieved = alg[dom] / (avg_us[dom] * 1e-6) / 1e9
+    traffic = _profile_traffic(dom_kernel, f"mix:{dom}")
+
+    # ---- end to end through the public API with host buffers ----
+    Ke = args.e2e_steps if args.e2e_steps is not None else max(3, min(K, 60))
+    h_acc = {T: torch.empty(N, dtype=torch.int32).pin_memory() for T in TEMPS}
+    h_nxt = {T: torch.empty(N, dtype=torch.int32).pin_memory() for T in TEMPS}
+    h_loss = torch.empty(R, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        t.copy_(h_t, non_blocking=True)
+        d.copy_(h_d, non_blocking=True)
+        cu.copy_(h_cu, non_blocking=True)
+        for T in TEMPS:
+            tok[T].copy_(h_tok[T], non_blocking=True)
+        step()
+        for T in TEMPS:
+            h_acc[T].copy_(acc[T], non_blocking=True)
+            h_nxt[T].copy_(nxt[T], non_blocking=True)
+        h_loss.copy_(loss, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(Ke):
+        e2e_step()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = f0.elapsed_time(f1)
+    if ws > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    h2d = (h_t.numel() + h_d.numel()) * 2 + h_cu.numel() * 4 + sum(v.numel() * 4 for v in h_tok.values())
+    d2h = 2 * 3 * N * 4 + R * 4
+    e2e = {"value": positions_per_step * ws / (e2e_ms / Ke / 1000.0), "unit": UNIT,
+           "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": Ke}
+
+    status_v = int(status.item())
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(b)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "mix: N=256 ragged L_i~U{2,4,8,16}, V=151936, bf16 log-Zipf "
+                               "logits; verify at T=0,0.6,1 + OPD fwd/bwd (T=1,c=1,lambda=0.1)",
+                   "N": N, "total_draft_rows": R, "V": V, "logits": "bf16",
+                   "per_rank_batch": True, "parallelism": f"replicas x{ws}",
+                   "l2": "inputs 1.25 GB per step > 129 MB L2; no flush"},
+        "roofline": {"bound": "hbm", "kernel": f"{dom_kernel} ({dom})", "achieved": achieved,
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": alg[dom]},
+        "kernels": {c: {"avg_us": avg_us[c], "gbs": alg[c] / (avg_us[c] * 1e-6) / 1e9,
+                        "frac_of_peak": alg[c] / (avg_us[c] * 1e-6) / 1e9 / peak}
+                    for c in calls},
+        "step_gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,
+        "e2e": e2e,
+        "gpu_launches": K * (2 * len(TEMPS) + 1),
+        "clocks": clk.summary(),
+        "device_status": status_v,
+        "cpu_baseline": cpu,
+    }
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores
+# ---------------------------------------------------------------------------
+def _oracle_sample(b, n_req):
+    sub = b.subset(range(n_req))
+    return sub, np.arange(n_req, dtype=np.int32)
+
+
+def oracle_step(sub, ids):
+    import oracle
+    for T in TEMPS:
+        oracle.spec_verify(sub.target, sub.draft, sub.cu, sub.tokens[T], T, 0, max_len=16,
+                           req_ids=ids)
+    oracle.opd_loss(sub.target, sub.draft, cu_draft=sub.cu, has_bonus=True, **OPD)
+
+
+def cpu_baseline(b, n_req=40):
+    """Oracle timed on a bounded sample: the first n_req requests of the batch,
+    one full step (three verifications and the OPD loss + gradient)."""
+    import oracle
+    oracle.build()
+    sub, ids = _oracle_sample(b, n_req)
+    t0 = time.perf_counter()
+    oracle_step(sub, ids)
+    dt = time.perf_counter() - t0
+    return {"value": 3 * sub.total_rows / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"first {n_req} requests ({sub.total_rows} positions) of the mix batch, "
+                      f"one step: verify T=0,0.6,1 + OPD fwd/bwd; {dt:.1f} s"}
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    b = make_batch(0)
+    # size each step's sample so that warmup + steps finish in about 90 s
+    probe, pids = _oracle_sample(b, 1)
+    t0 = time.perf_counter()
+    oracle_step(probe, pids)
+    per_req = max(1e-3, time.perf_counter() - t0)
+    n_req = int(max(1, min(b.N, 90.0 / (per_req * max(1, args.steps + args.warmup)))))
+    sub, ids = _oracle_sample(b, n_req)
+    for _ in range(args.warmup):
+        oracle_step(sub, ids)
+    K = args.steps
+    t0 = time.perf_counter()
+    for _ in range(K):
+        oracle_step(sub, ids)
+    dt = (time.perf_counter() - t0) / K
+    value = 3 * sub.total_rows / dt
+    sample = (f"first {n_req} requests ({sub.total_rows} positions) of the mix batch per step, "
+              f"single-threaded fp64 oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": K, "warmup": args.warmup, "ms_per_step": dt * 1000.0,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "mix: N=256 ragged L_i~U{2,4,8,16}, V=151936, bf16 log-Zipf "
+                               "logits; verify at T=0,0.6,1 + OPD fwd/bwd (T=1,c=1,lambda=0.1)",
+                   "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = _args()
+    ws, rank, local = _dist()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+    else:
+        run_native(args, ws, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,158 @@
+/*
+ * svw.h -- C ABI of the vocabulary-wide speculative-verification library
+ * (serving_vocab_wide_gb300).  Hand-written CUDA for sm_103a (GB300).
+ *
+ * Two operations, both over full-vocabulary logits:
+ *
+ *  spec_verify  batched speculative verification of a ragged batch.  Defined
+ *               by "DFlash 阅读笔记：并行起草、目标特征与精确验证" §5.1 (greedy
+ *               rule), §5.2 eqs. (6)-(8) and Algorithm 1, and by "AdaFlash:
+ *               Taming Variance in Diffusion Speculative Decoding", section
+ *               "Speculative Decoding: The Basic Idea", steps 3-4.  Requests
+ *               are packed by CSR offsets ("AdaFlash：基于在策略蒸馏扩散草稿器
+ *               的自适应投机解码" §2.3: the verify batch holds each request's
+ *               own length, not N x k).
+ *
+ *  opd_loss     entry-wise clipped reverse KL(q||p) + lambda * CE on the
+ *               target top-1 token, and its gradient wrt the draft logits.
+ *               Defined by "AdaFlash: Taming Variance in Diffusion Speculative
+ *               Decoding", sections "The Reverse-KL + Hard-Label Mixture Loss,
+ *               Derived" and "Algorithm 2: Entry-Wise Clipped Reverse-KL".
+ *
+ * Conventions for every entry point:
+ *  - Pointers named "device" are CUDA device pointers (cudaMalloc / PyTorch
+ *    CUDA tensors) on the current device.  The caller owns all memory; the
+ *    library allocates and frees nothing and keeps no per-call state.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Calls are stream-ordered and never synchronise the host.
+ *  - The return value covers host-side validation and launch errors only.
+ *    Problems that only the device can see (bad CSR offsets, out-of-range
+ *    tokens, non-finite rows) are reported by OR-ing SVW_DEV_* bits into
+ *    *status (device int32, may be NULL); the caller clears it.
+ *  - Logits are row-major [rows, V] in fp32 or bf16.  Rows whose byte pitch
+ *    V * sizeof(dtype) is a multiple of 16 with 16-byte aligned bases take the
+ *    vectorised / bulk-copy path; any other shape takes a scalar path with the
+ *    same results.
+ *  - Inputs are read-only; outputs must not alias inputs.
+ */
+#ifndef SVW_H_
+#define SVW_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum svw_status {
+  SVW_OK = 0,
+  SVW_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, bad temperature ... */
+  SVW_ERR_UNSUPPORTED = 2, /* dtype or size outside what the kernels handle         */
+  SVW_ERR_MISALIGNED = 3,  /* a pointer violates its documented alignment            */
+  SVW_ERR_WORKSPACE = 4,   /* workspace missing or smaller than svw_verify_workspace_size */
+  SVW_ERR_CUDA = 5         /* a CUDA runtime call or kernel launch failed            */
+} svw_status;
+
+typedef enum svw_dtype { SVW_F32 = 0, SVW_BF16 = 1 } svw_dtype;
+
+/* bits OR-ed into the device status word */
+#define SVW_DEV_BAD_INPUT 1 /* some request / row was invalid or non-finite   */
+#define SVW_DEV_TIMEOUT 2   /* a bounded wait inside a kernel gave up         */
+
+/* Largest draft length (positions per request) spec_verify accepts. */
+#define SVW_MAX_LEN 32
+
+/*
+ * Bytes of device workspace spec_verify needs for this batch shape (any
+ * temperature).  Depends only on (n_requests, total_draft_rows, V, dtype).
+ * Returns 0 for invalid arguments.
+ */
+size_t svw_verify_workspace_size(int32_t n_requests, int64_t total_draft_rows, int32_t V,
+                                 svw_dtype dtype);
+
+/*
+ * spec_verify -- verify every request of a ragged batch in one call.
+ *
+ * Request i owns L_i = cu_draft[i+1] - cu_draft[i] draft positions.
+ *   draft_logits  device [total_draft_rows, V]; request i's rows are
+ *                 cu_draft[i] .. cu_draft[i+1]-1 (position j at cu_draft[i]+j).
+ *   target_logits device [total_draft_rows + N, V]; request i's rows are
+ *                 cu_draft[i]+i .. cu_draft[i]+i+L_i: row j is the target's
+ *                 distribution at draft position j, the last (j = L_i) is the
+ *                 bonus row used when every candidate passes.
+ *   cu_draft      device int32 [N+1], cu_draft[0] = 0, non-decreasing,
+ *                 cu_draft[N] = total_draft_rows (passed on the host so that
+ *                 the call never reads device memory from the host).
+ *   max_len       1..SVW_MAX_LEN; requests with L_i outside [1, max_len] are bad.
+ *   draft_tokens  device int32 [total_draft_rows], x_j drawn from
+ *                 softmax(draft row j / temperature); must be in [0, V).
+ *   temperature   0 => greedy: accept x_j iff it is the target argmax of row j
+ *                 (raw logits, smallest index wins); next_token is the argmax
+ *                 of the first rejected row, or of the bonus row.
+ *                 > 0 => accept x_j iff u_j < min(1, p_j(x_j) / q_j(x_j)) with
+ *                 p = softmax(target/T), q = softmax(draft/T); the accepted
+ *                 length is the leftmost-rejection prefix; next_token is drawn
+ *                 by inverse CDF (vocabulary order, smallest v with C_v > w Z)
+ *                 from max(0, p - q) at the rejected row, or from p at the
+ *                 bonus row.
+ *   seed          Philox4x32-10 key (lo 32 bits, hi 32 bits).  u_j uses counter
+ *                 {i, j, 0, 0}; the sampling uniform w uses {i, j*, 1, 0}, j*
+ *                 the sampled row.  Uniform = (word0 >> 8) * 2^-24.
+ *   accept_len    device int32 [N] out; -1 for a bad request.
+ *   next_token    device int32 [N] out; -1 for a bad request.
+ *   status        device int32 scalar, may be NULL; SVW_DEV_BAD_INPUT is
+ *                 OR-ed in if any request is bad (invalid length, token out of
+ *                 range, a NaN row, or at T > 0 a row with +Inf or only -Inf).
+ *   workspace     device, 256-byte aligned, >= svw_verify_workspace_size(...)
+ *                 bytes; contents need not be initialised; not preserved.
+ */
+svw_status spec_verify(const void *target_logits, const void *draft_logits, svw_dtype dtype,
+                       int32_t V, int32_t N, const int32_t *cu_draft, int64_t total_draft_rows,
+                       int32_t max_len, const int32_t *draft_tokens, float temperature,
+                       uint64_t seed, int32_t *accept_len, int32_t *next_token, int32_t *status,
+                       void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * opd_loss -- per draft row r (0 <= r < total_draft_rows), paired with one
+ * target row:
+ *   lp = log softmax(target/T), lq = log softmax(draft/T), q = exp(lq)
+ *   t_v = q_v (lq_v - lp_v)          (t_v := 0 where q_v = 0)
+ *   loss[r] = sum_v clamp(t_v, -clip_c, clip_c) + lambda_ce * (-lq[x*]),
+ *             x* = argmax of the raw target row (smallest index wins)
+ *   dlogits[r, v] = grad_scale / T * ( q_v (a_v - S) + lambda_ce (q_v - [v == x*]) ),
+ *             a_v = [-clip_c < t_v < clip_c] (lq_v - lp_v + 1), S = sum_v q_v a_v
+ * i.e. dlogits is grad_scale times the gradient of sum_r loss[r] wrt the
+ * draft logits (the target is frozen).  Pass grad_scale = 1/k for the mean
+ * over k positions.
+ *
+ *   target_has_bonus_row  1: verify layout -- target has total_draft_rows + N
+ *                 rows and draft row r of request i pairs with target row r + i
+ *                 (cu_draft device [N+1] required).  0: rows pair 1:1, target
+ *                 has total_draft_rows rows, cu_draft and N are ignored.
+ *   temperature   > 0 (the reverse-KL temperature; 1.0 in the review).
+ *   clip_c        > 0 (may be +inf: no clipping).
+ *   loss          device float [total_draft_rows] out (NaN for a bad row).
+ *   dlogits       device float [total_draft_rows, V] out, 16-byte aligned;
+ *                 NULL computes the loss only.
+ *   status        as for spec_verify (SVW_DEV_BAD_INPUT for a non-finite row
+ *                 or a row outside its request's CSR range; SVW_DEV_TIMEOUT if
+ *                 a bounded wait on a bulk copy gave up).
+ */
+svw_status opd_loss(const void *target_logits, const void *draft_logits, svw_dtype dtype,
+                    int32_t V, int32_t N, const int32_t *cu_draft, int64_t total_draft_rows,
+                    int32_t target_has_bonus_row, float temperature, float clip_c,
+                    float lambda_ce, float grad_scale, float *loss, float *dlogits,
+                    int32_t *status, void *stream);
+
+/* Human-readable name of a status code (static string). */
+const char *svw_status_string(svw_status s);
+
+/* Library ABI version: 100 * major + minor. */
+int32_t svw_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SVW_H_ */

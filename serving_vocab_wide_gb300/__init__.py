@@ -1,0 +1,151 @@
+"""serving_vocab_wide_gb300 -- batched speculative verification and the OPD
+loss over full-vocabulary logits, as hand-written CUDA for GB300 (sm_103a).
+
+This module is a thin ctypes binding over the C ABI in ``include/svw.h``:
+it only marshals PyTorch CUDA tensors (data pointers, sizes, the current
+stream) into the library's entry points.  Every step of the computation runs
+in the library's kernels; there is no CPU or PyTorch fallback -- if the shared
+library is missing the calls raise.
+
+Build the library with ``serving_vocab_wide_gb300.build()`` (nvcc, sm_103a).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from .build import LIB_PATH, build  # noqa: F401
+
+SVW_F32 = 0
+SVW_BF16 = 1
+SVW_DEV_BAD_INPUT = 1
+SVW_DEV_TIMEOUT = 2
+SVW_MAX_LEN = 32
+
+_lib = None
+_lock = threading.Lock()
+
+
+class SvwError(RuntimeError):
+    pass
+
+
+def lib():
+    """The loaded shared library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise SvwError(f"CUDA library not built: {LIB_PATH} is missing "
+                               "(run serving_vocab_wide_gb300.build())")
+            L = ctypes.CDLL(LIB_PATH)
+            P, I32, I64, F, U64, SZ = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
+                                       ctypes.c_float, ctypes.c_uint64, ctypes.c_size_t)
+            L.svw_verify_workspace_size.argtypes = [I32, I64, I32, ctypes.c_int]
+            L.svw_verify_workspace_size.restype = SZ
+            L.spec_verify.argtypes = [P, P, ctypes.c_int, I32, I32, P, I64, I32, P, F, U64,
+                                      P, P, P, P, SZ, P]
+            L.spec_verify.restype = ctypes.c_int
+            L.opd_loss.argtypes = [P, P, ctypes.c_int, I32, I32, P, I64, I32, F, F, F, F,
+                                   P, P, P, P]
+            L.opd_loss.restype = ctypes.c_int
+            L.svw_status_string.argtypes = [ctypes.c_int]
+            L.svw_status_string.restype = ctypes.c_char_p
+            L.svw_version.argtypes = []
+            L.svw_version.restype = I32
+            _lib = L
+    return _lib
+
+
+def _check(rc: int):
+    if rc != 0:
+        raise SvwError(lib().svw_status_string(rc).decode())
+
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        return SVW_BF16
+    if t.dtype == torch.float32:
+        return SVW_F32
+    raise SvwError(f"logits must be bfloat16 or float32, got {t.dtype}")
+
+
+def _stream_ptr(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise SvwError("tensors must be contiguous CUDA tensors")
+
+
+def verify_workspace_size(n_requests: int, total_draft_rows: int, V: int, dtype_code: int) -> int:
+    return int(lib().svw_verify_workspace_size(n_requests, total_draft_rows, V, dtype_code))
+
+
+def spec_verify(target, draft, cu_draft, draft_tokens, temperature: float, seed: int,
+                max_len: int = SVW_MAX_LEN, total_draft_rows: int | None = None,
+                accept_len=None, next_token=None, status=None, workspace=None, stream=None):
+    """Verify a ragged batch.  Returns (accept_len, next_token) int32 CUDA tensors.
+
+    target: [total_draft_rows + N, V], draft: [total_draft_rows, V] (bf16 or
+    fp32); cu_draft: int32 [N + 1] CSR offsets; draft_tokens: int32
+    [total_draft_rows].  Output / workspace / status tensors may be passed in
+    to avoid allocation; `total_draft_rows` (= cu_draft[-1]) may be passed to
+    avoid a device read.
+    """
+    import torch
+    _need_cuda(target, draft, cu_draft, draft_tokens)
+    N = cu_draft.numel() - 1
+    V = target.shape[-1]
+    R = int(cu_draft[-1].item()) if total_draft_rows is None else int(total_draft_rows)
+    code = _dtype_code(target)
+    dev = target.device
+    if accept_len is None:
+        accept_len = torch.empty(N, dtype=torch.int32, device=dev)
+    if next_token is None:
+        next_token = torch.empty(N, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(1, verify_workspace_size(N, R, V, code)), dtype=torch.uint8,
+                                device=dev)
+    _need_cuda(accept_len, next_token, workspace, status)
+    rc = lib().spec_verify(_ptr(target), _ptr(draft), code, V, N, _ptr(cu_draft), R, max_len,
+                           _ptr(draft_tokens), float(temperature), int(seed) & (2**64 - 1),
+                           _ptr(accept_len), _ptr(next_token), _ptr(status), _ptr(workspace),
+                           workspace.numel(), _stream_ptr(stream))
+    _check(rc)
+    return accept_len, next_token
+
+
+def opd_loss(target, draft, temperature: float = 1.0, clip_c: float = 1.0,
+             lambda_ce: float = 0.1, grad_scale: float = 1.0, cu_draft=None,
+             has_bonus: bool = False, want_grad: bool = True, loss=None, dlogits=None,
+             status=None, stream=None):
+    """Clipped reverse-KL + lambda*CE per draft row, and its gradient wrt the
+    draft logits.  Returns (loss [R] fp32, dlogits [R, V] fp32 or None)."""
+    import torch
+    _need_cuda(target, draft, cu_draft)
+    R, V = draft.shape
+    code = _dtype_code(draft)
+    N = (cu_draft.numel() - 1) if has_bonus else 0
+    dev = draft.device
+    if loss is None:
+        loss = torch.empty(R, dtype=torch.float32, device=dev)
+    if want_grad and dlogits is None:
+        dlogits = torch.empty((R, V), dtype=torch.float32, device=dev)
+    _need_cuda(loss, dlogits, status)
+    rc = lib().opd_loss(_ptr(target), _ptr(draft), code, V, N, _ptr(cu_draft) if has_bonus else None,
+                        R, 1 if has_bonus else 0, float(temperature), float(clip_c),
+                        float(lambda_ce), float(grad_scale), _ptr(loss),
+                        _ptr(dlogits) if want_grad else None, _ptr(status), _stream_ptr(stream))
+    _check(rc)
+    return loss, (dlogits if want_grad else None)

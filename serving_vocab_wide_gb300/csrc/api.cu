@@ -1,0 +1,143 @@
+// api.cu -- the exported C ABI (see include/svw.h): host-side validation,
+// workspace carving, and dispatch to the kernel launchers.  No allocation,
+// no host synchronisation, no device-memory reads from the host.
+#include <cmath>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "svw_internal.h"
+
+namespace svw {
+bool opd_supported(int64_t V, int esize);
+}
+
+namespace {
+
+constexpr int64_t kMaxV = 1 << 20;  // sampler span cap (256 threads x 512 groups x 8)
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int esize_of(svw_dtype d) { return d == SVW_BF16 ? 2 : 4; }
+
+}  // namespace
+
+extern "C" {
+
+int32_t svw_version(void) { return 100; }
+
+const char *svw_status_string(svw_status s) {
+  switch (s) {
+    case SVW_OK: return "SVW_OK";
+    case SVW_ERR_INVALID_ARG: return "SVW_ERR_INVALID_ARG: invalid argument";
+    case SVW_ERR_UNSUPPORTED: return "SVW_ERR_UNSUPPORTED: dtype or size not supported";
+    case SVW_ERR_MISALIGNED: return "SVW_ERR_MISALIGNED: pointer alignment";
+    case SVW_ERR_WORKSPACE: return "SVW_ERR_WORKSPACE: workspace missing or too small";
+    case SVW_ERR_CUDA: return "SVW_ERR_CUDA: CUDA runtime or launch failure";
+  }
+  return "unknown svw_status";
+}
+
+size_t svw_verify_workspace_size(int32_t n_requests, int64_t total_draft_rows, int32_t V,
+                                 svw_dtype dtype) {
+  if (n_requests <= 0 || total_draft_rows < 0 || V <= 0 || V > kMaxV) return 0;
+  if (dtype != SVW_F32 && dtype != SVW_BF16) return 0;
+  return svw::verify_layout(n_requests, total_draft_rows, V, esize_of(dtype)).total;
+}
+
+svw_status spec_verify(const void *target_logits, const void *draft_logits, svw_dtype dtype,
+                       int32_t V, int32_t N, const int32_t *cu_draft, int64_t total_draft_rows,
+                       int32_t max_len, const int32_t *draft_tokens, float temperature,
+                       uint64_t seed, int32_t *accept_len, int32_t *next_token, int32_t *status,
+                       void *workspace, size_t workspace_bytes, void *stream) {
+  if (dtype != SVW_F32 && dtype != SVW_BF16) return SVW_ERR_UNSUPPORTED;
+  if (V <= 0 || N <= 0 || total_draft_rows < 0 || max_len < 1) return SVW_ERR_INVALID_ARG;
+  if (max_len > SVW_MAX_LEN || V > kMaxV) return SVW_ERR_UNSUPPORTED;
+  if (!target_logits || !draft_logits || !cu_draft || !draft_tokens || !accept_len || !next_token ||
+      !workspace)
+    return workspace ? SVW_ERR_INVALID_ARG : SVW_ERR_WORKSPACE;
+  if (!(temperature >= 0.f) || !std::isfinite(temperature)) return SVW_ERR_INVALID_ARG;
+  const double kd = (temperature > 0.f) ? 1.4426950408889634 / static_cast<double>(temperature) : 0.0;
+  if (temperature > 0.f && !(kd < 3.0e38)) return SVW_ERR_INVALID_ARG;
+  const int es = esize_of(dtype);
+  if (!aligned(target_logits, es) || !aligned(draft_logits, es) || !aligned(cu_draft, 4) ||
+      !aligned(draft_tokens, 4) || !aligned(accept_len, 4) || !aligned(next_token, 4) ||
+      (status && !aligned(status, 4)) || !aligned(workspace, 256))
+    return SVW_ERR_MISALIGNED;
+  const svw::VerifyLayout lay = svw::verify_layout(N, total_draft_rows, V, es);
+  if (workspace_bytes < lay.total) return SVW_ERR_WORKSPACE;
+
+  const svw::ChunkPlan plan = svw::plan_chunks(V, es);
+  const bool greedy = (temperature == 0.f);
+  const bool vec = ((static_cast<int64_t>(V) * es) % 16 == 0) && aligned(target_logits, 16) &&
+                   aligned(draft_logits, 16);
+  svw::VerifyArgs a;
+  a.target = target_logits;
+  a.draft = draft_logits;
+  a.V = V;
+  a.N = N;
+  a.cu = cu_draft;
+  a.total_rows = total_draft_rows;
+  a.rows_t = total_draft_rows + N;
+  a.max_len = max_len;
+  a.tokens = draft_tokens;
+  a.k = static_cast<float>(kd);
+  a.seed = seed;
+  a.accept_len = accept_len;
+  a.next_token = next_token;
+  a.status = status;
+  char *ws = static_cast<char *>(workspace);
+  a.part = reinterpret_cast<svw::Partial *>(ws + lay.part_off);
+  a.counters = reinterpret_cast<int32_t *>(ws + lay.counters_off);
+  a.req_ok = reinterpret_cast<int32_t *>(ws + lay.req_ok_off);
+  a.global_ok = reinterpret_cast<int32_t *>(ws + lay.global_ok_off);
+  a.C = plan.C;
+  a.chunk_len = plan.chunk_len;
+  const int64_t rows = greedy ? (total_draft_rows + N) : (2 * total_draft_rows + N);
+  a.total_items = rows * plan.C;
+  const cudaError_t e = svw::launch_verify(a, dtype, vec, greedy, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SVW_OK : SVW_ERR_CUDA;
+}
+
+svw_status opd_loss(const void *target_logits, const void *draft_logits, svw_dtype dtype,
+                    int32_t V, int32_t N, const int32_t *cu_draft, int64_t total_draft_rows,
+                    int32_t target_has_bonus_row, float temperature, float clip_c,
+                    float lambda_ce, float grad_scale, float *loss, float *dlogits,
+                    int32_t *status, void *stream) {
+  if (dtype != SVW_F32 && dtype != SVW_BF16) return SVW_ERR_UNSUPPORTED;
+  if (V <= 0 || total_draft_rows <= 0) return SVW_ERR_INVALID_ARG;
+  if (target_has_bonus_row && (N <= 0 || !cu_draft)) return SVW_ERR_INVALID_ARG;
+  if (!target_logits || !draft_logits || !loss) return SVW_ERR_INVALID_ARG;
+  if (!(temperature > 0.f) || !std::isfinite(temperature)) return SVW_ERR_INVALID_ARG;
+  if (!(clip_c > 0.f) || !std::isfinite(lambda_ce) || !std::isfinite(grad_scale))
+    return SVW_ERR_INVALID_ARG;
+  const double kd = 1.4426950408889634 / static_cast<double>(temperature);
+  if (!(kd < 3.0e38)) return SVW_ERR_INVALID_ARG;
+  const int es = esize_of(dtype);
+  if (!svw::opd_supported(V, es)) return SVW_ERR_UNSUPPORTED;
+  if (!aligned(target_logits, es) || !aligned(draft_logits, es) || !aligned(loss, 4) ||
+      (dlogits && !aligned(dlogits, 16)) || (cu_draft && !aligned(cu_draft, 4)) ||
+      (status && !aligned(status, 4)))
+    return SVW_ERR_MISALIGNED;
+  const bool bulk = ((static_cast<int64_t>(V) * es) % 16 == 0) && aligned(target_logits, 16) &&
+                    aligned(draft_logits, 16);
+  svw::OpdArgs a;
+  a.target = target_logits;
+  a.draft = draft_logits;
+  a.V = V;
+  a.N = target_has_bonus_row ? N : 0;
+  a.cu = cu_draft;
+  a.R = total_draft_rows;
+  a.has_bonus = target_has_bonus_row ? 1 : 0;
+  a.k = static_cast<float>(kd);
+  a.invT = static_cast<float>(1.0 / static_cast<double>(temperature));
+  a.clip_c = clip_c;
+  a.lambda_ce = lambda_ce;
+  a.grad_scale = grad_scale;
+  a.loss = loss;
+  a.dlogits = dlogits;
+  a.status = status;
+  const cudaError_t e = svw::launch_opd(a, dtype, bulk, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SVW_OK : SVW_ERR_CUDA;
+}
+
+}  // extern "C"

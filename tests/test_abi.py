@@ -1,0 +1,106 @@
+"""The C-ABI library loads and exports every symbol its header declares, and
+host-side validation rejects bad arguments without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "svw.h"), encoding="utf-8").read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"\b([A-Za-z_][A-Za-z0-9_]*)\s*\(", src)
+    skip = {"if", "sizeof", "defined"}
+    return sorted({n for n in names if n not in skip})
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import serving_vocab_wide_gb300 as svw
+    svw.build()
+    return svw.lib()
+
+
+def test_header_symbols_exported(lib):
+    names = _declared_functions()
+    assert {"spec_verify", "opd_loss", "svw_verify_workspace_size",
+            "svw_status_string", "svw_version"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in svw.h but not exported"
+
+
+def test_version_and_status_strings(lib):
+    assert lib.svw_version() == 100
+    for code in range(6):
+        assert lib.svw_status_string(code).startswith(b"SVW_")
+
+
+def test_workspace_size(lib):
+    import serving_vocab_wide_gb300 as svw
+    big = svw.verify_workspace_size(256, 1920, 151936, svw.SVW_BF16)
+    small = svw.verify_workspace_size(4, 64, 1024, svw.SVW_F32)
+    assert big > small > 0
+    assert big % 256 == 0
+    assert svw.verify_workspace_size(0, 10, 100, svw.SVW_BF16) == 0
+    assert svw.verify_workspace_size(4, 10, 0, svw.SVW_BF16) == 0
+    assert svw.verify_workspace_size(4, 10, 1 << 21, svw.SVW_BF16) == 0
+
+
+def _fake(n):
+    # aligned host addresses: validation rejects before any pointer is used
+    buf = ctypes.create_string_buffer(n + 256)
+    addr = (ctypes.addressof(buf) + 255) // 256 * 256
+    return buf, ctypes.c_void_p(addr)
+
+
+def test_verify_argument_validation(lib):
+    keep, p = _fake(4096)
+    ok_args = dict(t=p, d=p, dt=1, V=64, N=2, cu=p, R=4, ml=16, tok=p, T=1.0, seed=0,
+                   acc=p, nxt=p, st=None, ws=p, wsb=1 << 30)
+
+    def call(**kw):
+        a = dict(ok_args, **kw)
+        return lib.spec_verify(a["t"], a["d"], a["dt"], a["V"], a["N"], a["cu"], a["R"],
+                               a["ml"], a["tok"], a["T"], a["seed"], a["acc"], a["nxt"],
+                               a["st"], a["ws"], a["wsb"], None)
+
+    assert call(dt=7) == 2                  # unsupported dtype
+    assert call(V=0) == 1
+    assert call(N=0) == 1
+    assert call(ml=0) == 1
+    assert call(ml=33) == 2                 # above SVW_MAX_LEN
+    assert call(t=None) == 1
+    assert call(ws=None) == 4
+    assert call(wsb=16) == 4                # workspace too small
+    assert call(T=-1.0) == 1
+    assert call(T=float("nan")) == 1
+    assert call(T=float("inf")) == 1
+    assert call(T=1e-45) == 1               # log2(e)/T overflows
+    mis = ctypes.c_void_p(p.value + 1)
+    assert call(t=mis) == 3
+    assert call(ws=ctypes.c_void_p(p.value + 16)) == 3
+
+
+def test_opd_argument_validation(lib):
+    keep, p = _fake(4096)
+
+    def call(**kw):
+        a = dict(t=p, d=p, dt=1, V=64, N=0, cu=None, R=4, hb=0, T=1.0, c=1.0, lam=0.1, gs=1.0,
+                 loss=p, g=p, st=None)
+        a.update(kw)
+        return lib.opd_loss(a["t"], a["d"], a["dt"], a["V"], a["N"], a["cu"], a["R"], a["hb"],
+                            a["T"], a["c"], a["lam"], a["gs"], a["loss"], a["g"], a["st"], None)
+
+    assert call(dt=3) == 2
+    assert call(R=0) == 1
+    assert call(hb=1) == 1                  # bonus layout needs N and cu
+    assert call(T=0.0) == 1
+    assert call(c=0.0) == 1
+    assert call(c=float("nan")) == 1
+    assert call(lam=float("inf")) == 1
+    assert call(loss=None) == 1
+    assert call(g=ctypes.c_void_p(p.value + 4)) == 3   # dlogits must be 16-byte aligned
+    assert call(V=1 << 22, dt=0) == 2       # row too wide for the on-chip slices

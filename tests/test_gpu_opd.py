@@ -1,0 +1,106 @@
+"""GPU parity: opd_loss (CUDA, through the C ABI) against the oracle.
+
+Per-position loss within 1e-4 relative; every dlogits row within 1e-4 of the
+row's largest |gradient|.  Rows the oracle flags as having a term within
+1e-5 of the clip boundary are skipped and counted.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import compare_opd, to_torch_i32, to_torch_logits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    import serving_vocab_wide_gb300 as svw
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+    svw.build()
+    svw.lib()
+
+
+def _gpu(tgt, drf, cu=None, has_bonus=False, status=None, want_grad=True, **kw):
+    import serving_vocab_wide_gb300 as svw
+    loss, g = svw.opd_loss(to_torch_logits(tgt), to_torch_logits(drf),
+                           cu_draft=None if cu is None else to_torch_i32(cu),
+                           has_bonus=has_bonus, status=status, want_grad=want_grad, **kw)
+    return loss.cpu().numpy(), (None if g is None else g.cpu().numpy())
+
+
+@pytest.mark.parametrize("V,dtype", [(151936, "bf16"), (1024, "bf16"), (5003, "bf16"),
+                                     (1001, "f32"), (4096, "f32"), (8, "bf16"), (151936, "f32")])
+def test_paired_rows(V, dtype):
+    rows = 6
+    b = synth.make_batch("opd", seed=V + 1, lengths=np.full(1, rows, np.int32), V=V,
+                         dtype=dtype, draft_kind="scaled", temperatures=(), has_bonus=False)
+    loss, g = _gpu(b.target, b.draft)
+    ref = oracle.opd_loss(b.target, b.draft)
+    compare_opd(loss, g, ref, label=f"V={V} {dtype}")
+
+
+@pytest.mark.parametrize("T,c,lam,gs", [(1.0, 0.01, 0.1, 1.0), (0.7, 1e30, 0.5, 0.0625),
+                                        (1.3, 0.2, 0.0, 1.0), (1.0, float("inf"), 4.0, 0.2)])
+def test_parameters(T, c, lam, gs):
+    b = synth.make_batch("opd", seed=11, lengths=np.full(1, 5, np.int32), V=32768,
+                         draft_kind="scaled", temperatures=(), has_bonus=False)
+    loss, g = _gpu(b.target, b.draft, temperature=T, clip_c=c, lambda_ce=lam, grad_scale=gs)
+    ref = oracle.opd_loss(b.target, b.draft, temperature=T, clip_c=c, lambda_ce=lam,
+                          grad_scale=gs)
+    compare_opd(loss, g, ref, label=f"T={T} c={c}")
+
+
+def test_loss_only():
+    b = synth.make_batch("opd", seed=12, lengths=np.full(1, 4, np.int32), V=20000,
+                         draft_kind="scaled", temperatures=(), has_bonus=False)
+    loss, g = _gpu(b.target, b.draft, want_grad=False)
+    assert g is None
+    compare_opd(loss, None, oracle.opd_loss(b.target, b.draft, want_grad=False))
+
+
+def test_verify_layout_rows():
+    b = synth.config(5, N=7, V=40000, seed=21)
+    loss, g = _gpu(b.target, b.draft, cu=b.cu, has_bonus=True)
+    ref = oracle.opd_loss(b.target, b.draft, cu_draft=b.cu, has_bonus=True)
+    compare_opd(loss, g, ref, label="verify layout")
+
+
+def test_bad_rows():
+    import torch
+    import serving_vocab_wide_gb300 as svw
+    b = synth.make_batch("opd", seed=13, lengths=np.full(1, 4, np.int32), V=4096,
+                         draft_kind="scaled", temperatures=(), has_bonus=False)
+    t = b.target.copy()
+    d = b.draft.copy()
+    t[1, 5] = 0x7FC0          # NaN
+    d[2, :] = 0xFF80          # all -inf
+    t[3, 100] = 0x7F80        # +inf
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    loss, g = _gpu(t, d, status=status)
+    ref = oracle.opd_loss(t, d)
+    assert np.isfinite(loss[0]) and np.all(np.isnan(loss[1:]))
+    assert np.all(ref["flags"][1:] & oracle.FLAG_BAD)
+    assert np.all(np.isnan(g[1:]))
+    assert int(status.item()) & svw.SVW_DEV_BAD_INPUT
+    compare_opd(loss[:1], g[:1], {k: v[:1] for k, v in ref.items()})
+
+
+def test_full_size_sampled_rows():
+    b = synth.config(4)
+    loss, g = _gpu(b.target, b.draft, temperature=1.0, clip_c=1.0, lambda_ce=0.1)
+    rows = np.sort(np.random.default_rng(3).choice(b.total_rows, 16, replace=False))
+    ref = oracle.opd_loss(b.target[rows], b.draft[rows], clip_c=1.0, lambda_ce=0.1)
+    compare_opd(loss[rows], g[rows], ref, label="opd 1024 rows")
+    # every row's gradient sums to ~0
+    assert np.all(np.abs(g.sum(axis=1)) < 1e-4 * np.abs(g).max(axis=1) + 1e-6)
+    assert np.all(np.isfinite(loss))
+
+
+def test_deterministic_rerun():
+    b = synth.config(4, N=3)
+    l1, g1 = _gpu(b.target, b.draft)
+    l2, g2 = _gpu(b.target, b.draft)
+    assert np.array_equal(l1, l2) and np.array_equal(g1, g2)
