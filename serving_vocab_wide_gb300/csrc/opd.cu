@@ -7,26 +7,33 @@
 //   dz_v = gs/T (q_v (a_v - S) + lambda (q_v - [v = x*])),
 //   a_v = [-c < t_v < c] (lq_v - lp_v + 1),  S = sum_v q_v a_v.
 // The gradient needs two row-wide reductions (the two log-sum-exps, then S)
-// before any dz_v can be written, so the row must stay on chip between them.
+// before any dz_v can be written, so the row stays on chip between them.
 //
 // GPU design.  A thread-block cluster of CL CTAs (CL <= 8) owns one row at a
 // time; CTA r of the cluster holds vocabulary slice [r*SL, (r+1)*SL) of both
-// the target and the draft row in shared memory.
+// the target and the draft row in shared memory (76 KB at V = 151936 bf16,
+// so two CTAs of different clusters share an SM and overlap one's copies
+// with the other's arithmetic).
 //   * The slices arrive by 1-D bulk asynchronous copies (cp.async.bulk, one
-//     per tensor per CTA, completion counted on an mbarrier); with two stages
-//     the next row's copies are in flight while the current row computes, so
-//     HBM sees each logit byte once.
-//   * Pass A (max, argmax, sum of exp2 for both rows) -> CTA partial -> DSMEM
-//     exchange across the cluster (barrier.cluster) -> every CTA merges the
-//     CL partials in rank order (identical results everywhere).
-//   * Pass B (clamped terms, S) -> second exchange.
-//   * Pass C writes dz with 16-byte streaming stores.
+//     per tensor per CTA, completion counted on an mbarrier): HBM sees each
+//     logit byte once.
+//   * Pass A: packed bf16 max, then sum of exp2 for both rows -> CTA partial
+//     -> DSMEM exchange (barrier.cluster) -> every CTA merges the CL partials
+//     in rank order, so all CTAs hold identical row constants.
+//   * Pass B: clamped terms and S; the threads holding the row maximum look
+//     up the first argmax index -> second exchange.
+//   * Pass C: dz with 16-byte streaming stores.
+// In log2 units: A = log2 q = z k - Cd, Bp = log2 p = y k - Ct, d2 = A - Bp,
+// t/ln2 = q d2, q(d + 1) = t + q; the per-entry arithmetic runs on f32x2
+// pairs.  Entries whose term is clipped, or undefined (q = 0 against an
+// infinite log ratio, a term of 0), take a scalar slow path.
 // Every wait on a bulk copy is bounded by a clock deadline; on expiry the CTA
 // records SVW_DEV_TIMEOUT, stops issuing copies and keeps joining the cluster
 // barriers so that no peer can hang.
 #include <cfloat>
 #include <climits>
 #include <cooperative_groups.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "svw_device.cuh"
@@ -41,66 +48,18 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxCluster = 8;
-constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
 
 struct OpdSmem {
-  unsigned long long mbar[2];
+  unsigned long long mbar;
   float red[kWarps][4];
-  float redv[kWarps];
   int32_t redi[kWarps];
-  float partA[8];  // mt, st, md, sd, amax value, amax index (bits), abort, -
-  float partB[4];  // rkl, S, abort, -
+  float partA[8];  // this CTA's mt, st, md, sd, abort
+  float partB[4];  // this CTA's rkl (log2 units), S, argmax candidate (bits)
+  float rowA[8];   // merged over the cluster: Mt, St, Md, Sd, any abort
+  float rowB[4];   // merged over the cluster: rkl, S, argmax (bits)
+  int64_t tr;      // target row of the row in flight (-1: outside its request)
   int32_t abort;
 };
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(unsigned long long *bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long *bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-               "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(unsigned long long *bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(unsigned long long *bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// bounded wait: false if the deadline passed first
-__device__ __forceinline__ bool mbar_wait_bounded(unsigned long long *bar, uint32_t parity) {
-  const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > kWaitCycles) return false;
-  }
-  return true;
-}
-
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
-                                         unsigned long long *bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
 
 // target row paired with draft row r, or -1 if r lies outside its request's
 // CSR range (bad offsets)
@@ -117,8 +76,49 @@ __device__ __forceinline__ int64_t target_row_of(const OpdArgs &a, int64_t r) {
   return r + lo;
 }
 
-template <int DT, bool BULK, int STAGES>
-__global__ void __launch_bounds__(kThreads, 1) opd_kernel(OpdArgs a, int32_t SL, int32_t slice_bytes) {
+// max over a 16-byte vector (packed bf16 pairs or 4 floats) folded into m
+template <int DT>
+__device__ __forceinline__ float vec_max(const uint4 &w, float m) {
+  if (DT == 1) {
+    const float2 f = bf16x2_f2(bf16x2_max(bf16x2_max(w.x, w.y), bf16x2_max(w.z, w.w)));
+    return fmaxf(m, fmaxf(f.x, f.y));
+  }
+  return fmaxf(fmaxf(m, fmaxf(__uint_as_float(w.x), __uint_as_float(w.y))),
+               fmaxf(__uint_as_float(w.z), __uint_as_float(w.w)));
+}
+
+// the elements of a 16-byte vector as float pairs, in index order
+template <int DT>
+struct Pairs {
+  static constexpr int kN = (DT == 1) ? 4 : 2;
+  float2 p[kN];
+  __device__ __forceinline__ explicit Pairs(const uint4 &w) {
+    if (DT == 1) {
+      p[0] = bf16x2_f2(w.x);
+      p[1] = bf16x2_f2(w.y);
+      p[2] = bf16x2_f2(w.z);
+      p[3] = bf16x2_f2(w.w);
+    } else {
+      p[0] = make_float2(__uint_as_float(w.x), __uint_as_float(w.y));
+      p[kN - 1] = make_float2(__uint_as_float(w.z), __uint_as_float(w.w));
+    }
+  }
+};
+
+// one entry's contribution when its term is clipped or undefined (rare):
+// NaN arises only from q = 0 against an infinite log ratio, whose term is 0
+__device__ __forceinline__ void term_slow(float t2, float q, float c2, float &rkl2, float &S) {
+  if (t2 != t2) return;
+  if (fabsf(t2) < c2) {
+    rkl2 += t2;
+    S += fmaf(t2, kLn2, q);
+  } else {
+    rkl2 += (t2 > 0.f) ? c2 : -c2;
+  }
+}
+
+template <int DT, bool BULK>
+__global__ void __launch_bounds__(kThreads, 2) opd_kernel(OpdArgs a, int32_t SL, int32_t slice_bytes) {
   using E = Elem<DT>;
   constexpr int EPV = E::kPerVec;
   extern __shared__ __align__(128) unsigned char dyn[];
@@ -131,259 +131,268 @@ __global__ void __launch_bounds__(kThreads, 1) opd_kernel(OpdArgs a, int32_t SL,
   const int64_t cid = blockIdx.x / CL;
   const int64_t V = a.V;
   const int64_t lo = static_cast<int64_t>(rank) * SL;
-  const int64_t n = max(static_cast<int64_t>(0), min(static_cast<int64_t>(SL), V - lo));
+  const int n = static_cast<int>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(SL), V - lo)));
+  const int nvec = n / EPV;  // whole 16-byte vectors (the bulk path has no tail)
   const float k = a.k;
-
-  unsigned char *tbuf[2], *dbuf[2];
-  for (int s = 0; s < 2; ++s) {
-    const int ss = (STAGES == 2) ? s : 0;
-    tbuf[s] = dyn + static_cast<size_t>(ss) * 2 * slice_bytes;
-    dbuf[s] = tbuf[s] + slice_bytes;
-  }
+  unsigned char *tbuf = dyn;
+  unsigned char *dbuf = dyn + slice_bytes;
+  const uint32_t tb = smem_u32(tbuf), db = smem_u32(dbuf);
 
   if (tid == 0) {
-    mbar_init(&sm.mbar[0], 1);
-    mbar_init(&sm.mbar[1], 1);
+    mbar_init(&sm.mbar, 1);
     sm.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   __syncthreads();
 
-  // thread 0 starts the copies of row r into stage s
-  auto issue = [&](int64_t r, int s) {
-    const int64_t tr = target_row_of(a, r);
-    if (!BULK) return;
-    if (sm.abort) return;
-    const uint32_t bytes = static_cast<uint32_t>(n * E::kSize);
-    if (tr >= 0 && bytes > 0) {
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive_expect_tx(&sm.mbar[s], 2 * bytes);
-      bulk_g2s(tbuf[s], static_cast<const char *>(a.target) + (tr * V + lo) * E::kSize, bytes,
-               &sm.mbar[s]);
-      bulk_g2s(dbuf[s], static_cast<const char *>(a.draft) + (r * V + lo) * E::kSize, bytes,
-               &sm.mbar[s]);
-    } else {
-      mbar_arrive(&sm.mbar[s]);
-    }
-  };
-
-  int64_t it = 0;
-  if (STAGES == 2 && cid < a.R && tid == 0) issue(cid, 0);
-  for (int64_t r = cid; r < a.R; r += nclusters, ++it) {
-    const int s = (STAGES == 2) ? static_cast<int>(it & 1) : 0;
-    const uint32_t parity = static_cast<uint32_t>(((STAGES == 2) ? (it >> 1) : it) & 1);
-    if (tid == 0) {
-      if (STAGES == 2) {
-        if (r + nclusters < a.R) issue(r + nclusters, s ^ 1);
-      } else {
-        issue(r, 0);
-      }
-    }
-    const int64_t tr = target_row_of(a, r);
-    const bool valid = (tr >= 0);
+  for (int64_t r = cid, it = 0; r < a.R; r += nclusters, ++it) {
+    // ---- fill the slices ----
     if (BULK) {
-      if (!sm.abort) {
-        if (!mbar_wait_bounded(&sm.mbar[s], parity)) {
-          if (tid == 0 && a.status) atomicOr(a.status, SVW_DEV_TIMEOUT);
-          sm.abort = 1;
+      if (tid == 0) {
+        const int64_t t = target_row_of(a, r);
+        sm.tr = t;
+        const uint32_t bytes = static_cast<uint32_t>(n) * E::kSize;
+        if (!sm.abort && t >= 0 && bytes > 0) {
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          mbar_arrive_expect_tx(&sm.mbar, 2 * bytes);
+          bulk_g2s(tbuf, static_cast<const char *>(a.target) + (t * V + lo) * E::kSize, bytes, &sm.mbar);
+          bulk_g2s(dbuf, static_cast<const char *>(a.draft) + (r * V + lo) * E::kSize, bytes, &sm.mbar);
+        } else {
+          mbar_arrive(&sm.mbar);
         }
+      }
+      if (!mbar_wait_bounded(&sm.mbar, static_cast<uint32_t>(it & 1))) {
+        if (a.status) atomicOr(a.status, SVW_DEV_TIMEOUT);
+        sm.abort = 1;
       }
       __syncthreads();
     } else {
-      // scalar fill (rows not 16-byte pitched): plain loads into shared memory
-      if (valid) {
-        const char *ts = static_cast<const char *>(a.target) + (tr * V + lo) * E::kSize;
+      if (tid == 0) sm.tr = target_row_of(a, r);
+      __syncthreads();
+      const int64_t t = sm.tr;
+      if (t >= 0) {
+        const char *ts = static_cast<const char *>(a.target) + (t * V + lo) * E::kSize;
         const char *ds = static_cast<const char *>(a.draft) + (r * V + lo) * E::kSize;
-        for (int64_t v = tid; v < n; v += kThreads) {
+        for (int v = tid; v < n; v += kThreads) {
           if (DT == 1) {
-            reinterpret_cast<unsigned short *>(tbuf[s])[v] = __ldg(reinterpret_cast<const unsigned short *>(ts) + v);
-            reinterpret_cast<unsigned short *>(dbuf[s])[v] = __ldg(reinterpret_cast<const unsigned short *>(ds) + v);
+            reinterpret_cast<unsigned short *>(tbuf)[v] = __ldg(reinterpret_cast<const unsigned short *>(ts) + v);
+            reinterpret_cast<unsigned short *>(dbuf)[v] = __ldg(reinterpret_cast<const unsigned short *>(ds) + v);
           } else {
-            reinterpret_cast<float *>(tbuf[s])[v] = __ldg(reinterpret_cast<const float *>(ts) + v);
-            reinterpret_cast<float *>(dbuf[s])[v] = __ldg(reinterpret_cast<const float *>(ds) + v);
+            reinterpret_cast<float *>(tbuf)[v] = __ldg(reinterpret_cast<const float *>(ts) + v);
+            reinterpret_cast<float *>(dbuf)[v] = __ldg(reinterpret_cast<const float *>(ds) + v);
           }
         }
       }
       __syncthreads();
     }
+    const bool valid = (sm.tr >= 0);
     const bool work = valid && !sm.abort;
-    const unsigned char *T = tbuf[s];
-    const unsigned char *D = dbuf[s];
-    const int64_t nvec = n / EPV;      // whole 16-byte vectors of the slice
-    const int64_t ntail = n - nvec * EPV;
 
-    // ---------------- pass A: max / argmax / sum-exp of both rows ----------------
+    // ---------------- pass A: maxima, then sums of exp2 ----------------
     float mt = -INFINITY, md = -INFINITY, st = 0.f, sd = 0.f;
-    int32_t ai = INT32_MAX;
-    float av = -INFINITY;
     if (work) {
-      auto visit_max = [&](float y, float z, int64_t v) {
-        if (y > av || (ai == INT32_MAX && y == y)) {
-          av = y;
-          ai = static_cast<int32_t>(v);
-        }
-        mt = fmaxf(mt, y);
-        md = fmaxf(md, z);
-      };
-      for (int64_t vi = tid; vi < nvec; vi += kThreads) {
-        float y[EPV], z[EPV];
-        E::unpack(*reinterpret_cast<const uint4 *>(T + vi * 16), y);
-        E::unpack(*reinterpret_cast<const uint4 *>(D + vi * 16), z);
-#pragma unroll
-        for (int e = 0; e < EPV; ++e) visit_max(y[e], z[e], lo + vi * EPV + e);
+      for (int vi = tid; vi < nvec; vi += kThreads) {
+        mt = vec_max<DT>(lds128(tb + vi * 16), mt);
+        md = vec_max<DT>(lds128(db + vi * 16), md);
       }
-      if (tid == 0)
-        for (int64_t v = nvec * EPV; v < n; ++v) {
-          const float y = E::load_plain(T, v), z = E::load_plain(D, v);
-          visit_max(y, z, lo + v);
+      if (!BULK && tid == 0)
+        for (int v = nvec * EPV; v < n; ++v) {
+          mt = fmaxf(mt, E::load_plain(tbuf, v));
+          md = fmaxf(md, E::load_plain(dbuf, v));
         }
-      const float mtr = (mt == -INFINITY) ? 0.f : mt;
-      const float mdr = (md == -INFINITY) ? 0.f : md;
-      for (int64_t vi = tid; vi < nvec; vi += kThreads) {
-        float y[EPV], z[EPV];
-        E::unpack(*reinterpret_cast<const uint4 *>(T + vi * 16), y);
-        E::unpack(*reinterpret_cast<const uint4 *>(D + vi * 16), z);
-        float ps = 0.f, qs = 0.f;
+      const float nmt = (mt == -INFINITY) ? 0.f : -mt * k;
+      const float nmd = (md == -INFINITY) ? 0.f : -md * k;
+      const float2 kk = make_float2(k, k), nt2 = make_float2(nmt, nmt), nd2 = make_float2(nmd, nmd);
+      float2 at = make_float2(0.f, 0.f), ad = make_float2(0.f, 0.f);
+      for (int vi = tid; vi < nvec; vi += kThreads) {
+        const Pairs<DT> y(lds128(tb + vi * 16)), z(lds128(db + vi * 16));
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) {
-          ps = __fadd_rn(ps, ex2(__fmul_rn(__fsub_rn(y[e], mtr), k)));
-          qs = __fadd_rn(qs, ex2(__fmul_rn(__fsub_rn(z[e], mdr), k)));
+        for (int h = 0; h < Pairs<DT>::kN; ++h) {
+          const float2 ey = __ffma2_rn(y.p[h], kk, nt2);
+          const float2 ez = __ffma2_rn(z.p[h], kk, nd2);
+          at = __fadd2_rn(at, make_float2(ex2(ey.x), ex2(ey.y)));
+          ad = __fadd2_rn(ad, make_float2(ex2(ez.x), ex2(ez.y)));
         }
-        st = __fadd_rn(st, ps);
-        sd = __fadd_rn(sd, qs);
       }
-      if (tid == 0)
-        for (int64_t v = nvec * EPV; v < n; ++v) {
-          st = __fadd_rn(st, ex2(__fmul_rn(__fsub_rn(E::load_plain(T, v), mtr), k)));
-          sd = __fadd_rn(sd, ex2(__fmul_rn(__fsub_rn(E::load_plain(D, v), mdr), k)));
+      st = at.x + at.y;
+      sd = ad.x + ad.y;
+      if (!BULK && tid == 0)
+        for (int v = nvec * EPV; v < n; ++v) {
+          st += ex2(fmaf(E::load_plain(tbuf, v), k, nmt));
+          sd += ex2(fmaf(E::load_plain(dbuf, v), k, nmd));
         }
     }
-    (void)ntail;
-    // block reduction of (mt, st), (md, sd), (av, ai)
+    const float my_mt = mt;  // this thread's target maximum (argmax lookup below)
     warp_lse(mt, st, k);
     warp_lse(md, sd, k);
-    warp_amax(av, ai);
     if (lane == 0) {
       sm.red[warp][0] = mt;
       sm.red[warp][1] = st;
       sm.red[warp][2] = md;
       sm.red[warp][3] = sd;
-      sm.redv[warp] = av;
-      sm.redi[warp] = ai;
     }
     __syncthreads();
     if (warp == 0) {
-      float a0 = -INFINITY, a1 = 0.f, a2 = -INFINITY, a3 = 0.f, vv = -INFINITY;
-      int32_t ii = INT32_MAX;
+      float a0 = -INFINITY, a1 = 0.f, a2 = -INFINITY, a3 = 0.f;
       if (lane < kWarps) {
         a0 = sm.red[lane][0];
         a1 = sm.red[lane][1];
         a2 = sm.red[lane][2];
         a3 = sm.red[lane][3];
-        vv = sm.redv[lane];
-        ii = sm.redi[lane];
       }
       warp_lse(a0, a1, k);
       warp_lse(a2, a3, k);
-      warp_amax(vv, ii);
       if (lane == 0) {
         sm.partA[0] = a0;
         sm.partA[1] = a1;
         sm.partA[2] = a2;
         sm.partA[3] = a3;
-        sm.partA[4] = vv;
-        sm.partA[5] = __int_as_float(ii);
-        sm.partA[6] = sm.abort ? 1.f : 0.f;
+        sm.partA[4] = sm.abort ? 1.f : 0.f;
       }
     }
     cluster.sync();
-    // merge the CL partials in rank order (same result in every CTA)
-    float Mt = -INFINITY, St = 0.f, Md = -INFINITY, Sd = 0.f, Av = -INFINITY;
-    int32_t Ai = INT32_MAX;
-    bool any_abort = false;
-    for (int q = 0; q < CL; ++q) {
-      const float *pa = cluster.map_shared_rank(sm.partA, q);
-      lse_combine(Mt, St, pa[0], pa[1], k);
-      lse_combine(Md, Sd, pa[2], pa[3], k);
-      amax_combine(Av, Ai, pa[4], __float_as_int(pa[5]));
-      any_abort |= (pa[6] != 0.f);
+    // one warp gathers the CL partials (lane q <- rank q) and merges them in
+    // rank order; every CTA computes the same constants
+    if (warp == 0) {
+      float v0 = -INFINITY, v1 = 0.f, v2 = -INFINITY, v3 = 0.f, v4 = 0.f;
+      if (lane < CL) {
+        const float *pa = cluster.map_shared_rank(sm.partA, lane);
+        v0 = pa[0];
+        v1 = pa[1];
+        v2 = pa[2];
+        v3 = pa[3];
+        v4 = pa[4];
+      }
+      float M0 = -INFINITY, S0 = 0.f, M1 = -INFINITY, S1 = 0.f, ab = 0.f;
+      for (int q = 0; q < CL; ++q) {
+        lse_combine(M0, S0, __shfl_sync(0xffffffffu, v0, q), __shfl_sync(0xffffffffu, v1, q), k);
+        lse_combine(M1, S1, __shfl_sync(0xffffffffu, v2, q), __shfl_sync(0xffffffffu, v3, q), k);
+        ab += __shfl_sync(0xffffffffu, v4, q);
+      }
+      if (lane == 0) {
+        sm.rowA[0] = M0;
+        sm.rowA[1] = S0;
+        sm.rowA[2] = M1;
+        sm.rowA[3] = S1;
+        sm.rowA[4] = ab;
+      }
     }
+    __syncthreads();
+    const float Mt = sm.rowA[0], St = sm.rowA[1], Md = sm.rowA[2], Sd = sm.rowA[3];
+    const bool any_abort = sm.rowA[4] != 0.f;
     const bool row_ok = valid && !any_abort && (St > 0.f && St <= FLT_MAX) && (Sd > 0.f && Sd <= FLT_MAX);
-    const float lt = lg2(St), ld = lg2(Sd);
-    const float c = a.clip_c;
-
-    // ---------------- pass B: clamped reverse-KL terms and S ----------------
+    const float Ct = fmaf(Mt, k, lg2(St));  // log2 p = y k - Ct
+    const float Cd = fmaf(Md, k, lg2(Sd));  // log2 q = z k - Cd
+    const float c2 = a.clip_c * kLog2e;     // clip bound in log2 units of t
     float rkl = 0.f, S = 0.f;
-    auto term = [&](float y, float z, float &qv, float &qa, float &tcl) {
-      const float lp = __fsub_rn(__fmul_rn(__fsub_rn(y, Mt), k), lt);  // log2 p
-      const float lq = __fsub_rn(__fmul_rn(__fsub_rn(z, Md), k), ld);  // log2 q
-      qv = ex2(lq);
-      if (qv == 0.f) {
-        qa = 0.f;
-        tcl = 0.f;
-        return;
-      }
-      const float d = __fmul_rn(__fsub_rn(lq, lp), kLn2);  // ln q - ln p
-      const float t = __fmul_rn(qv, d);
-      tcl = fminf(fmaxf(t, -c), c);
-      qa = (t > -c && t < c) ? __fmul_rn(qv, __fadd_rn(d, 1.f)) : 0.f;
-    };
+    int32_t cand = INT32_MAX;
+
+    // ---------------- pass B: clamped terms, S, argmax ----------------
     if (row_ok) {
-      for (int64_t vi = tid; vi < nvec; vi += kThreads) {
-        float y[EPV], z[EPV];
-        E::unpack(*reinterpret_cast<const uint4 *>(T + vi * 16), y);
-        E::unpack(*reinterpret_cast<const uint4 *>(D + vi * 16), z);
-        float r1 = 0.f, s1 = 0.f;
+      const float2 kk = make_float2(k, k), nkk = make_float2(-k, -k);
+      const float2 nCd = make_float2(-Cd, -Cd), Ct2 = make_float2(Ct, Ct), l2 = make_float2(kLn2, kLn2);
+      float2 r2 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
+      for (int vi = tid; vi < nvec; vi += kThreads) {
+        const Pairs<DT> y(lds128(tb + vi * 16)), z(lds128(db + vi * 16));
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) {
-          float qv, qa, tcl;
-          term(y[e], z[e], qv, qa, tcl);
-          r1 = __fadd_rn(r1, tcl);
-          s1 = __fadd_rn(s1, qa);
+        for (int h = 0; h < Pairs<DT>::kN; ++h) {
+          const float2 A = __ffma2_rn(z.p[h], kk, nCd);    // log2 q
+          const float2 q = make_float2(ex2(A.x), ex2(A.y));
+          const float2 d = __fadd2_rn(A, __ffma2_rn(y.p[h], nkk, Ct2));  // log2 q - log2 p
+          const float2 t = __fmul2_rn(q, d);               // t / ln 2
+          if (fabsf(t.x) < c2 && fabsf(t.y) < c2) {
+            r2 = __fadd2_rn(r2, t);
+            s2 = __fadd2_rn(__ffma2_rn(t, l2, s2), q);
+          } else {
+            term_slow(t.x, q.x, c2, r2.x, s2.x);
+            term_slow(t.y, q.y, c2, r2.y, s2.y);
+          }
         }
-        rkl = __fadd_rn(rkl, r1);
-        S = __fadd_rn(S, s1);
       }
-      if (tid == 0)
-        for (int64_t v = nvec * EPV; v < n; ++v) {
-          float qv, qa, tcl;
-          term(E::load_plain(T, v), E::load_plain(D, v), qv, qa, tcl);
-          rkl = __fadd_rn(rkl, tcl);
-          S = __fadd_rn(S, qa);
+      rkl = r2.x + r2.y;
+      S = s2.x + s2.y;
+      if (!BULK && tid == 0)
+        for (int v = nvec * EPV; v < n; ++v) {
+          const float y = E::load_plain(tbuf, v), z = E::load_plain(dbuf, v);
+          const float A = fmaf(z, k, -Cd);
+          const float q = ex2(A);
+          term_slow(q * (A - fmaf(y, k, -Ct)), q, c2, rkl, S);
         }
+      // first index holding the row maximum (only threads that saw it look)
+      if (my_mt == Mt) {
+        for (int vi = tid; vi < nvec && cand == INT32_MAX; vi += kThreads) {
+          float y[EPV];
+          E::unpack(lds128(tb + vi * 16), y);
+          for (int e = 0; e < EPV; ++e)
+            if (y[e] == Mt) {
+              cand = static_cast<int32_t>(lo + vi * EPV + e);
+              break;
+            }
+        }
+        if (!BULK && tid == 0 && cand == INT32_MAX)
+          for (int v = nvec * EPV; v < n; ++v)
+            if (E::load_plain(tbuf, v) == Mt) {
+              cand = static_cast<int32_t>(lo + v);
+              break;
+            }
+      }
     }
     rkl = warp_sum(rkl);
     S = warp_sum(S);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, o));
     if (lane == 0) {
       sm.red[warp][0] = rkl;
       sm.red[warp][1] = S;
+      sm.redi[warp] = cand;
     }
     __syncthreads();
     if (warp == 0) {
       float r1 = (lane < kWarps) ? sm.red[lane][0] : 0.f;
       float s1 = (lane < kWarps) ? sm.red[lane][1] : 0.f;
+      int32_t c1 = (lane < kWarps) ? sm.redi[lane] : INT32_MAX;
       r1 = warp_sum(r1);
       s1 = warp_sum(s1);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) c1 = min(c1, __shfl_xor_sync(0xffffffffu, c1, o));
       if (lane == 0) {
         sm.partB[0] = r1;
         sm.partB[1] = s1;
+        sm.partB[2] = __int_as_float(c1);
       }
     }
     cluster.sync();
-    float RKL = 0.f, SS = 0.f;
-    for (int q = 0; q < CL; ++q) {
-      const float *pb = cluster.map_shared_rank(sm.partB, q);
-      RKL = __fadd_rn(RKL, pb[0]);
-      SS = __fadd_rn(SS, pb[1]);
+    if (warp == 0) {
+      float v0 = 0.f, v1 = 0.f;
+      int32_t v2 = INT32_MAX;
+      if (lane < CL) {
+        const float *pb = cluster.map_shared_rank(sm.partB, lane);
+        v0 = pb[0];
+        v1 = pb[1];
+        v2 = __float_as_int(pb[2]);
+      }
+      float R0 = 0.f, S0 = 0.f;
+      int32_t X = INT32_MAX;
+      for (int q = 0; q < CL; ++q) {
+        R0 += __shfl_sync(0xffffffffu, v0, q);
+        S0 += __shfl_sync(0xffffffffu, v1, q);
+        X = min(X, __shfl_sync(0xffffffffu, v2, q));
+      }
+      if (lane == 0) {
+        sm.rowB[0] = R0;
+        sm.rowB[1] = S0;
+        sm.rowB[2] = __int_as_float(X);
+      }
     }
-
+    __syncthreads();
+    const float RKL2 = sm.rowB[0], SS = sm.rowB[1];
+    const int32_t xs = __float_as_int(sm.rowB[2]);
     if (rank == 0 && tid == 0) {
       float out = __int_as_float(0x7fffffff);
-      if (row_ok) {
-        const float zx = E::load(a.draft, r * V + Ai);
-        const float lqx = __fsub_rn(__fmul_rn(__fsub_rn(zx, Md), k), ld);
-        out = __fadd_rn(RKL, __fmul_rn(a.lambda_ce, __fmul_rn(-lqx, kLn2)));
+      if (row_ok && xs != INT32_MAX) {
+        const float zx = E::load(a.draft, r * V + xs);
+        // loss = sum clamp(t) + lambda * (-lq[x*]);  t = ln2 * t2, lq = ln2 * A
+        out = kLn2 * (RKL2 - a.lambda_ce * fmaf(zx, k, -Cd));
       } else if (a.status && !any_abort) {
         atomicOr(a.status, SVW_DEV_BAD_INPUT);
       }
@@ -391,34 +400,61 @@ __global__ void __launch_bounds__(kThreads, 1) opd_kernel(OpdArgs a, int32_t SL,
     }
 
     // ---------------- pass C: gradient wrt the draft logits ----------------
+    // dz = gsT (qa + q (lambda - S)) - gsT lambda [v = x*], qa = t + q when
+    // |t| < c else 0; in log2 units dz = t2 gsT ln2 + q gsT (lambda - S + 1).
     if (a.dlogits != nullptr && valid && !any_abort) {
-      const float gsT = __fmul_rn(a.grad_scale, a.invT);
-      const float lam = a.lambda_ce;
+      const float gsT = a.grad_scale * a.invT;
+      const float gL0 = gsT * (a.lambda_ce - SS);
+      const float gL1 = gsT * (a.lambda_ce - SS + 1.f);
+      const float nan = __int_as_float(0x7fffffff);
       float *out = a.dlogits + r * V + lo;
-      auto grad = [&](float y, float z, int64_t v) -> float {
-        if (!row_ok) return __int_as_float(0x7fffffff);
-        float qv, qa, tcl;
-        term(y, z, qv, qa, tcl);
-        float g = __fadd_rn(__fsub_rn(qa, __fmul_rn(qv, SS)), __fmul_rn(lam, qv));
-        if (v == Ai) g = __fsub_rn(g, lam);
-        return __fmul_rn(gsT, g);
-      };
       if (BULK) {
-        for (int64_t vi = tid; vi < nvec; vi += kThreads) {
-          float y[EPV], z[EPV], g[EPV];
-          E::unpack(*reinterpret_cast<const uint4 *>(T + vi * 16), y);
-          E::unpack(*reinterpret_cast<const uint4 *>(D + vi * 16), z);
+        const float2 kk = make_float2(k, k), nkk = make_float2(-k, -k);
+        const float2 nCd = make_float2(-Cd, -Cd), Ct2 = make_float2(Ct, Ct);
+        const float2 gl = make_float2(gsT * kLn2, gsT * kLn2), g1 = make_float2(gL1, gL1);
+        for (int vi = tid; vi < nvec; vi += kThreads) {
+          const Pairs<DT> y(lds128(tb + vi * 16)), z(lds128(db + vi * 16));
+          float g[EPV];
 #pragma unroll
-          for (int e = 0; e < EPV; ++e) g[e] = grad(y[e], z[e], lo + vi * EPV + e);
+          for (int h = 0; h < Pairs<DT>::kN; ++h) {
+            const float2 A = __ffma2_rn(z.p[h], kk, nCd);
+            const float2 q = make_float2(ex2(A.x), ex2(A.y));
+            const float2 t = __fmul2_rn(q, __fadd2_rn(A, __ffma2_rn(y.p[h], nkk, Ct2)));
+            float2 gg = __ffma2_rn(t, gl, __fmul2_rn(q, g1));
+            if (!(fabsf(t.x) < c2 && fabsf(t.y) < c2)) {
+              if (!(fabsf(t.x) < c2)) gg.x = q.x * gL0;
+              if (!(fabsf(t.y) < c2)) gg.y = q.y * gL0;
+            }
+            g[2 * h] = gg.x;
+            g[2 * h + 1] = gg.y;
+          }
+          const int off = static_cast<int>(xs - (lo + vi * EPV));
+          if (off >= 0 && off < EPV) {
+#pragma unroll
+            for (int e = 0; e < EPV; ++e)
+              if (e == off) g[e] -= gsT * a.lambda_ce;
+          }
+          if (!row_ok) {
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) g[e] = nan;
+          }
 #pragma unroll
           for (int h = 0; h < EPV / 4; ++h)
             st_stream(out + vi * EPV + 4 * h, g[4 * h], g[4 * h + 1], g[4 * h + 2], g[4 * h + 3]);
         }
       } else {
-        for (int64_t v = tid; v < n; v += kThreads) out[v] = grad(E::load_plain(T, v), E::load_plain(D, v), lo + v);
+        for (int v = tid; v < n; v += kThreads) {
+          const float y = E::load_plain(tbuf, v), z = E::load_plain(dbuf, v);
+          const float A = fmaf(z, k, -Cd);
+          const float q = ex2(A);
+          const float t = q * (A - fmaf(y, k, -Ct));
+          float g = (fabsf(t) < c2) ? fmaf(t, gsT * kLn2, q * gL1) : q * gL0;
+          if (lo + v == xs) g -= gsT * a.lambda_ce;
+          out[v] = row_ok ? g : nan;
+        }
       }
     }
-    __syncthreads();  // stage s fully consumed before it is refilled
+    __syncthreads();  // the slices are fully consumed before the next copy
   }
   cluster.sync();  // peers may still read this CTA's partials
 }
@@ -427,14 +463,13 @@ struct OpdPlan {
   int CL;
   int SL;
   int slice_bytes;
-  int stages;
   size_t smem;
 };
 
 OpdPlan plan_opd(int64_t V, int esize) {
   OpdPlan p{};
   const int64_t row_bytes = V * esize * 2;
-  int64_t CL = (row_bytes + 32767) / 32768;
+  int64_t CL = (row_bytes + 16383) / 16384;
   if (CL < 1) CL = 1;
   if (CL > kMaxCluster) CL = kMaxCluster;
   int64_t SL = (V + CL - 1) / CL;
@@ -442,18 +477,13 @@ OpdPlan plan_opd(int64_t V, int esize) {
   p.CL = static_cast<int>(CL);
   p.SL = static_cast<int>(SL);
   p.slice_bytes = static_cast<int>((SL * esize + 127) / 128 * 128);
-  const size_t stage = static_cast<size_t>(p.slice_bytes) * 2;
-  const size_t cap = 200 * 1024;
-  if (2 * stage <= cap) p.stages = 2;
-  else if (stage <= cap) p.stages = 1;
-  else p.stages = 0;
-  p.smem = stage * (p.stages == 2 ? 2 : 1);
+  p.smem = static_cast<size_t>(p.slice_bytes) * 2;
   return p;
 }
 
-template <int DT, bool BULK, int STAGES>
+template <int DT, bool BULK>
 cudaError_t launch_opd_t(const OpdArgs &a, const OpdPlan &p, cudaStream_t st) {
-  auto kern = opd_kernel<DT, BULK, STAGES>;
+  auto kern = opd_kernel<DT, BULK>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(p.smem));
   if (e != cudaSuccess) return e;
@@ -470,7 +500,9 @@ cudaError_t launch_opd_t(const OpdArgs &a, const OpdPlan &p, cudaStream_t st) {
   cfg.numAttrs = 1;
   // persistent clusters: as many as can be co-resident (cached per shape)
   struct Entry {
-    int dev, CL;
+    int dev;
+    const void *fn;
+    int CL;
     size_t smem;
     int n;
   };
@@ -481,13 +513,15 @@ cudaError_t launch_opd_t(const OpdArgs &a, const OpdPlan &p, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   int maxc = 0;
   for (int q = 0; q < ncache; ++q)
-    if (cache[q].dev == dev && cache[q].CL == p.CL && cache[q].smem == p.smem) maxc = cache[q].n;
+    if (cache[q].dev == dev && cache[q].fn == reinterpret_cast<const void *>(kern) && cache[q].CL == p.CL &&
+        cache[q].smem == p.smem)
+      maxc = cache[q].n;
   if (maxc == 0) {
     cfg.gridDim = dim3(p.CL * 1024, 1, 1);
     e = cudaOccupancyMaxActiveClusters(&maxc, kern, &cfg);
     if (e != cudaSuccess) return e;
     if (maxc <= 0) return cudaErrorInvalidConfiguration;
-    if (ncache < 32) cache[ncache++] = Entry{dev, p.CL, p.smem, maxc};
+    if (ncache < 32) cache[ncache++] = Entry{dev, reinterpret_cast<const void *>(kern), p.CL, p.smem, maxc};
   }
   int64_t nclusters = maxc;
   if (nclusters > a.R) nclusters = a.R;
@@ -499,18 +533,14 @@ cudaError_t launch_opd_t(const OpdArgs &a, const OpdPlan &p, cudaStream_t st) {
 
 }  // namespace
 
-bool opd_supported(int64_t V, int esize) { return plan_opd(V, esize).stages > 0; }
+bool opd_supported(int64_t V, int esize) { return plan_opd(V, esize).smem <= 200 * 1024; }
 
 cudaError_t launch_opd(const OpdArgs &a, int dtype, bool bulk, cudaStream_t st) {
   const int esize = (dtype == SVW_BF16) ? 2 : 4;
   const OpdPlan p = plan_opd(a.V, esize);
-  if (p.stages == 0) return cudaErrorInvalidValue;
-  if (dtype == SVW_BF16) {
-    if (bulk) return p.stages == 2 ? launch_opd_t<1, true, 2>(a, p, st) : launch_opd_t<1, true, 1>(a, p, st);
-    return launch_opd_t<1, false, 1>(a, p, st);
-  }
-  if (bulk) return p.stages == 2 ? launch_opd_t<0, true, 2>(a, p, st) : launch_opd_t<0, true, 1>(a, p, st);
-  return launch_opd_t<0, false, 1>(a, p, st);
+  if (p.smem > 200 * 1024) return cudaErrorInvalidValue;
+  if (dtype == SVW_BF16) return bulk ? launch_opd_t<1, true>(a, p, st) : launch_opd_t<1, false>(a, p, st);
+  return bulk ? launch_opd_t<0, true>(a, p, st) : launch_opd_t<0, false>(a, p, st);
 }
 
 }  // namespace svw

@@ -25,10 +25,22 @@ struct ChunkPlan {
 };
 ChunkPlan plan_chunks(int64_t V, int esize);
 
+// what the stats kernel records for the sampling kernel (one per request)
+struct alignas(16) SampleInfo {
+  int32_t js;     // sampled row: first rejected position, or L (bonus)
+  int32_t resid;  // 1: residual [p - q]_+ at row js; 0: p of the bonus row
+  int32_t valid;  // request verified (0: bad request, nothing to sample)
+  float w;        // sampling uniform U(seed, i, js, 1)
+  float Mt, lt;   // target row max and log2 sum 2^((y - Mt) log2e/T)
+  float Md, ld;   // draft row (resid only)
+};
+
 struct VerifyLayout {
-  size_t part_off, counters_off, req_ok_off, global_ok_off, total;
+  size_t part_off, sample_counters_off, req_ok_off, sinfo_off, span_off, chunk_tot_off,
+      chunk_last_off, global_ok_off, total;
 };
 VerifyLayout verify_layout(int32_t N, int64_t total_rows, int64_t V, int esize);
+int32_t sampler_chunks(int64_t V);  // 4096-entry chunks of the inverse-CDF sampler
 
 struct VerifyArgs {
   const void *target;
@@ -45,10 +57,15 @@ struct VerifyArgs {
   int32_t *accept_len;
   int32_t *next_token;
   int32_t *status;
-  Partial *part;
-  int32_t *counters;
-  int32_t *req_ok;
-  int32_t *global_ok;
+  Partial *part;                     // [(rows_t + total_rows) * C * 8] per-warp chunk partials
+  int32_t *sample_counters;          // [N] sampling arrivals per request
+  int32_t *req_ok;                   // [N] request passed validation
+  SampleInfo *sinfo;                 // [N]
+  float *span_tot;                   // [N * Cs * 256] sampler lane totals
+  float *chunk_tot;                  // [N * Cs] sampler chunk totals
+  int32_t *chunk_last;               // [N * Cs] last positive entry per sampler chunk
+  int32_t *global_ok;                // CSR offsets consistent
+  int32_t Cs;                        // sampler chunks per row
   int32_t C;
   int32_t chunk_len;
   int64_t total_items;
