@@ -45,19 +45,18 @@ namespace svw {
 
 namespace {
 
-constexpr int kThreads = 512;
-constexpr int kWarps = kThreads / 32;
+constexpr int kMaxWarps = 32;
 constexpr int kMaxCluster = 8;
 
 struct OpdSmem {
-  unsigned long long mbar;
-  float red[kWarps][4];
-  int32_t redi[kWarps];
+  unsigned long long mbar[2];
+  float red[kMaxWarps][4];
+  int32_t redi[kMaxWarps];
   float partA[8];  // this CTA's mt, st, md, sd, abort
   float partB[4];  // this CTA's rkl (log2 units), S, argmax candidate (bits)
   float rowA[8];   // merged over the cluster: Mt, St, Md, Sd, any abort
   float rowB[4];   // merged over the cluster: rkl, S, argmax (bits)
-  int64_t tr;      // target row of the row in flight (-1: outside its request)
+  int64_t tr[2];   // target row of the row in each stage (-1: outside its request)
   int32_t abort;
 };
 
@@ -117,10 +116,15 @@ __device__ __forceinline__ void term_slow(float t2, float q, float c2, float &rk
   }
 }
 
-template <int DT, bool BULK>
-__global__ void __launch_bounds__(kThreads, 2) opd_kernel(OpdArgs a, int32_t SL, int32_t slice_bytes) {
+// NT threads per CTA; STAGES = 1: one slice buffer, two CTAs per SM overlap
+// each other's copies; STAGES = 2: the next row's slices are prefetched into
+// the second buffer while the current row is processed (one CTA per SM).
+template <int DT, bool BULK, int NT, int STAGES>
+__global__ void __launch_bounds__(NT, (STAGES == 1 ? 2 : 1)) opd_kernel(OpdArgs a, int32_t SL, int32_t slice_bytes) {
   using E = Elem<DT>;
   constexpr int EPV = E::kPerVec;
+  constexpr int kThreads = NT;
+  constexpr int kWarps = NT / 32;
   extern __shared__ __align__(128) unsigned char dyn[];
   __shared__ OpdSmem sm;
   cg::cluster_group cluster = cg::this_cluster();
@@ -134,42 +138,64 @@ __global__ void __launch_bounds__(kThreads, 2) opd_kernel(OpdArgs a, int32_t SL,
   const int n = static_cast<int>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(SL), V - lo)));
   const int nvec = n / EPV;  // whole 16-byte vectors (the bulk path has no tail)
   const float k = a.k;
-  unsigned char *tbuf = dyn;
-  unsigned char *dbuf = dyn + slice_bytes;
-  const uint32_t tb = smem_u32(tbuf), db = smem_u32(dbuf);
 
   if (tid == 0) {
-    mbar_init(&sm.mbar, 1);
+    mbar_init(&sm.mbar[0], 1);
+    mbar_init(&sm.mbar[1], 1);
     sm.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
 
+  // thread 0: start the bulk copies of row r's slices into stage s
+  auto issue = [&](int64_t r, int s) {
+    const int64_t t = target_row_of(a, r);
+    sm.tr[s] = t;
+    unsigned char *tb = dyn + static_cast<size_t>(s) * 2 * slice_bytes;
+    const uint32_t bytes = static_cast<uint32_t>(n) * E::kSize;
+    if (!sm.abort && t >= 0 && bytes > 0) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive_expect_tx(&sm.mbar[s], 2 * bytes);
+      bulk_g2s(tb, static_cast<const char *>(a.target) + (t * V + lo) * E::kSize, bytes, &sm.mbar[s]);
+      bulk_g2s(tb + slice_bytes, static_cast<const char *>(a.draft) + (r * V + lo) * E::kSize, bytes,
+               &sm.mbar[s]);
+    } else {
+      mbar_arrive(&sm.mbar[s]);
+    }
+  };
+  int pf_stage = -1;  // thread 0: stage of a prefetch still in flight
+  uint32_t pf_parity = 0;
+  if (BULK && STAGES == 2 && tid == 0 && cid < a.R) issue(cid, 0);
+
   for (int64_t r = cid, it = 0; r < a.R; r += nclusters, ++it) {
+    const int s = (STAGES == 2) ? static_cast<int>(it & 1) : 0;
+    const uint32_t parity = static_cast<uint32_t>(((STAGES == 2) ? (it >> 1) : it) & 1);
+    unsigned char *tbuf = dyn + static_cast<size_t>(s) * 2 * slice_bytes;
+    unsigned char *dbuf = tbuf + slice_bytes;
+    const uint32_t tb = smem_u32(tbuf), db = smem_u32(dbuf);
     // ---- fill the slices ----
     if (BULK) {
       if (tid == 0) {
-        const int64_t t = target_row_of(a, r);
-        sm.tr = t;
-        const uint32_t bytes = static_cast<uint32_t>(n) * E::kSize;
-        if (!sm.abort && t >= 0 && bytes > 0) {
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          mbar_arrive_expect_tx(&sm.mbar, 2 * bytes);
-          bulk_g2s(tbuf, static_cast<const char *>(a.target) + (t * V + lo) * E::kSize, bytes, &sm.mbar);
-          bulk_g2s(dbuf, static_cast<const char *>(a.draft) + (r * V + lo) * E::kSize, bytes, &sm.mbar);
+        if (STAGES == 2) {
+          pf_stage = -1;
+          if (r + nclusters < a.R) {
+            issue(r + nclusters, s ^ 1);
+            pf_stage = s ^ 1;
+            pf_parity = static_cast<uint32_t>(((it + 1) >> 1) & 1);
+          }
         } else {
-          mbar_arrive(&sm.mbar);
+          issue(r, 0);
         }
       }
-      if (!mbar_wait_bounded(&sm.mbar, static_cast<uint32_t>(it & 1))) {
+      if (!sm.abort && !mbar_wait_bounded(&sm.mbar[s], parity)) {
         if (a.status) atomicOr(a.status, SVW_DEV_TIMEOUT);
         sm.abort = 1;
       }
       __syncthreads();
     } else {
-      if (tid == 0) sm.tr = target_row_of(a, r);
+      if (tid == 0) sm.tr[s] = target_row_of(a, r);
       __syncthreads();
-      const int64_t t = sm.tr;
+      const int64_t t = sm.tr[s];
       if (t >= 0) {
         const char *ts = static_cast<const char *>(a.target) + (t * V + lo) * E::kSize;
         const char *ds = static_cast<const char *>(a.draft) + (r * V + lo) * E::kSize;
@@ -185,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 2) opd_kernel(OpdArgs a, int32_t SL,
       }
       __syncthreads();
     }
-    const bool valid = (sm.tr >= 0);
+    const bool valid = (sm.tr[s] >= 0);
     const bool work = valid && !sm.abort;
 
     // ---------------- pass A: maxima, then sums of exp2 ----------------
@@ -456,6 +482,320 @@ __global__ void __launch_bounds__(kThreads, 2) opd_kernel(OpdArgs a, int32_t SL,
     }
     __syncthreads();  // the slices are fully consumed before the next copy
   }
+  if (BULK && STAGES == 2 && tid == 0 && sm.abort && pf_stage >= 0)
+    mbar_wait_bounded(&sm.mbar[pf_stage], pf_parity);  // let a copy still in flight land
+  cluster.sync();  // peers may still read this CTA's partials
+}
+
+// Register-resident variant (16-byte-pitched rows).  Each thread owns the
+// 16-byte vectors tid + j*NT (j < VPT) of both slices: as soon as a row's bulk
+// copies land, every thread moves its vectors from shared memory into
+// registers and the buffer is handed straight back to the next row's copies,
+// so the next row streams in while this row's three passes run from registers.
+template <int DT, int NT, int VPT>
+__global__ void __launch_bounds__(NT, 2) opd_reg_kernel(OpdArgs a, int32_t SL, int32_t slice_bytes) {
+  using E = Elem<DT>;
+  constexpr int EPV = E::kPerVec;
+  constexpr int kWarps = NT / 32;
+  extern __shared__ __align__(128) unsigned char dyn[];
+  __shared__ OpdSmem sm;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int CL = static_cast<int>(cluster.num_blocks());
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t nclusters = gridDim.x / CL;
+  const int64_t cid = blockIdx.x / CL;
+  const int64_t V = a.V;
+  const int64_t lo = static_cast<int64_t>(rank) * SL;
+  const int n = static_cast<int>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(SL), V - lo)));
+  const int nvec = n / EPV;  // V is a multiple of EPV on this path: no tail
+  const int nj = (tid < nvec) ? min(VPT, (nvec - tid + NT - 1) / NT) : 0;  // my vectors
+  const float k = a.k;
+  unsigned char *tbuf = dyn;
+  unsigned char *dbuf = dyn + slice_bytes;
+  const uint32_t tb = smem_u32(tbuf), db = smem_u32(dbuf);
+
+  if (tid == 0) {
+    mbar_init(&sm.mbar[0], 1);
+    sm.abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  auto issue = [&](int64_t r) {
+    const int64_t t = target_row_of(a, r);
+    sm.tr[0] = t;
+    const uint32_t bytes = static_cast<uint32_t>(n) * E::kSize;
+    if (!sm.abort && t >= 0 && bytes > 0) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive_expect_tx(&sm.mbar[0], 2 * bytes);
+      bulk_g2s(tbuf, static_cast<const char *>(a.target) + (t * V + lo) * E::kSize, bytes, &sm.mbar[0]);
+      bulk_g2s(dbuf, static_cast<const char *>(a.draft) + (r * V + lo) * E::kSize, bytes, &sm.mbar[0]);
+    } else {
+      mbar_arrive(&sm.mbar[0]);
+    }
+  };
+  if (tid == 0 && cid < a.R) issue(cid);
+  bool issued_next = false;  // thread 0: a copy for a later row is in flight
+
+  for (int64_t r = cid, it = 0; r < a.R; r += nclusters, ++it) {
+    if (!sm.abort && !mbar_wait_bounded(&sm.mbar[0], static_cast<uint32_t>(it & 1))) {
+      if (a.status) atomicOr(a.status, SVW_DEV_TIMEOUT);
+      sm.abort = 1;
+    }
+    const bool valid = (sm.tr[0] >= 0);
+    uint4 ty[VPT], tz[VPT];
+#pragma unroll
+    for (int j = 0; j < VPT; ++j)
+      if (j < nj) {
+        ty[j] = lds128(tb + (tid + j * NT) * 16);
+        tz[j] = lds128(db + (tid + j * NT) * 16);
+      }
+    __syncthreads();  // the buffer is free: stream the next row in
+    if (tid == 0) {
+      issued_next = false;
+      if (r + nclusters < a.R) {
+        issue(r + nclusters);
+        issued_next = true;
+      }
+    }
+    const bool work = valid && !sm.abort;
+
+    // ---------------- pass A: maxima, then sums of exp2 ----------------
+    float mt = -INFINITY, md = -INFINITY, st = 0.f, sd = 0.f;
+    if (work) {
+#pragma unroll
+      for (int j = 0; j < VPT; ++j)
+        if (j < nj) {
+          mt = vec_max<DT>(ty[j], mt);
+          md = vec_max<DT>(tz[j], md);
+        }
+      const float nmt = (mt == -INFINITY) ? 0.f : -mt * k;
+      const float nmd = (md == -INFINITY) ? 0.f : -md * k;
+      const float2 kk = make_float2(k, k), nt2 = make_float2(nmt, nmt), nd2 = make_float2(nmd, nmd);
+      float2 at = make_float2(0.f, 0.f), ad = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < VPT; ++j)
+        if (j < nj) {
+          const Pairs<DT> y(ty[j]), z(tz[j]);
+#pragma unroll
+          for (int h = 0; h < Pairs<DT>::kN; ++h) {
+            const float2 ey = __ffma2_rn(y.p[h], kk, nt2);
+            const float2 ez = __ffma2_rn(z.p[h], kk, nd2);
+            at = __fadd2_rn(at, make_float2(ex2(ey.x), ex2(ey.y)));
+            ad = __fadd2_rn(ad, make_float2(ex2(ez.x), ex2(ez.y)));
+          }
+        }
+      st = at.x + at.y;
+      sd = ad.x + ad.y;
+    }
+    const float my_mt = mt;
+    warp_lse(mt, st, k);
+    warp_lse(md, sd, k);
+    if (lane == 0) {
+      sm.red[warp][0] = mt;
+      sm.red[warp][1] = st;
+      sm.red[warp][2] = md;
+      sm.red[warp][3] = sd;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      float a0 = -INFINITY, a1 = 0.f, a2 = -INFINITY, a3 = 0.f;
+      if (lane < kWarps) {
+        a0 = sm.red[lane][0];
+        a1 = sm.red[lane][1];
+        a2 = sm.red[lane][2];
+        a3 = sm.red[lane][3];
+      }
+      warp_lse(a0, a1, k);
+      warp_lse(a2, a3, k);
+      if (lane == 0) {
+        sm.partA[0] = a0;
+        sm.partA[1] = a1;
+        sm.partA[2] = a2;
+        sm.partA[3] = a3;
+        sm.partA[4] = sm.abort ? 1.f : 0.f;
+      }
+    }
+    cluster.sync();
+    if (warp == 0) {
+      float v0 = -INFINITY, v1 = 0.f, v2 = -INFINITY, v3 = 0.f, v4 = 0.f;
+      if (lane < CL) {
+        const float *pa = cluster.map_shared_rank(sm.partA, lane);
+        v0 = pa[0];
+        v1 = pa[1];
+        v2 = pa[2];
+        v3 = pa[3];
+        v4 = pa[4];
+      }
+      float M0 = -INFINITY, S0 = 0.f, M1 = -INFINITY, S1 = 0.f, ab = 0.f;
+      for (int q = 0; q < CL; ++q) {
+        lse_combine(M0, S0, __shfl_sync(0xffffffffu, v0, q), __shfl_sync(0xffffffffu, v1, q), k);
+        lse_combine(M1, S1, __shfl_sync(0xffffffffu, v2, q), __shfl_sync(0xffffffffu, v3, q), k);
+        ab += __shfl_sync(0xffffffffu, v4, q);
+      }
+      if (lane == 0) {
+        sm.rowA[0] = M0;
+        sm.rowA[1] = S0;
+        sm.rowA[2] = M1;
+        sm.rowA[3] = S1;
+        sm.rowA[4] = ab;
+      }
+    }
+    __syncthreads();
+    const float Mt = sm.rowA[0], St = sm.rowA[1], Md = sm.rowA[2], Sd = sm.rowA[3];
+    const bool any_abort = sm.rowA[4] != 0.f;
+    const bool row_ok = valid && !any_abort && (St > 0.f && St <= FLT_MAX) && (Sd > 0.f && Sd <= FLT_MAX);
+    const float Ct = fmaf(Mt, k, lg2(St));  // log2 p = y k - Ct
+    const float Cd = fmaf(Md, k, lg2(Sd));  // log2 q = z k - Cd
+    const float c2 = a.clip_c * kLog2e;     // clip bound in log2 units of t
+    float rkl = 0.f, S = 0.f;
+    int32_t cand = INT32_MAX;
+
+    // ---------------- pass B: clamped terms, S, argmax ----------------
+    if (row_ok) {
+      const float2 kk = make_float2(k, k), nkk = make_float2(-k, -k);
+      const float2 nCd = make_float2(-Cd, -Cd), Ct2 = make_float2(Ct, Ct), l2 = make_float2(kLn2, kLn2);
+      float2 r2 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < VPT; ++j)
+        if (j < nj) {
+          const Pairs<DT> y(ty[j]), z(tz[j]);
+#pragma unroll
+          for (int h = 0; h < Pairs<DT>::kN; ++h) {
+            const float2 A = __ffma2_rn(z.p[h], kk, nCd);                    // log2 q
+            const float2 q = make_float2(ex2(A.x), ex2(A.y));
+            const float2 d = __fadd2_rn(A, __ffma2_rn(y.p[h], nkk, Ct2));  // log2 q - log2 p
+            const float2 t = __fmul2_rn(q, d);                               // t / ln 2
+            if (fabsf(t.x) < c2 && fabsf(t.y) < c2) {
+              r2 = __fadd2_rn(r2, t);
+              s2 = __fadd2_rn(__ffma2_rn(t, l2, s2), q);
+            } else {
+              term_slow(t.x, q.x, c2, r2.x, s2.x);
+              term_slow(t.y, q.y, c2, r2.y, s2.y);
+            }
+          }
+        }
+      rkl = r2.x + r2.y;
+      S = s2.x + s2.y;
+      if (my_mt == Mt) {  // first index holding the row maximum
+#pragma unroll
+        for (int j = 0; j < VPT; ++j)
+          if (j < nj && cand == INT32_MAX) {
+            float y[EPV];
+            E::unpack(ty[j], y);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e)
+              if (cand == INT32_MAX && y[e] == Mt) cand = static_cast<int32_t>(lo + (tid + j * NT) * EPV + e);
+          }
+      }
+    }
+    rkl = warp_sum(rkl);
+    S = warp_sum(S);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, o));
+    if (lane == 0) {
+      sm.red[warp][0] = rkl;
+      sm.red[warp][1] = S;
+      sm.redi[warp] = cand;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      float r1 = (lane < kWarps) ? sm.red[lane][0] : 0.f;
+      float s1 = (lane < kWarps) ? sm.red[lane][1] : 0.f;
+      int32_t c1 = (lane < kWarps) ? sm.redi[lane] : INT32_MAX;
+      r1 = warp_sum(r1);
+      s1 = warp_sum(s1);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) c1 = min(c1, __shfl_xor_sync(0xffffffffu, c1, o));
+      if (lane == 0) {
+        sm.partB[0] = r1;
+        sm.partB[1] = s1;
+        sm.partB[2] = __int_as_float(c1);
+      }
+    }
+    cluster.sync();
+    if (warp == 0) {
+      float v0 = 0.f, v1 = 0.f;
+      int32_t v2 = INT32_MAX;
+      if (lane < CL) {
+        const float *pb = cluster.map_shared_rank(sm.partB, lane);
+        v0 = pb[0];
+        v1 = pb[1];
+        v2 = __float_as_int(pb[2]);
+      }
+      float R0 = 0.f, S0 = 0.f;
+      int32_t X = INT32_MAX;
+      for (int q = 0; q < CL; ++q) {
+        R0 += __shfl_sync(0xffffffffu, v0, q);
+        S0 += __shfl_sync(0xffffffffu, v1, q);
+        X = min(X, __shfl_sync(0xffffffffu, v2, q));
+      }
+      if (lane == 0) {
+        sm.rowB[0] = R0;
+        sm.rowB[1] = S0;
+        sm.rowB[2] = __int_as_float(X);
+      }
+    }
+    __syncthreads();
+    const float RKL2 = sm.rowB[0], SS = sm.rowB[1];
+    const int32_t xs = __float_as_int(sm.rowB[2]);
+    if (rank == 0 && tid == 0) {
+      float out = __int_as_float(0x7fffffff);
+      if (row_ok && xs != INT32_MAX) {
+        const float zx = E::load(a.draft, r * V + xs);
+        out = kLn2 * (RKL2 - a.lambda_ce * fmaf(zx, k, -Cd));
+      } else if (a.status && !any_abort) {
+        atomicOr(a.status, SVW_DEV_BAD_INPUT);
+      }
+      a.loss[r] = out;
+    }
+
+    // ---------------- pass C: gradient wrt the draft logits ----------------
+    if (a.dlogits != nullptr && valid && !any_abort) {
+      const float gsT = a.grad_scale * a.invT;
+      const float gL0 = gsT * (a.lambda_ce - SS);
+      const float gL1 = gsT * (a.lambda_ce - SS + 1.f);
+      const float nan = __int_as_float(0x7fffffff);
+      float *out = a.dlogits + r * V + lo;
+      const float2 kk = make_float2(k, k), nkk = make_float2(-k, -k);
+      const float2 nCd = make_float2(-Cd, -Cd), Ct2 = make_float2(Ct, Ct);
+      const float2 gl = make_float2(gsT * kLn2, gsT * kLn2), g1 = make_float2(gL1, gL1);
+#pragma unroll
+      for (int j = 0; j < VPT; ++j)
+        if (j < nj) {
+          const int vi = tid + j * NT;
+          const Pairs<DT> y(ty[j]), z(tz[j]);
+          float g[EPV];
+#pragma unroll
+          for (int h = 0; h < Pairs<DT>::kN; ++h) {
+            const float2 A = __ffma2_rn(z.p[h], kk, nCd);
+            const float2 q = make_float2(ex2(A.x), ex2(A.y));
+            const float2 t = __fmul2_rn(q, __fadd2_rn(A, __ffma2_rn(y.p[h], nkk, Ct2)));
+            float2 gg = __ffma2_rn(t, gl, __fmul2_rn(q, g1));
+            if (!(fabsf(t.x) < c2 && fabsf(t.y) < c2)) {
+              if (!(fabsf(t.x) < c2)) gg.x = q.x * gL0;
+              if (!(fabsf(t.y) < c2)) gg.y = q.y * gL0;
+            }
+            g[2 * h] = gg.x;
+            g[2 * h + 1] = gg.y;
+          }
+          const int off = static_cast<int>(xs - (lo + vi * EPV));
+          if (off >= 0 && off < EPV) {
+#pragma unroll
+            for (int e = 0; e < EPV; ++e)
+              if (e == off) g[e] -= gsT * a.lambda_ce;
+          }
+          if (!row_ok) {
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) g[e] = nan;
+          }
+#pragma unroll
+          for (int h = 0; h < EPV / 4; ++h)
+            st_stream(out + vi * EPV + 4 * h, g[4 * h], g[4 * h + 1], g[4 * h + 2], g[4 * h + 3]);
+        }
+    }
+  }
+  if (tid == 0 && sm.abort && issued_next) mbar_wait_bounded(&sm.mbar[0], 0);  // best effort drain
   cluster.sync();  // peers may still read this CTA's partials
 }
 
@@ -463,6 +803,7 @@ struct OpdPlan {
   int CL;
   int SL;
   int slice_bytes;
+  int stages;
   size_t smem;
 };
 
@@ -477,13 +818,15 @@ OpdPlan plan_opd(int64_t V, int esize) {
   p.CL = static_cast<int>(CL);
   p.SL = static_cast<int>(SL);
   p.slice_bytes = static_cast<int>((SL * esize + 127) / 128 * 128);
-  p.smem = static_cast<size_t>(p.slice_bytes) * 2;
+  const size_t stage = static_cast<size_t>(p.slice_bytes) * 2;
+  p.stages = 1;
+  p.smem = stage;
   return p;
 }
 
-template <int DT, bool BULK>
+template <int DT, bool BULK, int NT, int STAGES>
 cudaError_t launch_opd_t(const OpdArgs &a, const OpdPlan &p, cudaStream_t st) {
-  auto kern = opd_kernel<DT, BULK>;
+  auto kern = opd_kernel<DT, BULK, NT, STAGES>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(p.smem));
   if (e != cudaSuccess) return e;
@@ -493,7 +836,7 @@ cudaError_t launch_opd_t(const OpdArgs &a, const OpdPlan &p, cudaStream_t st) {
   attr[0].val.clusterDim.x = p.CL;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(NT, 1, 1);
   cfg.dynamicSmemBytes = p.smem;
   cfg.stream = st;
   cfg.attrs = attr;
@@ -531,6 +874,55 @@ cudaError_t launch_opd_t(const OpdArgs &a, const OpdPlan &p, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+template <int DT, int VPT>
+cudaError_t launch_opd_reg(const OpdArgs &a, const OpdPlan &p, cudaStream_t st) {
+  auto kern = opd_reg_kernel<DT, 512, VPT>;
+  const size_t smem = static_cast<size_t>(p.slice_bytes) * 2;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = p.CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(512, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  static int cached[64][9] = {};
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int &maxc = cached[dev & 63][p.CL];
+  if (maxc == 0) {
+    cfg.gridDim = dim3(p.CL * 1024, 1, 1);
+    e = cudaOccupancyMaxActiveClusters(&maxc, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (maxc <= 0) return cudaErrorInvalidConfiguration;
+  }
+  int64_t nclusters = maxc;
+  if (nclusters > a.R) nclusters = a.R;
+  cfg.gridDim = dim3(static_cast<unsigned>(nclusters * p.CL), 1, 1);
+  e = cudaLaunchKernelEx(&cfg, kern, a, p.SL, p.slice_bytes);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+template <int DT, bool BULK>
+cudaError_t launch_opd_cfg(const OpdArgs &a, const OpdPlan &p, cudaStream_t st) {
+  if (BULK) {
+    const int nvec = static_cast<int>(static_cast<int64_t>(p.SL) * Elem<DT>::kSize / 16);
+    const int vpt = (nvec + 511) / 512;
+    if (vpt <= 1) return launch_opd_reg<DT, 1>(a, p, st);
+    if (vpt <= 2) return launch_opd_reg<DT, 2>(a, p, st);
+    if (vpt <= 3) return launch_opd_reg<DT, 3>(a, p, st);
+    if (vpt <= 5) return launch_opd_reg<DT, 5>(a, p, st);
+  }
+  return launch_opd_t<DT, BULK, 512, 1>(a, p, st);
+}
+
 }  // namespace
 
 bool opd_supported(int64_t V, int esize) { return plan_opd(V, esize).smem <= 200 * 1024; }
@@ -539,8 +931,8 @@ cudaError_t launch_opd(const OpdArgs &a, int dtype, bool bulk, cudaStream_t st) 
   const int esize = (dtype == SVW_BF16) ? 2 : 4;
   const OpdPlan p = plan_opd(a.V, esize);
   if (p.smem > 200 * 1024) return cudaErrorInvalidValue;
-  if (dtype == SVW_BF16) return bulk ? launch_opd_t<1, true>(a, p, st) : launch_opd_t<1, false>(a, p, st);
-  return bulk ? launch_opd_t<0, true>(a, p, st) : launch_opd_t<0, false>(a, p, st);
+  if (dtype == SVW_BF16) return bulk ? launch_opd_cfg<1, true>(a, p, st) : launch_opd_cfg<1, false>(a, p, st);
+  return bulk ? launch_opd_cfg<0, true>(a, p, st) : launch_opd_cfg<0, false>(a, p, st);
 }
 
 }  // namespace svw

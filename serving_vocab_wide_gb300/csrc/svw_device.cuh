@@ -87,6 +87,13 @@ __device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
   return *reinterpret_cast<const uint32_t *>(&r);
 }
 
+// elementwise bf16 max that propagates NaN
+__device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t a, uint32_t b) {
+  const __nv_bfloat162 r = __hmax2_nan(*reinterpret_cast<const __nv_bfloat162 *>(&a),
+                                       *reinterpret_cast<const __nv_bfloat162 *>(&b));
+  return *reinterpret_cast<const uint32_t *>(&r);
+}
+
 // nonzero if either bf16 half of w is a NaN
 __device__ __forceinline__ uint32_t bf16x2_nan(uint32_t w) {
   return ((w & 0x7fff7fffu) + 0x007f007fu) & 0x80008000u;

@@ -190,12 +190,12 @@ __device__ __forceinline__ void warp_amax_smem(uint32_t base, int nvec, int32_t 
   float mx = -INFINITY;
   uint32_t nanw = 0;
   if (DT == 1) {
-    uint32_t mw = 0xff80ff80u;
+    uint32_t mw = 0xff80ff80u;  // NaN-propagating max: a NaN anywhere survives
     for (int vi = v0; vi < nvec; vi += kCW * 32) {
       const uint4 q = lds128(base + vi * 16);
-      mw = bf16x2_max(mw, bf16x2_max(bf16x2_max(q.x, q.y), bf16x2_max(q.z, q.w)));
-      nanw |= bf16x2_nan(q.x) | bf16x2_nan(q.y) | bf16x2_nan(q.z) | bf16x2_nan(q.w);
+      mw = bf16x2_max_nan(mw, bf16x2_max_nan(bf16x2_max_nan(q.x, q.y), bf16x2_max_nan(q.z, q.w)));
     }
+    nanw = bf16x2_nan(mw);
     const float2 f = bf16x2_f2(mw);
     mx = fmaxf(f.x, f.y);
   } else {
