@@ -145,6 +145,36 @@ svw_status opd_loss(const void *target_logits, const void *draft_logits, svw_dty
                     float lambda_ce, float grad_scale, float *loss, float *dlogits,
                     int32_t *status, void *stream);
 
+/*
+ * spec_verify_noalloc -- spec_verify for callers that cannot allocate device
+ * memory.  No counterpart on the pages: it exists only because some callers
+ * have no allocator to hand over a workspace (a plain C serving loop, a
+ * plug-in inside an engine whose memory pool is sized up front and which
+ * forbids cudaMalloc -- a device-synchronising call -- mid-step, a thin launch
+ * wrapper that only forwards tensors).
+ *
+ * Same arguments and results as spec_verify, minus the workspace: the library
+ * keeps one fixed scratch area of SVW_NOALLOC_SCRATCH_BYTES per GPU (a
+ * file-scope device array, resident for the life of the process on every GPU
+ * that loads the library).  This call allocates nothing and frees nothing.
+ *  - Batches whose svw_verify_workspace_size(...) exceeds the scratch return
+ *    SVW_ERR_UNSUPPORTED without launching (e.g. N = 256 requests, 4096 draft
+ *    rows at V = 151936 bf16 fit).
+ *  - The first call on each device looks the scratch's device address up
+ *    (cudaGetSymbolAddress with that device current); make that first call
+ *    before capturing the stream into a graph.
+ *  - All calls share the scratch.  Calls whose kernels may overlap on the GPU
+ *    (different streams without ordering, several host threads) race on it and
+ *    corrupt each other's results; serialise them on one stream.
+ */
+#define SVW_NOALLOC_SCRATCH_BYTES (32u << 20)
+svw_status spec_verify_noalloc(const void *target_logits, const void *draft_logits, svw_dtype dtype,
+                               int32_t V, int32_t N, const int32_t *cu_draft,
+                               int64_t total_draft_rows, int32_t max_len,
+                               const int32_t *draft_tokens, float temperature, uint64_t seed,
+                               int32_t *accept_len, int32_t *next_token, int32_t *status,
+                               void *stream);
+
 /* Human-readable name of a status code (static string). */
 const char *svw_status_string(svw_status s);
 

@@ -50,6 +50,9 @@ def lib():
             L.opd_loss.argtypes = [P, P, ctypes.c_int, I32, I32, P, I64, I32, F, F, F, F,
                                    P, P, P, P]
             L.opd_loss.restype = ctypes.c_int
+            L.spec_verify_noalloc.argtypes = [P, P, ctypes.c_int, I32, I32, P, I64, I32, P, F, U64,
+                                              P, P, P, P]
+            L.spec_verify_noalloc.restype = ctypes.c_int
             L.svw_status_string.argtypes = [ctypes.c_int]
             L.svw_status_string.restype = ctypes.c_char_p
             L.svw_version.argtypes = []
@@ -122,6 +125,31 @@ def spec_verify(target, draft, cu_draft, draft_tokens, temperature: float, seed:
                            _ptr(draft_tokens), float(temperature), int(seed) & (2**64 - 1),
                            _ptr(accept_len), _ptr(next_token), _ptr(status), _ptr(workspace),
                            workspace.numel(), _stream_ptr(stream))
+    _check(rc)
+    return accept_len, next_token
+
+
+def spec_verify_noalloc(target, draft, cu_draft, draft_tokens, temperature: float, seed: int,
+                        max_len: int = SVW_MAX_LEN, total_draft_rows: int | None = None,
+                        accept_len=None, next_token=None, status=None, stream=None):
+    """spec_verify on the library's fixed per-GPU scratch instead of a caller
+    workspace (for callers that cannot allocate).  Calls that may overlap on
+    the GPU share that scratch and must be serialised on one stream."""
+    import torch
+    _need_cuda(target, draft, cu_draft, draft_tokens)
+    N = cu_draft.numel() - 1
+    V = target.shape[-1]
+    R = int(cu_draft[-1].item()) if total_draft_rows is None else int(total_draft_rows)
+    dev = target.device
+    if accept_len is None:
+        accept_len = torch.empty(N, dtype=torch.int32, device=dev)
+    if next_token is None:
+        next_token = torch.empty(N, dtype=torch.int32, device=dev)
+    _need_cuda(accept_len, next_token, status)
+    rc = lib().spec_verify_noalloc(_ptr(target), _ptr(draft), _dtype_code(target), V, N,
+                                   _ptr(cu_draft), R, max_len, _ptr(draft_tokens),
+                                   float(temperature), int(seed) & (2**64 - 1), _ptr(accept_len),
+                                   _ptr(next_token), _ptr(status), _stream_ptr(stream))
     _check(rc)
     return accept_len, next_token
 
