@@ -161,6 +161,12 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # native arm
 # ---------------------------------------------------------------------------
+def launches_per_step():
+    """Kernels one step launches: spec_verify = prologue + stats + finalize
+    (+ sample at T > 0); opd_loss = fast pass + exact fix-up."""
+    return sum(3 if T == 0 else 4 for T in TEMPS) + 2
+
+
 def run_native(args, ws, rank, local):
     import torch
     import serving_vocab_wide_gb300 as svw
@@ -190,6 +196,7 @@ def run_native(args, ws, rank, local):
     tok = {T: h_tok[T].to(dev) for T in TEMPS}
     ws_bytes = svw.verify_workspace_size(N, R, V, svw.SVW_BF16)
     wsp = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    opd_ws = torch.empty(svw.opd_workspace_size(R), dtype=torch.uint8, device=dev)
     acc = {T: torch.empty(N, dtype=torch.int32, device=dev) for T in TEMPS}
     nxt = {T: torch.empty(N, dtype=torch.int32, device=dev) for T in TEMPS}
     loss = torch.empty(R, dtype=torch.float32, device=dev)
@@ -210,7 +217,7 @@ def run_native(args, ws, rank, local):
         if ev is not None:
             ev[6].record(stream)
         svw.opd_loss(t, d, cu_draft=cu, has_bonus=True, loss=loss, dlogits=grad,
-                     status=status, stream=stream, **OPD)
+                     status=status, workspace=opd_ws, stream=stream, **OPD)
         if ev is not None:
             ev[7].record(stream)
 
@@ -323,7 +330,7 @@ def run_native(args, ws, rank, local):
                     for c in calls},
         "step_gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,
         "e2e": e2e,
-        "gpu_launches": K * (2 * len(TEMPS) + 1),
+        "gpu_launches": K * launches_per_step(),
         "clocks": clk.summary(),
         "device_status": status_v,
         "cpu_baseline": cpu,

@@ -50,7 +50,7 @@ typedef enum svw_status {
   SVW_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, bad temperature ... */
   SVW_ERR_UNSUPPORTED = 2, /* dtype or size outside what the kernels handle         */
   SVW_ERR_MISALIGNED = 3,  /* a pointer violates its documented alignment            */
-  SVW_ERR_WORKSPACE = 4,   /* workspace missing or smaller than svw_verify_workspace_size */
+  SVW_ERR_WORKSPACE = 4,   /* workspace missing or smaller than its *_workspace_size  */
   SVW_ERR_CUDA = 5         /* a CUDA runtime call or kernel launch failed            */
 } svw_status;
 
@@ -138,12 +138,21 @@ svw_status spec_verify(const void *target_logits, const void *draft_logits, svw_
  *   status        as for spec_verify (SVW_DEV_BAD_INPUT for a non-finite row
  *                 or a row outside its request's CSR range; SVW_DEV_TIMEOUT if
  *                 a bounded wait on a bulk copy gave up).
+ *   workspace     device, 256-byte aligned, >= svw_opd_workspace_size(
+ *                 total_draft_rows) bytes, contents need not be initialised,
+ *                 not preserved; or NULL.  With a workspace, rows whose byte
+ *                 pitch is a multiple of 16 take a one-exchange fast pass and
+ *                 only rows where some term reaches the clip (or the draft has
+ *                 masked entries) are recomputed exactly; the results are the
+ *                 same either way (up to float rounding order).
  */
+size_t svw_opd_workspace_size(int64_t total_draft_rows);
+
 svw_status opd_loss(const void *target_logits, const void *draft_logits, svw_dtype dtype,
                     int32_t V, int32_t N, const int32_t *cu_draft, int64_t total_draft_rows,
                     int32_t target_has_bonus_row, float temperature, float clip_c,
                     float lambda_ce, float grad_scale, float *loss, float *dlogits,
-                    int32_t *status, void *stream);
+                    int32_t *status, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * spec_verify_noalloc -- spec_verify for callers that cannot allocate device

@@ -47,8 +47,10 @@ def lib():
             L.spec_verify.argtypes = [P, P, ctypes.c_int, I32, I32, P, I64, I32, P, F, U64,
                                       P, P, P, P, SZ, P]
             L.spec_verify.restype = ctypes.c_int
+            L.svw_opd_workspace_size.argtypes = [I64]
+            L.svw_opd_workspace_size.restype = SZ
             L.opd_loss.argtypes = [P, P, ctypes.c_int, I32, I32, P, I64, I32, F, F, F, F,
-                                   P, P, P, P]
+                                   P, P, P, P, SZ, P]
             L.opd_loss.restype = ctypes.c_int
             L.spec_verify_noalloc.argtypes = [P, P, ctypes.c_int, I32, I32, P, I64, I32, P, F, U64,
                                               P, P, P, P]
@@ -93,6 +95,10 @@ def _need_cuda(*ts):
 
 def verify_workspace_size(n_requests: int, total_draft_rows: int, V: int, dtype_code: int) -> int:
     return int(lib().svw_verify_workspace_size(n_requests, total_draft_rows, V, dtype_code))
+
+
+def opd_workspace_size(total_draft_rows: int) -> int:
+    return int(lib().svw_opd_workspace_size(total_draft_rows))
 
 
 def spec_verify(target, draft, cu_draft, draft_tokens, temperature: float, seed: int,
@@ -157,9 +163,13 @@ def spec_verify_noalloc(target, draft, cu_draft, draft_tokens, temperature: floa
 def opd_loss(target, draft, temperature: float = 1.0, clip_c: float = 1.0,
              lambda_ce: float = 0.1, grad_scale: float = 1.0, cu_draft=None,
              has_bonus: bool = False, want_grad: bool = True, loss=None, dlogits=None,
-             status=None, stream=None):
+             status=None, workspace=None, exact_only: bool = False, stream=None):
     """Clipped reverse-KL + lambda*CE per draft row, and its gradient wrt the
-    draft logits.  Returns (loss [R] fp32, dlogits [R, V] fp32 or None)."""
+    draft logits.  Returns (loss [R] fp32, dlogits [R, V] fp32 or None).
+
+    A workspace (uint8, >= opd_workspace_size(R) bytes) is allocated when not
+    given; exact_only=True passes none, so that every row takes the exact
+    three-pass kernel."""
     import torch
     _need_cuda(target, draft, cu_draft)
     R, V = draft.shape
@@ -170,10 +180,15 @@ def opd_loss(target, draft, temperature: float = 1.0, clip_c: float = 1.0,
         loss = torch.empty(R, dtype=torch.float32, device=dev)
     if want_grad and dlogits is None:
         dlogits = torch.empty((R, V), dtype=torch.float32, device=dev)
-    _need_cuda(loss, dlogits, status)
+    if exact_only:
+        workspace = None
+    elif workspace is None:
+        workspace = torch.empty(max(1, opd_workspace_size(R)), dtype=torch.uint8, device=dev)
+    _need_cuda(loss, dlogits, status, workspace)
     rc = lib().opd_loss(_ptr(target), _ptr(draft), code, V, N, _ptr(cu_draft) if has_bonus else None,
                         R, 1 if has_bonus else 0, float(temperature), float(clip_c),
                         float(lambda_ce), float(grad_scale), _ptr(loss),
-                        _ptr(dlogits) if want_grad else None, _ptr(status), _stream_ptr(stream))
+                        _ptr(dlogits) if want_grad else None, _ptr(status), _ptr(workspace),
+                        0 if workspace is None else workspace.numel(), _stream_ptr(stream))
     _check(rc)
     return loss, (dlogits if want_grad else None)

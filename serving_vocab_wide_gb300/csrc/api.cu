@@ -103,11 +103,19 @@ svw_status spec_verify(const void *target_logits, const void *draft_logits, svw_
   return e == cudaSuccess ? SVW_OK : SVW_ERR_CUDA;
 }
 
+// OPD workspace: flags int32 [R] | row constants float4 [R], each 256-aligned
+static size_t opd_flags_bytes(int64_t R) { return static_cast<size_t>((R * 4 + 255) / 256 * 256); }
+
+size_t svw_opd_workspace_size(int64_t total_draft_rows) {
+  if (total_draft_rows <= 0 || total_draft_rows > (int64_t{1} << 40)) return 0;
+  return opd_flags_bytes(total_draft_rows) + static_cast<size_t>((total_draft_rows * 16 + 255) / 256 * 256);
+}
+
 svw_status opd_loss(const void *target_logits, const void *draft_logits, svw_dtype dtype,
                     int32_t V, int32_t N, const int32_t *cu_draft, int64_t total_draft_rows,
                     int32_t target_has_bonus_row, float temperature, float clip_c,
                     float lambda_ce, float grad_scale, float *loss, float *dlogits,
-                    int32_t *status, void *stream) {
+                    int32_t *status, void *workspace, size_t workspace_bytes, void *stream) {
   if (dtype != SVW_F32 && dtype != SVW_BF16) return SVW_ERR_UNSUPPORTED;
   if (V <= 0 || total_draft_rows <= 0) return SVW_ERR_INVALID_ARG;
   if (target_has_bonus_row && (N <= 0 || !cu_draft)) return SVW_ERR_INVALID_ARG;
@@ -121,8 +129,9 @@ svw_status opd_loss(const void *target_logits, const void *draft_logits, svw_dty
   if (!svw::opd_supported(V, es)) return SVW_ERR_UNSUPPORTED;
   if (!aligned(target_logits, es) || !aligned(draft_logits, es) || !aligned(loss, 4) ||
       (dlogits && !aligned(dlogits, 16)) || (cu_draft && !aligned(cu_draft, 4)) ||
-      (status && !aligned(status, 4)))
+      (status && !aligned(status, 4)) || (workspace && !aligned(workspace, 256)))
     return SVW_ERR_MISALIGNED;
+  if (workspace && workspace_bytes < svw_opd_workspace_size(total_draft_rows)) return SVW_ERR_WORKSPACE;
   const bool bulk = ((static_cast<int64_t>(V) * es) % 16 == 0) && aligned(target_logits, 16) &&
                     aligned(draft_logits, 16);
   svw::OpdArgs a;
@@ -141,6 +150,9 @@ svw_status opd_loss(const void *target_logits, const void *draft_logits, svw_dty
   a.loss = loss;
   a.dlogits = dlogits;
   a.status = status;
+  a.flags = static_cast<int32_t *>(workspace);
+  a.rowc = workspace ? reinterpret_cast<float4 *>(static_cast<char *>(workspace) + opd_flags_bytes(total_draft_rows))
+                     : nullptr;
   const cudaError_t e = svw::launch_opd(a, dtype, bulk, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SVW_OK : SVW_ERR_CUDA;
 }

@@ -11,25 +11,29 @@
 //
 // GPU design.  A thread-block cluster of CL CTAs (CL <= 8) owns one row at a
 // time; CTA r of the cluster holds vocabulary slice [r*SL, (r+1)*SL) of both
-// the target and the draft row in shared memory (76 KB at V = 151936 bf16,
-// so two CTAs of different clusters share an SM and overlap one's copies
-// with the other's arithmetic).
-//   * The slices arrive by 1-D bulk asynchronous copies (cp.async.bulk, one
-//     per tensor per CTA, completion counted on an mbarrier): HBM sees each
-//     logit byte once.
-//   * Pass A: packed bf16 max, then sum of exp2 for both rows -> CTA partial
-//     -> DSMEM exchange (barrier.cluster) -> every CTA merges the CL partials
-//     in rank order, so all CTAs hold identical row constants.
-//   * Pass B: clamped terms and S; the threads holding the row maximum look
-//     up the first argmax index -> second exchange.
-//   * Pass C: dz with 16-byte streaming stores.
+// the target and the draft row (76 KB at V = 151936 bf16, two CTAs of
+// different clusters per SM).  Slices arrive by 1-D bulk async copies
+// (cp.async.bulk, mbarrier completion): HBM sees each logit byte once.
+//
+// Fast kernel (16-byte-pitched rows).  Each thread moves its vectors of the
+// slices from shared memory into registers as soon as they land, and the
+// buffer is handed to the next row's copies at once.  One pass over the
+// registers gives, per row, both log-sum-exps, the target argmax with the
+// draft logit there, and U = sum_v 2^((z_v - m_z)k) ((z_v - m_z)k - (y_v - m_y)k),
+// so that without clipping
+//   KL(q||p) = ln2 (U/S_z - log2 S_z + log2 S_y),  S = sum_v q_v a_v = KL + 1;
+// one DSMEM exchange (barrier.cluster) merges these over the cluster, and a
+// second register pass writes the gradient.  An entry whose term reaches the
+// clip bound, or a non-finite KL (masked entries), flags the row.
+// Exact kernel.  Rows the fast kernel flagged (and every row of shapes that
+// are not 16-byte pitched) are redone from shared memory in three passes:
+// log-sum-exps; clamped terms, S and the argmax; gradient -- two exchanges.
 // In log2 units: A = log2 q = z k - Cd, Bp = log2 p = y k - Ct, d2 = A - Bp,
-// t/ln2 = q d2, q(d + 1) = t + q; the per-entry arithmetic runs on f32x2
-// pairs.  Entries whose term is clipped, or undefined (q = 0 against an
-// infinite log ratio, a term of 0), take a scalar slow path.
+// t/ln2 = q d2, q(d + 1) = t + q; per-entry arithmetic runs on f32x2 pairs.
 // Every wait on a bulk copy is bounded by a clock deadline; on expiry the CTA
 // records SVW_DEV_TIMEOUT, stops issuing copies and keeps joining the cluster
 // barriers so that no peer can hang.
+#include <algorithm>
 #include <cfloat>
 #include <climits>
 #include <cooperative_groups.h>
@@ -48,16 +52,25 @@ namespace {
 constexpr int kMaxWarps = 32;
 constexpr int kMaxCluster = 8;
 
+// per-launch geometry: slice length and bytes per CTA, entries of the fast
+// kernel's target-row table (verify layout)
+struct OpdGeo {
+  int32_t SL;
+  int32_t slice_bytes;
+  int32_t ntab;
+};
+
 struct OpdSmem {
-  unsigned long long mbar[2];
+  unsigned long long mbar;
   float red[kMaxWarps][4];
   int32_t redi[kMaxWarps];
   float partA[8];  // this CTA's mt, st, md, sd, abort
   float partB[4];  // this CTA's rkl (log2 units), S, argmax candidate (bits)
   float rowA[8];   // merged over the cluster: Mt, St, Md, Sd, any abort
   float rowB[4];   // merged over the cluster: rkl, S, argmax (bits)
-  int64_t tr[2];   // target row of the row in each stage (-1: outside its request)
+  int64_t tr;      // target row of the current row (-1: outside its request)
   int32_t abort;
+  uint32_t abort_parity;  // phase of the copy that timed out
 };
 
 // target row paired with draft row r, or -1 if r lies outside its request's
@@ -116,11 +129,11 @@ __device__ __forceinline__ void term_slow(float t2, float q, float c2, float &rk
   }
 }
 
-// NT threads per CTA; STAGES = 1: one slice buffer, two CTAs per SM overlap
-// each other's copies; STAGES = 2: the next row's slices are prefetched into
-// the second buffer while the current row is processed (one CTA per SM).
-template <int DT, bool BULK, int NT, int STAGES>
-__global__ void __launch_bounds__(NT, (STAGES == 1 ? 2 : 1)) opd_kernel(OpdArgs a, int32_t SL, int32_t slice_bytes) {
+// Exact three-pass kernel (every row; the path without a workspace).
+template <int DT, bool BULK>
+__global__ void __launch_bounds__(512, 2) opd_exact_kernel(OpdArgs a, OpdGeo geo) {
+  constexpr int NT = 512;
+  const int32_t SL = geo.SL, slice_bytes = geo.slice_bytes;
   using E = Elem<DT>;
   constexpr int EPV = E::kPerVec;
   constexpr int kThreads = NT;
@@ -140,62 +153,47 @@ __global__ void __launch_bounds__(NT, (STAGES == 1 ? 2 : 1)) opd_kernel(OpdArgs 
   const float k = a.k;
 
   if (tid == 0) {
-    mbar_init(&sm.mbar[0], 1);
-    mbar_init(&sm.mbar[1], 1);
+    mbar_init(&sm.mbar, 1);
     sm.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
 
-  // thread 0: start the bulk copies of row r's slices into stage s
-  auto issue = [&](int64_t r, int s) {
+  unsigned char *tbuf = dyn;
+  unsigned char *dbuf = dyn + slice_bytes;
+  const uint32_t tb = smem_u32(tbuf), db = smem_u32(dbuf);
+  // thread 0: start the bulk copies of row r's slices (after a timeout the
+  // barrier is left alone: its phase never completed)
+  auto issue = [&](int64_t r) {
     const int64_t t = target_row_of(a, r);
-    sm.tr[s] = t;
-    unsigned char *tb = dyn + static_cast<size_t>(s) * 2 * slice_bytes;
+    sm.tr = t;
     const uint32_t bytes = static_cast<uint32_t>(n) * E::kSize;
-    if (!sm.abort && t >= 0 && bytes > 0) {
+    if (sm.abort) return;
+    if (t >= 0 && bytes > 0) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive_expect_tx(&sm.mbar[s], 2 * bytes);
-      bulk_g2s(tb, static_cast<const char *>(a.target) + (t * V + lo) * E::kSize, bytes, &sm.mbar[s]);
-      bulk_g2s(tb + slice_bytes, static_cast<const char *>(a.draft) + (r * V + lo) * E::kSize, bytes,
-               &sm.mbar[s]);
+      mbar_arrive_expect_tx(&sm.mbar, 2 * bytes);
+      bulk_g2s(tbuf, static_cast<const char *>(a.target) + (t * V + lo) * E::kSize, bytes, &sm.mbar);
+      bulk_g2s(dbuf, static_cast<const char *>(a.draft) + (r * V + lo) * E::kSize, bytes, &sm.mbar);
     } else {
-      mbar_arrive(&sm.mbar[s]);
+      mbar_arrive(&sm.mbar);
     }
   };
-  int pf_stage = -1;  // thread 0: stage of a prefetch still in flight
-  uint32_t pf_parity = 0;
-  if (BULK && STAGES == 2 && tid == 0 && cid < a.R) issue(cid, 0);
 
-  for (int64_t r = cid, it = 0; r < a.R; r += nclusters, ++it) {
-    const int s = (STAGES == 2) ? static_cast<int>(it & 1) : 0;
-    const uint32_t parity = static_cast<uint32_t>(((STAGES == 2) ? (it >> 1) : it) & 1);
-    unsigned char *tbuf = dyn + static_cast<size_t>(s) * 2 * slice_bytes;
-    unsigned char *dbuf = tbuf + slice_bytes;
-    const uint32_t tb = smem_u32(tbuf), db = smem_u32(dbuf);
+  for (int64_t r = cid, it = 0; r < a.R; r += nclusters) {
+    const uint32_t parity = static_cast<uint32_t>(it & 1);
     // ---- fill the slices ----
     if (BULK) {
-      if (tid == 0) {
-        if (STAGES == 2) {
-          pf_stage = -1;
-          if (r + nclusters < a.R) {
-            issue(r + nclusters, s ^ 1);
-            pf_stage = s ^ 1;
-            pf_parity = static_cast<uint32_t>(((it + 1) >> 1) & 1);
-          }
-        } else {
-          issue(r, 0);
-        }
-      }
-      if (!sm.abort && !mbar_wait_bounded(&sm.mbar[s], parity)) {
+      if (tid == 0) issue(r);
+      if (!sm.abort && !mbar_wait_bounded(&sm.mbar, parity)) {
         if (a.status) atomicOr(a.status, SVW_DEV_TIMEOUT);
+        sm.abort_parity = parity;
         sm.abort = 1;
       }
       __syncthreads();
     } else {
-      if (tid == 0) sm.tr[s] = target_row_of(a, r);
+      if (tid == 0) sm.tr = target_row_of(a, r);
       __syncthreads();
-      const int64_t t = sm.tr[s];
+      const int64_t t = sm.tr;
       if (t >= 0) {
         const char *ts = static_cast<const char *>(a.target) + (t * V + lo) * E::kSize;
         const char *ds = static_cast<const char *>(a.draft) + (r * V + lo) * E::kSize;
@@ -211,7 +209,7 @@ __global__ void __launch_bounds__(NT, (STAGES == 1 ? 2 : 1)) opd_kernel(OpdArgs 
       }
       __syncthreads();
     }
-    const bool valid = (sm.tr[s] >= 0);
+    const bool valid = (sm.tr >= 0);
     const bool work = valid && !sm.abort;
 
     // ---------------- pass A: maxima, then sums of exp2 ----------------
@@ -481,24 +479,123 @@ __global__ void __launch_bounds__(NT, (STAGES == 1 ? 2 : 1)) opd_kernel(OpdArgs 
       }
     }
     __syncthreads();  // the slices are fully consumed before the next copy
+    ++it;
   }
-  if (BULK && STAGES == 2 && tid == 0 && sm.abort && pf_stage >= 0)
-    mbar_wait_bounded(&sm.mbar[pf_stage], pf_parity);  // let a copy still in flight land
+  // after a timeout no copy is issued; let the one that timed out land if it can
+  if (BULK && tid == 0 && sm.abort) mbar_wait_bounded(&sm.mbar, sm.abort_parity);
   cluster.sync();  // peers may still read this CTA's partials
 }
 
-// Register-resident variant (16-byte-pitched rows).  Each thread owns the
-// 16-byte vectors tid + j*NT (j < VPT) of both slices: as soon as a row's bulk
-// copies land, every thread moves its vectors from shared memory into
-// registers and the buffer is handed straight back to the next row's copies,
-// so the next row streams in while this row's three passes run from registers.
-template <int DT, int NT, int VPT>
-__global__ void __launch_bounds__(NT, 2) opd_reg_kernel(OpdArgs a, int32_t SL, int32_t slice_bytes) {
+// Partial row statistics of the fast kernel over some vocabulary entries,
+// relative to offsets m_y, m_z (their maxima):
+//   s_y = sum 2^((y - m_y)k),  s_z = sum 2^((z - m_z)k),
+//   u   = sum 2^((z - m_z)k) ((z - m_z)k - (y - m_y)k),
+// and the first index holding the target maximum with the draft logit there.
+struct __align__(16) FastPart {
+  float my, sy, mz, sz, u;
+  int32_t idx;
+  float zx;
+  int32_t abort;
+};
+
+__device__ __forceinline__ FastPart empty_part() {
+  FastPart p;
+  p.my = -INFINITY;
+  p.mz = -INFINITY;
+  p.sy = 0.f;
+  p.sz = 0.f;
+  p.u = 0.f;
+  p.idx = INT32_MAX;
+  p.zx = 0.f;
+  p.abort = 0;
+  return p;
+}
+
+// Merge the partials held by lanes [0, SPAN) of a warp (SPAN a power of two;
+// lanes beyond the data hold empty partials).  Each lane rescales its own
+// partial to the merged offsets (one exp2 per sum, all lanes at once), then
+// the sums are added by a fixed butterfly, so every warp that merges the same
+// partials gets bit-identical results.  A NaN sum (a NaN or +Inf logit)
+// stays NaN; a non-finite u only makes the KL non-finite.
+template <int SPAN>
+__device__ __forceinline__ FastPart merge_lanes(const FastPart &p, float k) {
+  float My = p.my, Mz = p.mz;
+#pragma unroll
+  for (int o = SPAN / 2; o > 0; o >>= 1) {
+    My = fmaxf(My, __shfl_xor_sync(0xffffffffu, My, o));
+    Mz = fmaxf(Mz, __shfl_xor_sync(0xffffffffu, Mz, o));
+  }
+  const bool hy = p.my != -INFINITY, hz = p.mz != -INFINITY;
+  const float dy = hy ? (p.my - My) * k : 0.f;
+  const float dz = hz ? (p.mz - Mz) * k : 0.f;
+  float sy = p.sy * (hy ? ex2(dy) : 0.f);
+  const float fz = hz ? ex2(dz) : 0.f;
+  float sz = p.sz * fz;
+  float u = hz ? fz * (p.u + p.sz * (dz - dy)) : (p.u != p.u ? p.u : 0.f);
+#pragma unroll
+  for (int o = SPAN / 2; o > 0; o >>= 1) {
+    sy += __shfl_xor_sync(0xffffffffu, sy, o);
+    sz += __shfl_xor_sync(0xffffffffu, sz, o);
+    u += __shfl_xor_sync(0xffffffffu, u, o);
+  }
+  const int32_t cand = (p.my == My) ? p.idx : INT32_MAX;
+  const int32_t best = static_cast<int32_t>(__reduce_min_sync(0xffffffffu, static_cast<uint32_t>(cand)));
+  const uint32_t holders = __ballot_sync(0xffffffffu, cand == best);
+  const float zx = __shfl_sync(0xffffffffu, p.zx, holders ? __ffs(holders) - 1 : 0);
+  FastPart r;
+  r.my = My;
+  r.mz = Mz;
+  r.sy = sy;
+  r.sz = sz;
+  r.u = u;
+  r.idx = best;
+  r.zx = zx;
+  r.abort = __any_sync(0xffffffffu, p.abort != 0) ? 1 : 0;
+  return r;
+}
+
+struct FastSmem {
+  unsigned long long mbar;
+  FastPart red[16];  // one partial per warp
+  // this CTA's partial, read by the peers; double-buffered because a peer may
+  // still read row r's while this CTA writes row r+1's (one exchange per row)
+  FastPart part[2];
+  FastPart row;  // merged over the cluster
+  int64_t tr;
+  uint32_t nread;  // warps done reading the slice buffer (16 per row)
+  int32_t abort;
+  uint32_t abort_parity;  // phase of the copy that timed out
+};
+
+// Called by every thread after its reads of the slice buffer for the it-th
+// row.  True in exactly one thread (lane 0 of the last warp to finish): that
+// thread may overwrite the buffer.  The acq_rel counter orders every warp's
+// reads before the overwrite; the async proxy is fenced by the copy issue.
+template <int kWarps>
+__device__ __forceinline__ bool last_warp_done(uint32_t *cnt, int64_t it) {
+  __syncwarp();
+  bool last = false;
+  if ((threadIdx.x & 31) == 0) {
+    uint32_t prev;
+    asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;" : "=r"(prev) : "r"(smem_u32(cnt)) : "memory");
+    last = (prev == static_cast<uint32_t>(kWarps * it + kWarps - 1));
+  }
+  return last;
+}
+
+// named barriers: warps 1..15 arrive, warp 0 waits (only warp 0 acts on them)
+__device__ __forceinline__ void named_arrive(int id, int nt) { asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nt) : "memory"); }
+__device__ __forceinline__ void named_sync(int id, int nt) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nt) : "memory"); }
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait;" ::: "memory"); }
+
+template <int DT, int VPT, int NT>
+__global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) {
   using E = Elem<DT>;
-  constexpr int EPV = E::kPerVec;
   constexpr int kWarps = NT / 32;
+  constexpr int EPV = E::kPerVec;
   extern __shared__ __align__(128) unsigned char dyn[];
-  __shared__ OpdSmem sm;
+  __shared__ FastSmem sm;
   cg::cluster_group cluster = cg::this_cluster();
   const int CL = static_cast<int>(cluster.num_blocks());
   const int rank = static_cast<int>(cluster.block_rank());
@@ -506,43 +603,54 @@ __global__ void __launch_bounds__(NT, 2) opd_reg_kernel(OpdArgs a, int32_t SL, i
   const int64_t nclusters = gridDim.x / CL;
   const int64_t cid = blockIdx.x / CL;
   const int64_t V = a.V;
-  const int64_t lo = static_cast<int64_t>(rank) * SL;
-  const int n = static_cast<int>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(SL), V - lo)));
+  const int64_t lo = static_cast<int64_t>(rank) * geo.SL;
+  const int n = static_cast<int>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(geo.SL), V - lo)));
   const int nvec = n / EPV;  // V is a multiple of EPV on this path: no tail
-  const int nj = (tid < nvec) ? min(VPT, (nvec - tid + NT - 1) / NT) : 0;  // my vectors
+  const int nj = (tid < nvec) ? min(VPT, (nvec - tid + NT - 1) / NT) : 0;
   const float k = a.k;
   unsigned char *tbuf = dyn;
-  unsigned char *dbuf = dyn + slice_bytes;
+  unsigned char *dbuf = dyn + geo.slice_bytes;
+  int32_t *tab = reinterpret_cast<int32_t *>(dyn + 2 * static_cast<size_t>(geo.slice_bytes));
   const uint32_t tb = smem_u32(tbuf), db = smem_u32(dbuf);
 
   if (tid == 0) {
-    mbar_init(&sm.mbar[0], 1);
+    mbar_init(&sm.mbar, 1);
     sm.abort = 0;
+    sm.nread = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  auto issue = [&](int64_t r) {
-    const int64_t t = target_row_of(a, r);
-    sm.tr[0] = t;
+  // one thread: start the bulk copies of draft row r (target row t)
+  auto issue = [&](int64_t r, int64_t t) {
+    sm.tr = t;
     const uint32_t bytes = static_cast<uint32_t>(n) * E::kSize;
-    if (!sm.abort && t >= 0 && bytes > 0) {
+    if (sm.abort) return;  // after a timeout the barrier is left alone
+    if (t >= 0 && bytes > 0) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive_expect_tx(&sm.mbar[0], 2 * bytes);
-      bulk_g2s(tbuf, static_cast<const char *>(a.target) + (t * V + lo) * E::kSize, bytes, &sm.mbar[0]);
-      bulk_g2s(dbuf, static_cast<const char *>(a.draft) + (r * V + lo) * E::kSize, bytes, &sm.mbar[0]);
+      mbar_arrive_expect_tx(&sm.mbar, 2 * bytes);
+      bulk_g2s(tbuf, static_cast<const char *>(a.target) + (t * V + lo) * E::kSize, bytes, &sm.mbar);
+      bulk_g2s(dbuf, static_cast<const char *>(a.draft) + (r * V + lo) * E::kSize, bytes, &sm.mbar);
     } else {
-      mbar_arrive(&sm.mbar[0]);
+      mbar_arrive(&sm.mbar);
     }
   };
-  if (tid == 0 && cid < a.R) issue(cid);
-  bool issued_next = false;  // thread 0: a copy for a later row is in flight
+  if (tid == 0 && cid < a.R) issue(cid, target_row_of(a, cid));
+  // target rows of this cluster's later rows (verify layout), looked up once
+  for (int q = 1 + tid; q < geo.ntab; q += NT) {
+    const int64_t r = cid + q * nclusters;
+    tab[q] = (r < a.R) ? static_cast<int32_t>(target_row_of(a, r)) : -1;
+  }
+  __syncthreads();
 
   for (int64_t r = cid, it = 0; r < a.R; r += nclusters, ++it) {
-    if (!sm.abort && !mbar_wait_bounded(&sm.mbar[0], static_cast<uint32_t>(it & 1))) {
+    if (rank == 0 && tid == 0) a.flags[r] = 0;  // before this row's exchange
+    if (!sm.abort && !mbar_wait_bounded(&sm.mbar, static_cast<uint32_t>(it & 1))) {
       if (a.status) atomicOr(a.status, SVW_DEV_TIMEOUT);
+      sm.abort_parity = static_cast<uint32_t>(it & 1);
       sm.abort = 1;
     }
-    const bool valid = (sm.tr[0] >= 0);
+    const int64_t sm_tr_row = sm.tr;
+    const bool valid = (sm_tr_row >= 0);
     uint4 ty[VPT], tz[VPT];
 #pragma unroll
     for (int j = 0; j < VPT; ++j)
@@ -550,253 +658,459 @@ __global__ void __launch_bounds__(NT, 2) opd_reg_kernel(OpdArgs a, int32_t SL, i
         ty[j] = lds128(tb + (tid + j * NT) * 16);
         tz[j] = lds128(db + (tid + j * NT) * 16);
       }
-    __syncthreads();  // the buffer is free: stream the next row in
-    if (tid == 0) {
-      issued_next = false;
-      if (r + nclusters < a.R) {
-        issue(r + nclusters);
-        issued_next = true;
-      }
-    }
     const bool work = valid && !sm.abort;
+    // the buffer is free once every warp holds its vectors: the last warp to
+    // get there streams the next row in, nobody waits
+    if (last_warp_done<kWarps>(&sm.nread, it)) {
+      const int64_t rn = r + nclusters;
+      if (rn < a.R) {
+        const int64_t q = it + 1;
+        const int64_t tn = !a.has_bonus ? rn : (q < geo.ntab ? static_cast<int64_t>(tab[q]) : target_row_of(a, rn));
+        issue(rn, tn);
+      }
+    }
 
-    // ---------------- pass A: maxima, then sums of exp2 ----------------
-    float mt = -INFINITY, md = -INFINITY, st = 0.f, sd = 0.f;
+    // ---------------- pass 1: row statistics ----------------
+    FastPart P = empty_part();
+    P.abort = sm.abort;
     if (work) {
-#pragma unroll
-      for (int j = 0; j < VPT; ++j)
-        if (j < nj) {
-          mt = vec_max<DT>(ty[j], mt);
-          md = vec_max<DT>(tz[j], md);
-        }
-      const float nmt = (mt == -INFINITY) ? 0.f : -mt * k;
-      const float nmd = (md == -INFINITY) ? 0.f : -md * k;
-      const float2 kk = make_float2(k, k), nt2 = make_float2(nmt, nmt), nd2 = make_float2(nmd, nmd);
-      float2 at = make_float2(0.f, 0.f), ad = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int j = 0; j < VPT; ++j)
-        if (j < nj) {
-          const Pairs<DT> y(ty[j]), z(tz[j]);
-#pragma unroll
-          for (int h = 0; h < Pairs<DT>::kN; ++h) {
-            const float2 ey = __ffma2_rn(y.p[h], kk, nt2);
-            const float2 ez = __ffma2_rn(z.p[h], kk, nd2);
-            at = __fadd2_rn(at, make_float2(ex2(ey.x), ex2(ey.y)));
-            ad = __fadd2_rn(ad, make_float2(ex2(ez.x), ex2(ez.y)));
-          }
-        }
-      st = at.x + at.y;
-      sd = ad.x + ad.y;
-    }
-    const float my_mt = mt;
-    warp_lse(mt, st, k);
-    warp_lse(md, sd, k);
-    if (lane == 0) {
-      sm.red[warp][0] = mt;
-      sm.red[warp][1] = st;
-      sm.red[warp][2] = md;
-      sm.red[warp][3] = sd;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      float a0 = -INFINITY, a1 = 0.f, a2 = -INFINITY, a3 = 0.f;
-      if (lane < kWarps) {
-        a0 = sm.red[lane][0];
-        a1 = sm.red[lane][1];
-        a2 = sm.red[lane][2];
-        a3 = sm.red[lane][3];
-      }
-      warp_lse(a0, a1, k);
-      warp_lse(a2, a3, k);
-      if (lane == 0) {
-        sm.partA[0] = a0;
-        sm.partA[1] = a1;
-        sm.partA[2] = a2;
-        sm.partA[3] = a3;
-        sm.partA[4] = sm.abort ? 1.f : 0.f;
-      }
-    }
-    cluster.sync();
-    if (warp == 0) {
-      float v0 = -INFINITY, v1 = 0.f, v2 = -INFINITY, v3 = 0.f, v4 = 0.f;
-      if (lane < CL) {
-        const float *pa = cluster.map_shared_rank(sm.partA, lane);
-        v0 = pa[0];
-        v1 = pa[1];
-        v2 = pa[2];
-        v3 = pa[3];
-        v4 = pa[4];
-      }
-      float M0 = -INFINITY, S0 = 0.f, M1 = -INFINITY, S1 = 0.f, ab = 0.f;
-      for (int q = 0; q < CL; ++q) {
-        lse_combine(M0, S0, __shfl_sync(0xffffffffu, v0, q), __shfl_sync(0xffffffffu, v1, q), k);
-        lse_combine(M1, S1, __shfl_sync(0xffffffffu, v2, q), __shfl_sync(0xffffffffu, v3, q), k);
-        ab += __shfl_sync(0xffffffffu, v4, q);
-      }
-      if (lane == 0) {
-        sm.rowA[0] = M0;
-        sm.rowA[1] = S0;
-        sm.rowA[2] = M1;
-        sm.rowA[3] = S1;
-        sm.rowA[4] = ab;
-      }
-    }
-    __syncthreads();
-    const float Mt = sm.rowA[0], St = sm.rowA[1], Md = sm.rowA[2], Sd = sm.rowA[3];
-    const bool any_abort = sm.rowA[4] != 0.f;
-    const bool row_ok = valid && !any_abort && (St > 0.f && St <= FLT_MAX) && (Sd > 0.f && Sd <= FLT_MAX);
-    const float Ct = fmaf(Mt, k, lg2(St));  // log2 p = y k - Ct
-    const float Cd = fmaf(Md, k, lg2(Sd));  // log2 q = z k - Cd
-    const float c2 = a.clip_c * kLog2e;     // clip bound in log2 units of t
-    float rkl = 0.f, S = 0.f;
-    int32_t cand = INT32_MAX;
-
-    // ---------------- pass B: clamped terms, S, argmax ----------------
-    if (row_ok) {
-      const float2 kk = make_float2(k, k), nkk = make_float2(-k, -k);
-      const float2 nCd = make_float2(-Cd, -Cd), Ct2 = make_float2(Ct, Ct), l2 = make_float2(kLn2, kLn2);
-      float2 r2 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int j = 0; j < VPT; ++j)
-        if (j < nj) {
-          const Pairs<DT> y(ty[j]), z(tz[j]);
-#pragma unroll
-          for (int h = 0; h < Pairs<DT>::kN; ++h) {
-            const float2 A = __ffma2_rn(z.p[h], kk, nCd);                    // log2 q
-            const float2 q = make_float2(ex2(A.x), ex2(A.y));
-            const float2 d = __fadd2_rn(A, __ffma2_rn(y.p[h], nkk, Ct2));  // log2 q - log2 p
-            const float2 t = __fmul2_rn(q, d);                               // t / ln 2
-            if (fabsf(t.x) < c2 && fabsf(t.y) < c2) {
-              r2 = __fadd2_rn(r2, t);
-              s2 = __fadd2_rn(__ffma2_rn(t, l2, s2), q);
-            } else {
-              term_slow(t.x, q.x, c2, r2.x, s2.x);
-              term_slow(t.y, q.y, c2, r2.y, s2.y);
-            }
-          }
-        }
-      rkl = r2.x + r2.y;
-      S = s2.x + s2.y;
-      if (my_mt == Mt) {  // first index holding the row maximum
+      float my, mz;
+      if (DT == 1) {
+        uint32_t py = 0xff80ff80u, pz = 0xff80ff80u;
 #pragma unroll
         for (int j = 0; j < VPT; ++j)
-          if (j < nj && cand == INT32_MAX) {
-            float y[EPV];
-            E::unpack(ty[j], y);
+          if (j < nj) {
+            py = bf16x2_max(py, bf16x2_max(bf16x2_max(ty[j].x, ty[j].y), bf16x2_max(ty[j].z, ty[j].w)));
+            pz = bf16x2_max(pz, bf16x2_max(bf16x2_max(tz[j].x, tz[j].y), bf16x2_max(tz[j].z, tz[j].w)));
+          }
+        const float2 fy = bf16x2_f2(py), fz = bf16x2_f2(pz);
+        my = fmaxf(fy.x, fy.y);
+        mz = fmaxf(fz.x, fz.y);
+      } else {
+        my = -INFINITY;
+        mz = -INFINITY;
 #pragma unroll
-            for (int e = 0; e < EPV; ++e)
-              if (cand == INT32_MAX && y[e] == Mt) cand = static_cast<int32_t>(lo + (tid + j * NT) * EPV + e);
+        for (int j = 0; j < VPT; ++j)
+          if (j < nj) {
+            my = vec_max<DT>(ty[j], my);
+            mz = vec_max<DT>(tz[j], mz);
           }
       }
-    }
-    rkl = warp_sum(rkl);
-    S = warp_sum(S);
+      // warp offsets
+      float My = my, Mz = mz;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) cand = min(cand, __shfl_xor_sync(0xffffffffu, cand, o));
-    if (lane == 0) {
-      sm.red[warp][0] = rkl;
-      sm.red[warp][1] = S;
-      sm.redi[warp] = cand;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      float r1 = (lane < kWarps) ? sm.red[lane][0] : 0.f;
-      float s1 = (lane < kWarps) ? sm.red[lane][1] : 0.f;
-      int32_t c1 = (lane < kWarps) ? sm.redi[lane] : INT32_MAX;
-      r1 = warp_sum(r1);
-      s1 = warp_sum(s1);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) c1 = min(c1, __shfl_xor_sync(0xffffffffu, c1, o));
-      if (lane == 0) {
-        sm.partB[0] = r1;
-        sm.partB[1] = s1;
-        sm.partB[2] = __int_as_float(c1);
+      for (int o = 16; o > 0; o >>= 1) {
+        My = fmaxf(My, __shfl_xor_sync(0xffffffffu, My, o));
+        Mz = fmaxf(Mz, __shfl_xor_sync(0xffffffffu, Mz, o));
       }
+      // first index of the warp's target maximum (only its holders look)
+      int32_t idx = INT32_MAX;
+      float zx = 0.f;
+      if (my == My) {
+#pragma unroll
+        for (int j = 0; j < VPT; ++j)
+          if (j < nj && idx == INT32_MAX) {
+            float y[EPV], z[EPV];
+            E::unpack(ty[j], y);
+            E::unpack(tz[j], z);
+#pragma unroll
+            for (int e = EPV - 1; e >= 0; --e)
+              if (y[e] == My) {
+                idx = static_cast<int32_t>(lo + (tid + j * NT) * EPV + e);
+                zx = z[e];
+              }
+          }
+      }
+      const float nmy = (My == -INFINITY) ? 0.f : -My * k;
+      const float nmz = (Mz == -INFINITY) ? 0.f : -Mz * k;
+      const float2 kk = make_float2(k, k), ny2 = make_float2(nmy, nmy), nz2 = make_float2(nmz, nmz);
+      const float2 neg1 = make_float2(-1.f, -1.f);
+      float2 sy = make_float2(0.f, 0.f), sz = make_float2(0.f, 0.f), uu = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < VPT; ++j)
+        if (j < nj) {
+          const Pairs<DT> y(ty[j]), z(tz[j]);
+#pragma unroll
+          for (int h = 0; h < Pairs<DT>::kN; ++h) {
+            const float2 ay = __ffma2_rn(y.p[h], kk, ny2);  // (y - m_y) k
+            const float2 az = __ffma2_rn(z.p[h], kk, nz2);  // (z - m_z) k
+            const float2 ez = make_float2(ex2(az.x), ex2(az.y));
+            sy = __fadd2_rn(sy, make_float2(ex2(ay.x), ex2(ay.y)));
+            sz = __fadd2_rn(sz, ez);
+            uu = __ffma2_rn(ez, __ffma2_rn(ay, neg1, az), uu);
+          }
+        }
+      float s0 = sy.x + sy.y, s1 = sz.x + sz.y, s2 = uu.x + uu.y;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+        s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+        s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+      }
+      const int32_t best = static_cast<int32_t>(__reduce_min_sync(0xffffffffu, static_cast<uint32_t>(idx)));
+      const uint32_t holders = __ballot_sync(0xffffffffu, idx == best);
+      P.my = My;
+      P.mz = Mz;
+      P.sy = s0;
+      P.sz = s1;
+      P.u = s2;
+      P.idx = best;
+      P.zx = __shfl_sync(0xffffffffu, zx, holders ? __ffs(holders) - 1 : 0);
     }
-    cluster.sync();
+    if (lane == 0) sm.red[warp] = P;
+    FastPart Rw;
     if (warp == 0) {
-      float v0 = 0.f, v1 = 0.f;
-      int32_t v2 = INT32_MAX;
+      named_sync(2, NT);  // every warp's partial is in
+      const FastPart Pc = merge_lanes<kWarps>(lane < kWarps ? sm.red[lane] : empty_part(), k);
+      if (lane == 0) sm.part[it & 1] = Pc;
+      cluster_arrive();
+      cluster_wait();
+      FastPart Pq = empty_part();
       if (lane < CL) {
-        const float *pb = cluster.map_shared_rank(sm.partB, lane);
-        v0 = pb[0];
-        v1 = pb[1];
-        v2 = __float_as_int(pb[2]);
+        const uint4 *src = reinterpret_cast<const uint4 *>(cluster.map_shared_rank(&sm.part[it & 1], lane));
+        uint4 w0 = src[0], w1 = src[1];
+        Pq.my = __uint_as_float(w0.x);
+        Pq.sy = __uint_as_float(w0.y);
+        Pq.mz = __uint_as_float(w0.z);
+        Pq.sz = __uint_as_float(w0.w);
+        Pq.u = __uint_as_float(w1.x);
+        Pq.idx = static_cast<int32_t>(w1.y);
+        Pq.zx = __uint_as_float(w1.z);
+        Pq.abort = static_cast<int32_t>(w1.w);
       }
-      float R0 = 0.f, S0 = 0.f;
-      int32_t X = INT32_MAX;
-      for (int q = 0; q < CL; ++q) {
-        R0 += __shfl_sync(0xffffffffu, v0, q);
-        S0 += __shfl_sync(0xffffffffu, v1, q);
-        X = min(X, __shfl_sync(0xffffffffu, v2, q));
-      }
-      if (lane == 0) {
-        sm.rowB[0] = R0;
-        sm.rowB[1] = S0;
-        sm.rowB[2] = __int_as_float(X);
-      }
+      const FastPart M = merge_lanes<kMaxCluster>(Pq, k);
+      if (lane == 0) sm.row = M;
+    } else {
+      named_arrive(2, NT);
+      cluster_arrive();
     }
-    __syncthreads();
-    const float RKL2 = sm.rowB[0], SS = sm.rowB[1];
-    const int32_t xs = __float_as_int(sm.rowB[2]);
+    __syncthreads();  // the merged row is published
+    if (warp != 0) cluster_wait();  // long complete: warp 0 waited on it before publishing
+    Rw = sm.row;
+    const bool any_abort = Rw.abort != 0;
+    const bool row_ok = valid && !any_abort && (Rw.sy > 0.f && Rw.sy <= FLT_MAX) && (Rw.sz > 0.f && Rw.sz <= FLT_MAX);
+    const float lsy = lg2(Rw.sy), lsz = lg2(Rw.sz);
+    const float Ct = fmaf(Rw.my, k, lsy);  // log2 p = y k - Ct
+    const float Cd = fmaf(Rw.mz, k, lsz);  // log2 q = z k - Cd
+    const float kl = kLn2 * (Rw.u / Rw.sz - lsz + lsy);  // unclipped KL(q||p)
+    const float c2 = a.clip_c * kLog2e;                  // clip bound for t / ln 2
+    const int32_t xs = Rw.idx;
+    const bool exact = (kl == kl) && fabsf(kl) <= FLT_MAX;
     if (rank == 0 && tid == 0) {
       float out = __int_as_float(0x7fffffff);
       if (row_ok && xs != INT32_MAX) {
-        const float zx = E::load(a.draft, r * V + xs);
-        out = kLn2 * (RKL2 - a.lambda_ce * fmaf(zx, k, -Cd));
+        out = kl - a.lambda_ce * kLn2 * fmaf(Rw.zx, k, -Cd);
+        if (!exact) a.flags[r] = 1;  // masked entries: the fix-up kernel redoes this row
+        const int64_t t = sm_tr_row;
+        a.rowc[r] = make_float4(Ct, Cd, __int_as_float(xs),
+                                __int_as_float(t < (int64_t{1} << 31) ? static_cast<int32_t>(t) : -2));
       } else if (a.status && !any_abort) {
         atomicOr(a.status, SVW_DEV_BAD_INPUT);
       }
       a.loss[r] = out;
     }
 
-    // ---------------- pass C: gradient wrt the draft logits ----------------
-    if (a.dlogits != nullptr && valid && !any_abort) {
+    // ---------------- pass 2: gradient wrt the draft logits ----------------
+    // dz = gsT q (d + 1 - S + lambda) - gsT lambda [v = x*] with S = KL + 1,
+    // d = ln2 d2:  dz = q (d2 gsT ln2 + gsT (lambda - KL)).
+    if (valid && !any_abort && (a.dlogits != nullptr || row_ok)) {
       const float gsT = a.grad_scale * a.invT;
-      const float gL0 = gsT * (a.lambda_ce - SS);
-      const float gL1 = gsT * (a.lambda_ce - SS + 1.f);
-      const float nan = __int_as_float(0x7fffffff);
-      float *out = a.dlogits + r * V + lo;
       const float2 kk = make_float2(k, k), nkk = make_float2(-k, -k);
       const float2 nCd = make_float2(-Cd, -Cd), Ct2 = make_float2(Ct, Ct);
-      const float2 gl = make_float2(gsT * kLn2, gsT * kLn2), g1 = make_float2(gL1, gL1);
+      float tmax = 0.f;  // largest |t| / ln2 seen by this thread
+      if (a.dlogits != nullptr) {
+        const float nan = __int_as_float(0x7fffffff);
+        float *out = a.dlogits + r * V + lo;
+        const float2 gl = make_float2(gsT * kLn2, gsT * kLn2);
+        const float g0 = gsT * (a.lambda_ce - kl);
+        const float2 g02 = make_float2(g0, g0);
+#pragma unroll
+        for (int j = 0; j < VPT; ++j)
+          if (j < nj) {
+            const int vi = tid + j * NT;
+            const Pairs<DT> y(ty[j]), z(tz[j]);
+            float g[EPV];
+#pragma unroll
+            for (int h = 0; h < Pairs<DT>::kN; ++h) {
+              const float2 A = __ffma2_rn(z.p[h], kk, nCd);                    // log2 q
+              const float2 q = make_float2(ex2(A.x), ex2(A.y));
+              const float2 d = __fadd2_rn(A, __ffma2_rn(y.p[h], nkk, Ct2));  // log2 q - log2 p
+              const float2 t = __fmul2_rn(q, d);                               // t / ln 2
+              tmax = fmaxf(tmax, fmaxf(fabsf(t.x), fabsf(t.y)));
+              const float2 gg = __fmul2_rn(q, __ffma2_rn(d, gl, g02));
+              g[2 * h] = gg.x;
+              g[2 * h + 1] = gg.y;
+            }
+            const int off = static_cast<int>(xs - (lo + vi * EPV));
+            if (off >= 0 && off < EPV) {
+#pragma unroll
+              for (int e = 0; e < EPV; ++e)
+                if (e == off) g[e] -= gsT * a.lambda_ce;
+            }
+            if (!row_ok) {
+#pragma unroll
+              for (int e = 0; e < EPV; ++e) g[e] = nan;
+            }
+#pragma unroll
+            for (int h = 0; h < EPV / 4; ++h)
+              st_stream(out + vi * EPV + 4 * h, g[4 * h], g[4 * h + 1], g[4 * h + 2], g[4 * h + 3]);
+          }
+      } else {
+#pragma unroll
+        for (int j = 0; j < VPT; ++j)
+          if (j < nj) {
+            const Pairs<DT> y(ty[j]), z(tz[j]);
+#pragma unroll
+            for (int h = 0; h < Pairs<DT>::kN; ++h) {
+              const float2 A = __ffma2_rn(z.p[h], kk, nCd);
+              const float2 q = make_float2(ex2(A.x), ex2(A.y));
+              const float2 t = __fmul2_rn(q, __fadd2_rn(A, __ffma2_rn(y.p[h], nkk, Ct2)));
+              tmax = fmaxf(tmax, fmaxf(fabsf(t.x), fabsf(t.y)));
+            }
+          }
+      }
+      // some term reached the clip: the fix-up kernel redoes the row
+      if (row_ok && !(tmax < c2)) a.flags[r] = 1;
+    }
+  }
+  // after a timeout no copy is issued; let the one that timed out land if it can
+  if (tid == 0 && sm.abort) mbar_wait_bounded(&sm.mbar, sm.abort_parity);
+  cluster.sync();  // peers may still read this CTA's partials
+}
+
+// Fix-up kernel: redoes exactly the rows the fast kernel flagged, from the
+// row constants it stored (log-sum-exps, x*, target row): one pass for the
+// clamped terms and S, one cluster exchange, one pass for the gradient.
+// Flagged rows are dealt to clusters in order of appearance (the k-th flagged
+// row of a batch of kFixBatch rows goes to cluster k mod nclusters), so a
+// cluster gets at most one row more than any other.
+constexpr int kFixBatch = 4096;  // flags scanned per batch
+
+struct FixSmem {
+  unsigned long long mbar;
+  float2 red[16];
+  float4 part[2];  // this CTA's (RKL2, S, abort); double-buffered as in the fast kernel
+  float4 row;
+  int32_t wcnt[16];
+  int32_t total;
+  uint32_t nread;
+  int64_t tr;
+  int32_t abort;
+  uint32_t abort_parity;
+};
+
+template <int DT, int VPT, int NT>
+__global__ void __launch_bounds__(NT, 2) opd_fix_kernel(OpdArgs a, OpdGeo geo) {
+  using E = Elem<DT>;
+  constexpr int kWarps = NT / 32;
+  constexpr int kPer = kFixBatch / NT;  // flags per thread
+  constexpr int EPV = E::kPerVec;
+  extern __shared__ __align__(128) unsigned char dyn[];
+  __shared__ FixSmem sm;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int CL = static_cast<int>(cluster.num_blocks());
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t nclusters = gridDim.x / CL;
+  const int64_t cid = blockIdx.x / CL;
+  const int64_t V = a.V;
+  const int64_t lo = static_cast<int64_t>(rank) * geo.SL;
+  const int n = static_cast<int>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(geo.SL), V - lo)));
+  const int nvec = n / EPV;
+  const int nj = (tid < nvec) ? min(VPT, (nvec - tid + NT - 1) / NT) : 0;
+  const float k = a.k;
+  unsigned char *tbuf = dyn;
+  unsigned char *dbuf = dyn + geo.slice_bytes;
+  int32_t *list = reinterpret_cast<int32_t *>(dyn + 2 * static_cast<size_t>(geo.slice_bytes));
+  const uint32_t tb = smem_u32(tbuf), db = smem_u32(dbuf);
+  const float c2 = a.clip_c * kLog2e;
+
+  if (tid == 0) {
+    mbar_init(&sm.mbar, 1);
+    sm.abort = 0;
+    sm.nread = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  auto issue = [&](int64_t r) {
+    const float4 rc = __ldcg(a.rowc + r);
+    const int32_t t32 = __float_as_int(rc.w);
+    const int64_t t = (t32 >= 0) ? t32 : target_row_of(a, r);
+    sm.tr = t;
+    const uint32_t bytes = static_cast<uint32_t>(n) * E::kSize;
+    if (sm.abort) return;
+    if (t >= 0 && bytes > 0) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive_expect_tx(&sm.mbar, 2 * bytes);
+      bulk_g2s(tbuf, static_cast<const char *>(a.target) + (t * V + lo) * E::kSize, bytes, &sm.mbar);
+      bulk_g2s(dbuf, static_cast<const char *>(a.draft) + (r * V + lo) * E::kSize, bytes, &sm.mbar);
+    } else {
+      mbar_arrive(&sm.mbar);
+    }
+  };
+
+  int64_t it = 0;  // rows processed (mbarrier phase)
+  for (int64_t base = 0; base < a.R; base += kFixBatch) {
+    // ---- this cluster's flagged rows of the batch, in order ----
+    int32_t f[kPer];
+    int cnt = 0;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      const int64_t r = base + tid * kPer + e;
+      f[e] = (r < a.R) ? __ldcg(a.flags + r) : 0;
+      cnt += (f[e] != 0);
+    }
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) sm.wcnt[warp] = incl;
+    __syncthreads();
+    int before = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const int c = sm.wcnt[w];
+      before += (w < warp) ? c : 0;
+      total += c;
+    }
+    int g = before + incl - cnt;  // ordinal of this thread's first flagged row
+#pragma unroll
+    for (int e = 0; e < kPer; ++e)
+      if (f[e] != 0) {
+        if (g % nclusters == cid) list[g / nclusters] = static_cast<int32_t>(tid * kPer + e);
+        ++g;
+      }
+    const int mine = (cid < total) ? static_cast<int>((total - cid + nclusters - 1) / nclusters) : 0;
+    __syncthreads();  // list complete; also: every thread has read sm.wcnt
+    if (tid == 0 && mine > 0) issue(base + list[0]);
+
+    for (int i = 0; i < mine; ++i, ++it) {
+      const int64_t r = base + list[i];
+      const float4 rc = __ldcg(a.rowc + r);
+      if (!sm.abort && !mbar_wait_bounded(&sm.mbar, static_cast<uint32_t>(it & 1))) {
+        if (a.status) atomicOr(a.status, SVW_DEV_TIMEOUT);
+        sm.abort_parity = static_cast<uint32_t>(it & 1);
+        sm.abort = 1;
+      }
+      const bool valid = (sm.tr >= 0);
+      uint4 ty[VPT], tz[VPT];
 #pragma unroll
       for (int j = 0; j < VPT; ++j)
         if (j < nj) {
-          const int vi = tid + j * NT;
-          const Pairs<DT> y(ty[j]), z(tz[j]);
-          float g[EPV];
+          ty[j] = lds128(tb + (tid + j * NT) * 16);
+          tz[j] = lds128(db + (tid + j * NT) * 16);
+        }
+      const bool work = valid && !sm.abort;
+      if (last_warp_done<kWarps>(&sm.nread, it) && i + 1 < mine) issue(base + list[i + 1]);
+
+      const float Ct = rc.x, Cd = rc.y;
+      const int32_t xs = __float_as_int(rc.z);
+      const float2 kk = make_float2(k, k), nkk = make_float2(-k, -k);
+      const float2 nCd = make_float2(-Cd, -Cd), Ct2 = make_float2(Ct, Ct), l2 = make_float2(kLn2, kLn2);
+      // ---- clamped terms and S ----
+      float rkl = 0.f, S = 0.f;
+      if (work) {
+        float2 r2 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int h = 0; h < Pairs<DT>::kN; ++h) {
-            const float2 A = __ffma2_rn(z.p[h], kk, nCd);
-            const float2 q = make_float2(ex2(A.x), ex2(A.y));
-            const float2 t = __fmul2_rn(q, __fadd2_rn(A, __ffma2_rn(y.p[h], nkk, Ct2)));
-            float2 gg = __ffma2_rn(t, gl, __fmul2_rn(q, g1));
-            if (!(fabsf(t.x) < c2 && fabsf(t.y) < c2)) {
+        for (int j = 0; j < VPT; ++j)
+          if (j < nj) {
+            const Pairs<DT> y(ty[j]), z(tz[j]);
+#pragma unroll
+            for (int h = 0; h < Pairs<DT>::kN; ++h) {
+              const float2 A = __ffma2_rn(z.p[h], kk, nCd);
+              const float2 q = make_float2(ex2(A.x), ex2(A.y));
+              const float2 t = __fmul2_rn(q, __fadd2_rn(A, __ffma2_rn(y.p[h], nkk, Ct2)));
+              if (fabsf(t.x) < c2 && fabsf(t.y) < c2) {
+                r2 = __fadd2_rn(r2, t);
+                s2 = __fadd2_rn(__ffma2_rn(t, l2, s2), q);
+              } else {
+                term_slow(t.x, q.x, c2, r2.x, s2.x);
+                term_slow(t.y, q.y, c2, r2.y, s2.y);
+              }
+            }
+          }
+        rkl = r2.x + r2.y;
+        S = s2.x + s2.y;
+      }
+      rkl = warp_sum(rkl);
+      S = warp_sum(S);
+      if (lane == 0) sm.red[warp] = make_float2(rkl, S);
+      if (warp == 0) {
+        named_sync(2, NT);
+        float2 v = (lane < kWarps) ? sm.red[lane] : make_float2(0.f, 0.f);
+#pragma unroll
+        for (int o = kWarps / 2; o > 0; o >>= 1) {
+          v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+          v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+        }
+        if (lane == 0) sm.part[it & 1] = make_float4(v.x, v.y, sm.abort ? 1.f : 0.f, 0.f);
+        cluster_arrive();
+        cluster_wait();
+        float4 pq = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (lane < CL) pq = *cluster.map_shared_rank(&sm.part[it & 1], lane);
+#pragma unroll
+        for (int o = kMaxCluster / 2; o > 0; o >>= 1) {
+          pq.x += __shfl_xor_sync(0xffffffffu, pq.x, o);
+          pq.y += __shfl_xor_sync(0xffffffffu, pq.y, o);
+          pq.z += __shfl_xor_sync(0xffffffffu, pq.z, o);
+        }
+        if (lane == 0) sm.row = pq;
+      } else {
+        named_arrive(2, NT);
+        cluster_arrive();
+      }
+      __syncthreads();
+      if (warp != 0) cluster_wait();
+      const float4 rw = sm.row;
+      const bool any_abort = rw.z != 0.f;
+      if (!valid || any_abort) continue;
+      const float RKL2 = rw.x, SS = rw.y;
+      const float gsT = a.grad_scale * a.invT;
+      if (rank == 0 && tid == 0) {
+        const float zx = E::load(a.draft, r * V + xs);
+        a.loss[r] = kLn2 * (RKL2 - a.lambda_ce * fmaf(zx, k, -Cd));
+      }
+      // ---- gradient: gsT (qa + q (lambda - S)) - gsT lambda [v = x*] ----
+      if (a.dlogits != nullptr) {
+        const float gL0 = gsT * (a.lambda_ce - SS);
+        const float gL1 = gsT * (a.lambda_ce - SS + 1.f);
+        const float2 gl = make_float2(gsT * kLn2, gsT * kLn2), g1 = make_float2(gL1, gL1);
+        float *out = a.dlogits + r * V + lo;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j)
+          if (j < nj) {
+            const int vi = tid + j * NT;
+            const Pairs<DT> y(ty[j]), z(tz[j]);
+            float g[EPV];
+#pragma unroll
+            for (int h = 0; h < Pairs<DT>::kN; ++h) {
+              const float2 A = __ffma2_rn(z.p[h], kk, nCd);
+              const float2 q = make_float2(ex2(A.x), ex2(A.y));
+              const float2 t = __fmul2_rn(q, __fadd2_rn(A, __ffma2_rn(y.p[h], nkk, Ct2)));
+              float2 gg = __ffma2_rn(t, gl, __fmul2_rn(q, g1));
               if (!(fabsf(t.x) < c2)) gg.x = q.x * gL0;
               if (!(fabsf(t.y) < c2)) gg.y = q.y * gL0;
+              g[2 * h] = gg.x;
+              g[2 * h + 1] = gg.y;
             }
-            g[2 * h] = gg.x;
-            g[2 * h + 1] = gg.y;
-          }
-          const int off = static_cast<int>(xs - (lo + vi * EPV));
-          if (off >= 0 && off < EPV) {
+            const int off = static_cast<int>(xs - (lo + vi * EPV));
+            if (off >= 0 && off < EPV) {
 #pragma unroll
-            for (int e = 0; e < EPV; ++e)
-              if (e == off) g[e] -= gsT * a.lambda_ce;
-          }
-          if (!row_ok) {
+              for (int e = 0; e < EPV; ++e)
+                if (e == off) g[e] -= gsT * a.lambda_ce;
+            }
 #pragma unroll
-            for (int e = 0; e < EPV; ++e) g[e] = nan;
+            for (int h = 0; h < EPV / 4; ++h)
+              st_stream(out + vi * EPV + 4 * h, g[4 * h], g[4 * h + 1], g[4 * h + 2], g[4 * h + 3]);
           }
-#pragma unroll
-          for (int h = 0; h < EPV / 4; ++h)
-            st_stream(out + vi * EPV + 4 * h, g[4 * h], g[4 * h + 1], g[4 * h + 2], g[4 * h + 3]);
-        }
+      }
     }
+    __syncthreads();  // the list is rewritten by the next batch
   }
-  if (tid == 0 && sm.abort && issued_next) mbar_wait_bounded(&sm.mbar[0], 0);  // best effort drain
-  cluster.sync();  // peers may still read this CTA's partials
+  if (tid == 0 && sm.abort) mbar_wait_bounded(&sm.mbar, sm.abort_parity);
+  cluster.sync();
 }
 
 struct OpdPlan {
@@ -824,11 +1138,17 @@ OpdPlan plan_opd(int64_t V, int esize) {
   return p;
 }
 
-template <int DT, bool BULK, int NT, int STAGES>
-cudaError_t launch_opd_t(const OpdArgs &a, const OpdPlan &p, cudaStream_t st) {
-  auto kern = opd_kernel<DT, BULK, NT, STAGES>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(p.smem));
+constexpr int kTab = 1024;  // target-row table entries per cluster (beyond: binary search)
+
+// what follows the two slices in dynamic shared memory
+enum SmemTail { kNone, kTable, kList };
+
+// launch a persistent grid of clusters (as many as can be co-resident)
+template <typename Kern>
+cudaError_t launch_clusters(Kern kern, int nt, const OpdArgs &a, const OpdPlan &p, SmemTail tail, cudaStream_t st) {
+  const size_t tail_max = (tail == kTable) ? kTab * sizeof(int32_t) : (tail == kList) ? kFixBatch * sizeof(int32_t) : 0;
+  const size_t smem_max = p.smem + tail_max;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_max));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -836,12 +1156,11 @@ cudaError_t launch_opd_t(const OpdArgs &a, const OpdPlan &p, cudaStream_t st) {
   attr[0].val.clusterDim.x = p.CL;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(NT, 1, 1);
-  cfg.dynamicSmemBytes = p.smem;
+  cfg.blockDim = dim3(nt, 1, 1);
+  cfg.dynamicSmemBytes = smem_max;
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // persistent clusters: as many as can be co-resident (cached per shape)
   struct Entry {
     int dev;
     const void *fn;
@@ -849,7 +1168,7 @@ cudaError_t launch_opd_t(const OpdArgs &a, const OpdPlan &p, cudaStream_t st) {
     size_t smem;
     int n;
   };
-  static Entry cache[32];
+  static Entry cache[64];
   static int ncache = 0;
   int dev = 0;
   e = cudaGetDevice(&dev);
@@ -857,70 +1176,53 @@ cudaError_t launch_opd_t(const OpdArgs &a, const OpdPlan &p, cudaStream_t st) {
   int maxc = 0;
   for (int q = 0; q < ncache; ++q)
     if (cache[q].dev == dev && cache[q].fn == reinterpret_cast<const void *>(kern) && cache[q].CL == p.CL &&
-        cache[q].smem == p.smem)
+        cache[q].smem == smem_max)
       maxc = cache[q].n;
   if (maxc == 0) {
     cfg.gridDim = dim3(p.CL * 1024, 1, 1);
     e = cudaOccupancyMaxActiveClusters(&maxc, kern, &cfg);
     if (e != cudaSuccess) return e;
     if (maxc <= 0) return cudaErrorInvalidConfiguration;
-    if (ncache < 32) cache[ncache++] = Entry{dev, reinterpret_cast<const void *>(kern), p.CL, p.smem, maxc};
+    if (ncache < 64) cache[ncache++] = Entry{dev, reinterpret_cast<const void *>(kern), p.CL, smem_max, maxc};
   }
   int64_t nclusters = maxc;
   if (nclusters > a.R) nclusters = a.R;
+  OpdGeo geo;
+  geo.SL = p.SL;
+  geo.slice_bytes = p.slice_bytes;
+  geo.ntab = 0;
+  // target rows fit the int32 table when the target has fewer than 2^31 rows
+  size_t tail_bytes = 0;
+  if (tail == kTable && a.has_bonus && a.R + a.N < (int64_t{1} << 31)) {
+    geo.ntab = static_cast<int32_t>(std::min<int64_t>((a.R + nclusters - 1) / nclusters, kTab));
+    tail_bytes = static_cast<size_t>(geo.ntab) * sizeof(int32_t);
+  }
+  if (tail == kList) tail_bytes = static_cast<size_t>((kFixBatch + nclusters - 1) / nclusters) * sizeof(int32_t);
+  cfg.dynamicSmemBytes = p.smem + tail_bytes;
   cfg.gridDim = dim3(static_cast<unsigned>(nclusters * p.CL), 1, 1);
-  e = cudaLaunchKernelEx(&cfg, kern, a, p.SL, p.slice_bytes);
+  e = cudaLaunchKernelEx(&cfg, kern, a, geo);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-template <int DT, int VPT>
-cudaError_t launch_opd_reg(const OpdArgs &a, const OpdPlan &p, cudaStream_t st) {
-  auto kern = opd_reg_kernel<DT, 512, VPT>;
-  const size_t smem = static_cast<size_t>(p.slice_bytes) * 2;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+// fast pass + fix-up with NT threads and up to VPT vectors per thread
+template <int DT, int VPT, int NT>
+cudaError_t launch_fast(const OpdArgs &a, const OpdPlan &p, cudaStream_t st) {
+  const cudaError_t e = launch_clusters(opd_fast_kernel<DT, VPT, NT>, NT, a, p, kTable, st);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = p.CL;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(512, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  static int cached[64][9] = {};
-  int dev = 0;
-  e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  int &maxc = cached[dev & 63][p.CL];
-  if (maxc == 0) {
-    cfg.gridDim = dim3(p.CL * 1024, 1, 1);
-    e = cudaOccupancyMaxActiveClusters(&maxc, kern, &cfg);
-    if (e != cudaSuccess) return e;
-    if (maxc <= 0) return cudaErrorInvalidConfiguration;
-  }
-  int64_t nclusters = maxc;
-  if (nclusters > a.R) nclusters = a.R;
-  cfg.gridDim = dim3(static_cast<unsigned>(nclusters * p.CL), 1, 1);
-  e = cudaLaunchKernelEx(&cfg, kern, a, p.SL, p.slice_bytes);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  return launch_clusters(opd_fix_kernel<DT, VPT, NT>, NT, a, p, kList, st);
 }
 
 template <int DT, bool BULK>
 cudaError_t launch_opd_cfg(const OpdArgs &a, const OpdPlan &p, cudaStream_t st) {
-  if (BULK) {
+  if (BULK && a.flags != nullptr) {
     const int nvec = static_cast<int>(static_cast<int64_t>(p.SL) * Elem<DT>::kSize / 16);
-    const int vpt = (nvec + 511) / 512;
-    if (vpt <= 1) return launch_opd_reg<DT, 1>(a, p, st);
-    if (vpt <= 2) return launch_opd_reg<DT, 2>(a, p, st);
-    if (vpt <= 3) return launch_opd_reg<DT, 3>(a, p, st);
-    if (vpt <= 5) return launch_opd_reg<DT, 5>(a, p, st);
+    if (nvec <= 512 * 1) return launch_fast<DT, 1, 512>(a, p, st);
+    if (nvec <= 512 * 2) return launch_fast<DT, 2, 512>(a, p, st);
+    if (nvec <= 512 * 3) return launch_fast<DT, 3, 512>(a, p, st);
+    if (nvec <= 256 * 10) return launch_fast<DT, 10, 256>(a, p, st);
   }
-  return launch_opd_t<DT, BULK, 512, 1>(a, p, st);
+  return launch_clusters(opd_exact_kernel<DT, BULK>, 512, a, p, kNone, st);
 }
 
 }  // namespace

@@ -90,6 +90,9 @@ struct OpdArgs {
   float *loss;
   float *dlogits;
   int32_t *status;
+  // workspace of the fast path (NULL: the exact kernel takes every row)
+  int32_t *flags;  // [R] rows the fix-up kernel must redo
+  float4 *rowc;    // [R] row constants of the fast kernel: Ct, Cd, x*, target row
 };
 
 cudaError_t launch_opd(const OpdArgs &a, int dtype, bool bulk, cudaStream_t stream);

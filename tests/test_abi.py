@@ -27,7 +27,7 @@ def lib():
 
 def test_header_symbols_exported(lib):
     names = _declared_functions()
-    assert {"spec_verify", "opd_loss", "svw_verify_workspace_size",
+    assert {"spec_verify", "opd_loss", "svw_verify_workspace_size", "svw_opd_workspace_size",
             "svw_status_string", "svw_version", "spec_verify_noalloc"} <= set(names)
     for n in names:
         assert hasattr(lib, n), f"{n} declared in svw.h but not exported"
@@ -48,6 +48,9 @@ def test_workspace_size(lib):
     assert svw.verify_workspace_size(0, 10, 100, svw.SVW_BF16) == 0
     assert svw.verify_workspace_size(4, 10, 0, svw.SVW_BF16) == 0
     assert svw.verify_workspace_size(4, 10, 1 << 21, svw.SVW_BF16) == 0
+    assert svw.opd_workspace_size(0) == 0
+    assert svw.opd_workspace_size(1) == 512
+    assert svw.opd_workspace_size(1920) == 7680 + 30720
 
 
 def _fake(n):
@@ -90,10 +93,11 @@ def test_opd_argument_validation(lib):
 
     def call(**kw):
         a = dict(t=p, d=p, dt=1, V=64, N=0, cu=None, R=4, hb=0, T=1.0, c=1.0, lam=0.1, gs=1.0,
-                 loss=p, g=p, st=None)
+                 loss=p, g=p, st=None, ws=None, wsb=0)
         a.update(kw)
         return lib.opd_loss(a["t"], a["d"], a["dt"], a["V"], a["N"], a["cu"], a["R"], a["hb"],
-                            a["T"], a["c"], a["lam"], a["gs"], a["loss"], a["g"], a["st"], None)
+                            a["T"], a["c"], a["lam"], a["gs"], a["loss"], a["g"], a["st"],
+                            a["ws"], a["wsb"], None)
 
     assert call(dt=3) == 2
     assert call(R=0) == 1
@@ -105,3 +109,5 @@ def test_opd_argument_validation(lib):
     assert call(loss=None) == 1
     assert call(g=ctypes.c_void_p(p.value + 4)) == 3   # dlogits must be 16-byte aligned
     assert call(V=1 << 22, dt=0) == 2       # row too wide for the on-chip slices
+    assert call(ws=p, wsb=16) == 4          # workspace smaller than svw_opd_workspace_size
+    assert call(ws=ctypes.c_void_p(p.value + 16), wsb=4096) == 3

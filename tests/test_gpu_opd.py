@@ -3,6 +3,10 @@
 Per-position loss within 1e-4 relative; every dlogits row within 1e-4 of the
 row's largest |gradient|.  Rows the oracle flags as having a term within
 1e-5 of the clip boundary are skipped and counted.
+
+Both device paths are covered: with a workspace (one-exchange fast pass, then
+the exact kernel on rows where a term reaches the clip or the draft has
+masked entries) and without one (the exact kernel on every row).
 """
 import numpy as np
 import pytest
@@ -31,26 +35,78 @@ def _gpu(tgt, drf, cu=None, has_bonus=False, status=None, want_grad=True, **kw):
     return loss.cpu().numpy(), (None if g is None else g.cpu().numpy())
 
 
+PATHS = pytest.mark.parametrize("exact_only", [False, True], ids=["fast", "exact"])
+
+
+@PATHS
 @pytest.mark.parametrize("V,dtype", [(151936, "bf16"), (1024, "bf16"), (5003, "bf16"),
-                                     (1001, "f32"), (4096, "f32"), (8, "bf16"), (151936, "f32")])
-def test_paired_rows(V, dtype):
+                                     (1001, "f32"), (4096, "f32"), (8, "bf16"), (151936, "f32"),
+                                     (2048, "bf16"), (129024, "bf16"), (24, "f32")])
+def test_paired_rows(V, dtype, exact_only):
     rows = 6
     b = synth.make_batch("opd", seed=V + 1, lengths=np.full(1, rows, np.int32), V=V,
                          dtype=dtype, draft_kind="scaled", temperatures=(), has_bonus=False)
-    loss, g = _gpu(b.target, b.draft)
+    loss, g = _gpu(b.target, b.draft, exact_only=exact_only)
     ref = oracle.opd_loss(b.target, b.draft)
     compare_opd(loss, g, ref, label=f"V={V} {dtype}")
 
 
+@PATHS
 @pytest.mark.parametrize("T,c,lam,gs", [(1.0, 0.01, 0.1, 1.0), (0.7, 1e30, 0.5, 0.0625),
                                         (1.3, 0.2, 0.0, 1.0), (1.0, float("inf"), 4.0, 0.2)])
-def test_parameters(T, c, lam, gs):
+def test_parameters(T, c, lam, gs, exact_only):
     b = synth.make_batch("opd", seed=11, lengths=np.full(1, 5, np.int32), V=32768,
                          draft_kind="scaled", temperatures=(), has_bonus=False)
-    loss, g = _gpu(b.target, b.draft, temperature=T, clip_c=c, lambda_ce=lam, grad_scale=gs)
+    loss, g = _gpu(b.target, b.draft, temperature=T, clip_c=c, lambda_ce=lam, grad_scale=gs,
+                   exact_only=exact_only)
     ref = oracle.opd_loss(b.target, b.draft, temperature=T, clip_c=c, lambda_ce=lam,
                           grad_scale=gs)
     compare_opd(loss, g, ref, label=f"T={T} c={c}")
+
+
+def _row_max_term(y, z):
+    """max_v |q_v (lq_v - lp_v)| per row in fp64 (only to choose a clip bound
+    that splits the rows; the parity check itself is against the oracle)."""
+    y = synth.as_f32(y).astype(np.float64)
+    z = synth.as_f32(z).astype(np.float64)
+    lp = y - y.max(1, keepdims=True)
+    lp -= np.log(np.exp(lp).sum(1, keepdims=True))
+    lq = z - z.max(1, keepdims=True)
+    lq -= np.log(np.exp(lq).sum(1, keepdims=True))
+    return np.abs(np.exp(lq) * (lq - lp)).max(1)
+
+
+@PATHS
+def test_mixed_clipped_and_unclipped_rows(exact_only):
+    """About half the rows have a term beyond the clip: the fast pass must hand
+    exactly those to the exact kernel and keep the others."""
+    b = synth.make_batch("opd", seed=31, lengths=np.full(1, 40, np.int32), V=16384,
+                         draft_kind="add", temperatures=(), has_bonus=False,
+                         sigma_pos=lambda j: 0.1 + 0.1 * j)
+    mt = _row_max_term(b.target, b.draft)
+    c = float(np.median(mt))
+    assert 8 <= int((mt > c).sum()) <= 32
+    loss, g = _gpu(b.target, b.draft, clip_c=c, exact_only=exact_only)
+    ref = oracle.opd_loss(b.target, b.draft, clip_c=c)
+    compare_opd(loss, g, ref, label=f"c={c}")
+
+
+@PATHS
+def test_masked_entries(exact_only):
+    """-inf draft entries (q = 0) and -inf target entries under q > 0 (an
+    infinite term, clamped) in otherwise ordinary rows."""
+    b = synth.make_batch("opd", seed=32, lengths=np.full(1, 6, np.int32), V=8192,
+                         draft_kind="scaled", temperatures=(), has_bonus=False)
+    t = b.target.copy()
+    d = b.draft.copy()
+    d[1, ::7] = 0xFF80                # masked draft entries
+    t[2, 100:200] = 0xFF80            # masked target entries
+    d[3, ::5] = 0xFF80
+    t[3, 1::5] = 0xFF80               # both
+    loss, g = _gpu(t, d, clip_c=1.0, exact_only=exact_only)
+    ref = oracle.opd_loss(t, d, clip_c=1.0)
+    assert np.all(np.isfinite(loss))
+    compare_opd(loss, g, ref, label="masked")
 
 
 def test_loss_only():
@@ -61,14 +117,16 @@ def test_loss_only():
     compare_opd(loss, None, oracle.opd_loss(b.target, b.draft, want_grad=False))
 
 
-def test_verify_layout_rows():
+@PATHS
+def test_verify_layout_rows(exact_only):
     b = synth.config(5, N=7, V=40000, seed=21)
-    loss, g = _gpu(b.target, b.draft, cu=b.cu, has_bonus=True)
+    loss, g = _gpu(b.target, b.draft, cu=b.cu, has_bonus=True, exact_only=exact_only)
     ref = oracle.opd_loss(b.target, b.draft, cu_draft=b.cu, has_bonus=True)
     compare_opd(loss, g, ref, label="verify layout")
 
 
-def test_bad_rows():
+@PATHS
+def test_bad_rows(exact_only):
     import torch
     import serving_vocab_wide_gb300 as svw
     b = synth.make_batch("opd", seed=13, lengths=np.full(1, 4, np.int32), V=4096,
@@ -79,7 +137,7 @@ def test_bad_rows():
     d[2, :] = 0xFF80          # all -inf
     t[3, 100] = 0x7F80        # +inf
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    loss, g = _gpu(t, d, status=status)
+    loss, g = _gpu(t, d, status=status, exact_only=exact_only)
     ref = oracle.opd_loss(t, d)
     assert np.isfinite(loss[0]) and np.all(np.isnan(loss[1:]))
     assert np.all(ref["flags"][1:] & oracle.FLAG_BAD)
@@ -104,3 +162,14 @@ def test_deterministic_rerun():
     l1, g1 = _gpu(b.target, b.draft)
     l2, g2 = _gpu(b.target, b.draft)
     assert np.array_equal(l1, l2) and np.array_equal(g1, g2)
+
+
+def test_fast_and_exact_paths_agree_full_size():
+    """Every row of the full-size OPD batch: the two device paths agree to
+    float rounding (each is checked against the oracle elsewhere)."""
+    b = synth.config(4)
+    lf, gf = _gpu(b.target, b.draft)
+    le, ge = _gpu(b.target, b.draft, exact_only=True)
+    assert np.all(np.abs(lf - le) <= 1e-4 * np.abs(le) + 1e-6)
+    scale = np.abs(ge).max(axis=1)
+    assert np.all(np.abs(gf - ge).max(axis=1) <= 1e-4 * scale + 1e-12)
