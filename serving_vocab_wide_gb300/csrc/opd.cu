@@ -556,11 +556,14 @@ __device__ __forceinline__ FastPart merge_lanes(const FastPart &p, float k) {
 
 struct FastSmem {
   unsigned long long mbar;
+  // row exchange: every CTA pushes its partial into slot [rank] of each peer's
+  // inbox; xbar[s] completes when all CL partials of the row have landed.
+  // Two slots: a peer may send row r+1's partial before this CTA has merged
+  // row r's, but never row r+2's.
+  unsigned long long xbar[2];
+  FastPart inbox[2][kMaxCluster];
   FastPart red[16];  // one partial per warp
-  // this CTA's partial, read by the peers; double-buffered because a peer may
-  // still read row r's while this CTA writes row r+1's (one exchange per row)
-  FastPart part[2];
-  FastPart row;  // merged over the cluster
+  FastPart row;      // merged over the cluster
   int64_t tr;
   uint32_t nread;  // warps done reading the slice buffer (16 per row)
   int32_t abort;
@@ -586,8 +589,20 @@ __device__ __forceinline__ bool last_warp_done(uint32_t *cnt, int64_t it) {
 // named barriers: warps 1..15 arrive, warp 0 waits (only warp 0 acts on them)
 __device__ __forceinline__ void named_arrive(int id, int nt) { asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nt) : "memory"); }
 __device__ __forceinline__ void named_sync(int id, int nt) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nt) : "memory"); }
-__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive;" ::: "memory"); }
-__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait;" ::: "memory"); }
+// shared::cluster address of the same shared variable in CTA `rank`
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// 16-byte store into a peer's shared memory that completes 16 bytes of the
+// transaction count of the peer's mbarrier (no fence, no cluster barrier)
+__device__ __forceinline__ void st_async16(uint32_t dst, const uint4 &v, uint32_t mbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(dst),
+               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(mbar)
+               : "memory");
+}
 
 template <int DT, int VPT, int NT>
 __global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) {
@@ -615,11 +630,13 @@ __global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) 
 
   if (tid == 0) {
     mbar_init(&sm.mbar, 1);
+    mbar_init(&sm.xbar[0], 1);
+    mbar_init(&sm.xbar[1], 1);
     sm.abort = 0;
     sm.nread = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  __syncthreads();
+  cluster.sync();  // every inbox barrier exists before any peer sends
   // one thread: start the bulk copies of draft row r (target row t)
   auto issue = [&](int64_t r, int64_t t) {
     sm.tr = t;
@@ -758,35 +775,35 @@ __global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) 
       P.zx = __shfl_sync(0xffffffffu, zx, holders ? __ffs(holders) - 1 : 0);
     }
     if (lane == 0) sm.red[warp] = P;
-    FastPart Rw;
     if (warp == 0) {
+      const int slot = static_cast<int>(it & 1);
+      if (lane == 0) mbar_arrive_expect_tx(&sm.xbar[slot], static_cast<uint32_t>(CL) * sizeof(FastPart));
       named_sync(2, NT);  // every warp's partial is in
       const FastPart Pc = merge_lanes<kWarps>(lane < kWarps ? sm.red[lane] : empty_part(), k);
-      if (lane == 0) sm.part[it & 1] = Pc;
-      cluster_arrive();
-      cluster_wait();
+      if (lane < CL) {  // lane q pushes this CTA's partial to CTA q
+        const uint4 w0 = make_uint4(__float_as_uint(Pc.my), __float_as_uint(Pc.sy), __float_as_uint(Pc.mz),
+                                    __float_as_uint(Pc.sz));
+        const uint4 w1 = make_uint4(__float_as_uint(Pc.u), static_cast<uint32_t>(Pc.idx), __float_as_uint(Pc.zx),
+                                    static_cast<uint32_t>(Pc.abort));
+        const uint32_t dst = mapa_shared(smem_u32(&sm.inbox[slot][rank]), lane);
+        const uint32_t bar = mapa_shared(smem_u32(&sm.xbar[slot]), lane);
+        st_async16(dst, w0, bar);
+        st_async16(dst + 16, w1, bar);
+      }
       FastPart Pq = empty_part();
-      if (lane < CL) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(cluster.map_shared_rank(&sm.part[it & 1], lane));
-        uint4 w0 = src[0], w1 = src[1];
-        Pq.my = __uint_as_float(w0.x);
-        Pq.sy = __uint_as_float(w0.y);
-        Pq.mz = __uint_as_float(w0.z);
-        Pq.sz = __uint_as_float(w0.w);
-        Pq.u = __uint_as_float(w1.x);
-        Pq.idx = static_cast<int32_t>(w1.y);
-        Pq.zx = __uint_as_float(w1.z);
-        Pq.abort = static_cast<int32_t>(w1.w);
+      if (mbar_wait_bounded(&sm.xbar[slot], static_cast<uint32_t>((it >> 1) & 1))) {
+        if (lane < CL) Pq = sm.inbox[slot][lane];
+      } else {
+        if (lane == 0 && a.status) atomicOr(a.status, SVW_DEV_TIMEOUT);
+        Pq.abort = 1;
       }
       const FastPart M = merge_lanes<kMaxCluster>(Pq, k);
       if (lane == 0) sm.row = M;
     } else {
       named_arrive(2, NT);
-      cluster_arrive();
     }
     __syncthreads();  // the merged row is published
-    if (warp != 0) cluster_wait();  // long complete: warp 0 waited on it before publishing
-    Rw = sm.row;
+    const FastPart Rw = sm.row;
     const bool any_abort = Rw.abort != 0;
     const bool row_ok = valid && !any_abort && (Rw.sy > 0.f && Rw.sy <= FLT_MAX) && (Rw.sz > 0.f && Rw.sz <= FLT_MAX);
     const float lsy = lg2(Rw.sy), lsz = lg2(Rw.sz);
@@ -888,8 +905,9 @@ constexpr int kFixBatch = 4096;  // flags scanned per batch
 
 struct FixSmem {
   unsigned long long mbar;
+  unsigned long long xbar[2];          // row exchange, as in the fast kernel
+  float4 inbox[2][kMaxCluster];        // peers' (RKL2, S, abort)
   float2 red[16];
-  float4 part[2];  // this CTA's (RKL2, S, abort); double-buffered as in the fast kernel
   float4 row;
   int32_t wcnt[16];
   int32_t total;
@@ -927,11 +945,13 @@ __global__ void __launch_bounds__(NT, 2) opd_fix_kernel(OpdArgs a, OpdGeo geo) {
 
   if (tid == 0) {
     mbar_init(&sm.mbar, 1);
+    mbar_init(&sm.xbar[0], 1);
+    mbar_init(&sm.xbar[1], 1);
     sm.abort = 0;
     sm.nread = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  __syncthreads();
+  cluster.sync();  // every inbox barrier exists before any peer sends
   auto issue = [&](int64_t r) {
     const float4 rc = __ldcg(a.rowc + r);
     const int32_t t32 = __float_as_int(rc.w);
@@ -1038,6 +1058,8 @@ __global__ void __launch_bounds__(NT, 2) opd_fix_kernel(OpdArgs a, OpdGeo geo) {
       S = warp_sum(S);
       if (lane == 0) sm.red[warp] = make_float2(rkl, S);
       if (warp == 0) {
+        const int slot = static_cast<int>(it & 1);
+        if (lane == 0) mbar_arrive_expect_tx(&sm.xbar[slot], static_cast<uint32_t>(CL) * sizeof(float4));
         named_sync(2, NT);
         float2 v = (lane < kWarps) ? sm.red[lane] : make_float2(0.f, 0.f);
 #pragma unroll
@@ -1045,11 +1067,17 @@ __global__ void __launch_bounds__(NT, 2) opd_fix_kernel(OpdArgs a, OpdGeo geo) {
           v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
           v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
         }
-        if (lane == 0) sm.part[it & 1] = make_float4(v.x, v.y, sm.abort ? 1.f : 0.f, 0.f);
-        cluster_arrive();
-        cluster_wait();
+        if (lane < CL)
+          st_async16(mapa_shared(smem_u32(&sm.inbox[slot][rank]), lane),
+                     make_uint4(__float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(sm.abort ? 1.f : 0.f), 0u),
+                     mapa_shared(smem_u32(&sm.xbar[slot]), lane));
         float4 pq = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (lane < CL) pq = *cluster.map_shared_rank(&sm.part[it & 1], lane);
+        if (mbar_wait_bounded(&sm.xbar[slot], static_cast<uint32_t>((it >> 1) & 1))) {
+          if (lane < CL) pq = sm.inbox[slot][lane];
+        } else {
+          if (lane == 0 && a.status) atomicOr(a.status, SVW_DEV_TIMEOUT);
+          pq.z = 1.f;
+        }
 #pragma unroll
         for (int o = kMaxCluster / 2; o > 0; o >>= 1) {
           pq.x += __shfl_xor_sync(0xffffffffu, pq.x, o);
@@ -1059,10 +1087,8 @@ __global__ void __launch_bounds__(NT, 2) opd_fix_kernel(OpdArgs a, OpdGeo geo) {
         if (lane == 0) sm.row = pq;
       } else {
         named_arrive(2, NT);
-        cluster_arrive();
       }
       __syncthreads();
-      if (warp != 0) cluster_wait();
       const float4 rw = sm.row;
       const bool any_abort = rw.z != 0.f;
       if (!valid || any_abort) continue;
