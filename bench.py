@@ -73,8 +73,12 @@ def _src_hash(files):
 
 
 KERNEL_SOURCES = {
-    "verify_main": ["verify.cu", "svw_device.cuh", "svw_internal.h"],
-    "opd_kernel": ["opd.cu", "svw_device.cuh", "svw_internal.h"],
+    "spec_verify": ["verify.cu", "svw_device.cuh", "svw_internal.h"],
+    "opd_loss": ["opd.cu", "svw_device.cuh", "svw_internal.h"],
+}
+CALL_KERNELS = {
+    "spec_verify": "verify_prologue + verify_stats + verify_finalize (+ verify_sample at T > 0)",
+    "opd_loss": "opd_fast_kernel + opd_fix_kernel",
 }
 
 
@@ -265,7 +269,7 @@ def run_native(args, ws, rank, local):
     step_bytes = sum(alg.values())
     peak, peak_kind = _peaks()
     dom = max(calls, key=lambda c: avg_us[c])
-    dom_kernel = "opd_kernel" if dom == "opd" else "verify_main"
+    dom_kernel = "opd_loss" if dom == "opd" else "spec_verify"
     achieved = alg[dom] / (avg_us[dom] * 1e-6) / 1e9
     traffic = _profile_traffic(dom_kernel, f"mix:{dom}")
 
@@ -321,7 +325,8 @@ def run_native(args, ws, rank, local):
                    "N": N, "total_draft_rows": R, "V": V, "logits": "bf16",
                    "per_rank_batch": True, "parallelism": f"replicas x{ws}",
                    "l2": "inputs 1.25 GB per step > 129 MB L2; no flush"},
-        "roofline": {"bound": "hbm", "kernel": f"{dom_kernel} ({dom})", "achieved": achieved,
+        "roofline": {"bound": "hbm", "kernel": f"{dom_kernel} call ({dom}): {CALL_KERNELS[dom_kernel]}",
+                     "achieved": achieved,
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "algorithmic_bytes_per_launch": alg[dom]},
