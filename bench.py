@@ -77,7 +77,7 @@ KERNEL_SOURCES = {
     "opd_loss": ["opd.cu", "svw_device.cuh", "svw_internal.h"],
 }
 CALL_KERNELS = {
-    "spec_verify": "verify_prologue + verify_stats + verify_finalize (+ verify_sample at T > 0)",
+    "spec_verify": "verify_stats + verify_finalize (+ verify_sample at T > 0)",
     "opd_loss": "opd_fast_kernel + opd_fix_kernel",
 }
 
@@ -166,9 +166,9 @@ class ClockSampler:
 # native arm
 # ---------------------------------------------------------------------------
 def launches_per_step():
-    """Kernels one step launches: spec_verify = prologue + stats + finalize
-    (+ sample at T > 0); opd_loss = fast pass + exact fix-up."""
-    return sum(3 if T == 0 else 4 for T in TEMPS) + 2
+    """Kernels one step launches: spec_verify = stats + finalize (+ sample at
+    T > 0); opd_loss = fast pass + exact fix-up."""
+    return sum(2 if T == 0 else 3 for T in TEMPS) + 2
 
 
 def run_native(args, ws, rank, local):

@@ -88,12 +88,12 @@ svw_status spec_verify(const void *target_logits, const void *draft_logits, svw_
   char *ws = static_cast<char *>(workspace);
   a.part = reinterpret_cast<svw::Partial *>(ws + lay.part_off);
   a.sample_counters = reinterpret_cast<int32_t *>(ws + lay.sample_counters_off);
-  a.req_ok = reinterpret_cast<int32_t *>(ws + lay.req_ok_off);
   a.sinfo = reinterpret_cast<svw::SampleInfo *>(ws + lay.sinfo_off);
   a.span_tot = reinterpret_cast<float *>(ws + lay.span_off);
   a.chunk_tot = reinterpret_cast<float *>(ws + lay.chunk_tot_off);
   a.chunk_last = reinterpret_cast<int32_t *>(ws + lay.chunk_last_off);
-  a.global_ok = reinterpret_cast<int32_t *>(ws + lay.global_ok_off);
+  a.csr_bad = reinterpret_cast<int32_t *>(ws + lay.csr_bad_off);
+  a.stats_grid = 0;  // set by the launcher
   a.Cs = svw::sampler_chunks(V);
   a.C = plan.C;
   a.chunk_len = plan.chunk_len;

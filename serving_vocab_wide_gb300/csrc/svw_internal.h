@@ -36,11 +36,12 @@ struct alignas(16) SampleInfo {
 };
 
 struct VerifyLayout {
-  size_t part_off, sample_counters_off, req_ok_off, sinfo_off, span_off, chunk_tot_off,
-      chunk_last_off, global_ok_off, total;
+  size_t part_off, sample_counters_off, sinfo_off, span_off, chunk_tot_off, chunk_last_off, csr_bad_off,
+      total;
 };
 VerifyLayout verify_layout(int32_t N, int64_t total_rows, int64_t V, int esize);
-int32_t sampler_chunks(int64_t V);  // 4096-entry chunks of the inverse-CDF sampler
+int32_t sampler_chunks(int64_t V);  // 16384-entry chunks of the inverse-CDF sampler
+constexpr int kMaxStatsGrid = 1024;  // CTAs of the stats kernel (one CSR check flag each)
 
 struct VerifyArgs {
   const void *target;
@@ -59,12 +60,12 @@ struct VerifyArgs {
   int32_t *status;
   Partial *part;                     // [(rows_t + total_rows) * C * 8] per-warp chunk partials
   int32_t *sample_counters;          // [N] sampling arrivals per request
-  int32_t *req_ok;                   // [N] request passed validation
   SampleInfo *sinfo;                 // [N]
-  float *span_tot;                   // [N * Cs * 256] sampler lane totals
+  float *span_tot;                   // [N * Cs * 64] sampler warp totals (round, warp)
   float *chunk_tot;                  // [N * Cs] sampler chunk totals
-  int32_t *chunk_last;               // [N * Cs] last positive entry per sampler chunk
-  int32_t *global_ok;                // CSR offsets consistent
+  int32_t *chunk_last;               // [N * Cs] last group with positive weight per sampler chunk
+  int32_t *csr_bad;                  // [stats grid] CSR offsets inconsistent (per stats CTA)
+  int32_t stats_grid;                // CTAs of the stats kernel
   int32_t Cs;                        // sampler chunks per row
   int32_t C;
   int32_t chunk_len;

@@ -7,39 +7,45 @@
 //   prefix; draw one token from [p - q]_+ at the rejected row or from p at the
 //   bonus row.  Greedy (T = 0): accept iff x_j is the target argmax.
 //
-// GPU design: four stream-ordered kernels, no CTA ever waits for another.
-//  1. verify_prologue   validates CSR offsets and tokens, resets the sampler's
-//                       arrival counters, writes the -1 defaults.
-//  2. verify_stats      the HBM stream.  Each logit row is cut into C chunks
+// GPU design: three stream-ordered kernels; no CTA ever waits for another.
+//  1. verify_stats      the HBM stream.  Each logit row is cut into C chunks
 //                       (C <= 32, ~30 KB); a (row, chunk) pair is a work item.
 //                       Persistent CTAs take items in a fixed stride.  One
-//                       producer warp streams each chunk into a 4-stage
+//                       producer warp streams each chunk into a 3-stage
 //                       shared-memory ring with 1-D bulk async copies
 //                       (cp.async.bulk, full/empty mbarriers); eight consumer
 //                       warps reduce their share of the chunk to
 //                       (max, sum 2^((x - max) log2e/T)) -- or (max, argmax)
 //                       when greedy -- with packed bf16 max and f32x2
 //                       arithmetic, and write one Partial per warp.  No block
-//                       barrier in the steady state.
-//  3. verify_finalize   one CTA per request: merges the partials into row
-//                       log-sum-exps (or argmaxes), runs every accept test in
-//                       one warp (ballot + ffs = leftmost rejection), writes
-//                       accept_len and the sampling row (greedy: next_token).
-//  4. verify_sample     (T > 0) inverse-CDF draw over the sampling row (pair),
-//                       split into 4096-entry sampler chunks so the whole GPU
+//                       barrier in the steady state.  Each CTA also checks a
+//                       share of the CSR offsets.
+//  2. verify_finalize   one CTA per request: validates the request, merges the
+//                       partials into row log-sum-exps (or argmaxes), runs
+//                       every accept test in one warp (ballot + ffs = leftmost
+//                       rejection), writes accept_len and the sampling row
+//                       (greedy: next_token).
+//  3. verify_sample     (T > 0) inverse-CDF draw over the sampling row (pair),
+//                       split into 16384-entry sampler chunks so the whole GPU
 //                       takes part; the CTA that completes a request's chunks
 //                       (arrival counter) resolves the token.
+// Kernels 2 and 3 are launched as programmatic dependents of the kernel before
+// them: they are scheduled while it drains and wait (griddepcontrol.wait) only
+// before reading its results; finalize reads the draft tokens and their logits
+// before that point.
 //
 // Inverse-CDF prefix sums.  Weights w_v = [p_v - q_v]_+ (or p_v).  The prefix
 // C_v is defined level by level, each level a sequential fp32 sum (from 0, in
 // index order) of non-negative terms, so that it is reproducible,
 // non-decreasing and equal at every level boundary:
-//   group  8 consecutive entries           partial sums part_k, total a_g
-//   lane   2 consecutive groups            running R, total T_l
-//   warp   32 lanes                        prefix E_l, total W_w
-//   chunk  8 warps (4096 entries)          prefix P_w, total Z_c
-//   row    chunks                          prefix B_c, total Z
-//   C_v = fl(B_c + fl(P_w + fl(E_l + fl(R + part_k))))
+//   group  8 consecutive entries               partial sums part_k, total a_g
+//   warp   32 consecutive groups (one a lane)  prefix E_l, total W_w
+//   round  8 warps (2048 entries)              prefix Q_w, total R_r
+//   chunk  8 rounds (16384 entries)            prefix P_r, total Z_c
+//   row    chunks                              prefix B_c, total Z
+//   C_v = fl(B_c + fl(P_r + fl(Q_w + fl(E_l + part_k))))
+// A round is one 16-byte vector per thread of the CTA, so every load of the
+// sampler is coalesced.
 // next = smallest v with C_v > w Z; that v always has w_v > 0.  If rounding
 // leaves no crossing, the last positive entry is taken.
 #include <cfloat>
@@ -60,6 +66,11 @@ constexpr int kThreads = 256;                  // finalize / sample kernels
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxRows = 2 * SVW_MAX_LEN + 1;
 constexpr int kMaxGroupsPerSpan = 512;  // single-CTA fallback sampler: V <= 256 * 512 * 8
+
+// programmatic dependent launch: let the next kernel be scheduled / wait for
+// the previous kernel's results
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ Partial ldcg_partial(const Partial *p) {
   const float4 v = __ldcg(reinterpret_cast<const float4 *>(p));
@@ -107,15 +118,26 @@ __device__ __forceinline__ ItemMeta decode_item(const VerifyArgs &a, int64_t ite
   m.item = item;
   const int32_t i = find_request<GREEDY>(a, item);
   const int64_t c_i = __ldg(a.cu + i);
-  const int32_t L = __ldg(a.cu + i + 1) - static_cast<int32_t>(c_i);
+  const int64_t c_e = __ldg(a.cu + i + 1);
+  // requests the finalize kernel will reject are not read (this also keeps
+  // every address in range when the offsets are inconsistent)
+  const bool req_ok = (c_e - c_i >= 1 && c_e - c_i <= a.max_len && c_i >= 0 && c_e <= a.total_rows);
+  const int32_t L = req_ok ? static_cast<int32_t>(c_e - c_i) : 0;
   const int64_t off = static_cast<int64_t>(a.C) * (GREEDY ? (c_i + i) : (2 * c_i + i));
   const int64_t local = item - off;
+  const int32_t nrows = GREEDY ? L + 1 : 2 * L + 1;
+  m.valid = (req_ok && local >= 0 && local < static_cast<int64_t>(nrows) * a.C) ? 1 : 0;
+  if (!m.valid) {
+    m.prow = 0;
+    m.src = nullptr;
+    m.chunk = 0;
+    m.n = 0;
+    return m;
+  }
   const int32_t rl = static_cast<int32_t>(local / a.C);
   m.chunk = static_cast<int32_t>(local - static_cast<int64_t>(rl) * a.C);
   const int64_t c0 = static_cast<int64_t>(m.chunk) * a.chunk_len;
   m.n = static_cast<int32_t>(min(static_cast<int64_t>(a.chunk_len), a.V - c0));
-  const int32_t nrows = GREEDY ? L + 1 : 2 * L + 1;
-  m.valid = (a.req_ok[i] != 0 && rl < nrows) ? 1 : 0;
   const char *row;
   if (GREEDY || rl <= L) {
     m.prow = c_i + i + rl;
@@ -276,9 +298,21 @@ __global__ void __launch_bounds__(kStatsThreads, 2) verify_stats(VerifyArgs a, i
   extern __shared__ __align__(128) unsigned char ring[];
   __shared__ unsigned long long full[kStages], empty[kStages];
   __shared__ ItemMeta meta[kStages];
-  if (*a.global_ok == 0) return;  // inconsistent CSR offsets: nothing may be read
   const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t G = gridDim.x;
+  pdl_launch_dependents();  // the finalize grid may be scheduled now
+  {
+    // this CTA's share of the CSR consistency check: cu[0] = 0,
+    // cu[N] = total rows, non-decreasing (the finalize kernel ORs the flags)
+    int bad = 0;
+    for (int64_t j = static_cast<int64_t>(blockIdx.x) * kStatsThreads + threadIdx.x; j < a.N;
+         j += G * kStatsThreads)
+      bad |= (__ldg(a.cu + j) > __ldg(a.cu + j + 1)) ? 1 : 0;
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+      bad |= (__ldg(a.cu) != 0 || static_cast<int64_t>(__ldg(a.cu + a.N)) != a.total_rows) ? 1 : 0;
+    bad = __syncthreads_or(bad);
+    if (threadIdx.x == 0) a.csr_bad[blockIdx.x] = bad;
+  }
 
   if (!BULK) {
     // plain loads: every warp walks the CTA's items itself (no producer)
@@ -367,7 +401,7 @@ __global__ void __launch_bounds__(kStatsThreads, 2) verify_stats(VerifyArgs a, i
 }
 
 // ---------------------------------------------------------------------------
-// kernel 3: per-request merge + accept tests
+// kernel 2: per-request validation, merge, accept tests
 // ---------------------------------------------------------------------------
 template <int DT, bool GREEDY>
 __global__ void __launch_bounds__(kThreads) verify_finalize(VerifyArgs a) {
@@ -376,13 +410,50 @@ __global__ void __launch_bounds__(kThreads) verify_finalize(VerifyArgs a) {
   __shared__ float row_l[kMaxRows];
   __shared__ int32_t row_idx[kMaxRows];
   __shared__ int32_t row_bad[kMaxRows];
-  if (*a.global_ok == 0) return;
+  __shared__ int32_t s_ok;
   const int32_t i = blockIdx.x;
-  if (!a.req_ok[i]) return;  // outputs keep the -1 defaults
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t c_i = __ldg(a.cu + i);
-  const int32_t L = __ldg(a.cu + i + 1) - static_cast<int32_t>(c_i);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_launch_dependents();
+
+  // ---- inputs only: this part overlaps the end of the stats kernel ----
+  const int64_t c_i = __ldg(a.cu + i), c_e = __ldg(a.cu + i + 1);
+  const bool len_ok = (c_e - c_i >= 1 && c_e - c_i <= a.max_len && c_i >= 0 && c_e <= a.total_rows);
+  const int32_t L = len_ok ? static_cast<int32_t>(c_e - c_i) : 0;
   const int64_t t0 = c_i + i, d0 = c_i;
+  int32_t x = 0;
+  float yx = 0.f, zx = 0.f, u = 0.f;
+  if (warp == 0) {
+    bool tok_ok = true;
+    if (lane < L) {
+      x = __ldg(a.tokens + d0 + lane);
+      tok_ok = (x >= 0 && static_cast<int64_t>(x) < a.V);
+      if (tok_ok && !GREEDY) {
+        yx = E::load(a.target, (t0 + lane) * a.V + x);
+        zx = E::load(a.draft, (d0 + lane) * a.V + x);
+        u = philox_uniform(a.seed, static_cast<uint32_t>(i), static_cast<uint32_t>(lane), 0u);
+      }
+    }
+    const bool ok = len_ok && __all_sync(0xffffffffu, tok_ok);
+    if (lane == 0) {
+      s_ok = ok ? 1 : 0;
+      a.sample_counters[i] = 0;  // the sampling kernel starts after this grid
+    }
+  }
+  pdl_wait();  // the stats kernel's partials and CSR flags are complete
+
+  int csr_bad = 0;
+  for (int b = tid; b < a.stats_grid; b += kThreads) csr_bad |= __ldcg(a.csr_bad + b);
+  csr_bad = __syncthreads_or(csr_bad);
+  auto reject = [&]() {  // one thread: a bad request
+    a.accept_len[i] = -1;
+    a.next_token[i] = -1;
+    if (!GREEDY) a.sinfo[i].valid = 0;
+    if (a.status) atomicOr(a.status, SVW_DEV_BAD_INPUT);
+  };
+  if (!s_ok || csr_bad) {
+    if (tid == 0) reject();
+    return;
+  }
   const int32_t nrows = GREEDY ? L + 1 : 2 * L + 1;
   const int np = a.C * kCW;  // partials per row
   for (int r = warp; r < nrows; r += kWarps) {
@@ -423,13 +494,10 @@ __global__ void __launch_bounds__(kThreads) verify_finalize(VerifyArgs a) {
   bad = __any_sync(0xffffffffu, bad);
   bool acc = true;
   if (lane < L) {
-    const int32_t x = __ldg(a.tokens + d0 + lane);
     if (GREEDY) {
       acc = (x == row_idx[lane]);
     } else {
       // log2(p(x)/q(x)) from raw logits and row log-sum-exps
-      const float yx = E::load(a.target, (t0 + lane) * a.V + x);
-      const float zx = E::load(a.draft, (d0 + lane) * a.V + x);
       float thr;
       if (zx == -INFINITY) {
         thr = 1.f;  // q(x) = 0: accept
@@ -439,7 +507,6 @@ __global__ void __launch_bounds__(kThreads) verify_finalize(VerifyArgs a) {
             __fsub_rn(row_l[lane], row_l[L + 1 + lane]));
         thr = (dl >= 0.f) ? 1.f : ex2(dl);
       }
-      const float u = philox_uniform(a.seed, static_cast<uint32_t>(i), static_cast<uint32_t>(lane), 0u);
       acc = (u < thr);
     }
   }
@@ -447,7 +514,7 @@ __global__ void __launch_bounds__(kThreads) verify_finalize(VerifyArgs a) {
   const int32_t js = rej ? (__ffs(rej) - 1) : L;
   if (lane != 0) return;
   if (bad) {
-    if (a.status) atomicOr(a.status, SVW_DEV_BAD_INPUT);
+    reject();
     return;
   }
   a.accept_len[i] = js;
@@ -470,15 +537,31 @@ __global__ void __launch_bounds__(kThreads) verify_finalize(VerifyArgs a) {
 // ---------------------------------------------------------------------------
 // sampling weights
 // ---------------------------------------------------------------------------
+constexpr int kRounds = 8;                       // rounds per sampler chunk
+constexpr int kSChunk = kThreads * kRounds * 8;  // 16384 entries per sampler chunk
+constexpr int kSpan = kRounds * kWarps;          // warp totals stored per sampler chunk
+
+// log2 p = y k + nT, log2 q = z k + nD (one rounding each); the constants are
+// computed once per request from the row maxima and log-sum-exps
 struct RowConst {
-  float Mt, lt, Md, ld, k;
+  float k, nT, nD;
+  bool resid;
 };
 
-// [p - q]_+ (resid) or p, from raw logits and the row constants
-__device__ __forceinline__ float weight(float y, float z, bool resid, const RowConst &c) {
-  const float lp = __fsub_rn(__fmul_rn(__fsub_rn(y, c.Mt), c.k), c.lt);  // log2 p
-  if (!resid) return ex2(lp);
-  const float lq = __fsub_rn(__fmul_rn(__fsub_rn(z, c.Md), c.k), c.ld);  // log2 q
+__device__ __forceinline__ RowConst row_const(const SampleInfo &si, float k) {
+  RowConst c;
+  c.k = k;
+  c.nT = -__fmaf_rn(si.Mt, k, si.lt);
+  c.nD = -__fmaf_rn(si.Md, k, si.ld);
+  c.resid = si.resid != 0;
+  return c;
+}
+
+// [p - q]_+ (resid) or p
+__device__ __forceinline__ float weight(float y, float z, const RowConst &c) {
+  const float lp = __fmaf_rn(y, c.k, c.nT);
+  if (!c.resid) return ex2(lp);
+  const float lq = __fmaf_rn(z, c.k, c.nD);
   if (!(lq < lp)) return 0.f;
   return fmaxf(__fsub_rn(ex2(lp), ex2(lq)), 0.f);
 }
@@ -508,18 +591,32 @@ __device__ __forceinline__ void load_group(const char *row, int64_t g, int64_t V
 
 // the 8 weights of group g and their sequential sum a_g
 template <int DT, bool VEC>
-__device__ __forceinline__ float group_weights(const char *trow, const char *drow, bool resid, int64_t g,
-                                               int64_t V, const RowConst &c, float (&w)[8]) {
+__device__ __forceinline__ float group_weights(const char *trow, const char *drow, int64_t g, int64_t V,
+                                               const RowConst &c, float (&w)[8]) {
   float y[8], z[8];
   load_group<DT, VEC>(trow, g, V, y);
-  if (resid) load_group<DT, VEC>(drow, g, V, z);
+  if (c.resid) load_group<DT, VEC>(drow, g, V, z);
   float a = 0.f;
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
-    w[e] = weight(y[e], resid ? z[e] : 0.f, resid, c);
+    w[e] = weight(y[e], c.resid ? z[e] : 0.f, c);
     a = __fadd_rn(a, w[e]);
   }
   return a;
+}
+
+// last entry of group g with positive weight (-1: none)
+template <int DT, bool VEC>
+__device__ __forceinline__ int32_t last_positive(const char *trow, const char *drow, int64_t g, int64_t V,
+                                                 const RowConst &c) {
+  if (g < 0) return -1;
+  float w[8];
+  group_weights<DT, VEC>(trow, drow, g, V, c, w);
+  int32_t last = -1;
+#pragma unroll
+  for (int e = 0; e < 8; ++e)
+    if (w[e] > 0.f) last = static_cast<int32_t>(g * 8 + e);
+  return last;
 }
 
 struct SampleSmem {
@@ -528,7 +625,11 @@ struct SampleSmem {
   int32_t lastv[kThreads];
   float grp[kMaxGroupsPerSpan];
   float chunk_tot[1024];
-  float warp_tot[kWarps];
+  float ga[kRounds][kThreads];  // group totals of the chunk (round, thread)
+  float W[kRounds][kWarps];     // warp totals (round, warp)
+  float Rr[kRounds];            // round totals
+  int32_t warp_last[kWarps];
+  float gw[32][8];              // resolve: weights of the crossing warp's groups
   int32_t is_last;
   int32_t cstar;
   int32_t result;
@@ -545,9 +646,10 @@ struct SampleSmem {
 // row has no residual mass after rounding; its prefix is defined with 256
 // thread spans (sequential within and across spans).
 template <int DT, bool VEC>
-__device__ __noinline__ int32_t sample_whole_row_p(const char *trow, int64_t V, const RowConst &c, float wu,
+__device__ __noinline__ int32_t sample_whole_row_p(const char *trow, int64_t V, RowConst c, float wu,
                                                    SampleSmem &sm) {
   const int tid = threadIdx.x;
+  c.resid = false;
   const int64_t NG = (V + 7) / 8;
   const int64_t GPT = (NG + kThreads - 1) / kThreads;
   const int64_t g0 = min(NG, static_cast<int64_t>(tid) * GPT), g1 = min(NG, g0 + GPT);
@@ -555,7 +657,7 @@ __device__ __noinline__ int32_t sample_whole_row_p(const char *trow, int64_t V, 
   int32_t last = -1;
   for (int64_t g = g0; g < g1; ++g) {
     float w[8];
-    R = __fadd_rn(R, group_weights<DT, VEC>(trow, nullptr, false, g, V, c, w));
+    R = __fadd_rn(R, group_weights<DT, VEC>(trow, nullptr, g, V, c, w));
     for (int e = 0; e < 8; ++e)
       if (w[e] > 0.f) last = static_cast<int32_t>(g * 8 + e);
   }
@@ -589,7 +691,7 @@ __device__ __noinline__ int32_t sample_whole_row_p(const char *trow, int64_t V, 
   const int64_t h0 = min(NG, static_cast<int64_t>(ts) * GPT), h1 = min(NG, h0 + GPT);
   for (int64_t g = h0 + tid; g < h1; g += kThreads) {
     float w[8];
-    sm.grp[g - h0] = group_weights<DT, VEC>(trow, nullptr, false, g, V, c, w);
+    sm.grp[g - h0] = group_weights<DT, VEC>(trow, nullptr, g, V, c, w);
   }
   __syncthreads();
   if (tid == 0) {
@@ -600,7 +702,7 @@ __device__ __noinline__ int32_t sample_whole_row_p(const char *trow, int64_t V, 
       const float R2 = __fadd_rn(Rr, sm.grp[g - h0]);
       if (__fadd_rn(Es, R2) > t) {
         float w[8];
-        group_weights<DT, VEC>(trow, nullptr, false, g, V, c, w);
+        group_weights<DT, VEC>(trow, nullptr, g, V, c, w);
         float part = 0.f;
         for (int e = 0; e < 8; ++e) {
           part = __fadd_rn(part, w[e]);
@@ -619,75 +721,87 @@ __device__ __noinline__ int32_t sample_whole_row_p(const char *trow, int64_t V, 
 }
 
 // ---------------------------------------------------------------------------
-// kernel 4: inverse-CDF sampling over (request, sampler chunk) items
+// kernel 3: inverse-CDF sampling over (request, sampler chunk) items
 // ---------------------------------------------------------------------------
-constexpr int kGPL = 2;                               // groups per lane
-constexpr int kSChunk = kThreads * kGPL * 8;          // 4096 entries per sampler chunk
-
 template <int DT, bool VEC>
 __global__ void __launch_bounds__(kThreads) verify_sample(VerifyArgs a) {
-  using E = Elem<DT>;
   __shared__ SampleSmem sm;
-  if (*a.global_ok == 0) return;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int32_t Cs = a.Cs;
   // last requests first: their rows were streamed most recently
   const int64_t item = static_cast<int64_t>(a.N) * Cs - 1 - blockIdx.x;
   const int32_t i = static_cast<int32_t>(item / Cs);
   const int32_t c = static_cast<int32_t>(item - static_cast<int64_t>(i) * Cs);
+  pdl_wait();  // the finalize kernel's sampling rows and counters are in place
   const SampleInfo si = a.sinfo[i];
   if (!si.valid) return;
+  using E = Elem<DT>;
   const int64_t ci = __ldg(a.cu + i);
   const char *trow = static_cast<const char *>(a.target) + (ci + i + si.js) * a.V * E::kSize;
-  const bool resid = si.resid != 0;
-  const char *drow = resid ? static_cast<const char *>(a.draft) + (ci + si.js) * a.V * E::kSize : nullptr;
-  RowConst rc;
-  rc.Mt = si.Mt;
-  rc.lt = si.lt;
-  rc.Md = si.Md;
-  rc.ld = si.ld;
-  rc.k = a.k;
+  const RowConst rc = row_const(si, a.k);
+  const char *drow = rc.resid ? static_cast<const char *>(a.draft) + (ci + si.js) * a.V * E::kSize : nullptr;
   const int64_t NG = (a.V + 7) / 8;
 
-  // ---- this chunk: lane totals, warp totals, chunk total ----
-  const int64_t g0 = static_cast<int64_t>(c) * (kSChunk / 8) + static_cast<int64_t>(tid) * kGPL;
-  float a_g[kGPL];
-  int32_t last = -1;
-  {
-    float w[kGPL][8];
+  // ---- this chunk: group, warp, round and chunk totals ----
+  // round r, thread tid: group c * 2048 + r * 256 + tid
+  const int64_t gc = static_cast<int64_t>(c) * (kSChunk / 8);
+  int32_t lastg = -1;
+  if (VEC && DT == 1) {
+    uint4 ry[kRounds], rz[kRounds];  // all 16 loads of the thread first
 #pragma unroll
-    for (int u = 0; u < kGPL; ++u)
-      a_g[u] = (g0 + u < NG) ? group_weights<DT, VEC>(trow, drow, resid, g0 + u, a.V, rc, w[u]) : 0.f;
+    for (int r = 0; r < kRounds; ++r) {
+      const int64_t g = gc + r * kThreads + tid;
+      const bool in = g < NG;
+      ry[r] = in ? ld_vec(trow + g * 16) : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+      rz[r] = (in && rc.resid) ? ld_vec(drow + g * 16) : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+    }
 #pragma unroll
-    for (int u = 0; u < kGPL; ++u)
-      if (g0 + u < NG) {
+    for (int r = 0; r < kRounds; ++r) {
+      float y[8], z[8];
+      E::unpack(ry[r], y);
+      E::unpack(rz[r], z);
+      float ag = 0.f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          if (w[u][e] > 0.f) last = static_cast<int32_t>((g0 + u) * 8 + e);
+      for (int e = 0; e < 8; ++e) ag = __fadd_rn(ag, weight(y[e], z[e], rc));
+      sm.ga[r][tid] = ag;
+      if (ag > 0.f) lastg = static_cast<int32_t>(gc + r * kThreads + tid);
+    }
+  } else {
+#pragma unroll 2
+    for (int r = 0; r < kRounds; ++r) {
+      const int64_t g = gc + r * kThreads + tid;
+      float ag = 0.f;
+      if (g < NG) {
+        float w[8];
+        ag = group_weights<DT, VEC>(trow, drow, g, a.V, rc, w);
       }
+      sm.ga[r][tid] = ag;
+      if (ag > 0.f) lastg = static_cast<int32_t>(g);
+    }
   }
-  float T = 0.f;
 #pragma unroll
-  for (int u = 0; u < kGPL; ++u) T = __fadd_rn(T, a_g[u]);
+  for (int o = 16; o > 0; o >>= 1) lastg = max(lastg, __shfl_xor_sync(0xffffffffu, lastg, o));
+  if (lane == 0) sm.warp_last[warp] = lastg;
+  __syncthreads();
   const int64_t slot = static_cast<int64_t>(i) * Cs + c;
-  a.span_tot[slot * kThreads + tid] = T;
-  // warp total: sequential over lanes 0..31
-  float W = 0.f;
-  for (int l = 0; l < 32; ++l) W = __fadd_rn(W, __shfl_sync(0xffffffffu, T, l));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
-  if (lane == 0) {
-    sm.warp_tot[warp] = W;
-    sm.lastv[warp] = last;
+  if (lane < kRounds) {  // lane r of warp w: total of warp w in round r, over its 32 groups in order
+    float W = 0.f;
+    for (int l = 0; l < 32; ++l) W = __fadd_rn(W, sm.ga[lane][warp * 32 + l]);
+    sm.W[lane][warp] = W;
+    a.span_tot[slot * kSpan + lane * kWarps + warp] = W;
+  }
+  __syncthreads();
+  if (tid < kRounds) {
+    float R = 0.f;
+    for (int w = 0; w < kWarps; ++w) R = __fadd_rn(R, sm.W[tid][w]);
+    sm.Rr[tid] = R;
   }
   __syncthreads();
   if (tid == 0) {
     float Z = 0.f;
     int32_t lv = -1;
-    for (int w = 0; w < kWarps; ++w) {
-      Z = __fadd_rn(Z, sm.warp_tot[w]);
-      lv = max(lv, sm.lastv[w]);
-    }
+    for (int r = 0; r < kRounds; ++r) Z = __fadd_rn(Z, sm.Rr[r]);
+    for (int w = 0; w < kWarps; ++w) lv = max(lv, sm.warp_last[w]);
     a.chunk_tot[slot] = Z;
     a.chunk_last[slot] = lv;
     __threadfence();
@@ -706,7 +820,7 @@ __global__ void __launch_bounds__(kThreads) verify_sample(VerifyArgs a) {
     for (int q = 0; q < Cs; ++q) B = __fadd_rn(B, sm.chunk_tot[q]);
     const float t = __fmul_rn(si.w, B);
     sm.t = t;
-    sm.degenerate = (resid && !(B > 0.f)) ? 1 : 0;
+    sm.degenerate = (rc.resid && !(B > 0.f)) ? 1 : 0;
     int32_t cs = -1;
     float Bc = 0.f, Bp = 0.f;
     for (int q = 0; q < Cs && cs < 0; ++q) {
@@ -725,111 +839,90 @@ __global__ void __launch_bounds__(kThreads) verify_sample(VerifyArgs a) {
   } else if (sm.cstar < 0) {
     // w Z rounded up to Z: the last entry with positive weight
     if (tid == 0) {
-      int32_t lv = -1;
-      for (int q = 0; q < Cs; ++q) lv = max(lv, __ldcg(a.chunk_last + static_cast<int64_t>(i) * Cs + q));
-      sm.result = lv;
+      int32_t lg = -1;
+      for (int q = 0; q < Cs; ++q) lg = max(lg, __ldcg(a.chunk_last + static_cast<int64_t>(i) * Cs + q));
+      sm.result = last_positive<DT, VEC>(trow, drow, lg, a.V, rc);
     }
     __syncthreads();
     tok = sm.result;
   } else {
     const int32_t cs = sm.cstar;
-    sm.lane_tot[tid] = __ldcg(a.span_tot + (static_cast<int64_t>(i) * Cs + cs) * kThreads + tid);
+    if (tid < kSpan) sm.W[tid / kWarps][tid % kWarps] = __ldcg(a.span_tot + (static_cast<int64_t>(i) * Cs + cs) * kSpan + tid);
     __syncthreads();
     if (tid == 0) {
       const float t = sm.t, B = sm.Bc;
-      // warp level
-      float P = 0.f;
-      int32_t ws = -1;
-      float Pw = 0.f;
-      for (int w = 0; w < kWarps && ws < 0; ++w) {
-        float Ww = 0.f;
-        for (int l = 0; l < 32; ++l) Ww = __fadd_rn(Ww, sm.lane_tot[w * 32 + l]);
-        const float P2 = __fadd_rn(P, Ww);
+      // round level
+      float P = 0.f, Pr = 0.f;
+      int32_t rs = -1;
+      for (int r = 0; r < kRounds && rs < 0; ++r) {
+        float R = 0.f;
+        for (int w = 0; w < kWarps; ++w) R = __fadd_rn(R, sm.W[r][w]);
+        const float P2 = __fadd_rn(P, R);
         if (__fadd_rn(B, P2) > t) {
-          ws = w;
-          Pw = P;
+          rs = r;
+          Pr = P;
         }
         P = P2;
       }
-      // lane level
-      int32_t ls = -1;
-      float El = 0.f;
-      if (ws >= 0) {
-        float Ecur = 0.f;
-        for (int l = 0; l < 32 && ls < 0; ++l) {
-          const float E2 = __fadd_rn(Ecur, sm.lane_tot[ws * 32 + l]);
-          if (__fadd_rn(B, __fadd_rn(Pw, E2)) > t) {
-            ls = l;
-            El = Ecur;
+      // warp level
+      int32_t ws = -1;
+      float Qw = 0.f;
+      if (rs >= 0) {
+        float Q = 0.f;
+        for (int w = 0; w < kWarps && ws < 0; ++w) {
+          const float Q2 = __fadd_rn(Q, sm.W[rs][w]);
+          if (__fadd_rn(B, __fadd_rn(Pr, Q2)) > t) {
+            ws = w;
+            Qw = Q;
           }
-          Ecur = E2;
+          Q = Q2;
         }
       }
-      // group and entry level
+      sm.wstar = (rs >= 0 && ws >= 0) ? rs * kWarps + ws : -1;
+      sm.Pw = Pr;
+      sm.El = Qw;
+    }
+    __syncthreads();
+    // the crossing warp's 32 groups, one thread each
+    const int32_t rw = sm.wstar;
+    const int64_t gw0 = static_cast<int64_t>(cs) * (kSChunk / 8) +
+                        static_cast<int64_t>(rw / kWarps) * kThreads + static_cast<int64_t>(rw % kWarps) * 32;
+    if (rw >= 0 && tid < 32) {
+      float w[8];
+      const int64_t g = gw0 + tid;
+      sm.lane_tot[tid] = (g < NG) ? group_weights<DT, VEC>(trow, drow, g, a.V, rc, w) : 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sm.gw[tid][e] = (g < NG) ? w[e] : 0.f;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      const float t = sm.t, B = sm.Bc, Pr = sm.Pw, Qw = sm.El;
       int32_t pick = -1;
-      if (ls >= 0) {
-        const int64_t gg0 = static_cast<int64_t>(cs) * (kSChunk / 8) + static_cast<int64_t>(ws * 32 + ls) * kGPL;
-        float R = 0.f;
-        for (int u = 0; u < kGPL && pick < 0; ++u) {
-          if (gg0 + u >= NG) break;
-          float w[8];
-          const float ag = group_weights<DT, VEC>(trow, drow, resid, gg0 + u, a.V, rc, w);
-          const float R2 = __fadd_rn(R, ag);
-          if (__fadd_rn(B, __fadd_rn(Pw, __fadd_rn(El, R2))) > t) {
+      if (rw >= 0) {
+        float Ecur = 0.f;
+        for (int l = 0; l < 32 && pick < 0; ++l) {
+          const float E2 = __fadd_rn(Ecur, sm.lane_tot[l]);
+          if (__fadd_rn(B, __fadd_rn(Pr, __fadd_rn(Qw, E2))) > t) {
             float part = 0.f;
             for (int e = 0; e < 8; ++e) {
-              part = __fadd_rn(part, w[e]);
-              if (__fadd_rn(B, __fadd_rn(Pw, __fadd_rn(El, __fadd_rn(R, part)))) > t) {
-                pick = static_cast<int32_t>((gg0 + u) * 8 + e);
+              part = __fadd_rn(part, sm.gw[l][e]);
+              if (__fadd_rn(B, __fadd_rn(Pr, __fadd_rn(Qw, __fadd_rn(Ecur, part)))) > t) {
+                pick = static_cast<int32_t>((gw0 + l) * 8 + e);
                 break;
               }
             }
           }
-          R = R2;
+          Ecur = E2;
         }
       }
-      if (pick < 0) pick = __ldcg(a.chunk_last + static_cast<int64_t>(i) * Cs + cs);  // unreachable
+      if (pick < 0)  // unreachable: the levels' totals agree exactly
+        pick = last_positive<DT, VEC>(trow, drow, __ldcg(a.chunk_last + static_cast<int64_t>(i) * Cs + cs), a.V, rc);
       sm.result = pick;
     }
     __syncthreads();
     tok = sm.result;
   }
   if (tid == 0) a.next_token[i] = tok;
-}
-
-// ---------------------------------------------------------------------------
-// kernel 1: prologue
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(1024) verify_prologue(VerifyArgs a) {
-  __shared__ int s_bad;
-  if (threadIdx.x == 0) s_bad = 0;
-  __syncthreads();
-  int bad = 0;
-  if (threadIdx.x == 0 && (__ldg(a.cu) != 0 || static_cast<int64_t>(__ldg(a.cu + a.N)) != a.total_rows))
-    bad |= 2;
-  for (int i = threadIdx.x; i < a.N; i += blockDim.x) {
-    const int32_t c0 = __ldg(a.cu + i), c1 = __ldg(a.cu + i + 1);
-    const int32_t L = c1 - c0;
-    if (L < 0) bad |= 2;
-    bool ok = (L >= 1 && L <= a.max_len && c0 >= 0 && static_cast<int64_t>(c1) <= a.total_rows);
-    if (ok)
-      for (int j = 0; j < L; ++j) {
-        const int32_t x = __ldg(a.tokens + c0 + j);
-        if (x < 0 || static_cast<int64_t>(x) >= a.V) ok = false;
-      }
-    a.req_ok[i] = ok ? 1 : 0;
-    a.sample_counters[i] = 0;
-    a.sinfo[i].valid = 0;
-    a.accept_len[i] = -1;
-    a.next_token[i] = -1;
-    if (!ok) bad |= 1;
-  }
-  if (bad) atomicOr(&s_bad, bad);
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    *a.global_ok = (s_bad & 2) ? 0 : 1;
-    if (s_bad && a.status) atomicOr(a.status, SVW_DEV_BAD_INPUT);
-  }
 }
 
 // ---------------------------------------------------------------------------
@@ -860,10 +953,27 @@ int cached_grid(const void *fn, int threads, int smem, cudaError_t &e) {
   return blocks;
 }
 
+// launch as a programmatic dependent of the previous kernel in the stream
+template <typename Kern>
+cudaError_t launch_dependent(Kern kern, unsigned grid, const VerifyArgs &a, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 template <int DT, bool VEC, bool GREEDY>
-cudaError_t launch_all_t(const VerifyArgs &a, cudaStream_t st) {
+cudaError_t launch_all_t(const VerifyArgs &args, cudaStream_t st) {
   using E = Elem<DT>;
-  const int stage_bytes = VEC ? (a.chunk_len * E::kSize + 127) / 128 * 128 : 0;
+  const int stage_bytes = VEC ? (args.chunk_len * E::kSize + 127) / 128 * 128 : 0;
   const int smem = VEC ? kStages * stage_bytes : 0;
   auto fn = verify_stats<DT, VEC, GREEDY>;
   cudaError_t e = cudaSuccess;
@@ -873,15 +983,19 @@ cudaError_t launch_all_t(const VerifyArgs &a, cudaStream_t st) {
   }
   int grid = cached_grid(reinterpret_cast<const void *>(fn), kStatsThreads, smem, e);
   if (e != cudaSuccess) return e;
-  if (grid > a.total_items) grid = static_cast<int>(a.total_items);
+  if (grid > args.total_items) grid = static_cast<int>(args.total_items);
+  if (grid > kMaxStatsGrid) grid = kMaxStatsGrid;
+  if (grid < 1) grid = 1;
+  VerifyArgs a = args;
+  a.stats_grid = grid;
+  // the first kernel is an ordinary launch: it waits for all earlier work in
+  // the stream (a previous call's sampler may still read this workspace)
   fn<<<grid, kStatsThreads, smem, st>>>(a, stage_bytes);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  verify_finalize<DT, GREEDY><<<a.N, kThreads, 0, st>>>(a);
-  e = cudaGetLastError();
+  e = launch_dependent(verify_finalize<DT, GREEDY>, static_cast<unsigned>(a.N), a, st);
   if (e != cudaSuccess || GREEDY) return e;
-  verify_sample<DT, VEC><<<static_cast<unsigned>(static_cast<int64_t>(a.N) * a.Cs), kThreads, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_dependent(verify_sample<DT, VEC>, static_cast<unsigned>(static_cast<int64_t>(a.N) * a.Cs), a, st);
 }
 
 template <int DT, bool VEC>
@@ -917,26 +1031,21 @@ VerifyLayout verify_layout(int32_t N, int64_t total_rows, int64_t V, int esize) 
   off += align256(rows * static_cast<size_t>(p.C) * kCW * sizeof(Partial));
   l.sample_counters_off = off;
   off += align256(static_cast<size_t>(N) * 4);
-  l.req_ok_off = off;
-  off += align256(static_cast<size_t>(N) * 4);
   l.sinfo_off = off;
   off += align256(static_cast<size_t>(N) * sizeof(SampleInfo));
   l.span_off = off;
-  off += align256(ns * kThreads * sizeof(float));
+  off += align256(ns * kSpan * sizeof(float));
   l.chunk_tot_off = off;
   off += align256(ns * sizeof(float));
   l.chunk_last_off = off;
   off += align256(ns * sizeof(int32_t));
-  l.global_ok_off = off;
-  off += 256;
+  l.csr_bad_off = off;
+  off += align256(kMaxStatsGrid * sizeof(int32_t));
   l.total = off;
   return l;
 }
 
 cudaError_t launch_verify(const VerifyArgs &a, int dtype, bool vec, bool greedy, cudaStream_t st) {
-  verify_prologue<<<1, 1024, 0, st>>>(a);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
   if (dtype == SVW_BF16) return vec ? launch_all<1, true>(a, greedy, st) : launch_all<1, false>(a, greedy, st);
   return vec ? launch_all<0, true>(a, greedy, st) : launch_all<0, false>(a, greedy, st);
 }
