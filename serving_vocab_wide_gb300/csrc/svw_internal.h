@@ -58,7 +58,7 @@ struct VerifyArgs {
   int32_t *accept_len;
   int32_t *next_token;
   int32_t *status;
-  Partial *part;                     // [(rows_t + total_rows) * C * 8] per-warp chunk partials
+  Partial *part;                     // [(rows_t + total_rows) * C * 16] per-warp chunk partials
   int32_t *sample_counters;          // [N] sampling arrivals per request
   SampleInfo *sinfo;                 // [N]
   float *span_tot;                   // [N * Cs * 64] sampler warp totals (round, warp)

@@ -13,8 +13,8 @@
 //                       Persistent CTAs take items in a fixed stride.  One
 //                       producer warp streams each chunk into a 3-stage
 //                       shared-memory ring with 1-D bulk async copies
-//                       (cp.async.bulk, full/empty mbarriers); eight consumer
-//                       warps reduce their share of the chunk to
+//                       (cp.async.bulk, full/empty mbarriers); 8 consumer (16
+//                       when greedy) warps reduce their share of the chunk to
 //                       (max, sum 2^((x - max) log2e/T)) -- or (max, argmax)
 //                       when greedy -- with packed bf16 max and f32x2
 //                       arithmetic, and write one Partial per warp.  No block
@@ -59,11 +59,19 @@ namespace svw {
 
 namespace {
 
-constexpr int kCW = 8;                         // consumer warps of the stats kernel
-constexpr int kStatsThreads = (kCW + 1) * 32;  // + one producer warp
+// consumer warps of the stats kernel: the argmax reduction is cheap per entry
+// and latency-bound, so greedy mode takes twice the warps
+constexpr int kCWMax = 16;
+template <bool GREEDY>
+struct StatsShape {
+  static constexpr int kCW = GREEDY ? 16 : 8;
+  static constexpr int kThreads = (kCW + 1) * 32;  // + one producer warp
+};
 constexpr int kStages = 3;                     // bulk-copy ring depth (2 CTAs per SM)
-constexpr int kThreads = 256;                  // finalize / sample kernels
+constexpr int kThreads = 256;                  // sample kernel
 constexpr int kWarps = kThreads / 32;
+constexpr int kFinThreads = 1024;              // finalize kernel: about one row per warp
+constexpr int kFinWarps = kFinThreads / 32;
 constexpr int kMaxRows = 2 * SVW_MAX_LEN + 1;
 constexpr int kMaxGroupsPerSpan = 512;  // single-CTA fallback sampler: V <= 256 * 512 * 8
 
@@ -155,21 +163,21 @@ __device__ __forceinline__ ItemMeta decode_item(const VerifyArgs &a, int64_t ite
 // consumer-warp reductions over one chunk held in shared memory (16-byte
 // vectors vi = wid*32 + lane + j*256 of the chunk)
 // ---------------------------------------------------------------------------
-template <int DT>
+template <int DT, int CW>
 __device__ __forceinline__ void warp_lse_smem(uint32_t base, int nvec, int wid, int lane, float k,
                                               float &m, float &s) {
   const int v0 = wid * 32 + lane;
   float mx = -INFINITY;
   if (DT == 1) {
     uint32_t mw = 0xff80ff80u;  // (-inf, -inf)
-    for (int vi = v0; vi < nvec; vi += kCW * 32) {
+    for (int vi = v0; vi < nvec; vi += CW * 32) {
       const uint4 q = lds128(base + vi * 16);
       mw = bf16x2_max(mw, bf16x2_max(bf16x2_max(q.x, q.y), bf16x2_max(q.z, q.w)));
     }
     const float2 f = bf16x2_f2(mw);
     mx = fmaxf(f.x, f.y);
   } else {
-    for (int vi = v0; vi < nvec; vi += kCW * 32) {
+    for (int vi = v0; vi < nvec; vi += CW * 32) {
       const uint4 q = lds128(base + vi * 16);
       mx = fmaxf(fmaxf(mx, fmaxf(__uint_as_float(q.x), __uint_as_float(q.y))),
                  fmaxf(__uint_as_float(q.z), __uint_as_float(q.w)));
@@ -181,7 +189,7 @@ __device__ __forceinline__ void warp_lse_smem(uint32_t base, int nvec, int wid, 
   const float mref = (mx == -INFINITY) ? 0.f : mx;
   const float2 nm = make_float2(-mref, -mref), kk = make_float2(k, k);
   float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-  for (int vi = v0; vi < nvec; vi += kCW * 32) {
+  for (int vi = v0; vi < nvec; vi += CW * 32) {
     const uint4 q = lds128(base + vi * 16);
     if (DT == 1) {
       const float2 d0 = __fmul2_rn(__fadd2_rn(bf16x2_f2(q.x), nm), kk);  // (x - max) exact, then * log2e/T
@@ -203,7 +211,7 @@ __device__ __forceinline__ void warp_lse_smem(uint32_t base, int nvec, int wid, 
   if (!(mx == mx)) s = mx;  // all-NaN warp: keep the NaN visible
 }
 
-template <int DT>
+template <int DT, int CW>
 __device__ __forceinline__ void warp_amax_smem(uint32_t base, int nvec, int32_t c0, int wid, int lane,
                                                float &best, int32_t &idx, int32_t &nan) {
   using E = Elem<DT>;
@@ -213,7 +221,7 @@ __device__ __forceinline__ void warp_amax_smem(uint32_t base, int nvec, int32_t 
   uint32_t nanw = 0;
   if (DT == 1) {
     uint32_t mw = 0xff80ff80u;  // NaN-propagating max: a NaN anywhere survives
-    for (int vi = v0; vi < nvec; vi += kCW * 32) {
+    for (int vi = v0; vi < nvec; vi += CW * 32) {
       const uint4 q = lds128(base + vi * 16);
       mw = bf16x2_max_nan(mw, bf16x2_max_nan(bf16x2_max_nan(q.x, q.y), bf16x2_max_nan(q.z, q.w)));
     }
@@ -221,7 +229,7 @@ __device__ __forceinline__ void warp_amax_smem(uint32_t base, int nvec, int32_t 
     const float2 f = bf16x2_f2(mw);
     mx = fmaxf(f.x, f.y);
   } else {
-    for (int vi = v0; vi < nvec; vi += kCW * 32) {
+    for (int vi = v0; vi < nvec; vi += CW * 32) {
       const uint4 q = lds128(base + vi * 16);
       const float x[4] = {__uint_as_float(q.x), __uint_as_float(q.y), __uint_as_float(q.z),
                           __uint_as_float(q.w)};
@@ -239,7 +247,7 @@ __device__ __forceinline__ void warp_amax_smem(uint32_t base, int nvec, int32_t 
   // (each lane's vectors are in index order, lanes interleave by vector)
   idx = INT32_MAX;
   if (mx == wmx && nvec > 0) {
-    for (int vi = v0; vi < nvec && idx == INT32_MAX; vi += kCW * 32) {
+    for (int vi = v0; vi < nvec && idx == INT32_MAX; vi += CW * 32) {
       float x[EPV];
       E::unpack(lds128(base + vi * 16), x);
 #pragma unroll
@@ -255,15 +263,15 @@ __device__ __forceinline__ void warp_amax_smem(uint32_t base, int nvec, int32_t 
 
 // plain-load variants for rows that are not 16-byte pitched (whole warp,
 // elements v = wid*32 + lane + j*256 of the chunk)
-template <int DT>
+template <int DT, int CW>
 __device__ __forceinline__ void warp_lse_global(const char *p0, int n, int wid, int lane, float k, float &m,
                                                 float &s) {
   using E = Elem<DT>;
   float mx = -INFINITY;
-  for (int v = wid * 32 + lane; v < n; v += kCW * 32) mx = fmaxf(mx, E::load(p0, v));
+  for (int v = wid * 32 + lane; v < n; v += CW * 32) mx = fmaxf(mx, E::load(p0, v));
   const float mref = (mx == -INFINITY) ? 0.f : mx;
   float acc = 0.f;
-  for (int v = wid * 32 + lane; v < n; v += kCW * 32)
+  for (int v = wid * 32 + lane; v < n; v += CW * 32)
     acc = __fadd_rn(acc, ex2(__fmul_rn(__fsub_rn(E::load(p0, v), mref), k)));
   m = -INFINITY;
   s = 0.f;
@@ -271,14 +279,14 @@ __device__ __forceinline__ void warp_lse_global(const char *p0, int n, int wid, 
   warp_lse(m, s, k);
 }
 
-template <int DT>
+template <int DT, int CW>
 __device__ __forceinline__ void warp_amax_global(const char *p0, int n, int32_t c0, int wid, int lane,
                                                  float &best, int32_t &idx, int32_t &nan) {
   using E = Elem<DT>;
   best = -INFINITY;
   idx = INT32_MAX;
   nan = 0;
-  for (int v = wid * 32 + lane; v < n; v += kCW * 32) {
+  for (int v = wid * 32 + lane; v < n; v += CW * 32) {
     const float x = E::load(p0, v);
     nan |= (x != x);
     if (x > best || (idx == INT32_MAX && x == x)) {
@@ -294,7 +302,9 @@ __device__ __forceinline__ void warp_amax_global(const char *p0, int n, int32_t 
 // kernel 2: stats stream
 // ---------------------------------------------------------------------------
 template <int DT, bool BULK, bool GREEDY>
-__global__ void __launch_bounds__(kStatsThreads, 2) verify_stats(VerifyArgs a, int stage_bytes) {
+__global__ void __launch_bounds__(StatsShape<GREEDY>::kThreads, 2) verify_stats(VerifyArgs a, int stage_bytes) {
+  constexpr int kCW = StatsShape<GREEDY>::kCW;
+  constexpr int kStatsThreads = StatsShape<GREEDY>::kThreads;
   extern __shared__ __align__(128) unsigned char ring[];
   __shared__ unsigned long long full[kStages], empty[kStages];
   __shared__ ItemMeta meta[kStages];
@@ -322,10 +332,10 @@ __global__ void __launch_bounds__(kStatsThreads, 2) verify_stats(VerifyArgs a, i
       if (!m.valid) continue;
       Partial res;
       if (GREEDY) {
-        warp_amax_global<DT>(m.src, m.n, m.chunk * a.chunk_len, wid, lane, res.m, res.idx, res.nan);
+        warp_amax_global<DT, kCW>(m.src, m.n, m.chunk * a.chunk_len, wid, lane, res.m, res.idx, res.nan);
         res.s = 0.f;
       } else {
-        warp_lse_global<DT>(m.src, m.n, wid, lane, a.k, res.m, res.s);
+        warp_lse_global<DT, kCW>(m.src, m.n, wid, lane, a.k, res.m, res.s);
         res.idx = 0;
         res.nan = 0;
       }
@@ -386,10 +396,10 @@ __global__ void __launch_bounds__(kStatsThreads, 2) verify_stats(VerifyArgs a, i
       const int nvec = m.n / Elem<DT>::kPerVec;
       Partial res;
       if (GREEDY) {
-        warp_amax_smem<DT>(base, nvec, m.chunk * a.chunk_len, wid, lane, res.m, res.idx, res.nan);
+        warp_amax_smem<DT, kCW>(base, nvec, m.chunk * a.chunk_len, wid, lane, res.m, res.idx, res.nan);
         res.s = 0.f;
       } else {
-        warp_lse_smem<DT>(base, nvec, wid, lane, a.k, res.m, res.s);
+        warp_lse_smem<DT, kCW>(base, nvec, wid, lane, a.k, res.m, res.s);
         res.idx = 0;
         res.nan = 0;
       }
@@ -404,7 +414,7 @@ __global__ void __launch_bounds__(kStatsThreads, 2) verify_stats(VerifyArgs a, i
 // kernel 2: per-request validation, merge, accept tests
 // ---------------------------------------------------------------------------
 template <int DT, bool GREEDY>
-__global__ void __launch_bounds__(kThreads) verify_finalize(VerifyArgs a) {
+__global__ void __launch_bounds__(kFinThreads) verify_finalize(VerifyArgs a) {
   using E = Elem<DT>;
   __shared__ float row_m[kMaxRows];
   __shared__ float row_l[kMaxRows];
@@ -442,7 +452,7 @@ __global__ void __launch_bounds__(kThreads) verify_finalize(VerifyArgs a) {
   pdl_wait();  // the stats kernel's partials and CSR flags are complete
 
   int csr_bad = 0;
-  for (int b = tid; b < a.stats_grid; b += kThreads) csr_bad |= __ldcg(a.csr_bad + b);
+  for (int b = tid; b < a.stats_grid; b += kFinThreads) csr_bad |= __ldcg(a.csr_bad + b);
   csr_bad = __syncthreads_or(csr_bad);
   auto reject = [&]() {  // one thread: a bad request
     a.accept_len[i] = -1;
@@ -455,8 +465,8 @@ __global__ void __launch_bounds__(kThreads) verify_finalize(VerifyArgs a) {
     return;
   }
   const int32_t nrows = GREEDY ? L + 1 : 2 * L + 1;
-  const int np = a.C * kCW;  // partials per row
-  for (int r = warp; r < nrows; r += kWarps) {
+  const int np = a.C * StatsShape<GREEDY>::kCW;  // partials per row
+  for (int r = warp; r < nrows; r += kFinWarps) {
     const int64_t prow = (r <= L) ? (t0 + r) : (a.rows_t + d0 + (r - L - 1));
     const Partial *pp = a.part + prow * np;
     if (GREEDY) {
@@ -955,13 +965,13 @@ int cached_grid(const void *fn, int threads, int smem, cudaError_t &e) {
 
 // launch as a programmatic dependent of the previous kernel in the stream
 template <typename Kern>
-cudaError_t launch_dependent(Kern kern, unsigned grid, const VerifyArgs &a, cudaStream_t st) {
+cudaError_t launch_dependent(Kern kern, unsigned grid, unsigned block, const VerifyArgs &a, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(block, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = st;
   cfg.attrs = attr;
@@ -981,6 +991,7 @@ cudaError_t launch_all_t(const VerifyArgs &args, cudaStream_t st) {
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
   }
+  constexpr int kStatsThreads = StatsShape<GREEDY>::kThreads;
   int grid = cached_grid(reinterpret_cast<const void *>(fn), kStatsThreads, smem, e);
   if (e != cudaSuccess) return e;
   if (grid > args.total_items) grid = static_cast<int>(args.total_items);
@@ -993,9 +1004,10 @@ cudaError_t launch_all_t(const VerifyArgs &args, cudaStream_t st) {
   fn<<<grid, kStatsThreads, smem, st>>>(a, stage_bytes);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = launch_dependent(verify_finalize<DT, GREEDY>, static_cast<unsigned>(a.N), a, st);
+  e = launch_dependent(verify_finalize<DT, GREEDY>, static_cast<unsigned>(a.N), kFinThreads, a, st);
   if (e != cudaSuccess || GREEDY) return e;
-  return launch_dependent(verify_sample<DT, VEC>, static_cast<unsigned>(static_cast<int64_t>(a.N) * a.Cs), a, st);
+  return launch_dependent(verify_sample<DT, VEC>, static_cast<unsigned>(static_cast<int64_t>(a.N) * a.Cs), kThreads,
+                          a, st);
 }
 
 template <int DT, bool VEC>
@@ -1028,7 +1040,7 @@ VerifyLayout verify_layout(int32_t N, int64_t total_rows, int64_t V, int esize) 
   const size_t ns = static_cast<size_t>(N) * Cs;
   size_t off = 0;
   l.part_off = off;
-  off += align256(rows * static_cast<size_t>(p.C) * kCW * sizeof(Partial));
+  off += align256(rows * static_cast<size_t>(p.C) * kCWMax * sizeof(Partial));
   l.sample_counters_off = off;
   off += align256(static_cast<size_t>(N) * 4);
   l.sinfo_off = off;
