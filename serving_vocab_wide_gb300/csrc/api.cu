@@ -1,6 +1,7 @@
 // api.cu -- the exported C ABI (see include/svw.h): host-side validation,
 // workspace carving, and dispatch to the kernel launchers.  No allocation,
 // no host synchronisation, no device-memory reads from the host.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -151,6 +152,10 @@ svw_status opd_loss(const void *target_logits, const void *draft_logits, svw_dty
   a.dlogits = dlogits;
   a.status = status;
   a.flags = static_cast<int32_t *>(workspace);
+  static std::atomic<uint32_t> g_epoch{0x3c5a0000u};
+  uint32_t ep = ++g_epoch;
+  if (ep == 0) ep = ++g_epoch;
+  a.epoch = static_cast<int32_t>(ep);
   a.rowc = workspace ? reinterpret_cast<float4 *>(static_cast<char *>(workspace) + opd_flags_bytes(total_draft_rows))
                      : nullptr;
   const cudaError_t e = svw::launch_opd(a, dtype, bulk, static_cast<cudaStream_t>(stream));

@@ -24,7 +24,9 @@
 //   KL(q||p) = ln2 (U/S_z - log2 S_z + log2 S_y),  S = sum_v q_v a_v = KL + 1;
 // one DSMEM exchange (barrier.cluster) merges these over the cluster, and a
 // second register pass writes the gradient.  An entry whose term reaches the
-// clip bound, or a non-finite KL (masked entries), flags the row.
+// clip bound, or a non-finite KL (masked entries), flags the row: the flag
+// word is set to the call's tag (never cleared), so flags need no ordering
+// and a stale tag at worst sends a row to the exact fix-up once more.
 // Exact kernel.  Rows the fast kernel flagged (and every row of shapes that
 // are not 16-byte pitched) are redone from shared memory in three passes:
 // log-sum-exps; clamped terms, S and the argmax; gradient -- two exchanges.
@@ -660,7 +662,6 @@ __global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) 
   __syncthreads();
 
   for (int64_t r = cid, it = 0; r < a.R; r += nclusters, ++it) {
-    if (rank == 0 && tid == 0) a.flags[r] = 0;  // before this row's exchange
     if (!sm.abort && !mbar_wait_bounded(&sm.mbar, static_cast<uint32_t>(it & 1))) {
       if (a.status) atomicOr(a.status, SVW_DEV_TIMEOUT);
       sm.abort_parity = static_cast<uint32_t>(it & 1);
@@ -815,15 +816,17 @@ __global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) 
     const bool exact = (kl == kl) && fabsf(kl) <= FLT_MAX;
     if (rank == 0 && tid == 0) {
       float out = __int_as_float(0x7fffffff);
+      float4 rc = make_float4(__int_as_float(0x7fffffff), 0.f, 0.f, 0.f);  // NaN: not a row to fix
       if (row_ok && xs != INT32_MAX) {
         out = kl - a.lambda_ce * kLn2 * fmaf(Rw.zx, k, -Cd);
-        if (!exact) a.flags[r] = 1;  // masked entries: the fix-up kernel redoes this row
+        if (!exact) a.flags[r] = a.epoch;  // masked entries: the fix-up kernel redoes this row
         const int64_t t = sm_tr_row;
-        a.rowc[r] = make_float4(Ct, Cd, __int_as_float(xs),
-                                __int_as_float(t < (int64_t{1} << 31) ? static_cast<int32_t>(t) : -2));
+        rc = make_float4(Ct, Cd, __int_as_float(xs),
+                         __int_as_float(t < (int64_t{1} << 31) ? static_cast<int32_t>(t) : -2));
       } else if (a.status && !any_abort) {
         atomicOr(a.status, SVW_DEV_BAD_INPUT);
       }
+      a.rowc[r] = rc;
       a.loss[r] = out;
     }
 
@@ -886,8 +889,9 @@ __global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) 
             }
           }
       }
-      // some term reached the clip: the fix-up kernel redoes the row
-      if (row_ok && !(tmax < c2)) a.flags[r] = 1;
+      // some term reached the clip: the fix-up kernel redoes the row (every
+      // writer stores the same call tag, so no ordering is needed)
+      if (row_ok && !(tmax < c2)) a.flags[r] = a.epoch;
     }
   }
   // after a timeout no copy is issued; let the one that timed out land if it can
@@ -977,7 +981,8 @@ __global__ void __launch_bounds__(NT, 2) opd_fix_kernel(OpdArgs a, OpdGeo geo) {
 #pragma unroll
     for (int e = 0; e < kPer; ++e) {
       const int64_t r = base + tid * kPer + e;
-      f[e] = (r < a.R) ? __ldcg(a.flags + r) : 0;
+      f[e] = (r < a.R && __ldcg(a.flags + r) == a.epoch) ? 1 : 0;
+      if (f[e] && __ldcg(&a.rowc[r].x) != __ldcg(&a.rowc[r].x)) f[e] = 0;  // stale tag on a bad row
       cnt += (f[e] != 0);
     }
     int incl = cnt;

@@ -92,8 +92,9 @@ struct OpdArgs {
   float *dlogits;
   int32_t *status;
   // workspace of the fast path (NULL: the exact kernel takes every row)
-  int32_t *flags;  // [R] rows the fix-up kernel must redo
-  float4 *rowc;    // [R] row constants of the fast kernel: Ct, Cd, x*, target row
+  int32_t *flags;  // [R] == epoch: rows the fix-up kernel must redo
+  float4 *rowc;    // [R] row constants of the fast kernel: Ct, Cd, x*, target row (NaN: bad row)
+  int32_t epoch;   // this call's tag (never 0)
 };
 
 cudaError_t launch_opd(const OpdArgs &a, int dtype, bool bulk, cudaStream_t stream);
