@@ -58,10 +58,26 @@ def _dist():
     return ws, rank, local
 
 
-def make_batch(rank: int):
+def make_batch(rank: int, **overrides):
+    """This rank's batch.  Weak scaling: every rank verifies its own batch of
+    the same configuration (independent requests, its own data seed)."""
     import synth
-    # weak scaling: every rank verifies its own batch of the same shape
-    return synth.config(5, seed=1005 + 7919 * rank)
+    return synth.config(5, seed=1005 + 7919 * rank, **overrides)
+
+
+def reduce_over_ranks(ws: int, dev, elapsed_ms: float, units: float):
+    """Job-level timing: the slowest rank's timed region (max) and the units
+    all ranks processed (sum).  The only collectives of the run; none is on
+    the data path."""
+    if ws == 1:
+        return float(elapsed_ms), float(units)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
 
 
 def _src_hash(files):
@@ -246,11 +262,8 @@ def run_native(args, ws, rank, local):
         torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
-    elapsed_ms = e0.elapsed_time(e1)
-    if ws > 1:
-        tt = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    positions_per_step = 3 * R
+    elapsed_ms, job_positions = reduce_over_ranks(ws, dev, e0.elapsed_time(e1), positions_per_step)
     per_call = {c: [] for c in calls}
     for k in range(K):
         for ci, c in enumerate(calls):
@@ -264,8 +277,7 @@ def run_native(args, ws, rank, local):
            "verify_T1": (rows_t + R) * V * es,
            "opd": 2 * R * V * es + R * V * 4}
     ms_per_step = elapsed_ms / K
-    positions_per_step = 3 * R
-    value = positions_per_step * ws / (elapsed_ms / K / 1000.0)
+    value = job_positions / (elapsed_ms / K / 1000.0)
     step_bytes = sum(alg.values())
     peak, peak_kind = _peaks()
     dom = max(calls, key=lambda c: avg_us[c])
@@ -301,14 +313,10 @@ def run_native(args, ws, rank, local):
         e2e_step()
     f1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = f0.elapsed_time(f1)
-    if ws > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms, _ = reduce_over_ranks(ws, dev, f0.elapsed_time(f1), positions_per_step)
     h2d = (h_t.numel() + h_d.numel()) * 2 + h_cu.numel() * 4 + sum(v.numel() * 4 for v in h_tok.values())
     d2h = 2 * 3 * N * 4 + R * 4
-    e2e = {"value": positions_per_step * ws / (e2e_ms / Ke / 1000.0), "unit": UNIT,
+    e2e = {"value": job_positions / (e2e_ms / Ke / 1000.0), "unit": UNIT,
            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": Ke}
 
     status_v = int(status.item())
