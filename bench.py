@@ -2,8 +2,11 @@
 
 Workload (default "mix"): N = 256 requests, L_i ~ U{2,4,8,16} packed by CSR
 offsets, V = 151936, bf16 logits (log-Zipf target + Gaussian draft noise).
-One step = spec_verify at T = 0, 0.6 and 1.0 plus opd_loss (T = 1, c = 1,
-lambda = 0.1, forward + gradient) on the same batch: every step of the path.
+One step = spec_verify at T = 0 and 0.6, and spec_verify_opd at T = 1 --
+verification plus the OPD loss (T = 1, c = 1, lambda = 0.1, forward +
+gradient) on the same batch in one pass: every step of the path, three
+verifications and one loss per step.  The separate T = 1 spec_verify and
+opd_loss calls are timed beside it for comparison.
 
 Metric: verified draft positions per second (3 x sum_i L_i per step) for the
 whole job; the achieved HBM bandwidth of the dominant kernel is reported in
@@ -91,11 +94,17 @@ def _src_hash(files):
 KERNEL_SOURCES = {
     "spec_verify": ["verify.cu", "svw_device.cuh", "svw_internal.h"],
     "opd_loss": ["opd.cu", "svw_device.cuh", "svw_internal.h"],
+    "spec_verify_opd": ["opd.cu", "fused.cu", "verify.cu", "svw_device.cuh", "svw_internal.h"],
 }
 CALL_KERNELS = {
     "spec_verify": "verify_stats + verify_finalize (+ verify_sample at T > 0)",
     "opd_loss": "opd_fast_kernel + opd_fix_kernel",
+    "spec_verify_opd": "opd_fast_kernel (draft rows + bonus rows) + fused_finalize + verify_sample + opd_fix_kernel",
 }
+CALLS = ["verify_T0", "verify_T0.6", "verify_T1+opd"]
+WORKLOAD = ("mix: N=256 ragged L_i~U{2,4,8,16}, V=151936, bf16 log-Zipf logits; verify at T=0 and 0.6, "
+            "verify at T=1 fused with OPD fwd/bwd (T=1,c=1,lambda=0.1)")
+CALL_API = {"verify_T0": "spec_verify", "verify_T0.6": "spec_verify", "verify_T1+opd": "spec_verify_opd"}
 
 
 def _profile_traffic(kernel: str, workload: str):
@@ -183,8 +192,8 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 def launches_per_step():
     """Kernels one step launches: spec_verify = stats + finalize (+ sample at
-    T > 0); opd_loss = fast pass + exact fix-up."""
-    return sum(2 if T == 0 else 3 for T in TEMPS) + 2
+    T > 0), twice; spec_verify_opd = fast pass + finalize + sample + fix-up."""
+    return 2 + 3 + 4
 
 
 def run_native(args, ws, rank, local):
@@ -217,29 +226,32 @@ def run_native(args, ws, rank, local):
     ws_bytes = svw.verify_workspace_size(N, R, V, svw.SVW_BF16)
     wsp = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     opd_ws = torch.empty(svw.opd_workspace_size(R), dtype=torch.uint8, device=dev)
+    fused_ws = torch.empty(svw.verify_opd_workspace_size(N, R, V, svw.SVW_BF16), dtype=torch.uint8, device=dev)
     acc = {T: torch.empty(N, dtype=torch.int32, device=dev) for T in TEMPS}
     nxt = {T: torch.empty(N, dtype=torch.int32, device=dev) for T in TEMPS}
     loss = torch.empty(R, dtype=torch.float32, device=dev)
     grad = torch.empty((R, V), dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
-    calls = ["verify_T0", "verify_T0.6", "verify_T1", "opd"]
+    calls = CALLS
+
+    def verify(T):
+        svw.spec_verify(t, d, cu, tok[T], T, 0, max_len=16, total_draft_rows=R, accept_len=acc[T],
+                        next_token=nxt[T], status=status, workspace=wsp, stream=stream)
+
+    def verify_opd():
+        svw.spec_verify_opd(t, d, cu, tok[1.0], 1.0, 0, opd_temperature=OPD["temperature"],
+                            clip_c=OPD["clip_c"], lambda_ce=OPD["lambda_ce"], max_len=16,
+                            total_draft_rows=R, accept_len=acc[1.0], next_token=nxt[1.0], loss=loss,
+                            dlogits=grad, status=status, workspace=fused_ws, stream=stream)
 
     def step(ev=None):
-        for ci, T in enumerate(TEMPS):
+        for ci, fn in enumerate((lambda: verify(0.0), lambda: verify(0.6), verify_opd)):
             if ev is not None:
                 ev[2 * ci].record(stream)
-            svw.spec_verify(t, d, cu, tok[T], T, 0, max_len=16, total_draft_rows=R,
-                            accept_len=acc[T], next_token=nxt[T], status=status,
-                            workspace=wsp, stream=stream)
+            fn()
             if ev is not None:
                 ev[2 * ci + 1].record(stream)
-        if ev is not None:
-            ev[6].record(stream)
-        svw.opd_loss(t, d, cu_draft=cu, has_bonus=True, loss=loss, dlogits=grad,
-                     status=status, workspace=opd_ws, stream=stream, **OPD)
-        if ev is not None:
-            ev[7].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -249,7 +261,7 @@ def run_native(args, ws, rank, local):
 
     # ---- device-timed region: inputs resident in HBM ----
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(calls))] for _ in range(K)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if ws > 1:
         torch.distributed.barrier()
@@ -270,20 +282,39 @@ def run_native(args, ws, rank, local):
             per_call[c].append(evs[k][2 * ci].elapsed_time(evs[k][2 * ci + 1]))
     avg_us = {c: 1000.0 * float(np.mean(v)) for c, v in per_call.items()}
 
-    # algorithmic bytes per call (each logit byte read once; OPD also writes dz once)
+    # algorithmic bytes per call (each logit byte read once; the loss also
+    # writes its fp32 gradient once)
     es = 2
     alg = {"verify_T0": rows_t * V * es,
            "verify_T0.6": (rows_t + R) * V * es,
+           "verify_T1+opd": (rows_t + R) * V * es + R * V * 4,
            "verify_T1": (rows_t + R) * V * es,
            "opd": 2 * R * V * es + R * V * 4}
     ms_per_step = elapsed_ms / K
     value = job_positions / (elapsed_ms / K / 1000.0)
-    step_bytes = sum(alg.values())
+    step_bytes = sum(alg[c] for c in calls)
     peak, peak_kind = _peaks()
     dom = max(calls, key=lambda c: avg_us[c])
-    dom_kernel = "opd_loss" if dom == "opd" else "spec_verify"
+    dom_kernel = CALL_API[dom]
     achieved = alg[dom] / (avg_us[dom] * 1e-6) / 1e9
     traffic = _profile_traffic(dom_kernel, f"mix:{dom}")
+
+    # ---- for comparison: the T = 1 verification and the loss as two calls ----
+    Ks = max(3, min(K, 30))
+    sep = {}
+    for name, fn in (("verify_T1", lambda: verify(1.0)),
+                     ("opd", lambda: svw.opd_loss(t, d, cu_draft=cu, has_bonus=True, loss=loss, dlogits=grad,
+                                                  status=status, workspace=opd_ws, stream=stream, **OPD))):
+        fn()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(Ks):
+            fn()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        us = 1000.0 * s0.elapsed_time(s1) / Ks
+        sep[name] = {"avg_us": us, "gbs": alg[name] / (us * 1e-6) / 1e9}
+    sep["sum_us"] = sep["verify_T1"]["avg_us"] + sep["opd"]["avg_us"]
 
     # ---- end to end through the public API with host buffers ----
     Ke = args.e2e_steps if args.e2e_steps is not None else max(3, min(K, 60))
@@ -328,8 +359,7 @@ def run_native(args, ws, rank, local):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": "mix: N=256 ragged L_i~U{2,4,8,16}, V=151936, bf16 log-Zipf "
-                               "logits; verify at T=0,0.6,1 + OPD fwd/bwd (T=1,c=1,lambda=0.1)",
+        "config": {"workload": WORKLOAD,
                    "N": N, "total_draft_rows": R, "V": V, "logits": "bf16",
                    "per_rank_batch": True, "parallelism": f"replicas x{ws}",
                    "l2": "inputs 1.25 GB per step > 129 MB L2; no flush"},
@@ -341,6 +371,7 @@ def run_native(args, ws, rank, local):
         "kernels": {c: {"avg_us": avg_us[c], "gbs": alg[c] / (avg_us[c] * 1e-6) / 1e9,
                         "frac_of_peak": alg[c] / (avg_us[c] * 1e-6) / 1e9 / peak}
                     for c in calls},
+        "separate_calls": sep,
         "step_gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,
         "e2e": e2e,
         "gpu_launches": K * launches_per_step(),
@@ -412,8 +443,7 @@ def run_reference(args, ws, rank):
         "steps": K, "warmup": args.warmup, "ms_per_step": dt * 1000.0,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": "mix: N=256 ragged L_i~U{2,4,8,16}, V=151936, bf16 log-Zipf "
-                               "logits; verify at T=0,0.6,1 + OPD fwd/bwd (T=1,c=1,lambda=0.1)",
+        "config": {"workload": WORKLOAD,
                    "sample": sample},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": sample},

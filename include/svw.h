@@ -2,7 +2,8 @@
  * svw.h -- C ABI of the vocabulary-wide speculative-verification library
  * (serving_vocab_wide_gb300).  Hand-written CUDA for sm_103a (GB300).
  *
- * Two operations, both over full-vocabulary logits:
+ * Two operations, both over full-vocabulary logits (and spec_verify_opd,
+ * both on the same batch in one pass):
  *
  *  spec_verify  batched speculative verification of a ragged batch.  Defined
  *               by "DFlash 阅读笔记：并行起草、目标特征与精确验证" §5.1 (greedy
@@ -153,6 +154,44 @@ svw_status opd_loss(const void *target_logits, const void *draft_logits, svw_dty
                     int32_t target_has_bonus_row, float temperature, float clip_c,
                     float lambda_ce, float grad_scale, float *loss, float *dlogits,
                     int32_t *status, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * spec_verify_opd -- spec_verify and opd_loss (verify layout) on the same
+ * batch in one pass over the logits.  The distillation signal is a byproduct
+ * of verification ("AdaFlash: Taming Variance in Diffusion Speculative
+ * Decoding", "Method Part 1: On-Policy Distillation (OPD) for Diffusion
+ * Drafters", "Algorithm, Step by Step" step 3 and Figure 2: the target's
+ * distribution at every drafted position is already computed by
+ * verification), so both results come from one read of both logit tensors:
+ * the OPD kernel's row softmaxes serve the accept tests, and the bonus rows
+ * are reduced in the same pass.
+ *
+ * Arguments as for spec_verify and opd_loss, plus:
+ *   temperature      verification temperature (0: greedy).
+ *   opd_temperature  > 0, the reverse-KL temperature; must equal temperature
+ *                    when temperature > 0 (the softmaxes are shared), else
+ *                    SVW_ERR_INVALID_ARG.
+ *   loss, dlogits    as for opd_loss with target_has_bonus_row = 1.
+ *   workspace        device, 256-byte aligned, >= svw_verify_opd_workspace_size
+ *                    bytes; contents need not be initialised; not preserved.
+ * accept_len / next_token equal spec_verify's and loss / dlogits equal
+ * opd_loss's on the same inputs, with one difference: a request with a
+ * non-finite row (NaN, +Inf, or only -Inf in any of its target, bonus or
+ * draft rows) is reported bad at every temperature (spec_verify at T = 0
+ * only rejects NaN target rows).  Needs 16-byte aligned bases and a 16-byte
+ * row pitch (V * sizeof(dtype) % 16 == 0) and a row the one-pass kernel can
+ * hold on chip (V = 151936 bf16 fits); otherwise SVW_ERR_UNSUPPORTED.
+ */
+size_t svw_verify_opd_workspace_size(int32_t n_requests, int64_t total_draft_rows, int32_t V,
+                                     svw_dtype dtype);
+
+svw_status spec_verify_opd(const void *target_logits, const void *draft_logits, svw_dtype dtype,
+                           int32_t V, int32_t N, const int32_t *cu_draft, int64_t total_draft_rows,
+                           int32_t max_len, const int32_t *draft_tokens, float temperature,
+                           float opd_temperature, uint64_t seed, float clip_c, float lambda_ce,
+                           float grad_scale, int32_t *accept_len, int32_t *next_token, float *loss,
+                           float *dlogits, int32_t *status, void *workspace, size_t workspace_bytes,
+                           void *stream);
 
 /*
  * spec_verify_noalloc -- spec_verify for callers that cannot allocate device

@@ -54,6 +54,11 @@ def lib():
             L.opd_loss.restype = ctypes.c_int
             L.spec_verify_noalloc.argtypes = [P, P, ctypes.c_int, I32, I32, P, I64, I32, P, F, U64,
                                               P, P, P, P]
+            L.svw_verify_opd_workspace_size.argtypes = [I32, I64, I32, ctypes.c_int]
+            L.svw_verify_opd_workspace_size.restype = SZ
+            L.spec_verify_opd.argtypes = [P, P, ctypes.c_int, I32, I32, P, I64, I32, P, F, F, U64, F, F, F,
+                                          P, P, P, P, P, P, SZ, P]
+            L.spec_verify_opd.restype = ctypes.c_int
             L.spec_verify_noalloc.restype = ctypes.c_int
             L.svw_status_string.argtypes = [ctypes.c_int]
             L.svw_status_string.restype = ctypes.c_char_p
@@ -158,6 +163,49 @@ def spec_verify_noalloc(target, draft, cu_draft, draft_tokens, temperature: floa
                                    _ptr(next_token), _ptr(status), _stream_ptr(stream))
     _check(rc)
     return accept_len, next_token
+
+
+def verify_opd_workspace_size(n_requests: int, total_draft_rows: int, V: int, dtype_code: int) -> int:
+    return int(lib().svw_verify_opd_workspace_size(n_requests, total_draft_rows, V, dtype_code))
+
+
+def spec_verify_opd(target, draft, cu_draft, draft_tokens, temperature: float, seed: int,
+                    opd_temperature: float | None = None, clip_c: float = 1.0, lambda_ce: float = 0.1,
+                    grad_scale: float = 1.0, max_len: int = SVW_MAX_LEN,
+                    total_draft_rows: int | None = None, want_grad: bool = True, accept_len=None,
+                    next_token=None, loss=None, dlogits=None, status=None, workspace=None, stream=None):
+    """Verification and the OPD loss on the same batch in one pass.  Returns
+    (accept_len, next_token, loss, dlogits or None).  opd_temperature
+    defaults to temperature (or 1.0 when greedy)."""
+    import torch
+    _need_cuda(target, draft, cu_draft, draft_tokens)
+    N = cu_draft.numel() - 1
+    V = target.shape[-1]
+    R = int(cu_draft[-1].item()) if total_draft_rows is None else int(total_draft_rows)
+    code = _dtype_code(target)
+    dev = target.device
+    if opd_temperature is None:
+        opd_temperature = temperature if temperature > 0 else 1.0
+    if accept_len is None:
+        accept_len = torch.empty(N, dtype=torch.int32, device=dev)
+    if next_token is None:
+        next_token = torch.empty(N, dtype=torch.int32, device=dev)
+    if loss is None:
+        loss = torch.empty(R, dtype=torch.float32, device=dev)
+    if want_grad and dlogits is None:
+        dlogits = torch.empty((R, V), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(1, verify_opd_workspace_size(N, R, V, code)), dtype=torch.uint8,
+                                device=dev)
+    _need_cuda(accept_len, next_token, loss, dlogits, status, workspace)
+    rc = lib().spec_verify_opd(_ptr(target), _ptr(draft), code, V, N, _ptr(cu_draft), R, max_len,
+                               _ptr(draft_tokens), float(temperature), float(opd_temperature),
+                               int(seed) & (2**64 - 1), float(clip_c), float(lambda_ce),
+                               float(grad_scale), _ptr(accept_len), _ptr(next_token), _ptr(loss),
+                               _ptr(dlogits) if want_grad else None, _ptr(status), _ptr(workspace),
+                               workspace.numel(), _stream_ptr(stream))
+    _check(rc)
+    return accept_len, next_token, loss, (dlogits if want_grad else None)
 
 
 def opd_loss(target, draft, temperature: float = 1.0, clip_c: float = 1.0,

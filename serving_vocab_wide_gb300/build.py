@@ -13,7 +13,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libsvw.so")
-SOURCES = ["api.cu", "verify.cu", "opd.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "verify.cu", "opd.cu", "fused.cu", "noalloc.cu"]
 HEADERS = ["svw_device.cuh", "svw_internal.h"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 

@@ -22,6 +22,15 @@ int esize_of(svw_dtype d) { return d == SVW_BF16 ? 2 : 4; }
 
 }  // namespace
 
+// a new tag for every OPD call (never 0): flags set by an earlier call never
+// match it
+static int32_t next_epoch() {
+  static std::atomic<uint32_t> g_epoch{0x3c5a0000u};
+  uint32_t ep = ++g_epoch;
+  if (ep == 0) ep = ++g_epoch;
+  return static_cast<int32_t>(ep);
+}
+
 extern "C" {
 
 int32_t svw_version(void) { return 100; }
@@ -152,13 +161,127 @@ svw_status opd_loss(const void *target_logits, const void *draft_logits, svw_dty
   a.dlogits = dlogits;
   a.status = status;
   a.flags = static_cast<int32_t *>(workspace);
-  static std::atomic<uint32_t> g_epoch{0x3c5a0000u};
-  uint32_t ep = ++g_epoch;
-  if (ep == 0) ep = ++g_epoch;
-  a.epoch = static_cast<int32_t>(ep);
+  a.epoch = next_epoch();
   a.rowc = workspace ? reinterpret_cast<float4 *>(static_cast<char *>(workspace) + opd_flags_bytes(total_draft_rows))
                      : nullptr;
+  a.nbonus = 0;
+  a.brow = nullptr;
+  a.csr_bad = nullptr;
   const cudaError_t e = svw::launch_opd(a, dtype, bulk, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SVW_OK : SVW_ERR_CUDA;
+}
+
+size_t svw_verify_opd_workspace_size(int32_t n_requests, int64_t total_draft_rows, int32_t V, svw_dtype dtype) {
+  if (n_requests <= 0 || total_draft_rows < 0 || V <= 0 || V > kMaxV) return 0;
+  if (dtype != SVW_F32 && dtype != SVW_BF16) return 0;
+  return svw::fused_layout(n_requests, total_draft_rows, V).total;
+}
+
+svw_status spec_verify_opd(const void *target_logits, const void *draft_logits, svw_dtype dtype, int32_t V,
+                           int32_t N, const int32_t *cu_draft, int64_t total_draft_rows, int32_t max_len,
+                           const int32_t *draft_tokens, float temperature, float opd_temperature, uint64_t seed,
+                           float clip_c, float lambda_ce, float grad_scale, int32_t *accept_len,
+                           int32_t *next_token, float *loss, float *dlogits, int32_t *status, void *workspace,
+                           size_t workspace_bytes, void *stream) {
+  if (dtype != SVW_F32 && dtype != SVW_BF16) return SVW_ERR_UNSUPPORTED;
+  if (V <= 0 || N <= 0 || total_draft_rows <= 0 || max_len < 1) return SVW_ERR_INVALID_ARG;
+  if (max_len > SVW_MAX_LEN || V > kMaxV) return SVW_ERR_UNSUPPORTED;
+  if (!target_logits || !draft_logits || !cu_draft || !draft_tokens || !accept_len || !next_token || !loss ||
+      !workspace)
+    return workspace ? SVW_ERR_INVALID_ARG : SVW_ERR_WORKSPACE;
+  if (!(temperature >= 0.f) || !std::isfinite(temperature)) return SVW_ERR_INVALID_ARG;
+  if (!(opd_temperature > 0.f) || !std::isfinite(opd_temperature)) return SVW_ERR_INVALID_ARG;
+  if (temperature > 0.f && temperature != opd_temperature) return SVW_ERR_INVALID_ARG;  // shared softmaxes
+  if (!(clip_c > 0.f) || !std::isfinite(lambda_ce) || !std::isfinite(grad_scale)) return SVW_ERR_INVALID_ARG;
+  const double kd = 1.4426950408889634 / static_cast<double>(opd_temperature);
+  if (!(kd < 3.0e38)) return SVW_ERR_INVALID_ARG;
+  const int es = esize_of(dtype);
+  if (!aligned(target_logits, 16) || !aligned(draft_logits, 16) || !aligned(cu_draft, 4) ||
+      !aligned(draft_tokens, 4) || !aligned(accept_len, 4) || !aligned(next_token, 4) || !aligned(loss, 4) ||
+      (dlogits && !aligned(dlogits, 16)) || (status && !aligned(status, 4)) || !aligned(workspace, 256))
+    return SVW_ERR_MISALIGNED;
+  // one pass needs the 16-byte-pitched register-resident path
+  if ((static_cast<int64_t>(V) * es) % 16 != 0 || !svw::opd_fast_supported(V, es)) return SVW_ERR_UNSUPPORTED;
+  const svw::FusedLayout lay = svw::fused_layout(N, total_draft_rows, V);
+  if (workspace_bytes < lay.total) return SVW_ERR_WORKSPACE;
+  char *ws = static_cast<char *>(workspace);
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool greedy = (temperature == 0.f);
+
+  svw::OpdArgs o;
+  o.target = target_logits;
+  o.draft = draft_logits;
+  o.V = V;
+  o.N = N;
+  o.cu = cu_draft;
+  o.R = total_draft_rows;
+  o.has_bonus = 1;
+  o.k = static_cast<float>(kd);
+  o.invT = static_cast<float>(1.0 / static_cast<double>(opd_temperature));
+  o.clip_c = clip_c;
+  o.lambda_ce = lambda_ce;
+  o.grad_scale = grad_scale;
+  o.loss = loss;
+  o.dlogits = dlogits;
+  o.status = status;
+  o.flags = reinterpret_cast<int32_t *>(ws + lay.flags_off);
+  o.rowc = reinterpret_cast<float4 *>(ws + lay.rowc_off);
+  o.epoch = next_epoch();
+  o.nbonus = N;
+  o.brow = reinterpret_cast<float4 *>(ws + lay.brow_off);
+  o.csr_bad = reinterpret_cast<int32_t *>(ws + lay.csr_bad_off);
+  int grid = 0;
+  cudaError_t e = svw::launch_opd_fused_fast(o, dtype, &grid, st);
+  if (e != cudaSuccess) return SVW_ERR_CUDA;
+
+  svw::FusedArgs f;
+  f.target = target_logits;
+  f.draft = draft_logits;
+  f.V = V;
+  f.N = N;
+  f.cu = cu_draft;
+  f.total_rows = total_draft_rows;
+  f.max_len = max_len;
+  f.tokens = draft_tokens;
+  f.k = o.k;
+  f.seed = seed;
+  f.rowc = o.rowc;
+  f.brow = o.brow;
+  f.csr_bad = o.csr_bad;
+  f.csr_grid = grid;
+  f.accept_len = accept_len;
+  f.next_token = next_token;
+  f.status = status;
+  f.sinfo = reinterpret_cast<svw::SampleInfo *>(ws + lay.sinfo_off);
+  f.sample_counters = reinterpret_cast<int32_t *>(ws + lay.sample_counters_off);
+  e = svw::launch_fused_finalize(f, dtype, greedy, st);
+  if (e != cudaSuccess) return SVW_ERR_CUDA;
+  if (!greedy) {
+    svw::VerifyArgs v = {};
+    v.target = target_logits;
+    v.draft = draft_logits;
+    v.V = V;
+    v.N = N;
+    v.cu = cu_draft;
+    v.total_rows = total_draft_rows;
+    v.rows_t = total_draft_rows + N;
+    v.max_len = max_len;
+    v.tokens = draft_tokens;
+    v.k = o.k;
+    v.seed = seed;
+    v.accept_len = accept_len;
+    v.next_token = next_token;
+    v.status = status;
+    v.sample_counters = f.sample_counters;
+    v.sinfo = f.sinfo;
+    v.span_tot = reinterpret_cast<float *>(ws + lay.span_off);
+    v.chunk_tot = reinterpret_cast<float *>(ws + lay.chunk_tot_off);
+    v.chunk_last = reinterpret_cast<int32_t *>(ws + lay.chunk_last_off);
+    v.Cs = svw::sampler_chunks(V);
+    e = svw::launch_verify_sample(v, dtype, true, st);
+    if (e != cudaSuccess) return SVW_ERR_CUDA;
+  }
+  e = svw::launch_opd_fix(o, dtype, st);  // rows with a clipped term, exactly
   return e == cudaSuccess ? SVW_OK : SVW_ERR_CUDA;
 }
 

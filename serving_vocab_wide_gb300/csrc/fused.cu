@@ -1,0 +1,141 @@
+// fused.cu -- per-request step of spec_verify_opd (verification and the OPD
+// loss on the same batch in one pass over the logits).
+//
+// The OPD fast kernel has already reduced every draft row together with its
+// target row (log-sum-exp offsets Ct, Cd in log2 units: log2 p = y k - Ct,
+// log2 q = z k - Cd; the target argmax x*) and every bonus row (Ct, argmax).
+// What verification still needs per request is what "Speculative Decoding:
+// The Basic Idea" steps 3-4 ("AdaFlash: Taming Variance in Diffusion
+// Speculative Decoding") and "DFlash 阅读笔记" §5.1-§5.2 define on top of the
+// two softmaxes: the accept test at each drafted token, the leftmost
+// rejection and the row the next token is drawn from.  One warp per request:
+// lane j tests position j.
+#include <cfloat>
+#include <climits>
+#include <cuda_runtime.h>
+
+#include "svw_device.cuh"
+#include "svw_internal.h"
+
+namespace svw {
+
+namespace {
+
+constexpr int kReqPerCta = 8;  // one warp per request
+
+template <int DT, bool GREEDY>
+__global__ void __launch_bounds__(kReqPerCta * 32) fused_finalize(FusedArgs a) {
+  using E = Elem<DT>;
+  const int lane = threadIdx.x & 31;
+  const int32_t i = blockIdx.x * kReqPerCta + (threadIdx.x >> 5);
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (i >= a.N) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    return;
+  }
+  // ---- inputs only: overlaps the end of the fast kernel ----
+  const int64_t c_i = __ldg(a.cu + i), c_e = __ldg(a.cu + i + 1);
+  const bool len_ok = (c_e - c_i >= 1 && c_e - c_i <= a.max_len && c_i >= 0 && c_e <= a.total_rows);
+  const int32_t L = len_ok ? static_cast<int32_t>(c_e - c_i) : 0;
+  const int64_t t0 = c_i + i, d0 = c_i;
+  int32_t x = 0;
+  bool tok_ok = true;
+  float yx = 0.f, zx = 0.f, u = 0.f;
+  if (lane < L) {
+    x = __ldg(a.tokens + d0 + lane);
+    tok_ok = (x >= 0 && static_cast<int64_t>(x) < a.V);
+    if (tok_ok && !GREEDY) {
+      yx = E::load(a.target, (t0 + lane) * a.V + x);
+      zx = E::load(a.draft, (d0 + lane) * a.V + x);
+      u = philox_uniform(a.seed, static_cast<uint32_t>(i), static_cast<uint32_t>(lane), 0u);
+    }
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // row constants and CSR flags are complete
+
+  int csr_bad = 0;
+  for (int b = lane; b < a.csr_grid; b += 32) csr_bad |= __ldcg(a.csr_bad + b);
+  float Ct = 0.f, Cd = 0.f;
+  int32_t xs = -1;
+  bool row_bad = false;
+  if (lane < L) {
+    const float4 rc = __ldcg(a.rowc + d0 + lane);
+    Ct = rc.x;
+    Cd = rc.y;
+    xs = __float_as_int(rc.z);
+    row_bad = !(Ct == Ct);
+  }
+  float4 br = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (len_ok) br = __ldcg(a.brow + i);
+  const bool bonus_bad = len_ok && !(br.x == br.x);
+  const bool bad = !len_ok || __any_sync(0xffffffffu, csr_bad != 0 || !tok_ok || row_bad) || bonus_bad;
+  if (bad) {
+    if (lane == 0) {
+      a.accept_len[i] = -1;
+      a.next_token[i] = -1;
+      if (!GREEDY) a.sinfo[i].valid = 0;
+      a.sample_counters[i] = 0;
+      if (a.status) atomicOr(a.status, SVW_DEV_BAD_INPUT);
+    }
+    return;
+  }
+  bool acc = true;
+  if (lane < L) {
+    if (GREEDY) {
+      acc = (x == xs);
+    } else if (zx == -INFINITY) {
+      acc = true;  // q(x) = 0: accept
+    } else {
+      // log2 p(x) - log2 q(x) from the raw logits and the row offsets
+      const float dl = __fsub_rn(__fmaf_rn(yx, a.k, -Ct), __fmaf_rn(zx, a.k, -Cd));
+      acc = u < ((dl >= 0.f) ? 1.f : ex2(dl));
+    }
+  }
+  const unsigned rej = __ballot_sync(0xffffffffu, !acc);
+  const int32_t js = rej ? (__ffs(rej) - 1) : L;
+  const int src = (js < L) ? js : 0;
+  const int32_t xs_js = __shfl_sync(0xffffffffu, xs, src);
+  const float Ct_js = __shfl_sync(0xffffffffu, Ct, src);
+  const float Cd_js = __shfl_sync(0xffffffffu, Cd, src);
+  if (lane != 0) return;
+  a.accept_len[i] = js;
+  a.sample_counters[i] = 0;
+  if (GREEDY) {
+    a.next_token[i] = (js < L) ? xs_js : __float_as_int(br.y);
+  } else {
+    // the sampler's offsets: log2 p = y k - lt with Mt = 0 (and the draft alike)
+    SampleInfo si;
+    si.js = js;
+    si.resid = (js < L) ? 1 : 0;
+    si.valid = 1;
+    si.w = philox_uniform(a.seed, static_cast<uint32_t>(i), static_cast<uint32_t>(js), 1u);
+    si.Mt = 0.f;
+    si.lt = (js < L) ? Ct_js : br.x;
+    si.Md = 0.f;
+    si.ld = (js < L) ? Cd_js : 0.f;
+    a.sinfo[i] = si;
+  }
+}
+
+template <int DT>
+cudaError_t launch_t(const FusedArgs &a, bool greedy, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>((a.N + kReqPerCta - 1) / kReqPerCta), 1, 1);
+  cfg.blockDim = dim3(kReqPerCta * 32, 1, 1);
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = greedy ? cudaLaunchKernelEx(&cfg, fused_finalize<DT, true>, a)
+                               : cudaLaunchKernelEx(&cfg, fused_finalize<DT, false>, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fused_finalize(const FusedArgs &a, int dtype, bool greedy, cudaStream_t st) {
+  return (dtype == SVW_BF16) ? launch_t<1>(a, greedy, st) : launch_t<0>(a, greedy, st);
+}
+
+}  // namespace svw

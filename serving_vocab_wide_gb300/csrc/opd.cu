@@ -90,6 +90,15 @@ __device__ __forceinline__ int64_t target_row_of(const OpdArgs &a, int64_t r) {
   return r + lo;
 }
 
+// target row of fast-kernel row r: draft row r < R pairs with its target row;
+// r = R + i is request i's bonus row cu[i+1] + i (-1 if the offset is out of range)
+__device__ __forceinline__ int64_t fast_target_row(const OpdArgs &a, int64_t r) {
+  if (r < a.R) return target_row_of(a, r);
+  const int64_t i = r - a.R;
+  const int64_t c1 = __ldg(a.cu + i + 1);
+  return (c1 >= 0 && c1 <= a.R) ? c1 + i : -1;
+}
+
 // max over a 16-byte vector (packed bf16 pairs or 4 floats) folded into m
 template <int DT>
 __device__ __forceinline__ float vec_max(const uint4 &w, float m) {
@@ -639,29 +648,46 @@ __global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) 
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   cluster.sync();  // every inbox barrier exists before any peer sends
-  // one thread: start the bulk copies of draft row r (target row t)
+  const int64_t R_all = a.R + a.nbonus;  // draft rows, then bonus rows (fused verification)
+  if (a.nbonus > 0) {
+    // the fused finalize kernel may be scheduled as this grid drains
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // this CTA's share of the CSR consistency check: cu[0] = 0, cu[N] = R,
+    // non-decreasing (the fused finalize kernel ORs the flags)
+    int bad = 0;
+    for (int64_t j = static_cast<int64_t>(blockIdx.x) * NT + tid; j < a.N; j += static_cast<int64_t>(gridDim.x) * NT)
+      bad |= (__ldg(a.cu + j) > __ldg(a.cu + j + 1)) ? 1 : 0;
+    if (blockIdx.x == 0 && tid == 0)
+      bad |= (__ldg(a.cu) != 0 || static_cast<int64_t>(__ldg(a.cu + a.N)) != a.R) ? 1 : 0;
+    bad = __syncthreads_or(bad);
+    if (tid == 0) a.csr_bad[blockIdx.x] = bad;
+  }
+  // one thread: start the bulk copies of row r (target row t; draft row r
+  // unless r is a bonus row)
   auto issue = [&](int64_t r, int64_t t) {
     sm.tr = t;
     const uint32_t bytes = static_cast<uint32_t>(n) * E::kSize;
     if (sm.abort) return;  // after a timeout the barrier is left alone
     if (t >= 0 && bytes > 0) {
+      const bool pair = r < a.R;
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive_expect_tx(&sm.mbar, 2 * bytes);
+      mbar_arrive_expect_tx(&sm.mbar, (pair ? 2 : 1) * bytes);
       bulk_g2s(tbuf, static_cast<const char *>(a.target) + (t * V + lo) * E::kSize, bytes, &sm.mbar);
-      bulk_g2s(dbuf, static_cast<const char *>(a.draft) + (r * V + lo) * E::kSize, bytes, &sm.mbar);
+      if (pair) bulk_g2s(dbuf, static_cast<const char *>(a.draft) + (r * V + lo) * E::kSize, bytes, &sm.mbar);
     } else {
       mbar_arrive(&sm.mbar);
     }
   };
-  if (tid == 0 && cid < a.R) issue(cid, target_row_of(a, cid));
+  if (tid == 0 && cid < R_all) issue(cid, fast_target_row(a, cid));
   // target rows of this cluster's later rows (verify layout), looked up once
   for (int q = 1 + tid; q < geo.ntab; q += NT) {
     const int64_t r = cid + q * nclusters;
-    tab[q] = (r < a.R) ? static_cast<int32_t>(target_row_of(a, r)) : -1;
+    tab[q] = (r < R_all) ? static_cast<int32_t>(fast_target_row(a, r)) : -1;
   }
   __syncthreads();
 
-  for (int64_t r = cid, it = 0; r < a.R; r += nclusters, ++it) {
+  for (int64_t r = cid, it = 0; r < R_all; r += nclusters, ++it) {
+    const bool pair = r < a.R;  // false: a bonus row (target only, statistics only)
     if (!sm.abort && !mbar_wait_bounded(&sm.mbar, static_cast<uint32_t>(it & 1))) {
       if (a.status) atomicOr(a.status, SVW_DEV_TIMEOUT);
       sm.abort_parity = static_cast<uint32_t>(it & 1);
@@ -670,20 +696,21 @@ __global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) 
     const int64_t sm_tr_row = sm.tr;
     const bool valid = (sm_tr_row >= 0);
     uint4 ty[VPT], tz[VPT];
+    const uint32_t ninf = (DT == 1) ? 0xff80ff80u : 0xff800000u;  // -inf in every lane of the vector
 #pragma unroll
     for (int j = 0; j < VPT; ++j)
       if (j < nj) {
         ty[j] = lds128(tb + (tid + j * NT) * 16);
-        tz[j] = lds128(db + (tid + j * NT) * 16);
+        tz[j] = pair ? lds128(db + (tid + j * NT) * 16) : make_uint4(ninf, ninf, ninf, ninf);
       }
     const bool work = valid && !sm.abort;
     // the buffer is free once every warp holds its vectors: the last warp to
     // get there streams the next row in, nobody waits
     if (last_warp_done<kWarps>(&sm.nread, it)) {
       const int64_t rn = r + nclusters;
-      if (rn < a.R) {
+      if (rn < R_all) {
         const int64_t q = it + 1;
-        const int64_t tn = !a.has_bonus ? rn : (q < geo.ntab ? static_cast<int64_t>(tab[q]) : target_row_of(a, rn));
+        const int64_t tn = !a.has_bonus ? rn : (q < geo.ntab ? static_cast<int64_t>(tab[q]) : fast_target_row(a, rn));
         issue(rn, tn);
       }
     }
@@ -806,6 +833,15 @@ __global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) 
     __syncthreads();  // the merged row is published
     const FastPart Rw = sm.row;
     const bool any_abort = Rw.abort != 0;
+    if (!pair) {
+      // bonus row: its log-sum-exp offset and argmax, nothing else
+      if (rank == 0 && tid == 0) {
+        const bool ok = valid && !any_abort && (Rw.sy > 0.f && Rw.sy <= FLT_MAX) && Rw.idx != INT32_MAX;
+        a.brow[r - a.R] = make_float4(ok ? fmaf(Rw.my, k, lg2(Rw.sy)) : __int_as_float(0x7fffffff),
+                                      __int_as_float(Rw.idx), 0.f, 0.f);
+      }
+      continue;
+    }
     const bool row_ok = valid && !any_abort && (Rw.sy > 0.f && Rw.sy <= FLT_MAX) && (Rw.sz > 0.f && Rw.sz <= FLT_MAX);
     const float lsy = lg2(Rw.sy), lsz = lg2(Rw.sz);
     const float Ct = fmaf(Rw.my, k, lsy);  // log2 p = y k - Ct
@@ -1176,7 +1212,8 @@ enum SmemTail { kNone, kTable, kList };
 
 // launch a persistent grid of clusters (as many as can be co-resident)
 template <typename Kern>
-cudaError_t launch_clusters(Kern kern, int nt, const OpdArgs &a, const OpdPlan &p, SmemTail tail, cudaStream_t st) {
+cudaError_t launch_clusters(Kern kern, int nt, const OpdArgs &a, const OpdPlan &p, SmemTail tail, cudaStream_t st,
+                            int *grid_out = nullptr) {
   const size_t tail_max = (tail == kTable) ? kTab * sizeof(int32_t) : (tail == kList) ? kFixBatch * sizeof(int32_t) : 0;
   const size_t smem_max = p.smem + tail_max;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_max));
@@ -1216,8 +1253,9 @@ cudaError_t launch_clusters(Kern kern, int nt, const OpdArgs &a, const OpdPlan &
     if (maxc <= 0) return cudaErrorInvalidConfiguration;
     if (ncache < 64) cache[ncache++] = Entry{dev, reinterpret_cast<const void *>(kern), p.CL, smem_max, maxc};
   }
+  const int64_t rows = (tail == kTable) ? a.R + a.nbonus : a.R;  // rows the kernel walks
   int64_t nclusters = maxc;
-  if (nclusters > a.R) nclusters = a.R;
+  if (nclusters > rows) nclusters = rows;
   OpdGeo geo;
   geo.SL = p.SL;
   geo.slice_bytes = p.slice_bytes;
@@ -1225,33 +1263,48 @@ cudaError_t launch_clusters(Kern kern, int nt, const OpdArgs &a, const OpdPlan &
   // target rows fit the int32 table when the target has fewer than 2^31 rows
   size_t tail_bytes = 0;
   if (tail == kTable && a.has_bonus && a.R + a.N < (int64_t{1} << 31)) {
-    geo.ntab = static_cast<int32_t>(std::min<int64_t>((a.R + nclusters - 1) / nclusters, kTab));
+    geo.ntab = static_cast<int32_t>(std::min<int64_t>((rows + nclusters - 1) / nclusters, kTab));
     tail_bytes = static_cast<size_t>(geo.ntab) * sizeof(int32_t);
   }
   if (tail == kList) tail_bytes = static_cast<size_t>((kFixBatch + nclusters - 1) / nclusters) * sizeof(int32_t);
   cfg.dynamicSmemBytes = p.smem + tail_bytes;
   cfg.gridDim = dim3(static_cast<unsigned>(nclusters * p.CL), 1, 1);
+  if (grid_out) *grid_out = static_cast<int>(nclusters * p.CL);
   e = cudaLaunchKernelEx(&cfg, kern, a, geo);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-// fast pass + fix-up with NT threads and up to VPT vectors per thread
+// fast pass and / or fix-up with NT threads and up to VPT vectors per thread
 template <int DT, int VPT, int NT>
-cudaError_t launch_fast(const OpdArgs &a, const OpdPlan &p, cudaStream_t st) {
-  const cudaError_t e = launch_clusters(opd_fast_kernel<DT, VPT, NT>, NT, a, p, kTable, st);
-  if (e != cudaSuccess) return e;
+cudaError_t launch_fast(const OpdArgs &a, const OpdPlan &p, cudaStream_t st, bool fast, bool fix, int *grid) {
+  if (fast) {
+    const cudaError_t e = launch_clusters(opd_fast_kernel<DT, VPT, NT>, NT, a, p, kTable, st, grid);
+    if (e != cudaSuccess || !fix) return e;
+  }
   return launch_clusters(opd_fix_kernel<DT, VPT, NT>, NT, a, p, kList, st);
+}
+
+// the fast-path variant for this row geometry; false if the row is too wide
+template <int DT>
+cudaError_t launch_fast_any(const OpdArgs &a, const OpdPlan &p, cudaStream_t st, bool fast, bool fix, int *grid,
+                            bool *ok) {
+  const int nvec = static_cast<int>(static_cast<int64_t>(p.SL) * Elem<DT>::kSize / 16);
+  *ok = true;
+  if (nvec <= 512 * 1) return launch_fast<DT, 1, 512>(a, p, st, fast, fix, grid);
+  if (nvec <= 512 * 2) return launch_fast<DT, 2, 512>(a, p, st, fast, fix, grid);
+  if (nvec <= 512 * 3) return launch_fast<DT, 3, 512>(a, p, st, fast, fix, grid);
+  if (nvec <= 256 * 10) return launch_fast<DT, 10, 256>(a, p, st, fast, fix, grid);
+  *ok = false;
+  return cudaErrorInvalidValue;
 }
 
 template <int DT, bool BULK>
 cudaError_t launch_opd_cfg(const OpdArgs &a, const OpdPlan &p, cudaStream_t st) {
   if (BULK && a.flags != nullptr) {
-    const int nvec = static_cast<int>(static_cast<int64_t>(p.SL) * Elem<DT>::kSize / 16);
-    if (nvec <= 512 * 1) return launch_fast<DT, 1, 512>(a, p, st);
-    if (nvec <= 512 * 2) return launch_fast<DT, 2, 512>(a, p, st);
-    if (nvec <= 512 * 3) return launch_fast<DT, 3, 512>(a, p, st);
-    if (nvec <= 256 * 10) return launch_fast<DT, 10, 256>(a, p, st);
+    bool ok = false;
+    const cudaError_t e = launch_fast_any<DT>(a, p, st, true, true, nullptr, &ok);
+    if (ok) return e;
   }
   return launch_clusters(opd_exact_kernel<DT, BULK>, 512, a, p, kNone, st);
 }
@@ -1259,6 +1312,29 @@ cudaError_t launch_opd_cfg(const OpdArgs &a, const OpdPlan &p, cudaStream_t st) 
 }  // namespace
 
 bool opd_supported(int64_t V, int esize) { return plan_opd(V, esize).smem <= 200 * 1024; }
+
+bool opd_fast_supported(int64_t V, int esize) {
+  const OpdPlan p = plan_opd(V, esize);
+  return p.smem <= 200 * 1024 && static_cast<int64_t>(p.SL) * esize / 16 <= 256 * 10;
+}
+
+cudaError_t launch_opd_fused_fast(const OpdArgs &a, int dtype, int *grid, cudaStream_t st) {
+  const int esize = (dtype == SVW_BF16) ? 2 : 4;
+  const OpdPlan p = plan_opd(a.V, esize);
+  bool ok = false;
+  const cudaError_t e = (dtype == SVW_BF16) ? launch_fast_any<1>(a, p, st, true, false, grid, &ok)
+                                            : launch_fast_any<0>(a, p, st, true, false, grid, &ok);
+  return ok ? e : cudaErrorInvalidValue;
+}
+
+cudaError_t launch_opd_fix(const OpdArgs &a, int dtype, cudaStream_t st) {
+  const int esize = (dtype == SVW_BF16) ? 2 : 4;
+  const OpdPlan p = plan_opd(a.V, esize);
+  bool ok = false;
+  const cudaError_t e = (dtype == SVW_BF16) ? launch_fast_any<1>(a, p, st, false, true, nullptr, &ok)
+                                            : launch_fast_any<0>(a, p, st, false, true, nullptr, &ok);
+  return ok ? e : cudaErrorInvalidValue;
+}
 
 cudaError_t launch_opd(const OpdArgs &a, int dtype, bool bulk, cudaStream_t st) {
   const int esize = (dtype == SVW_BF16) ? 2 : 4;

@@ -74,6 +74,41 @@ struct VerifyArgs {
 
 cudaError_t launch_verify(const VerifyArgs &a, int dtype, bool vec, bool greedy,
                           cudaStream_t stream);
+// the inverse-CDF sampling kernel alone, as a programmatic dependent of the
+// kernel before it (reads a.sinfo, a.sample_counters, the sampler buffers)
+cudaError_t launch_verify_sample(const VerifyArgs &a, int dtype, bool vec, cudaStream_t stream);
+
+// workspace of spec_verify_opd (fused verification + OPD)
+struct FusedLayout {
+  size_t flags_off, rowc_off, brow_off, csr_bad_off, sample_counters_off, sinfo_off, span_off, chunk_tot_off,
+      chunk_last_off, total;
+};
+FusedLayout fused_layout(int32_t N, int64_t total_rows, int64_t V);
+
+// per-request step of spec_verify_opd: validation, accept tests from the
+// fast kernel's row constants, leftmost rejection, next token / sampling row
+struct FusedArgs {
+  const void *target;
+  const void *draft;
+  int64_t V;
+  int32_t N;
+  const int32_t *cu;
+  int64_t total_rows;
+  int32_t max_len;
+  const int32_t *tokens;
+  float k;  // log2(e) / T of the verification (T > 0)
+  uint64_t seed;
+  const float4 *rowc;  // [R] Ct, Cd, x*, target row (NaN: bad row)
+  const float4 *brow;  // [N] bonus rows: Ct (NaN: bad), argmax
+  const int32_t *csr_bad;
+  int32_t csr_grid;
+  int32_t *accept_len;
+  int32_t *next_token;
+  int32_t *status;
+  SampleInfo *sinfo;
+  int32_t *sample_counters;
+};
+cudaError_t launch_fused_finalize(const FusedArgs &a, int dtype, bool greedy, cudaStream_t stream);
 
 struct OpdArgs {
   const void *target;
@@ -95,8 +130,19 @@ struct OpdArgs {
   int32_t *flags;  // [R] == epoch: rows the fix-up kernel must redo
   float4 *rowc;    // [R] row constants of the fast kernel: Ct, Cd, x*, target row (NaN: bad row)
   int32_t epoch;   // this call's tag (never 0)
+  // fused verification (spec_verify_opd): after the R draft rows the fast
+  // kernel also reduces the N bonus target rows (brow[i] = {Ct or NaN, argmax})
+  // and checks the CSR offsets (csr_bad[CTA])
+  int32_t nbonus;
+  float4 *brow;
+  int32_t *csr_bad;
 };
 
 cudaError_t launch_opd(const OpdArgs &a, int dtype, bool bulk, cudaStream_t stream);
+// fast kernel with bonus rows and CSR checks, then the fix-up kernel is left
+// to launch_opd_fix; returns the fast kernel's grid size in *grid
+bool opd_fast_supported(int64_t V, int esize);
+cudaError_t launch_opd_fused_fast(const OpdArgs &a, int dtype, int *grid, cudaStream_t stream);
+cudaError_t launch_opd_fix(const OpdArgs &a, int dtype, cudaStream_t stream);
 
 }  // namespace svw

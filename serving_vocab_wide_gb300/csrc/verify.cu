@@ -1057,6 +1057,43 @@ VerifyLayout verify_layout(int32_t N, int64_t total_rows, int64_t V, int esize) 
   return l;
 }
 
+cudaError_t launch_verify_sample(const VerifyArgs &a, int dtype, bool vec, cudaStream_t st) {
+  const unsigned grid = static_cast<unsigned>(static_cast<int64_t>(a.N) * a.Cs);
+  if (dtype == SVW_BF16)
+    return vec ? launch_dependent(verify_sample<1, true>, grid, kThreads, a, st)
+               : launch_dependent(verify_sample<1, false>, grid, kThreads, a, st);
+  return vec ? launch_dependent(verify_sample<0, true>, grid, kThreads, a, st)
+             : launch_dependent(verify_sample<0, false>, grid, kThreads, a, st);
+}
+
+FusedLayout fused_layout(int32_t N, int64_t total_rows, int64_t V) {
+  const size_t Cs = static_cast<size_t>(sampler_chunks(V));
+  const size_t ns = static_cast<size_t>(N) * Cs;
+  const size_t R = static_cast<size_t>(total_rows);
+  FusedLayout l;
+  size_t off = 0;
+  l.flags_off = off;
+  off += align256(R * 4);
+  l.rowc_off = off;
+  off += align256(R * 16);
+  l.brow_off = off;
+  off += align256(static_cast<size_t>(N) * 16);
+  l.csr_bad_off = off;
+  off += align256(kMaxStatsGrid * sizeof(int32_t));
+  l.sample_counters_off = off;
+  off += align256(static_cast<size_t>(N) * 4);
+  l.sinfo_off = off;
+  off += align256(static_cast<size_t>(N) * sizeof(SampleInfo));
+  l.span_off = off;
+  off += align256(ns * kSpan * sizeof(float));
+  l.chunk_tot_off = off;
+  off += align256(ns * sizeof(float));
+  l.chunk_last_off = off;
+  off += align256(ns * sizeof(int32_t));
+  l.total = off;
+  return l;
+}
+
 cudaError_t launch_verify(const VerifyArgs &a, int dtype, bool vec, bool greedy, cudaStream_t st) {
   if (dtype == SVW_BF16) return vec ? launch_all<1, true>(a, greedy, st) : launch_all<1, false>(a, greedy, st);
   return vec ? launch_all<0, true>(a, greedy, st) : launch_all<0, false>(a, greedy, st);

@@ -111,3 +111,32 @@ def test_opd_argument_validation(lib):
     assert call(V=1 << 22, dt=0) == 2       # row too wide for the on-chip slices
     assert call(ws=p, wsb=16) == 4          # workspace smaller than svw_opd_workspace_size
     assert call(ws=ctypes.c_void_p(p.value + 16), wsb=4096) == 3
+
+
+def test_verify_opd_argument_validation(lib):
+    keep, p = _fake(4096)
+
+    def call(**kw):
+        a = dict(t=p, d=p, dt=1, V=64, N=2, cu=p, R=4, ml=16, tok=p, T=1.0, To=1.0, seed=0, c=1.0,
+                 lam=0.1, gs=1.0, acc=p, nxt=p, loss=p, g=p, st=None, ws=p, wsb=1 << 30)
+        a.update(kw)
+        return lib.spec_verify_opd(a["t"], a["d"], a["dt"], a["V"], a["N"], a["cu"], a["R"], a["ml"],
+                                   a["tok"], a["T"], a["To"], a["seed"], a["c"], a["lam"], a["gs"],
+                                   a["acc"], a["nxt"], a["loss"], a["g"], a["st"], a["ws"], a["wsb"],
+                                   None)
+
+    assert call(dt=5) == 2
+    assert call(N=0) == 1
+    assert call(R=0) == 1
+    assert call(ml=33) == 2
+    assert call(loss=None) == 1
+    assert call(ws=None) == 4
+    assert call(wsb=64) == 4
+    assert call(To=0.0) == 1                # the reverse-KL temperature must be positive
+    assert call(T=0.6, To=1.0) == 1         # sampling softmaxes are shared with the loss
+    assert call(T=-1.0) == 1
+    assert call(c=0.0) == 1
+    assert call(t=ctypes.c_void_p(p.value + 2)) == 3   # bases must be 16-byte aligned
+    assert call(V=63) == 2                  # 126-byte rows are not 16-byte pitched
+    assert lib.svw_verify_opd_workspace_size(4, 64, 151936, 1) > lib.svw_verify_opd_workspace_size(4, 64, 1024, 1) > 0
+    assert lib.svw_verify_opd_workspace_size(0, 64, 1024, 1) == 0
