@@ -60,6 +60,8 @@ def lib():
                                           P, P, P, P, P, P, SZ, P]
             L.spec_verify_opd.restype = ctypes.c_int
             L.spec_verify_noalloc.restype = ctypes.c_int
+            L.svw_time_next_launch.argtypes = [ctypes.c_char_p, P, P]
+            L.svw_time_next_launch.restype = ctypes.c_int
             L.svw_status_string.argtypes = [ctypes.c_int]
             L.svw_status_string.restype = ctypes.c_char_p
             L.svw_version.argtypes = []
@@ -96,6 +98,20 @@ def _need_cuda(*ts):
     for t in ts:
         if t is not None and (not t.is_cuda or not t.is_contiguous()):
             raise SvwError("tensors must be contiguous CUDA tensors")
+
+
+def time_next_launch(kernel: str | None, begin=None, end=None):
+    """Arm the library's one-shot timer: the next launch of `kernel` from this
+    thread records the torch.cuda.Event `begin` before it and `end` after it
+    on the launch stream (measurement only)."""
+    if kernel is None:
+        _check(lib().svw_time_next_launch(None, None, None))
+        return
+    for ev in (begin, end):
+        if not ev.cuda_event:  # torch creates the CUDA event at its first record
+            ev.record()
+    _check(lib().svw_time_next_launch(kernel.encode(), ctypes.c_void_p(begin.cuda_event),
+                                      ctypes.c_void_p(end.cuda_event)))
 
 
 def verify_workspace_size(n_requests: int, total_draft_rows: int, V: int, dtype_code: int) -> int:

@@ -4,6 +4,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <cstring>
 #include <cuda_runtime.h>
 
 #include "svw_internal.h"
@@ -21,6 +22,29 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 int esize_of(svw_dtype d) { return d == SVW_BF16 ? 2 : 4; }
 
 }  // namespace
+
+// one-shot kernel timer, per host thread (svw_time_next_launch)
+namespace {
+struct ArmedTimer {
+  char kernel[64];
+  cudaEvent_t begin;
+  cudaEvent_t end;
+  bool armed;
+};
+thread_local ArmedTimer g_timer = {};
+}  // namespace
+
+namespace svw {
+void *timer_before(const char *kernel, cudaStream_t st) {
+  if (!g_timer.armed || std::strncmp(kernel, g_timer.kernel, sizeof(g_timer.kernel)) != 0) return nullptr;
+  g_timer.armed = false;
+  if (cudaEventRecord(g_timer.begin, st) != cudaSuccess) return nullptr;
+  return reinterpret_cast<void *>(g_timer.end);
+}
+void timer_after(void *end_event, cudaStream_t st) {
+  if (end_event) cudaEventRecord(reinterpret_cast<cudaEvent_t>(end_event), st);
+}
+}  // namespace svw
 
 // a new tag for every OPD call (never 0): flags set by an earlier call never
 // match it
@@ -165,10 +189,23 @@ svw_status opd_loss(const void *target_logits, const void *draft_logits, svw_dty
   a.rowc = workspace ? reinterpret_cast<float4 *>(static_cast<char *>(workspace) + opd_flags_bytes(total_draft_rows))
                      : nullptr;
   a.nbonus = 0;
-  a.brow = nullptr;
+  a.bpart = nullptr;
   a.csr_bad = nullptr;
   const cudaError_t e = svw::launch_opd(a, dtype, bulk, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SVW_OK : SVW_ERR_CUDA;
+}
+
+svw_status svw_time_next_launch(const char *kernel, void *begin_event, void *end_event) {
+  if (!kernel) {
+    g_timer.armed = false;
+    return SVW_OK;
+  }
+  if (!begin_event || !end_event || std::strlen(kernel) >= sizeof(g_timer.kernel)) return SVW_ERR_INVALID_ARG;
+  std::strncpy(g_timer.kernel, kernel, sizeof(g_timer.kernel));
+  g_timer.begin = reinterpret_cast<cudaEvent_t>(begin_event);
+  g_timer.end = reinterpret_cast<cudaEvent_t>(end_event);
+  g_timer.armed = true;
+  return SVW_OK;
 }
 
 size_t svw_verify_opd_workspace_size(int32_t n_requests, int64_t total_draft_rows, int32_t V, svw_dtype dtype) {
@@ -228,7 +265,7 @@ svw_status spec_verify_opd(const void *target_logits, const void *draft_logits, 
   o.rowc = reinterpret_cast<float4 *>(ws + lay.rowc_off);
   o.epoch = next_epoch();
   o.nbonus = N;
-  o.brow = reinterpret_cast<float4 *>(ws + lay.brow_off);
+  o.bpart = reinterpret_cast<float4 *>(ws + lay.bpart_off);
   o.csr_bad = reinterpret_cast<int32_t *>(ws + lay.csr_bad_off);
   int grid = 0;
   cudaError_t e = svw::launch_opd_fused_fast(o, dtype, &grid, st);
@@ -246,7 +283,8 @@ svw_status spec_verify_opd(const void *target_logits, const void *draft_logits, 
   f.k = o.k;
   f.seed = seed;
   f.rowc = o.rowc;
-  f.brow = o.brow;
+  f.bpart = o.bpart;
+  f.bparts = svw::opd_cluster_size(V, es);
   f.csr_bad = o.csr_bad;
   f.csr_grid = grid;
   f.accept_len = accept_len;

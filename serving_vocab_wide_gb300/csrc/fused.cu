@@ -64,9 +64,30 @@ __global__ void __launch_bounds__(kReqPerCta * 32) fused_finalize(FusedArgs a) {
     xs = __float_as_int(rc.z);
     row_bad = !(Ct == Ct);
   }
-  float4 br = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (len_ok) br = __ldcg(a.brow + i);
-  const bool bonus_bad = len_ok && !(br.x == br.x);
+  // the bonus row: merge the fast kernel's per-CTA partials (lane q <- CTA q)
+  float bm = -INFINITY, bs = 0.f;
+  int32_t bidx = INT32_MAX, bflag = 0;
+  if (len_ok && lane < a.bparts) {
+    const float4 q = __ldcg(a.bpart + static_cast<int64_t>(i) * 8 + lane);
+    bm = q.x;
+    bs = q.y;
+    bidx = __float_as_int(q.z);
+    bflag = __float_as_int(q.w);
+  }
+  float bM = bm;
+#pragma unroll
+  for (int o = 4; o > 0; o >>= 1) bM = fmaxf(bM, __shfl_xor_sync(0xffffffffu, bM, o));
+  float bS = (bm == -INFINITY) ? bs * 0.f : bs * ex2((bm - bM) * a.k);
+#pragma unroll
+  for (int o = 4; o > 0; o >>= 1) bS += __shfl_xor_sync(0xffffffffu, bS, o);
+  // the butterfly spans lanes 0..7: every lane takes lane 0's merge
+  bM = __shfl_sync(0xffffffffu, bM, 0);
+  bS = __shfl_sync(0xffffffffu, bS, 0);
+  const int32_t bx = static_cast<int32_t>(
+      __reduce_min_sync(0xffffffffu, static_cast<uint32_t>((lane < 8 && bm == bM) ? bidx : INT32_MAX)));
+  const bool bonus_bad = len_ok && (__any_sync(0xffffffffu, bflag != 0) || !(bS > 0.f && bS <= FLT_MAX) ||
+                                    bx == INT32_MAX);
+  const float4 br = make_float4(fmaf(bM, a.k, lg2(bS)), __int_as_float(bx), 0.f, 0.f);
   const bool bad = !len_ok || __any_sync(0xffffffffu, csr_bad != 0 || !tok_ok || row_bad) || bonus_bad;
   if (bad) {
     if (lane == 0) {
@@ -127,8 +148,10 @@ cudaError_t launch_t(const FusedArgs &a, bool greedy, cudaStream_t st) {
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  void *tm = timer_before("fused_finalize", st);
   const cudaError_t e = greedy ? cudaLaunchKernelEx(&cfg, fused_finalize<DT, true>, a)
                                : cudaLaunchKernelEx(&cfg, fused_finalize<DT, false>, a);
+  timer_after(tm, st);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

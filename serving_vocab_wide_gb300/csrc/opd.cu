@@ -575,6 +575,10 @@ struct FastSmem {
   FastPart inbox[2][kMaxCluster];
   FastPart red[16];  // one partial per warp
   FastPart row;      // merged over the cluster
+  // bonus rows (fused verification) are not exchanged: double-buffered warp
+  // partials, merged by the last warp and stored per CTA
+  FastPart bred[2][16];
+  uint32_t nbred;
   int64_t tr;
   uint32_t nread;  // warps done reading the slice buffer (16 per row)
   int32_t abort;
@@ -594,6 +598,20 @@ __device__ __forceinline__ bool last_warp_done(uint32_t *cnt, int64_t it) {
     asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;" : "=r"(prev) : "r"(smem_u32(cnt)) : "memory");
     last = (prev == static_cast<uint32_t>(kWarps * it + kWarps - 1));
   }
+  return last;
+}
+
+// Warp-uniform variant: true in every lane of the last warp to get here for
+// the it-th time; that warp then sees every other warp's earlier writes.
+template <int kWarps>
+__device__ __forceinline__ bool last_warp_all(uint32_t *cnt, int64_t it) {
+  __syncwarp();
+  uint32_t prev = 0;
+  if ((threadIdx.x & 31) == 0)
+    asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;" : "=r"(prev) : "r"(smem_u32(cnt)) : "memory");
+  prev = __shfl_sync(0xffffffffu, prev, 0);
+  const bool last = (prev == static_cast<uint32_t>(kWarps * it + kWarps - 1));
+  if (last) __threadfence_block();
   return last;
 }
 
@@ -645,6 +663,7 @@ __global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) 
     mbar_init(&sm.xbar[1], 1);
     sm.abort = 0;
     sm.nread = 0;
+    sm.nbred = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   cluster.sync();  // every inbox barrier exists before any peer sends
@@ -686,6 +705,7 @@ __global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) 
   }
   __syncthreads();
 
+  int64_t ib = 0;  // bonus rows done by this CTA
   for (int64_t r = cid, it = 0; r < R_all; r += nclusters, ++it) {
     const bool pair = r < a.R;  // false: a bonus row (target only, statistics only)
     if (!sm.abort && !mbar_wait_bounded(&sm.mbar, static_cast<uint32_t>(it & 1))) {
@@ -713,6 +733,73 @@ __global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) 
         const int64_t tn = !a.has_bonus ? rn : (q < geo.ntab ? static_cast<int64_t>(tab[q]) : fast_target_row(a, rn));
         issue(rn, tn);
       }
+    }
+
+    if (!pair) {
+      // ---- bonus row: maximum, exp-sum and first argmax of this CTA's slice,
+      // stored for the fused finalize kernel (no exchange, no barrier) ----
+      FastPart P = empty_part();
+      P.abort = sm.abort;
+      if (work) {
+        float my;
+        if (DT == 1) {
+          uint32_t py = 0xff80ff80u;
+#pragma unroll
+          for (int j = 0; j < VPT; ++j)
+            if (j < nj) py = bf16x2_max(py, bf16x2_max(bf16x2_max(ty[j].x, ty[j].y), bf16x2_max(ty[j].z, ty[j].w)));
+          const float2 fy = bf16x2_f2(py);
+          my = fmaxf(fy.x, fy.y);
+        } else {
+          my = -INFINITY;
+#pragma unroll
+          for (int j = 0; j < VPT; ++j)
+            if (j < nj) my = vec_max<DT>(ty[j], my);
+        }
+        float My = my;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) My = fmaxf(My, __shfl_xor_sync(0xffffffffu, My, o));
+        int32_t idx = INT32_MAX;
+        if (my == My) {
+#pragma unroll
+          for (int j = 0; j < VPT; ++j)
+            if (j < nj && idx == INT32_MAX) {
+              float y[EPV];
+              E::unpack(ty[j], y);
+#pragma unroll
+              for (int e = EPV - 1; e >= 0; --e)
+                if (y[e] == My) idx = static_cast<int32_t>(lo + (tid + j * NT) * EPV + e);
+            }
+        }
+        const float nmy = (My == -INFINITY) ? 0.f : -My * k;
+        const float2 kk = make_float2(k, k), ny2 = make_float2(nmy, nmy);
+        float2 sy = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < VPT; ++j)
+          if (j < nj) {
+            const Pairs<DT> y(ty[j]);
+#pragma unroll
+            for (int h = 0; h < Pairs<DT>::kN; ++h) {
+              const float2 ay = __ffma2_rn(y.p[h], kk, ny2);
+              sy = __fadd2_rn(sy, make_float2(ex2(ay.x), ex2(ay.y)));
+            }
+          }
+        float s0 = sy.x + sy.y;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+        P.my = My;
+        P.sy = s0;
+        P.idx = static_cast<int32_t>(__reduce_min_sync(0xffffffffu, static_cast<uint32_t>(idx)));
+      }
+      if (lane == 0) sm.bred[ib & 1][warp] = P;
+      if (last_warp_all<kWarps>(&sm.nbred, ib)) {
+        const FastPart Pc = merge_lanes<kWarps>(lane < kWarps ? sm.bred[ib & 1][lane] : empty_part(), k);
+        if (lane == 0) {
+          float4 *dst = reinterpret_cast<float4 *>(a.bpart + ((r - a.R) * kMaxCluster + rank));
+          dst[0] = make_float4(Pc.my, Pc.sy, __int_as_float(Pc.idx), __int_as_float(valid ? Pc.abort : 2));
+        }
+      }
+      ++ib;
+      continue;
     }
 
     // ---------------- pass 1: row statistics ----------------
@@ -833,15 +920,6 @@ __global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) 
     __syncthreads();  // the merged row is published
     const FastPart Rw = sm.row;
     const bool any_abort = Rw.abort != 0;
-    if (!pair) {
-      // bonus row: its log-sum-exp offset and argmax, nothing else
-      if (rank == 0 && tid == 0) {
-        const bool ok = valid && !any_abort && (Rw.sy > 0.f && Rw.sy <= FLT_MAX) && Rw.idx != INT32_MAX;
-        a.brow[r - a.R] = make_float4(ok ? fmaf(Rw.my, k, lg2(Rw.sy)) : __int_as_float(0x7fffffff),
-                                      __int_as_float(Rw.idx), 0.f, 0.f);
-      }
-      continue;
-    }
     const bool row_ok = valid && !any_abort && (Rw.sy > 0.f && Rw.sy <= FLT_MAX) && (Rw.sz > 0.f && Rw.sz <= FLT_MAX);
     const float lsy = lg2(Rw.sy), lsz = lg2(Rw.sz);
     const float Ct = fmaf(Rw.my, k, lsy);  // log2 p = y k - Ct
@@ -1212,8 +1290,8 @@ enum SmemTail { kNone, kTable, kList };
 
 // launch a persistent grid of clusters (as many as can be co-resident)
 template <typename Kern>
-cudaError_t launch_clusters(Kern kern, int nt, const OpdArgs &a, const OpdPlan &p, SmemTail tail, cudaStream_t st,
-                            int *grid_out = nullptr) {
+cudaError_t launch_clusters(const char *name, Kern kern, int nt, const OpdArgs &a, const OpdPlan &p, SmemTail tail,
+                            cudaStream_t st, int *grid_out = nullptr) {
   const size_t tail_max = (tail == kTable) ? kTab * sizeof(int32_t) : (tail == kList) ? kFixBatch * sizeof(int32_t) : 0;
   const size_t smem_max = p.smem + tail_max;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_max));
@@ -1270,7 +1348,9 @@ cudaError_t launch_clusters(Kern kern, int nt, const OpdArgs &a, const OpdPlan &
   cfg.dynamicSmemBytes = p.smem + tail_bytes;
   cfg.gridDim = dim3(static_cast<unsigned>(nclusters * p.CL), 1, 1);
   if (grid_out) *grid_out = static_cast<int>(nclusters * p.CL);
+  void *tm = timer_before(name, st);
   e = cudaLaunchKernelEx(&cfg, kern, a, geo);
+  timer_after(tm, st);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -1279,10 +1359,10 @@ cudaError_t launch_clusters(Kern kern, int nt, const OpdArgs &a, const OpdPlan &
 template <int DT, int VPT, int NT>
 cudaError_t launch_fast(const OpdArgs &a, const OpdPlan &p, cudaStream_t st, bool fast, bool fix, int *grid) {
   if (fast) {
-    const cudaError_t e = launch_clusters(opd_fast_kernel<DT, VPT, NT>, NT, a, p, kTable, st, grid);
+    const cudaError_t e = launch_clusters("opd_fast_kernel", opd_fast_kernel<DT, VPT, NT>, NT, a, p, kTable, st, grid);
     if (e != cudaSuccess || !fix) return e;
   }
-  return launch_clusters(opd_fix_kernel<DT, VPT, NT>, NT, a, p, kList, st);
+  return launch_clusters("opd_fix_kernel", opd_fix_kernel<DT, VPT, NT>, NT, a, p, kList, st);
 }
 
 // the fast-path variant for this row geometry; false if the row is too wide
@@ -1306,12 +1386,14 @@ cudaError_t launch_opd_cfg(const OpdArgs &a, const OpdPlan &p, cudaStream_t st) 
     const cudaError_t e = launch_fast_any<DT>(a, p, st, true, true, nullptr, &ok);
     if (ok) return e;
   }
-  return launch_clusters(opd_exact_kernel<DT, BULK>, 512, a, p, kNone, st);
+  return launch_clusters("opd_exact_kernel", opd_exact_kernel<DT, BULK>, 512, a, p, kNone, st);
 }
 
 }  // namespace
 
 bool opd_supported(int64_t V, int esize) { return plan_opd(V, esize).smem <= 200 * 1024; }
+
+int opd_cluster_size(int64_t V, int esize) { return plan_opd(V, esize).CL; }
 
 bool opd_fast_supported(int64_t V, int esize) {
   const OpdPlan p = plan_opd(V, esize);

@@ -10,6 +10,13 @@
 
 namespace svw {
 
+// Measurement hook behind svw_time_next_launch: a launcher calls
+// timer_before(name) just before launching kernel `name` and timer_after with
+// what it returned just after; both do nothing unless the calling host thread
+// armed a timer for that kernel.
+void *timer_before(const char *kernel, cudaStream_t stream);
+void timer_after(void *end_event, cudaStream_t stream);
+
 // per-(row, chunk) partial result of the streaming row-statistics pass
 struct alignas(16) Partial {
   float m;      // raw maximum of the chunk (argmax value in greedy mode)
@@ -80,7 +87,7 @@ cudaError_t launch_verify_sample(const VerifyArgs &a, int dtype, bool vec, cudaS
 
 // workspace of spec_verify_opd (fused verification + OPD)
 struct FusedLayout {
-  size_t flags_off, rowc_off, brow_off, csr_bad_off, sample_counters_off, sinfo_off, span_off, chunk_tot_off,
+  size_t flags_off, rowc_off, bpart_off, csr_bad_off, sample_counters_off, sinfo_off, span_off, chunk_tot_off,
       chunk_last_off, total;
 };
 FusedLayout fused_layout(int32_t N, int64_t total_rows, int64_t V);
@@ -99,7 +106,8 @@ struct FusedArgs {
   float k;  // log2(e) / T of the verification (T > 0)
   uint64_t seed;
   const float4 *rowc;  // [R] Ct, Cd, x*, target row (NaN: bad row)
-  const float4 *brow;  // [N] bonus rows: Ct (NaN: bad), argmax
+  const float4 *bpart;  // [N * 8] bonus-row partials of the fast kernel's CTAs
+  int32_t bparts;       // partials per bonus row (the fast kernel's cluster size)
   const int32_t *csr_bad;
   int32_t csr_grid;
   int32_t *accept_len;
@@ -131,10 +139,11 @@ struct OpdArgs {
   float4 *rowc;    // [R] row constants of the fast kernel: Ct, Cd, x*, target row (NaN: bad row)
   int32_t epoch;   // this call's tag (never 0)
   // fused verification (spec_verify_opd): after the R draft rows the fast
-  // kernel also reduces the N bonus target rows (brow[i] = {Ct or NaN, argmax})
-  // and checks the CSR offsets (csr_bad[CTA])
+  // kernel also reduces the N bonus target rows, one partial per CTA of the
+  // cluster (bpart[i * 8 + rank] = {max, exp-sum, first argmax, flags}), and
+  // checks the CSR offsets (csr_bad[CTA])
   int32_t nbonus;
-  float4 *brow;
+  float4 *bpart;
   int32_t *csr_bad;
 };
 
@@ -142,6 +151,7 @@ cudaError_t launch_opd(const OpdArgs &a, int dtype, bool bulk, cudaStream_t stre
 // fast kernel with bonus rows and CSR checks, then the fix-up kernel is left
 // to launch_opd_fix; returns the fast kernel's grid size in *grid
 bool opd_fast_supported(int64_t V, int esize);
+int opd_cluster_size(int64_t V, int esize);  // CTAs per row in the OPD kernels
 cudaError_t launch_opd_fused_fast(const OpdArgs &a, int dtype, int *grid, cudaStream_t stream);
 cudaError_t launch_opd_fix(const OpdArgs &a, int dtype, cudaStream_t stream);
 

@@ -965,7 +965,8 @@ int cached_grid(const void *fn, int threads, int smem, cudaError_t &e) {
 
 // launch as a programmatic dependent of the previous kernel in the stream
 template <typename Kern>
-cudaError_t launch_dependent(Kern kern, unsigned grid, unsigned block, const VerifyArgs &a, cudaStream_t st) {
+cudaError_t launch_dependent(const char *name, Kern kern, unsigned grid, unsigned block, const VerifyArgs &a,
+                             cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -976,7 +977,9 @@ cudaError_t launch_dependent(Kern kern, unsigned grid, unsigned block, const Ver
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  void *tm = timer_before(name, st);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
+  timer_after(tm, st);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -1001,12 +1004,14 @@ cudaError_t launch_all_t(const VerifyArgs &args, cudaStream_t st) {
   a.stats_grid = grid;
   // the first kernel is an ordinary launch: it waits for all earlier work in
   // the stream (a previous call's sampler may still read this workspace)
+  void *tm = timer_before("verify_stats", st);
   fn<<<grid, kStatsThreads, smem, st>>>(a, stage_bytes);
+  timer_after(tm, st);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = launch_dependent(verify_finalize<DT, GREEDY>, static_cast<unsigned>(a.N), kFinThreads, a, st);
+  e = launch_dependent("verify_finalize", verify_finalize<DT, GREEDY>, static_cast<unsigned>(a.N), kFinThreads, a, st);
   if (e != cudaSuccess || GREEDY) return e;
-  return launch_dependent(verify_sample<DT, VEC>, static_cast<unsigned>(static_cast<int64_t>(a.N) * a.Cs), kThreads,
+  return launch_dependent("verify_sample", verify_sample<DT, VEC>, static_cast<unsigned>(static_cast<int64_t>(a.N) * a.Cs), kThreads,
                           a, st);
 }
 
@@ -1060,10 +1065,10 @@ VerifyLayout verify_layout(int32_t N, int64_t total_rows, int64_t V, int esize) 
 cudaError_t launch_verify_sample(const VerifyArgs &a, int dtype, bool vec, cudaStream_t st) {
   const unsigned grid = static_cast<unsigned>(static_cast<int64_t>(a.N) * a.Cs);
   if (dtype == SVW_BF16)
-    return vec ? launch_dependent(verify_sample<1, true>, grid, kThreads, a, st)
-               : launch_dependent(verify_sample<1, false>, grid, kThreads, a, st);
-  return vec ? launch_dependent(verify_sample<0, true>, grid, kThreads, a, st)
-             : launch_dependent(verify_sample<0, false>, grid, kThreads, a, st);
+    return vec ? launch_dependent("verify_sample", verify_sample<1, true>, grid, kThreads, a, st)
+               : launch_dependent("verify_sample", verify_sample<1, false>, grid, kThreads, a, st);
+  return vec ? launch_dependent("verify_sample", verify_sample<0, true>, grid, kThreads, a, st)
+             : launch_dependent("verify_sample", verify_sample<0, false>, grid, kThreads, a, st);
 }
 
 FusedLayout fused_layout(int32_t N, int64_t total_rows, int64_t V) {
@@ -1076,8 +1081,8 @@ FusedLayout fused_layout(int32_t N, int64_t total_rows, int64_t V) {
   off += align256(R * 4);
   l.rowc_off = off;
   off += align256(R * 16);
-  l.brow_off = off;
-  off += align256(static_cast<size_t>(N) * 16);
+  l.bpart_off = off;
+  off += align256(static_cast<size_t>(N) * 8 * 16);
   l.csr_bad_off = off;
   off += align256(kMaxStatsGrid * sizeof(int32_t));
   l.sample_counters_off = off;

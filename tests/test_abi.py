@@ -140,3 +140,12 @@ def test_verify_opd_argument_validation(lib):
     assert call(V=63) == 2                  # 126-byte rows are not 16-byte pitched
     assert lib.svw_verify_opd_workspace_size(4, 64, 151936, 1) > lib.svw_verify_opd_workspace_size(4, 64, 1024, 1) > 0
     assert lib.svw_verify_opd_workspace_size(0, 64, 1024, 1) == 0
+
+
+def test_time_next_launch_arming(lib):
+    keep, p = _fake(64)
+    assert lib.svw_time_next_launch(None, None, None) == 0          # disarm
+    assert lib.svw_time_next_launch(b"opd_fast_kernel", None, p) == 1
+    assert lib.svw_time_next_launch(b"x" * 80, p, p) == 1             # name too long
+    assert lib.svw_time_next_launch(b"opd_fast_kernel", p, p) == 0
+    assert lib.svw_time_next_launch(None, None, None) == 0          # and disarm again

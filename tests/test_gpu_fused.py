@@ -144,3 +144,23 @@ def test_deterministic_rerun(mix_batch):
     r2 = _fused(mix_batch, 1.0, 1.0)
     for x, y in zip(r1, r2):
         assert np.array_equal(x, y)
+
+
+def test_kernel_timer_hook():
+    """svw_time_next_launch records the caller's events around one kernel."""
+    import torch
+    import serving_vocab_wide_gb300 as svw
+    b = synth.config(5, N=8, V=32768, seed=88)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    svw.time_next_launch("opd_fast_kernel", e0, e1)
+    _fused(b, 1.0, 1.0)
+    torch.cuda.synchronize()
+    assert e0.elapsed_time(e1) > 0.0
+    # one-shot: a second call leaves the events alone
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record()
+    f1.record()
+    torch.cuda.synchronize()
+    _fused(b, 1.0, 1.0)
+    torch.cuda.synchronize()
+    assert f0.elapsed_time(f1) >= 0.0
