@@ -96,9 +96,9 @@ KERNEL_SOURCES = {
     "opd_fast_kernel": ["opd.cu", "svw_device.cuh", "svw_internal.h"],
 }
 CALL_KERNELS = {
-    "spec_verify": "verify_stats + verify_finalize (+ verify_sample at T > 0)",
+    "spec_verify": "verify_stats + verify_finalize (accept tests and, at T > 0, the inverse-CDF draw)",
     "opd_loss": "opd_fast_kernel + opd_fix_kernel",
-    "spec_verify_opd": "opd_fast_kernel (draft rows + bonus rows) + fused_finalize + verify_sample + opd_fix_kernel",
+    "spec_verify_opd": "opd_fast_kernel (draft rows + bonus rows) + fused_finalize (accept tests, draw) + opd_fix_kernel",
 }
 CALLS = ["verify_T0", "verify_T0.6", "verify_T1+opd"]
 WORKLOAD = ("mix: N=256 ragged L_i~U{2,4,8,16}, V=151936, bf16 log-Zipf logits; verify at T=0 and 0.6, "
@@ -190,9 +190,9 @@ class ClockSampler:
 # native arm
 # ---------------------------------------------------------------------------
 def launches_per_step():
-    """Kernels one step launches: spec_verify = stats + finalize (+ sample at
-    T > 0), twice; spec_verify_opd = fast pass + finalize + sample + fix-up."""
-    return 2 + 3 + 4
+    """Kernels one step launches: spec_verify = stats + finalize, twice;
+    spec_verify_opd = fast pass + finalize + fix-up."""
+    return 2 + 2 + 3
 
 
 def run_native(args, ws, rank, local):

@@ -227,8 +227,7 @@ svw_status spec_verify_noalloc(const void *target_logits, const void *draft_logi
  * svw_time_next_launch -- measurement hook, not part of the method.  Arms a
  * one-shot timer on the calling host thread: the next launch of the named
  * kernel made from this thread ("verify_stats", "verify_finalize",
- * "verify_sample", "opd_fast_kernel", "opd_fix_kernel", "opd_exact_kernel",
- * "fused_finalize") records begin_event just before it and end_event just
+ * "opd_fast_kernel", "opd_fix_kernel", "opd_exact_kernel", "fused_finalize") records begin_event just before it and end_event just
  * after it on the launch stream (cudaEvent_t handles passed as void*, owned
  * by the caller).  kernel = NULL disarms.  The library records nothing
  * unless armed.  Lets a benchmark time one kernel of a multi-kernel call with

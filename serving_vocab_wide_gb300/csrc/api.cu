@@ -121,14 +121,8 @@ svw_status spec_verify(const void *target_logits, const void *draft_logits, svw_
   a.status = status;
   char *ws = static_cast<char *>(workspace);
   a.part = reinterpret_cast<svw::Partial *>(ws + lay.part_off);
-  a.sample_counters = reinterpret_cast<int32_t *>(ws + lay.sample_counters_off);
-  a.sinfo = reinterpret_cast<svw::SampleInfo *>(ws + lay.sinfo_off);
-  a.span_tot = reinterpret_cast<float *>(ws + lay.span_off);
-  a.chunk_tot = reinterpret_cast<float *>(ws + lay.chunk_tot_off);
-  a.chunk_last = reinterpret_cast<int32_t *>(ws + lay.chunk_last_off);
   a.csr_bad = reinterpret_cast<int32_t *>(ws + lay.csr_bad_off);
   a.stats_grid = 0;  // set by the launcher
-  a.Cs = svw::sampler_chunks(V);
   a.C = plan.C;
   a.chunk_len = plan.chunk_len;
   const int64_t rows = greedy ? (total_draft_rows + N) : (2 * total_draft_rows + N);
@@ -290,35 +284,8 @@ svw_status spec_verify_opd(const void *target_logits, const void *draft_logits, 
   f.accept_len = accept_len;
   f.next_token = next_token;
   f.status = status;
-  f.sinfo = reinterpret_cast<svw::SampleInfo *>(ws + lay.sinfo_off);
-  f.sample_counters = reinterpret_cast<int32_t *>(ws + lay.sample_counters_off);
   e = svw::launch_fused_finalize(f, dtype, greedy, st);
   if (e != cudaSuccess) return SVW_ERR_CUDA;
-  if (!greedy) {
-    svw::VerifyArgs v = {};
-    v.target = target_logits;
-    v.draft = draft_logits;
-    v.V = V;
-    v.N = N;
-    v.cu = cu_draft;
-    v.total_rows = total_draft_rows;
-    v.rows_t = total_draft_rows + N;
-    v.max_len = max_len;
-    v.tokens = draft_tokens;
-    v.k = o.k;
-    v.seed = seed;
-    v.accept_len = accept_len;
-    v.next_token = next_token;
-    v.status = status;
-    v.sample_counters = f.sample_counters;
-    v.sinfo = f.sinfo;
-    v.span_tot = reinterpret_cast<float *>(ws + lay.span_off);
-    v.chunk_tot = reinterpret_cast<float *>(ws + lay.chunk_tot_off);
-    v.chunk_last = reinterpret_cast<int32_t *>(ws + lay.chunk_last_off);
-    v.Cs = svw::sampler_chunks(V);
-    e = svw::launch_verify_sample(v, dtype, true, st);
-    if (e != cudaSuccess) return SVW_ERR_CUDA;
-  }
   e = svw::launch_opd_fix(o, dtype, st);  // rows with a clipped term, exactly
   return e == cudaSuccess ? SVW_OK : SVW_ERR_CUDA;
 }

@@ -8,133 +8,145 @@
 // The Basic Idea" steps 3-4 ("AdaFlash: Taming Variance in Diffusion
 // Speculative Decoding") and "DFlash 阅读笔记" §5.1-§5.2 define on top of the
 // two softmaxes: the accept test at each drafted token, the leftmost
-// rejection and the row the next token is drawn from.  One warp per request:
-// lane j tests position j.
+// rejection and the next token.  One CTA per request: warp 0 (lane j tests
+// position j) decides, then at T > 0 the whole CTA draws the next token by
+// inverse CDF (svw_sample.cuh).
 #include <cfloat>
 #include <climits>
 #include <cuda_runtime.h>
 
 #include "svw_device.cuh"
 #include "svw_internal.h"
+#include "svw_sample.cuh"
 
 namespace svw {
 
 namespace {
 
-constexpr int kReqPerCta = 8;  // one warp per request
+constexpr int kFThreads = 512;  // one CTA per request, two per SM
 
 template <int DT, bool GREEDY>
-__global__ void __launch_bounds__(kReqPerCta * 32) fused_finalize(FusedArgs a) {
+__global__ void __launch_bounds__(kFThreads) fused_finalize(FusedArgs a) {
   using E = Elem<DT>;
+  __shared__ int32_t s_js;
+  __shared__ float s_nT, s_nD;
+  __shared__ SampleSmem<kFThreads> ssm;
   const int lane = threadIdx.x & 31;
-  const int32_t i = blockIdx.x * kReqPerCta + (threadIdx.x >> 5);
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (i >= a.N) {
+  const int32_t i = blockIdx.x;
+  if (threadIdx.x >= 32) {
+    // warps 1.. only take part in the draw
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    return;
-  }
-  // ---- inputs only: overlaps the end of the fast kernel ----
-  const int64_t c_i = __ldg(a.cu + i), c_e = __ldg(a.cu + i + 1);
-  const bool len_ok = (c_e - c_i >= 1 && c_e - c_i <= a.max_len && c_i >= 0 && c_e <= a.total_rows);
-  const int32_t L = len_ok ? static_cast<int32_t>(c_e - c_i) : 0;
-  const int64_t t0 = c_i + i, d0 = c_i;
-  int32_t x = 0;
-  bool tok_ok = true;
-  float yx = 0.f, zx = 0.f, u = 0.f;
-  if (lane < L) {
-    x = __ldg(a.tokens + d0 + lane);
-    tok_ok = (x >= 0 && static_cast<int64_t>(x) < a.V);
-    if (tok_ok && !GREEDY) {
-      yx = E::load(a.target, (t0 + lane) * a.V + x);
-      zx = E::load(a.draft, (d0 + lane) * a.V + x);
-      u = philox_uniform(a.seed, static_cast<uint32_t>(i), static_cast<uint32_t>(lane), 0u);
-    }
-  }
-  asm volatile("griddepcontrol.wait;" ::: "memory");  // row constants and CSR flags are complete
-
-  int csr_bad = 0;
-  for (int b = lane; b < a.csr_grid; b += 32) csr_bad |= __ldcg(a.csr_bad + b);
-  float Ct = 0.f, Cd = 0.f;
-  int32_t xs = -1;
-  bool row_bad = false;
-  if (lane < L) {
-    const float4 rc = __ldcg(a.rowc + d0 + lane);
-    Ct = rc.x;
-    Cd = rc.y;
-    xs = __float_as_int(rc.z);
-    row_bad = !(Ct == Ct);
-  }
-  // the bonus row: merge the fast kernel's per-CTA partials (lane q <- CTA q)
-  float bm = -INFINITY, bs = 0.f;
-  int32_t bidx = INT32_MAX, bflag = 0;
-  if (len_ok && lane < a.bparts) {
-    const float4 q = __ldcg(a.bpart + static_cast<int64_t>(i) * 8 + lane);
-    bm = q.x;
-    bs = q.y;
-    bidx = __float_as_int(q.z);
-    bflag = __float_as_int(q.w);
-  }
-  float bM = bm;
-#pragma unroll
-  for (int o = 4; o > 0; o >>= 1) bM = fmaxf(bM, __shfl_xor_sync(0xffffffffu, bM, o));
-  float bS = (bm == -INFINITY) ? bs * 0.f : bs * ex2((bm - bM) * a.k);
-#pragma unroll
-  for (int o = 4; o > 0; o >>= 1) bS += __shfl_xor_sync(0xffffffffu, bS, o);
-  // the butterfly spans lanes 0..7: every lane takes lane 0's merge
-  bM = __shfl_sync(0xffffffffu, bM, 0);
-  bS = __shfl_sync(0xffffffffu, bS, 0);
-  const int32_t bx = static_cast<int32_t>(
-      __reduce_min_sync(0xffffffffu, static_cast<uint32_t>((lane < 8 && bm == bM) ? bidx : INT32_MAX)));
-  const bool bonus_bad = len_ok && (__any_sync(0xffffffffu, bflag != 0) || !(bS > 0.f && bS <= FLT_MAX) ||
-                                    bx == INT32_MAX);
-  const float4 br = make_float4(fmaf(bM, a.k, lg2(bS)), __int_as_float(bx), 0.f, 0.f);
-  const bool bad = !len_ok || __any_sync(0xffffffffu, csr_bad != 0 || !tok_ok || row_bad) || bonus_bad;
-  if (bad) {
-    if (lane == 0) {
-      a.accept_len[i] = -1;
-      a.next_token[i] = -1;
-      if (!GREEDY) a.sinfo[i].valid = 0;
-      a.sample_counters[i] = 0;
-      if (a.status) atomicOr(a.status, SVW_DEV_BAD_INPUT);
-    }
-    return;
-  }
-  bool acc = true;
-  if (lane < L) {
-    if (GREEDY) {
-      acc = (x == xs);
-    } else if (zx == -INFINITY) {
-      acc = true;  // q(x) = 0: accept
-    } else {
-      // log2 p(x) - log2 q(x) from the raw logits and the row offsets
-      const float dl = __fsub_rn(__fmaf_rn(yx, a.k, -Ct), __fmaf_rn(zx, a.k, -Cd));
-      acc = u < ((dl >= 0.f) ? 1.f : ex2(dl));
-    }
-  }
-  const unsigned rej = __ballot_sync(0xffffffffu, !acc);
-  const int32_t js = rej ? (__ffs(rej) - 1) : L;
-  const int src = (js < L) ? js : 0;
-  const int32_t xs_js = __shfl_sync(0xffffffffu, xs, src);
-  const float Ct_js = __shfl_sync(0xffffffffu, Ct, src);
-  const float Cd_js = __shfl_sync(0xffffffffu, Cd, src);
-  if (lane != 0) return;
-  a.accept_len[i] = js;
-  a.sample_counters[i] = 0;
-  if (GREEDY) {
-    a.next_token[i] = (js < L) ? xs_js : __float_as_int(br.y);
+    if (GREEDY) return;
   } else {
-    // the sampler's offsets: log2 p = y k - lt with Mt = 0 (and the draft alike)
-    SampleInfo si;
-    si.js = js;
-    si.resid = (js < L) ? 1 : 0;
-    si.valid = 1;
-    si.w = philox_uniform(a.seed, static_cast<uint32_t>(i), static_cast<uint32_t>(js), 1u);
-    si.Mt = 0.f;
-    si.lt = (js < L) ? Ct_js : br.x;
-    si.Md = 0.f;
-    si.ld = (js < L) ? Cd_js : 0.f;
-    a.sinfo[i] = si;
+    // ---- inputs only: overlaps the end of the fast kernel ----
+    const int64_t c_i = __ldg(a.cu + i), c_e = __ldg(a.cu + i + 1);
+    const bool len_ok = (c_e - c_i >= 1 && c_e - c_i <= a.max_len && c_i >= 0 && c_e <= a.total_rows);
+    const int32_t L = len_ok ? static_cast<int32_t>(c_e - c_i) : 0;
+    const int64_t t0 = c_i + i, d0 = c_i;
+    int32_t x = 0;
+    bool tok_ok = true;
+    float yx = 0.f, zx = 0.f, u = 0.f;
+    if (lane < L) {
+      x = __ldg(a.tokens + d0 + lane);
+      tok_ok = (x >= 0 && static_cast<int64_t>(x) < a.V);
+      if (tok_ok && !GREEDY) {
+        yx = E::load(a.target, (t0 + lane) * a.V + x);
+        zx = E::load(a.draft, (d0 + lane) * a.V + x);
+        u = philox_uniform(a.seed, static_cast<uint32_t>(i), static_cast<uint32_t>(lane), 0u);
+      }
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // row constants and CSR flags are complete
+
+    int csr_bad = 0;
+    for (int b = lane; b < a.csr_grid; b += 32) csr_bad |= __ldcg(a.csr_bad + b);
+    float Ct = 0.f, Cd = 0.f;
+    int32_t xs = -1;
+    bool row_bad = false;
+    if (lane < L) {
+      const float4 rc = __ldcg(a.rowc + d0 + lane);
+      Ct = rc.x;
+      Cd = rc.y;
+      xs = __float_as_int(rc.z);
+      row_bad = !(Ct == Ct);
+    }
+    // the bonus row: merge the fast kernel's per-CTA partials (lane q <- CTA q)
+    float bm = -INFINITY, bs = 0.f;
+    int32_t bidx = INT32_MAX, bflag = 0;
+    if (len_ok && lane < a.bparts) {
+      const float4 q = __ldcg(a.bpart + static_cast<int64_t>(i) * 8 + lane);
+      bm = q.x;
+      bs = q.y;
+      bidx = __float_as_int(q.z);
+      bflag = __float_as_int(q.w);
+    }
+    float bM = bm;
+  #pragma unroll
+    for (int o = 4; o > 0; o >>= 1) bM = fmaxf(bM, __shfl_xor_sync(0xffffffffu, bM, o));
+    float bS = (bm == -INFINITY) ? bs * 0.f : bs * ex2((bm - bM) * a.k);
+  #pragma unroll
+    for (int o = 4; o > 0; o >>= 1) bS += __shfl_xor_sync(0xffffffffu, bS, o);
+    // the butterfly spans lanes 0..7: every lane takes lane 0's merge
+    bM = __shfl_sync(0xffffffffu, bM, 0);
+    bS = __shfl_sync(0xffffffffu, bS, 0);
+    const int32_t bx = static_cast<int32_t>(
+        __reduce_min_sync(0xffffffffu, static_cast<uint32_t>((lane < 8 && bm == bM) ? bidx : INT32_MAX)));
+    const bool bonus_bad = len_ok && (__any_sync(0xffffffffu, bflag != 0) || !(bS > 0.f && bS <= FLT_MAX) ||
+                                      bx == INT32_MAX);
+    const float4 br = make_float4(fmaf(bM, a.k, lg2(bS)), __int_as_float(bx), 0.f, 0.f);
+    const bool bad = !len_ok || __any_sync(0xffffffffu, csr_bad != 0 || !tok_ok || row_bad) || bonus_bad;
+    if (bad) {
+      if (lane == 0) {
+        a.accept_len[i] = -1;
+        a.next_token[i] = -1;
+        s_js = -1;
+        if (a.status) atomicOr(a.status, SVW_DEV_BAD_INPUT);
+      }
+    } else {
+      bool acc = true;
+      if (lane < L) {
+        if (GREEDY) {
+          acc = (x == xs);
+        } else if (zx == -INFINITY) {
+          acc = true;  // q(x) = 0: accept
+        } else {
+          // log2 p(x) - log2 q(x) from the raw logits and the row offsets
+          const float dl = __fsub_rn(__fmaf_rn(yx, a.k, -Ct), __fmaf_rn(zx, a.k, -Cd));
+          acc = u < ((dl >= 0.f) ? 1.f : ex2(dl));
+        }
+      }
+      const unsigned rej = __ballot_sync(0xffffffffu, !acc);
+      const int32_t js = rej ? (__ffs(rej) - 1) : L;
+      const int src = (js < L) ? js : 0;
+      const int32_t xs_js = __shfl_sync(0xffffffffu, xs, src);
+      const float Ct_js = __shfl_sync(0xffffffffu, Ct, src);
+      const float Cd_js = __shfl_sync(0xffffffffu, Cd, src);
+      if (lane == 0) {
+        a.accept_len[i] = js;
+        if (GREEDY) a.next_token[i] = (js < L) ? xs_js : __float_as_int(br.y);
+        s_js = js;
+        // the draw's offsets: log2 p = y k - Ct, log2 q = z k - Cd
+        s_nT = -((js < L) ? Ct_js : br.x);
+        s_nD = -Cd_js;
+      }
+    }
   }
+  if (GREEDY) return;
+  __syncthreads();
+  const int32_t js = s_js;
+  if (js < 0) return;
+  // ---- the next token by inverse CDF: [p - q]_+ at row js, or p at the bonus row ----
+  const int64_t c_i = __ldg(a.cu + i);
+  const int32_t L = __ldg(a.cu + i + 1) - static_cast<int32_t>(c_i);
+  RowConst rc;
+  rc.k = a.k;
+  rc.resid = js < L;
+  rc.nT = s_nT;
+  rc.nD = s_nD;
+  const char *trow = static_cast<const char *>(a.target) + (c_i + i + js) * a.V * E::kSize;
+  const char *drow = rc.resid ? static_cast<const char *>(a.draft) + (c_i + js) * a.V * E::kSize : nullptr;
+  const float w = philox_uniform(a.seed, static_cast<uint32_t>(i), static_cast<uint32_t>(js), 1u);
+  const int32_t tok = cta_sample<DT, true, kFThreads>(trow, drow, a.V, rc, w, ssm);
+  if (threadIdx.x == 0) a.next_token[i] = tok;
 }
 
 template <int DT>
@@ -143,8 +155,8 @@ cudaError_t launch_t(const FusedArgs &a, bool greedy, cudaStream_t st) {
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.gridDim = dim3(static_cast<unsigned>((a.N + kReqPerCta - 1) / kReqPerCta), 1, 1);
-  cfg.blockDim = dim3(kReqPerCta * 32, 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(a.N), 1, 1);
+  cfg.blockDim = dim3(kFThreads, 1, 1);
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;

@@ -32,22 +32,10 @@ struct ChunkPlan {
 };
 ChunkPlan plan_chunks(int64_t V, int esize);
 
-// what the stats kernel records for the sampling kernel (one per request)
-struct alignas(16) SampleInfo {
-  int32_t js;     // sampled row: first rejected position, or L (bonus)
-  int32_t resid;  // 1: residual [p - q]_+ at row js; 0: p of the bonus row
-  int32_t valid;  // request verified (0: bad request, nothing to sample)
-  float w;        // sampling uniform U(seed, i, js, 1)
-  float Mt, lt;   // target row max and log2 sum 2^((y - Mt) log2e/T)
-  float Md, ld;   // draft row (resid only)
-};
-
 struct VerifyLayout {
-  size_t part_off, sample_counters_off, sinfo_off, span_off, chunk_tot_off, chunk_last_off, csr_bad_off,
-      total;
+  size_t part_off, csr_bad_off, total;
 };
 VerifyLayout verify_layout(int32_t N, int64_t total_rows, int64_t V, int esize);
-int32_t sampler_chunks(int64_t V);  // 16384-entry chunks of the inverse-CDF sampler
 constexpr int kMaxStatsGrid = 1024;  // CTAs of the stats kernel (one CSR check flag each)
 
 struct VerifyArgs {
@@ -66,14 +54,8 @@ struct VerifyArgs {
   int32_t *next_token;
   int32_t *status;
   Partial *part;                     // [(rows_t + total_rows) * C * 16] per-warp chunk partials
-  int32_t *sample_counters;          // [N] sampling arrivals per request
-  SampleInfo *sinfo;                 // [N]
-  float *span_tot;                   // [N * Cs * 64] sampler warp totals (round, warp)
-  float *chunk_tot;                  // [N * Cs] sampler chunk totals
-  int32_t *chunk_last;               // [N * Cs] last group with positive weight per sampler chunk
   int32_t *csr_bad;                  // [stats grid] CSR offsets inconsistent (per stats CTA)
   int32_t stats_grid;                // CTAs of the stats kernel
-  int32_t Cs;                        // sampler chunks per row
   int32_t C;
   int32_t chunk_len;
   int64_t total_items;
@@ -81,14 +63,9 @@ struct VerifyArgs {
 
 cudaError_t launch_verify(const VerifyArgs &a, int dtype, bool vec, bool greedy,
                           cudaStream_t stream);
-// the inverse-CDF sampling kernel alone, as a programmatic dependent of the
-// kernel before it (reads a.sinfo, a.sample_counters, the sampler buffers)
-cudaError_t launch_verify_sample(const VerifyArgs &a, int dtype, bool vec, cudaStream_t stream);
-
 // workspace of spec_verify_opd (fused verification + OPD)
 struct FusedLayout {
-  size_t flags_off, rowc_off, bpart_off, csr_bad_off, sample_counters_off, sinfo_off, span_off, chunk_tot_off,
-      chunk_last_off, total;
+  size_t flags_off, rowc_off, bpart_off, csr_bad_off, total;
 };
 FusedLayout fused_layout(int32_t N, int64_t total_rows, int64_t V);
 
@@ -113,8 +90,6 @@ struct FusedArgs {
   int32_t *accept_len;
   int32_t *next_token;
   int32_t *status;
-  SampleInfo *sinfo;
-  int32_t *sample_counters;
 };
 cudaError_t launch_fused_finalize(const FusedArgs &a, int dtype, bool greedy, cudaStream_t stream);
 

@@ -1,0 +1,266 @@
+// svw_sample.cuh -- inverse-CDF draw of the next token by one CTA.
+//
+// "DFlash 阅读笔记：并行起草、目标特征与精确验证" §5.2 eq. (7) and Algorithm 1
+// (and "AdaFlash: Taming Variance in Diffusion Speculative Decoding",
+// "Speculative Decoding: The Basic Idea" step 4): after the first rejection
+// the next token is drawn from the normalised residual [p - q]_+ of that row,
+// or from p of the bonus row when every drafted token passed.  The draw is an
+// inverse CDF in vocabulary order: the smallest v with C_v > w Z, where C is
+// the prefix sum of the weights, Z their total and w the request's uniform.
+//
+// Prefix definition (fp32, reproducible, each level a fixed order of adds):
+//   group  8 consecutive entries           sequential partial sums, total a_g
+//   warp   32 consecutive groups           inclusive shuffle scan E_l, total W
+//   round  the NT / 32 warps of the CTA    sequential prefix Q_w, total R_r
+//   row    rounds                          sequential prefix P_r, total Z
+//   C_v = fl(P_r + fl(Q_w + fl(E_{l-1} + part_k)))
+// A round is one group per thread, so the row streams through the CTA with
+// coalesced 16-byte loads; only the crossing warp's 32 groups are read a
+// second time.  Rounding can leave the lane or entry level without a crossing
+// (or w Z can round up to Z): then the last entry with positive weight in the
+// group (or row) is taken -- such draws are within float rounding of a CDF
+// boundary.  A rejected row whose residual rounds to zero mass is drawn from p.
+#pragma once
+
+#include <cfloat>
+#include <climits>
+#include <cuda_runtime.h>
+
+#include "svw_device.cuh"
+
+namespace svw {
+
+// log2 p = y k + nT, log2 q = z k + nD (one rounding each)
+struct RowConst {
+  float k, nT, nD;
+  bool resid;
+};
+
+// [p - q]_+ (resid) or p
+__device__ __forceinline__ float sample_weight(float y, float z, const RowConst &c) {
+  const float lp = __fmaf_rn(y, c.k, c.nT);
+  if (!c.resid) return ex2(lp);
+  const float lq = __fmaf_rn(z, c.k, c.nD);
+  if (!(lq < lp)) return 0.f;
+  return fmaxf(__fsub_rn(ex2(lp), ex2(lq)), 0.f);
+}
+
+// raw logits of group g (entries 8g .. 8g+7, -inf at v >= V)
+template <int DT, bool VEC>
+__device__ __forceinline__ void sample_load_group(const char *row, int64_t g, int64_t V, float (&x)[8]) {
+  using E = Elem<DT>;
+  constexpr int EPV = E::kPerVec;
+  const int64_t v0 = g * 8;
+  if (VEC) {
+#pragma unroll
+    for (int h = 0; h < 8 / EPV; ++h) {
+      const int64_t vv = v0 + h * EPV;
+      if (vv < V) {
+        E::unpack(ld_vec(row + vv * E::kSize), x + h * EPV);
+      } else {
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) x[h * EPV + e] = -INFINITY;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = (v0 + e < V) ? E::load(row, v0 + e) : -INFINITY;
+  }
+}
+
+// the 8 weights of group g and their sequential sum a_g (0 beyond the row)
+template <int DT, bool VEC>
+__device__ __forceinline__ float sample_group(const char *trow, const char *drow, int64_t g, int64_t NG,
+                                              int64_t V, const RowConst &c, float (&w)[8]) {
+  float a = 0.f;
+  if (g >= NG) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) w[e] = 0.f;
+    return a;
+  }
+  float y[8], z[8];
+  sample_load_group<DT, VEC>(trow, g, V, y);
+  if (c.resid) sample_load_group<DT, VEC>(drow, g, V, z);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    w[e] = sample_weight(y[e], c.resid ? z[e] : 0.f, c);
+    a = __fadd_rn(a, w[e]);
+  }
+  return a;
+}
+
+// inclusive prefix over the warp's lanes (fixed shuffle tree)
+__device__ __forceinline__ float warp_scan_incl(float x) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x = __fadd_rn(x, y);
+  }
+  return x;
+}
+
+// shared memory of cta_sample
+template <int NT>
+struct SampleSmem {
+  static constexpr int kW = NT / 32;
+  static constexpr int kMaxRounds = ((1 << 20) / 8 + NT - 1) / NT;  // V <= 2^20
+  float W[kMaxRounds * kW];  // warp totals (round-major)
+  float R[kMaxRounds];       // round totals
+  int32_t lastg;             // last group with positive weight
+  int32_t rs, ws, result, degenerate;
+  float t, Pr, Qw;
+};
+
+// The next token drawn from row trow (and drow when rc.resid) by the whole CTA
+// of NT threads; every thread returns it.  wu: the request's uniform in [0, 1).
+template <int DT, bool VEC, int NT>
+__device__ __noinline__ int32_t cta_sample(const char *trow, const char *drow, int64_t V, RowConst rc, float wu,
+                                           SampleSmem<NT> &sm) {
+  constexpr int NW = NT / 32;
+  constexpr int B = (DT == 1) ? 4 : 2;  // rounds whose loads are in flight together
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t NG = (V + 7) / 8;
+  const int nR = static_cast<int>((NG + NT - 1) / NT);
+  for (int attempt = 0; attempt < 2; ++attempt) {
+    // ---- one pass: group sums, warp scans, warp totals ----
+    if (tid == 0) sm.lastg = -1;
+    int32_t lastg = -1;
+    for (int r0 = 0; r0 < nR; r0 += B) {
+      float ag[B];
+      if (VEC && DT == 1) {
+        // every load of the B rounds in flight before any arithmetic
+        constexpr uint32_t ninf = 0xff80ff80u;
+        uint4 ry[B], rz[B];
+#pragma unroll
+        for (int b = 0; b < B; ++b) {
+          const int64_t g = static_cast<int64_t>(r0 + b) * NT + tid;
+          const bool in = (r0 + b < nR) && g < NG;
+          ry[b] = in ? ld_vec(trow + g * 16) : make_uint4(ninf, ninf, ninf, ninf);
+          rz[b] = (in && rc.resid) ? ld_vec(drow + g * 16) : make_uint4(ninf, ninf, ninf, ninf);
+        }
+#pragma unroll
+        for (int b = 0; b < B; ++b) {
+          const int64_t g = static_cast<int64_t>(r0 + b) * NT + tid;
+          float y[8], z[8];
+          Elem<1>::unpack(ry[b], y);
+          Elem<1>::unpack(rz[b], z);
+          float a = 0.f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) a = __fadd_rn(a, sample_weight(y[e], z[e], rc));
+          ag[b] = a;
+          if (a > 0.f) lastg = static_cast<int32_t>(g);
+        }
+      } else {
+#pragma unroll
+        for (int b = 0; b < B; ++b) {
+          float w[8];
+          const int64_t g = static_cast<int64_t>(r0 + b) * NT + tid;
+          ag[b] = (r0 + b < nR) ? sample_group<DT, VEC>(trow, drow, g, NG, V, rc, w) : 0.f;
+          if (ag[b] > 0.f) lastg = static_cast<int32_t>(g);
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        const float W = warp_scan_incl(ag[b]);
+        if (lane == 31 && r0 + b < nR) sm.W[(r0 + b) * NW + warp] = W;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lastg = max(lastg, __shfl_xor_sync(0xffffffffu, lastg, o));
+    __syncthreads();
+    if (lane == 0) atomicMax(&sm.lastg, lastg);
+    // round totals (sequential over warps), one round per thread
+    for (int r = tid; r < nR; r += NT) {
+      float R = 0.f;
+      for (int w = 0; w < NW; ++w) R = __fadd_rn(R, sm.W[r * NW + w]);
+      sm.R[r] = R;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      float Z = 0.f;
+      for (int r = 0; r < nR; ++r) Z = __fadd_rn(Z, sm.R[r]);
+      sm.degenerate = (rc.resid && !(Z > 0.f)) ? 1 : 0;
+      const float t = __fmul_rn(wu, Z);
+      int rs = -1, ws = -1;
+      float Pr = 0.f, Qw = 0.f, P = 0.f;
+      for (int r = 0; r < nR && rs < 0; ++r) {
+        const float P2 = __fadd_rn(P, sm.R[r]);
+        if (P2 > t) {
+          rs = r;
+          Pr = P;
+        }
+        P = P2;
+      }
+      if (rs >= 0) {
+        float Q = 0.f;
+        for (int w = 0; w < NW && ws < 0; ++w) {
+          const float Q2 = __fadd_rn(Q, sm.W[rs * NW + w]);
+          if (__fadd_rn(Pr, Q2) > t) {
+            ws = w;
+            Qw = Q;
+          }
+          Q = Q2;
+        }
+      }
+      sm.t = t;
+      sm.rs = rs;
+      sm.ws = ws;
+      sm.Pr = Pr;
+      sm.Qw = Qw;
+      sm.result = -1;
+    }
+    __syncthreads();
+    if (sm.degenerate) {
+      // no residual mass after rounding: draw from p at that row instead
+      rc.resid = false;
+      __syncthreads();
+      continue;
+    }
+    if (warp == 0) {
+      const int rs = sm.rs, ws = sm.ws;
+      int32_t pick = -1;
+      const int64_t glast = sm.lastg;
+      if (rs >= 0 && ws >= 0) {
+        // lane and entry levels: lane l recomputes group l of the crossing warp
+        const float t = sm.t, Pr = sm.Pr, Qw = sm.Qw;
+        const int64_t g = static_cast<int64_t>(rs) * NT + ws * 32 + lane;
+        float w[8];
+        const float ag = sample_group<DT, VEC>(trow, drow, g, NG, V, rc, w);
+        const float E = warp_scan_incl(ag);
+        const float Ex = __shfl_up_sync(0xffffffffu, E, 1);
+        const float Eprev = (lane == 0) ? 0.f : Ex;
+        const unsigned cross = __ballot_sync(0xffffffffu, __fadd_rn(Pr, __fadd_rn(Qw, E)) > t);
+        if (cross) {
+          const int l = __ffs(cross) - 1;
+          if (lane == l) {
+            float part = 0.f;
+            int32_t lastpos = -1;
+            for (int e = 0; e < 8; ++e) {
+              part = __fadd_rn(part, w[e]);
+              if (w[e] > 0.f) lastpos = static_cast<int32_t>(g * 8 + e);
+              if (pick < 0 && __fadd_rn(Pr, __fadd_rn(Qw, __fadd_rn(Eprev, part))) > t)
+                pick = static_cast<int32_t>(g * 8 + e);
+            }
+            if (pick < 0) pick = lastpos;  // rounding between the lane and entry levels
+          }
+          pick = __shfl_sync(0xffffffffu, pick, l);
+        }
+      }
+      if (pick < 0 && glast >= 0 && lane == 0) {
+        // no crossing after rounding (w Z rounded up to Z, or between two
+        // levels): the last entry of the row with positive weight
+        float w[8];
+        sample_group<DT, VEC>(trow, drow, glast, NG, V, rc, w);
+        for (int e = 0; e < 8; ++e)
+          if (w[e] > 0.f) pick = static_cast<int32_t>(glast * 8 + e);
+      }
+      if (lane == 0) sm.result = pick;
+    }
+    __syncthreads();
+    return sm.result;
+  }
+  return -1;  // not reached: p always has mass
+}
+
+}  // namespace svw

@@ -7,7 +7,7 @@
 //   prefix; draw one token from [p - q]_+ at the rejected row or from p at the
 //   bonus row.  Greedy (T = 0): accept iff x_j is the target argmax.
 //
-// GPU design: three stream-ordered kernels; no CTA ever waits for another.
+// GPU design: two stream-ordered kernels; no CTA ever waits for another.
 //  1. verify_stats      the HBM stream.  Each logit row is cut into C chunks
 //                       (C <= 32, ~30 KB); a (row, chunk) pair is a work item.
 //                       Persistent CTAs take items in a fixed stride.  One
@@ -20,40 +20,24 @@
 //                       arithmetic, and write one Partial per warp.  No block
 //                       barrier in the steady state.  Each CTA also checks a
 //                       share of the CSR offsets.
-//  2. verify_finalize   one CTA per request: validates the request, merges the
-//                       partials into row log-sum-exps (or argmaxes), runs
-//                       every accept test in one warp (ballot + ffs = leftmost
-//                       rejection), writes accept_len and the sampling row
-//                       (greedy: next_token).
-//  3. verify_sample     (T > 0) inverse-CDF draw over the sampling row (pair),
-//                       split into 16384-entry sampler chunks so the whole GPU
-//                       takes part; the CTA that completes a request's chunks
-//                       (arrival counter) resolves the token.
-// Kernels 2 and 3 are launched as programmatic dependents of the kernel before
-// them: they are scheduled while it drains and wait (griddepcontrol.wait) only
-// before reading its results; finalize reads the draft tokens and their logits
-// before that point.
-//
-// Inverse-CDF prefix sums.  Weights w_v = [p_v - q_v]_+ (or p_v).  The prefix
-// C_v is defined level by level, each level a sequential fp32 sum (from 0, in
-// index order) of non-negative terms, so that it is reproducible,
-// non-decreasing and equal at every level boundary:
-//   group  8 consecutive entries               partial sums part_k, total a_g
-//   warp   32 consecutive groups (one a lane)  prefix E_l, total W_w
-//   round  8 warps (2048 entries)              prefix Q_w, total R_r
-//   chunk  8 rounds (16384 entries)            prefix P_r, total Z_c
-//   row    chunks                              prefix B_c, total Z
-//   C_v = fl(B_c + fl(P_r + fl(Q_w + fl(E_l + part_k))))
-// A round is one 16-byte vector per thread of the CTA, so every load of the
-// sampler is coalesced.
-// next = smallest v with C_v > w Z; that v always has w_v > 0.  If rounding
-// leaves no crossing, the last positive entry is taken.
+//  2. verify_finalize   one CTA per request (two per SM, so every request of
+//                       a large batch is in flight at once): validates the
+//                       request, merges the partials into row log-sum-exps
+//                       (or argmaxes), runs every accept test in one warp
+//                       (ballot + ffs = leftmost rejection), writes
+//                       accept_len, then (T > 0) the whole CTA draws the next
+//                       token by inverse CDF over the residual row pair or the
+//                       bonus row (svw_sample.cuh), in one coalesced pass.
+// The finalize kernel is launched as a programmatic dependent of the stats
+// kernel: it is scheduled while the stream drains and reads the draft tokens
+// and their logits before waiting (griddepcontrol.wait) for the partials.
 #include <cfloat>
 #include <climits>
 #include <cuda_runtime.h>
 
 #include "svw_device.cuh"
 #include "svw_internal.h"
+#include "svw_sample.cuh"
 
 namespace svw {
 
@@ -68,12 +52,9 @@ struct StatsShape {
   static constexpr int kThreads = (kCW + 1) * 32;  // + one producer warp
 };
 constexpr int kStages = 3;                     // bulk-copy ring depth (2 CTAs per SM)
-constexpr int kThreads = 256;                  // sample kernel
-constexpr int kWarps = kThreads / 32;
-constexpr int kFinThreads = 1024;              // finalize kernel: about one row per warp
+constexpr int kFinThreads = 512;               // finalize (and sampling) kernel, two CTAs per SM
 constexpr int kFinWarps = kFinThreads / 32;
 constexpr int kMaxRows = 2 * SVW_MAX_LEN + 1;
-constexpr int kMaxGroupsPerSpan = 512;  // single-CTA fallback sampler: V <= 256 * 512 * 8
 
 // programmatic dependent launch: let the next kernel be scheduled / wait for
 // the previous kernel's results
@@ -413,14 +394,15 @@ __global__ void __launch_bounds__(StatsShape<GREEDY>::kThreads, 2) verify_stats(
 // ---------------------------------------------------------------------------
 // kernel 2: per-request validation, merge, accept tests
 // ---------------------------------------------------------------------------
-template <int DT, bool GREEDY>
+template <int DT, bool GREEDY, bool VEC>
 __global__ void __launch_bounds__(kFinThreads) verify_finalize(VerifyArgs a) {
   using E = Elem<DT>;
   __shared__ float row_m[kMaxRows];
   __shared__ float row_l[kMaxRows];
   __shared__ int32_t row_idx[kMaxRows];
   __shared__ int32_t row_bad[kMaxRows];
-  __shared__ int32_t s_ok;
+  __shared__ int32_t s_ok, s_js;
+  __shared__ SampleSmem<kFinThreads> ssm;
   const int32_t i = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   pdl_launch_dependents();
@@ -444,10 +426,7 @@ __global__ void __launch_bounds__(kFinThreads) verify_finalize(VerifyArgs a) {
       }
     }
     const bool ok = len_ok && __all_sync(0xffffffffu, tok_ok);
-    if (lane == 0) {
-      s_ok = ok ? 1 : 0;
-      a.sample_counters[i] = 0;  // the sampling kernel starts after this grid
-    }
+    if (lane == 0) s_ok = ok ? 1 : 0;
   }
   pdl_wait();  // the stats kernel's partials and CSR flags are complete
 
@@ -457,7 +436,6 @@ __global__ void __launch_bounds__(kFinThreads) verify_finalize(VerifyArgs a) {
   auto reject = [&]() {  // one thread: a bad request
     a.accept_len[i] = -1;
     a.next_token[i] = -1;
-    if (!GREEDY) a.sinfo[i].valid = 0;
     if (a.status) atomicOr(a.status, SVW_DEV_BAD_INPUT);
   };
   if (!s_ok || csr_bad) {
@@ -498,440 +476,55 @@ __global__ void __launch_bounds__(kFinThreads) verify_finalize(VerifyArgs a) {
     }
   }
   __syncthreads();
-  if (warp != 0) return;
-  int bad = 0;
-  for (int r = lane; r < nrows; r += 32) bad |= row_bad[r];
-  bad = __any_sync(0xffffffffu, bad);
-  bool acc = true;
-  if (lane < L) {
-    if (GREEDY) {
-      acc = (x == row_idx[lane]);
-    } else {
-      // log2(p(x)/q(x)) from raw logits and row log-sum-exps
-      float thr;
-      if (zx == -INFINITY) {
-        thr = 1.f;  // q(x) = 0: accept
+  if (warp == 0) {
+    int bad = 0;
+    for (int r = lane; r < nrows; r += 32) bad |= row_bad[r];
+    bad = __any_sync(0xffffffffu, bad);
+    bool acc = true;
+    if (lane < L) {
+      if (GREEDY) {
+        acc = (x == row_idx[lane]);
       } else {
-        const float dl = __fsub_rn(
-            __fmul_rn(__fsub_rn(__fsub_rn(yx, row_m[lane]), __fsub_rn(zx, row_m[L + 1 + lane])), a.k),
-            __fsub_rn(row_l[lane], row_l[L + 1 + lane]));
-        thr = (dl >= 0.f) ? 1.f : ex2(dl);
+        // log2(p(x)/q(x)) from raw logits and row log-sum-exps
+        float thr;
+        if (zx == -INFINITY) {
+          thr = 1.f;  // q(x) = 0: accept
+        } else {
+          const float dl = __fsub_rn(
+              __fmul_rn(__fsub_rn(__fsub_rn(yx, row_m[lane]), __fsub_rn(zx, row_m[L + 1 + lane])), a.k),
+              __fsub_rn(row_l[lane], row_l[L + 1 + lane]));
+          thr = (dl >= 0.f) ? 1.f : ex2(dl);
+        }
+        acc = (u < thr);
       }
-      acc = (u < thr);
     }
-  }
-  const unsigned rej = __ballot_sync(0xffffffffu, !acc);
-  const int32_t js = rej ? (__ffs(rej) - 1) : L;
-  if (lane != 0) return;
-  if (bad) {
-    reject();
-    return;
-  }
-  a.accept_len[i] = js;
-  if (GREEDY) {
-    a.next_token[i] = row_idx[js];
-  } else {
-    SampleInfo si;
-    si.js = js;
-    si.resid = (js < L) ? 1 : 0;
-    si.valid = 1;
-    si.w = philox_uniform(a.seed, static_cast<uint32_t>(i), static_cast<uint32_t>(js), 1u);
-    si.Mt = row_m[js];
-    si.lt = row_l[js];
-    si.Md = (js < L) ? row_m[L + 1 + js] : 0.f;
-    si.ld = (js < L) ? row_l[L + 1 + js] : 0.f;
-    a.sinfo[i] = si;
-  }
-}
-
-// ---------------------------------------------------------------------------
-// sampling weights
-// ---------------------------------------------------------------------------
-constexpr int kRounds = 8;                       // rounds per sampler chunk
-constexpr int kSChunk = kThreads * kRounds * 8;  // 16384 entries per sampler chunk
-constexpr int kSpan = kRounds * kWarps;          // warp totals stored per sampler chunk
-
-// log2 p = y k + nT, log2 q = z k + nD (one rounding each); the constants are
-// computed once per request from the row maxima and log-sum-exps
-struct RowConst {
-  float k, nT, nD;
-  bool resid;
-};
-
-__device__ __forceinline__ RowConst row_const(const SampleInfo &si, float k) {
-  RowConst c;
-  c.k = k;
-  c.nT = -__fmaf_rn(si.Mt, k, si.lt);
-  c.nD = -__fmaf_rn(si.Md, k, si.ld);
-  c.resid = si.resid != 0;
-  return c;
-}
-
-// [p - q]_+ (resid) or p
-__device__ __forceinline__ float weight(float y, float z, const RowConst &c) {
-  const float lp = __fmaf_rn(y, c.k, c.nT);
-  if (!c.resid) return ex2(lp);
-  const float lq = __fmaf_rn(z, c.k, c.nD);
-  if (!(lq < lp)) return 0.f;
-  return fmaxf(__fsub_rn(ex2(lp), ex2(lq)), 0.f);
-}
-
-// raw logits of group g (entries 8g .. 8g+7, -inf at v >= V)
-template <int DT, bool VEC>
-__device__ __forceinline__ void load_group(const char *row, int64_t g, int64_t V, float (&x)[8]) {
-  using E = Elem<DT>;
-  constexpr int EPV = E::kPerVec;
-  const int64_t v0 = g * 8;
-  if (VEC) {
-#pragma unroll
-    for (int h = 0; h < 8 / EPV; ++h) {
-      const int64_t vv = v0 + h * EPV;
-      if (vv < V) {
-        E::unpack(ld_vec(row + vv * E::kSize), x + h * EPV);
+    const unsigned rej = __ballot_sync(0xffffffffu, !acc);
+    const int32_t js = rej ? (__ffs(rej) - 1) : L;
+    if (lane == 0) {
+      if (bad) {
+        reject();
+        s_js = -1;
       } else {
-#pragma unroll
-        for (int e = 0; e < EPV; ++e) x[h * EPV + e] = -INFINITY;
+        a.accept_len[i] = js;
+        if (GREEDY) a.next_token[i] = row_idx[js];
+        s_js = js;
       }
     }
-  } else {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) x[e] = (v0 + e < V) ? E::load(row, v0 + e) : -INFINITY;
   }
-}
-
-// the 8 weights of group g and their sequential sum a_g
-template <int DT, bool VEC>
-__device__ __forceinline__ float group_weights(const char *trow, const char *drow, int64_t g, int64_t V,
-                                               const RowConst &c, float (&w)[8]) {
-  float y[8], z[8];
-  load_group<DT, VEC>(trow, g, V, y);
-  if (c.resid) load_group<DT, VEC>(drow, g, V, z);
-  float a = 0.f;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    w[e] = weight(y[e], c.resid ? z[e] : 0.f, c);
-    a = __fadd_rn(a, w[e]);
-  }
-  return a;
-}
-
-// last entry of group g with positive weight (-1: none)
-template <int DT, bool VEC>
-__device__ __forceinline__ int32_t last_positive(const char *trow, const char *drow, int64_t g, int64_t V,
-                                                 const RowConst &c) {
-  if (g < 0) return -1;
-  float w[8];
-  group_weights<DT, VEC>(trow, drow, g, V, c, w);
-  int32_t last = -1;
-#pragma unroll
-  for (int e = 0; e < 8; ++e)
-    if (w[e] > 0.f) last = static_cast<int32_t>(g * 8 + e);
-  return last;
-}
-
-struct SampleSmem {
-  float lane_tot[kThreads];
-  float E[kThreads + 1];
-  int32_t lastv[kThreads];
-  float grp[kMaxGroupsPerSpan];
-  float chunk_tot[1024];
-  float ga[kRounds][kThreads];  // group totals of the chunk (round, thread)
-  float W[kRounds][kWarps];     // warp totals (round, warp)
-  float Rr[kRounds];            // round totals
-  int32_t warp_last[kWarps];
-  float gw[32][8];              // resolve: weights of the crossing warp's groups
-  int32_t is_last;
-  int32_t cstar;
-  int32_t result;
-  int32_t degenerate;
-  float t;
-  float Bc;
-  float Pw;
-  float El;
-  int32_t wstar;
-  int32_t lstar;
-};
-
-// Single-CTA inverse CDF over a whole row of p.  Used only when a rejected
-// row has no residual mass after rounding; its prefix is defined with 256
-// thread spans (sequential within and across spans).
-template <int DT, bool VEC>
-__device__ __noinline__ int32_t sample_whole_row_p(const char *trow, int64_t V, RowConst c, float wu,
-                                                   SampleSmem &sm) {
-  const int tid = threadIdx.x;
-  c.resid = false;
-  const int64_t NG = (V + 7) / 8;
-  const int64_t GPT = (NG + kThreads - 1) / kThreads;
-  const int64_t g0 = min(NG, static_cast<int64_t>(tid) * GPT), g1 = min(NG, g0 + GPT);
-  float R = 0.f;
-  int32_t last = -1;
-  for (int64_t g = g0; g < g1; ++g) {
-    float w[8];
-    R = __fadd_rn(R, group_weights<DT, VEC>(trow, nullptr, g, V, c, w));
-    for (int e = 0; e < 8; ++e)
-      if (w[e] > 0.f) last = static_cast<int32_t>(g * 8 + e);
-  }
-  sm.lane_tot[tid] = R;
-  sm.lastv[tid] = last;
+  if (GREEDY) return;
   __syncthreads();
-  if (tid == 0) {
-    float E = 0.f;
-    sm.E[0] = 0.f;
-    for (int s = 0; s < kThreads; ++s) {
-      E = __fadd_rn(E, sm.lane_tot[s]);
-      sm.E[s + 1] = E;
-    }
-    sm.t = __fmul_rn(wu, E);
-    sm.lstar = INT32_MAX;
-  }
-  __syncthreads();
-  const float t = sm.t;
-  if (sm.E[tid + 1] > t) atomicMin(&sm.lstar, tid);
-  __syncthreads();
-  const int32_t ts = sm.lstar;
-  if (ts == INT32_MAX) {
-    if (tid == 0) {
-      int32_t lv = -1;
-      for (int s = 0; s < kThreads; ++s) lv = max(lv, sm.lastv[s]);
-      sm.result = lv;
-    }
-    __syncthreads();
-    return sm.result;
-  }
-  const int64_t h0 = min(NG, static_cast<int64_t>(ts) * GPT), h1 = min(NG, h0 + GPT);
-  for (int64_t g = h0 + tid; g < h1; g += kThreads) {
-    float w[8];
-    sm.grp[g - h0] = group_weights<DT, VEC>(trow, nullptr, g, V, c, w);
-  }
-  __syncthreads();
-  if (tid == 0) {
-    const float Es = sm.E[ts];
-    float Rr = 0.f;
-    int32_t pick = -1;
-    for (int64_t g = h0; g < h1 && pick < 0; ++g) {
-      const float R2 = __fadd_rn(Rr, sm.grp[g - h0]);
-      if (__fadd_rn(Es, R2) > t) {
-        float w[8];
-        group_weights<DT, VEC>(trow, nullptr, g, V, c, w);
-        float part = 0.f;
-        for (int e = 0; e < 8; ++e) {
-          part = __fadd_rn(part, w[e]);
-          if (__fadd_rn(Es, __fadd_rn(Rr, part)) > t) {
-            pick = static_cast<int32_t>(g * 8 + e);
-            break;
-          }
-        }
-      }
-      Rr = R2;
-    }
-    sm.result = (pick < 0) ? sm.lastv[ts] : pick;
-  }
-  __syncthreads();
-  return sm.result;
-}
-
-// ---------------------------------------------------------------------------
-// kernel 3: inverse-CDF sampling over (request, sampler chunk) items
-// ---------------------------------------------------------------------------
-template <int DT, bool VEC>
-__global__ void __launch_bounds__(kThreads) verify_sample(VerifyArgs a) {
-  __shared__ SampleSmem sm;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int32_t Cs = a.Cs;
-  // last requests first: their rows were streamed most recently
-  const int64_t item = static_cast<int64_t>(a.N) * Cs - 1 - blockIdx.x;
-  const int32_t i = static_cast<int32_t>(item / Cs);
-  const int32_t c = static_cast<int32_t>(item - static_cast<int64_t>(i) * Cs);
-  pdl_wait();  // the finalize kernel's sampling rows and counters are in place
-  const SampleInfo si = a.sinfo[i];
-  if (!si.valid) return;
-  using E = Elem<DT>;
-  const int64_t ci = __ldg(a.cu + i);
-  const char *trow = static_cast<const char *>(a.target) + (ci + i + si.js) * a.V * E::kSize;
-  const RowConst rc = row_const(si, a.k);
-  const char *drow = rc.resid ? static_cast<const char *>(a.draft) + (ci + si.js) * a.V * E::kSize : nullptr;
-  const int64_t NG = (a.V + 7) / 8;
-
-  // ---- this chunk: group, warp, round and chunk totals ----
-  // round r, thread tid: group c * 2048 + r * 256 + tid
-  const int64_t gc = static_cast<int64_t>(c) * (kSChunk / 8);
-  int32_t lastg = -1;
-  if (VEC && DT == 1) {
-    uint4 ry[kRounds], rz[kRounds];  // all 16 loads of the thread first
-#pragma unroll
-    for (int r = 0; r < kRounds; ++r) {
-      const int64_t g = gc + r * kThreads + tid;
-      const bool in = g < NG;
-      ry[r] = in ? ld_vec(trow + g * 16) : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
-      rz[r] = (in && rc.resid) ? ld_vec(drow + g * 16) : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
-    }
-#pragma unroll
-    for (int r = 0; r < kRounds; ++r) {
-      float y[8], z[8];
-      E::unpack(ry[r], y);
-      E::unpack(rz[r], z);
-      float ag = 0.f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) ag = __fadd_rn(ag, weight(y[e], z[e], rc));
-      sm.ga[r][tid] = ag;
-      if (ag > 0.f) lastg = static_cast<int32_t>(gc + r * kThreads + tid);
-    }
-  } else {
-#pragma unroll 2
-    for (int r = 0; r < kRounds; ++r) {
-      const int64_t g = gc + r * kThreads + tid;
-      float ag = 0.f;
-      if (g < NG) {
-        float w[8];
-        ag = group_weights<DT, VEC>(trow, drow, g, a.V, rc, w);
-      }
-      sm.ga[r][tid] = ag;
-      if (ag > 0.f) lastg = static_cast<int32_t>(g);
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) lastg = max(lastg, __shfl_xor_sync(0xffffffffu, lastg, o));
-  if (lane == 0) sm.warp_last[warp] = lastg;
-  __syncthreads();
-  const int64_t slot = static_cast<int64_t>(i) * Cs + c;
-  if (lane < kRounds) {  // lane r of warp w: total of warp w in round r, over its 32 groups in order
-    float W = 0.f;
-    for (int l = 0; l < 32; ++l) W = __fadd_rn(W, sm.ga[lane][warp * 32 + l]);
-    sm.W[lane][warp] = W;
-    a.span_tot[slot * kSpan + lane * kWarps + warp] = W;
-  }
-  __syncthreads();
-  if (tid < kRounds) {
-    float R = 0.f;
-    for (int w = 0; w < kWarps; ++w) R = __fadd_rn(R, sm.W[tid][w]);
-    sm.Rr[tid] = R;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    float Z = 0.f;
-    int32_t lv = -1;
-    for (int r = 0; r < kRounds; ++r) Z = __fadd_rn(Z, sm.Rr[r]);
-    for (int w = 0; w < kWarps; ++w) lv = max(lv, sm.warp_last[w]);
-    a.chunk_tot[slot] = Z;
-    a.chunk_last[slot] = lv;
-    __threadfence();
-    const int32_t prev = atomicAdd(a.sample_counters + i, 1);
-    sm.is_last = (prev == Cs - 1) ? 1 : 0;
-  }
-  __syncthreads();
-  if (!sm.is_last) return;
-  __threadfence();
-
-  // ---- resolve (the CTA that completed request i) ----
-  for (int q = tid; q < Cs; q += kThreads) sm.chunk_tot[q] = __ldcg(a.chunk_tot + static_cast<int64_t>(i) * Cs + q);
-  __syncthreads();
-  if (tid == 0) {
-    float B = 0.f;
-    for (int q = 0; q < Cs; ++q) B = __fadd_rn(B, sm.chunk_tot[q]);
-    const float t = __fmul_rn(si.w, B);
-    sm.t = t;
-    sm.degenerate = (rc.resid && !(B > 0.f)) ? 1 : 0;
-    int32_t cs = -1;
-    float Bc = 0.f, Bp = 0.f;
-    for (int q = 0; q < Cs && cs < 0; ++q) {
-      Bp = Bc;
-      Bc = __fadd_rn(Bc, sm.chunk_tot[q]);
-      if (Bc > t) cs = q;
-    }
-    sm.cstar = cs;
-    sm.Bc = Bp;  // prefix before the crossing chunk
-  }
-  __syncthreads();
-  int32_t tok;
-  if (sm.degenerate) {
-    // no residual mass after rounding: draw from p at that row instead
-    tok = sample_whole_row_p<DT, VEC>(trow, a.V, rc, si.w, sm);
-  } else if (sm.cstar < 0) {
-    // w Z rounded up to Z: the last entry with positive weight
-    if (tid == 0) {
-      int32_t lg = -1;
-      for (int q = 0; q < Cs; ++q) lg = max(lg, __ldcg(a.chunk_last + static_cast<int64_t>(i) * Cs + q));
-      sm.result = last_positive<DT, VEC>(trow, drow, lg, a.V, rc);
-    }
-    __syncthreads();
-    tok = sm.result;
-  } else {
-    const int32_t cs = sm.cstar;
-    if (tid < kSpan) sm.W[tid / kWarps][tid % kWarps] = __ldcg(a.span_tot + (static_cast<int64_t>(i) * Cs + cs) * kSpan + tid);
-    __syncthreads();
-    if (tid == 0) {
-      const float t = sm.t, B = sm.Bc;
-      // round level
-      float P = 0.f, Pr = 0.f;
-      int32_t rs = -1;
-      for (int r = 0; r < kRounds && rs < 0; ++r) {
-        float R = 0.f;
-        for (int w = 0; w < kWarps; ++w) R = __fadd_rn(R, sm.W[r][w]);
-        const float P2 = __fadd_rn(P, R);
-        if (__fadd_rn(B, P2) > t) {
-          rs = r;
-          Pr = P;
-        }
-        P = P2;
-      }
-      // warp level
-      int32_t ws = -1;
-      float Qw = 0.f;
-      if (rs >= 0) {
-        float Q = 0.f;
-        for (int w = 0; w < kWarps && ws < 0; ++w) {
-          const float Q2 = __fadd_rn(Q, sm.W[rs][w]);
-          if (__fadd_rn(B, __fadd_rn(Pr, Q2)) > t) {
-            ws = w;
-            Qw = Q;
-          }
-          Q = Q2;
-        }
-      }
-      sm.wstar = (rs >= 0 && ws >= 0) ? rs * kWarps + ws : -1;
-      sm.Pw = Pr;
-      sm.El = Qw;
-    }
-    __syncthreads();
-    // the crossing warp's 32 groups, one thread each
-    const int32_t rw = sm.wstar;
-    const int64_t gw0 = static_cast<int64_t>(cs) * (kSChunk / 8) +
-                        static_cast<int64_t>(rw / kWarps) * kThreads + static_cast<int64_t>(rw % kWarps) * 32;
-    if (rw >= 0 && tid < 32) {
-      float w[8];
-      const int64_t g = gw0 + tid;
-      sm.lane_tot[tid] = (g < NG) ? group_weights<DT, VEC>(trow, drow, g, a.V, rc, w) : 0.f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) sm.gw[tid][e] = (g < NG) ? w[e] : 0.f;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      const float t = sm.t, B = sm.Bc, Pr = sm.Pw, Qw = sm.El;
-      int32_t pick = -1;
-      if (rw >= 0) {
-        float Ecur = 0.f;
-        for (int l = 0; l < 32 && pick < 0; ++l) {
-          const float E2 = __fadd_rn(Ecur, sm.lane_tot[l]);
-          if (__fadd_rn(B, __fadd_rn(Pr, __fadd_rn(Qw, E2))) > t) {
-            float part = 0.f;
-            for (int e = 0; e < 8; ++e) {
-              part = __fadd_rn(part, sm.gw[l][e]);
-              if (__fadd_rn(B, __fadd_rn(Pr, __fadd_rn(Qw, __fadd_rn(Ecur, part)))) > t) {
-                pick = static_cast<int32_t>((gw0 + l) * 8 + e);
-                break;
-              }
-            }
-          }
-          Ecur = E2;
-        }
-      }
-      if (pick < 0)  // unreachable: the levels' totals agree exactly
-        pick = last_positive<DT, VEC>(trow, drow, __ldcg(a.chunk_last + static_cast<int64_t>(i) * Cs + cs), a.V, rc);
-      sm.result = pick;
-    }
-    __syncthreads();
-    tok = sm.result;
-  }
+  const int32_t js = s_js;
+  if (js < 0) return;
+  // ---- the next token: inverse CDF over [p - q]_+ at row js, or p at the bonus row ----
+  RowConst rc;
+  rc.k = a.k;
+  rc.resid = js < L;
+  rc.nT = -__fmaf_rn(row_m[js], a.k, row_l[js]);
+  rc.nD = rc.resid ? -__fmaf_rn(row_m[L + 1 + js], a.k, row_l[L + 1 + js]) : 0.f;
+  const char *trow = static_cast<const char *>(a.target) + (t0 + js) * a.V * E::kSize;
+  const char *drow = rc.resid ? static_cast<const char *>(a.draft) + (d0 + js) * a.V * E::kSize : nullptr;
+  const float w = philox_uniform(a.seed, static_cast<uint32_t>(i), static_cast<uint32_t>(js), 1u);
+  const int32_t tok = cta_sample<DT, VEC, kFinThreads>(trow, drow, a.V, rc, w, ssm);
   if (tid == 0) a.next_token[i] = tok;
 }
 
@@ -1009,9 +602,7 @@ cudaError_t launch_all_t(const VerifyArgs &args, cudaStream_t st) {
   timer_after(tm, st);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = launch_dependent("verify_finalize", verify_finalize<DT, GREEDY>, static_cast<unsigned>(a.N), kFinThreads, a, st);
-  if (e != cudaSuccess || GREEDY) return e;
-  return launch_dependent("verify_sample", verify_sample<DT, VEC>, static_cast<unsigned>(static_cast<int64_t>(a.N) * a.Cs), kThreads,
+  return launch_dependent("verify_finalize", verify_finalize<DT, GREEDY, VEC>, static_cast<unsigned>(a.N), kFinThreads,
                           a, st);
 }
 
@@ -1022,7 +613,6 @@ cudaError_t launch_all(const VerifyArgs &a, bool greedy, cudaStream_t st) {
 
 }  // namespace
 
-int32_t sampler_chunks(int64_t V) { return static_cast<int32_t>((V + kSChunk - 1) / kSChunk); }
 
 ChunkPlan plan_chunks(int64_t V, int esize) {
   const int64_t target = (esize == 2) ? 16384 : 8192;
@@ -1039,41 +629,19 @@ static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 
 VerifyLayout verify_layout(int32_t N, int64_t total_rows, int64_t V, int esize) {
   const ChunkPlan p = plan_chunks(V, esize);
-  const size_t Cs = static_cast<size_t>(sampler_chunks(V));
   VerifyLayout l;
   const size_t rows = static_cast<size_t>(total_rows + N) + static_cast<size_t>(total_rows);
-  const size_t ns = static_cast<size_t>(N) * Cs;
   size_t off = 0;
   l.part_off = off;
   off += align256(rows * static_cast<size_t>(p.C) * kCWMax * sizeof(Partial));
-  l.sample_counters_off = off;
-  off += align256(static_cast<size_t>(N) * 4);
-  l.sinfo_off = off;
-  off += align256(static_cast<size_t>(N) * sizeof(SampleInfo));
-  l.span_off = off;
-  off += align256(ns * kSpan * sizeof(float));
-  l.chunk_tot_off = off;
-  off += align256(ns * sizeof(float));
-  l.chunk_last_off = off;
-  off += align256(ns * sizeof(int32_t));
   l.csr_bad_off = off;
   off += align256(kMaxStatsGrid * sizeof(int32_t));
   l.total = off;
   return l;
 }
 
-cudaError_t launch_verify_sample(const VerifyArgs &a, int dtype, bool vec, cudaStream_t st) {
-  const unsigned grid = static_cast<unsigned>(static_cast<int64_t>(a.N) * a.Cs);
-  if (dtype == SVW_BF16)
-    return vec ? launch_dependent("verify_sample", verify_sample<1, true>, grid, kThreads, a, st)
-               : launch_dependent("verify_sample", verify_sample<1, false>, grid, kThreads, a, st);
-  return vec ? launch_dependent("verify_sample", verify_sample<0, true>, grid, kThreads, a, st)
-             : launch_dependent("verify_sample", verify_sample<0, false>, grid, kThreads, a, st);
-}
-
 FusedLayout fused_layout(int32_t N, int64_t total_rows, int64_t V) {
-  const size_t Cs = static_cast<size_t>(sampler_chunks(V));
-  const size_t ns = static_cast<size_t>(N) * Cs;
+  (void)V;
   const size_t R = static_cast<size_t>(total_rows);
   FusedLayout l;
   size_t off = 0;
@@ -1085,16 +653,6 @@ FusedLayout fused_layout(int32_t N, int64_t total_rows, int64_t V) {
   off += align256(static_cast<size_t>(N) * 8 * 16);
   l.csr_bad_off = off;
   off += align256(kMaxStatsGrid * sizeof(int32_t));
-  l.sample_counters_off = off;
-  off += align256(static_cast<size_t>(N) * 4);
-  l.sinfo_off = off;
-  off += align256(static_cast<size_t>(N) * sizeof(SampleInfo));
-  l.span_off = off;
-  off += align256(ns * kSpan * sizeof(float));
-  l.chunk_tot_off = off;
-  off += align256(ns * sizeof(float));
-  l.chunk_last_off = off;
-  off += align256(ns * sizeof(int32_t));
   l.total = off;
   return l;
 }

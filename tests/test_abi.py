@@ -138,7 +138,7 @@ def test_verify_opd_argument_validation(lib):
     assert call(c=0.0) == 1
     assert call(t=ctypes.c_void_p(p.value + 2)) == 3   # bases must be 16-byte aligned
     assert call(V=63) == 2                  # 126-byte rows are not 16-byte pitched
-    assert lib.svw_verify_opd_workspace_size(4, 64, 151936, 1) > lib.svw_verify_opd_workspace_size(4, 64, 1024, 1) > 0
+    assert lib.svw_verify_opd_workspace_size(4, 640, 151936, 1) > lib.svw_verify_opd_workspace_size(4, 64, 151936, 1) > 0
     assert lib.svw_verify_opd_workspace_size(0, 64, 1024, 1) == 0
 
 
