@@ -199,42 +199,51 @@ __device__ __forceinline__ void warp_amax_smem(uint32_t base, int nvec, int32_t 
   constexpr int EPV = E::kPerVec;
   const int v0 = wid * 32 + lane;
   float mx = -INFINITY;
+  int bvi = (v0 < nvec) ? v0 : -1;  // this lane's first vector holding its maximum (-inf rows: the first)
   uint32_t nanw = 0;
   if (DT == 1) {
-    uint32_t mw = 0xff80ff80u;  // NaN-propagating max: a NaN anywhere survives
     for (int vi = v0; vi < nvec; vi += CW * 32) {
       const uint4 q = lds128(base + vi * 16);
-      mw = bf16x2_max_nan(mw, bf16x2_max_nan(bf16x2_max_nan(q.x, q.y), bf16x2_max_nan(q.z, q.w)));
+      // NaN-propagating max of the vector: a NaN anywhere survives
+      const uint32_t m2 = bf16x2_max_nan(bf16x2_max_nan(q.x, q.y), bf16x2_max_nan(q.z, q.w));
+      nanw |= bf16x2_nan(m2);
+      const float2 f = bf16x2_f2(m2);
+      const float vm = fmaxf(f.x, f.y);
+      if (vm > mx) {
+        mx = vm;
+        bvi = vi;
+      }
     }
-    nanw = bf16x2_nan(mw);
-    const float2 f = bf16x2_f2(mw);
-    mx = fmaxf(f.x, f.y);
   } else {
     for (int vi = v0; vi < nvec; vi += CW * 32) {
       const uint4 q = lds128(base + vi * 16);
       const float x[4] = {__uint_as_float(q.x), __uint_as_float(q.y), __uint_as_float(q.z),
                           __uint_as_float(q.w)};
+      float vm = -INFINITY;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         nanw |= (x[e] != x[e]);
-        mx = fmaxf(mx, x[e]);
+        vm = fmaxf(vm, x[e]);
+      }
+      if (vm > mx) {
+        mx = vm;
+        bvi = vi;
       }
     }
   }
   float wmx = mx;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) wmx = fmaxf(wmx, __shfl_xor_sync(0xffffffffu, wmx, o));
-  // only lanes holding the warp maximum look for its first index
-  // (each lane's vectors are in index order, lanes interleave by vector)
+  // only lanes holding the warp maximum look for its first index, in the
+  // one vector where their maximum first appeared (each lane's vectors are in
+  // index order, lanes interleave by vector)
   idx = INT32_MAX;
-  if (mx == wmx && nvec > 0) {
-    for (int vi = v0; vi < nvec && idx == INT32_MAX; vi += CW * 32) {
-      float x[EPV];
-      E::unpack(lds128(base + vi * 16), x);
+  if (mx == wmx && bvi >= 0) {
+    float x[EPV];
+    E::unpack(lds128(base + bvi * 16), x);
 #pragma unroll
-      for (int e = 0; e < EPV; ++e)
-        if (idx == INT32_MAX && x[e] == wmx) idx = c0 + vi * EPV + e;
-    }
+    for (int e = EPV - 1; e >= 0; --e)
+      if (x[e] == wmx) idx = c0 + bvi * EPV + e;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) idx = min(idx, __shfl_xor_sync(0xffffffffu, idx, o));
@@ -242,8 +251,6 @@ __device__ __forceinline__ void warp_amax_smem(uint32_t base, int nvec, int32_t 
   nan = __any_sync(0xffffffffu, nanw != 0) ? 1 : 0;
 }
 
-// plain-load variants for rows that are not 16-byte pitched (whole warp,
-// elements v = wid*32 + lane + j*256 of the chunk)
 template <int DT, int CW>
 __device__ __forceinline__ void warp_lse_global(const char *p0, int n, int wid, int lane, float k, float &m,
                                                 float &s) {
