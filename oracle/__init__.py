@@ -31,6 +31,7 @@ FLAG_NEAR_CDF = 2
 FLAG_DEGENERATE = 4
 FLAG_BAD = 8
 FLAG_NEAR_CLIP = 16
+FLAG_NEAR_FLOOR = 32
 
 _lib = None
 _lock = threading.Lock()
@@ -70,6 +71,12 @@ def _load():
                 ctypes.c_int64, ctypes.c_int32, ctypes.c_double, ctypes.c_double,
                 ctypes.c_double, ctypes.c_double, P, P, P]
             lib.oracle_opd_loss.restype = ctypes.c_int
+            lib.oracle_length_head.argtypes = [
+                P, P, ctypes.c_int, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                P, P, ctypes.c_float, ctypes.c_double, P, P, P]
+            lib.oracle_length_head.restype = ctypes.c_int
+            lib.oracle_length_label.argtypes = [P, P, P, ctypes.c_int32, P, P]
+            lib.oracle_length_label.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -159,3 +166,40 @@ def opd_loss(target, draft, temperature=1.0, clip_c=1.0, lambda_ce=0.1, grad_sca
     if rc != 0:
         raise MemoryError("oracle_opd_loss failed to allocate")
     return dict(loss=loss, dlogits=grad, flags=flg)
+
+
+def length_head(hidden, w1, b1, w2, b2, gamma=1.0):
+    """Adaptive length head forward.  hidden: [N, k, H] (uint16 bf16 bits or
+    float32), w1: [H', H] same dtype, b1: [H'], w2: [H'] float32, b2 scalar.
+    Returns dict(a_hat [N] float64, k_hat [N] int32, flags [N])."""
+    lib = _load()
+    h, dt = _logits(hidden)
+    w, dt2 = _logits(w1)
+    if dt != dt2:
+        raise TypeError("hidden and w1 must have the same dtype")
+    N, k, H = h.shape
+    Hp = w.shape[0]
+    assert w.shape == (Hp, H)
+    b1 = np.ascontiguousarray(b1, dtype=np.float32)
+    w2 = np.ascontiguousarray(w2, dtype=np.float32)
+    a_hat = np.zeros(N, np.float64)
+    k_hat = np.zeros(N, np.int32)
+    flags = np.zeros(N, np.int32)
+    rc = lib.oracle_length_head(_ptr(h), _ptr(w), dt, N, k, H, Hp, _ptr(b1), _ptr(w2), float(b2),
+                                float(gamma), _ptr(a_hat), _ptr(k_hat), _ptr(flags))
+    if rc != 0:
+        raise ValueError(f"oracle_length_head failed ({rc})")
+    return {"a_hat": a_hat, "k_hat": k_hat, "flags": flags}
+
+
+def length_label(accept_len, cu_draft, a_hat):
+    """a* = accept_len / L per request and the MSE (a_hat - a*)^2."""
+    lib = _load()
+    acc = np.ascontiguousarray(accept_len, dtype=np.int32)
+    cu = np.ascontiguousarray(cu_draft, dtype=np.int32)
+    ah = np.ascontiguousarray(a_hat, dtype=np.float64)
+    N = acc.shape[0]
+    a_star = np.zeros(N, np.float64)
+    loss = np.zeros(N, np.float64)
+    lib.oracle_length_label(_ptr(acc), _ptr(cu), _ptr(ah), N, _ptr(a_star), _ptr(loss))
+    return {"a_star": a_star, "loss": loss}

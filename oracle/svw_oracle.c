@@ -28,7 +28,12 @@
  *        Example".
  *  [AP]  "AdaFlash：基于在策略蒸馏扩散草稿器的自适应投机解码" §2.3: the verify
  *        batch packs each request's own verified length (sum of k_i tokens,
- *        not N x k), which this build expresses with CSR offsets.
+ *        not N x k), which this build expresses with CSR offsets; §2.2 the
+ *        adaptive length head (k_hat = clamp(floor(gamma a_hat k), 1, k)).
+ *  [AR]  also "Method Part 2: The Adaptive Length Head": "Algorithm 3:
+ *        Adaptive Length Head, Forward Pass" and "Online Update of the Length
+ *        Head, Derived" (l_len = (a_hat - a*)^2, a* the accepted fraction of
+ *        the verified tokens).
  *
  * Readings where the pages leave a step open (each is also listed in the
  * design notes of the repository):
@@ -56,6 +61,11 @@
  *    "Parallel Random Numbers: As Easy as 1, 2, 3", SC'11).
  *  - A row holding NaN, +Inf, or only -Inf has no softmax: the request (or
  *    OPD row) is reported bad.  At temperature 0 only NaN makes a row bad.
+ *  - Length head: the pages fix the layer order (per-position Linear + SiLU,
+ *    mean over the k positions, Linear + sigmoid, times gamma, floor, clamp)
+ *    but not the projected width H' (only H' < H); it is an argument.  The
+ *    MSE label compares the unscaled sigmoid output a_hat with a* =
+ *    accept_len / L (gamma is a serving knob applied after the prediction).
  */
 #include <math.h>
 #include <stddef.h>
@@ -72,6 +82,7 @@
 #define FLAG_DEGENERATE 4  /* Z == 0 after a rejection                    */
 #define FLAG_BAD 8         /* invalid request / non-finite row            */
 #define FLAG_NEAR_CLIP 16  /* some |t_v| within 1e-5 * c of the clip c    */
+#define FLAG_NEAR_FLOOR 32 /* gamma a_hat k within 1e-4 of an integer       */
 
 #define BAND 1e-5
 
@@ -422,5 +433,70 @@ int oracle_opd_loss(const void *target, const void *draft, int dtype, int64_t V,
   free(lq);
   free(q);
   free(t);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Adaptive length head ([AR] "Algorithm 3: Adaptive Length Head, Forward    */
+/* Pass"; [AP] §2.2).  For each request i with hidden states h[i] (k x H):   */
+/*   h'_p = SiLU(W1 h[i][p] + b1)        per position p, W1 is H' x H        */
+/*   hbar = (1/k) sum_p h'_p                                                 */
+/*   a_hat = sigmoid(w2 . hbar + b2)                                         */
+/*   k_hat = clamp(floor(gamma a_hat k), 1, k)                               */
+/* hidden and W1 are bf16 bits (dtype ORACLE_BF16) or fp32.                  */
+/* ------------------------------------------------------------------------ */
+static double silu(double x) { return x / (1.0 + exp(-x)); }
+
+int oracle_length_head(const void *hidden, const void *w1, int dtype, int32_t N, int32_t k, int32_t H,
+                       int32_t Hp, const float *b1, const float *w2, float b2, double gamma, double *a_hat,
+                       int32_t *k_hat, int32_t *flags) {
+  if (N < 0 || k < 1 || H < 1 || Hp < 1) return 1;
+  double *hbar = (double *)malloc(sizeof(double) * (size_t)Hp);
+  if (!hbar) return 2;
+  for (int32_t i = 0; i < N; ++i) {
+    for (int32_t j = 0; j < Hp; ++j) hbar[j] = 0.0;
+    for (int32_t p = 0; p < k; ++p) {
+      const int64_t row = (int64_t)i * k + p;
+      for (int32_t j = 0; j < Hp; ++j) {
+        double g = 0.0;
+        for (int32_t h = 0; h < H; ++h) g += elem(w1, dtype, j, H, h) * elem(hidden, dtype, row, H, h);
+        hbar[j] += silu(g + (double)b1[j]);
+      }
+    }
+    double z = (double)b2;
+    for (int32_t j = 0; j < Hp; ++j) z += (double)w2[j] * (hbar[j] / (double)k);
+    const double a = 1.0 / (1.0 + exp(-z));
+    const double x = gamma * a * (double)k;
+    double kh = floor(x);
+    if (kh < 1.0) kh = 1.0;
+    if (kh > (double)k) kh = (double)k;
+    a_hat[i] = a;
+    k_hat[i] = (int32_t)kh;
+    if (flags) {
+      const double frac = x - floor(x);
+      flags[i] = (frac < 1e-4 || frac > 1.0 - 1e-4) ? FLAG_NEAR_FLOOR : 0;
+    }
+  }
+  free(hbar);
+  return 0;
+}
+
+/* Length-head label and loss ([AR] "Online Update of the Length Head,
+ * Derived"): a* = accept_len / L (the accepted fraction of the L verified
+ * tokens of request i, L = cu[i+1] - cu[i]); loss = (a_hat - a*)^2.  A bad
+ * request (accept_len < 0 or L < 1) gets a* = loss = NaN. */
+int oracle_length_label(const int32_t *accept_len, const int32_t *cu, const double *a_hat, int32_t N,
+                        double *a_star, double *loss) {
+  for (int32_t i = 0; i < N; ++i) {
+    const int32_t L = cu[i + 1] - cu[i];
+    if (accept_len[i] < 0 || L < 1) {
+      a_star[i] = NAN;
+      loss[i] = NAN;
+      continue;
+    }
+    a_star[i] = (double)accept_len[i] / (double)L;
+    const double d = a_hat[i] - a_star[i];
+    loss[i] = d * d;
+  }
   return 0;
 }
