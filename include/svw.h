@@ -3,7 +3,8 @@
  * (serving_vocab_wide_gb300).  Hand-written CUDA for sm_103a (GB300).
  *
  * Two operations, both over full-vocabulary logits (and spec_verify_opd,
- * both on the same batch in one pass):
+ * both on the same batch in one pass), plus the adaptive length head that
+ * sets the next round's verified lengths (length_head, length_head_label):
  *
  *  spec_verify  batched speculative verification of a ragged batch.  Defined
  *               by "DFlash 阅读笔记：并行起草、目标特征与精确验证" §5.1 (greedy
@@ -23,7 +24,8 @@
  * Conventions for every entry point:
  *  - Pointers named "device" are CUDA device pointers (cudaMalloc / PyTorch
  *    CUDA tensors) on the current device.  The caller owns all memory; the
- *    library allocates and frees nothing and keeps no per-call state.
+ *    library allocates and frees no device memory and keeps no per-call state
+ *    (length_head's GEMM library keeps a host handle and per-shape plans).
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Calls are stream-ordered and never synchronise the host.
  *  - The return value covers host-side validation and launch errors only.
@@ -194,6 +196,42 @@ svw_status spec_verify_opd(const void *target_logits, const void *draft_logits, 
                            void *stream);
 
 /*
+ * length_head -- the adaptive length head's forward pass ("AdaFlash: Taming
+ * Variance in Diffusion Speculative Decoding", "Algorithm 3: Adaptive Length
+ * Head, Forward Pass"; "AdaFlash：基于在策略蒸馏扩散草稿器的自适应投机解码" §2.2):
+ * for each request i, from its drafter hidden states h_i (k positions x H),
+ *   h'_p = SiLU(W1 h_i[p] + b1),  hbar = (1/k) sum_p h'_p,
+ *   a_hat[i] = sigmoid(w2 . hbar + b2),
+ *   k_hat[i] = clamp(floor(gamma a_hat[i] k), 1, k)   (next round's verified length).
+ *   hidden     device bf16 [N, k, H] row-major, 16-byte aligned, H % 8 == 0.
+ *   w1         device bf16 [hidden_out, H] row-major (H' = hidden_out < H).
+ *   b1, w2     device float [hidden_out];  b2, gamma > 0 on the host.
+ *   a_hat      device float [N] out (before the gamma scaling);  k_hat device int32 [N] out.
+ *   workspace  device, 256-byte aligned, >= svw_length_head_workspace_size(N, k,
+ *              hidden_out) bytes; holds the projection and the GEMM library's scratch.
+ * The projection of the N k positions is one dense GEMM run by cuBLASLt on
+ * the workspace (the library allocates no device memory; cuBLASLt keeps a
+ * host handle and one plan per shape); bias, SiLU, mean, dot, sigmoid and
+ * clamp are one kernel.  SVW_ERR_CUDA if cuBLASLt has no plan for the shape.
+ */
+size_t svw_length_head_workspace_size(int32_t n_requests, int32_t k, int32_t hidden_out);
+
+svw_status length_head(const void *hidden, const void *w1, const float *b1, const float *w2, float b2,
+                       int32_t N, int32_t k, int32_t H, int32_t hidden_out, float gamma, float *a_hat,
+                       int32_t *k_hat, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * length_head_label -- the length head's training signal ("AdaFlash: Taming
+ * Variance in Diffusion Speculative Decoding", "Online Update of the Length
+ * Head, Derived"): a_star[i] = accept_len[i] / L_i, the accepted fraction of
+ * the L_i = cu_draft[i+1] - cu_draft[i] verified tokens, and (loss not NULL)
+ * loss[i] = (a_hat[i] - a_star[i])^2.  A bad request (accept_len < 0) gets
+ * NaN.  All pointers device; a_hat may be NULL when loss is NULL.
+ */
+svw_status length_head_label(const int32_t *accept_len, const int32_t *cu_draft, const float *a_hat, int32_t N,
+                             float *a_star, float *loss, void *stream);
+
+/*
  * spec_verify_noalloc -- spec_verify for callers that cannot allocate device
  * memory.  No counterpart on the pages: it exists only because some callers
  * have no allocator to hand over a workspace (a plain C serving loop, a
@@ -227,7 +265,8 @@ svw_status spec_verify_noalloc(const void *target_logits, const void *draft_logi
  * svw_time_next_launch -- measurement hook, not part of the method.  Arms a
  * one-shot timer on the calling host thread: the next launch of the named
  * kernel made from this thread ("verify_stats", "verify_finalize",
- * "opd_fast_kernel", "opd_fix_kernel", "opd_exact_kernel", "fused_finalize") records begin_event just before it and end_event just
+ * "opd_fast_kernel", "opd_fix_kernel", "opd_exact_kernel", "fused_finalize",
+ * "length_head_gemm", "length_head_epilogue") records begin_event just before it and end_event just
  * after it on the launch stream (cudaEvent_t handles passed as void*, owned
  * by the caller).  kernel = NULL disarms.  The library records nothing
  * unless armed.  Lets a benchmark time one kernel of a multi-kernel call with

@@ -60,6 +60,12 @@ def lib():
                                           P, P, P, P, P, P, SZ, P]
             L.spec_verify_opd.restype = ctypes.c_int
             L.spec_verify_noalloc.restype = ctypes.c_int
+            L.svw_length_head_workspace_size.argtypes = [I32, I32, I32]
+            L.svw_length_head_workspace_size.restype = SZ
+            L.length_head.argtypes = [P, P, P, P, F, I32, I32, I32, I32, F, P, P, P, SZ, P]
+            L.length_head.restype = ctypes.c_int
+            L.length_head_label.argtypes = [P, P, P, I32, P, P, P]
+            L.length_head_label.restype = ctypes.c_int
             L.svw_time_next_launch.argtypes = [ctypes.c_char_p, P, P]
             L.svw_time_next_launch.restype = ctypes.c_int
             L.svw_status_string.argtypes = [ctypes.c_int]
@@ -222,6 +228,48 @@ def spec_verify_opd(target, draft, cu_draft, draft_tokens, temperature: float, s
                                workspace.numel(), _stream_ptr(stream))
     _check(rc)
     return accept_len, next_token, loss, (dlogits if want_grad else None)
+
+
+def length_head(hidden, w1, b1, w2, b2: float, gamma: float = 1.0, a_hat=None, k_hat=None, workspace=None,
+                stream=None):
+    """Adaptive length head forward.  hidden: bf16 [N, k, H], w1: bf16 [H', H],
+    b1, w2: float32 [H'].  Returns (a_hat float32 [N], k_hat int32 [N])."""
+    import torch
+    _need_cuda(hidden, w1, b1, w2)
+    if hidden.dtype != torch.bfloat16 or w1.dtype != torch.bfloat16:
+        raise SvwError("hidden states and W1 must be bfloat16")
+    N, k, H = hidden.shape
+    Hp = w1.shape[0]
+    dev = hidden.device
+    if a_hat is None:
+        a_hat = torch.empty(N, dtype=torch.float32, device=dev)
+    if k_hat is None:
+        k_hat = torch.empty(N, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(1, int(lib().svw_length_head_workspace_size(N, k, Hp))), dtype=torch.uint8,
+                                device=dev)
+    _need_cuda(a_hat, k_hat, workspace)
+    rc = lib().length_head(_ptr(hidden), _ptr(w1), _ptr(b1), _ptr(w2), float(b2), N, k, H, Hp, float(gamma),
+                           _ptr(a_hat), _ptr(k_hat), _ptr(workspace), workspace.numel(), _stream_ptr(stream))
+    _check(rc)
+    return a_hat, k_hat
+
+
+def length_head_label(accept_len, cu_draft, a_hat=None, a_star=None, loss=None, stream=None):
+    """a* = accept_len / L per request and, with a_hat, the MSE (a_hat - a*)^2."""
+    import torch
+    _need_cuda(accept_len, cu_draft, a_hat)
+    N = accept_len.numel()
+    dev = accept_len.device
+    if a_star is None:
+        a_star = torch.empty(N, dtype=torch.float32, device=dev)
+    if a_hat is not None and loss is None:
+        loss = torch.empty(N, dtype=torch.float32, device=dev)
+    _need_cuda(a_star, loss)
+    rc = lib().length_head_label(_ptr(accept_len), _ptr(cu_draft), _ptr(a_hat), N, _ptr(a_star), _ptr(loss),
+                                 _stream_ptr(stream))
+    _check(rc)
+    return a_star, loss
 
 
 def opd_loss(target, draft, temperature: float = 1.0, clip_c: float = 1.0,

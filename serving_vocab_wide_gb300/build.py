@@ -13,8 +13,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libsvw.so")
-SOURCES = ["api.cu", "verify.cu", "opd.cu", "fused.cu", "noalloc.cu"]
-HEADERS = ["svw_device.cuh", "svw_internal.h"]
+SOURCES = ["api.cu", "verify.cu", "opd.cu", "fused.cu", "lengthhead.cu", "noalloc.cu"]
+HEADERS = ["svw_device.cuh", "svw_internal.h", "svw_sample.cuh"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 
@@ -40,7 +40,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
             return LIB_PATH
     tmp = LIB_PATH + f".tmp{os.getpid()}"
     cmd = [_nvcc(), ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
-           "--threads", "0", "-o", tmp] + [os.path.join(CSRC, s) for s in SOURCES]
+           "--threads", "0", "-o", tmp] + [os.path.join(CSRC, s) for s in SOURCES] + ["-lcublasLt"]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     subprocess.run(cmd, check=True, cwd=CSRC)

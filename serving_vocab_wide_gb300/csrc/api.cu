@@ -290,4 +290,38 @@ svw_status spec_verify_opd(const void *target_logits, const void *draft_logits, 
   return e == cudaSuccess ? SVW_OK : SVW_ERR_CUDA;
 }
 
+size_t svw_length_head_workspace_size(int32_t n_requests, int32_t k, int32_t hidden_out) {
+  if (n_requests <= 0 || k <= 0 || k > SVW_MAX_LEN || hidden_out <= 0) return 0;
+  return svw::length_head_gemm_bytes(n_requests, k, hidden_out) + svw::kLengthHeadGemmWorkspace;
+}
+
+svw_status length_head(const void *hidden, const void *w1, const float *b1, const float *w2, float b2, int32_t N,
+                       int32_t k, int32_t H, int32_t hidden_out, float gamma, float *a_hat, int32_t *k_hat,
+                       void *workspace, size_t workspace_bytes, void *stream) {
+  if (N <= 0 || k <= 0 || H <= 0 || hidden_out <= 0) return SVW_ERR_INVALID_ARG;
+  if (k > SVW_MAX_LEN) return SVW_ERR_UNSUPPORTED;
+  if (!hidden || !w1 || !b1 || !w2 || !a_hat || !k_hat) return SVW_ERR_INVALID_ARG;
+  if (!workspace) return SVW_ERR_WORKSPACE;
+  if (!(gamma > 0.f) || !std::isfinite(gamma) || !std::isfinite(b2)) return SVW_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || !aligned(w1, 16) || !aligned(b1, 4) || !aligned(w2, 4) || !aligned(a_hat, 4) ||
+      !aligned(k_hat, 4) || !aligned(workspace, 256))
+    return SVW_ERR_MISALIGNED;
+  if (H % 8 != 0) return SVW_ERR_UNSUPPORTED;  // 16-byte rows for the GEMM
+  if (workspace_bytes < svw_length_head_workspace_size(N, k, hidden_out)) return SVW_ERR_WORKSPACE;
+  const int rc = svw::launch_length_head(hidden, w1, b1, w2, b2, N, k, H, hidden_out, gamma, a_hat, k_hat,
+                                         workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+  return rc == 0 ? SVW_OK : SVW_ERR_CUDA;
+}
+
+svw_status length_head_label(const int32_t *accept_len, const int32_t *cu_draft, const float *a_hat, int32_t N,
+                             float *a_star, float *loss, void *stream) {
+  if (N <= 0 || !accept_len || !cu_draft || !a_star || (loss && !a_hat)) return SVW_ERR_INVALID_ARG;
+  if (!aligned(accept_len, 4) || !aligned(cu_draft, 4) || (a_hat && !aligned(a_hat, 4)) || !aligned(a_star, 4) ||
+      (loss && !aligned(loss, 4)))
+    return SVW_ERR_MISALIGNED;
+  const int rc = svw::launch_length_label(accept_len, cu_draft, a_hat, N, a_star, loss,
+                                          static_cast<cudaStream_t>(stream));
+  return rc == 0 ? SVW_OK : SVW_ERR_CUDA;
+}
+
 }  // extern "C"

@@ -149,3 +149,24 @@ def test_time_next_launch_arming(lib):
     assert lib.svw_time_next_launch(b"x" * 80, p, p) == 1             # name too long
     assert lib.svw_time_next_launch(b"opd_fast_kernel", p, p) == 0
     assert lib.svw_time_next_launch(None, None, None) == 0          # and disarm again
+
+
+def test_length_head_argument_validation(lib):
+    keep, p = _fake(4096)
+
+    def call(**kw):
+        a = dict(h=p, w1=p, b1=p, w2=p, b2=0.0, N=4, k=16, H=64, Hp=8, g=1.0, a=p, kh=p, ws=p, wsb=1 << 30)
+        a.update(kw)
+        return lib.length_head(a["h"], a["w1"], a["b1"], a["w2"], a["b2"], a["N"], a["k"], a["H"], a["Hp"],
+                               a["g"], a["a"], a["kh"], a["ws"], a["wsb"], None)
+
+    assert call(N=0) == 1
+    assert call(k=40) == 2                  # above SVW_MAX_LEN
+    assert call(h=None) == 1
+    assert call(ws=None) == 4
+    assert call(wsb=1024) == 4
+    assert call(g=0.0) == 1
+    assert call(H=60) == 2                  # rows must be 16-byte pitched
+    assert call(h=ctypes.c_void_p(p.value + 8)) == 3
+    assert lib.svw_length_head_workspace_size(256, 16, 256) > (4 << 20)
+    assert lib.svw_length_head_workspace_size(0, 16, 256) == 0

@@ -1,0 +1,98 @@
+"""GPU parity: the adaptive length head (forward and label) against the oracle.
+
+a_hat within 1e-4 (absolute; it is a probability), k_hat bit-exact except
+where the oracle flags gamma a_hat k within 1e-4 of an integer (the floor
+could go either way under float rounding); the label within fp32 rounding of
+what the oracle computes from the same a_hat.
+"""
+import numpy as np
+import pytest
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    import serving_vocab_wide_gb300 as svw
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+    svw.build()
+    svw.lib()
+
+
+def _bf16_bits(x):
+    x = np.ascontiguousarray(x, np.float32)
+    u = x.view(np.uint32)
+    r = u + 0x7FFF + ((u >> 16) & 1)  # round to nearest even
+    return (r >> 16).astype(np.uint16)
+
+
+def _inputs(seed, N, k, H, Hp):
+    rng = np.random.default_rng(seed)
+    h = _bf16_bits(rng.normal(size=(N, k, H)))
+    w1 = _bf16_bits(rng.normal(size=(Hp, H)) / np.sqrt(H) * 2.0)
+    b1 = rng.normal(0, 0.3, size=Hp).astype(np.float32)
+    w2 = (rng.normal(size=Hp) / np.sqrt(Hp) * 2.0).astype(np.float32)
+    return h, w1, b1, w2
+
+
+def _gpu(h, w1, b1, w2, b2, gamma):
+    import torch
+    import serving_vocab_wide_gb300 as svw
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    hb = t(h.view(np.int16)).view(torch.bfloat16)
+    wb = t(w1.view(np.int16)).view(torch.bfloat16)
+    a, kh = svw.length_head(hb, wb, t(b1), t(w2), b2, gamma)
+    return a.cpu().numpy(), kh.cpu().numpy()
+
+
+def _compare(a, kh, ref, label):
+    assert np.all(np.abs(a.astype(np.float64) - ref["a_hat"]) <= 1e-4), \
+        f"{label}: a_hat err {np.abs(a - ref['a_hat']).max()}"
+    ok = (ref["flags"] & oracle.FLAG_NEAR_FLOOR) == 0
+    assert np.array_equal(kh[ok], ref["k_hat"][ok]), label
+    assert np.all((kh >= 1) & (kh <= 16))
+
+
+@pytest.mark.parametrize("N,k,H,Hp,b2,gamma", [(5, 16, 256, 32, 0.5, 1.0), (9, 7, 512, 64, -0.8, 1.3),
+                                               (3, 1, 64, 8, 2.0, 0.7), (33, 16, 1024, 128, 0.0, 1.0)])
+def test_small_shapes(N, k, H, Hp, b2, gamma):
+    h, w1, b1, w2 = _inputs(N * 7 + H, N, k, H, Hp)
+    a, kh = _gpu(h, w1, b1, w2, b2, gamma)
+    _compare(a, kh, oracle.length_head(h, w1, b1, w2, b2, gamma), f"N={N} H={H}")
+
+
+def test_drafter_scale_sampled():
+    """N = 256 requests, k = 16, H = 4096 (drafter hidden size), H' = 256:
+    the whole batch on the GPU, 12 sampled requests through the oracle."""
+    N, k, H, Hp = 256, 16, 4096, 256
+    h, w1, b1, w2 = _inputs(77, N, k, H, Hp)
+    a, kh = _gpu(h, w1, b1, w2, 0.2, 1.0)
+    rows = np.sort(np.random.default_rng(5).choice(N, 12, replace=False))
+    ref = oracle.length_head(h[rows], w1, b1, w2, 0.2, 1.0)
+    _compare(a[rows], kh[rows], ref, "drafter scale")
+    assert len(np.unique(kh)) > 3  # the lengths actually vary
+
+
+def test_label():
+    import torch
+    import serving_vocab_wide_gb300 as svw
+    rng = np.random.default_rng(9)
+    N = 300
+    L = rng.integers(1, 17, size=N)
+    cu = np.concatenate([[0], np.cumsum(L)]).astype(np.int32)
+    acc = rng.integers(0, L + 1).astype(np.int32)
+    acc[[3, 17]] = -1
+    a_hat = rng.uniform(0, 1, size=N).astype(np.float32)
+    t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    a_star, loss = svw.length_head_label(t(acc), t(cu), t(a_hat))
+    ref = oracle.length_label(acc, cu, a_hat.astype(np.float64))
+    a_star, loss = a_star.cpu().numpy(), loss.cpu().numpy()
+    ok = acc >= 0
+    assert np.allclose(a_star[ok], ref["a_star"][ok], rtol=0, atol=1e-7)
+    # (a_hat - a*)^2 in fp32: a* and the difference each round once, so the
+    # error is about 2 |a_hat - a*| 2^-24 <= 2.4e-7, absolute
+    assert np.all(np.abs(loss[ok] - ref["loss"][ok]) <= 1e-6)
+    assert np.all(np.isnan(a_star[~ok])) and np.all(np.isnan(loss[~ok]))
