@@ -4,7 +4,10 @@ Workload (default "mix"): N = 256 requests, L_i ~ U{2,4,8,16} packed by CSR
 offsets, V = 151936, bf16 logits (log-Zipf target + Gaussian draft noise).
 One step = spec_verify at T = 0 and 0.6, and spec_verify_opd at T = 1 --
 verification plus the OPD loss (T = 1, c = 1, lambda = 0.1, forward +
-gradient) on the same batch in one pass: every step of the path, three
+gradient) on the same batch in one pass -- then the adaptive length head:
+its label from this round's accepted lengths and its forward pass for the
+next round's verified lengths (k = 16, drafter hidden H = 4096, H' = 256,
+synthetic hidden states and random weights).  Every step of the path, three
 verifications and one loss per step.  The separate T = 1 spec_verify and
 opd_loss calls are timed beside it for comparison.
 
@@ -99,11 +102,15 @@ CALL_KERNELS = {
     "spec_verify": "verify_stats + verify_finalize (accept tests and, at T > 0, the inverse-CDF draw)",
     "opd_loss": "opd_fast_kernel + opd_fix_kernel",
     "spec_verify_opd": "opd_fast_kernel (draft rows + bonus rows) + fused_finalize (accept tests, draw) + opd_fix_kernel",
+    "length_head": "length_head_label + length_head_gemm (cuBLASLt bf16 GEMM) + length_head_epilogue",
 }
-CALLS = ["verify_T0", "verify_T0.6", "verify_T1+opd"]
+CALLS = ["verify_T0", "verify_T0.6", "verify_T1+opd", "length_head"]
+HEAD = dict(k=16, H=4096, Hp=256, gamma=1.0)
 WORKLOAD = ("mix: N=256 ragged L_i~U{2,4,8,16}, V=151936, bf16 log-Zipf logits; verify at T=0 and 0.6, "
-            "verify at T=1 fused with OPD fwd/bwd (T=1,c=1,lambda=0.1)")
-CALL_API = {"verify_T0": "spec_verify", "verify_T0.6": "spec_verify", "verify_T1+opd": "spec_verify_opd"}
+            "verify at T=1 fused with OPD fwd/bwd (T=1,c=1,lambda=0.1); length head label + forward "
+            "(k=16, H=4096, H'=256)")
+CALL_API = {"verify_T0": "spec_verify", "verify_T0.6": "spec_verify", "verify_T1+opd": "spec_verify_opd",
+            "length_head": "length_head"}
 
 
 def _profile_traffic(kernel: str, workload: str):
@@ -120,6 +127,15 @@ def _profile_traffic(kernel: str, workload: str):
             except (KeyError, ValueError):
                 return None
     return None
+
+
+def _peak_tflops():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"])
+    except (OSError, KeyError, ValueError):
+        return 1900.0
 
 
 def _peaks():
@@ -191,8 +207,9 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 def launches_per_step():
     """Kernels one step launches: spec_verify = stats + finalize, twice;
-    spec_verify_opd = fast pass + finalize + fix-up."""
-    return 2 + 2 + 3
+    spec_verify_opd = fast pass + finalize + fix-up; length head = label +
+    epilogue (the GEMM's kernels belong to cuBLASLt and are not counted)."""
+    return 2 + 2 + 3 + 2
 
 
 def run_native(args, ws, rank, local):
@@ -226,6 +243,19 @@ def run_native(args, ws, rank, local):
     wsp = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     opd_ws = torch.empty(svw.opd_workspace_size(R), dtype=torch.uint8, device=dev)
     fused_ws = torch.empty(svw.verify_opd_workspace_size(N, R, V, svw.SVW_BF16), dtype=torch.uint8, device=dev)
+    # adaptive length head: synthetic drafter hidden states and random weights
+    hk, hH, hHp = HEAD["k"], HEAD["H"], HEAD["Hp"]
+    g = torch.Generator().manual_seed(2000 + rank)
+    h_hid = torch.randn(N, hk, hH, generator=g).to(torch.bfloat16).pin_memory()
+    hid = h_hid.to(dev)
+    w1 = (torch.randn(hHp, hH, generator=g) * (2.0 / hH ** 0.5)).to(torch.bfloat16).to(dev)
+    b1 = (torch.randn(hHp, generator=g) * 0.3).to(dev)
+    w2 = (torch.randn(hHp, generator=g) * (2.0 / hHp ** 0.5)).to(dev)
+    head_ws = torch.empty(svw.lib().svw_length_head_workspace_size(N, hk, hHp), dtype=torch.uint8, device=dev)
+    a_hat = torch.empty(N, dtype=torch.float32, device=dev)
+    k_hat = torch.empty(N, dtype=torch.int32, device=dev)
+    a_star = torch.empty(N, dtype=torch.float32, device=dev)
+    len_loss = torch.empty(N, dtype=torch.float32, device=dev)
     acc = {T: torch.empty(N, dtype=torch.int32, device=dev) for T in TEMPS}
     nxt = {T: torch.empty(N, dtype=torch.int32, device=dev) for T in TEMPS}
     loss = torch.empty(R, dtype=torch.float32, device=dev)
@@ -245,10 +275,18 @@ def run_native(args, ws, rank, local):
                             dlogits=grad, status=status, workspace=fused_ws, stream=stream)
 
     # the main kernel of each call, timed inside the call (svw_time_next_launch)
-    call_kernel = {"verify_T0": "verify_stats", "verify_T0.6": "verify_stats", "verify_T1+opd": "opd_fast_kernel"}
+    call_kernel = {"verify_T0": "verify_stats", "verify_T0.6": "verify_stats", "verify_T1+opd": "opd_fast_kernel",
+                   "length_head": "length_head_gemm"}
+
+    def head():
+        # this round's label (T = 1 accepted lengths against last round's a_hat), then the
+        # forward pass that sets the next round's verified lengths
+        svw.length_head_label(acc[1.0], cu, a_hat, a_star=a_star, loss=len_loss, stream=stream)
+        svw.length_head(hid, w1, b1, w2, 0.2, HEAD["gamma"], a_hat=a_hat, k_hat=k_hat, workspace=head_ws,
+                        stream=stream)
 
     def step(ev=None, kev=None):
-        for ci, fn in enumerate((lambda: verify(0.0), lambda: verify(0.6), verify_opd)):
+        for ci, fn in enumerate((lambda: verify(0.0), lambda: verify(0.6), verify_opd, head)):
             if kev is not None:
                 svw.time_next_launch(call_kernel[calls[ci]], kev[2 * ci], kev[2 * ci + 1])
             if ev is not None:
@@ -304,7 +342,8 @@ def run_native(args, ws, rank, local):
            "verify_T0.6": (rows_t + R) * V * es,
            "verify_T1+opd": (rows_t + R) * V * es + R * V * 4,
            "verify_T1": (rows_t + R) * V * es,
-           "opd": 2 * R * V * es + R * V * 4}
+           "opd": 2 * R * V * es + R * V * 4,
+           "length_head": N * hk * hH * 2 + hHp * hH * 2 + N * hk * hHp * 4 * 2}
     ms_per_step = elapsed_ms / K
     value = job_positions / (elapsed_ms / K / 1000.0)
     step_bytes = sum(alg[c] for c in calls)
@@ -312,8 +351,10 @@ def run_native(args, ws, rank, local):
     # the dominant kernel: the longest main kernel of a call, timed on the
     # launch stream inside the call; its algorithmic bytes
     kalg = {"verify_T0": alg["verify_T0"], "verify_T0.6": alg["verify_T0.6"],
-            "verify_T1+opd": 2 * R * V * es + R * V * 4 + N * V * es}
-    dom = max(calls, key=lambda c: kern_us[c])
+            "verify_T1+opd": 2 * R * V * es + R * V * 4 + N * V * es,
+            "length_head": N * hk * hH * 2 + hHp * hH * 2 + N * hk * hHp * 4}
+    head_flops = 2.0 * N * hk * hH * hHp
+    dom = max((c for c in calls if c != "length_head"), key=lambda c: kern_us[c])
     dom_kernel = call_kernel[dom]
     achieved = kalg[dom] / (kern_us[dom] * 1e-6) / 1e9
     traffic = _profile_traffic(dom_kernel, f"mix:{dom}")
@@ -340,6 +381,7 @@ def run_native(args, ws, rank, local):
     h_acc = {T: torch.empty(N, dtype=torch.int32).pin_memory() for T in TEMPS}
     h_nxt = {T: torch.empty(N, dtype=torch.int32).pin_memory() for T in TEMPS}
     h_loss = torch.empty(R, dtype=torch.float32).pin_memory()
+    h_khat = torch.empty(N, dtype=torch.int32).pin_memory()
 
     def e2e_step():
         t.copy_(h_t, non_blocking=True)
@@ -347,11 +389,13 @@ def run_native(args, ws, rank, local):
         cu.copy_(h_cu, non_blocking=True)
         for T in TEMPS:
             tok[T].copy_(h_tok[T], non_blocking=True)
+        hid.copy_(h_hid, non_blocking=True)
         step()
         for T in TEMPS:
             h_acc[T].copy_(acc[T], non_blocking=True)
             h_nxt[T].copy_(nxt[T], non_blocking=True)
         h_loss.copy_(loss, non_blocking=True)
+        h_khat.copy_(k_hat, non_blocking=True)
 
     e2e_step()
     torch.cuda.synchronize()
@@ -364,8 +408,9 @@ def run_native(args, ws, rank, local):
     f1.record(stream)
     torch.cuda.synchronize()
     e2e_ms, _ = reduce_over_ranks(ws, dev, f0.elapsed_time(f1), positions_per_step)
-    h2d = (h_t.numel() + h_d.numel()) * 2 + h_cu.numel() * 4 + sum(v.numel() * 4 for v in h_tok.values())
-    d2h = 2 * 3 * N * 4 + R * 4
+    h2d = ((h_t.numel() + h_d.numel()) * 2 + h_cu.numel() * 4 + sum(v.numel() * 4 for v in h_tok.values())
+           + h_hid.numel() * 2)
+    d2h = 2 * 3 * N * 4 + R * 4 + N * 4
     e2e = {"value": job_positions / (e2e_ms / Ke / 1000.0), "unit": UNIT,
            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": Ke}
 
@@ -387,6 +432,10 @@ def run_native(args, ws, rank, local):
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "algorithmic_bytes_per_launch": kalg[dom], "avg_launch_us": kern_us[dom]},
+        "length_head_gemm": {"tflops": head_flops / (kern_us["length_head"] * 1e-6) / 1e12,
+                             "avg_us": kern_us["length_head"], "unit": "TFLOP/s",
+                             "peak_bf16": _peak_tflops(), "frac": head_flops / (kern_us["length_head"] * 1e-6)
+                             / 1e12 / _peak_tflops()},
         "calls": {c: {"api": CALL_API[c], "kernels": CALL_KERNELS[CALL_API[c]], "avg_us": avg_us[c],
                       "gbs": alg[c] / (avg_us[c] * 1e-6) / 1e9,
                       "frac_of_peak": alg[c] / (avg_us[c] * 1e-6) / 1e9 / peak,
