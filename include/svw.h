@@ -117,6 +117,41 @@ svw_status spec_verify(const void *target_logits, const void *draft_logits, svw_
                        void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * spec_verify_early -- spec_verify that stops reading a request at its first
+ * rejection.
+ *
+ * Leftmost rejection ("DFlash 阅读笔记：并行起草、目标特征与精确验证" §5.2,
+ * Algorithm 1) makes every row after a request's first rejected position
+ * irrelevant to its result, and acceptance falls with the position
+ * ("AdaFlash：基于在策略蒸馏扩散草稿器的自适应投机解码" §3.3, Figure 2(c):
+ * from about 0.9 at the first position to 0.13-0.26 at the fifteenth).  The
+ * rows are streamed position by position across the batch and each accept
+ * test runs as soon as its two rows are reduced; rows at positions after a
+ * known rejection are skipped.  Which later rows still get read depends on
+ * timing, the results do not.
+ *
+ * Arguments and results as for spec_verify (same accept_len and next_token,
+ * bit for bit, same uniforms), with these differences:
+ *   - a request is bad (accept_len = next_token = -1) if a row at or before
+ *     its first rejected position (the bonus row when none is rejected) is
+ *     non-finite, or if any of its tokens is out of range; rows after the
+ *     first rejection are not checked (they need not be read);
+ *   bytes_read    device uint64 scalar out, may be NULL: the logit bytes this
+ *                 call streamed from the two tensors (without the one row
+ *                 pair the draw reads again).  Reset by the call.  8-byte
+ *                 aligned.
+ *   workspace     >= svw_verify_early_workspace_size(...) bytes.
+ */
+size_t svw_verify_early_workspace_size(int32_t n_requests, int64_t total_draft_rows, int32_t V,
+                                       svw_dtype dtype);
+
+svw_status spec_verify_early(const void *target_logits, const void *draft_logits, svw_dtype dtype, int32_t V,
+                             int32_t N, const int32_t *cu_draft, int64_t total_draft_rows, int32_t max_len,
+                             const int32_t *draft_tokens, float temperature, uint64_t seed, int32_t *accept_len,
+                             int32_t *next_token, int32_t *status, unsigned long long *bytes_read,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * opd_loss -- per draft row r (0 <= r < total_draft_rows), paired with one
  * target row:
  *   lp = log softmax(target/T), lq = log softmax(draft/T), q = exp(lq)
@@ -264,10 +299,10 @@ svw_status spec_verify_noalloc(const void *target_logits, const void *draft_logi
 /*
  * svw_time_next_launch -- measurement hook, not part of the method.  Arms a
  * one-shot timer on the calling host thread: the next launch of the named
- * kernel made from this thread ("verify_stats", "verify_finalize",
- * "opd_fast_kernel", "opd_fix_kernel", "opd_exact_kernel", "fused_finalize",
- * "length_head_gemm", "length_head_epilogue") records begin_event just before it and end_event just
- * after it on the launch stream (cudaEvent_t handles passed as void*, owned
+ * kernel made from this thread ("early_plan", "verify_stats",
+ * "verify_finalize", "opd_fast_kernel", "opd_fix_kernel", "opd_exact_kernel",
+ * "fused_finalize", "length_head_gemm", "length_head_epilogue") records
+ * begin_event just before it and end_event just after it on the launch stream (cudaEvent_t handles passed as void*, owned
  * by the caller).  kernel = NULL disarms.  The library records nothing
  * unless armed.  Lets a benchmark time one kernel of a multi-kernel call with
  * CUDA events on the launch stream.

@@ -78,11 +78,15 @@ size_t svw_verify_workspace_size(int32_t n_requests, int64_t total_draft_rows, i
   return svw::verify_layout(n_requests, total_draft_rows, V, esize_of(dtype)).total;
 }
 
-svw_status spec_verify(const void *target_logits, const void *draft_logits, svw_dtype dtype,
-                       int32_t V, int32_t N, const int32_t *cu_draft, int64_t total_draft_rows,
-                       int32_t max_len, const int32_t *draft_tokens, float temperature,
-                       uint64_t seed, int32_t *accept_len, int32_t *next_token, int32_t *status,
-                       void *workspace, size_t workspace_bytes, void *stream) {
+}  // extern "C"
+
+// spec_verify and spec_verify_early: same validation, same results
+static svw_status verify_entry(bool early, const void *target_logits, const void *draft_logits, svw_dtype dtype,
+                               int32_t V, int32_t N, const int32_t *cu_draft, int64_t total_draft_rows,
+                               int32_t max_len, const int32_t *draft_tokens, float temperature, uint64_t seed,
+                               int32_t *accept_len, int32_t *next_token, int32_t *status,
+                               unsigned long long *bytes_read, void *workspace, size_t workspace_bytes,
+                               void *stream) {
   if (dtype != SVW_F32 && dtype != SVW_BF16) return SVW_ERR_UNSUPPORTED;
   if (V <= 0 || N <= 0 || total_draft_rows < 0 || max_len < 1) return SVW_ERR_INVALID_ARG;
   if (max_len > SVW_MAX_LEN || V > kMaxV) return SVW_ERR_UNSUPPORTED;
@@ -95,16 +99,18 @@ svw_status spec_verify(const void *target_logits, const void *draft_logits, svw_
   const int es = esize_of(dtype);
   if (!aligned(target_logits, es) || !aligned(draft_logits, es) || !aligned(cu_draft, 4) ||
       !aligned(draft_tokens, 4) || !aligned(accept_len, 4) || !aligned(next_token, 4) ||
-      (status && !aligned(status, 4)) || !aligned(workspace, 256))
+      (status && !aligned(status, 4)) || (bytes_read && !aligned(bytes_read, 8)) || !aligned(workspace, 256))
     return SVW_ERR_MISALIGNED;
   const svw::VerifyLayout lay = svw::verify_layout(N, total_draft_rows, V, es);
-  if (workspace_bytes < lay.total) return SVW_ERR_WORKSPACE;
+  const svw::EarlyLayout elay = svw::early_layout(N, total_draft_rows, V, es);
+  if (early && total_draft_rows + N >= (int64_t{1} << 31)) return SVW_ERR_UNSUPPORTED;  // int32 row records
+  if (workspace_bytes < (early ? elay.total : lay.total)) return SVW_ERR_WORKSPACE;
 
   const svw::ChunkPlan plan = svw::plan_chunks(V, es);
   const bool greedy = (temperature == 0.f);
   const bool vec = ((static_cast<int64_t>(V) * es) % 16 == 0) && aligned(target_logits, 16) &&
                    aligned(draft_logits, 16);
-  svw::VerifyArgs a;
+  svw::VerifyArgs a{};
   a.target = target_logits;
   a.draft = draft_logits;
   a.V = V;
@@ -127,8 +133,54 @@ svw_status spec_verify(const void *target_logits, const void *draft_logits, svw_
   a.chunk_len = plan.chunk_len;
   const int64_t rows = greedy ? (total_draft_rows + N) : (2 * total_draft_rows + N);
   a.total_items = rows * plan.C;
-  const cudaError_t e = svw::launch_verify(a, dtype, vec, greedy, static_cast<cudaStream_t>(stream));
+  cudaError_t e;
+  if (early) {
+    a.cnt = reinterpret_cast<int32_t *>(ws + elay.cnt_off);
+    a.rej = reinterpret_cast<int32_t *>(ws + elay.rej_off);
+    a.badpos = reinterpret_cast<int32_t *>(ws + elay.badpos_off);
+    a.stop = reinterpret_cast<int32_t *>(ws + elay.stop_off);
+    a.pinfo = reinterpret_cast<int4 *>(ws + elay.pinfo_off);
+    a.W = reinterpret_cast<int64_t *>(ws + elay.wave_off);
+    a.waveA = reinterpret_cast<int32_t *>(ws + elay.wave_off + (SVW_MAX_LEN + 2) * sizeof(int64_t));
+    a.nvalid = a.waveA + (SVW_MAX_LEN + 1);
+    a.qnext = a.nvalid + 1;
+    a.eres = reinterpret_cast<int4 *>(ws + elay.eres_off);
+    a.erow = reinterpret_cast<float4 *>(ws + elay.erow_off);
+    a.bytes_read = bytes_read;
+    e = svw::launch_verify_early(a, dtype, vec, greedy, static_cast<cudaStream_t>(stream));
+  } else {
+    e = svw::launch_verify(a, dtype, vec, greedy, static_cast<cudaStream_t>(stream));
+  }
   return e == cudaSuccess ? SVW_OK : SVW_ERR_CUDA;
+}
+
+extern "C" {
+
+svw_status spec_verify(const void *target_logits, const void *draft_logits, svw_dtype dtype,
+                       int32_t V, int32_t N, const int32_t *cu_draft, int64_t total_draft_rows,
+                       int32_t max_len, const int32_t *draft_tokens, float temperature,
+                       uint64_t seed, int32_t *accept_len, int32_t *next_token, int32_t *status,
+                       void *workspace, size_t workspace_bytes, void *stream) {
+  return verify_entry(false, target_logits, draft_logits, dtype, V, N, cu_draft, total_draft_rows, max_len,
+                      draft_tokens, temperature, seed, accept_len, next_token, status, nullptr, workspace,
+                      workspace_bytes, stream);
+}
+
+size_t svw_verify_early_workspace_size(int32_t n_requests, int64_t total_draft_rows, int32_t V,
+                                       svw_dtype dtype) {
+  if (n_requests <= 0 || total_draft_rows < 0 || V <= 0 || V > kMaxV) return 0;
+  if (dtype != SVW_F32 && dtype != SVW_BF16) return 0;
+  return svw::early_layout(n_requests, total_draft_rows, V, esize_of(dtype)).total;
+}
+
+svw_status spec_verify_early(const void *target_logits, const void *draft_logits, svw_dtype dtype, int32_t V,
+                             int32_t N, const int32_t *cu_draft, int64_t total_draft_rows, int32_t max_len,
+                             const int32_t *draft_tokens, float temperature, uint64_t seed, int32_t *accept_len,
+                             int32_t *next_token, int32_t *status, unsigned long long *bytes_read,
+                             void *workspace, size_t workspace_bytes, void *stream) {
+  return verify_entry(true, target_logits, draft_logits, dtype, V, N, cu_draft, total_draft_rows, max_len,
+                      draft_tokens, temperature, seed, accept_len, next_token, status, bytes_read, workspace,
+                      workspace_bytes, stream);
 }
 
 // OPD workspace: flags int32 [R] | row constants float4 [R], each 256-aligned

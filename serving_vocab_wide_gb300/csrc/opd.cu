@@ -615,23 +615,6 @@ __device__ __forceinline__ bool last_warp_all(uint32_t *cnt, int64_t it) {
   return last;
 }
 
-// named barriers: warps 1..15 arrive, warp 0 waits (only warp 0 acts on them)
-__device__ __forceinline__ void named_arrive(int id, int nt) { asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nt) : "memory"); }
-__device__ __forceinline__ void named_sync(int id, int nt) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nt) : "memory"); }
-// shared::cluster address of the same shared variable in CTA `rank`
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-  return r;
-}
-
-// 16-byte store into a peer's shared memory that completes 16 bytes of the
-// transaction count of the peer's mbarrier (no fence, no cluster barrier)
-__device__ __forceinline__ void st_async16(uint32_t dst, const uint4 &v, uint32_t mbar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(dst),
-               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(mbar)
-               : "memory");
-}
 
 template <int DT, int VPT, int NT>
 __global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) {

@@ -139,6 +139,47 @@ __device__ __forceinline__ bool mbar_wait_bounded(unsigned long long *bar, uint3
     if (clock64() - t0 > kWaitCycles) return false;
   return true;
 }
+// the accept test u < min(1, p(x)/q(x)) of speculative verification from the
+// raw logits at x and the row statistics (m: maximum, l = log2 of the sum of
+// 2^((x - m) k)): log2 p(x) = (y_x - m_T) k - l_T, log2 q(x) = (z_x - m_D) k - l_D
+__device__ __forceinline__ bool accept_token(float u, float yx, float zx, float mT, float lT, float mD, float lD,
+                                             float k) {
+  float thr;
+  if (zx == -INFINITY) {
+    thr = 1.f;  // q(x) = 0: accept
+  } else {
+    const float dl = __fsub_rn(__fmul_rn(__fsub_rn(__fsub_rn(yx, mT), __fsub_rn(zx, mD)), k), __fsub_rn(lT, lD));
+    thr = (dl >= 0.f) ? 1.f : ex2(dl);
+  }
+  return u < thr;
+}
+
+// ---------------------------------------------------------------------------
+// thread-block clusters: named barriers, peer shared memory, async stores
+// ---------------------------------------------------------------------------
+// named barriers: some warps arrive, others wait
+__device__ __forceinline__ void named_arrive(int id, int nt) { asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nt) : "memory"); }
+__device__ __forceinline__ void named_sync(int id, int nt) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nt) : "memory"); }
+// shared::cluster address of the same shared variable in CTA `rank`
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// 16-byte store into a peer's shared memory that completes 16 bytes of the
+// transaction count of the peer's mbarrier (no fence, no cluster barrier)
+__device__ __forceinline__ void st_async16(uint32_t dst, const uint4 &v, uint32_t mbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(dst),
+               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(mbar)
+               : "memory");
+}
+// the same for one 32-bit word (4 bytes of the transaction count)
+__device__ __forceinline__ void st_async4(uint32_t dst, uint32_t v, uint32_t mbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(dst), "r"(v),
+               "r"(mbar)
+               : "memory");
+}
+
 // 1-D bulk asynchronous copy global -> this CTA's shared memory, completion
 // counted (in bytes) on the mbarrier
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
@@ -256,6 +297,117 @@ __device__ __forceinline__ uint32_t philox_word0(uint64_t seed, uint32_t c0, uin
 __device__ __forceinline__ float philox_uniform(uint64_t seed, uint32_t i, uint32_t j,
                                                 uint32_t stream) {
   return static_cast<float>(philox_word0(seed, i, j, stream) >> 8) * (1.0f / 16777216.0f);
+}
+
+// ---------------------------------------------------------------------------
+// warp reductions over a span of 16-byte vectors held in shared memory (warp
+// wid of CW reads vectors vi = wid*32 + lane + q*CW*32)
+// ---------------------------------------------------------------------------
+template <int DT, int CW>
+__device__ __forceinline__ void warp_lse_smem(uint32_t base, int nvec, int wid, int lane, float k,
+                                              float &m, float &s) {
+  const int v0 = wid * 32 + lane;
+  float mx = -INFINITY;
+  if (DT == 1) {
+    uint32_t mw = 0xff80ff80u;  // (-inf, -inf)
+    for (int vi = v0; vi < nvec; vi += CW * 32) {
+      const uint4 q = lds128(base + vi * 16);
+      mw = bf16x2_max(mw, bf16x2_max(bf16x2_max(q.x, q.y), bf16x2_max(q.z, q.w)));
+    }
+    const float2 f = bf16x2_f2(mw);
+    mx = fmaxf(f.x, f.y);
+  } else {
+    for (int vi = v0; vi < nvec; vi += CW * 32) {
+      const uint4 q = lds128(base + vi * 16);
+      mx = fmaxf(fmaxf(mx, fmaxf(__uint_as_float(q.x), __uint_as_float(q.y))),
+                 fmaxf(__uint_as_float(q.z), __uint_as_float(q.w)));
+    }
+  }
+  // one reference for the whole warp, so the lane sums add directly
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  const float mref = (mx == -INFINITY) ? 0.f : mx;
+  const float2 nm = make_float2(-mref, -mref), kk = make_float2(k, k);
+  float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+  for (int vi = v0; vi < nvec; vi += CW * 32) {
+    const uint4 q = lds128(base + vi * 16);
+    if (DT == 1) {
+      const float2 d0 = __fmul2_rn(__fadd2_rn(bf16x2_f2(q.x), nm), kk);  // (x - max) exact, then * log2e/T
+      const float2 d1 = __fmul2_rn(__fadd2_rn(bf16x2_f2(q.y), nm), kk);
+      const float2 d2 = __fmul2_rn(__fadd2_rn(bf16x2_f2(q.z), nm), kk);
+      const float2 d3 = __fmul2_rn(__fadd2_rn(bf16x2_f2(q.w), nm), kk);
+      acc0 = __fadd2_rn(acc0, __fadd2_rn(make_float2(ex2(d0.x), ex2(d0.y)), make_float2(ex2(d1.x), ex2(d1.y))));
+      acc1 = __fadd2_rn(acc1, __fadd2_rn(make_float2(ex2(d2.x), ex2(d2.y)), make_float2(ex2(d3.x), ex2(d3.y))));
+    } else {
+      const float2 d0 = __fmul2_rn(__fadd2_rn(make_float2(__uint_as_float(q.x), __uint_as_float(q.y)), nm), kk);
+      const float2 d1 = __fmul2_rn(__fadd2_rn(make_float2(__uint_as_float(q.z), __uint_as_float(q.w)), nm), kk);
+      acc0 = __fadd2_rn(acc0, make_float2(ex2(d0.x), ex2(d0.y)));
+      acc1 = __fadd2_rn(acc1, make_float2(ex2(d1.x), ex2(d1.y)));
+    }
+  }
+  const float2 acc = __fadd2_rn(acc0, acc1);
+  s = warp_sum(__fadd_rn(acc.x, acc.y));
+  m = mx;
+  if (!(mx == mx)) s = mx;  // all-NaN warp: keep the NaN visible
+}
+
+template <int DT, int CW>
+__device__ __forceinline__ void warp_amax_smem(uint32_t base, int nvec, int32_t c0, int wid, int lane,
+                                               float &best, int32_t &idx, int32_t &nan) {
+  using E = Elem<DT>;
+  constexpr int EPV = E::kPerVec;
+  const int v0 = wid * 32 + lane;
+  float mx = -INFINITY;
+  int bvi = (v0 < nvec) ? v0 : -1;  // this lane's first vector holding its maximum (-inf rows: the first)
+  uint32_t nanw = 0;
+  if (DT == 1) {
+    for (int vi = v0; vi < nvec; vi += CW * 32) {
+      const uint4 q = lds128(base + vi * 16);
+      // NaN-propagating max of the vector: a NaN anywhere survives
+      const uint32_t m2 = bf16x2_max_nan(bf16x2_max_nan(q.x, q.y), bf16x2_max_nan(q.z, q.w));
+      nanw |= bf16x2_nan(m2);
+      const float2 f = bf16x2_f2(m2);
+      const float vm = fmaxf(f.x, f.y);
+      if (vm > mx) {
+        mx = vm;
+        bvi = vi;
+      }
+    }
+  } else {
+    for (int vi = v0; vi < nvec; vi += CW * 32) {
+      const uint4 q = lds128(base + vi * 16);
+      const float x[4] = {__uint_as_float(q.x), __uint_as_float(q.y), __uint_as_float(q.z),
+                          __uint_as_float(q.w)};
+      float vm = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        nanw |= (x[e] != x[e]);
+        vm = fmaxf(vm, x[e]);
+      }
+      if (vm > mx) {
+        mx = vm;
+        bvi = vi;
+      }
+    }
+  }
+  float wmx = mx;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) wmx = fmaxf(wmx, __shfl_xor_sync(0xffffffffu, wmx, o));
+  // only lanes holding the warp maximum look for its first index, in the
+  // one vector where their maximum first appeared (each lane's vectors are in
+  // index order, lanes interleave by vector)
+  idx = INT32_MAX;
+  if (mx == wmx && bvi >= 0) {
+    float x[EPV];
+    E::unpack(lds128(base + bvi * 16), x);
+#pragma unroll
+    for (int e = EPV - 1; e >= 0; --e)
+      if (x[e] == wmx) idx = c0 + bvi * EPV + e;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) idx = min(idx, __shfl_xor_sync(0xffffffffu, idx, o));
+  best = wmx;
+  nan = __any_sync(0xffffffffu, nanw != 0) ? 1 : 0;
 }
 
 }  // namespace svw

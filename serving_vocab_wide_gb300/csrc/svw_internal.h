@@ -59,10 +59,40 @@ struct VerifyArgs {
   int32_t C;
   int32_t chunk_len;
   int64_t total_items;
+  // early exit (spec_verify_early); unused otherwise
+  int32_t *cnt;                    // [N * max_len] partials delivered per accept test (by slot)
+  int32_t *rej;                    // [N] first rejected position found (INT32_MAX: none yet)
+  int32_t *badpos;                 // [N] first position with a bad row or token found
+  int32_t *stop;                   // [N] by slot: first position that stops the request
+  int4 *pinfo;                     // [valid requests] {request, first draft row, L, 0}, longest first
+  int64_t *W;                      // [max_len + 2] first item of each position wave
+  int32_t *waveA;                  // [max_len + 1] requests longer than each position
+  unsigned long long *bytes_read;  // logit bytes streamed (may be NULL)
+  int32_t *nvalid;                 // valid requests (the plan's record count)
+  int32_t *qnext;                  // cluster path: next record slot to hand out
+  int4 *eres;                      // cluster path, per request: {stop position, bad, greedy argmax, 0}
+  float4 *erow;                    // cluster path, per request: {m_T, l_T, m_D, l_D} at the stop position
 };
 
 cudaError_t launch_verify(const VerifyArgs &a, int dtype, bool vec, bool greedy,
                           cudaStream_t stream);
+// workspace of spec_verify_early: spec_verify's, then the early-exit state
+struct EarlyLayout {
+  size_t part_off, csr_bad_off, cnt_off, rej_off, badpos_off, stop_off, pinfo_off, wave_off, eres_off, erow_off,
+      total;
+};
+// the cluster path of spec_verify_early (early.cu): CL = 0 if not applicable
+struct EarlyClusterPlan {
+  int CL;
+  int SL;
+  int slice_bytes;
+  size_t smem;
+};
+EarlyClusterPlan early_cluster_plan(int64_t V, int esize, bool greedy);
+cudaError_t launch_early_cluster(const VerifyArgs &a, int dtype, bool greedy, const EarlyClusterPlan &p,
+                                 cudaStream_t stream);
+EarlyLayout early_layout(int32_t N, int64_t total_rows, int64_t V, int esize);
+cudaError_t launch_verify_early(const VerifyArgs &a, int dtype, bool vec, bool greedy, cudaStream_t stream);
 // workspace of spec_verify_opd (fused verification + OPD)
 struct FusedLayout {
   size_t flags_off, rowc_off, bpart_off, csr_bad_off, total;

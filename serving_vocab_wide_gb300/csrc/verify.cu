@@ -46,10 +46,11 @@ namespace {
 // consumer warps of the stats kernel: the argmax reduction is cheap per entry
 // and latency-bound, so greedy mode takes twice the warps
 constexpr int kCWMax = 16;
-template <bool GREEDY>
+template <bool GREEDY, bool EARLY = false>
 struct StatsShape {
   static constexpr int kCW = GREEDY ? 16 : 8;
-  static constexpr int kThreads = (kCW + 1) * 32;  // + one producer warp
+  // + one producer warp (+ one accounting warp with early exit)
+  static constexpr int kThreads = (kCW + (EARLY ? 2 : 1)) * 32;
 };
 constexpr int kStages = 3;                     // bulk-copy ring depth (2 CTAs per SM)
 constexpr int kFinThreads = 512;               // finalize (and sampling) kernel, two CTAs per SM
@@ -81,7 +82,10 @@ struct ItemMeta {
   int32_t chunk;
   int32_t n;  // elements in this chunk
   int32_t valid;
-  int32_t pad;
+  int32_t test;  // early exit: the accept test (kq * max_len + j) this item feeds, -1 if none
+  int64_t c_i;   // early exit: the request's first draft row
+  int32_t req;   // early exit: the request
+  int32_t pos;   // early exit: the position j
 };
 
 template <bool GREEDY>
@@ -116,6 +120,7 @@ __device__ __forceinline__ ItemMeta decode_item(const VerifyArgs &a, int64_t ite
   const int64_t local = item - off;
   const int32_t nrows = GREEDY ? L + 1 : 2 * L + 1;
   m.valid = (req_ok && local >= 0 && local < static_cast<int64_t>(nrows) * a.C) ? 1 : 0;
+  m.test = -1;
   if (!m.valid) {
     m.prow = 0;
     m.src = nullptr;
@@ -140,115 +145,91 @@ __device__ __forceinline__ ItemMeta decode_item(const VerifyArgs &a, int64_t ite
   return m;
 }
 
-// ---------------------------------------------------------------------------
-// consumer-warp reductions over one chunk held in shared memory (16-byte
-// vectors vi = wid*32 + lane + j*256 of the chunk)
-// ---------------------------------------------------------------------------
-template <int DT, int CW>
-__device__ __forceinline__ void warp_lse_smem(uint32_t base, int nvec, int wid, int lane, float k,
-                                              float &m, float &s) {
-  const int v0 = wid * 32 + lane;
-  float mx = -INFINITY;
-  if (DT == 1) {
-    uint32_t mw = 0xff80ff80u;  // (-inf, -inf)
-    for (int vi = v0; vi < nvec; vi += CW * 32) {
-      const uint4 q = lds128(base + vi * 16);
-      mw = bf16x2_max(mw, bf16x2_max(bf16x2_max(q.x, q.y), bf16x2_max(q.z, q.w)));
-    }
-    const float2 f = bf16x2_f2(mw);
-    mx = fmaxf(f.x, f.y);
+// Early exit: items are numbered position-major.  Wave j holds position j of
+// every request that has it, requests in the order of the plan's permutation
+// (longest first): the first A_j requests (L_i > j) contribute target row j
+// and draft row j (greedy: target row j only), C chunks each; the next B_j
+// (L_i = j) contribute their bonus row.  W[j] is the first item of wave j.
+// An item whose request already stopped (a rejection or a bad row at a
+// position before j) is skipped: no copy, no partial.
+//
+// The producer locates an item (shared-memory arithmetic only) and starts the
+// two loads it depends on -- the request record and the stop word, both kept
+// in permutation order -- before it waits for a free stage, and finishes the
+// decode after the wait.
+struct EarlyPre {
+  int64_t item;
+  int32_t j, kq, kind, chunk;
+  int4 info;     // {request, first draft row, L, 0}
+  int32_t stop;  // first position known to stop the request
+};
+
+template <bool GREEDY>
+__device__ __forceinline__ EarlyPre early_locate(const VerifyArgs &a, int64_t item, int64_t total, const int64_t *W,
+                                                 const int32_t *A) {
+  EarlyPre e;
+  e.item = item;
+  e.j = 0;
+  e.kq = 0;
+  e.kind = 0;
+  e.chunk = 0;
+  e.info = make_int4(0, 0, 0, 0);
+  e.stop = -1;
+  if (item >= total) return e;
+  int32_t j = 0;
+  while (j < a.max_len && W[j + 1] <= item) ++j;
+  const int64_t local = item - W[j];
+  const int64_t C = a.C;
+  int64_t kq;
+  if (!GREEDY && local < 2 * C * A[j]) {
+    kq = local / (2 * C);
+    const int64_t rem = local - kq * 2 * C;
+    e.kind = rem >= C ? 1 : 0;
+    e.chunk = static_cast<int32_t>(rem - e.kind * C);
   } else {
-    for (int vi = v0; vi < nvec; vi += CW * 32) {
-      const uint4 q = lds128(base + vi * 16);
-      mx = fmaxf(fmaxf(mx, fmaxf(__uint_as_float(q.x), __uint_as_float(q.y))),
-                 fmaxf(__uint_as_float(q.z), __uint_as_float(q.w)));
-    }
+    const int64_t l2 = GREEDY ? local : local - 2 * C * A[j];
+    const int64_t q = l2 / C;
+    kq = (GREEDY ? 0 : A[j]) + q;
+    e.chunk = static_cast<int32_t>(l2 - q * C);
   }
-  // one reference for the whole warp, so the lane sums add directly
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  const float mref = (mx == -INFINITY) ? 0.f : mx;
-  const float2 nm = make_float2(-mref, -mref), kk = make_float2(k, k);
-  float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-  for (int vi = v0; vi < nvec; vi += CW * 32) {
-    const uint4 q = lds128(base + vi * 16);
-    if (DT == 1) {
-      const float2 d0 = __fmul2_rn(__fadd2_rn(bf16x2_f2(q.x), nm), kk);  // (x - max) exact, then * log2e/T
-      const float2 d1 = __fmul2_rn(__fadd2_rn(bf16x2_f2(q.y), nm), kk);
-      const float2 d2 = __fmul2_rn(__fadd2_rn(bf16x2_f2(q.z), nm), kk);
-      const float2 d3 = __fmul2_rn(__fadd2_rn(bf16x2_f2(q.w), nm), kk);
-      acc0 = __fadd2_rn(acc0, __fadd2_rn(make_float2(ex2(d0.x), ex2(d0.y)), make_float2(ex2(d1.x), ex2(d1.y))));
-      acc1 = __fadd2_rn(acc1, __fadd2_rn(make_float2(ex2(d2.x), ex2(d2.y)), make_float2(ex2(d3.x), ex2(d3.y))));
-    } else {
-      const float2 d0 = __fmul2_rn(__fadd2_rn(make_float2(__uint_as_float(q.x), __uint_as_float(q.y)), nm), kk);
-      const float2 d1 = __fmul2_rn(__fadd2_rn(make_float2(__uint_as_float(q.z), __uint_as_float(q.w)), nm), kk);
-      acc0 = __fadd2_rn(acc0, make_float2(ex2(d0.x), ex2(d0.y)));
-      acc1 = __fadd2_rn(acc1, make_float2(ex2(d1.x), ex2(d1.y)));
-    }
-  }
-  const float2 acc = __fadd2_rn(acc0, acc1);
-  s = warp_sum(__fadd_rn(acc.x, acc.y));
-  m = mx;
-  if (!(mx == mx)) s = mx;  // all-NaN warp: keep the NaN visible
+  e.j = j;
+  e.kq = static_cast<int32_t>(kq);
+  e.info = __ldcg(a.pinfo + kq);
+  e.stop = __ldcg(a.stop + kq);
+  return e;
 }
 
-template <int DT, int CW>
-__device__ __forceinline__ void warp_amax_smem(uint32_t base, int nvec, int32_t c0, int wid, int lane,
-                                               float &best, int32_t &idx, int32_t &nan) {
+template <int DT>
+__device__ __forceinline__ ItemMeta early_finish(const VerifyArgs &a, const EarlyPre &e) {
   using E = Elem<DT>;
-  constexpr int EPV = E::kPerVec;
-  const int v0 = wid * 32 + lane;
-  float mx = -INFINITY;
-  int bvi = (v0 < nvec) ? v0 : -1;  // this lane's first vector holding its maximum (-inf rows: the first)
-  uint32_t nanw = 0;
-  if (DT == 1) {
-    for (int vi = v0; vi < nvec; vi += CW * 32) {
-      const uint4 q = lds128(base + vi * 16);
-      // NaN-propagating max of the vector: a NaN anywhere survives
-      const uint32_t m2 = bf16x2_max_nan(bf16x2_max_nan(q.x, q.y), bf16x2_max_nan(q.z, q.w));
-      nanw |= bf16x2_nan(m2);
-      const float2 f = bf16x2_f2(m2);
-      const float vm = fmaxf(f.x, f.y);
-      if (vm > mx) {
-        mx = vm;
-        bvi = vi;
-      }
-    }
+  ItemMeta m;
+  m.item = e.item;
+  m.valid = 0;
+  m.test = -1;
+  m.prow = 0;
+  m.src = nullptr;
+  m.chunk = e.chunk;
+  m.n = 0;
+  const int32_t i = e.info.x, L = e.info.z, j = e.j;
+  const int64_t c_i = e.info.y;
+  m.c_i = c_i;
+  m.req = i;
+  m.pos = j;
+  if (e.stop < j) return m;  // the request stopped before j
+  const int64_t c0 = static_cast<int64_t>(m.chunk) * a.chunk_len;
+  m.n = static_cast<int32_t>(min(static_cast<int64_t>(a.chunk_len), a.V - c0));
+  const char *row;
+  if (e.kind == 0) {
+    m.prow = c_i + i + j;
+    row = static_cast<const char *>(a.target) + m.prow * a.V * E::kSize;
   } else {
-    for (int vi = v0; vi < nvec; vi += CW * 32) {
-      const uint4 q = lds128(base + vi * 16);
-      const float x[4] = {__uint_as_float(q.x), __uint_as_float(q.y), __uint_as_float(q.z),
-                          __uint_as_float(q.w)};
-      float vm = -INFINITY;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        nanw |= (x[e] != x[e]);
-        vm = fmaxf(vm, x[e]);
-      }
-      if (vm > mx) {
-        mx = vm;
-        bvi = vi;
-      }
-    }
+    m.prow = a.rows_t + c_i + j;
+    row = static_cast<const char *>(a.draft) + (c_i + j) * a.V * E::kSize;
   }
-  float wmx = mx;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) wmx = fmaxf(wmx, __shfl_xor_sync(0xffffffffu, wmx, o));
-  // only lanes holding the warp maximum look for its first index, in the
-  // one vector where their maximum first appeared (each lane's vectors are in
-  // index order, lanes interleave by vector)
-  idx = INT32_MAX;
-  if (mx == wmx && bvi >= 0) {
-    float x[EPV];
-    E::unpack(lds128(base + bvi * 16), x);
-#pragma unroll
-    for (int e = EPV - 1; e >= 0; --e)
-      if (x[e] == wmx) idx = c0 + bvi * EPV + e;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) idx = min(idx, __shfl_xor_sync(0xffffffffu, idx, o));
-  best = wmx;
-  nan = __any_sync(0xffffffffu, nanw != 0) ? 1 : 0;
+  m.src = row + c0 * E::kSize;
+  m.test = (j < L) ? e.kq * a.max_len + j : -1;
+  m.valid = 1;
+  return m;
 }
 
 template <int DT, int CW>
@@ -287,19 +268,217 @@ __device__ __forceinline__ void warp_amax_global(const char *p0, int n, int32_t 
 }
 
 // ---------------------------------------------------------------------------
+// one row's statistics merged from its np partials by one warp, in a fixed
+// order (lane-strided, then a butterfly), so that every caller -- the
+// finalize kernels and the early-exit tests -- gets the same bits
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void merge_row_lse(const Partial *pp, int np, float k, int lane, float &m, float &l,
+                                              int32_t &bad) {
+  float mm = -INFINITY, s = 0.f;
+  for (int p = lane; p < np; p += 32) {
+    const Partial q = ldcg_partial(pp + p);
+    lse_combine(mm, s, q.m, q.s, k);
+  }
+  warp_lse(mm, s, k);
+  m = mm;
+  l = lg2(s);
+  bad = (s > 0.f && s <= FLT_MAX) ? 0 : 1;
+}
+
+__device__ __forceinline__ void merge_row_amax(const Partial *pp, int np, int lane, int32_t &idx, int32_t &bad) {
+  float v = -INFINITY;
+  int32_t id = INT32_MAX, nan = 0;
+  for (int p = lane; p < np; p += 32) {
+    const Partial q = ldcg_partial(pp + p);
+    amax_combine(v, id, q.m, q.idx);
+    nan |= q.nan;
+  }
+  warp_amax(v, id);
+  idx = id;
+  bad = __any_sync(0xffffffffu, nan != 0) ? 1 : 0;
+}
+
+// Two rows merged as merge_row_lse merges each (same order per row, same
+// bits), with both rows' loads in flight together.
+__device__ __forceinline__ void merge_two_rows_lse(const Partial *pa, const Partial *pb, int np, float k, int lane,
+                                                   float &ma, float &la, int32_t &bada, float &mb, float &lb,
+                                                   int32_t &badb) {
+  float m0 = -INFINITY, s0 = 0.f, m1 = -INFINITY, s1 = 0.f;
+#pragma unroll 4
+  for (int p = lane; p < np; p += 32) {
+    const Partial qa = ldcg_partial(pa + p);
+    const Partial qb = ldcg_partial(pb + p);
+    lse_combine(m0, s0, qa.m, qa.s, k);
+    lse_combine(m1, s1, qb.m, qb.s, k);
+  }
+  warp_lse(m0, s0, k);
+  warp_lse(m1, s1, k);
+  ma = m0;
+  la = lg2(s0);
+  bada = (s0 > 0.f && s0 <= FLT_MAX) ? 0 : 1;
+  mb = m1;
+  lb = lg2(s1);
+  badb = (s1 > 0.f && s1 <= FLT_MAX) ? 0 : 1;
+}
+
+// Early exit: the accept test of position j of request i, run by the warp
+// that delivered the last partial of its rows.  A rejection or a bad row
+// (non-finite statistics, token out of range) lowers the request's stop word
+// (so later positions are no longer read) and its first rejected / bad
+// position (for the finalize kernel).
+template <int DT, bool GREEDY, int CW>
+__device__ __noinline__ void early_test(const VerifyArgs &a, int32_t kq, int32_t i, int64_t c_i, int32_t j,
+                                        int lane) {
+  using E = Elem<DT>;
+  const int64_t trow = c_i + i + j, drow = c_i + j;
+  const int np = a.C * CW;
+  const int32_t x = __ldg(a.tokens + drow);
+  int32_t bad = (x < 0 || static_cast<int64_t>(x) >= a.V) ? 1 : 0;
+  bool acc = false;
+  if (GREEDY) {
+    int32_t idx = INT32_MAX, nan = 0;
+    merge_row_amax(a.part + trow * np, np, lane, idx, nan);
+    bad |= nan;
+    acc = (x == idx);
+  } else {
+    // the logits at x and the uniform do not depend on the partials
+    const float yx = bad ? 0.f : E::load(a.target, trow * a.V + x);
+    const float zx = bad ? 0.f : E::load(a.draft, drow * a.V + x);
+    const float u = philox_uniform(a.seed, static_cast<uint32_t>(i), static_cast<uint32_t>(j), 0u);
+    float mT, lT, mD, lD;
+    int32_t bT, bD;
+    merge_two_rows_lse(a.part + trow * np, a.part + (a.rows_t + drow) * np, np, a.k, lane, mT, lT, bT, mD, lD,
+                       bD);
+    bad |= bT | bD;
+    acc = !bad && accept_token(u, yx, zx, mT, lT, mD, lD, a.k);
+  }
+  if (lane == 0) {
+    if (bad) {
+      atomicMin(a.stop + kq, j);
+      atomicMin(a.badpos + i, j);
+    } else if (!acc) {
+      atomicMin(a.stop + kq, j);
+      atomicMin(a.rej + i, j);
+    }
+  }
+}
+
+// Early exit: count inc consumer-warp partials towards their accept test; the
+// warp that completes the count (2 rows x C chunks x CW warps; greedy: the
+// target row only) runs the test.  Store -> (CTA sync) -> release on every
+// side, acquire -> loads on the last.
+template <int DT, bool GREEDY, int CW>
+__device__ __forceinline__ void early_arrive(const VerifyArgs &a, const ItemMeta &m, int lane, int inc) {
+  int last = 0;
+  if (lane == 0) {
+    const int need = (GREEDY ? 1 : 2) * a.C * CW;
+    int old;
+    // release: the partials written before it (by this thread, or by the
+    // consumer warps whose mbarrier arrivals this thread observed) are
+    // visible before the count; acquire: the last counter sees all of them
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(a.cnt + m.test), "r"(inc)
+                 : "memory");
+    last = (old == need - inc) ? 1 : 0;
+  }
+  last = __shfl_sync(0xffffffffu, last, 0);
+  __syncwarp();  // lane 0's acquire orders the whole warp's loads below
+  if (last) early_test<DT, GREEDY, CW>(a, m.test / a.max_len, m.req, m.c_i, m.pos, lane);
+}
+
+// Early exit, ahead of the stats stream (one CTA): per-request checks, the
+// position-major wave layout (W[j], A_j = requests longer than j), the valid
+// requests' records {request, first draft row, L} in permutation order by
+// length (longest first; the order within a length is arbitrary and does not
+// affect any result), the CSR flag, and this call's state reset: test
+// counters, stop words, first rejected / bad positions, byte counter.
+template <bool GREEDY>
+__global__ void __launch_bounds__(1024) early_plan(VerifyArgs a) {
+  __shared__ int32_t hist[SVW_MAX_LEN + 1];
+  __shared__ int32_t cur[SVW_MAX_LEN + 1];
+  pdl_launch_dependents();  // the stats grid may be scheduled now
+  const int tid = threadIdx.x;
+  if (tid <= SVW_MAX_LEN) hist[tid] = 0;
+  __syncthreads();
+  auto length_of = [&](int32_t i, int64_t &c_i) -> int32_t {
+    c_i = __ldg(a.cu + i);
+    const int64_t c_e = __ldg(a.cu + i + 1);
+    const int64_t L = c_e - c_i;
+    return (L >= 1 && L <= a.max_len && c_i >= 0 && c_e <= a.total_rows) ? static_cast<int32_t>(L) : 0;
+  };
+  int bad = 0;
+  for (int32_t i = tid; i < a.N; i += 1024) {
+    int64_t c_i;
+    const int32_t L = length_of(i, c_i);
+    bad |= (c_i > static_cast<int64_t>(__ldg(a.cu + i + 1))) ? 1 : 0;
+    if (L > 0) atomicAdd(&hist[L], 1);
+    a.rej[i] = INT32_MAX;
+    a.badpos[i] = INT32_MAX;
+    a.stop[i] = INT32_MAX;  // indexed by permutation slot; N slots at most
+    if (a.eres) a.eres[i] = make_int4(-1, 1, 0, 0);  // a request no cluster finished is bad
+  }
+  if (tid == 0) bad |= (__ldg(a.cu) != 0 || static_cast<int64_t>(__ldg(a.cu + a.N)) != a.total_rows) ? 1 : 0;
+  const int64_t ncnt = static_cast<int64_t>(a.N) * a.max_len;
+  for (int64_t q = tid; q < ncnt; q += 1024) a.cnt[q] = 0;
+  bad = __syncthreads_or(bad);
+  if (tid == 0) {
+    a.csr_bad[0] = bad;
+    if (a.bytes_read) *a.bytes_read = 0ull;
+    int32_t above = 0;  // valid requests longer than Lq
+    for (int32_t Lq = a.max_len; Lq >= 1; --Lq) {
+      cur[Lq] = above;
+      above += hist[Lq];
+    }
+    int32_t Aj = above;  // every valid request has position 0
+    int64_t w = 0;
+    for (int32_t j = 0; j <= a.max_len; ++j) {
+      const int32_t Bj = (j >= 1) ? hist[j] : 0;  // bonus rows at position j
+      if (j >= 1) Aj -= hist[j];
+      a.waveA[j] = Aj;
+      a.W[j] = w;
+      w += static_cast<int64_t>(a.C) * (GREEDY ? (Aj + Bj) : (2 * static_cast<int64_t>(Aj) + Bj));
+    }
+    a.W[a.max_len + 1] = w;
+    *a.nvalid = above;
+    *a.qnext = 0;
+  }
+  __syncthreads();
+  for (int32_t i = tid; i < a.N; i += 1024) {
+    int64_t c_i;
+    const int32_t L = length_of(i, c_i);
+    if (L > 0) a.pinfo[atomicAdd(&cur[L], 1)] = make_int4(i, static_cast<int32_t>(c_i), L, 0);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // kernel 2: stats stream
 // ---------------------------------------------------------------------------
-template <int DT, bool BULK, bool GREEDY>
-__global__ void __launch_bounds__(StatsShape<GREEDY>::kThreads, 2) verify_stats(VerifyArgs a, int stage_bytes) {
+template <int DT, bool BULK, bool GREEDY, bool EARLY>
+__global__ void __launch_bounds__(StatsShape<GREEDY, EARLY>::kThreads, 2)
+    verify_stats(VerifyArgs a, int stage_bytes) {
   constexpr int kCW = StatsShape<GREEDY>::kCW;
-  constexpr int kStatsThreads = StatsShape<GREEDY>::kThreads;
+  constexpr int kStatsThreads = StatsShape<GREEDY, EARLY>::kThreads;
   extern __shared__ __align__(128) unsigned char ring[];
   __shared__ unsigned long long full[kStages], empty[kStages];
+  __shared__ unsigned long long done[kStages];  // early exit: the consumers' partials of a stage are written
   __shared__ ItemMeta meta[kStages];
+  __shared__ int64_t waveW[SVW_MAX_LEN + 2];  // early exit: first item of each wave
+  __shared__ int32_t waveA[SVW_MAX_LEN + 1];  // early exit: requests longer than j
   const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t G = gridDim.x;
   pdl_launch_dependents();  // the finalize grid may be scheduled now
-  {
+  int64_t total_items = a.total_items;
+  if (EARLY) {
+    // the plan kernel's layout and reset state (the CSR check is its job too)
+    pdl_wait();
+    for (int q = threadIdx.x; q <= a.max_len + 1; q += kStatsThreads) {
+      waveW[q] = __ldcg(a.W + q);
+      if (q <= a.max_len) waveA[q] = __ldcg(a.waveA + q);
+    }
+    __syncthreads();
+    total_items = waveW[a.max_len + 1];
+  } else {
     // this CTA's share of the CSR consistency check: cu[0] = 0,
     // cu[N] = total rows, non-decreasing (the finalize kernel ORs the flags)
     int bad = 0;
@@ -311,13 +490,19 @@ __global__ void __launch_bounds__(StatsShape<GREEDY>::kThreads, 2) verify_stats(
     bad = __syncthreads_or(bad);
     if (threadIdx.x == 0) a.csr_bad[blockIdx.x] = bad;
   }
+  auto decode = [&](int64_t item) {
+    return EARLY ? early_finish<DT>(a, early_locate<GREEDY>(a, item, total_items, waveW, waveA))
+                 : decode_item<DT, GREEDY>(a, item);
+  };
 
   if (!BULK) {
     // plain loads: every warp walks the CTA's items itself (no producer)
-    if (wid == kCW) return;
-    for (int64_t item = blockIdx.x; item < a.total_items; item += G) {
-      const ItemMeta m = decode_item<DT, GREEDY>(a, item);
+    if (wid >= kCW) return;
+    unsigned long long nbytes = 0;
+    for (int64_t item = blockIdx.x; item < total_items; item += G) {
+      const ItemMeta m = decode(item);
       if (!m.valid) continue;
+      nbytes += static_cast<unsigned long long>(m.n) * Elem<DT>::kSize;
       Partial res;
       if (GREEDY) {
         warp_amax_global<DT, kCW>(m.src, m.n, m.chunk * a.chunk_len, wid, lane, res.m, res.idx, res.nan);
@@ -328,14 +513,17 @@ __global__ void __launch_bounds__(StatsShape<GREEDY>::kThreads, 2) verify_stats(
         res.nan = 0;
       }
       if (lane == 0) a.part[(m.prow * a.C + m.chunk) * kCW + wid] = res;
+      if (EARLY && m.test >= 0) early_arrive<DT, GREEDY, kCW>(a, m, lane, 1);
     }
+    if (EARLY && a.bytes_read && wid == 0 && lane == 0) atomicAdd(a.bytes_read, nbytes);
     return;
   }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kCW);
+      mbar_init(&empty[s], EARLY ? 1 : kCW);  // early exit: released by the accounting warp
+      mbar_init(&done[s], kCW);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -344,29 +532,66 @@ __global__ void __launch_bounds__(StatsShape<GREEDY>::kThreads, 2) verify_stats(
   if (wid == kCW) {
     // ---------------- producer warp (one lane) ----------------
     if (lane != 0) return;
+    unsigned long long nbytes = 0;
+    auto add_bytes = [&]() {
+      if (EARLY && a.bytes_read) atomicAdd(a.bytes_read, nbytes);
+    };
     int k = 0;
+    // early exit: the next item's two loads are in flight while this lane
+    // waits for its stage
+    EarlyPre pre;
+    if (EARLY) pre = early_locate<GREEDY>(a, blockIdx.x, total_items, waveW, waveA);
     for (int64_t item = blockIdx.x;; item += G, ++k) {
       const int s = k % kStages;
       if (k >= kStages && !mbar_wait_bounded(&empty[s], static_cast<uint32_t>(((k / kStages) - 1) & 1))) {
         // consumers stopped releasing stages: report, hand them an end marker
         if (a.status) atomicOr(a.status, SVW_DEV_TIMEOUT);
+        add_bytes();
         return;
       }
-      if (item >= a.total_items) {
+      if (item >= total_items) {
         meta[s].item = -1;
         mbar_arrive(&full[s]);
+        add_bytes();
         return;
       }
-      const ItemMeta m = decode_item<DT, GREEDY>(a, item);
+      const ItemMeta m = EARLY ? early_finish<DT>(a, pre) : decode_item<DT, GREEDY>(a, item);
       meta[s] = m;
-      if (!m.valid) {
+      if (m.valid) {
+        const uint32_t bytes = static_cast<uint32_t>(m.n) * Elem<DT>::kSize;
+        nbytes += bytes;
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive_expect_tx(&full[s], bytes);
+        bulk_g2s(ring + static_cast<size_t>(s) * stage_bytes, m.src, bytes, &full[s]);
+      } else {
         mbar_arrive(&full[s]);
-        continue;
       }
-      const uint32_t bytes = static_cast<uint32_t>(m.n) * Elem<DT>::kSize;
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive_expect_tx(&full[s], bytes);
-      bulk_g2s(ring + static_cast<size_t>(s) * stage_bytes, m.src, bytes, &full[s]);
+      if (EARLY) pre = early_locate<GREEDY>(a, item + G, total_items, waveW, waveA);
+    }
+  }
+
+  if (EARLY && wid == kCW + 1) {
+    // ---------------- accounting warp (early exit) ----------------
+    // Follows the ring one stage behind the consumers: once a stage's
+    // partials are written it frees the stage, then counts them towards their
+    // accept test with one fenced atomic, and runs the test if they complete
+    // it -- all off the consumers' path.
+    for (int k = 0;; ++k) {
+      const int s = k % kStages;
+      const uint32_t par = static_cast<uint32_t>((k / kStages) & 1);
+      if (!mbar_wait_bounded(&full[s], par)) {
+        if (lane == 0 && a.status) atomicOr(a.status, SVW_DEV_TIMEOUT);
+        return;
+      }
+      const ItemMeta m = meta[s];
+      if (m.item < 0) return;
+      if (!mbar_wait_bounded(&done[s], par)) {
+        if (lane == 0 && a.status) atomicOr(a.status, SVW_DEV_TIMEOUT);
+        return;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      if (m.valid && m.test >= 0) early_arrive<DT, GREEDY, kCW>(a, m, lane, kCW);
     }
   }
 
@@ -394,14 +619,17 @@ __global__ void __launch_bounds__(StatsShape<GREEDY>::kThreads, 2) verify_stats(
       if (lane == 0) a.part[(m.prow * a.C + m.chunk) * kCW + wid] = res;
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
+    if (lane == 0) mbar_arrive(EARLY ? &done[s] : &empty[s]);
   }
 }
 
 // ---------------------------------------------------------------------------
 // kernel 2: per-request validation, merge, accept tests
 // ---------------------------------------------------------------------------
-template <int DT, bool GREEDY, bool VEC>
+// MODE 0: spec_verify (merge every row's partials, run every test);
+// MODE 1: early exit by the chunk stream (the tests ran in the stats kernel);
+// MODE 2: early exit by clusters (stop position and statistics recorded).
+template <int DT, bool GREEDY, bool VEC, int MODE>
 __global__ void __launch_bounds__(kFinThreads) verify_finalize(VerifyArgs a) {
   using E = Elem<DT>;
   __shared__ float row_m[kMaxRows];
@@ -426,7 +654,7 @@ __global__ void __launch_bounds__(kFinThreads) verify_finalize(VerifyArgs a) {
     if (lane < L) {
       x = __ldg(a.tokens + d0 + lane);
       tok_ok = (x >= 0 && static_cast<int64_t>(x) < a.V);
-      if (tok_ok && !GREEDY) {
+      if (tok_ok && !GREEDY && MODE == 0) {
         yx = E::load(a.target, (t0 + lane) * a.V + x);
         zx = E::load(a.draft, (d0 + lane) * a.V + x);
         u = philox_uniform(a.seed, static_cast<uint32_t>(i), static_cast<uint32_t>(lane), 0u);
@@ -449,72 +677,108 @@ __global__ void __launch_bounds__(kFinThreads) verify_finalize(VerifyArgs a) {
     if (tid == 0) reject();
     return;
   }
-  const int32_t nrows = GREEDY ? L + 1 : 2 * L + 1;
   const int np = a.C * StatsShape<GREEDY>::kCW;  // partials per row
-  for (int r = warp; r < nrows; r += kFinWarps) {
-    const int64_t prow = (r <= L) ? (t0 + r) : (a.rows_t + d0 + (r - L - 1));
-    const Partial *pp = a.part + prow * np;
-    if (GREEDY) {
-      float v = -INFINITY;
-      int32_t idx = INT32_MAX, nan = 0;
-      for (int p = lane; p < np; p += 32) {
-        const Partial q = ldcg_partial(pp + p);
-        amax_combine(v, idx, q.m, q.idx);
-        nan |= q.nan;
-      }
-      warp_amax(v, idx);
-      nan = __any_sync(0xffffffffu, nan);
+  if (MODE == 2) {
+    if (warp == 0) {
+      const int4 r = __ldcg(a.eres + i);
+      const float4 f = __ldcg(a.erow + i);
+      const int32_t js = r.x;
       if (lane == 0) {
-        row_idx[r] = idx;
-        row_bad[r] = nan;
-      }
-    } else {
-      float mm = -INFINITY, s = 0.f;
-      for (int p = lane; p < np; p += 32) {
-        const Partial q = ldcg_partial(pp + p);
-        lse_combine(mm, s, q.m, q.s, a.k);
-      }
-      warp_lse(mm, s, a.k);
-      if (lane == 0) {
-        row_m[r] = mm;
-        row_l[r] = lg2(s);
-        row_bad[r] = !(s > 0.f && s <= FLT_MAX);
-      }
-    }
-  }
-  __syncthreads();
-  if (warp == 0) {
-    int bad = 0;
-    for (int r = lane; r < nrows; r += 32) bad |= row_bad[r];
-    bad = __any_sync(0xffffffffu, bad);
-    bool acc = true;
-    if (lane < L) {
-      if (GREEDY) {
-        acc = (x == row_idx[lane]);
-      } else {
-        // log2(p(x)/q(x)) from raw logits and row log-sum-exps
-        float thr;
-        if (zx == -INFINITY) {
-          thr = 1.f;  // q(x) = 0: accept
+        if (r.y != 0 || js < 0 || js > L) {
+          reject();
+          s_js = -1;
         } else {
-          const float dl = __fsub_rn(
-              __fmul_rn(__fsub_rn(__fsub_rn(yx, row_m[lane]), __fsub_rn(zx, row_m[L + 1 + lane])), a.k),
-              __fsub_rn(row_l[lane], row_l[L + 1 + lane]));
-          thr = (dl >= 0.f) ? 1.f : ex2(dl);
+          a.accept_len[i] = js;
+          if (GREEDY) a.next_token[i] = r.z;
+          row_m[js] = f.x;
+          row_l[js] = f.y;
+          if (js < L) {
+            row_m[L + 1 + js] = f.z;
+            row_l[L + 1 + js] = f.w;
+          }
+          s_js = js;
         }
-        acc = (u < thr);
       }
     }
-    const unsigned rej = __ballot_sync(0xffffffffu, !acc);
-    const int32_t js = rej ? (__ffs(rej) - 1) : L;
-    if (lane == 0) {
-      if (bad) {
-        reject();
-        s_js = -1;
+  } else if (MODE == 1) {
+    // the stats stream ran the accept tests in position order and stopped
+    // reading a request at its first rejection (or bad row): only the rows
+    // at that position are merged here
+    if (warp == 0) {
+      const int32_t r = min(__ldcg(a.rej + i), L);
+      int32_t bad = (__ldcg(a.badpos + i) <= r) ? 1 : 0;
+      int32_t idx = INT32_MAX, b = 0;
+      if (GREEDY) {
+        merge_row_amax(a.part + (t0 + r) * np, np, lane, idx, b);
+        bad |= b;
       } else {
-        a.accept_len[i] = js;
-        if (GREEDY) a.next_token[i] = row_idx[js];
-        s_js = js;
+        float m, l;
+        merge_row_lse(a.part + (t0 + r) * np, np, a.k, lane, m, l, b);
+        bad |= b;
+        if (lane == 0) {
+          row_m[r] = m;
+          row_l[r] = l;
+        }
+        if (r < L) {
+          merge_row_lse(a.part + (a.rows_t + d0 + r) * np, np, a.k, lane, m, l, b);
+          bad |= b;
+          if (lane == 0) {
+            row_m[L + 1 + r] = m;
+            row_l[L + 1 + r] = l;
+          }
+        }
+      }
+      if (lane == 0) {
+        if (bad) {
+          reject();
+          s_js = -1;
+        } else {
+          a.accept_len[i] = r;
+          if (GREEDY) a.next_token[i] = idx;
+          s_js = r;
+        }
+      }
+    }
+  } else {
+    const int32_t nrows = GREEDY ? L + 1 : 2 * L + 1;
+    for (int r = warp; r < nrows; r += kFinWarps) {
+      const int64_t prow = (r <= L) ? (t0 + r) : (a.rows_t + d0 + (r - L - 1));
+      const Partial *pp = a.part + prow * np;
+      int32_t b;
+      if (GREEDY) {
+        int32_t idx;
+        merge_row_amax(pp, np, lane, idx, b);
+        if (lane == 0) row_idx[r] = idx;
+      } else {
+        float m, l;
+        merge_row_lse(pp, np, a.k, lane, m, l, b);
+        if (lane == 0) {
+          row_m[r] = m;
+          row_l[r] = l;
+        }
+      }
+      if (lane == 0) row_bad[r] = b;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      int bad = 0;
+      for (int r = lane; r < nrows; r += 32) bad |= row_bad[r];
+      bad = __any_sync(0xffffffffu, bad);
+      bool acc = true;
+      if (lane < L)
+        acc = GREEDY ? (x == row_idx[lane])
+                     : accept_token(u, yx, zx, row_m[lane], row_l[lane], row_m[L + 1 + lane], row_l[L + 1 + lane], a.k);
+      const unsigned rej = __ballot_sync(0xffffffffu, !acc);
+      const int32_t js = rej ? (__ffs(rej) - 1) : L;
+      if (lane == 0) {
+        if (bad) {
+          reject();
+          s_js = -1;
+        } else {
+          a.accept_len[i] = js;
+          if (GREEDY) a.next_token[i] = row_idx[js];
+          s_js = js;
+        }
       }
     }
   }
@@ -564,58 +828,86 @@ int cached_grid(const void *fn, int threads, int smem, cudaError_t &e) {
 }
 
 // launch as a programmatic dependent of the previous kernel in the stream
-template <typename Kern>
-cudaError_t launch_dependent(const char *name, Kern kern, unsigned grid, unsigned block, const VerifyArgs &a,
-                             cudaStream_t st) {
+template <typename Kern, typename... Args>
+cudaError_t launch_dependent(const char *name, Kern kern, unsigned grid, unsigned block, size_t smem,
+                             cudaStream_t st, Args... args) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(block, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   void *tm = timer_before(name, st);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
   timer_after(tm, st);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-template <int DT, bool VEC, bool GREEDY>
+template <int DT, bool VEC, bool GREEDY, bool EARLY>
 cudaError_t launch_all_t(const VerifyArgs &args, cudaStream_t st) {
   using E = Elem<DT>;
+  if (EARLY && VEC) {
+    // the cluster path when the rows fit it: plan, clusters, finalize
+    const EarlyClusterPlan cp = early_cluster_plan(args.V, E::kSize, GREEDY);
+    if (cp.CL > 0) {
+      VerifyArgs a = args;
+      a.stats_grid = 1;  // the plan kernel writes the one CSR flag
+      void *tm = timer_before("early_plan", st);
+      early_plan<GREEDY><<<1, 1024, 0, st>>>(a);
+      timer_after(tm, st);
+      cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+      e = launch_early_cluster(a, DT == 1 ? SVW_BF16 : SVW_F32, GREEDY, cp, st);
+      if (e != cudaSuccess) return e;
+      return launch_dependent("verify_finalize", verify_finalize<DT, GREEDY, VEC, 2>, static_cast<unsigned>(a.N),
+                              kFinThreads, 0, st, a);
+    }
+  }
   const int stage_bytes = VEC ? (args.chunk_len * E::kSize + 127) / 128 * 128 : 0;
   const int smem = VEC ? kStages * stage_bytes : 0;
-  auto fn = verify_stats<DT, VEC, GREEDY>;
+  auto fn = verify_stats<DT, VEC, GREEDY, EARLY>;
   cudaError_t e = cudaSuccess;
   if (VEC) {
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
   }
-  constexpr int kStatsThreads = StatsShape<GREEDY>::kThreads;
+  constexpr int kStatsThreads = StatsShape<GREEDY, EARLY>::kThreads;
   int grid = cached_grid(reinterpret_cast<const void *>(fn), kStatsThreads, smem, e);
   if (e != cudaSuccess) return e;
   if (grid > args.total_items) grid = static_cast<int>(args.total_items);
   if (grid > kMaxStatsGrid) grid = kMaxStatsGrid;
   if (grid < 1) grid = 1;
   VerifyArgs a = args;
-  a.stats_grid = grid;
-  // the first kernel is an ordinary launch: it waits for all earlier work in
-  // the stream (a previous call's sampler may still read this workspace)
-  void *tm = timer_before("verify_stats", st);
-  fn<<<grid, kStatsThreads, smem, st>>>(a, stage_bytes);
-  timer_after(tm, st);
-  e = cudaGetLastError();
+  a.stats_grid = EARLY ? 1 : grid;  // early exit: the plan kernel writes the one CSR flag
+  if (EARLY) {
+    // the plan is an ordinary launch: it waits for all earlier work in the
+    // stream (a previous call's kernels may still read this workspace); the
+    // stats stream and the finalize kernel follow as programmatic dependents
+    void *tm = timer_before("early_plan", st);
+    early_plan<GREEDY><<<1, 1024, 0, st>>>(a);
+    timer_after(tm, st);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = launch_dependent("verify_stats", fn, static_cast<unsigned>(grid), kStatsThreads, smem, st, a, stage_bytes);
+  } else {
+    // the first kernel is an ordinary launch (see above)
+    void *tm = timer_before("verify_stats", st);
+    fn<<<grid, kStatsThreads, smem, st>>>(a, stage_bytes);
+    timer_after(tm, st);
+    e = cudaGetLastError();
+  }
   if (e != cudaSuccess) return e;
-  return launch_dependent("verify_finalize", verify_finalize<DT, GREEDY, VEC>, static_cast<unsigned>(a.N), kFinThreads,
-                          a, st);
+  return launch_dependent("verify_finalize", verify_finalize<DT, GREEDY, VEC, EARLY ? 1 : 0>,
+                          static_cast<unsigned>(a.N), kFinThreads, 0, st, a);
 }
 
-template <int DT, bool VEC>
+template <int DT, bool VEC, bool EARLY>
 cudaError_t launch_all(const VerifyArgs &a, bool greedy, cudaStream_t st) {
-  return greedy ? launch_all_t<DT, VEC, true>(a, st) : launch_all_t<DT, VEC, false>(a, st);
+  return greedy ? launch_all_t<DT, VEC, true, EARLY>(a, st) : launch_all_t<DT, VEC, false, EARLY>(a, st);
 }
 
 }  // namespace
@@ -665,8 +957,42 @@ FusedLayout fused_layout(int32_t N, int64_t total_rows, int64_t V) {
 }
 
 cudaError_t launch_verify(const VerifyArgs &a, int dtype, bool vec, bool greedy, cudaStream_t st) {
-  if (dtype == SVW_BF16) return vec ? launch_all<1, true>(a, greedy, st) : launch_all<1, false>(a, greedy, st);
-  return vec ? launch_all<0, true>(a, greedy, st) : launch_all<0, false>(a, greedy, st);
+  if (dtype == SVW_BF16)
+    return vec ? launch_all<1, true, false>(a, greedy, st) : launch_all<1, false, false>(a, greedy, st);
+  return vec ? launch_all<0, true, false>(a, greedy, st) : launch_all<0, false, false>(a, greedy, st);
+}
+
+EarlyLayout early_layout(int32_t N, int64_t total_rows, int64_t V, int esize) {
+  const VerifyLayout v = verify_layout(N, total_rows, V, esize);
+  EarlyLayout l;
+  size_t off = v.total;
+  l.part_off = v.part_off;
+  l.csr_bad_off = v.csr_bad_off;
+  l.cnt_off = off;
+  off += align256(static_cast<size_t>(N) * SVW_MAX_LEN * sizeof(int32_t));
+  l.rej_off = off;
+  off += align256(static_cast<size_t>(N) * sizeof(int32_t));
+  l.badpos_off = off;
+  off += align256(static_cast<size_t>(N) * sizeof(int32_t));
+  l.stop_off = off;
+  off += align256(static_cast<size_t>(N) * sizeof(int32_t));
+  l.pinfo_off = off;
+  off += align256(static_cast<size_t>(N) * sizeof(int4));
+  l.wave_off = off;
+  // W[max_len + 2] (int64), A_j[max_len + 1], valid-request count, queue head
+  off += align256((SVW_MAX_LEN + 2) * sizeof(int64_t) + (SVW_MAX_LEN + 3) * sizeof(int32_t));
+  l.eres_off = off;
+  off += align256(static_cast<size_t>(N) * sizeof(int4));
+  l.erow_off = off;
+  off += align256(static_cast<size_t>(N) * sizeof(float4));
+  l.total = off;
+  return l;
+}
+
+cudaError_t launch_verify_early(const VerifyArgs &a, int dtype, bool vec, bool greedy, cudaStream_t st) {
+  if (dtype == SVW_BF16)
+    return vec ? launch_all<1, true, true>(a, greedy, st) : launch_all<1, false, true>(a, greedy, st);
+  return vec ? launch_all<0, true, true>(a, greedy, st) : launch_all<0, false, true>(a, greedy, st);
 }
 
 }  // namespace svw

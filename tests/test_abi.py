@@ -28,7 +28,8 @@ def lib():
 def test_header_symbols_exported(lib):
     names = _declared_functions()
     assert {"spec_verify", "opd_loss", "svw_verify_workspace_size", "svw_opd_workspace_size",
-            "svw_status_string", "svw_version", "spec_verify_noalloc"} <= set(names)
+            "svw_status_string", "svw_version", "spec_verify_noalloc", "spec_verify_early",
+            "svw_verify_early_workspace_size"} <= set(names)
     for n in names:
         assert hasattr(lib, n), f"{n} declared in svw.h but not exported"
 
@@ -86,6 +87,33 @@ def test_verify_argument_validation(lib):
     mis = ctypes.c_void_p(p.value + 1)
     assert call(t=mis) == 3
     assert call(ws=ctypes.c_void_p(p.value + 16)) == 3
+
+
+def test_verify_early_argument_validation(lib):
+    import serving_vocab_wide_gb300 as svw
+    keep, p = _fake(4096)
+    ok_args = dict(t=p, d=p, dt=1, V=64, N=2, cu=p, R=4, ml=16, tok=p, T=1.0, seed=0,
+                   acc=p, nxt=p, st=None, nb=None, ws=p, wsb=1 << 30)
+
+    def call(**kw):
+        a = dict(ok_args, **kw)
+        return lib.spec_verify_early(a["t"], a["d"], a["dt"], a["V"], a["N"], a["cu"], a["R"], a["ml"],
+                                     a["tok"], a["T"], a["seed"], a["acc"], a["nxt"], a["st"], a["nb"],
+                                     a["ws"], a["wsb"], None)
+
+    assert call(dt=7) == 2
+    assert call(V=0) == 1
+    assert call(ml=33) == 2
+    assert call(tok=None) == 1
+    assert call(ws=None) == 4
+    assert call(T=float("nan")) == 1
+    assert call(nb=ctypes.c_void_p(p.value + 4)) == 3       # bytes_read must be 8-byte aligned
+    need = svw.verify_early_workspace_size(2, 4, 64, svw.SVW_BF16)
+    assert call(wsb=need - 1) == 4
+    # the early-exit state comes after spec_verify's workspace
+    for args in ((2, 4, 64, svw.SVW_BF16), (256, 1964, 151936, svw.SVW_BF16), (4, 64, 1024, svw.SVW_F32)):
+        assert svw.verify_early_workspace_size(*args) > svw.verify_workspace_size(*args)
+    assert svw.verify_early_workspace_size(0, 4, 64, svw.SVW_BF16) == 0
 
 
 def test_opd_argument_validation(lib):
