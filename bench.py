@@ -376,6 +376,46 @@ def run_native(args, ws, rank, local):
         sep[name] = {"avg_us": us, "gbs": alg[name] / (us * 1e-6) / 1e9}
     sep["sum_us"] = sep["verify_T1"]["avg_us"] + sep["opd"]["avg_us"]
 
+    # ---- early-exit verification of the same batch: the same accepted lengths
+    # and tokens from the rows up to each request's first rejection ----
+    early_ws = torch.empty(svw.verify_early_workspace_size(N, R, V, svw.SVW_BF16), dtype=torch.uint8, device=dev)
+    nbytes = torch.zeros(1, dtype=torch.int64, device=dev)
+    acc_e = torch.empty(N, dtype=torch.int32, device=dev)
+    nxt_e = torch.empty(N, dtype=torch.int32, device=dev)
+    full_us = {0.0: avg_us["verify_T0"], 0.6: avg_us["verify_T0.6"], 1.0: sep["verify_T1"]["avg_us"]}
+    early = {}
+    for T in TEMPS:
+        def fn():
+            svw.spec_verify_early(t, d, cu, tok[T], T, 0, max_len=16, total_draft_rows=R, accept_len=acc_e,
+                                  next_token=nxt_e, status=status, bytes_read=nbytes, workspace=early_ws,
+                                  stream=stream)
+        fn()
+        torch.cuda.synchronize()
+        differ = int(((acc_e != acc[T]) | (nxt_e != nxt[T])).sum().item())
+        read = int(nbytes.item())
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(Ks):
+            fn()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        us = 1000.0 * s0.elapsed_time(s1) / Ks
+        kus = []
+        for _ in range(Ks):
+            k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            svw.time_next_launch("verify_early_cluster", k0, k1)
+            fn()
+            torch.cuda.synchronize()
+            kus.append(1000.0 * k0.elapsed_time(k1))
+        kus = float(np.mean(kus))
+        full_bytes = (rows_t if T == 0.0 else rows_t + R) * V * 2
+        early[f"T{T:g}"] = {"avg_us": us, "effective_positions_per_s": R / (us * 1e-6),
+                            "full_read_call_us": full_us[T], "speedup_vs_full_read": full_us[T] / us,
+                            "bytes_read": read, "read_frac": read / full_bytes,
+                            "kernel": "verify_early_cluster", "kernel_us": kus,
+                            "kernel_gbs": read / (kus * 1e-6) / 1e9,
+                            "requests_differing_from_spec_verify": differ}
+
     # ---- end to end through the public API with host buffers ----
     Ke = args.e2e_steps if args.e2e_steps is not None else max(3, min(K, 60))
     h_acc = {T: torch.empty(N, dtype=torch.int32).pin_memory() for T in TEMPS}
@@ -443,6 +483,7 @@ def run_native(args, ws, rank, local):
                       "main_kernel_gbs": kalg[c] / (kern_us[c] * 1e-6) / 1e9}
                   for c in calls},
         "separate_calls": sep,
+        "early_exit": early,
         "step_gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,
         "e2e": e2e,
         "gpu_launches": K * launches_per_step(),
