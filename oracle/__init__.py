@@ -32,6 +32,7 @@ FLAG_DEGENERATE = 4
 FLAG_BAD = 8
 FLAG_NEAR_CLIP = 16
 FLAG_NEAR_FLOOR = 32
+FLAG_NEAR_FILTER = 64
 
 _lib = None
 _lock = threading.Lock()
@@ -66,6 +67,11 @@ def _load():
                 P, P, ctypes.c_int, ctypes.c_int64, ctypes.c_int32, P, P,
                 ctypes.c_double, ctypes.c_uint64, ctypes.c_int32, P, P, P, P, P]
             lib.oracle_spec_verify.restype = ctypes.c_int
+            lib.oracle_spec_verify_filtered.argtypes = [
+                P, P, ctypes.c_int, ctypes.c_int64, ctypes.c_int32, P, P,
+                ctypes.c_double, ctypes.c_int32, ctypes.c_double, ctypes.c_uint64, ctypes.c_int32,
+                P, P, P, P]
+            lib.oracle_spec_verify_filtered.restype = ctypes.c_int
             lib.oracle_opd_loss.argtypes = [
                 P, P, ctypes.c_int, ctypes.c_int64, ctypes.c_int32, P,
                 ctypes.c_int64, ctypes.c_int32, ctypes.c_double, ctypes.c_double,
@@ -139,6 +145,31 @@ def spec_verify(target, draft, cu_draft, tokens, temperature, seed, max_len=32,
     if want_thr:
         out["thr"] = thr[: tok.shape[0]]
     return out
+
+
+def spec_verify_filtered(target, draft, cu_draft, tokens, temperature, top_k, top_p, seed, max_len=32,
+                         req_ids=None):
+    """Verification with both distributions top-k / top-p filtered (same T,
+    top_k, top_p); tokens drawn from the filtered draft distribution.
+    Returns dict(accept_len, next_token, flags)."""
+    lib = _load()
+    t, dt = _logits(target)
+    d, dd = _logits(draft)
+    assert dt == dd, "target and draft must share a dtype"
+    V = t.shape[-1]
+    cu = np.ascontiguousarray(cu_draft, dtype=np.int32)
+    tok = np.ascontiguousarray(tokens, dtype=np.int32)
+    N = cu.shape[0] - 1
+    rid = None if req_ids is None else np.ascontiguousarray(req_ids, dtype=np.int32)
+    acc = np.zeros(N, dtype=np.int32)
+    nxt = np.zeros(N, dtype=np.int32)
+    flg = np.zeros(N, dtype=np.int32)
+    rc = lib.oracle_spec_verify_filtered(_ptr(t), _ptr(d), dt, V, N, _ptr(cu), _ptr(tok), float(temperature),
+                                         int(top_k), float(top_p), int(seed), int(max_len), _ptr(rid),
+                                         _ptr(acc), _ptr(nxt), _ptr(flg))
+    if rc != 0:
+        raise MemoryError("oracle_spec_verify_filtered failed to allocate")
+    return dict(accept_len=acc, next_token=nxt, flags=flg)
 
 
 def opd_loss(target, draft, temperature=1.0, clip_c=1.0, lambda_ce=0.1, grad_scale=1.0,

@@ -61,6 +61,16 @@
  *    "Parallel Random Numbers: As Easy as 1, 2, 3", SC'11).
  *  - A row holding NaN, +Inf, or only -Inf has no softmax: the request (or
  *    OPD row) is reported bad.  At temperature 0 only NaN makes a row bad.
+ *  - Top-k / top-p filtered verification is not on the pages (a serving
+ *    variant).  This build's reading: both distributions are filtered with
+ *    the same (T, top_k, top_p) before the method runs.  Entries are ordered
+ *    by raw logit descending, smaller index first among equal logits; the
+ *    first K = min(top_k, V) are kept; of those, the shortest prefix whose
+ *    cumulative probability reaches top_p times their total (summed in that
+ *    order) is kept; the kept probabilities are renormalised.  The accept
+ *    test, residual and bonus draw then use the filtered p' and q'; a token
+ *    outside the target's kept set has p'(x) = 0 and is rejected.  At T = 0
+ *    filtering keeps the argmax, so greedy verification is unchanged.
  *  - Length head: the pages fix the layer order (per-position Linear + SiLU,
  *    mean over the k positions, Linear + sigmoid, times gamma, floor, clamp)
  *    but not the projected width H' (only H' < H); it is an argument.  The
@@ -83,6 +93,7 @@
 #define FLAG_BAD 8         /* invalid request / non-finite row            */
 #define FLAG_NEAR_CLIP 16  /* some |t_v| within 1e-5 * c of the clip c    */
 #define FLAG_NEAR_FLOOR 32 /* gamma a_hat k within 1e-4 of an integer       */
+#define FLAG_NEAR_FILTER 64 /* a top-p cut within 1e-5 of the threshold     */
 
 #define BAND 1e-5
 
@@ -347,6 +358,145 @@ int oracle_spec_verify(const void *target, const void *draft, int dtype, int64_t
   free(P);
   free(Q);
   free(R);
+  return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* top-k / top-p filtered verification (a serving variant; see above)  */
+/* ------------------------------------------------------------------ */
+static const double *g_sort_keys; /* logits of the row being ordered (single-threaded) */
+
+/* raw logit descending, smaller index first among equal logits */
+static int by_logit_desc(const void *a, const void *b) {
+  int64_t i = *(const int64_t *)a, j = *(const int64_t *)b;
+  double x = g_sort_keys[i], y = g_sort_keys[j];
+  if (x > y) return -1;
+  if (x < y) return 1;
+  return (i < j) ? -1 : (i > j);
+}
+
+/* out[v] = filtered softmax(x_row / T): keep the first min(top_k, V) entries
+ * in logit order, then the shortest prefix of those whose cumulative
+ * probability reaches top_p times their total; renormalise.  *near is set
+ * when the cumulative probability at the cut (or just before it) lies within
+ * BAND of the threshold.  keys, order: scratch of V entries. */
+static void row_filtered(const void *x, int dtype, int64_t row, int64_t V, double T, int32_t top_k, double top_p,
+                         double *out, double *keys, int64_t *order, int *near) {
+  row_softmax(x, dtype, row, V, T, out);
+  for (int64_t v = 0; v < V; ++v) {
+    keys[v] = elem(x, dtype, row, V, v);
+    order[v] = v;
+  }
+  g_sort_keys = keys;
+  qsort(order, (size_t)V, sizeof(int64_t), by_logit_desc);
+  int64_t K = (top_k >= 1 && (int64_t)top_k < V) ? (int64_t)top_k : V;
+  double Zk = 0.0;
+  for (int64_t n = 0; n < K; ++n) Zk += out[order[n]];
+  int64_t keep = K;
+  if (top_p < 1.0) {
+    double cum = 0.0, prev = 0.0, thr = top_p * Zk;
+    for (int64_t n = 0; n < K; ++n) {
+      prev = cum;
+      cum += out[order[n]];
+      if (cum >= thr) {
+        keep = n + 1;
+        if (fabs(cum - thr) < BAND * Zk || fabs(prev - thr) < BAND * Zk) *near = 1;
+        break;
+      }
+    }
+  }
+  double Zf = 0.0;
+  for (int64_t n = 0; n < keep; ++n) Zf += out[order[n]];
+  for (int64_t n = keep; n < V; ++n) out[order[n]] = 0.0;
+  for (int64_t n = 0; n < keep; ++n) out[order[n]] /= Zf;
+}
+
+/*
+ * Arguments as for oracle_spec_verify, plus top_k (1..V; values <= 0 or >= V
+ * keep every entry) and top_p (in (0, 1]; 1 keeps every entry of the top-k set).
+ * tokens are drawn from the filtered draft distribution q'.
+ */
+int oracle_spec_verify_filtered(const void *target, const void *draft, int dtype, int64_t V, int32_t N,
+                                const int32_t *cu, const int32_t *tokens, double temperature, int32_t top_k,
+                                double top_p, uint64_t seed, int32_t max_len, const int32_t *req_ids,
+                                int32_t *accept_len, int32_t *next_token, int32_t *flags) {
+  if (temperature == 0.0)
+    /* filtering keeps the argmax: greedy verification is unchanged */
+    return oracle_spec_verify(target, draft, dtype, V, N, cu, tokens, 0.0, seed, max_len, req_ids, accept_len,
+                              next_token, flags, NULL);
+  double *P = (double *)malloc(sizeof(double) * (size_t)V);
+  double *Q = (double *)malloc(sizeof(double) * (size_t)V);
+  double *R = (double *)malloc(sizeof(double) * (size_t)V);
+  double *keys = (double *)malloc(sizeof(double) * (size_t)V);
+  int64_t *order = (int64_t *)malloc(sizeof(int64_t) * (size_t)V);
+  if (!P || !Q || !R || !keys || !order) {
+    free(P); free(Q); free(R); free(keys); free(order);
+    return -1;
+  }
+  for (int32_t n = 0; n < N; ++n) {
+    int32_t L = cu[n + 1] - cu[n];
+    int64_t trow0 = (int64_t)cu[n] + n;
+    int64_t drow0 = (int64_t)cu[n];
+    uint32_t rid = req_ids ? (uint32_t)req_ids[n] : (uint32_t)n;
+    flags[n] = 0;
+    accept_len[n] = -1;
+    next_token[n] = -1;
+    if (L < 1 || L > max_len) {
+      flags[n] = FLAG_BAD;
+      continue;
+    }
+    int bad = 0;
+    for (int32_t j = 0; j < L; ++j)
+      if (tokens[drow0 + j] < 0 || tokens[drow0 + j] >= V) bad = 1;
+    for (int32_t j = 0; j <= L && !bad; ++j)
+      if (row_defects(target, dtype, trow0 + j, V)) bad = 1;
+    for (int32_t j = 0; j < L && !bad; ++j)
+      if (row_defects(draft, dtype, drow0 + j, V)) bad = 1;
+    if (bad) {
+      flags[n] = FLAG_BAD;
+      continue;
+    }
+    /* [DF] §5.2 eq. (6) with the filtered p' and q' */
+    int32_t a = L;
+    int near_filter = 0;
+    for (int32_t j = 0; j < L && a == L; ++j) {
+      int nf = 0;
+      row_filtered(target, dtype, trow0 + j, V, temperature, top_k, top_p, P, keys, order, &nf);
+      row_filtered(draft, dtype, drow0 + j, V, temperature, top_k, top_p, Q, keys, order, &nf);
+      near_filter |= nf;
+      int32_t x = tokens[drow0 + j];
+      double thr = (P[x] == 0.0) ? 0.0 : ((Q[x] > 0.0) ? fmin(1.0, P[x] / Q[x]) : 1.0);
+      double u = oracle_uniform(seed, rid, (uint32_t)j, 0u);
+      if (fabs(u - thr) < BAND) flags[n] |= FLAG_NEAR_ACCEPT;
+      if (!(u < thr)) a = j; /* leftmost rejection */
+    }
+    accept_len[n] = a;
+    double w = oracle_uniform(seed, rid, (uint32_t)a, 1u);
+    double Z = 0.0;
+    int nf = 0;
+    if (a < L) {
+      /* eq. (7) on the filtered distributions (P, Q still hold row a) */
+      for (int64_t v = 0; v < V; ++v) {
+        R[v] = fmax(0.0, P[v] - Q[v]);
+        Z += R[v];
+      }
+      if (Z == 0.0) {
+        flags[n] |= FLAG_DEGENERATE;
+        for (int64_t v = 0; v < V; ++v) {
+          R[v] = P[v];
+          Z += R[v];
+        }
+      }
+    } else {
+      row_filtered(target, dtype, trow0 + L, V, temperature, top_k, top_p, R, keys, order, &nf);
+      for (int64_t v = 0; v < V; ++v) Z += R[v];
+    }
+    if (near_filter || nf) flags[n] |= FLAG_NEAR_FILTER;
+    int near = 0;
+    next_token[n] = (int32_t)inverse_cdf(R, V, Z, w, &near);
+    if (near) flags[n] |= FLAG_NEAR_CDF;
+  }
+  free(P); free(Q); free(R); free(keys); free(order);
   return 0;
 }
 

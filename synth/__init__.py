@@ -176,6 +176,51 @@ def sample_tokens(draft, T: float, seed: int, tag: int = 7) -> np.ndarray:
     return out
 
 
+def filter_mask(row, T: float, top_k: int, top_p: float) -> np.ndarray:
+    """Kept entries of one row under top-k then top-p (order: logit
+    descending, smaller index first among equals; top_p is a fraction of the
+    top-k set's probability).  Used to draw filtered draft tokens."""
+    y = np.asarray(row, dtype=np.float64)
+    V = y.shape[0]
+    k = top_k if 1 <= top_k < V else V
+    if k < V:
+        # the k-th largest value, then ties at it in index order
+        kth = np.partition(-y, k - 1)[k - 1]
+        above = np.nonzero(-y < kth)[0]
+        ties = np.nonzero(-y == kth)[0][: k - above.shape[0]]
+        cand = np.concatenate([above, ties])
+    else:
+        cand = np.arange(V)
+    cand = cand[np.lexsort((cand, -y[cand]))]
+    e = np.exp((y[cand] - y[cand[0]]) / T)
+    c = np.cumsum(e)
+    n = int(np.searchsorted(c, top_p * c[-1], side="left")) + 1 if top_p < 1.0 else cand.shape[0]
+    keep = np.zeros(V, dtype=bool)
+    keep[cand[:min(n, cand.shape[0])]] = True
+    return keep
+
+
+def sample_tokens_filtered(draft, T: float, top_k: int, top_p: float, seed: int, tag: int = 9) -> np.ndarray:
+    """Draft tokens from the top-k / top-p filtered softmax(draft/T): Gumbel-max
+    over the kept entries."""
+    z = draft
+    R = z.shape[0]
+    out = np.zeros(R, dtype=np.int32)
+    rngs = _block_rngs(seed, 100 + tag, (R + BLOCK_ROWS - 1) // BLOCK_ROWS)
+
+    def work(b, r0, r1):
+        zz = as_f32(z[r0:r1]).astype(np.float64)
+        u = rngs[b].random(zz.shape)
+        g = -np.log(-np.log(np.maximum(u, 1e-300)))
+        for q in range(r1 - r0):
+            keep = filter_mask(zz[q], T, top_k, top_p)
+            s = np.where(keep, zz[q] / T + g[q], -np.inf)
+            out[r0 + q] = int(np.argmax(s))
+
+    _parallel_rows(R, work)
+    return out
+
+
 def make_batch(name: str, *, seed: int, lengths, V: int, dtype: str = "bf16",
                target_kind: str = "normal", target_sd: float = 3.0,
                zipf_s: float = 1.1, draft_kind: str = "add",
