@@ -151,6 +151,44 @@ svw_status spec_verify_early(const void *target_logits, const void *draft_logits
                              int32_t *next_token, int32_t *status, unsigned long long *bytes_read,
                              void *workspace, size_t workspace_bytes, void *stream);
 
+/* Largest top_k spec_verify_filtered accepts. */
+#define SVW_FILTER_MAX_K 1024
+
+/*
+ * spec_verify_filtered -- spec_verify with both distributions top-k / top-p
+ * filtered.
+ *
+ * The pages verify with the full temperature softmax; serving stacks usually
+ * filter first.  This variant is not on the pages and follows this reading:
+ * p and q are filtered with the same (temperature, top_k, top_p) -- entries
+ * ordered by raw logit descending, the smaller index first among equal
+ * logits; the first top_k kept; of those, the shortest prefix whose
+ * probability reaches top_p times their total kept; renormalised -- and the
+ * method of spec_verify ("DFlash 阅读笔记：并行起草、目标特征与精确验证" §5.2
+ * eqs. (6)-(8), Algorithm 1) runs on the filtered p' and q': x_j is accepted
+ * iff u_j < min(1, p'(x_j) / q'(x_j)) (a token outside the target's kept set
+ * is rejected; q'(x_j) = 0 with p'(x_j) > 0 is accepted), the next token is
+ * drawn from [p' - q']_+ at the rejected row or from p' at the bonus row, by
+ * the same inverse CDF in vocabulary order.  draft_tokens are drawn from q'.
+ *
+ * Arguments and results as for spec_verify, plus:
+ *   top_k         1 .. SVW_FILTER_MAX_K (a larger value returns
+ *                 SVW_ERR_UNSUPPORTED; values >= V keep every entry).
+ *   top_p         (0, 1]; 1 keeps the whole top-k set.
+ *   temperature   0 => greedy spec_verify (filtering keeps the argmax).
+ *   workspace     >= svw_verify_filtered_workspace_size(...) bytes.
+ * V is limited by shared memory (about 200 KB per CTA: V <= ~600 k for bf16
+ * at top_k <= 256); larger rows return SVW_ERR_UNSUPPORTED.
+ */
+size_t svw_verify_filtered_workspace_size(int32_t n_requests, int64_t total_draft_rows, int32_t V,
+                                          svw_dtype dtype);
+
+svw_status spec_verify_filtered(const void *target_logits, const void *draft_logits, svw_dtype dtype, int32_t V,
+                                int32_t N, const int32_t *cu_draft, int64_t total_draft_rows, int32_t max_len,
+                                const int32_t *draft_tokens, float temperature, int32_t top_k, float top_p,
+                                uint64_t seed, int32_t *accept_len, int32_t *next_token, int32_t *status,
+                                void *workspace, size_t workspace_bytes, void *stream);
+
 /*
  * opd_loss -- per draft row r (0 <= r < total_draft_rows), paired with one
  * target row:
@@ -300,7 +338,8 @@ svw_status spec_verify_noalloc(const void *target_logits, const void *draft_logi
  * svw_time_next_launch -- measurement hook, not part of the method.  Arms a
  * one-shot timer on the calling host thread: the next launch of the named
  * kernel made from this thread ("early_plan", "verify_stats",
- * "verify_finalize", "opd_fast_kernel", "opd_fix_kernel", "opd_exact_kernel",
+ * "verify_finalize", "verify_early_cluster", "filter_rows", "filtered_finalize",
+ * "opd_fast_kernel", "opd_fix_kernel", "opd_exact_kernel",
  * "fused_finalize", "length_head_gemm", "length_head_epilogue") records
  * begin_event just before it and end_event just after it on the launch stream (cudaEvent_t handles passed as void*, owned
  * by the caller).  kernel = NULL disarms.  The library records nothing

@@ -52,6 +52,11 @@ def lib():
             L.spec_verify_early.argtypes = [P, P, ctypes.c_int, I32, I32, P, I64, I32, P, F, U64,
                                             P, P, P, P, P, SZ, P]
             L.spec_verify_early.restype = ctypes.c_int
+            L.svw_verify_filtered_workspace_size.argtypes = [I32, I64, I32, ctypes.c_int]
+            L.svw_verify_filtered_workspace_size.restype = SZ
+            L.spec_verify_filtered.argtypes = [P, P, ctypes.c_int, I32, I32, P, I64, I32, P, F, I32, F, U64,
+                                               P, P, P, P, SZ, P]
+            L.spec_verify_filtered.restype = ctypes.c_int
             L.svw_opd_workspace_size.argtypes = [I64]
             L.svw_opd_workspace_size.restype = SZ
             L.opd_loss.argtypes = [P, P, ctypes.c_int, I32, I32, P, I64, I32, F, F, F, F,
@@ -199,6 +204,41 @@ def spec_verify_early(target, draft, cu_draft, draft_tokens, temperature: float,
                                  _ptr(draft_tokens), float(temperature), int(seed) & (2**64 - 1),
                                  _ptr(accept_len), _ptr(next_token), _ptr(status), _ptr(bytes_read),
                                  _ptr(workspace), workspace.numel(), _stream_ptr(stream))
+    _check(rc)
+    return accept_len, next_token
+
+
+SVW_FILTER_MAX_K = 1024
+
+
+def verify_filtered_workspace_size(n_requests: int, total_draft_rows: int, V: int, dtype_code: int) -> int:
+    return int(lib().svw_verify_filtered_workspace_size(n_requests, total_draft_rows, V, dtype_code))
+
+
+def spec_verify_filtered(target, draft, cu_draft, draft_tokens, temperature: float, top_k: int, top_p: float,
+                         seed: int, max_len: int = SVW_MAX_LEN, total_draft_rows: int | None = None,
+                         accept_len=None, next_token=None, status=None, workspace=None, stream=None):
+    """spec_verify with both distributions top-k / top-p filtered (draft tokens
+    drawn from the filtered draft distribution).  Returns (accept_len, next_token)."""
+    import torch
+    _need_cuda(target, draft, cu_draft, draft_tokens)
+    N = cu_draft.numel() - 1
+    V = target.shape[-1]
+    R = int(cu_draft[-1].item()) if total_draft_rows is None else int(total_draft_rows)
+    code = _dtype_code(target)
+    dev = target.device
+    if accept_len is None:
+        accept_len = torch.empty(N, dtype=torch.int32, device=dev)
+    if next_token is None:
+        next_token = torch.empty(N, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(1, verify_filtered_workspace_size(N, R, V, code)), dtype=torch.uint8,
+                                device=dev)
+    _need_cuda(accept_len, next_token, workspace, status)
+    rc = lib().spec_verify_filtered(_ptr(target), _ptr(draft), code, V, N, _ptr(cu_draft), R, max_len,
+                                    _ptr(draft_tokens), float(temperature), int(top_k), float(top_p),
+                                    int(seed) & (2**64 - 1), _ptr(accept_len), _ptr(next_token), _ptr(status),
+                                    _ptr(workspace), workspace.numel(), _stream_ptr(stream))
     _check(rc)
     return accept_len, next_token
 

@@ -173,6 +173,79 @@ size_t svw_verify_early_workspace_size(int32_t n_requests, int64_t total_draft_r
   return svw::early_layout(n_requests, total_draft_rows, V, esize_of(dtype)).total;
 }
 
+static_assert(svw::kFilterMaxK == SVW_FILTER_MAX_K, "one top-k limit");
+
+static size_t filtered_lists_bytes(int32_t N, int64_t R) {
+  const size_t rows = static_cast<size_t>(2 * R + N);
+  return (rows * 4 + 255) / 256 * 256 + 2 * ((rows * svw::kFilterMaxK * 4 + 255) / 256 * 256);
+}
+
+size_t svw_verify_filtered_workspace_size(int32_t n_requests, int64_t total_draft_rows, int32_t V,
+                                          svw_dtype dtype) {
+  const size_t v = svw_verify_workspace_size(n_requests, total_draft_rows, V, dtype);
+  if (v == 0) return 0;
+  const size_t f = filtered_lists_bytes(n_requests, total_draft_rows);
+  return v > f ? v : f;
+}
+
+svw_status spec_verify_filtered(const void *target_logits, const void *draft_logits, svw_dtype dtype, int32_t V,
+                                int32_t N, const int32_t *cu_draft, int64_t total_draft_rows, int32_t max_len,
+                                const int32_t *draft_tokens, float temperature, int32_t top_k, float top_p,
+                                uint64_t seed, int32_t *accept_len, int32_t *next_token, int32_t *status,
+                                void *workspace, size_t workspace_bytes, void *stream) {
+  if (dtype != SVW_F32 && dtype != SVW_BF16) return SVW_ERR_UNSUPPORTED;
+  if (V <= 0 || N <= 0 || total_draft_rows < 0 || max_len < 1) return SVW_ERR_INVALID_ARG;
+  if (max_len > SVW_MAX_LEN || V > kMaxV) return SVW_ERR_UNSUPPORTED;
+  if (!(top_p > 0.f && top_p <= 1.f)) return SVW_ERR_INVALID_ARG;
+  if (top_k < 1) return SVW_ERR_INVALID_ARG;
+  if (top_k > SVW_FILTER_MAX_K) return SVW_ERR_UNSUPPORTED;
+  if (!target_logits || !draft_logits || !cu_draft || !draft_tokens || !accept_len || !next_token ||
+      !workspace)
+    return workspace ? SVW_ERR_INVALID_ARG : SVW_ERR_WORKSPACE;
+  if (!(temperature >= 0.f) || !std::isfinite(temperature)) return SVW_ERR_INVALID_ARG;
+  if (temperature == 0.f)
+    // filtering keeps the argmax: greedy verification is unchanged
+    return spec_verify(target_logits, draft_logits, dtype, V, N, cu_draft, total_draft_rows, max_len, draft_tokens,
+                       0.f, seed, accept_len, next_token, status, workspace, workspace_bytes, stream);
+  const double kd = 1.4426950408889634 / static_cast<double>(temperature);
+  if (!(kd < 3.0e38)) return SVW_ERR_INVALID_ARG;
+  const int es = esize_of(dtype);
+  if (!aligned(target_logits, es) || !aligned(draft_logits, es) || !aligned(cu_draft, 4) ||
+      !aligned(draft_tokens, 4) || !aligned(accept_len, 4) || !aligned(next_token, 4) ||
+      (status && !aligned(status, 4)) || !aligned(workspace, 256))
+    return SVW_ERR_MISALIGNED;
+  if (workspace_bytes < svw_verify_filtered_workspace_size(N, total_draft_rows, V, dtype)) return SVW_ERR_WORKSPACE;
+  if (svw::filter_smem_bytes(V, es, top_k) > 200 * 1024) return SVW_ERR_UNSUPPORTED;
+  const size_t rows = static_cast<size_t>(2 * total_draft_rows + N);
+  char *ws = static_cast<char *>(workspace);
+  svw::FilterArgs a{};
+  a.target = target_logits;
+  a.draft = draft_logits;
+  a.V = V;
+  a.N = N;
+  a.cu = cu_draft;
+  a.R = total_draft_rows;
+  a.rows_t = total_draft_rows + N;
+  a.max_len = max_len;
+  a.tokens = draft_tokens;
+  a.k = static_cast<float>(kd);
+  a.top_k = top_k;
+  a.top_p = top_p;
+  a.cand = svw::filter_candidates(top_k);
+  a.seed = seed;
+  a.accept_len = accept_len;
+  a.next_token = next_token;
+  a.status = status;
+  a.cnt = reinterpret_cast<int32_t *>(ws);
+  const size_t off1 = (rows * 4 + 255) / 256 * 256;
+  a.lidx = reinterpret_cast<int32_t *>(ws + off1);
+  a.lp = reinterpret_cast<float *>(ws + off1 + (rows * svw::kFilterMaxK * 4 + 255) / 256 * 256);
+  const bool vec = ((static_cast<int64_t>(V) * es) % 16 == 0) && aligned(target_logits, 16) &&
+                   aligned(draft_logits, 16);
+  const cudaError_t e = svw::launch_filtered(a, dtype, vec, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SVW_OK : SVW_ERR_CUDA;
+}
+
 svw_status spec_verify_early(const void *target_logits, const void *draft_logits, svw_dtype dtype, int32_t V,
                              int32_t N, const int32_t *cu_draft, int64_t total_draft_rows, int32_t max_len,
                              const int32_t *draft_tokens, float temperature, uint64_t seed, int32_t *accept_len,

@@ -132,6 +132,34 @@ int launch_length_head(const void *hidden, const void *w1, const float *b1, cons
 int launch_length_label(const int32_t *accept_len, const int32_t *cu, const float *a_hat, int32_t N,
                         float *a_star, float *loss, cudaStream_t stream);
 
+// top-k / top-p filtered verification (filtered.cu)
+constexpr int kFilterMaxK = 1024;  // largest top_k (one kept entry per thread of a CTA)
+struct FilterArgs {
+  const void *target;
+  const void *draft;
+  int64_t V;
+  int32_t N;
+  const int32_t *cu;
+  int64_t R;       // draft rows
+  int64_t rows_t;  // target rows (R + N)
+  int32_t max_len;
+  const int32_t *tokens;
+  float k;  // log2(e) / T  (T > 0)
+  int32_t top_k;
+  float top_p;
+  int32_t cand;  // candidate slots per CTA
+  uint64_t seed;
+  int32_t *accept_len;
+  int32_t *next_token;
+  int32_t *status;
+  int32_t *cnt;   // [rows_t + R] kept entries per row (-1: the row has no softmax)
+  int32_t *lidx;  // [rows_t + R][kFilterMaxK] kept indices, ascending
+  float *lp;      // [rows_t + R][kFilterMaxK] their filtered probabilities
+};
+int filter_candidates(int32_t top_k);
+size_t filter_smem_bytes(int64_t V, int esize, int32_t top_k);
+cudaError_t launch_filtered(const FilterArgs &a, int dtype, bool vec, cudaStream_t stream);
+
 struct OpdArgs {
   const void *target;
   const void *draft;

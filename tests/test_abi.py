@@ -29,7 +29,8 @@ def test_header_symbols_exported(lib):
     names = _declared_functions()
     assert {"spec_verify", "opd_loss", "svw_verify_workspace_size", "svw_opd_workspace_size",
             "svw_status_string", "svw_version", "spec_verify_noalloc", "spec_verify_early",
-            "svw_verify_early_workspace_size"} <= set(names)
+            "svw_verify_early_workspace_size", "spec_verify_filtered",
+            "svw_verify_filtered_workspace_size"} <= set(names)
     for n in names:
         assert hasattr(lib, n), f"{n} declared in svw.h but not exported"
 
@@ -114,6 +115,33 @@ def test_verify_early_argument_validation(lib):
     for args in ((2, 4, 64, svw.SVW_BF16), (256, 1964, 151936, svw.SVW_BF16), (4, 64, 1024, svw.SVW_F32)):
         assert svw.verify_early_workspace_size(*args) > svw.verify_workspace_size(*args)
     assert svw.verify_early_workspace_size(0, 4, 64, svw.SVW_BF16) == 0
+
+
+def test_verify_filtered_argument_validation(lib):
+    import serving_vocab_wide_gb300 as svw
+    keep, p = _fake(4096)
+    ok_args = dict(t=p, d=p, dt=1, V=64, N=2, cu=p, R=4, ml=16, tok=p, T=1.0, k=20, tp=0.9, seed=0,
+                   acc=p, nxt=p, st=None, ws=p, wsb=1 << 30)
+
+    def call(**kw):
+        a = dict(ok_args, **kw)
+        return lib.spec_verify_filtered(a["t"], a["d"], a["dt"], a["V"], a["N"], a["cu"], a["R"], a["ml"],
+                                        a["tok"], a["T"], a["k"], a["tp"], a["seed"], a["acc"], a["nxt"], a["st"],
+                                        a["ws"], a["wsb"], None)
+
+    assert call(dt=7) == 2
+    assert call(k=0) == 1
+    assert call(k=1025) == 2                # above SVW_FILTER_MAX_K
+    assert call(tp=0.0) == 1
+    assert call(tp=1.5) == 1
+    assert call(tp=float("nan")) == 1
+    assert call(T=-1.0) == 1
+    assert call(ws=None) == 4
+    assert call(t=ctypes.c_void_p(p.value + 1)) == 3
+    need = svw.verify_filtered_workspace_size(2, 4, 64, svw.SVW_BF16)
+    assert call(wsb=need - 1) == 4
+    for args in ((2, 4, 64, svw.SVW_BF16), (256, 1964, 151936, svw.SVW_BF16)):
+        assert svw.verify_filtered_workspace_size(*args) >= svw.verify_workspace_size(*args)
 
 
 def test_opd_argument_validation(lib):
