@@ -105,6 +105,8 @@ CALL_KERNELS = {
     "length_head": "length_head_label + length_head_gemm (cuBLASLt bf16 GEMM) + length_head_epilogue",
 }
 CALLS = ["verify_T0", "verify_T0.6", "verify_T1+opd", "length_head"]
+# top-k / top-p settings of the filtered-verification measurement: (T, top_k, top_p)
+FILTERS = [(1.0, 50, 0.9), (0.6, 20, 0.95)]
 HEAD = dict(k=16, H=4096, Hp=256, gamma=1.0)
 WORKLOAD = ("mix: N=256 ragged L_i~U{2,4,8,16}, V=151936, bf16 log-Zipf logits; verify at T=0 and 0.6, "
             "verify at T=1 fused with OPD fwd/bwd (T=1,c=1,lambda=0.1); length head label + forward "
@@ -416,6 +418,42 @@ def run_native(args, ws, rank, local):
                             "kernel_gbs": read / (kus * 1e-6) / 1e9,
                             "requests_differing_from_spec_verify": differ}
 
+    # ---- top-k / top-p filtered verification of the same batch (draft tokens
+    # redrawn from the filtered draft distribution) ----
+    filt_ws = torch.empty(svw.verify_filtered_workspace_size(N, R, V, svw.SVW_BF16), dtype=torch.uint8,
+                          device=dev)
+    filtered = {}
+    for T, kf, pf in FILTERS:
+        import synth
+        ftok = torch.from_numpy(synth.sample_tokens_filtered(b.draft, T, kf, pf, 4000 + rank)).to(dev)
+
+        def fn():
+            svw.spec_verify_filtered(t, d, cu, ftok, T, kf, pf, 0, max_len=16, total_draft_rows=R,
+                                     accept_len=acc_e, next_token=nxt_e, status=status, workspace=filt_ws,
+                                     stream=stream)
+        fn()
+        torch.cuda.synchronize()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(Ks):
+            fn()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        us = 1000.0 * s0.elapsed_time(s1) / Ks
+        kus = []
+        for _ in range(Ks):
+            k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            svw.time_next_launch("filter_rows", k0, k1)
+            fn()
+            torch.cuda.synchronize()
+            kus.append(1000.0 * k0.elapsed_time(k1))
+        kus = float(np.mean(kus))
+        rows_bytes = (rows_t + R) * V * 2
+        filtered[f"T{T:g}_k{kf}_p{pf:g}"] = {
+            "avg_us": us, "positions_per_s": R / (us * 1e-6), "kernel": "filter_rows", "kernel_us": kus,
+            "kernel_gbs": rows_bytes / (kus * 1e-6) / 1e9, "algorithmic_bytes": rows_bytes,
+            "mean_accept_len": float(acc_e.float().mean().item())}
+
     # ---- end to end through the public API with host buffers ----
     Ke = args.e2e_steps if args.e2e_steps is not None else max(3, min(K, 60))
     h_acc = {T: torch.empty(N, dtype=torch.int32).pin_memory() for T in TEMPS}
@@ -484,6 +522,7 @@ def run_native(args, ws, rank, local):
                   for c in calls},
         "separate_calls": sep,
         "early_exit": early,
+        "filtered": filtered,
         "step_gbs": step_bytes / (ms_per_step * 1e-3) / 1e9,
         "e2e": e2e,
         "gpu_launches": K * launches_per_step(),
