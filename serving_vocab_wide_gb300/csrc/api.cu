@@ -232,6 +232,7 @@ svw_status spec_verify_filtered(const void *target_logits, const void *draft_log
   a.top_k = top_k;
   a.top_p = top_p;
   a.cand = svw::filter_candidates(top_k);
+  a.gs = svw::filter_group(top_k);
   a.seed = seed;
   a.accept_len = accept_len;
   a.next_token = next_token;

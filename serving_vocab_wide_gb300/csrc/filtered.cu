@@ -44,9 +44,9 @@ namespace svw {
 
 namespace {
 
-constexpr int kFT = 1024;  // threads of filter_rows
+constexpr int kFT = 512;  // threads of filter_rows (two CTAs per SM: one streams while the other sorts)
 constexpr int kFW = kFT / 32;
-constexpr int kUnroll = 4;  // groups per thread whose loads are in flight together
+constexpr int kUnroll = 8;  // vectors per thread whose loads are in flight together
 
 // order-preserving keys: a larger logit has a larger key; -0 is keyed as +0
 __device__ __forceinline__ uint32_t key_of_bits16(uint32_t b) {
@@ -144,13 +144,13 @@ __device__ __forceinline__ uint32_t block_scan_u32(uint32_t v, FSmem &sm, uint32
   if (lane == 31) sm.wu[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    uint32_t w = sm.wu[lane];
+    uint32_t w = (lane < kFW) ? sm.wu[lane] : 0u;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
       if (lane >= o) w += y;
     }
-    sm.wu[lane] = w;  // inclusive over warps
+    if (lane < kFW) sm.wu[lane] = w;  // inclusive over warps
   }
   __syncthreads();
   const uint32_t r = x + (warp ? sm.wu[warp - 1] : 0u);
@@ -159,7 +159,9 @@ __device__ __forceinline__ uint32_t block_scan_u32(uint32_t v, FSmem &sm, uint32
   return r;
 }
 
-__device__ __forceinline__ float block_scan_f32(float v, FSmem &sm, float *total) {
+// the same for floats (fixed order of additions), also giving the exclusive
+// prefix: the inclusive value of the thread before (0 for thread 0)
+__device__ __forceinline__ float block_scan_f32(float v, FSmem &sm, float *total, float *excl) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   float x = v;
 #pragma unroll
@@ -167,19 +169,22 @@ __device__ __forceinline__ float block_scan_f32(float v, FSmem &sm, float *total
     const float y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x = __fadd_rn(x, y);
   }
+  const float xe = __shfl_up_sync(0xffffffffu, x, 1);
   if (lane == 31) sm.wf[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    float w = sm.wf[lane];
+    float w = (lane < kFW) ? sm.wf[lane] : 0.f;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const float y = __shfl_up_sync(0xffffffffu, w, o);
       if (lane >= o) w = __fadd_rn(w, y);
     }
-    sm.wf[lane] = w;
+    if (lane < kFW) sm.wf[lane] = w;
   }
   __syncthreads();
-  const float r = warp ? __fadd_rn(sm.wf[warp - 1], x) : x;
+  const float base = warp ? sm.wf[warp - 1] : 0.f;
+  const float r = warp ? __fadd_rn(base, x) : x;
+  *excl = (lane == 0) ? base : (warp ? __fadd_rn(base, xe) : xe);
   *total = sm.wf[kFW - 1];
   __syncthreads();
   return r;
@@ -226,47 +231,117 @@ __device__ void bitonic(uint32_t *key, int32_t *idx, float *val, int P) {
   }
 }
 
+// the largest of the 8 entries of vector q (entries 8q .. 8q+7; entries past
+// V count as -inf) and whether any of them is NaN
 template <int DT, bool VEC>
-__global__ void __launch_bounds__(kFT, 1) filter_rows(FilterArgs a) {
+__device__ __forceinline__ void vector_max(const char *row, int64_t q, int64_t V, float &mx, bool &nan) {
+  const int64_t v0 = q * 8;
+  if (VEC && v0 + 8 <= V) {
+    if (DT == 1) {
+      const uint4 w = ld_vec(row + v0 * 2);
+      const uint32_t m2 = bf16x2_max_nan(bf16x2_max_nan(w.x, w.y), bf16x2_max_nan(w.z, w.w));
+      nan = bf16x2_nan(m2) != 0;
+      const float2 f = bf16x2_f2(m2);
+      mx = fmaxf(f.x, f.y);
+    } else {
+      const uint4 w0 = ld_vec(row + v0 * 4), w1 = ld_vec(row + v0 * 4 + 16);
+      const float x[8] = {__uint_as_float(w0.x), __uint_as_float(w0.y), __uint_as_float(w0.z),
+                          __uint_as_float(w0.w), __uint_as_float(w1.x), __uint_as_float(w1.y),
+                          __uint_as_float(w1.z), __uint_as_float(w1.w)};
+      mx = -INFINITY;
+      nan = false;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        nan |= (x[e] != x[e]);
+        mx = fmaxf(mx, x[e]);
+      }
+    }
+  } else {
+    mx = -INFINITY;
+    nan = false;
+    for (int e = 0; e < 8; ++e)
+      if (v0 + e < V) {
+        const float x = Elem<DT>::load(row, v0 + e);
+        nan |= (x != x);
+        mx = fmaxf(mx, x);
+      }
+  }
+}
+
+// the rank of candidate t among the C in (key descending, index ascending)
+// order: how many candidates come before it
+__device__ __forceinline__ int rank_desc(const uint32_t *key, const int32_t *idx, int C, int t) {
+  const uint32_t kt = key[t];
+  const int32_t it = idx[t];
+  int r = 0;
+  for (int j = 0; j < C; ++j) {
+    const uint32_t kj = key[j];
+    r += (kj > kt || (kj == kt && idx[j] < it)) ? 1 : 0;
+  }
+  return r;
+}
+
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(kFT, 2) filter_rows(FilterArgs a) {
   using KeyT = typename std::conditional<DT == 1, unsigned short, uint32_t>::type;
   extern __shared__ __align__(16) unsigned char dyn[];
   __shared__ FSmem sm;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t V = a.V;
-  const int64_t NG = (V + 7) / 8;
-  const int kCand = a.cand;  // 8 x (top_k rounded up to a power of two): fits every entry above tau
+  const int gv = a.gs / 8;                  // 16-byte (8-entry) vectors per group, a power of two <= 16
+  const int64_t NVec = (V + 7) / 8;         // 8-entry vectors of the row
+  const int64_t NG = (NVec + gv - 1) / gv;  // groups
+  const int kCand = a.cand;                 // gs x (top_k rounded up to a power of two)
   uint32_t *ckey = reinterpret_cast<uint32_t *>(dyn);
   int32_t *cidx = reinterpret_cast<int32_t *>(ckey + kCand);
-  float *cval = reinterpret_cast<float *>(cidx + kCand);
-  KeyT *gkey = reinterpret_cast<KeyT *>(cval + kCand);
+  uint32_t *skey = reinterpret_cast<uint32_t *>(cidx + kCand);  // [kFilterMaxK] in logit order
+  int32_t *sidx = reinterpret_cast<int32_t *>(skey + kFilterMaxK);
+  float *spv = reinterpret_cast<float *>(sidx + kFilterMaxK);  // their probabilities (unnormalised)
+  KeyT *gkey = reinterpret_cast<KeyT *>(spv + kFilterMaxK);
   const int64_t nrows = a.rows_t + a.R;
   const uint32_t K = static_cast<uint32_t>(min(static_cast<int64_t>(a.top_k), V));
 
   for (int64_t r = blockIdx.x; r < nrows; r += gridDim.x) {
     const char *row = (r < a.rows_t) ? static_cast<const char *>(a.target) + r * V * Elem<DT>::kSize
                                      : static_cast<const char *>(a.draft) + (r - a.rows_t) * V * Elem<DT>::kSize;
-    // ---- pass 1: group maxima (keys), row maximum, NaN ----
+    // ---- pass 1: each group's largest entry (as a key), the row maximum, NaN ----
+    // thread t of a round holds vector t; a group is gv consecutive lanes
     float mx = -INFINITY;
     bool nan = false;
-    for (int64_t g0 = tid; g0 < NG; g0 += kUnroll * kFT) {
-      uint32_t k[kUnroll][8];
-      bool gn[kUnroll];
-      float gm[kUnroll];
+    for (int64_t q0 = 0; q0 < NVec; q0 += static_cast<int64_t>(kUnroll) * kFT) {
+      float vm[kUnroll];
+      bool vn[kUnroll];
+      if (VEC && DT == 1 && q0 + static_cast<int64_t>(kUnroll) * kFT <= V / 8) {
+        // a whole round of full vectors: every load in flight before any arithmetic
+        uint4 w[kUnroll];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int64_t g = g0 + static_cast<int64_t>(u) * kFT;
-        if (g < NG) group_keys<DT, VEC>(row, g, V, k[u], gn[u], gm[u]);
+        for (int u = 0; u < kUnroll; ++u) w[u] = ld_vec(row + (q0 + static_cast<int64_t>(u) * kFT + tid) * 16);
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const uint32_t m2 = bf16x2_max_nan(bf16x2_max_nan(w[u].x, w[u].y), bf16x2_max_nan(w[u].z, w[u].w));
+          vn[u] = bf16x2_nan(m2) != 0;
+          const float2 f = bf16x2_f2(m2);
+          vm[u] = fmaxf(f.x, f.y);
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const int64_t q = q0 + static_cast<int64_t>(u) * kFT + tid;
+          vm[u] = -INFINITY;
+          vn[u] = false;
+          if (q < NVec) vector_max<DT, VEC>(row, q, V, vm[u], vn[u]);
+        }
       }
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
-        const int64_t g = g0 + static_cast<int64_t>(u) * kFT;
-        if (g < NG) {
-          nan |= gn[u];
-          mx = fmaxf(mx, gm[u]);
-          uint32_t km = 0;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) km = max(km, k[u][e]);
-          gkey[g] = static_cast<KeyT>(DT == 1 ? (km >> 16) : km);
+        const int64_t q = q0 + static_cast<int64_t>(u) * kFT + tid;
+        nan |= vn[u];
+        mx = fmaxf(mx, vm[u]);
+        float gm = vm[u];
+        for (int o = 1; o < gv; o <<= 1) gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, o));
+        if ((lane & (gv - 1)) == 0 && q < NVec) {
+          const uint32_t kk = (DT == 1) ? key_of_bits16(__float_as_uint(gm) >> 16) : key_of_f32(gm);
+          gkey[q / gv] = static_cast<KeyT>(DT == 1 ? (kk >> 16) : kk);
         }
       }
     }
@@ -277,7 +352,7 @@ __global__ void __launch_bounds__(kFT, 1) filter_rows(FilterArgs a) {
     if (tid == 0) sm.ncand = 0;
     __syncthreads();
     if (warp == 0) {
-      float w = sm.wf[lane];
+      float w = (lane < kFW) ? sm.wf[lane] : -INFINITY;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) w = fmaxf(w, __shfl_xor_sync(0xffffffffu, w, o));
       if (lane == 0) {
@@ -296,9 +371,7 @@ __global__ void __launch_bounds__(kFT, 1) filter_rows(FilterArgs a) {
     // ---- tau: the K-th largest group maximum (radix select, 8-bit digits) ----
     constexpr int kBits = (DT == 1) ? 16 : 32;
     uint32_t prefix = 0, pmask = 0, need = K;
-    if (static_cast<int64_t>(K) >= NG) {
-      prefix = 0;  // every group qualifies: tau is the smallest key
-    } else {
+    if (static_cast<int64_t>(K) < NG) {
       for (int shift = kBits - 8; shift >= 0; shift -= 8) {
         for (int b = tid; b < 256; b += kFT) sm.hist[b] = 0;
         __syncthreads();
@@ -342,43 +415,68 @@ __global__ void __launch_bounds__(kFT, 1) filter_rows(FilterArgs a) {
         __syncthreads();
       }
     }
-    const uint32_t tau = (DT == 1) ? (prefix << 16) : prefix;  // as a full 32-bit key
+    // as a full 32-bit key; when every group qualifies, 0 (below every real key)
+    const uint32_t tau = (static_cast<int64_t>(K) < NG) ? ((DT == 1) ? (prefix << 16) : prefix) : 1u;
 
-    // ---- gather: every entry above tau (fewer than 8 K), any order ----
-    for (int64_t g = tid; g < NG; g += kFT) {
-      const uint32_t kg = (DT == 1) ? (static_cast<uint32_t>(gkey[g]) << 16) : static_cast<uint32_t>(gkey[g]);
-      if (kg > tau) {
+    // ---- gather every entry at or above tau, from the vectors of the groups that reach it ----
+    const int lgv = __ffs(gv) - 1;
+    auto gkey32 = [&](int64_t g) -> uint32_t {
+      return (DT == 1) ? (static_cast<uint32_t>(gkey[g]) << 16) : static_cast<uint32_t>(gkey[g]);
+    };
+    for (int64_t q = tid; q < NVec; q += kFT) {
+      if (gkey32(q >> lgv) >= tau) {
         uint32_t k[8];
         bool gn;
         float gm;
-        group_keys<DT, VEC>(row, g, V, k, gn, gm);
+        group_keys<DT, VEC>(row, q, V, k, gn, gm);
 #pragma unroll
         for (int e = 0; e < 8; ++e)
-          if (k[e] > tau) {
+          if (k[e] >= tau) {
             const int p = atomicAdd(&sm.ncand, 1);
             if (p < kCand) {
               ckey[p] = k[e];
-              cidx[p] = static_cast<int32_t>(g * 8 + e);
+              cidx[p] = static_cast<int32_t>(q * 8 + e);
             }
           }
       }
     }
     __syncthreads();
-    const uint32_t above = static_cast<uint32_t>(sm.ncand);  // < 8 K by the choice of tau
-    // ---- then entries equal to tau, in index order, while fewer than K ----
-    if (above < K) {
-      uint32_t want = K - above, base = 0;
-      for (int64_t g0 = 0; g0 < NG && base < want; g0 += kFT) {
-        const int64_t g = g0 + tid;
+    if (sm.ncand > kCand) {
+      // many entries equal to tau: every entry above tau (fewer than gs K),
+      // then those equal to tau in index order while fewer than K
+      __syncthreads();
+      if (tid == 0) sm.ncand = 0;
+      __syncthreads();
+      for (int64_t q = tid; q < NVec; q += kFT) {
+        if (gkey32(q >> lgv) > tau) {
+          uint32_t k[8];
+          bool gn;
+          float gm;
+          group_keys<DT, VEC>(row, q, V, k, gn, gm);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            if (k[e] > tau) {
+              const int p = atomicAdd(&sm.ncand, 1);
+              if (p < kCand) {
+                ckey[p] = k[e];
+                cidx[p] = static_cast<int32_t>(q * 8 + e);
+              }
+            }
+        }
+      }
+      __syncthreads();
+      const uint32_t above = static_cast<uint32_t>(sm.ncand);
+      const uint32_t want = (above < K) ? K - above : 0u;
+      uint32_t base = 0;
+      for (int64_t q0 = 0; q0 < NVec && base < want; q0 += kFT) {
+        const int64_t q = q0 + tid;
         uint32_t k[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         uint32_t c = 0;
-        if (g < NG) {
-          const uint32_t kg =
-              (DT == 1) ? (static_cast<uint32_t>(gkey[g]) << 16) : static_cast<uint32_t>(gkey[g]);
-          if (kg >= tau) {
+        if (q < NVec) {
+          if (gkey32(q >> lgv) >= tau) {
             bool gn;
             float gm;
-            group_keys<DT, VEC>(row, g, V, k, gn, gm);
+            group_keys<DT, VEC>(row, q, V, k, gn, gm);
 #pragma unroll
             for (int e = 0; e < 8; ++e) c += (k[e] == tau) ? 1u : 0u;
           }
@@ -391,7 +489,7 @@ __global__ void __launch_bounds__(kFT, 1) filter_rows(FilterArgs a) {
           if (c && k[e] == tau) {
             if (rank < want) {
               ckey[above + rank] = k[e];
-              cidx[above + rank] = static_cast<int32_t>(g * 8 + e);
+              cidx[above + rank] = static_cast<int32_t>(q * 8 + e);
             }
             ++rank;
           }
@@ -402,41 +500,61 @@ __global__ void __launch_bounds__(kFT, 1) filter_rows(FilterArgs a) {
       __syncthreads();
     }
     const int C = min(sm.ncand, kCand);
-    // ---- sort the candidates by logit (then index); the first K are kept ----
-    int P = 1;
-    while (P < C) P <<= 1;
-    for (int i = C + tid; i < P; i += kFT) {
-      ckey[i] = 0u;
-      cidx[i] = INT32_MAX;
-    }
-    __syncthreads();
-    bitonic<true>(ckey, cidx, nullptr, P);
     const int Kc = min(static_cast<int>(K), C);
+    // ---- the first K candidates in (logit descending, index ascending) order ----
+    if (C <= kFilterMaxK) {
+      // rank sort: every candidate counts those before it
+      for (int t = tid; t < C; t += kFT) {
+        const int rk = rank_desc(ckey, cidx, C, t);
+        if (rk < Kc) {
+          skey[rk] = ckey[t];
+          sidx[rk] = cidx[t];
+        }
+      }
+      __syncthreads();
+    } else {
+      int P = 1;
+      while (P < C) P <<= 1;
+      for (int i = C + tid; i < P; i += kFT) {
+        ckey[i] = 0u;
+        cidx[i] = INT32_MAX;
+      }
+      __syncthreads();
+      bitonic<true>(ckey, cidx, nullptr, P);
+      for (int t = tid; t < Kc; t += kFT) {
+        skey[t] = ckey[t];
+        sidx[t] = cidx[t];
+      }
+      __syncthreads();
+    }
     // ---- probabilities in that order; the top-p cut; renormalised ----
-    float pv = 0.f;
-    if (tid < Kc) pv = ex2(__fmul_rn(__fsub_rn(value_of_key<DT>(ckey[tid]), m), a.k));
-    float zk;
-    const float cum = block_scan_f32(pv, sm, &zk);
+    // thread t holds entries 2t and 2t + 1; the prefix is fixed-order
+    for (int t = tid; t < Kc; t += kFT) spv[t] = ex2(__fmul_rn(__fsub_rn(value_of_key<DT>(skey[t]), m), a.k));
+    __syncthreads();
+    const int e0 = 2 * tid;
+    const float a0 = (e0 < Kc) ? spv[e0] : 0.f, a1 = (e0 + 1 < Kc) ? spv[e0 + 1] : 0.f;
+    float zk, excl;
+    const float cum1 = block_scan_f32(__fadd_rn(a0, a1), sm, &zk, &excl);
+    const float cum0 = __fadd_rn(excl, a0);
     int np = Kc;
     if (a.top_p < 1.f) {
       const float thr = __fmul_rn(a.top_p, zk);
-      np = min(Kc, __syncthreads_count(tid < Kc && cum < thr) + 1);
+      const uint32_t below = ((e0 < Kc && cum0 < thr) ? 1u : 0u) + ((e0 + 1 < Kc && cum1 < thr) ? 1u : 0u);
+      uint32_t nb;
+      block_scan_u32(below, sm, &nb);
+      np = min(Kc, static_cast<int>(nb) + 1);
     }
-    if (tid == np - 1) sm.zf = cum;
+    if (e0 == np - 1) sm.zf = cum0;
+    if (e0 + 1 == np - 1) sm.zf = cum1;
     __syncthreads();
     const float zf = sm.zf;
-    // the kept entries, sorted by index, with p' = p / (kept mass)
-    int Q = 1;
-    while (Q < np) Q <<= 1;  // Q <= top_k rounded up <= the candidate slots
-    if (tid < Q) {
-      cval[tid] = (tid < np) ? __fdiv_rn(pv, zf) : 0.f;
-      if (tid >= np) cidx[tid] = INT32_MAX;
-    }
-    __syncthreads();
-    bitonic<false>(ckey, cidx, cval, Q);
-    if (tid < np) {
-      a.lidx[r * kFilterMaxK + tid] = cidx[tid];
-      a.lp[r * kFilterMaxK + tid] = cval[tid];
+    // ---- stored sorted by index (rank by index among the kept), p' = p / kept mass ----
+    for (int t = tid; t < np; t += kFT) {
+      const int32_t it = sidx[t];
+      int rk = 0;
+      for (int j = 0; j < np; ++j) rk += (sidx[j] < it) ? 1 : 0;
+      a.lidx[r * kFilterMaxK + rk] = it;
+      a.lp[r * kFilterMaxK + rk] = __fdiv_rn(spv[t], zf);
     }
     if (tid == 0) a.cnt[r] = np;
     __syncthreads();
@@ -564,15 +682,29 @@ __global__ void __launch_bounds__(32 * kFinReqPerCta) filtered_finalize(FilterAr
 
 }  // namespace
 
-int filter_candidates(int32_t top_k) {
+// top_k rounded up to a power of two
+static int pow2_at_least(int32_t k) {
   int P = 1;
-  while (P < top_k) P <<= 1;
-  return 8 * P;
+  while (P < k) P <<= 1;
+  return P;
 }
 
+// entries per group: as large as the candidate space allows (every entry above
+// tau lies in one of fewer than top_k groups), between 8 and 128
+int filter_group(int32_t top_k) {
+  int gs = 8192 / pow2_at_least(top_k);
+  if (gs < 8) gs = 8;
+  if (gs > 128) gs = 128;
+  return gs;
+}
+
+int filter_candidates(int32_t top_k) { return filter_group(top_k) * pow2_at_least(top_k); }
+
 size_t filter_smem_bytes(int64_t V, int esize, int32_t top_k) {
-  const int64_t NG = (V + 7) / 8;
-  return static_cast<size_t>(filter_candidates(top_k)) * 12 + static_cast<size_t>(NG) * (esize == 2 ? 2 : 4);
+  const int64_t gv = filter_group(top_k) / 8;
+  const int64_t NG = ((V + 7) / 8 + gv - 1) / gv;
+  return static_cast<size_t>(filter_candidates(top_k)) * 8 + static_cast<size_t>(kFilterMaxK) * 12 +
+         static_cast<size_t>(NG) * (esize == 2 ? 2 : 4);
 }
 
 cudaError_t launch_filtered(const FilterArgs &a, int dtype, bool vec, cudaStream_t st) {

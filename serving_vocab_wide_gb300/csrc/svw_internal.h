@@ -148,6 +148,7 @@ struct FilterArgs {
   int32_t top_k;
   float top_p;
   int32_t cand;  // candidate slots per CTA
+  int32_t gs;    // entries per group (8 .. 128, a power of two)
   uint64_t seed;
   int32_t *accept_len;
   int32_t *next_token;
@@ -157,6 +158,7 @@ struct FilterArgs {
   float *lp;      // [rows_t + R][kFilterMaxK] their filtered probabilities
 };
 int filter_candidates(int32_t top_k);
+int filter_group(int32_t top_k);
 size_t filter_smem_bytes(int64_t V, int esize, int32_t top_k);
 cudaError_t launch_filtered(const FilterArgs &a, int dtype, bool vec, cudaStream_t stream);
 
