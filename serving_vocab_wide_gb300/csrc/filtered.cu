@@ -44,7 +44,8 @@ namespace svw {
 
 namespace {
 
-constexpr int kFT = 512;  // threads of filter_rows (two CTAs per SM: one streams while the other sorts)
+constexpr int kFT = 256;  // threads of filter_rows (several CTAs per SM: some stream while others sort)
+constexpr int kPer = kFilterMaxK / kFT;  // kept entries per thread in the top-p prefix
 constexpr int kFW = kFT / 32;
 constexpr int kUnroll = 8;  // vectors per thread whose loads are in flight together
 
@@ -122,6 +123,7 @@ struct FSmem {
   float wf[kFW];
   uint32_t wu[kFW];
   int32_t ncand;
+  int32_t ngl;
   int32_t bad;
   float mx;
   uint32_t tau;
@@ -282,7 +284,7 @@ __device__ __forceinline__ int rank_desc(const uint32_t *key, const int32_t *idx
 }
 
 template <int DT, bool VEC>
-__global__ void __launch_bounds__(kFT, 2) filter_rows(FilterArgs a) {
+__global__ void __launch_bounds__(kFT, 4) filter_rows(FilterArgs a) {
   using KeyT = typename std::conditional<DT == 1, unsigned short, uint32_t>::type;
   extern __shared__ __align__(16) unsigned char dyn[];
   __shared__ FSmem sm;
@@ -423,22 +425,39 @@ __global__ void __launch_bounds__(kFT, 2) filter_rows(FilterArgs a) {
     auto gkey32 = [&](int64_t g) -> uint32_t {
       return (DT == 1) ? (static_cast<uint32_t>(gkey[g]) << 16) : static_cast<uint32_t>(gkey[g]);
     };
-    for (int64_t q = tid; q < NVec; q += kFT) {
-      if (gkey32(q >> lgv) >= tau) {
-        uint32_t k[8];
-        bool gn;
-        float gm;
-        group_keys<DT, VEC>(row, q, V, k, gn, gm);
+    auto take = [&](int64_t q) {  // the entries of vector q at or above tau
+      uint32_t k[8];
+      bool gn;
+      float gm;
+      group_keys<DT, VEC>(row, q, V, k, gn, gm);
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          if (k[e] >= tau) {
-            const int p = atomicAdd(&sm.ncand, 1);
-            if (p < kCand) {
-              ckey[p] = k[e];
-              cidx[p] = static_cast<int32_t>(q * 8 + e);
-            }
+      for (int e = 0; e < 8; ++e)
+        if (k[e] >= tau) {
+          const int p = atomicAdd(&sm.ncand, 1);
+          if (p < kCand) {
+            ckey[p] = k[e];
+            cidx[p] = static_cast<int32_t>(q * 8 + e);
           }
+        }
+    };
+    // the groups that reach tau (about top_k of them), listed in sidx first
+    if (tid == 0) sm.ngl = 0;
+    __syncthreads();
+    for (int64_t g = tid; g < NG; g += kFT)
+      if (gkey32(g) >= tau) {
+        const int p = atomicAdd(&sm.ngl, 1);
+        if (p < kFilterMaxK) sidx[p] = static_cast<int32_t>(g);
       }
+    __syncthreads();
+    const int ngl = sm.ngl;
+    if (ngl <= kFilterMaxK) {
+      for (int j = tid; j < ngl * gv; j += kFT) {
+        const int64_t q = static_cast<int64_t>(sidx[j >> lgv]) * gv + (j & (gv - 1));
+        if (q < NVec) take(q);
+      }
+    } else {
+      for (int64_t q = tid; q < NVec; q += kFT)
+        if (gkey32(q >> lgv) >= tau) take(q);
     }
     __syncthreads();
     if (sm.ncand > kCand) {
@@ -528,24 +547,35 @@ __global__ void __launch_bounds__(kFT, 2) filter_rows(FilterArgs a) {
       __syncthreads();
     }
     // ---- probabilities in that order; the top-p cut; renormalised ----
-    // thread t holds entries 2t and 2t + 1; the prefix is fixed-order
+    // thread t holds entries kPer t .. kPer t + kPer - 1; the prefix is fixed-order
     for (int t = tid; t < Kc; t += kFT) spv[t] = ex2(__fmul_rn(__fsub_rn(value_of_key<DT>(skey[t]), m), a.k));
     __syncthreads();
-    const int e0 = 2 * tid;
-    const float a0 = (e0 < Kc) ? spv[e0] : 0.f, a1 = (e0 + 1 < Kc) ? spv[e0 + 1] : 0.f;
+    const int e0 = kPer * tid;
+    float loc[kPer];
+    float run = 0.f;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      run = __fadd_rn(run, (e0 + e < Kc) ? spv[e0 + e] : 0.f);
+      loc[e] = run;
+    }
     float zk, excl;
-    const float cum1 = block_scan_f32(__fadd_rn(a0, a1), sm, &zk, &excl);
-    const float cum0 = __fadd_rn(excl, a0);
+    block_scan_f32(run, sm, &zk, &excl);
+    float cum[kPer];
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) cum[e] = __fadd_rn(excl, loc[e]);
     int np = Kc;
     if (a.top_p < 1.f) {
       const float thr = __fmul_rn(a.top_p, zk);
-      const uint32_t below = ((e0 < Kc && cum0 < thr) ? 1u : 0u) + ((e0 + 1 < Kc && cum1 < thr) ? 1u : 0u);
+      uint32_t below = 0;
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) below += (e0 + e < Kc && cum[e] < thr) ? 1u : 0u;
       uint32_t nb;
       block_scan_u32(below, sm, &nb);
       np = min(Kc, static_cast<int>(nb) + 1);
     }
-    if (e0 == np - 1) sm.zf = cum0;
-    if (e0 + 1 == np - 1) sm.zf = cum1;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e)
+      if (e0 + e == np - 1) sm.zf = cum[e];
     __syncthreads();
     const float zf = sm.zf;
     // ---- stored sorted by index (rank by index among the kept), p' = p / kept mass ----
@@ -692,7 +722,7 @@ static int pow2_at_least(int32_t k) {
 // entries per group: as large as the candidate space allows (every entry above
 // tau lies in one of fewer than top_k groups), between 8 and 128
 int filter_group(int32_t top_k) {
-  int gs = 8192 / pow2_at_least(top_k);
+  int gs = 2048 / pow2_at_least(top_k);
   if (gs < 8) gs = 8;
   if (gs > 128) gs = 128;
   return gs;
