@@ -46,6 +46,7 @@ namespace {
 
 constexpr int kFT = 256;  // threads of filter_rows (several CTAs per SM: some stream while others sort)
 constexpr int kPer = kFilterMaxK / kFT;  // kept entries per thread in the top-p prefix
+constexpr int kRankMax = 256;  // rank sorts (quadratic, no barriers) up to this many entries; bitonic above
 constexpr int kFW = kFT / 32;
 constexpr int kUnroll = 8;  // vectors per thread whose loads are in flight together
 
@@ -521,7 +522,7 @@ __global__ void __launch_bounds__(kFT, 4) filter_rows(FilterArgs a) {
     const int C = min(sm.ncand, kCand);
     const int Kc = min(static_cast<int>(K), C);
     // ---- the first K candidates in (logit descending, index ascending) order ----
-    if (C <= kFilterMaxK) {
+    if (C <= kRankMax) {
       // rank sort: every candidate counts those before it
       for (int t = tid; t < C; t += kFT) {
         const int rk = rank_desc(ckey, cidx, C, t);
@@ -578,13 +579,25 @@ __global__ void __launch_bounds__(kFT, 4) filter_rows(FilterArgs a) {
       if (e0 + e == np - 1) sm.zf = cum[e];
     __syncthreads();
     const float zf = sm.zf;
-    // ---- stored sorted by index (rank by index among the kept), p' = p / kept mass ----
-    for (int t = tid; t < np; t += kFT) {
-      const int32_t it = sidx[t];
-      int rk = 0;
-      for (int j = 0; j < np; ++j) rk += (sidx[j] < it) ? 1 : 0;
-      a.lidx[r * kFilterMaxK + rk] = it;
-      a.lp[r * kFilterMaxK + rk] = __fdiv_rn(spv[t], zf);
+    // ---- stored sorted by index, p' = p / kept mass ----
+    if (np <= kRankMax) {
+      for (int t = tid; t < np; t += kFT) {
+        const int32_t it = sidx[t];
+        int rk = 0;
+        for (int j = 0; j < np; ++j) rk += (sidx[j] < it) ? 1 : 0;
+        a.lidx[r * kFilterMaxK + rk] = it;
+        a.lp[r * kFilterMaxK + rk] = __fdiv_rn(spv[t], zf);
+      }
+    } else {
+      int Q = 1;
+      while (Q < np) Q <<= 1;
+      for (int t = np + tid; t < Q; t += kFT) sidx[t] = INT32_MAX;
+      __syncthreads();
+      bitonic<false>(skey, sidx, spv, Q);
+      for (int t = tid; t < np; t += kFT) {
+        a.lidx[r * kFilterMaxK + t] = sidx[t];
+        a.lp[r * kFilterMaxK + t] = __fdiv_rn(spv[t], zf);
+      }
     }
     if (tid == 0) a.cnt[r] = np;
     __syncthreads();
@@ -663,10 +676,27 @@ __global__ void __launch_bounds__(32 * kFinReqPerCta) filtered_finalize(FilterAr
   const int32_t *di = a.lidx + dr * kFilterMaxK;
   const float *dp = a.lp + dr * kFilterMaxK;
   const float w = philox_uniform(a.seed, static_cast<uint32_t>(i), static_cast<uint32_t>(js), 1u);
+  // the draft row's list in shared memory: every q' lookup of the draw is a
+  // binary search there rather than a chain of global loads
+  __shared__ int32_t sdi[kFinReqPerCta][kFilterMaxK];
+  __shared__ float sdp[kFinReqPerCta][kFilterMaxK];
+  const int wq = threadIdx.x >> 5;
+  for (int t = lane; t < nd; t += 32) {
+    sdi[wq][t] = __ldcg(di + t);
+    sdp[wq][t] = __ldcg(dp + t);
+  }
+  __syncwarp();
   auto weight = [&](int t, bool use_q) -> float {  // entry t of the target row's list
     const float p = __ldcg(tp + t);
     if (!use_q) return p;
-    const float q = list_prob(di, dp, nd, __ldcg(ti + t));
+    const int32_t v = __ldcg(ti + t);
+    int lo = 0, hi = nd;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (sdi[wq][mid] < v) lo = mid + 1;
+      else hi = mid;
+    }
+    const float q = (lo < nd && sdi[wq][lo] == v) ? sdp[wq][lo] : 0.f;
     return fmaxf(__fsub_rn(p, q), 0.f);
   };
   int32_t tok = -1;
