@@ -3,8 +3,11 @@
  * (serving_vocab_wide_gb300).  Hand-written CUDA for sm_103a (GB300).
  *
  * Two operations, both over full-vocabulary logits (and spec_verify_opd,
- * both on the same batch in one pass), plus the adaptive length head that
- * sets the next round's verified lengths (length_head, length_head_label):
+ * both on the same batch in one pass), two variants of the verification
+ * (spec_verify_early: stops reading each request at its first rejection;
+ * spec_verify_filtered: top-k / top-p filtered distributions), plus the
+ * adaptive length head that sets the next round's verified lengths
+ * (length_head, length_head_label):
  *
  *  spec_verify  batched speculative verification of a ragged batch.  Defined
  *               by "DFlash 阅读笔记：并行起草、目标特征与精确验证" §5.1 (greedy
