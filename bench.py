@@ -266,12 +266,17 @@ def run_native(args, ws, rank, local):
     stream = torch.cuda.current_stream()
     calls = CALLS
 
+    # the input set the step reads (the end-to-end loop alternates two)
+    cur = [dict(t=t, d=d, cu=cu, tok=tok, hid=hid)]
+
     def verify(T):
-        svw.spec_verify(t, d, cu, tok[T], T, 0, max_len=16, total_draft_rows=R, accept_len=acc[T],
-                        next_token=nxt[T], status=status, workspace=wsp, stream=stream)
+        x = cur[0]
+        svw.spec_verify(x["t"], x["d"], x["cu"], x["tok"][T], T, 0, max_len=16, total_draft_rows=R,
+                        accept_len=acc[T], next_token=nxt[T], status=status, workspace=wsp, stream=stream)
 
     def verify_opd():
-        svw.spec_verify_opd(t, d, cu, tok[1.0], 1.0, 0, opd_temperature=OPD["temperature"],
+        x = cur[0]
+        svw.spec_verify_opd(x["t"], x["d"], x["cu"], x["tok"][1.0], 1.0, 0, opd_temperature=OPD["temperature"],
                             clip_c=OPD["clip_c"], lambda_ce=OPD["lambda_ce"], max_len=16,
                             total_draft_rows=R, accept_len=acc[1.0], next_token=nxt[1.0], loss=loss,
                             dlogits=grad, status=status, workspace=fused_ws, stream=stream)
@@ -283,8 +288,9 @@ def run_native(args, ws, rank, local):
     def head():
         # this round's label (T = 1 accepted lengths against last round's a_hat), then the
         # forward pass that sets the next round's verified lengths
-        svw.length_head_label(acc[1.0], cu, a_hat, a_star=a_star, loss=len_loss, stream=stream)
-        svw.length_head(hid, w1, b1, w2, 0.2, HEAD["gamma"], a_hat=a_hat, k_hat=k_hat, workspace=head_ws,
+        x = cur[0]
+        svw.length_head_label(acc[1.0], x["cu"], a_hat, a_star=a_star, loss=len_loss, stream=stream)
+        svw.length_head(x["hid"], w1, b1, w2, 0.2, HEAD["gamma"], a_hat=a_hat, k_hat=k_hat, workspace=head_ws,
                         stream=stream)
 
     def step(ev=None, kev=None):
@@ -461,36 +467,63 @@ def run_native(args, ws, rank, local):
     h_loss = torch.empty(R, dtype=torch.float32).pin_memory()
     h_khat = torch.empty(N, dtype=torch.int32).pin_memory()
 
-    def e2e_step():
-        t.copy_(h_t, non_blocking=True)
-        d.copy_(h_d, non_blocking=True)
-        cu.copy_(h_cu, non_blocking=True)
-        for T in TEMPS:
-            tok[T].copy_(h_tok[T], non_blocking=True)
-        hid.copy_(h_hid, non_blocking=True)
+    # double-buffered inputs: step k+1's host-to-device copies run on a copy
+    # stream while step k's kernels run; every step's copies and result reads
+    # are inside the timed region
+    sets = [cur[0], dict(t=torch.empty_like(t), d=torch.empty_like(d), cu=torch.empty_like(cu),
+                         tok={T: torch.empty_like(tok[T]) for T in TEMPS}, hid=torch.empty_like(hid))]
+    copy_stream = torch.cuda.Stream()
+    ready = [torch.cuda.Event(), torch.cuda.Event()]
+    free = [torch.cuda.Event(), torch.cuda.Event()]
+
+    def h2d_into(s):
+        x = sets[s]
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(free[s])  # the set's previous step is done reading it
+            x["t"].copy_(h_t, non_blocking=True)
+            x["d"].copy_(h_d, non_blocking=True)
+            x["cu"].copy_(h_cu, non_blocking=True)
+            for T in TEMPS:
+                x["tok"][T].copy_(h_tok[T], non_blocking=True)
+            x["hid"].copy_(h_hid, non_blocking=True)
+            ready[s].record(copy_stream)
+
+    def run_on(s):
+        stream.wait_event(ready[s])
+        cur[0] = sets[s]
         step()
+        free[s].record(stream)
         for T in TEMPS:
             h_acc[T].copy_(acc[T], non_blocking=True)
             h_nxt[T].copy_(nxt[T], non_blocking=True)
         h_loss.copy_(loss, non_blocking=True)
         h_khat.copy_(k_hat, non_blocking=True)
 
-    e2e_step()
+    def e2e_run(n):
+        copy_stream.wait_stream(stream)
+        h2d_into(0)
+        for k in range(n):
+            if k + 1 < n:
+                h2d_into((k + 1) % 2)
+            run_on(k % 2)
+
+    e2e_run(2)
     torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     f0.record(stream)
-    for _ in range(Ke):
-        e2e_step()
+    e2e_run(Ke)
     f1.record(stream)
     torch.cuda.synchronize()
+    cur[0] = sets[0]
     e2e_ms, _ = reduce_over_ranks(ws, dev, f0.elapsed_time(f1), positions_per_step)
     h2d = ((h_t.numel() + h_d.numel()) * 2 + h_cu.numel() * 4 + sum(v.numel() * 4 for v in h_tok.values())
            + h_hid.numel() * 2)
     d2h = 2 * 3 * N * 4 + R * 4 + N * 4
     e2e = {"value": job_positions / (e2e_ms / Ke / 1000.0), "unit": UNIT,
-           "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": Ke}
+           "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": Ke,
+           "pipelining": "double-buffered inputs: step k+1's host-to-device copies overlap step k's kernels"}
 
     status_v = int(status.item())
     cpu = None
