@@ -96,7 +96,7 @@ def _src_hash(files):
 
 KERNEL_SOURCES = {
     "verify_stats": ["verify.cu", "svw_device.cuh", "svw_internal.h"],
-    "opd_fast_kernel": ["opd.cu", "svw_device.cuh", "svw_internal.h"],
+    "opd_fast_kernel": ["opd.cu", "opd_common.cuh", "svw_device.cuh", "svw_internal.h"],
 }
 CALL_KERNELS = {
     "spec_verify": "verify_stats + verify_finalize (accept tests and, at T > 0, the inverse-CDF draw)",

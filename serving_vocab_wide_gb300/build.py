@@ -14,7 +14,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libsvw.so")
 SOURCES = ["api.cu", "verify.cu", "early.cu", "filtered.cu", "opd.cu", "fused.cu", "lengthhead.cu", "noalloc.cu"]
-HEADERS = ["svw_device.cuh", "svw_internal.h", "svw_sample.cuh"]
+HEADERS = ["svw_device.cuh", "svw_internal.h", "svw_sample.cuh", "opd_common.cuh"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 

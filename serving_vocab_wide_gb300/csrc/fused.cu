@@ -73,7 +73,7 @@ __global__ void __launch_bounds__(kFThreads) fused_finalize(FusedArgs a) {
     float bm = -INFINITY, bs = 0.f;
     int32_t bidx = INT32_MAX, bflag = 0;
     if (len_ok && lane < a.bparts) {
-      const float4 q = __ldcg(a.bpart + static_cast<int64_t>(i) * 8 + lane);
+      const float4 q = __ldcg(a.bpart + static_cast<int64_t>(i) * kBonusParts + lane);
       bm = q.x;
       bs = q.y;
       bidx = __float_as_int(q.z);
@@ -81,15 +81,15 @@ __global__ void __launch_bounds__(kFThreads) fused_finalize(FusedArgs a) {
     }
     float bM = bm;
   #pragma unroll
-    for (int o = 4; o > 0; o >>= 1) bM = fmaxf(bM, __shfl_xor_sync(0xffffffffu, bM, o));
+    for (int o = kBonusParts / 2; o > 0; o >>= 1) bM = fmaxf(bM, __shfl_xor_sync(0xffffffffu, bM, o));
     float bS = (bm == -INFINITY) ? bs * 0.f : bs * ex2((bm - bM) * a.k);
   #pragma unroll
-    for (int o = 4; o > 0; o >>= 1) bS += __shfl_xor_sync(0xffffffffu, bS, o);
-    // the butterfly spans lanes 0..7: every lane takes lane 0's merge
+    for (int o = kBonusParts / 2; o > 0; o >>= 1) bS += __shfl_xor_sync(0xffffffffu, bS, o);
+    // the butterfly spans lanes 0 .. kBonusParts - 1: every lane takes lane 0's merge
     bM = __shfl_sync(0xffffffffu, bM, 0);
     bS = __shfl_sync(0xffffffffu, bS, 0);
-    const int32_t bx = static_cast<int32_t>(
-        __reduce_min_sync(0xffffffffu, static_cast<uint32_t>((lane < 8 && bm == bM) ? bidx : INT32_MAX)));
+    const int32_t bx = static_cast<int32_t>(__reduce_min_sync(
+        0xffffffffu, static_cast<uint32_t>((lane < kBonusParts && bm == bM) ? bidx : INT32_MAX)));
     const bool bonus_bad = len_ok && (__any_sync(0xffffffffu, bflag != 0) || !(bS > 0.f && bS <= FLT_MAX) ||
                                       bx == INT32_MAX);
     const float4 br = make_float4(fmaf(bM, a.k, lg2(bS)), __int_as_float(bx), 0.f, 0.f);

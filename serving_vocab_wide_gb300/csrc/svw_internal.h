@@ -113,7 +113,7 @@ struct FusedArgs {
   float k;  // log2(e) / T of the verification (T > 0)
   uint64_t seed;
   const float4 *rowc;  // [R] Ct, Cd, x*, target row (NaN: bad row)
-  const float4 *bpart;  // [N * 8] bonus-row partials of the fast kernel's CTAs
+  const float4 *bpart;  // [N * kBonusParts] bonus-row partials of the fast kernel's CTAs
   int32_t bparts;       // partials per bonus row (the fast kernel's cluster size)
   const int32_t *csr_bad;
   int32_t csr_grid;
@@ -162,6 +162,8 @@ int filter_group(int32_t top_k);
 size_t filter_smem_bytes(int64_t V, int esize, int32_t top_k);
 cudaError_t launch_filtered(const FilterArgs &a, int dtype, bool vec, cudaStream_t stream);
 
+constexpr int kBonusParts = 8;  // bonus-row partial slots per request (the largest OPD cluster)
+
 struct OpdArgs {
   const void *target;
   const void *draft;
@@ -184,8 +186,8 @@ struct OpdArgs {
   int32_t epoch;   // this call's tag (never 0)
   // fused verification (spec_verify_opd): after the R draft rows the fast
   // kernel also reduces the N bonus target rows, one partial per CTA of the
-  // cluster (bpart[i * 8 + rank] = {max, exp-sum, first argmax, flags}), and
-  // checks the CSR offsets (csr_bad[CTA])
+  // cluster (bpart[i * kBonusParts + rank] = {max, exp-sum, first argmax,
+  // flags}), and checks the CSR offsets (csr_bad[CTA])
   int32_t nbonus;
   float4 *bpart;
   int32_t *csr_bad;

@@ -133,6 +133,42 @@ def mix_batch():
     return synth.config(5)
 
 
+@pytest.mark.parametrize("V", [106504, 163840])
+def test_wide_clusters(V):
+    """Wide rows (up to the one-pass path's widest), several rows and bonus
+    rows per cluster."""
+    b = synth.config(5, N=20, V=V, seed=V)
+    _check(b, 1.0, 1.0, label=f"fused V={V} T=1")
+    _check(b, 0.0, 1.0, label=f"fused V={V} T=0")
+
+
+def test_workspace_contents_do_not_matter(mix_batch):
+    """Every workspace word the finalize reads is written by the same call:
+    a workspace filled with 0xff bytes (NaN row constants, set flags) before
+    each call gives the same results as a zeroed one, call after call."""
+    import torch
+    import serving_vocab_wide_gb300 as svw
+    b = mix_batch
+    N, R, V = b.N, b.total_rows, b.target.shape[1]
+    t, d = to_torch_logits(b.target), to_torch_logits(b.draft)
+    cu, tok = to_torch_i32(b.cu), to_torch_i32(b.tokens[1.0])
+    ws = torch.zeros(svw.verify_opd_workspace_size(N, R, V, svw.SVW_BF16), dtype=torch.uint8, device="cuda")
+    outs = []
+    for rep in range(4):
+        if rep:
+            ws.fill_(255)
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        acc, nxt, loss, _ = svw.spec_verify_opd(t, d, cu, tok, 1.0, b.seed, opd_temperature=1.0, max_len=32,
+                                                total_draft_rows=R, status=st, workspace=ws, **OPD)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        outs.append((acc.cpu().numpy(), nxt.cpu().numpy(), loss.cpu().numpy()))
+    for o in outs[1:]:
+        for x, y in zip(outs[0], o):
+            assert np.array_equal(x, y)
+    assert np.all(outs[0][0] >= 0)
+
+
 @pytest.mark.parametrize("T", [1.0, 0.0])
 def test_mix_full_size_sampled(T, mix_batch):
     reqs = np.sort(np.random.default_rng(4).choice(mix_batch.N, 12, replace=False))

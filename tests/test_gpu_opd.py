@@ -51,6 +51,18 @@ def test_paired_rows(V, dtype, exact_only):
     compare_opd(loss, g, ref, label=f"V={V} {dtype}")
 
 
+@pytest.mark.parametrize("V", [40000, 106504, 163840])
+def test_many_rows_per_cluster(V):
+    """Clusters that each walk several rows (and bonus rows) of the verify
+    layout, up to the widest row of the one-pass path (163840 bf16 entries:
+    8 CTAs of 2560 16-byte vectors)."""
+    b = synth.make_batch("opd", seed=V + 3, lengths=np.full(20, 8, np.int32), V=V, dtype="bf16",
+                         draft_kind="scaled", temperatures=(), has_bonus=True)
+    loss, g = _gpu(b.target, b.draft, cu=b.cu, has_bonus=True)
+    ref = oracle.opd_loss(b.target, b.draft, cu_draft=b.cu, has_bonus=True)
+    compare_opd(loss, g, ref, label=f"many rows V={V}")
+
+
 @PATHS
 @pytest.mark.parametrize("T,c,lam,gs", [(1.0, 0.01, 0.1, 1.0), (0.7, 1e30, 0.5, 0.0625),
                                         (1.3, 0.2, 0.0, 1.0), (1.0, float("inf"), 4.0, 0.2)])
