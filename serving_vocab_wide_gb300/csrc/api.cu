@@ -259,10 +259,13 @@ svw_status spec_verify_early(const void *target_logits, const void *draft_logits
 
 // OPD workspace: flags int32 [R] | row constants float4 [R], each 256-aligned
 static size_t opd_flags_bytes(int64_t R) { return static_cast<size_t>((R * 4 + 255) / 256 * 256); }
+static size_t opd_rowc_bytes(int64_t R) { return static_cast<size_t>((R * 16 + 255) / 256 * 256); }
 
+// flags [R] int32 | row constants [R] float4 | fix-up chunk partials [R][kOpdFixChunks] float2
 size_t svw_opd_workspace_size(int64_t total_draft_rows) {
   if (total_draft_rows <= 0 || total_draft_rows > (int64_t{1} << 40)) return 0;
-  return opd_flags_bytes(total_draft_rows) + static_cast<size_t>((total_draft_rows * 16 + 255) / 256 * 256);
+  return opd_flags_bytes(total_draft_rows) + opd_rowc_bytes(total_draft_rows) +
+         static_cast<size_t>(total_draft_rows) * svw::kOpdFixChunks * sizeof(float2);
 }
 
 svw_status opd_loss(const void *target_logits, const void *draft_logits, svw_dtype dtype,
@@ -307,6 +310,9 @@ svw_status opd_loss(const void *target_logits, const void *draft_logits, svw_dty
   a.flags = static_cast<int32_t *>(workspace);
   a.epoch = next_epoch();
   a.rowc = workspace ? reinterpret_cast<float4 *>(static_cast<char *>(workspace) + opd_flags_bytes(total_draft_rows))
+                     : nullptr;
+  a.fixp = workspace ? reinterpret_cast<float2 *>(static_cast<char *>(workspace) + opd_flags_bytes(total_draft_rows) +
+                                                  opd_rowc_bytes(total_draft_rows))
                      : nullptr;
   a.nbonus = 0;
   a.bpart = nullptr;
@@ -383,6 +389,7 @@ svw_status spec_verify_opd(const void *target_logits, const void *draft_logits, 
   o.status = status;
   o.flags = reinterpret_cast<int32_t *>(ws + lay.flags_off);
   o.rowc = reinterpret_cast<float4 *>(ws + lay.rowc_off);
+  o.fixp = reinterpret_cast<float2 *>(ws + lay.fixp_off);
   o.epoch = next_epoch();
   o.nbonus = N;
   o.bpart = reinterpret_cast<float4 *>(ws + lay.bpart_off);

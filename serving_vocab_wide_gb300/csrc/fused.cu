@@ -56,6 +56,8 @@ __global__ void __launch_bounds__(kFThreads) fused_finalize(FusedArgs a) {
       }
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");  // row constants and CSR flags are complete
+    // the fix-up grid that follows reads only the fast kernel's output: it may start now
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     int csr_bad = 0;
     for (int b = lane; b < a.csr_grid; b += 32) csr_bad |= __ldcg(a.csr_bad + b);

@@ -27,8 +27,11 @@
 // clip bound, or a non-finite KL (masked entries), flags the row: the flag
 // word is set to the call's tag (never cleared), so flags need no ordering
 // and a stale tag at worst sends a row to the exact fix-up once more.
-// Exact kernel.  Rows the fast kernel flagged (and every row of shapes that
-// are not 16-byte pitched) are redone from shared memory in three passes:
+// Fix-up.  Rows the fast kernel flagged are redone exactly from the row
+// constants it stored, by two flat grids over (row, vocabulary chunk) items:
+// clamped terms and S per chunk, then the row totals and the gradient.
+// Exact kernel.  Without a workspace (or for rows that are not 16-byte
+// pitched) every row is done from shared memory in three passes:
 // log-sum-exps; clamped terms, S and the argmax; gradient -- two exchanges.
 // In log2 units: A = log2 q = z k - Cd, Bp = log2 p = y k - Ct, d2 = A - Bp,
 // t/ln2 = q d2, q(d + 1) = t + q; per-entry arithmetic runs on f32x2 pairs.
@@ -840,234 +843,240 @@ __global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) 
   cluster.sync();  // peers may still read this CTA's partials
 }
 
-// Fix-up kernel: redoes exactly the rows the fast kernel flagged, from the
-// row constants it stored (log-sum-exps, x*, target row): one pass for the
-// clamped terms and S, one cluster exchange, one pass for the gradient.
-// Flagged rows are dealt to clusters in order of appearance (the k-th flagged
-// row of a batch of kFixBatch rows goes to cluster k mod nclusters), so a
-// cluster gets at most one row more than any other.
+// Fix-up of the rows the fast kernel flagged (a term at the clip bound, or
+// masked draft entries), exactly, from the row constants it stored (Ct, Cd,
+// x*, target row).  Two flat grids over (flagged row, vocabulary chunk)
+// items, kOpdFixChunks chunks per row, so every SM streams a share of the
+// flagged rows at once whatever their number:
+//   opd_fix_sums: per chunk, the clamped sum of t/ln2 and S = sum q a
+//                 (fixed-order reduction) into the workspace;
+//   opd_fix_grad: per chunk, the row totals (a fixed butterfly over the
+//                 chunk partials, identical in every warp), the loss (chunk 0)
+//                 and the chunk's gradient; the chunk's logits come back from
+//                 L2 (the flagged rows of a call are a few tens of MB).
+// Both walk the flags in batches of kFixBatch rows; a batch's flagged rows
+// are listed in row order by every CTA (a block scan), so the item order is
+// the same everywhere.  No waits on other CTAs: nothing can hang.
 constexpr int kFixBatch = 4096;  // flags scanned per batch
+constexpr int kFixNT = 256;
+constexpr int kFixU = 4;  // 16-byte vectors of each row in flight per thread
 
-struct FixSmem {
-  unsigned long long mbar;
-  unsigned long long xbar[2];          // row exchange, as in the fast kernel
-  float4 inbox[2][kMaxCluster];        // peers' (RKL2, S, abort)
-  float2 red[16];
-  float4 row;
-  int32_t wcnt[16];
-  int32_t total;
-  uint32_t nread;
-  int64_t tr;
-  int32_t abort;
-  uint32_t abort_parity;
+struct FixGeo {
+  int32_t CH;   // entries per chunk (a multiple of 8)
+  int32_t nch;  // chunks per row (<= kOpdFixChunks)
 };
 
-template <int DT, int VPT, int NT>
-__global__ void __launch_bounds__(NT, 2) opd_fix_kernel(OpdArgs a, OpdGeo geo) {
-  using E = Elem<DT>;
-  constexpr int kWarps = NT / 32;
-  constexpr int kPer = kFixBatch / NT;  // flags per thread
-  constexpr int EPV = E::kPerVec;
-  extern __shared__ __align__(128) unsigned char dyn[];
-  __shared__ FixSmem sm;
-  cg::cluster_group cluster = cg::this_cluster();
-  const int CL = static_cast<int>(cluster.num_blocks());
-  const int rank = static_cast<int>(cluster.block_rank());
+struct FixList {
+  int32_t list[kFixBatch];  // flagged rows of the batch (offsets from its base), in order
+  int32_t wcnt[kFixNT / 32];
+  float2 red[kFixNT / 32];
+};
+
+// The flagged rows of batch [base, base + kFixBatch) into fl.list, in row
+// order; returns their number (in every thread).  Warp w reads rows
+// [w 512, (w + 1) 512) of the batch 32 at a time (coalesced) and keeps one
+// ballot per 32.  A flag is this call's tag; a stale tag on a row the fast
+// kernel found bad (NaN row constants) is not.
+__device__ __forceinline__ int fix_scan(const OpdArgs &a, int64_t base, FixList &fl) {
+  constexpr int kWarps = kFixNT / 32;
+  constexpr int kPerWarp = kFixBatch / kWarps;
+  constexpr int kRounds = kPerWarp / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t nclusters = gridDim.x / CL;
-  const int64_t cid = blockIdx.x / CL;
-  const int64_t V = a.V;
-  const int64_t lo = static_cast<int64_t>(rank) * geo.SL;
-  const int n = static_cast<int>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(geo.SL), V - lo)));
-  const int nvec = n / EPV;
-  const int nj = (tid < nvec) ? min(VPT, (nvec - tid + NT - 1) / NT) : 0;
-  const float k = a.k;
-  unsigned char *tbuf = dyn;
-  unsigned char *dbuf = dyn + geo.slice_bytes;
-  int32_t *list = reinterpret_cast<int32_t *>(dyn + 2 * static_cast<size_t>(geo.slice_bytes));
-  const uint32_t tb = smem_u32(tbuf), db = smem_u32(dbuf);
-  const float c2 = a.clip_c * kLog2e;
-
-  if (tid == 0) {
-    mbar_init(&sm.mbar, 1);
-    mbar_init(&sm.xbar[0], 1);
-    mbar_init(&sm.xbar[1], 1);
-    sm.abort = 0;
-    sm.nread = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  const int64_t wb = base + static_cast<int64_t>(warp) * kPerWarp;
+  uint32_t ball[kRounds];
+  int cnt = 0;
+#pragma unroll
+  for (int i = 0; i < kRounds; ++i) {
+    const int64_t r = wb + i * 32 + lane;
+    bool f = r < a.R && __ldcg(a.flags + r) == a.epoch;
+    if (f) {
+      const float ct = __ldcg(&a.rowc[r].x);
+      f = (ct == ct);
+    }
+    ball[i] = __ballot_sync(0xffffffffu, f);
+    cnt += __popc(ball[i]);
   }
-  cluster.sync();  // every inbox barrier exists before any peer sends
-  auto issue = [&](int64_t r) {
-    const float4 rc = __ldcg(a.rowc + r);
-    const int32_t t32 = __float_as_int(rc.w);
-    const int64_t t = (t32 >= 0) ? t32 : target_row_of(a, r);
-    sm.tr = t;
-    const uint32_t bytes = static_cast<uint32_t>(n) * E::kSize;
-    if (sm.abort) return;
-    if (t >= 0 && bytes > 0) {
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive_expect_tx(&sm.mbar, 2 * bytes);
-      bulk_g2s(tbuf, static_cast<const char *>(a.target) + (t * V + lo) * E::kSize, bytes, &sm.mbar);
-      bulk_g2s(dbuf, static_cast<const char *>(a.draft) + (r * V + lo) * E::kSize, bytes, &sm.mbar);
-    } else {
-      mbar_arrive(&sm.mbar);
-    }
-  };
+  if (lane == 0) fl.wcnt[warp] = cnt;
+  __syncthreads();
+  int before = 0, total = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const int c = fl.wcnt[w];
+    before += (w < warp) ? c : 0;
+    total += c;
+  }
+  const uint32_t below = (1u << lane) - 1u;
+  int g = before;
+#pragma unroll
+  for (int i = 0; i < kRounds; ++i) {
+    if (ball[i] & (1u << lane)) fl.list[g + __popc(ball[i] & below)] = warp * kPerWarp + i * 32 + lane;
+    g += __popc(ball[i]);
+  }
+  __syncthreads();  // the list is complete; every thread has read fl.wcnt
+  return total;
+}
 
-  int64_t it = 0;  // rows processed (mbarrier phase)
+// target row of flagged row r from its row constants (the fast kernel stores
+// it when it fits an int32, else -2)
+__device__ __forceinline__ int64_t fix_target_row(const OpdArgs &a, int64_t r, const float4 &rc) {
+  const int32_t t32 = __float_as_int(rc.w);
+  return (t32 >= 0) ? static_cast<int64_t>(t32) : target_row_of(a, r);
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kFixNT, 4) opd_fix_sums(OpdArgs a, FixGeo fg) {
+  using E = Elem<DT>;
+  constexpr int EPV = E::kPerVec;
+  constexpr int kWarps = kFixNT / 32;
+  __shared__ FixList fl;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t V = a.V;
+  const float k = a.k, c2 = a.clip_c * kLog2e;
+  // The gradient grid may be scheduled now: it scans the flags, then waits
+  // for this grid.  This grid itself may start before the kernel launched
+  // ahead of it in the stream ends (the fused finalize kernel, which lets its
+  // dependents go only once the fast kernel's flags and row constants are
+  // complete): it reads only those, and waits for that kernel at its end.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   for (int64_t base = 0; base < a.R; base += kFixBatch) {
-    // ---- this cluster's flagged rows of the batch, in order ----
-    int32_t f[kPer];
-    int cnt = 0;
-#pragma unroll
-    for (int e = 0; e < kPer; ++e) {
-      const int64_t r = base + tid * kPer + e;
-      f[e] = (r < a.R && __ldcg(a.flags + r) == a.epoch) ? 1 : 0;
-      if (f[e] && __ldcg(&a.rowc[r].x) != __ldcg(&a.rowc[r].x)) f[e] = 0;  // stale tag on a bad row
-      cnt += (f[e] != 0);
-    }
-    int incl = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    if (lane == 31) sm.wcnt[warp] = incl;
-    __syncthreads();
-    int before = 0, total = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const int c = sm.wcnt[w];
-      before += (w < warp) ? c : 0;
-      total += c;
-    }
-    int g = before + incl - cnt;  // ordinal of this thread's first flagged row
-#pragma unroll
-    for (int e = 0; e < kPer; ++e)
-      if (f[e] != 0) {
-        if (g % nclusters == cid) list[g / nclusters] = static_cast<int32_t>(tid * kPer + e);
-        ++g;
-      }
-    const int mine = (cid < total) ? static_cast<int>((total - cid + nclusters - 1) / nclusters) : 0;
-    __syncthreads();  // list complete; also: every thread has read sm.wcnt
-    if (tid == 0 && mine > 0) issue(base + list[0]);
-
-    for (int i = 0; i < mine; ++i, ++it) {
-      const int64_t r = base + list[i];
+    const int m = fix_scan(a, base, fl);
+    const int64_t items = static_cast<int64_t>(m) * fg.nch;
+    for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
+      const int kq = static_cast<int>(item / fg.nch), c = static_cast<int>(item % fg.nch);
+      const int64_t r = base + fl.list[kq];
       const float4 rc = __ldcg(a.rowc + r);
-      if (!sm.abort && !mbar_wait_bounded(&sm.mbar, static_cast<uint32_t>(it & 1))) {
-        if (a.status) atomicOr(a.status, SVW_DEV_TIMEOUT);
-        sm.abort_parity = static_cast<uint32_t>(it & 1);
-        sm.abort = 1;
-      }
-      const bool valid = (sm.tr >= 0);
-      uint4 ty[VPT], tz[VPT];
-#pragma unroll
-      for (int j = 0; j < VPT; ++j)
-        if (j < nj) {
-          ty[j] = lds128(tb + (tid + j * NT) * 16);
-          tz[j] = lds128(db + (tid + j * NT) * 16);
-        }
-      const bool work = valid && !sm.abort;
-      if (last_warp_done<kWarps>(&sm.nread, it) && i + 1 < mine) issue(base + list[i + 1]);
-
-      const float Ct = rc.x, Cd = rc.y;
-      const int32_t xs = __float_as_int(rc.z);
+      const int64_t t = fix_target_row(a, r, rc);
+      const int64_t lo = static_cast<int64_t>(c) * fg.CH;
+      const int nv = static_cast<int>(min(static_cast<int64_t>(fg.CH), V - lo)) / EPV;
       const float2 kk = make_float2(k, k), nkk = make_float2(-k, -k);
-      const float2 nCd = make_float2(-Cd, -Cd), Ct2 = make_float2(Ct, Ct), l2 = make_float2(kLn2, kLn2);
-      // ---- clamped terms and S ----
-      float rkl = 0.f, S = 0.f;
-      if (work) {
-        float2 r2 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
+      const float2 nCd = make_float2(-rc.y, -rc.y), Ct2 = make_float2(rc.x, rc.x), l2 = make_float2(kLn2, kLn2);
+      float2 r2 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
+      if (t >= 0) {
+        const char *trow = static_cast<const char *>(a.target) + (t * V + lo) * E::kSize;
+        const char *drow = static_cast<const char *>(a.draft) + (r * V + lo) * E::kSize;
+        for (int v0 = tid; v0 < nv; v0 += kFixNT * kFixU) {
+          uint4 ty[kFixU], tz[kFixU];
 #pragma unroll
-        for (int j = 0; j < VPT; ++j)
-          if (j < nj) {
-            const Pairs<DT> y(ty[j]), z(tz[j]);
-#pragma unroll
-            for (int h = 0; h < Pairs<DT>::kN; ++h) {
-              const float2 A = __ffma2_rn(z.p[h], kk, nCd);
-              const float2 q = make_float2(ex2(A.x), ex2(A.y));
-              const float2 t = __fmul2_rn(q, __fadd2_rn(A, __ffma2_rn(y.p[h], nkk, Ct2)));
-              if (fabsf(t.x) < c2 && fabsf(t.y) < c2) {
-                r2 = __fadd2_rn(r2, t);
-                s2 = __fadd2_rn(__ffma2_rn(t, l2, s2), q);
-              } else {
-                term_slow(t.x, q.x, c2, r2.x, s2.x);
-                term_slow(t.y, q.y, c2, r2.y, s2.y);
-              }
+          for (int u = 0; u < kFixU; ++u) {
+            const int v = v0 + u * kFixNT;
+            if (v < nv) {
+              ty[u] = ld_vec(trow + static_cast<int64_t>(v) * 16);
+              tz[u] = ld_vec(drow + static_cast<int64_t>(v) * 16);
             }
           }
-        rkl = r2.x + r2.y;
-        S = s2.x + s2.y;
-      }
-      rkl = warp_sum(rkl);
-      S = warp_sum(S);
-      if (lane == 0) sm.red[warp] = make_float2(rkl, S);
-      if (warp == 0) {
-        const int slot = static_cast<int>(it & 1);
-        if (lane == 0) mbar_arrive_expect_tx(&sm.xbar[slot], static_cast<uint32_t>(CL) * sizeof(float4));
-        named_sync(2, NT);
-        float2 v = (lane < kWarps) ? sm.red[lane] : make_float2(0.f, 0.f);
 #pragma unroll
-        for (int o = kWarps / 2; o > 0; o >>= 1) {
-          v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
-          v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
-        }
-        if (lane < CL)
-          st_async16(mapa_shared(smem_u32(&sm.inbox[slot][rank]), lane),
-                     make_uint4(__float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(sm.abort ? 1.f : 0.f), 0u),
-                     mapa_shared(smem_u32(&sm.xbar[slot]), lane));
-        float4 pq = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (mbar_wait_bounded(&sm.xbar[slot], static_cast<uint32_t>((it >> 1) & 1))) {
-          if (lane < CL) pq = sm.inbox[slot][lane];
-        } else {
-          if (lane == 0 && a.status) atomicOr(a.status, SVW_DEV_TIMEOUT);
-          pq.z = 1.f;
-        }
+          for (int u = 0; u < kFixU; ++u)
+            if (v0 + u * kFixNT < nv) {
+              const Pairs<DT> y(ty[u]), z(tz[u]);
 #pragma unroll
-        for (int o = kMaxCluster / 2; o > 0; o >>= 1) {
-          pq.x += __shfl_xor_sync(0xffffffffu, pq.x, o);
-          pq.y += __shfl_xor_sync(0xffffffffu, pq.y, o);
-          pq.z += __shfl_xor_sync(0xffffffffu, pq.z, o);
+              for (int h = 0; h < Pairs<DT>::kN; ++h) {
+                const float2 A = __ffma2_rn(z.p[h], kk, nCd);  // log2 q
+                const float2 q = make_float2(ex2(A.x), ex2(A.y));
+                const float2 tt = __fmul2_rn(q, __fadd2_rn(A, __ffma2_rn(y.p[h], nkk, Ct2)));  // t / ln2
+                if (fabsf(tt.x) < c2 && fabsf(tt.y) < c2) {
+                  r2 = __fadd2_rn(r2, tt);
+                  s2 = __fadd2_rn(__ffma2_rn(tt, l2, s2), q);
+                } else {
+                  term_slow(tt.x, q.x, c2, r2.x, s2.x);
+                  term_slow(tt.y, q.y, c2, r2.y, s2.y);
+                }
+              }
+            }
         }
-        if (lane == 0) sm.row = pq;
-      } else {
-        named_arrive(2, NT);
       }
+      const float rk = warp_sum(r2.x + r2.y), S = warp_sum(s2.x + s2.y);
+      if (lane == 0) fl.red[warp] = make_float2(rk, S);
       __syncthreads();
-      const float4 rw = sm.row;
-      const bool any_abort = rw.z != 0.f;
-      if (!valid || any_abort) continue;
-      const float RKL2 = rw.x, SS = rw.y;
-      const float gsT = a.grad_scale * a.invT;
-      if (rank == 0 && tid == 0) {
+      if (tid == 0) {
+        float2 p = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) p = make_float2(p.x + fl.red[w].x, p.y + fl.red[w].y);
+        a.fixp[r * kOpdFixChunks + c] = p;
+      }
+      __syncthreads();  // fl.red is rewritten by the next item
+    }
+  }
+  // complete only after the kernel ahead of it, so that the stream's order holds
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kFixNT, 4) opd_fix_grad(OpdArgs a, FixGeo fg) {
+  using E = Elem<DT>;
+  constexpr int EPV = E::kPerVec;
+  __shared__ FixList fl;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int64_t V = a.V;
+  const float k = a.k, c2 = a.clip_c * kLog2e;
+  const float gsT = a.grad_scale * a.invT;
+  bool waited = false;
+  for (int64_t base = 0; base < a.R; base += kFixBatch) {
+    const int m = fix_scan(a, base, fl);  // the flags predate the sums grid
+    if (!waited) {
+      asm volatile("griddepcontrol.wait;" ::: "memory");  // the chunk partials are complete
+      waited = true;
+    }
+    const int64_t items = static_cast<int64_t>(m) * fg.nch;
+    for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
+      const int kq = static_cast<int>(item / fg.nch), c = static_cast<int>(item % fg.nch);
+      const int64_t r = base + fl.list[kq];
+      const float4 rc = __ldcg(a.rowc + r);
+      const int64_t t = fix_target_row(a, r, rc);
+      if (t < 0) continue;
+      const float Ct = rc.x, Cd = rc.y;
+      const int32_t xs = __float_as_int(rc.z);
+      // row totals: a fixed butterfly over the chunk partials, the same in every warp
+      float2 p = (lane < fg.nch) ? __ldcg(a.fixp + r * kOpdFixChunks + lane) : make_float2(0.f, 0.f);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        p.x += __shfl_xor_sync(0xffffffffu, p.x, o);
+        p.y += __shfl_xor_sync(0xffffffffu, p.y, o);
+      }
+      const float RKL2 = p.x, SS = p.y;
+      if (c == 0 && tid == 0) {
         const float zx = E::load(a.draft, r * V + xs);
         a.loss[r] = kLn2 * (RKL2 - a.lambda_ce * fmaf(zx, k, -Cd));
       }
-      // ---- gradient: gsT (qa + q (lambda - S)) - gsT lambda [v = x*] ----
-      if (a.dlogits != nullptr) {
-        const float gL0 = gsT * (a.lambda_ce - SS);
-        const float gL1 = gsT * (a.lambda_ce - SS + 1.f);
-        const float2 gl = make_float2(gsT * kLn2, gsT * kLn2), g1 = make_float2(gL1, gL1);
-        float *out = a.dlogits + r * V + lo;
+      if (a.dlogits == nullptr) continue;
+      // gradient: gsT (q a + q (lambda - S)) - gsT lambda [v = x*]
+      const int64_t lo = static_cast<int64_t>(c) * fg.CH;
+      const int nv = static_cast<int>(min(static_cast<int64_t>(fg.CH), V - lo)) / EPV;
+      const char *trow = static_cast<const char *>(a.target) + (t * V + lo) * E::kSize;
+      const char *drow = static_cast<const char *>(a.draft) + (r * V + lo) * E::kSize;
+      float *out = a.dlogits + r * V + lo;
+      const float gL0 = gsT * (a.lambda_ce - SS);
+      const float gL1 = gsT * (a.lambda_ce - SS + 1.f);
+      const float2 kk = make_float2(k, k), nkk = make_float2(-k, -k);
+      const float2 nCd = make_float2(-Cd, -Cd), Ct2 = make_float2(Ct, Ct);
+      const float2 gl = make_float2(gsT * kLn2, gsT * kLn2), g1 = make_float2(gL1, gL1);
+      for (int v0 = tid; v0 < nv; v0 += kFixNT * kFixU) {
+        uint4 ty[kFixU], tz[kFixU];
 #pragma unroll
-        for (int j = 0; j < VPT; ++j)
-          if (j < nj) {
-            const int vi = tid + j * NT;
-            const Pairs<DT> y(ty[j]), z(tz[j]);
+        for (int u = 0; u < kFixU; ++u) {
+          const int v = v0 + u * kFixNT;
+          if (v < nv) {
+            ty[u] = ld_vec(trow + static_cast<int64_t>(v) * 16);
+            tz[u] = ld_vec(drow + static_cast<int64_t>(v) * 16);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kFixU; ++u) {
+          const int v = v0 + u * kFixNT;
+          if (v < nv) {
+            const Pairs<DT> y(ty[u]), z(tz[u]);
             float g[EPV];
 #pragma unroll
             for (int h = 0; h < Pairs<DT>::kN; ++h) {
               const float2 A = __ffma2_rn(z.p[h], kk, nCd);
               const float2 q = make_float2(ex2(A.x), ex2(A.y));
-              const float2 t = __fmul2_rn(q, __fadd2_rn(A, __ffma2_rn(y.p[h], nkk, Ct2)));
-              float2 gg = __ffma2_rn(t, gl, __fmul2_rn(q, g1));
-              if (!(fabsf(t.x) < c2)) gg.x = q.x * gL0;
-              if (!(fabsf(t.y) < c2)) gg.y = q.y * gL0;
+              const float2 tt = __fmul2_rn(q, __fadd2_rn(A, __ffma2_rn(y.p[h], nkk, Ct2)));
+              float2 gg = __ffma2_rn(tt, gl, __fmul2_rn(q, g1));
+              if (!(fabsf(tt.x) < c2)) gg.x = q.x * gL0;
+              if (!(fabsf(tt.y) < c2)) gg.y = q.y * gL0;
               g[2 * h] = gg.x;
               g[2 * h + 1] = gg.y;
             }
-            const int off = static_cast<int>(xs - (lo + vi * EPV));
+            const int off = static_cast<int>(xs - (lo + static_cast<int64_t>(v) * EPV));
             if (off >= 0 && off < EPV) {
 #pragma unroll
               for (int e = 0; e < EPV; ++e)
@@ -1075,14 +1084,61 @@ __global__ void __launch_bounds__(NT, 2) opd_fix_kernel(OpdArgs a, OpdGeo geo) {
             }
 #pragma unroll
             for (int h = 0; h < EPV / 4; ++h)
-              st_stream(out + vi * EPV + 4 * h, g[4 * h], g[4 * h + 1], g[4 * h + 2], g[4 * h + 3]);
+              st_stream(out + static_cast<int64_t>(v) * EPV + 4 * h, g[4 * h], g[4 * h + 1], g[4 * h + 2],
+                        g[4 * h + 3]);
           }
+        }
       }
     }
     __syncthreads();  // the list is rewritten by the next batch
   }
-  if (tid == 0 && sm.abort) mbar_wait_bounded(&sm.mbar, sm.abort_parity);
-  cluster.sync();
+  if (!waited) asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// chunk geometry of the fix-up grids
+FixGeo fix_geo(int64_t V) {
+  FixGeo g;
+  int64_t CH = (V + kOpdFixChunks - 1) / kOpdFixChunks;
+  CH = (CH + 7) / 8 * 8;
+  g.CH = static_cast<int32_t>(CH);
+  g.nch = static_cast<int32_t>((V + CH - 1) / CH);
+  return g;
+}
+
+template <int DT>
+cudaError_t launch_fix(const OpdArgs &a, cudaStream_t st) {
+  static int nsm_cache[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int nsm = (dev >= 0 && dev < 64) ? nsm_cache[dev] : 0;
+  if (nsm == 0) {
+    if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) nsm_cache[dev] = nsm;
+  }
+  const FixGeo fg = fix_geo(a.V);
+  const unsigned grid = static_cast<unsigned>(4 * nsm);
+  // both grids are programmatic launches: the sums grid overlaps the kernel
+  // ahead of it (see opd_fix_sums), the gradient grid the sums grid's tail
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kFixNT, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void *tm = timer_before("opd_fix_sums", st);
+  e = cudaLaunchKernelEx(&cfg, opd_fix_sums<DT>, a, fg);
+  timer_after(tm, st);
+  if (e != cudaSuccess) return e;
+  tm = timer_before("opd_fix_grad", st);
+  e = cudaLaunchKernelEx(&cfg, opd_fix_grad<DT>, a, fg);
+  timer_after(tm, st);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
 
 struct OpdPlan {
@@ -1113,13 +1169,13 @@ OpdPlan plan_opd(int64_t V, int esize) {
 constexpr int kTab = 1024;  // target-row table entries per cluster (beyond: binary search)
 
 // what follows the two slices in dynamic shared memory
-enum SmemTail { kNone, kTable, kList };
+enum SmemTail { kNone, kTable };
 
 // launch a persistent grid of clusters (as many as can be co-resident)
 template <typename Kern>
 cudaError_t launch_clusters(const char *name, Kern kern, int nt, const OpdArgs &a, const OpdPlan &p, SmemTail tail,
                             cudaStream_t st, int *grid_out = nullptr) {
-  const size_t tail_max = (tail == kTable) ? kTab * sizeof(int32_t) : (tail == kList) ? kFixBatch * sizeof(int32_t) : 0;
+  const size_t tail_max = (tail == kTable) ? kTab * sizeof(int32_t) : 0;
   const size_t smem_max = p.smem + tail_max;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_max));
   if (e != cudaSuccess) return e;
@@ -1171,7 +1227,6 @@ cudaError_t launch_clusters(const char *name, Kern kern, int nt, const OpdArgs &
     geo.ntab = static_cast<int32_t>(std::min<int64_t>((rows + nclusters - 1) / nclusters, kTab));
     tail_bytes = static_cast<size_t>(geo.ntab) * sizeof(int32_t);
   }
-  if (tail == kList) tail_bytes = static_cast<size_t>((kFixBatch + nclusters - 1) / nclusters) * sizeof(int32_t);
   cfg.dynamicSmemBytes = p.smem + tail_bytes;
   cfg.gridDim = dim3(static_cast<unsigned>(nclusters * p.CL), 1, 1);
   if (grid_out) *grid_out = static_cast<int>(nclusters * p.CL);
@@ -1189,7 +1244,7 @@ cudaError_t launch_fast(const OpdArgs &a, const OpdPlan &p, cudaStream_t st, boo
     const cudaError_t e = launch_clusters("opd_fast_kernel", opd_fast_kernel<DT, VPT, NT>, NT, a, p, kTable, st, grid);
     if (e != cudaSuccess || !fix) return e;
   }
-  return launch_clusters("opd_fix_kernel", opd_fix_kernel<DT, VPT, NT>, NT, a, p, kList, st);
+  return launch_fix<DT>(a, st);
 }
 
 // the fast-path variant for this row geometry; false if the row is too wide

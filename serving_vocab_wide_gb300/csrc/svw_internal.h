@@ -95,7 +95,7 @@ EarlyLayout early_layout(int32_t N, int64_t total_rows, int64_t V, int esize);
 cudaError_t launch_verify_early(const VerifyArgs &a, int dtype, bool vec, bool greedy, cudaStream_t stream);
 // workspace of spec_verify_opd (fused verification + OPD)
 struct FusedLayout {
-  size_t flags_off, rowc_off, bpart_off, csr_bad_off, total;
+  size_t flags_off, rowc_off, bpart_off, fixp_off, csr_bad_off, total;
 };
 FusedLayout fused_layout(int32_t N, int64_t total_rows, int64_t V);
 
@@ -162,6 +162,7 @@ int filter_group(int32_t top_k);
 size_t filter_smem_bytes(int64_t V, int esize, int32_t top_k);
 cudaError_t launch_filtered(const FilterArgs &a, int dtype, bool vec, cudaStream_t stream);
 
+constexpr int kOpdFixChunks = 32;  // vocabulary chunks per row of the OPD fix-up grids
 constexpr int kBonusParts = 8;  // bonus-row partial slots per request (the largest OPD cluster)
 
 struct OpdArgs {
@@ -183,6 +184,7 @@ struct OpdArgs {
   // workspace of the fast path (NULL: the exact kernel takes every row)
   int32_t *flags;  // [R] == epoch: rows the fix-up kernel must redo
   float4 *rowc;    // [R] row constants of the fast kernel: Ct, Cd, x*, target row (NaN: bad row)
+  float2 *fixp;    // [R][kOpdFixChunks] chunk partials of the fix-up (clamped sum / ln2, S)
   int32_t epoch;   // this call's tag (never 0)
   // fused verification (spec_verify_opd): after the R draft rows the fast
   // kernel also reduces the N bonus target rows, one partial per CTA of the
