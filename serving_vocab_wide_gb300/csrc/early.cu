@@ -28,6 +28,7 @@
 #include <climits>
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
+#include <mutex>
 
 #include "svw_device.cuh"
 #include "svw_internal.h"
@@ -348,10 +349,12 @@ cudaError_t launch_cluster_t(const VerifyArgs &a, const EarlyClusterPlan &p, cud
   };
   static Entry cache[32];
   static int ncache = 0;
+  static std::mutex mu;  // calls from several host threads share the cache
   int dev = 0;
   e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   int maxc = 0;
+  std::unique_lock<std::mutex> lk(mu);
   for (int q = 0; q < ncache; ++q)
     if (cache[q].dev == dev && cache[q].fn == reinterpret_cast<const void *>(kern) && cache[q].CL == p.CL &&
         cache[q].smem == p.smem)
@@ -363,6 +366,7 @@ cudaError_t launch_cluster_t(const VerifyArgs &a, const EarlyClusterPlan &p, cud
     if (maxc <= 0) return cudaErrorInvalidConfiguration;
     if (ncache < 32) cache[ncache++] = Entry{dev, reinterpret_cast<const void *>(kern), p.CL, p.smem, maxc};
   }
+  lk.unlock();
   int64_t nclusters = maxc;
   if (nclusters > a.N) nclusters = a.N;
   cfg.gridDim = dim3(static_cast<unsigned>(nclusters * p.CL), 1, 1);

@@ -39,11 +39,13 @@
 // records SVW_DEV_TIMEOUT, stops issuing copies and keeps joining the cluster
 // barriers so that no peer can hang.
 #include <algorithm>
+#include <atomic>
 #include <cfloat>
 #include <climits>
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <mutex>
 
 #include "opd_common.cuh"
 #include "svw_device.cuh"
@@ -1107,14 +1109,14 @@ FixGeo fix_geo(int64_t V) {
 
 template <int DT>
 cudaError_t launch_fix(const OpdArgs &a, cudaStream_t st) {
-  static int nsm_cache[64] = {0};
+  static std::atomic<int> nsm_cache[64];  // zero-initialised (static storage)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  int nsm = (dev >= 0 && dev < 64) ? nsm_cache[dev] : 0;
+  int nsm = (dev >= 0 && dev < 64) ? nsm_cache[dev].load(std::memory_order_relaxed) : 0;
   if (nsm == 0) {
     if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) nsm_cache[dev] = nsm;
+    if (dev >= 0 && dev < 64) nsm_cache[dev].store(nsm, std::memory_order_relaxed);
   }
   const FixGeo fg = fix_geo(a.V);
   const unsigned grid = static_cast<unsigned>(4 * nsm);
@@ -1199,10 +1201,12 @@ cudaError_t launch_clusters(const char *name, Kern kern, int nt, const OpdArgs &
   };
   static Entry cache[64];
   static int ncache = 0;
+  static std::mutex mu;  // calls from several host threads share the cache
   int dev = 0;
   e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   int maxc = 0;
+  std::unique_lock<std::mutex> lk(mu);
   for (int q = 0; q < ncache; ++q)
     if (cache[q].dev == dev && cache[q].fn == reinterpret_cast<const void *>(kern) && cache[q].CL == p.CL &&
         cache[q].smem == smem_max)
@@ -1214,6 +1218,7 @@ cudaError_t launch_clusters(const char *name, Kern kern, int nt, const OpdArgs &
     if (maxc <= 0) return cudaErrorInvalidConfiguration;
     if (ncache < 64) cache[ncache++] = Entry{dev, reinterpret_cast<const void *>(kern), p.CL, smem_max, maxc};
   }
+  lk.unlock();
   const int64_t rows = (tail == kTable) ? a.R + a.nbonus : a.R;  // rows the kernel walks
   int64_t nclusters = maxc;
   if (nclusters > rows) nclusters = rows;

@@ -34,6 +34,7 @@
 #include <cfloat>
 #include <climits>
 #include <cuda_runtime.h>
+#include <mutex>
 
 #include "svw_device.cuh"
 #include "svw_internal.h"
@@ -814,9 +815,11 @@ struct GridCache {
 int cached_grid(const void *fn, int threads, int smem, cudaError_t &e) {
   static GridCache cache[64];
   static int n = 0;
+  static std::mutex mu;  // calls from several host threads share the cache
   int dev = 0;
   e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lk(mu);
   for (int q = 0; q < n; ++q)
     if (cache[q].dev == dev && cache[q].fn == fn && cache[q].smem == smem) return cache[q].blocks;
   int nsm = 0, occ = 0;

@@ -88,6 +88,20 @@ def _row_max_term(y, z):
     return np.abs(np.exp(lq) * (lq - lp)).max(1)
 
 
+def test_fix_up_over_several_flag_batches():
+    """More rows than one batch of the fix-up's flag scan (4096 rows), with a
+    clip bound between the rows' largest terms: the flagged rows of every
+    batch are redone exactly and the others keep the one-pass result."""
+    b = synth.make_batch("opd", seed=37, lengths=np.full(1, 9000, np.int32), V=1024,
+                         draft_kind="scaled", temperatures=(), has_bonus=False)
+    mt = _row_max_term(b.target, b.draft)
+    c = float(np.median(mt))
+    assert (mt > c).sum() > 4096
+    loss, g = _gpu(b.target, b.draft, clip_c=c)
+    ref = oracle.opd_loss(b.target, b.draft, clip_c=c)
+    compare_opd(loss, g, ref, label=f"9000 rows c={c}")
+
+
 @PATHS
 def test_mixed_clipped_and_unclipped_rows(exact_only):
     """About half the rows have a term beyond the clip: the fast pass must hand

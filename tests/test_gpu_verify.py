@@ -137,6 +137,42 @@ def test_inconsistent_csr_is_rejected_on_device():
     assert int(status.item()) & svw.SVW_DEV_BAD_INPUT
 
 
+def test_concurrent_host_threads():
+    """Calls from several host threads at once, each on its own stream with
+    its own workspace, give the results of the same calls made one by one
+    (the library's launch caches are shared between threads)."""
+    import threading
+    import torch
+    import serving_vocab_wide_gb300 as svw
+    batches = [synth.config(5, N=6, lengths=np.array([3, 16, 1, 8, 5, 2], np.int32), V=32768, seed=300 + q)
+               for q in range(4)]
+    temps = [1.0, 0.0, 1.0, 0.0]
+
+    def call(b, T, stream):
+        with torch.cuda.stream(stream):
+            acc, nxt = svw.spec_verify(to_torch_logits(b.target), to_torch_logits(b.draft), to_torch_i32(b.cu),
+                                       to_torch_i32(b.tokens[T]), T, b.seed, max_len=32,
+                                       total_draft_rows=b.total_rows, stream=stream)
+        stream.synchronize()
+        return acc.cpu().numpy(), nxt.cpu().numpy()
+
+    ref = [call(b, T, torch.cuda.Stream()) for b, T in zip(batches, temps)]
+    out = [None] * len(batches)
+    streams = [torch.cuda.Stream() for _ in batches]
+
+    def work(q):
+        for _ in range(5):
+            out[q] = call(batches[q], temps[q], streams[q])
+
+    threads = [threading.Thread(target=work, args=(q,)) for q in range(len(batches))]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    for q in range(len(batches)):
+        assert np.array_equal(out[q][0], ref[q][0]) and np.array_equal(out[q][1], ref[q][1])
+
+
 def test_deterministic_rerun():
     b = synth.config(3, N=12, seed=5)
     a1, n1 = gpu_verify(b, 1.0)
