@@ -854,8 +854,9 @@ __global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) 
 //                 (fixed-order reduction) into the workspace;
 //   opd_fix_grad: per chunk, the row totals (a fixed butterfly over the
 //                 chunk partials, identical in every warp), the loss (chunk 0)
-//                 and the chunk's gradient; the chunk's logits come back from
-//                 L2 (the flagged rows of a call are a few tens of MB).
+//                 and the chunk's gradient (its logits read again; the
+//                 flagged rows of a call are a few tens of MB, so much of
+//                 the re-read can come from the 129 MB L2).
 // Both walk the flags in batches of kFixBatch rows; a batch's flagged rows
 // are listed in row order by every CTA (a block scan), so the item order is
 // the same everywhere.  No waits on other CTAs: nothing can hang.
