@@ -208,10 +208,11 @@ class ClockSampler:
 # native arm
 # ---------------------------------------------------------------------------
 def launches_per_step():
-    """Kernels one step launches: spec_verify = stats + finalize, twice;
-    spec_verify_opd = fast pass + finalize + fix-up; length head = label +
-    epilogue (the GEMM's kernels belong to cuBLASLt and are not counted)."""
-    return 2 + 2 + 3 + 2
+    """Kernels of this library one step launches: spec_verify = stats +
+    finalize, twice; spec_verify_opd = fast pass + finalize + the fix-up's sums
+    and gradient grids; length head = label + epilogue (the GEMM's kernels
+    belong to cuBLASLt and are not counted)."""
+    return 2 + 2 + 4 + 2
 
 
 def run_native(args, ws, rank, local):
