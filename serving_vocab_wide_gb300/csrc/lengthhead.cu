@@ -43,9 +43,18 @@ __global__ void __launch_bounds__(kHeadThreads) length_head_epilogue(const float
   for (int j = tid; j < Hp; j += kHeadThreads) {
     const float bj = __ldg(b1 + j);
     float s = 0.f;
-    for (int p = 0; p < k; ++p) {
-      const float g = __ldg(Y + (static_cast<int64_t>(i) * k + p) * Hp + j) + bj;
-      s += g / (1.f + expf(-g));  // SiLU
+    // eight positions' loads in flight at once; the sum stays sequential over p
+    for (int p0 = 0; p0 < k; p0 += 8) {
+      float y[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        y[u] = (p0 + u < k) ? __ldg(Y + (static_cast<int64_t>(i) * k + p0 + u) * Hp + j) : 0.f;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (p0 + u < k) {
+          const float g = y[u] + bj;
+          s += g / (1.f + expf(-g));  // SiLU
+        }
     }
     part = fmaf(__ldg(w2 + j), s / static_cast<float>(k), part);
   }
