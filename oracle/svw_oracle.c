@@ -28,7 +28,7 @@
  *        Example".
  *  [AP]  "AdaFlash：基于在策略蒸馏扩散草稿器的自适应投机解码" §2.3: the verify
  *        batch packs each request's own verified length (sum of k_i tokens,
- *        not N x k), which this build expresses with CSR offsets; §2.2 the
+ *        not N x k), expressed here by CSR offsets; §2.2 the
  *        adaptive length head (k_hat = clamp(floor(gamma a_hat k), 1, k)).
  *  [AR]  also "Method Part 2: The Adaptive Length Head": "Algorithm 3:
  *        Adaptive Length Head, Forward Pass" and "Online Update of the Length
