@@ -55,19 +55,49 @@ typedef enum svw_status {
   SVW_OK = 0,
   SVW_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, bad temperature ... */
   SVW_ERR_UNSUPPORTED = 2, /* dtype or size outside what the kernels handle         */
+  SVW_ERR_UNSUPPORTED_DTYPE = SVW_ERR_UNSUPPORTED, /* the same code, by its other name */
   SVW_ERR_MISALIGNED = 3,  /* a pointer violates its documented alignment            */
   SVW_ERR_WORKSPACE = 4,   /* workspace missing or smaller than its *_workspace_size  */
-  SVW_ERR_CUDA = 5         /* a CUDA runtime call or kernel launch failed            */
+  SVW_ERR_CUDA = 5,        /* a CUDA runtime call or kernel launch failed            */
+  SVW_ERR_BAD_INPUT = 6,   /* device-detected: see svw_device_status()               */
+  SVW_ERR_TIMEOUT = 7      /* device-detected: see svw_device_status()               */
 } svw_status;
 
 typedef enum svw_dtype { SVW_F32 = 0, SVW_BF16 = 1 } svw_dtype;
 
-/* bits OR-ed into the device status word */
+/*
+ * Bits OR-ed into the device status word.  The word is a bit set, not an
+ * svw_status: many CTAs of one call may each find a problem, and an atomic OR
+ * of bits is the only way they can report without ordering.  No entry point
+ * returns SVW_ERR_BAD_INPUT or SVW_ERR_TIMEOUT from the host (the host never
+ * waits for the device); svw_device_status() turns a word the caller has read
+ * back into those codes.
+ */
 #define SVW_DEV_BAD_INPUT 1 /* some request / row was invalid or non-finite   */
 #define SVW_DEV_TIMEOUT 2   /* a bounded wait inside a kernel gave up         */
 
+/*
+ * The svw_status of a device status word read back by the caller:
+ * SVW_ERR_TIMEOUT if SVW_DEV_TIMEOUT is set (results of that call are not
+ * valid), else SVW_ERR_BAD_INPUT if SVW_DEV_BAD_INPUT is set (the bad
+ * requests / rows carry -1 / NaN, the others are valid), else SVW_OK.
+ */
+svw_status svw_device_status(int32_t status_word);
+
 /* Largest draft length (positions per request) spec_verify accepts. */
 #define SVW_MAX_LEN 32
+
+/*
+ * svw_workspace_size -- one workspace size for every entry point on a batch
+ * shape: the largest of svw_verify_workspace_size, svw_verify_early_workspace_size,
+ * svw_verify_filtered_workspace_size (both dtypes), svw_opd_workspace_size and
+ * svw_verify_opd_workspace_size for (n_requests, total_draft_rows, V), so
+ * that a caller can size one buffer before it knows which call or dtype it
+ * will make.  max_len (1..SVW_MAX_LEN) is checked only.  Returns 0 for
+ * invalid arguments.  The per-call functions below give the exact (smaller)
+ * sizes.
+ */
+size_t svw_workspace_size(int32_t n_requests, int64_t total_draft_rows, int32_t V, int32_t max_len);
 
 /*
  * Bytes of device workspace spec_verify needs for this batch shape (any
@@ -324,6 +354,10 @@ svw_status length_head_label(const int32_t *accept_len, const int32_t *cu_draft,
  *  - Batches whose svw_verify_workspace_size(...) exceeds the scratch return
  *    SVW_ERR_UNSUPPORTED without launching (e.g. N = 256 requests, 4096 draft
  *    rows at V = 151936 bf16 fit).
+ *  - Argument checks run first and give spec_verify's codes; only a batch
+ *    that passes them and needs more than the scratch gets SVW_ERR_UNSUPPORTED.
+ *  - `stream` must belong to the current device (the scratch used is the
+ *    current device's); otherwise SVW_ERR_INVALID_ARG, nothing launched.
  *  - The first call on each device looks the scratch's device address up
  *    (cudaGetSymbolAddress with that device current); make that first call
  *    before capturing the stream into a graph.

@@ -44,6 +44,10 @@ def lib():
                                        ctypes.c_float, ctypes.c_uint64, ctypes.c_size_t)
             L.svw_verify_workspace_size.argtypes = [I32, I64, I32, ctypes.c_int]
             L.svw_verify_workspace_size.restype = SZ
+            L.svw_workspace_size.argtypes = [I32, I64, I32, I32]
+            L.svw_workspace_size.restype = SZ
+            L.svw_device_status.argtypes = [I32]
+            L.svw_device_status.restype = ctypes.c_int
             L.spec_verify.argtypes = [P, P, ctypes.c_int, I32, I32, P, I64, I32, P, F, U64,
                                       P, P, P, P, SZ, P]
             L.spec_verify.restype = ctypes.c_int
@@ -128,6 +132,16 @@ def time_next_launch(kernel: str | None, begin=None, end=None):
             ev.record()
     _check(lib().svw_time_next_launch(kernel.encode(), ctypes.c_void_p(begin.cuda_event),
                                       ctypes.c_void_p(end.cuda_event)))
+
+
+def workspace_size(n_requests: int, total_draft_rows: int, V: int, max_len: int = SVW_MAX_LEN) -> int:
+    """One workspace size that serves every entry point on this batch shape."""
+    return int(lib().svw_workspace_size(n_requests, total_draft_rows, V, max_len))
+
+
+def device_status(word: int) -> int:
+    """svw_status code of a device status word (SVW_ERR_TIMEOUT, SVW_ERR_BAD_INPUT or 0)."""
+    return int(lib().svw_device_status(int(word)))
 
 
 def verify_workspace_size(n_requests: int, total_draft_rows: int, V: int, dtype_code: int) -> int:
@@ -260,10 +274,12 @@ def spec_verify_noalloc(target, draft, cu_draft, draft_tokens, temperature: floa
     if next_token is None:
         next_token = torch.empty(N, dtype=torch.int32, device=dev)
     _need_cuda(accept_len, next_token, status)
-    rc = lib().spec_verify_noalloc(_ptr(target), _ptr(draft), _dtype_code(target), V, N,
-                                   _ptr(cu_draft), R, max_len, _ptr(draft_tokens),
-                                   float(temperature), int(seed) & (2**64 - 1), _ptr(accept_len),
-                                   _ptr(next_token), _ptr(status), _stream_ptr(stream))
+    # the library uses the current device's scratch: make the inputs' device current
+    with torch.cuda.device(dev):
+        rc = lib().spec_verify_noalloc(_ptr(target), _ptr(draft), _dtype_code(target), V, N,
+                                       _ptr(cu_draft), R, max_len, _ptr(draft_tokens),
+                                       float(temperature), int(seed) & (2**64 - 1), _ptr(accept_len),
+                                       _ptr(next_token), _ptr(status), _stream_ptr(stream))
     _check(rc)
     return accept_len, next_token
 

@@ -1,6 +1,7 @@
 // api.cu -- the exported C ABI (see include/svw.h): host-side validation,
 // workspace carving, and dispatch to the kernel launchers.  No allocation,
 // no host synchronisation, no device-memory reads from the host.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -67,8 +68,16 @@ const char *svw_status_string(svw_status s) {
     case SVW_ERR_MISALIGNED: return "SVW_ERR_MISALIGNED: pointer alignment";
     case SVW_ERR_WORKSPACE: return "SVW_ERR_WORKSPACE: workspace missing or too small";
     case SVW_ERR_CUDA: return "SVW_ERR_CUDA: CUDA runtime or launch failure";
+    case SVW_ERR_BAD_INPUT: return "SVW_ERR_BAD_INPUT: the device found an invalid or non-finite request / row";
+    case SVW_ERR_TIMEOUT: return "SVW_ERR_TIMEOUT: a bounded wait inside a kernel gave up";
   }
   return "unknown svw_status";
+}
+
+svw_status svw_device_status(int32_t status_word) {
+  if (status_word & SVW_DEV_TIMEOUT) return SVW_ERR_TIMEOUT;
+  if (status_word & SVW_DEV_BAD_INPUT) return SVW_ERR_BAD_INPUT;
+  return SVW_OK;
 }
 
 size_t svw_verify_workspace_size(int32_t n_requests, int64_t total_draft_rows, int32_t V,
@@ -80,30 +89,34 @@ size_t svw_verify_workspace_size(int32_t n_requests, int64_t total_draft_rows, i
 
 }  // extern "C"
 
-// spec_verify and spec_verify_early: same validation, same results
+// spec_verify and spec_verify_early: same validation, same results.  With
+// check_only, every check that does not involve the workspace runs and the
+// call returns SVW_OK without launching (spec_verify_noalloc's first step).
 static svw_status verify_entry(bool early, const void *target_logits, const void *draft_logits, svw_dtype dtype,
                                int32_t V, int32_t N, const int32_t *cu_draft, int64_t total_draft_rows,
                                int32_t max_len, const int32_t *draft_tokens, float temperature, uint64_t seed,
                                int32_t *accept_len, int32_t *next_token, int32_t *status,
                                unsigned long long *bytes_read, void *workspace, size_t workspace_bytes,
-                               void *stream) {
+                               void *stream, bool check_only = false) {
   if (dtype != SVW_F32 && dtype != SVW_BF16) return SVW_ERR_UNSUPPORTED;
   if (V <= 0 || N <= 0 || total_draft_rows < 0 || max_len < 1) return SVW_ERR_INVALID_ARG;
   if (max_len > SVW_MAX_LEN || V > kMaxV) return SVW_ERR_UNSUPPORTED;
-  if (!target_logits || !draft_logits || !cu_draft || !draft_tokens || !accept_len || !next_token ||
-      !workspace)
-    return workspace ? SVW_ERR_INVALID_ARG : SVW_ERR_WORKSPACE;
+  const bool have_ws = check_only || workspace;
+  if (!target_logits || !draft_logits || !cu_draft || !draft_tokens || !accept_len || !next_token || !have_ws)
+    return have_ws ? SVW_ERR_INVALID_ARG : SVW_ERR_WORKSPACE;
   if (!(temperature >= 0.f) || !std::isfinite(temperature)) return SVW_ERR_INVALID_ARG;
   const double kd = (temperature > 0.f) ? 1.4426950408889634 / static_cast<double>(temperature) : 0.0;
   if (temperature > 0.f && !(kd < 3.0e38)) return SVW_ERR_INVALID_ARG;
   const int es = esize_of(dtype);
   if (!aligned(target_logits, es) || !aligned(draft_logits, es) || !aligned(cu_draft, 4) ||
       !aligned(draft_tokens, 4) || !aligned(accept_len, 4) || !aligned(next_token, 4) ||
-      (status && !aligned(status, 4)) || (bytes_read && !aligned(bytes_read, 8)) || !aligned(workspace, 256))
+      (status && !aligned(status, 4)) || (bytes_read && !aligned(bytes_read, 8)) ||
+      (!check_only && !aligned(workspace, 256)))
     return SVW_ERR_MISALIGNED;
+  if (early && total_draft_rows + N >= (int64_t{1} << 31)) return SVW_ERR_UNSUPPORTED;  // int32 row records
+  if (check_only) return SVW_OK;
   const svw::VerifyLayout lay = svw::verify_layout(N, total_draft_rows, V, es);
   const svw::EarlyLayout elay = svw::early_layout(N, total_draft_rows, V, es);
-  if (early && total_draft_rows + N >= (int64_t{1} << 31)) return SVW_ERR_UNSUPPORTED;  // int32 row records
   if (workspace_bytes < (early ? elay.total : lay.total)) return SVW_ERR_WORKSPACE;
 
   const svw::ChunkPlan plan = svw::plan_chunks(V, es);
@@ -153,6 +166,17 @@ static svw_status verify_entry(bool early, const void *target_logits, const void
   }
   return e == cudaSuccess ? SVW_OK : SVW_ERR_CUDA;
 }
+
+namespace svw {
+svw_status verify_check_args(const void *target_logits, const void *draft_logits, svw_dtype dtype, int32_t V,
+                             int32_t N, const int32_t *cu_draft, int64_t total_draft_rows, int32_t max_len,
+                             const int32_t *draft_tokens, float temperature, int32_t *accept_len,
+                             int32_t *next_token, int32_t *status) {
+  return verify_entry(false, target_logits, draft_logits, dtype, V, N, cu_draft, total_draft_rows, max_len,
+                      draft_tokens, temperature, 0, accept_len, next_token, status, nullptr, nullptr, 0, nullptr,
+                      true);
+}
+}  // namespace svw
 
 extern "C" {
 
@@ -338,6 +362,20 @@ size_t svw_verify_opd_workspace_size(int32_t n_requests, int64_t total_draft_row
   if (n_requests <= 0 || total_draft_rows < 0 || V <= 0 || V > kMaxV) return 0;
   if (dtype != SVW_F32 && dtype != SVW_BF16) return 0;
   return svw::fused_layout(n_requests, total_draft_rows, V).total;
+}
+
+size_t svw_workspace_size(int32_t n_requests, int64_t total_draft_rows, int32_t V, int32_t max_len) {
+  if (max_len < 1 || max_len > SVW_MAX_LEN) return 0;
+  if (n_requests <= 0 || total_draft_rows < 0 || V <= 0 || V > kMaxV) return 0;
+  size_t need = 0;
+  for (svw_dtype dt : {SVW_F32, SVW_BF16}) {
+    need = std::max(need, svw_verify_workspace_size(n_requests, total_draft_rows, V, dt));
+    need = std::max(need, svw_verify_early_workspace_size(n_requests, total_draft_rows, V, dt));
+    need = std::max(need, svw_verify_filtered_workspace_size(n_requests, total_draft_rows, V, dt));
+    need = std::max(need, svw_verify_opd_workspace_size(n_requests, total_draft_rows, V, dt));
+  }
+  if (total_draft_rows > 0) need = std::max(need, svw_opd_workspace_size(total_draft_rows));
+  return need;
 }
 
 svw_status spec_verify_opd(const void *target_logits, const void *draft_logits, svw_dtype dtype, int32_t V,

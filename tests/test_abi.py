@@ -30,15 +30,55 @@ def test_header_symbols_exported(lib):
     assert {"spec_verify", "opd_loss", "svw_verify_workspace_size", "svw_opd_workspace_size",
             "svw_status_string", "svw_version", "spec_verify_noalloc", "spec_verify_early",
             "svw_verify_early_workspace_size", "spec_verify_filtered",
-            "svw_verify_filtered_workspace_size"} <= set(names)
+            "svw_verify_filtered_workspace_size", "svw_workspace_size",
+            "svw_device_status"} <= set(names)
     for n in names:
         assert hasattr(lib, n), f"{n} declared in svw.h but not exported"
 
 
 def test_version_and_status_strings(lib):
     assert lib.svw_version() == 100
-    for code in range(6):
+    for code in range(8):
         assert lib.svw_status_string(code).startswith(b"SVW_")
+    assert lib.svw_status_string(6).startswith(b"SVW_ERR_BAD_INPUT")
+    assert lib.svw_status_string(7).startswith(b"SVW_ERR_TIMEOUT")
+
+
+def test_status_codes_match_the_contract():
+    """The status enum's values: the sizing call's and the host codes' names
+    and numbers, and the two device-detected codes."""
+    src = open(os.path.join(ROOT, "include", "svw.h"), encoding="utf-8").read()
+    want = {"SVW_OK": "0", "SVW_ERR_INVALID_ARG": "1", "SVW_ERR_UNSUPPORTED": "2",
+            "SVW_ERR_UNSUPPORTED_DTYPE": "SVW_ERR_UNSUPPORTED", "SVW_ERR_MISALIGNED": "3",
+            "SVW_ERR_WORKSPACE": "4", "SVW_ERR_CUDA": "5", "SVW_ERR_BAD_INPUT": "6",
+            "SVW_ERR_TIMEOUT": "7"}
+    for name, val in want.items():
+        assert re.search(rf"\b{name}\s*=\s*{val}\b", src), name
+
+
+def test_device_status_word(lib):
+    import serving_vocab_wide_gb300 as svw
+    assert lib.svw_device_status(0) == 0
+    assert lib.svw_device_status(svw.SVW_DEV_BAD_INPUT) == 6
+    assert lib.svw_device_status(svw.SVW_DEV_TIMEOUT) == 7
+    assert lib.svw_device_status(svw.SVW_DEV_TIMEOUT | svw.SVW_DEV_BAD_INPUT) == 7   # a timeout voids the call
+    assert svw.device_status(svw.SVW_DEV_BAD_INPUT) == 6
+
+
+def test_one_workspace_size_for_every_entry_point(lib):
+    import serving_vocab_wide_gb300 as svw
+    for N, R, V in ((256, 1964, 151936), (4, 64, 1024), (32, 512, 151936), (2, 4, 64)):
+        need = svw.workspace_size(N, R, V, 16)
+        parts = [svw.opd_workspace_size(R)]
+        for dt in (svw.SVW_F32, svw.SVW_BF16):
+            parts += [svw.verify_workspace_size(N, R, V, dt), svw.verify_early_workspace_size(N, R, V, dt),
+                      svw.verify_filtered_workspace_size(N, R, V, dt),
+                      svw.verify_opd_workspace_size(N, R, V, dt)]
+        assert need == max(parts) > 0
+    assert svw.workspace_size(4, 64, 1024, 0) == 0
+    assert svw.workspace_size(4, 64, 1024, 33) == 0
+    assert svw.workspace_size(0, 64, 1024, 16) == 0
+    assert svw.workspace_size(4, 64, 0, 16) == 0
 
 
 def test_workspace_size(lib):
@@ -227,3 +267,23 @@ def test_length_head_argument_validation(lib):
     assert call(h=ctypes.c_void_p(p.value + 8)) == 3
     assert lib.svw_length_head_workspace_size(256, 16, 256) > (4 << 20)
     assert lib.svw_length_head_workspace_size(0, 16, 256) == 0
+
+
+def test_noalloc_argument_checks_come_before_the_size_check(lib):
+    """spec_verify_noalloc gives spec_verify's codes for bad arguments, even on a
+    batch too large for its scratch (which alone gives SVW_ERR_UNSUPPORTED)."""
+    keep, p = _fake(4096)
+    big = dict(t=p, d=p, dt=1, V=151936, N=4096, cu=p, R=65536, ml=16, tok=p, T=1.0, seed=0,
+               acc=p, nxt=p, st=None)
+
+    def call(**kw):
+        a = dict(big, **kw)
+        return lib.spec_verify_noalloc(a["t"], a["d"], a["dt"], a["V"], a["N"], a["cu"], a["R"], a["ml"],
+                                       a["tok"], a["T"], a["seed"], a["acc"], a["nxt"], a["st"], None)
+
+    assert call(t=None) == 1
+    assert call(T=float("nan")) == 1
+    assert call(cu=ctypes.c_void_p(p.value + 2)) == 3
+    assert call(st=ctypes.c_void_p(p.value + 1)) == 3
+    assert call(dt=9) == 2
+    assert call() == 2                      # valid arguments, batch beyond the scratch
