@@ -71,6 +71,12 @@ def make_batch(rank: int, **overrides):
     return synth.config(5, seed=1005 + 7919 * rank, **overrides)
 
 
+def head_inputs(N: int, rank: int):
+    """This rank's length-head inputs (drafter hidden states, random weights)."""
+    import synth
+    return synth.length_head_inputs(N, HEAD["k"], HEAD["H"], HEAD["Hp"], 2000 + rank)
+
+
 def reduce_over_ranks(ws: int, dev, elapsed_ms: float, units: float):
     """Job-level timing: the slowest rank's timed region (max) and the units
     all ranks processed (sum).  The only collectives of the run; none is on
@@ -107,7 +113,7 @@ CALL_KERNELS = {
 CALLS = ["verify_T0", "verify_T0.6", "verify_T1+opd", "length_head"]
 # top-k / top-p settings of the filtered-verification measurement: (T, top_k, top_p)
 FILTERS = [(1.0, 50, 0.9), (0.6, 20, 0.95)]
-HEAD = dict(k=16, H=4096, Hp=256, gamma=1.0)
+HEAD = dict(k=16, H=4096, Hp=256)
 WORKLOAD = ("mix: N=256 ragged L_i~U{2,4,8,16}, V=151936, bf16 log-Zipf logits; verify at T=0 and 0.6, "
             "verify at T=1 fused with OPD fwd/bwd (T=1,c=1,lambda=0.1); length head label + forward "
             "(k=16, H=4096, H'=256)")
@@ -205,6 +211,112 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
+# the other workload configurations: one measurement each (their parity is
+# tested in tests/); the headline stays on the mix workload
+# ---------------------------------------------------------------------------
+CONFIG_DESC = {
+    1: "tiny: N=4, L=16 (+bonus), V=1024, fp32 logits, T=1 (0.54 MB: L2-resident, latency only)",
+    2: "fixed: N=32, L=16 (+bonus), V=151936, bf16, T=1",
+    3: "ragged: N=128, L_i~U{2,4,8,16} packed by CSR, V=151936, bf16, T=1",
+    4: "opd: 64 requests x 16 draft rows paired 1:1, V=151936, bf16 in, fp32 dlogits, T=1, c=1, lambda=0.1",
+}
+
+
+def _dev_logits(torch, a, dev):
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+    return torch.from_numpy(a).to(dev)
+
+
+def _time_calls(torch, stream, fn, K):
+    """Average time of K back-to-back calls (CUDA events on the launch stream)."""
+    fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return 1000.0 * e0.elapsed_time(e1) / K
+
+
+def _time_kernel(torch, svw, kernel, fn, K):
+    """Average duration of one named kernel inside the call (its own events)."""
+    us = []
+    for _ in range(K):
+        k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        svw.time_next_launch(kernel, k0, k1)
+        fn()
+        torch.cuda.synchronize()
+        us.append(1000.0 * k0.elapsed_time(k1))
+    return float(np.mean(us))
+
+
+def bench_configs(svw, torch, dev, stream, rank, peak, K=30):
+    """spec_verify on workloads 1-3 and opd_loss on workload 4, each with its
+    algorithmic bytes (both logit tensors read once; the loss also writes its
+    fp32 gradient once), GB/s and fraction of the measured copy bandwidth, for
+    the call and for its main kernel."""
+    import synth
+    out = {}
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    for cfg in (1, 2, 3, 4):
+        b = synth.config(cfg, seed=1000 + cfg + 7919 * rank)
+        N, R, V = b.N, b.total_rows, b.V
+        es = 2 if b.dtype == "bf16" else 4
+        code = svw.SVW_BF16 if es == 2 else svw.SVW_F32
+        t, d = _dev_logits(torch, b.target, dev), _dev_logits(torch, b.draft, dev)
+        cu = torch.from_numpy(b.cu.astype(np.int32)).to(dev)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        if cfg < 4:
+            tok = torch.from_numpy(b.tokens[1.0].astype(np.int32)).to(dev)
+            acc = torch.empty(N, dtype=torch.int32, device=dev)
+            nxt = torch.empty(N, dtype=torch.int32, device=dev)
+            ws = torch.empty(svw.verify_workspace_size(N, R, V, code), dtype=torch.uint8, device=dev)
+
+            def fn():
+                svw.spec_verify(t, d, cu, tok, 1.0, 0, max_len=16, total_draft_rows=R, accept_len=acc,
+                                next_token=nxt, status=st, workspace=ws, stream=stream)
+            api, kernel = "spec_verify", "verify_stats"
+            alg = (2 * R + N) * V * es
+        else:
+            loss = torch.empty(R, dtype=torch.float32, device=dev)
+            grad = torch.empty((R, V), dtype=torch.float32, device=dev)
+            ws = torch.empty(svw.opd_workspace_size(R), dtype=torch.uint8, device=dev)
+
+            def fn():
+                svw.opd_loss(t, d, loss=loss, dlogits=grad, status=st, workspace=ws, stream=stream, **OPD)
+            api, kernel = "opd_loss", "opd_fast_kernel"
+            alg = 2 * R * V * es + R * V * 4
+        for _ in range(3):
+            fn()
+        call_us = _time_calls(torch, stream, fn, K)
+        kern_us = _time_kernel(torch, svw, kernel, fn, max(3, K // 2))
+        torch.cuda.synchronize()
+        rec = {"workload": CONFIG_DESC[cfg], "api": api, "positions": int(R), "call_us": call_us,
+               "positions_per_s": R / (call_us * 1e-6), "device_status": int(st.item())}
+        if cfg == 1:
+            rec["latency_us"] = call_us
+        else:
+            gbs = alg / (call_us * 1e-6) / 1e9
+            kgbs = alg / (kern_us * 1e-6) / 1e9
+            rec.update({"algorithmic_bytes": int(alg), "gbs": gbs, "frac_of_peak": gbs / peak,
+                        "frac_of_8tbs": gbs / 8000.0, "main_kernel": kernel, "main_kernel_us": kern_us,
+                        "main_kernel_gbs": kgbs, "main_kernel_frac_of_peak": kgbs / peak})
+        if cfg < 4:
+            rec["mean_accept_len"] = float(acc.float().mean().item())
+            C = -(-V * es // 36864)  # (row, chunk) items of the stats pass: <= 36 KB chunks
+            rec["stats_items"] = int((2 * R + N) * C)
+            rec["stats_items_per_sm"] = (2 * R + N) * C / nsm
+        out[f"cfg{cfg}"] = rec
+        del t, d, ws
+        torch.cuda.empty_cache()
+    return out
+
+
+# ---------------------------------------------------------------------------
 # native arm
 # ---------------------------------------------------------------------------
 def launches_per_step():
@@ -248,12 +360,12 @@ def run_native(args, ws, rank, local):
     fused_ws = torch.empty(svw.verify_opd_workspace_size(N, R, V, svw.SVW_BF16), dtype=torch.uint8, device=dev)
     # adaptive length head: synthetic drafter hidden states and random weights
     hk, hH, hHp = HEAD["k"], HEAD["H"], HEAD["Hp"]
-    g = torch.Generator().manual_seed(2000 + rank)
-    h_hid = torch.randn(N, hk, hH, generator=g).to(torch.bfloat16).pin_memory()
+    hin = head_inputs(N, rank)
+    h_hid = torch.from_numpy(hin["hidden"].view(np.int16)).view(torch.bfloat16).pin_memory()
     hid = h_hid.to(dev)
-    w1 = (torch.randn(hHp, hH, generator=g) * (2.0 / hH ** 0.5)).to(torch.bfloat16).to(dev)
-    b1 = (torch.randn(hHp, generator=g) * 0.3).to(dev)
-    w2 = (torch.randn(hHp, generator=g) * (2.0 / hHp ** 0.5)).to(dev)
+    w1 = torch.from_numpy(hin["w1"].view(np.int16)).view(torch.bfloat16).to(dev)
+    b1 = torch.from_numpy(hin["b1"]).to(dev)
+    w2 = torch.from_numpy(hin["w2"]).to(dev)
     head_ws = torch.empty(svw.lib().svw_length_head_workspace_size(N, hk, hHp), dtype=torch.uint8, device=dev)
     a_hat = torch.empty(N, dtype=torch.float32, device=dev)
     k_hat = torch.empty(N, dtype=torch.int32, device=dev)
@@ -291,8 +403,8 @@ def run_native(args, ws, rank, local):
         # forward pass that sets the next round's verified lengths
         x = cur[0]
         svw.length_head_label(acc[1.0], x["cu"], a_hat, a_star=a_star, loss=len_loss, stream=stream)
-        svw.length_head(x["hid"], w1, b1, w2, 0.2, HEAD["gamma"], a_hat=a_hat, k_hat=k_hat, workspace=head_ws,
-                        stream=stream)
+        svw.length_head(x["hid"], w1, b1, w2, hin["b2"], hin["gamma"], a_hat=a_hat, k_hat=k_hat,
+                        workspace=head_ws, stream=stream)
 
     def step(ev=None, kev=None):
         for ci, fn in enumerate((lambda: verify(0.0), lambda: verify(0.6), verify_opd, head)):
@@ -527,11 +639,20 @@ def run_native(args, ws, rank, local):
            "pipelining": "double-buffered inputs: step k+1's host-to-device copies overlap step k's kernels"}
 
     status_v = int(status.item())
+    gpu_acc = {T: acc[T].cpu().numpy() for T in TEMPS}
+    gpu_nxt = {T: nxt[T].cpu().numpy() for T in TEMPS}
+
+    # ---- the other workload configurations (parity cases of their own; one
+    # number each, not part of the step) ----
+    configs = bench_configs(svw, torch, dev, stream, rank, peak)
+
     cpu = None
     cpu_all = None
+    ties = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(b)
-        cpu_all = cpu_baseline_all_cores(b)
+        cpu = cpu_baseline(b, hin)
+        cpu_all = cpu_baseline_all_cores(b, hin)
+        ties = near_ties(b, gpu_acc, gpu_nxt)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
@@ -566,6 +687,8 @@ def run_native(args, ws, rank, local):
         "device_status": status_v,
         "cpu_baseline": cpu,
         "cpu_baseline_all_cores": cpu_all,
+        "near_ties": ties,
+        "configs": configs,
     }
     if ws > 1:
         torch.distributed.destroy_process_group()
@@ -581,26 +704,34 @@ def _oracle_sample(b, n_req):
     return sub, np.arange(n_req, dtype=np.int32)
 
 
-def oracle_step(sub, ids):
+def oracle_step(sub, ids, head):
+    """One step of the oracle on requests `ids`: the three verifications, the
+    OPD loss and gradient, and the length head's label and forward pass --
+    the same work as one native step."""
     import oracle
+    acc = None
     for T in TEMPS:
-        oracle.spec_verify(sub.target, sub.draft, sub.cu, sub.tokens[T], T, 0, max_len=16,
-                           req_ids=ids)
+        r = oracle.spec_verify(sub.target, sub.draft, sub.cu, sub.tokens[T], T, 0, max_len=16, req_ids=ids)
+        if T == 1.0:
+            acc = r["accept_len"]
     oracle.opd_loss(sub.target, sub.draft, cu_draft=sub.cu, has_bonus=True, **OPD)
+    h = oracle.length_head(head["hidden"][ids], head["w1"], head["b1"], head["w2"], head["b2"], head["gamma"])
+    oracle.length_label(acc, sub.cu, h["a_hat"])
 
 
-def cpu_baseline(b, n_req=40):
+def cpu_baseline(b, head, n_req=40):
     """Oracle timed on a bounded sample: the first n_req requests of the batch,
-    one full step (three verifications and the OPD loss + gradient)."""
+    one full step (three verifications, the OPD loss + gradient, the length
+    head)."""
     import oracle
     oracle.build()
     sub, ids = _oracle_sample(b, n_req)
     t0 = time.perf_counter()
-    oracle_step(sub, ids)
+    oracle_step(sub, ids, head)
     dt = time.perf_counter() - t0
     return {"value": 3 * sub.total_rows / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"first {n_req} requests ({sub.total_rows} positions) of the mix batch, "
-                      f"one step: verify T=0,0.6,1 + OPD fwd/bwd; {dt:.1f} s"}
+                      f"one step: verify T=0,0.6,1 + OPD fwd/bwd + length head; {dt:.1f} s"}
 
 
 def _host_cores():
@@ -622,13 +753,13 @@ def _oracle_groups(b, n_req, nt):
     return groups
 
 
-def oracle_step_threads(groups, pool):
+def oracle_step_threads(groups, pool, head):
     """One step of the unchanged oracle, its requests spread over threads (the
     requests are independent; the C calls release the GIL)."""
-    list(pool.map(lambda g: oracle_step(*g), groups))
+    list(pool.map(lambda g: oracle_step(g[0], g[1], head), groups))
 
 
-def cpu_baseline_all_cores(b):
+def cpu_baseline_all_cores(b, head):
     """The oracle on every request of the batch, one thread per host core."""
     import oracle
     from concurrent.futures import ThreadPoolExecutor
@@ -639,11 +770,55 @@ def cpu_baseline_all_cores(b):
     rows = sum(g[0].total_rows for g in groups)
     with ThreadPoolExecutor(max_workers=nt) as pool:
         t0 = time.perf_counter()
-        oracle_step_threads(groups, pool)
+        oracle_step_threads(groups, pool, head)
         dt = time.perf_counter() - t0
     return {"value": 3 * rows / dt, "unit": UNIT, "cores": nt, "kind": "oracle",
             "sample": f"all {b.N} requests ({rows} positions) of the mix batch, one step: verify T=0,0.6,1 "
-                      f"+ OPD fwd/bwd, requests split over {nt} threads; {dt:.1f} s"}
+                      f"+ OPD fwd/bwd + length head, requests split over {nt} threads; {dt:.1f} s"}
+
+
+NEAR_BAND = 1e-5
+
+
+def near_ties(b, acc, nxt):
+    """The oracle's near-tie flags on the whole batch at each temperature of
+    the step, against the GPU's results (one oracle pass per temperature on
+    all host cores, outside any timed region): requests flagged near an
+    accept threshold / a CDF boundary (band 1e-5), how many of them the GPU
+    decided differently, and whether each such difference is within the band
+    (the oracle's distance from its draw point to the GPU token's CDF
+    interval).  Unflagged differences would be parity failures."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    oracle.build()
+    nt = _host_cores()
+    groups = _oracle_groups(b, b.N, 4 * nt)
+    out = {}
+    for T in TEMPS:
+        def work(g):
+            sub, ids = g
+            return ids, oracle.spec_verify(sub.target, sub.draft, sub.cu, sub.tokens[T], T, 0, max_len=16,
+                                           req_ids=ids, alt_next=nxt[T][ids])
+        with ThreadPoolExecutor(max_workers=nt) as pool:
+            res = list(pool.map(work, groups))
+        fl = np.zeros(b.N, np.int32)
+        ra = np.zeros(b.N, np.int32)
+        rn = np.zeros(b.N, np.int32)
+        dist = np.zeros(b.N)
+        for ids, r in res:
+            fl[ids], ra[ids], rn[ids], dist[ids] = r["flags"], r["accept_len"], r["next_token"], r["alt_dist"]
+        near = (fl & (oracle.FLAG_NEAR_ACCEPT | oracle.FLAG_NEAR_CDF | oracle.FLAG_DEGENERATE)) != 0
+        diff = (acc[T] != ra) | (nxt[T] != rn)
+        tok_diff = diff & (acc[T] == ra)
+        out[f"T{T:g}"] = {
+            "requests": int(b.N), "band": NEAR_BAND,
+            "flagged_near_accept": int(((fl & oracle.FLAG_NEAR_ACCEPT) != 0).sum()),
+            "flagged_near_cdf": int(((fl & oracle.FLAG_NEAR_CDF) != 0).sum()),
+            "flagged_and_differing": int((diff & near).sum()),
+            "unflagged_differing": int((diff & ~near).sum()),
+            "differing_tokens_within_band": bool(np.all(dist[tok_diff] <= NEAR_BAND)),
+        }
+    return out
 
 
 def run_reference(args, ws, rank):
@@ -656,26 +831,27 @@ def run_reference(args, ws, rank):
     oracle.build()
     oracle._load()
     b = make_batch(0)
+    head = head_inputs(b.N, 0)
     nt = _host_cores()
     # size each step's sample so that warmup + steps finish in about 90 s
     probe, pids = _oracle_sample(b, 1)
     t0 = time.perf_counter()
-    oracle_step(probe, pids)
+    oracle_step(probe, pids, head)
     per_req = max(1e-3, time.perf_counter() - t0)
     n_req = int(max(1, min(b.N, 90.0 * nt / (per_req * max(1, args.steps + args.warmup)))))
     groups = _oracle_groups(b, n_req, nt)
     rows = sum(g[0].total_rows for g in groups)
     with ThreadPoolExecutor(max_workers=nt) as pool:
         for _ in range(args.warmup):
-            oracle_step_threads(groups, pool)
+            oracle_step_threads(groups, pool, head)
         K = args.steps
         t0 = time.perf_counter()
         for _ in range(K):
-            oracle_step_threads(groups, pool)
+            oracle_step_threads(groups, pool, head)
         dt = (time.perf_counter() - t0) / K
     value = 3 * rows / dt
-    sample = (f"first {n_req} requests ({rows} positions) of the mix batch per step, "
-              f"fp64 oracle, requests split over {nt} threads")
+    sample = (f"first {n_req} requests ({rows} positions) of the mix batch per step (verify T=0,0.6,1 + "
+              f"OPD fwd/bwd + length head), fp64 oracle, requests split over {nt} threads")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
         "steps": K, "warmup": args.warmup, "ms_per_step": dt * 1000.0,

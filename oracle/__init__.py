@@ -65,7 +65,7 @@ def _load():
             lib.oracle_uniform.restype = ctypes.c_double
             lib.oracle_spec_verify.argtypes = [
                 P, P, ctypes.c_int, ctypes.c_int64, ctypes.c_int32, P, P,
-                ctypes.c_double, ctypes.c_uint64, ctypes.c_int32, P, P, P, P, P]
+                ctypes.c_double, ctypes.c_uint64, ctypes.c_int32, P, P, P, P, P, P, P]
             lib.oracle_spec_verify.restype = ctypes.c_int
             lib.oracle_spec_verify_filtered.argtypes = [
                 P, P, ctypes.c_int, ctypes.c_int64, ctypes.c_int32, P, P,
@@ -117,11 +117,15 @@ def uniform(seed: int, i: int, j: int, s: int) -> float:
 
 
 def spec_verify(target, draft, cu_draft, tokens, temperature, seed, max_len=32,
-                req_ids=None, want_thr=False):
-    """Verify a ragged batch.  Returns dict(accept_len, next_token, flags[, thr]).
+                req_ids=None, want_thr=False, alt_next=None):
+    """Verify a ragged batch.  Returns dict(accept_len, next_token, flags[, thr]
+    [, alt_dist]).
 
     target: [total_rows + N, V], draft: [total_rows, V] (uint16 bf16 bits or
     float32); cu_draft: int32 [N + 1]; tokens: int32 [total_rows].
+    alt_next: optional int32 [N], another implementation's next tokens; then
+    alt_dist[n] is the distance (fraction of Z) from w Z to that token's CDF
+    interval in the distribution the oracle drew from (0: the same draw).
     """
     lib = _load()
     t, dt = _logits(target)
@@ -136,14 +140,18 @@ def spec_verify(target, draft, cu_draft, tokens, temperature, seed, max_len=32,
     nxt = np.zeros(N, dtype=np.int32)
     flg = np.zeros(N, dtype=np.int32)
     thr = np.full(max(1, tok.shape[0]), np.nan) if want_thr else None
+    alt = None if alt_next is None else np.ascontiguousarray(alt_next, dtype=np.int32)
+    adist = None if alt is None else np.zeros(N, dtype=np.float64)
     rc = lib.oracle_spec_verify(_ptr(t), _ptr(d), dt, V, N, _ptr(cu), _ptr(tok),
                                 float(temperature), int(seed), int(max_len), _ptr(rid),
-                                _ptr(acc), _ptr(nxt), _ptr(flg), _ptr(thr))
+                                _ptr(acc), _ptr(nxt), _ptr(flg), _ptr(thr), _ptr(alt), _ptr(adist))
     if rc != 0:
         raise MemoryError("oracle_spec_verify failed to allocate")
     out = dict(accept_len=acc, next_token=nxt, flags=flg)
     if want_thr:
         out["thr"] = thr[: tok.shape[0]]
+    if alt is not None:
+        out["alt_dist"] = adist
     return out
 
 

@@ -229,6 +229,20 @@ static int64_t inverse_cdf(const double *r, int64_t V, double Z, double w, int *
   return pick;
 }
 
+/* Distance, as a fraction of Z, from t = w Z to the CDF interval
+ * [C_{alt-1}, C_alt) of token alt (0 if t lies inside it, i.e. if the inverse
+ * CDF of [DF] §5.2 eq. (7) would draw alt): how far another implementation's
+ * token is from being this draw's.  +inf for an index outside [0, V). */
+static double cdf_interval_distance(const double *r, int64_t V, double Z, double w, int64_t alt) {
+  if (alt < 0 || alt >= V) return INFINITY;
+  double t = w * Z, C = 0.0;
+  for (int64_t v = 0; v < alt; ++v) C += r[v];
+  double lo = C, hi = C + r[alt];
+  if (t < lo) return (lo - t) / Z;
+  if (t >= hi) return (t - hi) / Z;
+  return 0.0;
+}
+
 /* ------------------------------------------------------------------ */
 /* speculative verification                                            */
 /* ------------------------------------------------------------------ */
@@ -242,12 +256,19 @@ static int64_t inverse_cdf(const double *r, int64_t V, double Z, double w, int *
  *          batch's own uniforms.
  * thr_out: optional [total_rows]; acceptance threshold min(1, p/q) per
  *          position (NaN where not computed).
+ * alt_next, alt_dist: optional [N] each; for request n, alt_dist[n] is the
+ *          distance (a fraction of Z) from w Z to the CDF interval of token
+ *          alt_next[n] in the distribution this oracle drew from (0: the
+ *          same draw; at T = 0, 0 if alt_next[n] is the argmax else +inf).
+ *          A test passes the GPU's tokens to check that every mismatch it
+ *          excuses as near a CDF boundary really is within the band.
  * Returns 0; per-request problems are reported through flags.
  */
 int oracle_spec_verify(const void *target, const void *draft, int dtype, int64_t V, int32_t N,
                        const int32_t *cu, const int32_t *tokens, double temperature, uint64_t seed,
                        int32_t max_len, const int32_t *req_ids, int32_t *accept_len,
-                       int32_t *next_token, int32_t *flags, double *thr_out) {
+                       int32_t *next_token, int32_t *flags, double *thr_out, const int32_t *alt_next,
+                       double *alt_dist) {
   double *P = (double *)malloc(sizeof(double) * (size_t)V);
   double *Q = (double *)malloc(sizeof(double) * (size_t)V);
   double *R = (double *)malloc(sizeof(double) * (size_t)V);
@@ -263,6 +284,7 @@ int oracle_spec_verify(const void *target, const void *draft, int dtype, int64_t
     flags[n] = 0;
     accept_len[n] = -1;
     next_token[n] = -1;
+    if (alt_dist) alt_dist[n] = NAN;
     if (thr_out)
       for (int32_t j = 0; j < L && j >= 0; ++j) thr_out[drow0 + j] = NAN;
     if (L < 1 || L > max_len) {
@@ -298,6 +320,7 @@ int oracle_spec_verify(const void *target, const void *draft, int dtype, int64_t
       }
       accept_len[n] = a;
       next_token[n] = (int32_t)row_argmax(target, dtype, trow0 + a, V);
+      if (alt_dist) alt_dist[n] = (alt_next[n] == next_token[n]) ? 0.0 : INFINITY;
       continue;
     }
 
@@ -354,6 +377,7 @@ int oracle_spec_verify(const void *target, const void *draft, int dtype, int64_t
     int near = 0;
     next_token[n] = (int32_t)inverse_cdf(R, V, Z, w, &near);
     if (near) flags[n] |= FLAG_NEAR_CDF;
+    if (alt_dist) alt_dist[n] = cdf_interval_distance(R, V, Z, w, alt_next[n]);
   }
   free(P);
   free(Q);
@@ -423,7 +447,7 @@ int oracle_spec_verify_filtered(const void *target, const void *draft, int dtype
   if (temperature == 0.0)
     /* filtering keeps the argmax: greedy verification is unchanged */
     return oracle_spec_verify(target, draft, dtype, V, N, cu, tokens, 0.0, seed, max_len, req_ids, accept_len,
-                              next_token, flags, NULL);
+                              next_token, flags, NULL, NULL, NULL);
   double *P = (double *)malloc(sizeof(double) * (size_t)V);
   double *Q = (double *)malloc(sizeof(double) * (size_t)V);
   double *R = (double *)malloc(sizeof(double) * (size_t)V);

@@ -2,8 +2,8 @@
 // loss on the same batch in one pass over the logits).
 //
 // The OPD fast kernel has already reduced every draft row together with its
-// target row (log-sum-exp offsets Ct, Cd in log2 units: log2 p = y k - Ct,
-// log2 q = z k - Cd; the target argmax x*) and every bonus row (Ct, argmax).
+// target row (in log2 units log2 p = y k - Ct and log2 q - log2 p =
+// (z - y) k - dC; the target argmax x*) and every bonus row (Ct, argmax).
 // What verification still needs per request is what "Speculative Decoding:
 // The Basic Idea" steps 3-4 ("AdaFlash: Taming Variance in Diffusion
 // Speculative Decoding") and "DFlash 阅读笔记" §5.1-§5.2 define on top of the
@@ -61,13 +61,13 @@ __global__ void __launch_bounds__(kFThreads) fused_finalize(FusedArgs a) {
 
     int csr_bad = 0;
     for (int b = lane; b < a.csr_grid; b += 32) csr_bad |= __ldcg(a.csr_bad + b);
-    float Ct = 0.f, Cd = 0.f;
+    float Ct = 0.f, dC = 0.f;
     int32_t xs = -1;
     bool row_bad = false;
     if (lane < L) {
       const float4 rc = __ldcg(a.rowc + d0 + lane);
       Ct = rc.x;
-      Cd = rc.y;
+      dC = rc.y;
       xs = __float_as_int(rc.z);
       row_bad = !(Ct == Ct);
     }
@@ -111,8 +111,8 @@ __global__ void __launch_bounds__(kFThreads) fused_finalize(FusedArgs a) {
         } else if (zx == -INFINITY) {
           acc = true;  // q(x) = 0: accept
         } else {
-          // log2 p(x) - log2 q(x) from the raw logits and the row offsets
-          const float dl = __fsub_rn(__fmaf_rn(yx, a.k, -Ct), __fmaf_rn(zx, a.k, -Cd));
+          // log2 p(x) - log2 q(x) = (y_x - z_x) k + dC (the logit difference is exact)
+          const float dl = __fmaf_rn(__fsub_rn(yx, zx), a.k, dC);
           acc = u < ((dl >= 0.f) ? 1.f : ex2(dl));
         }
       }
@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(kFThreads) fused_finalize(FusedArgs a) {
       const int src = (js < L) ? js : 0;
       const int32_t xs_js = __shfl_sync(0xffffffffu, xs, src);
       const float Ct_js = __shfl_sync(0xffffffffu, Ct, src);
-      const float Cd_js = __shfl_sync(0xffffffffu, Cd, src);
+      const float Cd_js = Ct_js + __shfl_sync(0xffffffffu, dC, src);
       if (lane == 0) {
         a.accept_len[i] = js;
         if (GREEDY) a.next_token[i] = (js < L) ? xs_js : __float_as_int(br.y);

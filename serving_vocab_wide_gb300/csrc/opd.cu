@@ -18,23 +18,38 @@
 // Fast kernel (16-byte-pitched rows).  Each thread moves its vectors of the
 // slices from shared memory into registers as soon as they land, and the
 // buffer is handed to the next row's copies at once.  One pass over the
-// registers gives, per row, both log-sum-exps, the target argmax with the
-// draft logit there, and U = sum_v 2^((z_v - m_z)k) ((z_v - m_z)k - (y_v - m_y)k),
+// registers gives, per row, S_y = sum 2^((y - m_y)k), W = sum (2^((z - m_z)k)
+// - 2^((y - m_y)k)) (so S_z = S_y + W), the target argmax with the draft
+// logit there, and U = sum_v 2^((z_v - m_z)k) ((z_v - y_v)k - (m_z - m_y)k),
 // so that without clipping
-//   KL(q||p) = ln2 (U/S_z - log2 S_z + log2 S_y),  S = sum_v q_v a_v = KL + 1;
-// one DSMEM exchange (barrier.cluster) merges these over the cluster, and a
-// second register pass writes the gradient.  An entry whose term reaches the
-// clip bound, or a non-finite KL (masked entries), flags the row: the flag
-// word is set to the call's tag (never cleared), so flags need no ordering
-// and a stale tag at worst sends a row to the exact fix-up once more.
+//   KL(q||p) = ln2 (U/S_z - log2(1 + W/S_y)),  S = sum_v q_v a_v = KL + 1;
+// one exchange of partials merges these over the cluster, and a second
+// register pass writes the gradient.  Precision: where the draft is close to
+// its target (on-policy distillation converges there) log q - log p is small
+// and the KL is its second moment, so nothing may be formed as a difference
+// of two quantities of magnitude ~20.  The log ratio of an entry is
+// (z - y)k - dC (the logit difference is exact for bf16, dC = Cd - Ct comes
+// from W with an accurate log1p), never (z k - Cd) - (y k - Ct); W is summed
+// term by term, never as S_z - S_y.  What is left is about 1e-7 (absolute)
+// of KL from the exp2 unit and rounding; a row whose loss is small enough
+// for that to matter (below kFastLossFloor) is flagged for a loss-only
+// recomputation by the fix-up.  An entry whose term reaches the clip bound,
+// or a non-finite KL (masked entries), flags the row for the full
+// recomputation: the flag word is set to the call's tag (never cleared), so
+// flags need no ordering and a stale tag at worst sends a row to the exact
+// fix-up once more.
 // Fix-up.  Rows the fast kernel flagged are redone exactly from the row
 // constants it stored, by two flat grids over (row, vocabulary chunk) items:
 // clamped terms and S per chunk, then the row totals and the gradient.
 // Exact kernel.  Without a workspace (or for rows that are not 16-byte
 // pitched) every row is done from shared memory in three passes:
 // log-sum-exps; clamped terms, S and the argmax; gradient -- two exchanges.
-// In log2 units: A = log2 q = z k - Cd, Bp = log2 p = y k - Ct, d2 = A - Bp,
-// t/ln2 = q d2, q(d + 1) = t + q; per-entry arithmetic runs on f32x2 pairs.
+// The exact kernel and the fix-up sum sum_v [clamp(t_v) - q_v + p_v] (= the
+// clamped sum, since both rows are normalised; see psi_nat): this form is to
+// first order insensitive to the rounding of the row constants, and it keeps
+// the small-KL regime precise without the fast kernel's W machinery.
+// In log2 units: log2 q = z k - Cd, log2 p = y k - Ct, d2 = (z - y) k - dC,
+// t/ln2 = q d2; per-entry arithmetic runs on f32x2 pairs.
 // Every wait on a bulk copy is bounded by a clock deadline; on expiry the CTA
 // records SVW_DEV_TIMEOUT, stops issuing copies and keeps joining the cluster
 // barriers so that no peer can hang.
@@ -58,6 +73,12 @@ namespace svw {
 namespace {
 
 constexpr int kMaxWarps = 32;
+// The fast kernel's KL comes from the row sums s_y, w, u: rounding and the
+// SFU's exp2 error leave about 1e-7 (absolute, nats) in it.  A loss smaller
+// than this bound (a draft almost equal to its target with a small lambda) is
+// summed again exactly by the fix-up grids, so that it keeps its relative
+// precision; the gradient does not need it (its scale is that of log q - log p).
+constexpr float kFastLossFloor = 4e-3f;
 constexpr int kMaxCluster = 8;
 static_assert(kMaxCluster <= kBonusParts, "bonus partial stride");
 
@@ -73,18 +94,6 @@ struct OpdSmem {
   int32_t abort;
   uint32_t abort_parity;  // phase of the copy that timed out
 };
-
-// one entry's contribution when its term is clipped or undefined (rare):
-// NaN arises only from q = 0 against an infinite log ratio, whose term is 0
-__device__ __forceinline__ void term_slow(float t2, float q, float c2, float &rkl2, float &S) {
-  if (t2 != t2) return;
-  if (fabsf(t2) < c2) {
-    rkl2 += t2;
-    S += fmaf(t2, kLn2, q);
-  } else {
-    rkl2 += (t2 > 0.f) ? c2 : -c2;
-  }
-}
 
 // Exact three-pass kernel (every row; the path without a workspace).
 template <int DT, bool BULK>
@@ -263,41 +272,37 @@ __global__ void __launch_bounds__(512, 2) opd_exact_kernel(OpdArgs a, OpdGeo geo
     const bool any_abort = sm.rowA[4] != 0.f;
     const bool row_ok = valid && !any_abort && (St > 0.f && St <= FLT_MAX) && (Sd > 0.f && Sd <= FLT_MAX);
     const float Ct = fmaf(Mt, k, lg2(St));  // log2 p = y k - Ct
-    const float Cd = fmaf(Md, k, lg2(Sd));  // log2 q = z k - Cd
+    // dC = Cd - Ct from the maxima's exact difference and an accurate log2 of
+    // the ratio of the sums: log2 q - log2 p = (z - y) k - dC, with no
+    // cancellation between two row offsets of magnitude ~20
+    const float dC = fmaf(Md - Mt, k, log2f(Sd / St));
+    const float Cd = Ct + dC;               // log2 q = z k - Cd
     const float c2 = a.clip_c * kLog2e;     // clip bound in log2 units of t
     float rkl = 0.f, S = 0.f;
     int32_t cand = INT32_MAX;
 
     // ---------------- pass B: clamped terms, S, argmax ----------------
+    // rkl = sum_v [clamp(t_v) - q_v + p_v] (nats), insensitive to first order
+    // to the rounding of Ct and dC (see psi_nat)
     if (row_ok) {
-      const float2 kk = make_float2(k, k), nkk = make_float2(-k, -k);
-      const float2 nCd = make_float2(-Cd, -Cd), Ct2 = make_float2(Ct, Ct), l2 = make_float2(kLn2, kLn2);
-      float2 r2 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
+      const float2 kk = make_float2(k, k), neg1 = make_float2(-1.f, -1.f);
+      const float2 nCd = make_float2(-Cd, -Cd), ndC = make_float2(-dC, -dC);
       for (int vi = tid; vi < nvec; vi += kThreads) {
         const Pairs<DT> y(lds128(tb + vi * 16)), z(lds128(db + vi * 16));
 #pragma unroll
         for (int h = 0; h < Pairs<DT>::kN; ++h) {
-          const float2 A = __ffma2_rn(z.p[h], kk, nCd);    // log2 q
+          const float2 A = __ffma2_rn(z.p[h], kk, nCd);                                  // log2 q
           const float2 q = make_float2(ex2(A.x), ex2(A.y));
-          const float2 d = __fadd2_rn(A, __ffma2_rn(y.p[h], nkk, Ct2));  // log2 q - log2 p
-          const float2 t = __fmul2_rn(q, d);               // t / ln 2
-          if (fabsf(t.x) < c2 && fabsf(t.y) < c2) {
-            r2 = __fadd2_rn(r2, t);
-            s2 = __fadd2_rn(__ffma2_rn(t, l2, s2), q);
-          } else {
-            term_slow(t.x, q.x, c2, r2.x, s2.x);
-            term_slow(t.y, q.y, c2, r2.y, s2.y);
-          }
+          const float2 d = __ffma2_rn(__ffma2_rn(y.p[h], neg1, z.p[h]), kk, ndC);        // log2 q - log2 p
+          clamped_term(q.x, d.x, y.p[h].x, k, Ct, c2, a.clip_c, rkl, S);
+          clamped_term(q.y, d.y, y.p[h].y, k, Ct, c2, a.clip_c, rkl, S);
         }
       }
-      rkl = r2.x + r2.y;
-      S = s2.x + s2.y;
       if (!BULK && tid == 0)
         for (int v = nvec * EPV; v < n; ++v) {
           const float y = E::load_plain(tbuf, v), z = E::load_plain(dbuf, v);
-          const float A = fmaf(z, k, -Cd);
-          const float q = ex2(A);
-          term_slow(q * (A - fmaf(y, k, -Ct)), q, c2, rkl, S);
+          const float q = ex2(fmaf(z, k, -Cd));
+          clamped_term(q, fmaf(z - y, k, -dC), y, k, Ct, c2, a.clip_c, rkl, S);
         }
       // first index holding the row maximum (only threads that saw it look)
       if (my_mt == Mt) {
@@ -366,14 +371,14 @@ __global__ void __launch_bounds__(512, 2) opd_exact_kernel(OpdArgs a, OpdGeo geo
       }
     }
     __syncthreads();
-    const float RKL2 = sm.rowB[0], SS = sm.rowB[1];
+    const float RKL = sm.rowB[0], SS = sm.rowB[1];
     const int32_t xs = __float_as_int(sm.rowB[2]);
     if (rank == 0 && tid == 0) {
       float out = __int_as_float(0x7fffffff);
       if (row_ok && xs != INT32_MAX) {
         const float zx = E::load(a.draft, r * V + xs);
-        // loss = sum clamp(t) + lambda * (-lq[x*]);  t = ln2 * t2, lq = ln2 * A
-        out = kLn2 * (RKL2 - a.lambda_ce * fmaf(zx, k, -Cd));
+        // loss = sum clamp(t) + lambda * (-lq[x*]);  -lq[x*] = ln2 ((Md - z_x*) k + log2 Sd)
+        out = fmaf(a.lambda_ce * kLn2, fmaf(Md - zx, k, lg2(Sd)), RKL);
       } else if (a.status && !any_abort) {
         atomicOr(a.status, SVW_DEV_BAD_INPUT);
       }
@@ -383,15 +388,16 @@ __global__ void __launch_bounds__(512, 2) opd_exact_kernel(OpdArgs a, OpdGeo geo
     // ---------------- pass C: gradient wrt the draft logits ----------------
     // dz = gsT (qa + q (lambda - S)) - gsT lambda [v = x*], qa = t + q when
     // |t| < c else 0; in log2 units dz = t2 gsT ln2 + q gsT (lambda - S + 1).
+    // SS holds S - 1.
     if (a.dlogits != nullptr && valid && !any_abort) {
       const float gsT = a.grad_scale * a.invT;
-      const float gL0 = gsT * (a.lambda_ce - SS);
-      const float gL1 = gsT * (a.lambda_ce - SS + 1.f);
+      const float gL0 = gsT * (a.lambda_ce - SS - 1.f);
+      const float gL1 = gsT * (a.lambda_ce - SS);
       const float nan = __int_as_float(0x7fffffff);
       float *out = a.dlogits + r * V + lo;
       if (BULK) {
-        const float2 kk = make_float2(k, k), nkk = make_float2(-k, -k);
-        const float2 nCd = make_float2(-Cd, -Cd), Ct2 = make_float2(Ct, Ct);
+        const float2 kk = make_float2(k, k), neg1 = make_float2(-1.f, -1.f);
+        const float2 nCd = make_float2(-Cd, -Cd), ndC = make_float2(-dC, -dC);
         const float2 gl = make_float2(gsT * kLn2, gsT * kLn2), g1 = make_float2(gL1, gL1);
         for (int vi = tid; vi < nvec; vi += kThreads) {
           const Pairs<DT> y(lds128(tb + vi * 16)), z(lds128(db + vi * 16));
@@ -400,7 +406,7 @@ __global__ void __launch_bounds__(512, 2) opd_exact_kernel(OpdArgs a, OpdGeo geo
           for (int h = 0; h < Pairs<DT>::kN; ++h) {
             const float2 A = __ffma2_rn(z.p[h], kk, nCd);
             const float2 q = make_float2(ex2(A.x), ex2(A.y));
-            const float2 t = __fmul2_rn(q, __fadd2_rn(A, __ffma2_rn(y.p[h], nkk, Ct2)));
+            const float2 t = __fmul2_rn(q, __ffma2_rn(__ffma2_rn(y.p[h], neg1, z.p[h]), kk, ndC));
             float2 gg = __ffma2_rn(t, gl, __fmul2_rn(q, g1));
             if (!(fabsf(t.x) < c2 && fabsf(t.y) < c2)) {
               if (!(fabsf(t.x) < c2)) gg.x = q.x * gL0;
@@ -426,9 +432,8 @@ __global__ void __launch_bounds__(512, 2) opd_exact_kernel(OpdArgs a, OpdGeo geo
       } else {
         for (int v = tid; v < n; v += kThreads) {
           const float y = E::load_plain(tbuf, v), z = E::load_plain(dbuf, v);
-          const float A = fmaf(z, k, -Cd);
-          const float q = ex2(A);
-          const float t = q * (A - fmaf(y, k, -Ct));
+          const float q = ex2(fmaf(z, k, -Cd));
+          const float t = q * fmaf(z - y, k, -dC);
           float g = (fabsf(t) < c2) ? fmaf(t, gsT * kLn2, q * gL1) : q * gL0;
           if (lo + v == xs) g -= gsT * a.lambda_ce;
           out[v] = row_ok ? g : nan;
@@ -687,9 +692,11 @@ __global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) 
       }
       const float nmy = (My == -INFINITY) ? 0.f : -My * k;
       const float nmz = (Mz == -INFINITY) ? 0.f : -Mz * k;
+      // log-ratio reference (m_z - m_y) k of this warp's partial
+      const float ncw = (My == -INFINITY || Mz == -INFINITY) ? 0.f : -(Mz - My) * k;
       const float2 kk = make_float2(k, k), ny2 = make_float2(nmy, nmy), nz2 = make_float2(nmz, nmz);
-      const float2 neg1 = make_float2(-1.f, -1.f);
-      float2 sy = make_float2(0.f, 0.f), sz = make_float2(0.f, 0.f), uu = make_float2(0.f, 0.f);
+      const float2 nc2 = make_float2(ncw, ncw), neg1 = make_float2(-1.f, -1.f);
+      float2 sy = make_float2(0.f, 0.f), ww = make_float2(0.f, 0.f), uu = make_float2(0.f, 0.f);
 #pragma unroll
       for (int j = 0; j < VPT; ++j)
         if (j < nj) {
@@ -698,13 +705,15 @@ __global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) 
           for (int h = 0; h < Pairs<DT>::kN; ++h) {
             const float2 ay = __ffma2_rn(y.p[h], kk, ny2);  // (y - m_y) k
             const float2 az = __ffma2_rn(z.p[h], kk, nz2);  // (z - m_z) k
+            const float2 ey = make_float2(ex2(ay.x), ex2(ay.y));
             const float2 ez = make_float2(ex2(az.x), ex2(az.y));
-            sy = __fadd2_rn(sy, make_float2(ex2(ay.x), ex2(ay.y)));
-            sz = __fadd2_rn(sz, ez);
-            uu = __ffma2_rn(ez, __ffma2_rn(ay, neg1, az), uu);
+            const float2 xd = __ffma2_rn(__ffma2_rn(y.p[h], neg1, z.p[h]), kk, nc2);  // (z - y) k - (m_z - m_y) k
+            sy = __fadd2_rn(sy, ey);
+            ww = __fadd2_rn(ww, __ffma2_rn(ey, neg1, ez));
+            uu = __ffma2_rn(ez, xd, uu);
           }
         }
-      float s0 = sy.x + sy.y, s1 = sz.x + sz.y, s2 = uu.x + uu.y;
+      float s0 = sy.x + sy.y, s1 = ww.x + ww.y, s2 = uu.x + uu.y;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         s0 += __shfl_xor_sync(0xffffffffu, s0, o);
@@ -716,7 +725,7 @@ __global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) 
       P.my = My;
       P.mz = Mz;
       P.sy = s0;
-      P.sz = s1;
+      P.w = s1;
       P.u = s2;
       P.idx = best;
       P.zx = __shfl_sync(0xffffffffu, zx, holders ? __ffs(holders) - 1 : 0);
@@ -729,7 +738,7 @@ __global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) 
       const FastPart Pc = merge_lanes<kWarps>(lane < kWarps ? sm.red[lane] : empty_part(), k);
       if (lane < CL) {  // lane q pushes this CTA's partial to CTA q
         const uint4 w0 = make_uint4(__float_as_uint(Pc.my), __float_as_uint(Pc.sy), __float_as_uint(Pc.mz),
-                                    __float_as_uint(Pc.sz));
+                                    __float_as_uint(Pc.w));
         const uint4 w1 = make_uint4(__float_as_uint(Pc.u), static_cast<uint32_t>(Pc.idx), __float_as_uint(Pc.zx),
                                     static_cast<uint32_t>(Pc.abort));
         const uint32_t dst = mapa_shared(smem_u32(&sm.inbox[slot][rank]), lane);
@@ -752,22 +761,31 @@ __global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) 
     __syncthreads();  // the merged row is published
     const FastPart Rw = sm.row;
     const bool any_abort = Rw.abort != 0;
-    const bool row_ok = valid && !any_abort && (Rw.sy > 0.f && Rw.sy <= FLT_MAX) && (Rw.sz > 0.f && Rw.sz <= FLT_MAX);
-    const float lsy = lg2(Rw.sy), lsz = lg2(Rw.sz);
-    const float Ct = fmaf(Rw.my, k, lsy);  // log2 p = y k - Ct
-    const float Cd = fmaf(Rw.mz, k, lsz);  // log2 q = z k - Cd
-    const float kl = kLn2 * (Rw.u / Rw.sz - lsz + lsy);  // unclipped KL(q||p)
-    const float c2 = a.clip_c * kLog2e;                  // clip bound for t / ln 2
+    const float Sz = Rw.sy + Rw.w;
+    const bool row_ok = valid && !any_abort && (Rw.sy > 0.f && Rw.sy <= FLT_MAX) && (Sz > 0.f && Sz <= FLT_MAX);
+    const float Ct = fmaf(Rw.my, k, lg2(Rw.sy));  // log2 p = y k - Ct
+    // log2(S_z / S_y) from the termwise difference w (accurate log1p), and
+    // dC = Cd - Ct: log2 q - log2 p = (z - y) k - dC
+    const float l2r = log1pf(Rw.w / Rw.sy) * kLog2e;
+    const float dC = fmaf(Rw.mz - Rw.my, k, l2r);
+    const float Cd = Ct + dC;                     // log2 q = z k - Cd
+    // unclipped KL(q||p) = E_q[(z - y) k - (m_z - m_y) k] - log2(S_z / S_y), in nats
+    const float kl = kLn2 * (Rw.u / Sz - l2r);
+    const float c2 = a.clip_c * kLog2e;           // clip bound for t / ln 2
     const int32_t xs = Rw.idx;
     const bool exact = (kl == kl) && fabsf(kl) <= FLT_MAX;
     if (rank == 0 && tid == 0) {
       float out = __int_as_float(0x7fffffff);
       float4 rc = make_float4(__int_as_float(0x7fffffff), 0.f, 0.f, 0.f);  // NaN: not a row to fix
       if (row_ok && xs != INT32_MAX) {
-        out = kl - a.lambda_ce * kLn2 * fmaf(Rw.zx, k, -Cd);
-        if (!exact) a.flags[r] = a.epoch;  // masked entries: the fix-up kernel redoes this row
+        // loss = KL + lambda (-lq[x*]),  -lq[x*] = ln2 ((m_z - z_x*) k + log2 S_z)
+        out = fmaf(a.lambda_ce * kLn2, fmaf(Rw.mz - Rw.zx, k, lg2(Sz)), kl);
+        if (!exact)
+          atomicExch(a.flags + r, a.epoch);  // masked entries: the fix-up redoes this row
+        else if (!(fabsf(out) >= kFastLossFloor))
+          flag_loss_only(a.flags + r, a.epoch);  // a loss this small: the fix-up sums it exactly
         const int64_t t = sm_tr_row;
-        rc = make_float4(Ct, Cd, __int_as_float(xs),
+        rc = make_float4(Ct, dC, __int_as_float(xs),
                          __int_as_float(t < (int64_t{1} << 31) ? static_cast<int32_t>(t) : -2));
       } else if (a.status && !any_abort) {
         atomicOr(a.status, SVW_DEV_BAD_INPUT);
@@ -781,8 +799,8 @@ __global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) 
     // d = ln2 d2:  dz = q (d2 gsT ln2 + gsT (lambda - KL)).
     if (valid && !any_abort && (a.dlogits != nullptr || row_ok)) {
       const float gsT = a.grad_scale * a.invT;
-      const float2 kk = make_float2(k, k), nkk = make_float2(-k, -k);
-      const float2 nCd = make_float2(-Cd, -Cd), Ct2 = make_float2(Ct, Ct);
+      const float2 kk = make_float2(k, k), neg1 = make_float2(-1.f, -1.f);
+      const float2 nCd = make_float2(-Cd, -Cd), ndC = make_float2(-dC, -dC);
       float tmax = 0.f;  // largest |t| / ln2 seen by this thread
       if (a.dlogits != nullptr) {
         const float nan = __int_as_float(0x7fffffff);
@@ -798,10 +816,10 @@ __global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) 
             float g[EPV];
 #pragma unroll
             for (int h = 0; h < Pairs<DT>::kN; ++h) {
-              const float2 A = __ffma2_rn(z.p[h], kk, nCd);                    // log2 q
+              const float2 A = __ffma2_rn(z.p[h], kk, nCd);                               // log2 q
               const float2 q = make_float2(ex2(A.x), ex2(A.y));
-              const float2 d = __fadd2_rn(A, __ffma2_rn(y.p[h], nkk, Ct2));  // log2 q - log2 p
-              const float2 t = __fmul2_rn(q, d);                               // t / ln 2
+              const float2 d = __ffma2_rn(__ffma2_rn(y.p[h], neg1, z.p[h]), kk, ndC);   // log2 q - log2 p
+              const float2 t = __fmul2_rn(q, d);                                          // t / ln 2
               tmax = fmaxf(tmax, fmaxf(fabsf(t.x), fabsf(t.y)));
               const float2 gg = __fmul2_rn(q, __ffma2_rn(d, gl, g02));
               g[2 * h] = gg.x;
@@ -830,14 +848,14 @@ __global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) 
             for (int h = 0; h < Pairs<DT>::kN; ++h) {
               const float2 A = __ffma2_rn(z.p[h], kk, nCd);
               const float2 q = make_float2(ex2(A.x), ex2(A.y));
-              const float2 t = __fmul2_rn(q, __fadd2_rn(A, __ffma2_rn(y.p[h], nkk, Ct2)));
+              const float2 t = __fmul2_rn(q, __ffma2_rn(__ffma2_rn(y.p[h], neg1, z.p[h]), kk, ndC));
               tmax = fmaxf(tmax, fmaxf(fabsf(t.x), fabsf(t.y)));
             }
           }
       }
       // some term reached the clip: the fix-up kernel redoes the row (every
       // writer stores the same call tag, so no ordering is needed)
-      if (row_ok && !(tmax < c2)) a.flags[r] = a.epoch;
+      if (row_ok && !(tmax < c2)) atomicExch(a.flags + r, a.epoch);
     }
   }
   // after a timeout no copy is issued; let the one that timed out land if it can
@@ -846,12 +864,13 @@ __global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) 
 }
 
 // Fix-up of the rows the fast kernel flagged (a term at the clip bound, or
-// masked draft entries), exactly, from the row constants it stored (Ct, Cd,
-// x*, target row).  Two flat grids over (flagged row, vocabulary chunk)
-// items, kOpdFixChunks chunks per row, so every SM streams a share of the
-// flagged rows at once whatever their number:
-//   opd_fix_sums: per chunk, the clamped sum of t/ln2 and S = sum q a
-//                 (fixed-order reduction) into the workspace;
+// masked draft entries; or, loss only, a loss below kFastLossFloor),
+// exactly, from the row constants it stored (Ct, dC, x*, target row).  Two
+// flat grids over (flagged row, vocabulary chunk) items, kOpdFixChunks chunks
+// per row, so every SM streams a share of the flagged rows at once whatever
+// their number:
+//   opd_fix_sums: per chunk, sum [clamp(t) - q + p] and S - 1 (nats,
+//                 fixed-order reduction) into the workspace;
 //   opd_fix_grad: per chunk, the row totals (a fixed butterfly over the
 //                 chunk partials, identical in every warp), the loss (chunk 0)
 //                 and the chunk's gradient (its logits read again; the
@@ -891,7 +910,11 @@ __device__ __forceinline__ int fix_scan(const OpdArgs &a, int64_t base, FixList 
 #pragma unroll
   for (int i = 0; i < kRounds; ++i) {
     const int64_t r = wb + i * 32 + lane;
-    bool f = r < a.R && __ldcg(a.flags + r) == a.epoch;
+    bool f = false;
+    if (r < a.R) {
+      const int32_t fv = __ldcg(a.flags + r);
+      f = (fv == a.epoch) || (fv == (a.epoch ^ kLossOnlyTag));
+    }
     if (f) {
       const float ct = __ldcg(&a.rowc[r].x);
       f = (ct == ct);
@@ -951,9 +974,11 @@ __global__ void __launch_bounds__(kFixNT, 4) opd_fix_sums(OpdArgs a, FixGeo fg) 
       const int64_t t = fix_target_row(a, r, rc);
       const int64_t lo = static_cast<int64_t>(c) * fg.CH;
       const int nv = static_cast<int>(min(static_cast<int64_t>(fg.CH), V - lo)) / EPV;
-      const float2 kk = make_float2(k, k), nkk = make_float2(-k, -k);
-      const float2 nCd = make_float2(-rc.y, -rc.y), Ct2 = make_float2(rc.x, rc.x), l2 = make_float2(kLn2, kLn2);
-      float2 r2 = make_float2(0.f, 0.f), s2 = make_float2(0.f, 0.f);
+      // sum_v [clamp(t_v) - q_v + p_v] and S over the chunk, in nats (see psi_nat)
+      const float Ct = rc.x, dC = rc.y, Cd = Ct + dC;
+      const float2 kk = make_float2(k, k), neg1 = make_float2(-1.f, -1.f);
+      const float2 nCd = make_float2(-Cd, -Cd), ndC = make_float2(-dC, -dC);
+      float rk1 = 0.f, S1 = 0.f;
       if (t >= 0) {
         const char *trow = static_cast<const char *>(a.target) + (t * V + lo) * E::kSize;
         const char *drow = static_cast<const char *>(a.draft) + (r * V + lo) * E::kSize;
@@ -973,20 +998,16 @@ __global__ void __launch_bounds__(kFixNT, 4) opd_fix_sums(OpdArgs a, FixGeo fg) 
               const Pairs<DT> y(ty[u]), z(tz[u]);
 #pragma unroll
               for (int h = 0; h < Pairs<DT>::kN; ++h) {
-                const float2 A = __ffma2_rn(z.p[h], kk, nCd);  // log2 q
+                const float2 A = __ffma2_rn(z.p[h], kk, nCd);                              // log2 q
                 const float2 q = make_float2(ex2(A.x), ex2(A.y));
-                const float2 tt = __fmul2_rn(q, __fadd2_rn(A, __ffma2_rn(y.p[h], nkk, Ct2)));  // t / ln2
-                if (fabsf(tt.x) < c2 && fabsf(tt.y) < c2) {
-                  r2 = __fadd2_rn(r2, tt);
-                  s2 = __fadd2_rn(__ffma2_rn(tt, l2, s2), q);
-                } else {
-                  term_slow(tt.x, q.x, c2, r2.x, s2.x);
-                  term_slow(tt.y, q.y, c2, r2.y, s2.y);
-                }
+                const float2 d = __ffma2_rn(__ffma2_rn(y.p[h], neg1, z.p[h]), kk, ndC);  // log2 q - log2 p
+                clamped_term(q.x, d.x, y.p[h].x, k, Ct, c2, a.clip_c, rk1, S1);
+                clamped_term(q.y, d.y, y.p[h].y, k, Ct, c2, a.clip_c, rk1, S1);
               }
             }
         }
       }
+      const float2 r2 = make_float2(rk1, 0.f), s2 = make_float2(S1, 0.f);
       const float rk = warp_sum(r2.x + r2.y), S = warp_sum(s2.x + s2.y);
       if (lane == 0) fl.red[warp] = make_float2(rk, S);
       __syncthreads();
@@ -1026,7 +1047,7 @@ __global__ void __launch_bounds__(kFixNT, 4) opd_fix_grad(OpdArgs a, FixGeo fg) 
       const float4 rc = __ldcg(a.rowc + r);
       const int64_t t = fix_target_row(a, r, rc);
       if (t < 0) continue;
-      const float Ct = rc.x, Cd = rc.y;
+      const float Ct = rc.x, dC = rc.y, Cd = Ct + dC;
       const int32_t xs = __float_as_int(rc.z);
       // row totals: a fixed butterfly over the chunk partials, the same in every warp
       float2 p = (lane < fg.nch) ? __ldcg(a.fixp + r * kOpdFixChunks + lane) : make_float2(0.f, 0.f);
@@ -1035,22 +1056,23 @@ __global__ void __launch_bounds__(kFixNT, 4) opd_fix_grad(OpdArgs a, FixGeo fg) 
         p.x += __shfl_xor_sync(0xffffffffu, p.x, o);
         p.y += __shfl_xor_sync(0xffffffffu, p.y, o);
       }
-      const float RKL2 = p.x, SS = p.y;
+      const float RKL = p.x, SS = p.y;
       if (c == 0 && tid == 0) {
         const float zx = E::load(a.draft, r * V + xs);
-        a.loss[r] = kLn2 * (RKL2 - a.lambda_ce * fmaf(zx, k, -Cd));
+        a.loss[r] = fmaf(a.lambda_ce * kLn2, Cd - zx * k, RKL);  // -lq[x*] = ln2 (Cd - z_x* k)
       }
-      if (a.dlogits == nullptr) continue;
-      // gradient: gsT (q a + q (lambda - S)) - gsT lambda [v = x*]
+      // rows flagged only for the size of their loss keep the fast kernel's gradient
+      if (a.dlogits == nullptr || __ldcg(a.flags + r) != a.epoch) continue;
+      // gradient: gsT (q a + q (lambda - S)) - gsT lambda [v = x*]  (SS holds S - 1)
       const int64_t lo = static_cast<int64_t>(c) * fg.CH;
       const int nv = static_cast<int>(min(static_cast<int64_t>(fg.CH), V - lo)) / EPV;
       const char *trow = static_cast<const char *>(a.target) + (t * V + lo) * E::kSize;
       const char *drow = static_cast<const char *>(a.draft) + (r * V + lo) * E::kSize;
       float *out = a.dlogits + r * V + lo;
-      const float gL0 = gsT * (a.lambda_ce - SS);
-      const float gL1 = gsT * (a.lambda_ce - SS + 1.f);
-      const float2 kk = make_float2(k, k), nkk = make_float2(-k, -k);
-      const float2 nCd = make_float2(-Cd, -Cd), Ct2 = make_float2(Ct, Ct);
+      const float gL0 = gsT * (a.lambda_ce - SS - 1.f);
+      const float gL1 = gsT * (a.lambda_ce - SS);
+      const float2 kk = make_float2(k, k), neg1 = make_float2(-1.f, -1.f);
+      const float2 nCd = make_float2(-Cd, -Cd), ndC = make_float2(-dC, -dC);
       const float2 gl = make_float2(gsT * kLn2, gsT * kLn2), g1 = make_float2(gL1, gL1);
       for (int v0 = tid; v0 < nv; v0 += kFixNT * kFixU) {
         uint4 ty[kFixU], tz[kFixU];
@@ -1072,7 +1094,7 @@ __global__ void __launch_bounds__(kFixNT, 4) opd_fix_grad(OpdArgs a, FixGeo fg) 
             for (int h = 0; h < Pairs<DT>::kN; ++h) {
               const float2 A = __ffma2_rn(z.p[h], kk, nCd);
               const float2 q = make_float2(ex2(A.x), ex2(A.y));
-              const float2 tt = __fmul2_rn(q, __fadd2_rn(A, __ffma2_rn(y.p[h], nkk, Ct2)));
+              const float2 tt = __fmul2_rn(q, __ffma2_rn(__ffma2_rn(y.p[h], neg1, z.p[h]), kk, ndC));
               float2 gg = __ffma2_rn(tt, gl, __fmul2_rn(q, g1));
               if (!(fabsf(tt.x) < c2)) gg.x = q.x * gL0;
               if (!(fabsf(tt.y) < c2)) gg.y = q.y * gL0;

@@ -79,11 +79,18 @@ struct Pairs {
 
 // Partial row statistics of the fast kernel over some vocabulary entries,
 // relative to offsets m_y, m_z (their maxima):
-//   s_y = sum 2^((y - m_y)k),  s_z = sum 2^((z - m_z)k),
-//   u   = sum 2^((z - m_z)k) ((z - m_z)k - (y - m_y)k),
+//   s_y = sum 2^((y - m_y)k),
+//   w   = sum (2^((z - m_z)k) - 2^((y - m_y)k))   (so s_z = s_y + w),
+//   u   = sum 2^((z - m_z)k) ((z - y)k - (m_z - m_y)k),
 // and the first index holding the target maximum with the draft logit there.
+// w is summed term by term rather than as the difference of two sums: where
+// the draft is close to the target, s_z / s_y - 1 = w / s_y is small, and a
+// difference of two rounded sums would carry the sums' rounding (~1e-7 of
+// s_y) into log(s_z / s_y) and from there into the KL.  Likewise the
+// log-ratio reference (z - y)k - (m_z - m_y)k is formed from the exact logit
+// difference, not from two row offsets of magnitude ~20.
 struct __align__(16) FastPart {
-  float my, sy, mz, sz, u;
+  float my, sy, mz, w, u;
   int32_t idx;
   float zx;
   int32_t abort;
@@ -94,7 +101,7 @@ __device__ __forceinline__ FastPart empty_part() {
   p.my = -INFINITY;
   p.mz = -INFINITY;
   p.sy = 0.f;
-  p.sz = 0.f;
+  p.w = 0.f;
   p.u = 0.f;
   p.idx = INT32_MAX;
   p.zx = 0.f;
@@ -106,8 +113,11 @@ __device__ __forceinline__ FastPart empty_part() {
 // lanes beyond the data hold empty partials).  Each lane rescales its own
 // partial to the merged offsets (one exp2 per sum, all lanes at once), then
 // the sums are added by a fixed butterfly, so every warp that merges the same
-// partials gets bit-identical results.  A NaN sum (a NaN or +Inf logit)
-// stays NaN; a non-finite u only makes the KL non-finite.
+// partials gets bit-identical results.  A lane's w moves to the merged
+// offsets as w fz + s_y fy (2^sh - 1), sh = ((m_z - m_y) - (M_z - M_y)) k the
+// change of log-ratio reference, with an accurate expm1 (no cancellation when
+// sh is small).  A NaN sum (a NaN or +Inf logit) stays NaN; a non-finite u
+// only makes the KL non-finite.
 template <int SPAN>
 __device__ __forceinline__ FastPart merge_lanes(const FastPart &p, float k) {
   float My = p.my, Mz = p.mz;
@@ -117,16 +127,23 @@ __device__ __forceinline__ FastPart merge_lanes(const FastPart &p, float k) {
     Mz = fmaxf(Mz, __shfl_xor_sync(0xffffffffu, Mz, o));
   }
   const bool hy = p.my != -INFINITY, hz = p.mz != -INFINITY;
-  const float dy = hy ? (p.my - My) * k : 0.f;
-  const float dz = hz ? (p.mz - Mz) * k : 0.f;
-  float sy = p.sy * (hy ? ex2(dy) : 0.f);
-  const float fz = hz ? ex2(dz) : 0.f;
-  float sz = p.sz * fz;
-  float u = hz ? fz * (p.u + p.sz * (dz - dy)) : (p.u != p.u ? p.u : 0.f);
+  const float fy = hy ? ex2((p.my - My) * k) : 0.f;
+  const float fz = hz ? ex2((p.mz - Mz) * k) : 0.f;
+  float sy = p.sy * fy;
+  // change of the log-ratio reference from (m_z - m_y) to (M_z - M_y)
+  const float sh = (hy && hz) ? ((p.mz - p.my) - (Mz - My)) * k : 0.f;
+  float u = hz ? fz * fmaf(p.sy + p.w, sh, p.u) : (p.u != p.u ? p.u : 0.f);
+  float w;
+  if (!hz)
+    w = -sy;  // no draft mass here: s_z = 0
+  else if (!hy)
+    w = p.w * fz;  // no target mass here: w = s_z
+  else
+    w = fmaf(p.w, fz, sy * expm1f(sh * kLn2));
 #pragma unroll
   for (int o = SPAN / 2; o > 0; o >>= 1) {
     sy += __shfl_xor_sync(0xffffffffu, sy, o);
-    sz += __shfl_xor_sync(0xffffffffu, sz, o);
+    w += __shfl_xor_sync(0xffffffffu, w, o);
     u += __shfl_xor_sync(0xffffffffu, u, o);
   }
   const int32_t cand = (p.my == My) ? p.idx : INT32_MAX;
@@ -137,12 +154,76 @@ __device__ __forceinline__ FastPart merge_lanes(const FastPart &p, float k) {
   r.my = My;
   r.mz = Mz;
   r.sy = sy;
-  r.sz = sz;
+  r.w = w;
   r.u = u;
   r.idx = best;
   r.zx = zx;
   r.abort = __any_sync(0xffffffffu, p.abort != 0) ? 1 : 0;
   return r;
+}
+
+// psi(d) = d - 1 + e^-d = sum_{n >= 2} (-d)^n / n!, d in nats.  With d the
+// log ratio log q - log p of one vocabulary entry, q psi(d) = t - q + p, so
+// sum_v q psi(d_v) = KL(q||p) - sum q + sum p: the same value as the KL when
+// both rows are normalised, but to first order insensitive to an error in
+// the row normalisers (a constant error e in d moves the sum by
+// e sum q (1 - e^-d) = e (sum q - sum p) = 0).  For |d| < 1/8 the series is
+// summed to d^7 (remainder below 2e-10 relative); beyond, d + expm1(-d) has
+// no cancellation worth the name.
+__device__ __forceinline__ float psi_nat(float d) {
+  if (fabsf(d) < 0.125f) {
+    float c = -1.f / 5040.f;
+    c = fmaf(c, d, 1.f / 720.f);
+    c = fmaf(c, d, -1.f / 120.f);
+    c = fmaf(c, d, 1.f / 24.f);
+    c = fmaf(c, d, -1.f / 6.f);
+    c = fmaf(c, d, 0.5f);
+    return d * d * c;
+  }
+  return d + expm1f(-d);
+}
+
+// One entry's share of the clamped reverse KL in the form
+//   sum_v [clamp(t_v, -c, c) - q_v + p_v]   (= sum_v clamp(t_v, -c, c), since
+//   both rows sum to one), and of S - 1 = sum_v q_v a_v - sum_v q_v, in nats:
+//   q d for an unclipped entry, -q for a clipped one.  Accumulating S - 1
+//   rather than S keeps the normaliser's rounding (sum q = 1 + eta) out of
+//   the gradient's q (a - S) term, whose scale is only that of log q - log p.
+//   q = 2^(log2 q), d2 = log2 q - log2 p, log2 p = y k - Ct;  t / ln2 = q d2,
+//   compared with c2 = c / ln2 as in the gradient passes.
+// An entry with q = 0 has t = 0 (it contributes p); an entry whose term
+// reaches the clip contributes +-c - q + p.
+// (lp2 = y k - Ct is formed only where it is needed.)
+__device__ __forceinline__ void clamped_term(float q, float d2, float y, float k, float Ct, float c2, float c,
+                                             float &rkl, float &Sm1) {
+  if (q == 0.f) {
+    rkl += ex2(fmaf(y, k, -Ct));
+    return;
+  }
+  const float t2 = q * d2;
+  if (fabsf(t2) < c2) {
+    const float d = d2 * kLn2;
+    rkl = fmaf(q, psi_nat(d), rkl);
+    Sm1 = fmaf(q, d, Sm1);
+  } else {
+    rkl += ((t2 > 0.f) ? c : -c) - q + ex2(fmaf(y, k, -Ct));
+    Sm1 -= q;
+  }
+}
+
+// Flag a row for the fix-up's loss-only recomputation (tag epoch ^
+// kLossOnlyTag) unless it is already flagged for the full recomputation
+// (tag epoch, stored by atomicExch from any CTA at any time): a
+// compare-and-swap that gives up as soon as it sees the full tag.  Bounded:
+// only a full-tag store can make it retry.
+constexpr int32_t kLossOnlyTag = 0x40000000;
+__device__ __forceinline__ void flag_loss_only(int32_t *f, int32_t epoch) {
+  int32_t old = atomicAdd(f, 0);
+  for (int it = 0; it < 4 && old != epoch; ++it) {
+    const int32_t prev = atomicCAS(f, old, epoch ^ kLossOnlyTag);
+    if (prev == old) return;
+    old = prev;
+  }
 }
 
 // Called by every thread after its reads of the slice buffer for the it-th

@@ -112,7 +112,7 @@ struct FusedArgs {
   const int32_t *tokens;
   float k;  // log2(e) / T of the verification (T > 0)
   uint64_t seed;
-  const float4 *rowc;  // [R] Ct, Cd, x*, target row (NaN: bad row)
+  const float4 *rowc;  // [R] Ct, dC = Cd - Ct, x*, target row (NaN: bad row)
   const float4 *bpart;  // [N * kBonusParts] bonus-row partials of the fast kernel's CTAs
   int32_t bparts;       // partials per bonus row (the fast kernel's cluster size)
   const int32_t *csr_bad;
@@ -182,9 +182,9 @@ struct OpdArgs {
   float *dlogits;
   int32_t *status;
   // workspace of the fast path (NULL: the exact kernel takes every row)
-  int32_t *flags;  // [R] == epoch: rows the fix-up kernel must redo
-  float4 *rowc;    // [R] row constants of the fast kernel: Ct, Cd, x*, target row (NaN: bad row)
-  float2 *fixp;    // [R][kOpdFixChunks] chunk partials of the fix-up (clamped sum / ln2, S)
+  int32_t *flags;  // [R] == epoch: rows the fix-up must redo; == epoch ^ 0x40000000: only their loss
+  float4 *rowc;    // [R] row constants of the fast kernel: Ct, dC = Cd - Ct, x*, target row (NaN: bad row)
+  float2 *fixp;    // [R][kOpdFixChunks] chunk partials of the fix-up (clamped sum, S - 1; nats)
   int32_t epoch;   // this call's tag (never 0)
   // fused verification (spec_verify_opd): after the R draft rows the fast
   // kernel also reduces the N bonus target rows, one partial per CTA of the

@@ -354,3 +354,17 @@ def config(cfg: int, *, N=None, V=None, lengths=None, seed=None) -> Batch:
                           temperatures=(0.0, 0.6, 1.0),
                           opd=dict(temperature=1.0, clip_c=1.0, lambda_ce=0.1))
     raise ValueError(f"unknown preset {cfg}")
+
+
+def length_head_inputs(N: int, k: int, H: int, Hp: int, seed: int):
+    """Synthetic inputs of the adaptive length head: drafter hidden states
+    h ~ N(0, 1) (bf16 bits, [N, k, H]) and random weights W1 ~ N(0, 4/H) (bf16
+    bits, [H', H]), b1 ~ N(0, 0.3^2), w2 ~ N(0, 4/H') (float32), b2 = 0.2,
+    gamma = 1.  There are no trained weights to load; these only give the
+    projection its shape and a spread of outputs."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 31])))
+    h = bf16_bits(rng.standard_normal((N, k, H), dtype=np.float32))
+    w1 = bf16_bits(rng.standard_normal((Hp, H), dtype=np.float32) * np.float32(2.0 / np.sqrt(H)))
+    b1 = (rng.standard_normal(Hp, dtype=np.float32) * np.float32(0.3)).astype(np.float32)
+    w2 = (rng.standard_normal(Hp, dtype=np.float32) * np.float32(2.0 / np.sqrt(Hp))).astype(np.float32)
+    return dict(hidden=h, w1=w1, b1=b1, w2=w2, b2=0.2, gamma=1.0)

@@ -246,3 +246,59 @@ def test_invalid_requests_are_flagged():
     assert r["flags"][2] & oracle.FLAG_BAD and r["accept_len"][2] == -1
     r = oracle.spec_verify(y, z, cu, tok, 1.0, seed=0, max_len=1)  # L = 2 > max_len
     assert np.all(r["flags"] & oracle.FLAG_BAD)
+
+
+def test_threaded_whole_batch_oracle_matches_one_call():
+    """The test helper that runs the oracle's requests on host threads (for
+    whole-batch GPU parity) returns exactly what one call over the batch does."""
+    from helpers import _groups, compare_opd_all, oracle_verify_all
+    b = synth.config(5, N=21, V=2048, seed=99)
+    for T in (1.0, 0.0):
+        one = oracle.spec_verify(b.target, b.draft, b.cu, b.tokens[float(T)], T, b.seed)
+        many = oracle_verify_all(b, T)
+        for k in ("accept_len", "next_token", "flags"):
+            assert np.array_equal(one[k], many[k]), k
+    ref = oracle.opd_loss(b.target, b.draft, cu_draft=b.cu, has_bonus=True)
+    assert compare_opd_all(b, ref["loss"].astype(np.float32), ref["dlogits"].astype(np.float32)) >= 0
+    assert sum(e - a for a, e in _groups(21, 64)) == 21
+
+
+def test_cdf_interval_distance_of_another_token():
+    """The oracle's alt_dist output (used to check every mismatch a GPU test
+    excuses as near a CDF boundary): for each candidate token, the distance
+    from w Z to that token's interval [C_{v-1}, C_v) of the distribution the
+    draw used, recomputed here in fp64 from the residual [p - q]_+ ([DF] §5.2
+    eq. (7)) or the bonus row."""
+    V, T = 7, 1.0
+    b = synth.make_batch("alt", seed=5, lengths=np.array([3, 2, 4], np.int32), V=V, dtype="f32",
+                         sigma_req=[1.5, 0.3, 2.0], temperatures=(T,))
+    base = oracle.spec_verify(b.target, b.draft, b.cu, b.tokens[T], T, b.seed)
+
+    def softmax(x):
+        e = np.exp(x.astype(np.float64) / T - (x.astype(np.float64) / T).max())
+        return e / e.sum()
+
+    for alt_tok in range(-1, V + 1):
+        alt = np.full(b.N, alt_tok, np.int32)
+        r = oracle.spec_verify(b.target, b.draft, b.cu, b.tokens[T], T, b.seed, alt_next=alt)
+        assert np.array_equal(r["next_token"], base["next_token"])
+        for n in range(b.N):
+            L, a = int(b.cu[n + 1] - b.cu[n]), int(base["accept_len"][n])
+            t0, d0 = int(b.cu[n]) + n, int(b.cu[n])
+            p = softmax(b.target[t0 + a])
+            w = oracle.uniform(b.seed, n, a, 1)
+            rr = np.maximum(0.0, p - softmax(b.draft[d0 + a])) if a < L else p
+            Z = rr.sum()
+            if not 0 <= alt_tok < V:
+                assert np.isinf(r["alt_dist"][n])
+                continue
+            lo, hi = rr[:alt_tok].sum(), rr[:alt_tok + 1].sum()
+            want = (lo - w * Z) / Z if w * Z < lo else ((w * Z - hi) / Z if w * Z >= hi else 0.0)
+            assert abs(r["alt_dist"][n] - want) < 1e-12, (n, alt_tok)
+            assert (r["alt_dist"][n] == 0.0) == (alt_tok == base["next_token"][n])
+    # greedy: 0 for the argmax, +inf for anything else
+    g = oracle.spec_verify(b.target, b.draft, b.cu, b.tokens[T], 0.0, b.seed)
+    r = oracle.spec_verify(b.target, b.draft, b.cu, b.tokens[T], 0.0, b.seed, alt_next=g["next_token"])
+    assert np.all(r["alt_dist"] == 0.0)
+    r = oracle.spec_verify(b.target, b.draft, b.cu, b.tokens[T], 0.0, b.seed, alt_next=(g["next_token"] + 1) % V)
+    assert np.all(np.isinf(r["alt_dist"]))
