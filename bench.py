@@ -108,7 +108,7 @@ CALL_KERNELS = {
     "spec_verify": "verify_stats + verify_finalize (accept tests and, at T > 0, the inverse-CDF draw)",
     "opd_loss": "opd_fast_kernel + opd_fix_sums + opd_fix_grad",
     "spec_verify_opd": "opd_fast_kernel (draft rows + bonus rows) + fused_finalize (accept tests, draw) + opd_fix_sums + opd_fix_grad",
-    "length_head": "length_head_label + length_head_gemm (cuBLASLt bf16 GEMM) + length_head_epilogue",
+    "length_head": "length_head_label + length_head_mma (tcgen05 projection, four K quarters) + length_head_reduce (quarters summed, bias, SiLU, mean, w2 dot, sigmoid, clamp)",
 }
 CALLS = ["verify_T0", "verify_T0.6", "verify_T1+opd", "length_head"]
 # top-k / top-p settings of the filtered-verification measurement: (T, top_k, top_p)
@@ -322,9 +322,9 @@ def bench_configs(svw, torch, dev, stream, rank, peak, K=30):
 def launches_per_step():
     """Kernels of this library one step launches: spec_verify = stats +
     finalize, twice; spec_verify_opd = fast pass + finalize + the fix-up's sums
-    and gradient grids; length head = label + epilogue (the GEMM's kernels
-    belong to cuBLASLt and are not counted)."""
-    return 2 + 2 + 4 + 2
+    and gradient grids; length head = label + the tcgen05 projection + the
+    per-request finish."""
+    return 2 + 2 + 4 + 3
 
 
 def run_native(args, ws, rank, local):
@@ -396,7 +396,7 @@ def run_native(args, ws, rank, local):
 
     # the main kernel of each call, timed inside the call (svw_time_next_launch)
     call_kernel = {"verify_T0": "verify_stats", "verify_T0.6": "verify_stats", "verify_T1+opd": "opd_fast_kernel",
-                   "length_head": "length_head_gemm"}
+                   "length_head": "length_head_mma"}
 
     def head():
         # this round's label (T = 1 accepted lengths against last round's a_hat), then the
@@ -667,7 +667,7 @@ def run_native(args, ws, rank, local):
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "algorithmic_bytes_per_launch": kalg[dom], "avg_launch_us": kern_us[dom]},
-        "length_head_gemm": {"tflops": head_flops / (kern_us["length_head"] * 1e-6) / 1e12,
+        "length_head_mma": {"tflops": head_flops / (kern_us["length_head"] * 1e-6) / 1e12,
                              "avg_us": kern_us["length_head"], "unit": "TFLOP/s",
                              "peak_bf16": _peak_tflops(), "frac": head_flops / (kern_us["length_head"] * 1e-6)
                              / 1e12 / _peak_tflops()},

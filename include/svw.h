@@ -316,11 +316,17 @@ svw_status spec_verify_opd(const void *target_logits, const void *draft_logits, 
  *   b1, w2     device float [hidden_out];  b2, gamma > 0 on the host.
  *   a_hat      device float [N] out (before the gamma scaling);  k_hat device int32 [N] out.
  *   workspace  device, 256-byte aligned, >= svw_length_head_workspace_size(N, k,
- *              hidden_out) bytes; holds the projection and the GEMM library's scratch.
- * The projection of the N k positions is one dense GEMM run by cuBLASLt on
- * the workspace (the library allocates no device memory; cuBLASLt keeps a
- * host handle and one plan per shape); bias, SiLU, mean, dot, sigmoid and
- * clamp are one kernel.  SVW_ERR_CUDA if cuBLASLt has no plan for the shape.
+ *              hidden_out) bytes: the projection's fp32 partial products (four
+ *              K quarters of N k positions, rounded up to 512, times H' rounded
+ *              up to 32, or to 256-wide tiles above 256); contents need not be
+ *              initialised.
+ * The projection of the N k positions runs on the tensor cores (tcgen05 MMA,
+ * operands staged by TMA, fp32 accumulation in tensor memory) in four K
+ * quarters; a second kernel, one CTA per request, sums the quarters and
+ * applies bias, SiLU, the mean over positions, the dot with w2, sigmoid,
+ * gamma, floor and clamp.  Two kernel launches, no library call; the host
+ * only encodes the two TMA descriptors.  If a bounded wait inside the
+ * projection gives up, the affected requests get a_hat = NaN.
  */
 size_t svw_length_head_workspace_size(int32_t n_requests, int32_t k, int32_t hidden_out);
 
@@ -379,7 +385,7 @@ svw_status spec_verify_noalloc(const void *target_logits, const void *draft_logi
  * kernel made from this thread ("early_plan", "verify_stats",
  * "verify_finalize", "verify_early_cluster", "filter_rows", "filtered_finalize",
  * "opd_fast_kernel", "opd_fix_sums", "opd_fix_grad", "opd_exact_kernel",
- * "fused_finalize", "length_head_gemm", "length_head_epilogue") records
+ * "fused_finalize", "length_head_mma", "length_head_reduce") records
  * begin_event just before it and end_event just after it on the launch stream (cudaEvent_t handles passed as void*, owned
  * by the caller).  kernel = NULL disarms.  The library records nothing
  * unless armed.  Lets a benchmark time one kernel of a multi-kernel call with

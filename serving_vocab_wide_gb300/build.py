@@ -40,7 +40,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
             return LIB_PATH
     tmp = LIB_PATH + f".tmp{os.getpid()}"
     cmd = [_nvcc(), ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
-           "--threads", "0", "-o", tmp] + [os.path.join(CSRC, s) for s in SOURCES] + ["-lcublasLt"]
+           "--threads", "0", "-o", tmp] + [os.path.join(CSRC, s) for s in SOURCES]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     subprocess.run(cmd, check=True, cwd=CSRC)

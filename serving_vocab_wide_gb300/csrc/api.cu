@@ -463,7 +463,7 @@ svw_status spec_verify_opd(const void *target_logits, const void *draft_logits, 
 
 size_t svw_length_head_workspace_size(int32_t n_requests, int32_t k, int32_t hidden_out) {
   if (n_requests <= 0 || k <= 0 || k > SVW_MAX_LEN || hidden_out <= 0) return 0;
-  return svw::length_head_gemm_bytes(n_requests, k, hidden_out) + svw::kLengthHeadGemmWorkspace;
+  return svw::length_head_gemm_bytes(n_requests, k, hidden_out);
 }
 
 svw_status length_head(const void *hidden, const void *w1, const float *b1, const float *w2, float b2, int32_t N,

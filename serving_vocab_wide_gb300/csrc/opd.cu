@@ -45,7 +45,7 @@
 // pitched) every row is done from shared memory in three passes:
 // log-sum-exps; clamped terms, S and the argmax; gradient -- two exchanges.
 // The exact kernel and the fix-up sum sum_v [clamp(t_v) - q_v + p_v] (= the
-// clamped sum, since both rows are normalised; see psi_nat): this form is to
+// clamped sum, since both rows are normalised; see psi_series): this form is to
 // first order insensitive to the rounding of the row constants, and it keeps
 // the small-KL regime precise without the fast kernel's W machinery.
 // In log2 units: log2 q = z k - Cd, log2 p = y k - Ct, d2 = (z - y) k - dC,
@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(512, 2) opd_exact_kernel(OpdArgs a, OpdGeo geo
 
     // ---------------- pass B: clamped terms, S, argmax ----------------
     // rkl = sum_v [clamp(t_v) - q_v + p_v] (nats), insensitive to first order
-    // to the rounding of Ct and dC (see psi_nat)
+    // to the rounding of Ct and dC (see psi_series)
     if (row_ok) {
       const float2 kk = make_float2(k, k), neg1 = make_float2(-1.f, -1.f);
       const float2 nCd = make_float2(-Cd, -Cd), ndC = make_float2(-dC, -dC);
@@ -974,7 +974,7 @@ __global__ void __launch_bounds__(kFixNT, 4) opd_fix_sums(OpdArgs a, FixGeo fg) 
       const int64_t t = fix_target_row(a, r, rc);
       const int64_t lo = static_cast<int64_t>(c) * fg.CH;
       const int nv = static_cast<int>(min(static_cast<int64_t>(fg.CH), V - lo)) / EPV;
-      // sum_v [clamp(t_v) - q_v + p_v] and S over the chunk, in nats (see psi_nat)
+      // sum_v [clamp(t_v) - q_v + p_v] and S over the chunk, in nats (see psi_series)
       const float Ct = rc.x, dC = rc.y, Cd = Ct + dC;
       const float2 kk = make_float2(k, k), neg1 = make_float2(-1.f, -1.f);
       const float2 nCd = make_float2(-Cd, -Cd), ndC = make_float2(-dC, -dC);

@@ -109,6 +109,22 @@ __device__ __forceinline__ FastPart empty_part() {
   return p;
 }
 
+// e^x - 1 without cancellation: the series to x^7 for |x| < 1/8 (remainder
+// below 2e-10 relative), the library's expm1f beyond.
+__device__ __forceinline__ float expm1_nat(float x) {
+  if (fabsf(x) < 0.125f) {
+    float c = 1.f / 5040.f;
+    c = fmaf(c, x, 1.f / 720.f);
+    c = fmaf(c, x, 1.f / 120.f);
+    c = fmaf(c, x, 1.f / 24.f);
+    c = fmaf(c, x, 1.f / 6.f);
+    c = fmaf(c, x, 0.5f);
+    c = fmaf(c, x, 1.f);
+    return x * c;
+  }
+  return expm1f(x);
+}
+
 // Merge the partials held by lanes [0, SPAN) of a warp (SPAN a power of two;
 // lanes beyond the data hold empty partials).  Each lane rescales its own
 // partial to the merged offsets (one exp2 per sum, all lanes at once), then
@@ -139,7 +155,7 @@ __device__ __forceinline__ FastPart merge_lanes(const FastPart &p, float k) {
   else if (!hy)
     w = p.w * fz;  // no target mass here: w = s_z
   else
-    w = fmaf(p.w, fz, sy * expm1f(sh * kLn2));
+    w = fmaf(p.w, fz, sy * expm1_nat(sh * kLn2));
 #pragma unroll
   for (int o = SPAN / 2; o > 0; o >>= 1) {
     sy += __shfl_xor_sync(0xffffffffu, sy, o);
@@ -167,20 +183,19 @@ __device__ __forceinline__ FastPart merge_lanes(const FastPart &p, float k) {
 // sum_v q psi(d_v) = KL(q||p) - sum q + sum p: the same value as the KL when
 // both rows are normalised, but to first order insensitive to an error in
 // the row normalisers (a constant error e in d moves the sum by
-// e sum q (1 - e^-d) = e (sum q - sum p) = 0).  For |d| < 1/8 the series is
-// summed to d^7 (remainder below 2e-10 relative); beyond, d + expm1(-d) has
-// no cancellation worth the name.
-__device__ __forceinline__ float psi_nat(float d) {
-  if (fabsf(d) < 0.125f) {
-    float c = -1.f / 5040.f;
-    c = fmaf(c, d, 1.f / 720.f);
-    c = fmaf(c, d, -1.f / 120.f);
-    c = fmaf(c, d, 1.f / 24.f);
-    c = fmaf(c, d, -1.f / 6.f);
-    c = fmaf(c, d, 0.5f);
-    return d * d * c;
-  }
-  return d + expm1f(-d);
+// e sum q (1 - e^-d) = e (sum q - sum p) = 0).  For |d| < 1/8 the series,
+// summed to d^7 (remainder below 2e-10 relative), gives q psi(d) without the
+// cancellation of t - q + p; beyond, t - q + p (q, p from the exp2 unit) is
+// within ~3e-5 of q psi(d) per entry, and such entries carry a KL of their
+// own well above that.
+__device__ __forceinline__ float psi_series(float d) {
+  float c = -1.f / 5040.f;
+  c = fmaf(c, d, 1.f / 720.f);
+  c = fmaf(c, d, -1.f / 120.f);
+  c = fmaf(c, d, 1.f / 24.f);
+  c = fmaf(c, d, -1.f / 6.f);
+  c = fmaf(c, d, 0.5f);
+  return d * d * c;
 }
 
 // One entry's share of the clamped reverse KL in the form
@@ -192,21 +207,23 @@ __device__ __forceinline__ float psi_nat(float d) {
 //   q = 2^(log2 q), d2 = log2 q - log2 p, log2 p = y k - Ct;  t / ln2 = q d2,
 //   compared with c2 = c / ln2 as in the gradient passes.
 // An entry with q = 0 has t = 0 (it contributes p); an entry whose term
-// reaches the clip contributes +-c - q + p.
-// (lp2 = y k - Ct is formed only where it is needed.)
+// reaches the clip contributes +-c - q + p.  Branch-free but for the clip.
 __device__ __forceinline__ void clamped_term(float q, float d2, float y, float k, float Ct, float c2, float c,
                                              float &rkl, float &Sm1) {
+  const float p = ex2(fmaf(y, k, -Ct));
   if (q == 0.f) {
-    rkl += ex2(fmaf(y, k, -Ct));
+    rkl += p;
     return;
   }
   const float t2 = q * d2;
+  const float d = d2 * kLn2;
   if (fabsf(t2) < c2) {
-    const float d = d2 * kLn2;
-    rkl = fmaf(q, psi_nat(d), rkl);
+    const float near = q * psi_series(d);
+    const float far = fmaf(q, d, p) - q;
+    rkl += (fabsf(d) < 0.125f) ? near : far;
     Sm1 = fmaf(q, d, Sm1);
   } else {
-    rkl += ((t2 > 0.f) ? c : -c) - q + ex2(fmaf(y, k, -Ct));
+    rkl += ((t2 > 0.f) ? c : -c) - q + p;
     Sm1 -= q;
   }
 }

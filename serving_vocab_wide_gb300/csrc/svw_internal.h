@@ -124,8 +124,7 @@ struct FusedArgs {
 cudaError_t launch_fused_finalize(const FusedArgs &a, int dtype, bool greedy, cudaStream_t stream);
 
 // adaptive length head (lengthhead.cu); 0 on success
-size_t length_head_gemm_bytes(int32_t N, int32_t k, int32_t Hp);
-constexpr size_t kLengthHeadGemmWorkspace = size_t{4} << 20;  // cuBLASLt scratch inside the workspace
+size_t length_head_gemm_bytes(int32_t N, int32_t k, int32_t Hp);  // per-position partial dots
 int launch_length_head(const void *hidden, const void *w1, const float *b1, const float *w2, float b2, int32_t N,
                        int32_t k, int32_t H, int32_t Hp, float gamma, float *a_hat, int32_t *k_hat,
                        void *workspace, size_t workspace_bytes, cudaStream_t stream);

@@ -261,11 +261,14 @@ def test_length_head_argument_validation(lib):
     assert call(k=40) == 2                  # above SVW_MAX_LEN
     assert call(h=None) == 1
     assert call(ws=None) == 4
-    assert call(wsb=1024) == 4
+    assert call(wsb=4096) == 4              # needs 4 x 512 x 32 x 4 bytes
     assert call(g=0.0) == 1
     assert call(H=60) == 2                  # rows must be 16-byte pitched
     assert call(h=ctypes.c_void_p(p.value + 8)) == 3
-    assert lib.svw_length_head_workspace_size(256, 16, 256) > (4 << 20)
+    # fp32 partial products: column tiles x 4 K quarters x positions (rounded up to 256) x tile width
+    assert lib.svw_length_head_workspace_size(256, 16, 256) == 4 * 4096 * 256 * 4
+    assert lib.svw_length_head_workspace_size(3, 5, 300) == 2 * 4 * 512 * 256 * 4
+    assert lib.svw_length_head_workspace_size(5, 16, 40) == 4 * 512 * 64 * 4
     assert lib.svw_length_head_workspace_size(0, 16, 256) == 0
 
 

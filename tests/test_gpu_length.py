@@ -57,22 +57,36 @@ def _compare(a, kh, ref, label):
 
 
 @pytest.mark.parametrize("N,k,H,Hp,b2,gamma", [(5, 16, 256, 32, 0.5, 1.0), (9, 7, 512, 64, -0.8, 1.3),
-                                               (3, 1, 64, 8, 2.0, 0.7), (33, 16, 1024, 128, 0.0, 1.0)])
+                                               (3, 1, 64, 8, 2.0, 0.7), (33, 16, 1024, 128, 0.0, 1.0),
+                                               # two 256-wide column tiles of W1, the second partial
+                                               (7, 5, 512, 300, 0.1, 1.0),
+                                               # K not a multiple of 64 (zero-filled tail); split ranks
+                                               # with and without K blocks
+                                               (4, 3, 200, 48, -0.3, 1.0), (6, 9, 136, 16, 0.4, 1.2),
+                                               # several 128-row tiles, the last one partial
+                                               (40, 13, 768, 200, 0.0, 0.9)])
 def test_small_shapes(N, k, H, Hp, b2, gamma):
     h, w1, b1, w2 = _inputs(N * 7 + H, N, k, H, Hp)
     a, kh = _gpu(h, w1, b1, w2, b2, gamma)
     _compare(a, kh, oracle.length_head(h, w1, b1, w2, b2, gamma), f"N={N} H={H}")
 
 
-def test_drafter_scale_sampled():
-    """N = 256 requests, k = 16, H = 4096 (drafter hidden size), H' = 256:
-    the whole batch on the GPU, 12 sampled requests through the oracle."""
+def test_drafter_scale_all_requests():
+    """N = 256 requests, k = 16, H = 4096 (drafter hidden size), H' = 256
+    (the benchmark's shape): every request against the oracle (its requests
+    split over host threads), and the same bits on a second call."""
+    from concurrent.futures import ThreadPoolExecutor
+    from helpers import host_threads
     N, k, H, Hp = 256, 16, 4096, 256
     h, w1, b1, w2 = _inputs(77, N, k, H, Hp)
     a, kh = _gpu(h, w1, b1, w2, 0.2, 1.0)
-    rows = np.sort(np.random.default_rng(5).choice(N, 12, replace=False))
-    ref = oracle.length_head(h[rows], w1, b1, w2, 0.2, 1.0)
-    _compare(a[rows], kh[rows], ref, "drafter scale")
+    a2, kh2 = _gpu(h, w1, b1, w2, 0.2, 1.0)
+    assert np.array_equal(a, a2) and np.array_equal(kh, kh2)
+    groups = np.array_split(np.arange(N), min(N, 2 * host_threads()))
+    with ThreadPoolExecutor(host_threads()) as pool:
+        refs = list(pool.map(lambda g: oracle.length_head(h[g], w1, b1, w2, 0.2, 1.0), groups))
+    ref = {key: np.concatenate([r[key] for r in refs]) for key in ("a_hat", "k_hat", "flags")}
+    _compare(a, kh, ref, "drafter scale")
     assert len(np.unique(kh)) > 3  # the lengths actually vary
 
 
