@@ -393,6 +393,27 @@ svw_status spec_verify_noalloc(const void *target_logits, const void *draft_logi
  */
 svw_status svw_time_next_launch(const char *kernel, void *begin_event, void *end_event);
 
+/*
+ * Test hooks for the bounded waits, not part of the method ("failure
+ * detection": a wait that runs out is reported, never a hang).
+ *
+ * svw_set_wait_limit -- the deadline, in SM clock cycles, of every bounded
+ * wait in the library's kernels on the current device (default 4e9, about
+ * 2 s).  cycles > 0, else SVW_ERR_INVALID_ARG.  Takes effect for kernels
+ * launched after it returns.  A limit far below a copy's latency makes
+ * healthy waits give up too; use it with svw_set_fault, at about 1e6 cycles,
+ * so that only the injected wait runs out.
+ *
+ * svw_set_fault -- 0: none (default); 1: in the next calls until reset, CTA 0
+ * of verify_stats (spec_verify) and cluster 0 of opd_fast_kernel
+ * (opd_loss, spec_verify_opd) issue no bulk copy, so their first wait
+ * runs out with nothing in flight: the call returns, its status word holds
+ * SVW_DEV_TIMEOUT, and the results of the affected rows are void.  Other
+ * values: SVW_ERR_INVALID_ARG.  Host-side state, shared by all threads.
+ */
+svw_status svw_set_wait_limit(int64_t cycles);
+svw_status svw_set_fault(int32_t kind);
+
 /* Human-readable name of a status code (static string). */
 const char *svw_status_string(svw_status s);
 

@@ -21,6 +21,8 @@ SVW_F32 = 0
 SVW_BF16 = 1
 SVW_DEV_BAD_INPUT = 1
 SVW_DEV_TIMEOUT = 2
+SVW_ERR_BAD_INPUT = 6
+SVW_ERR_TIMEOUT = 7
 SVW_MAX_LEN = 32
 
 _lib = None
@@ -82,6 +84,10 @@ def lib():
             L.length_head_label.restype = ctypes.c_int
             L.svw_time_next_launch.argtypes = [ctypes.c_char_p, P, P]
             L.svw_time_next_launch.restype = ctypes.c_int
+            L.svw_set_wait_limit.argtypes = [I64]
+            L.svw_set_wait_limit.restype = ctypes.c_int
+            L.svw_set_fault.argtypes = [I32]
+            L.svw_set_fault.restype = ctypes.c_int
             L.svw_status_string.argtypes = [ctypes.c_int]
             L.svw_status_string.restype = ctypes.c_char_p
             L.svw_version.argtypes = []
@@ -132,6 +138,21 @@ def time_next_launch(kernel: str | None, begin=None, end=None):
             ev.record()
     _check(lib().svw_time_next_launch(kernel.encode(), ctypes.c_void_p(begin.cuda_event),
                                       ctypes.c_void_p(end.cuda_event)))
+
+
+DEFAULT_WAIT_CYCLES = 4_000_000_000
+
+
+def set_wait_limit(cycles: int = DEFAULT_WAIT_CYCLES):
+    """Test hook: the deadline (SM cycles) of every bounded wait in the
+    library's kernels on the current device."""
+    _check(lib().svw_set_wait_limit(int(cycles)))
+
+
+def set_fault(kind: int = 0):
+    """Test hook: 1 = the next calls' stats / OPD fast kernels leave one CTA
+    (cluster) without its copies, so that its first wait runs out; 0 = none."""
+    _check(lib().svw_set_fault(int(kind)))
 
 
 def workspace_size(n_requests: int, total_draft_rows: int, V: int, max_len: int = SVW_MAX_LEN) -> int:

@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <cuda_runtime.h>
 
 #include "svw_internal.h"
@@ -45,6 +46,21 @@ void *timer_before(const char *kernel, cudaStream_t st) {
 void timer_after(void *end_event, cudaStream_t st) {
   if (end_event) cudaEventRecord(reinterpret_cast<cudaEvent_t>(end_event), st);
 }
+
+// test hooks: the wait deadline of every translation unit, and an injected fault
+namespace {
+constexpr int kMaxWaitSetters = 32;
+std::mutex g_wait_mu;
+cudaError_t (*g_wait_set[kMaxWaitSetters])(long long);
+int g_nwait = 0;
+std::atomic<int32_t> g_fault{0};
+}  // namespace
+cudaError_t register_wait_limit(cudaError_t (*set)(long long)) {
+  std::lock_guard<std::mutex> lk(g_wait_mu);
+  if (g_nwait < kMaxWaitSetters) g_wait_set[g_nwait++] = set;
+  return cudaSuccess;
+}
+int32_t test_fault() { return g_fault.load(std::memory_order_relaxed); }
 }  // namespace svw
 
 // a new tag for every OPD call (never 0): flags set by an earlier call never
@@ -59,6 +75,20 @@ static int32_t next_epoch() {
 extern "C" {
 
 int32_t svw_version(void) { return 100; }
+
+svw_status svw_set_wait_limit(int64_t cycles) {
+  if (cycles <= 0) return SVW_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(svw::g_wait_mu);
+  for (int q = 0; q < svw::g_nwait; ++q)
+    if (svw::g_wait_set[q](static_cast<long long>(cycles)) != cudaSuccess) return SVW_ERR_CUDA;
+  return SVW_OK;
+}
+
+svw_status svw_set_fault(int32_t kind) {
+  if (kind < 0 || kind > 1) return SVW_ERR_INVALID_ARG;
+  svw::g_fault.store(kind, std::memory_order_relaxed);
+  return SVW_OK;
+}
 
 const char *svw_status_string(svw_status s) {
   switch (s) {
@@ -124,6 +154,7 @@ static svw_status verify_entry(bool early, const void *target_logits, const void
   const bool vec = ((static_cast<int64_t>(V) * es) % 16 == 0) && aligned(target_logits, 16) &&
                    aligned(draft_logits, 16);
   svw::VerifyArgs a{};
+  a.fault = svw::test_fault();
   a.target = target_logits;
   a.draft = draft_logits;
   a.V = V;
@@ -316,6 +347,7 @@ svw_status opd_loss(const void *target_logits, const void *draft_logits, svw_dty
   const bool bulk = ((static_cast<int64_t>(V) * es) % 16 == 0) && aligned(target_logits, 16) &&
                     aligned(draft_logits, 16);
   svw::OpdArgs a;
+  a.fault = svw::test_fault();
   a.target = target_logits;
   a.draft = draft_logits;
   a.V = V;
@@ -410,6 +442,7 @@ svw_status spec_verify_opd(const void *target_logits, const void *draft_logits, 
   const bool greedy = (temperature == 0.f);
 
   svw::OpdArgs o;
+  o.fault = svw::test_fault();
   o.target = target_logits;
   o.draft = draft_logits;
   o.V = V;

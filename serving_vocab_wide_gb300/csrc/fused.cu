@@ -8,9 +8,9 @@
 // The Basic Idea" steps 3-4 ("AdaFlash: Taming Variance in Diffusion
 // Speculative Decoding") and "DFlash 阅读笔记" §5.1-§5.2 define on top of the
 // two softmaxes: the accept test at each drafted token, the leftmost
-// rejection and the next token.  One CTA per request: warp 0 (lane j tests
-// position j) decides, then at T > 0 the whole CTA draws the next token by
-// inverse CDF (svw_sample.cuh).
+// rejection and the next token.  One CTA per request (at T > 0 a cluster of
+// CTAs): warp 0 of CTA 0 (lane j tests position j) decides, then at T > 0 the
+// cluster draws the next token by inverse CDF (svw_sample.cuh).
 #include <cfloat>
 #include <climits>
 #include <cuda_runtime.h>
@@ -23,17 +23,26 @@ namespace svw {
 
 namespace {
 
-constexpr int kFThreads = 512;  // one CTA per request, two per SM
+constexpr int kFThreads = 512;  // one CTA (or, at T > 0, a cluster of CTAs) per request
 
 template <int DT, bool GREEDY>
 __global__ void __launch_bounds__(kFThreads) fused_finalize(FusedArgs a) {
   using E = Elem<DT>;
   __shared__ int32_t s_js;
   __shared__ float s_nT, s_nD;
+  __shared__ uint32_t s_draw[4];  // the draw's inputs from CTA 0 of the cluster: js, nT, nD, resid
   __shared__ SampleSmem<kFThreads> ssm;
+  extern __shared__ float sample_w[];  // T > 0: the draw's warp totals
+  // at T > 0 a cluster of CL CTAs serves request i: warp 0 of CTA 0 tests,
+  // then all of them draw the next token (one slice of the row each)
+  const int CL = GREEDY ? 1 : static_cast<int>(cluster_size());
+  const int rank = GREEDY ? 0 : static_cast<int>(cluster_rank());
   const int lane = threadIdx.x & 31;
-  const int32_t i = blockIdx.x;
-  if (threadIdx.x >= 32) {
+  const int32_t i = blockIdx.x / CL;
+  if (rank != 0) {
+    // the other CTAs of the cluster only draw (they read no output of the stream kernel)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  } else if (threadIdx.x >= 32) {
     // warps 1.. only take part in the draw
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (GREEDY) return;
@@ -134,37 +143,63 @@ __global__ void __launch_bounds__(kFThreads) fused_finalize(FusedArgs a) {
   }
   if (GREEDY) return;
   __syncthreads();
-  const int32_t js = s_js;
-  if (js < 0) return;
+  // the draw's inputs to every CTA of the cluster
+  if (rank == 0 && threadIdx.x < static_cast<unsigned>(CL)) {
+    const int32_t js = s_js;
+    const int32_t L = __ldg(a.cu + i + 1) - __ldg(a.cu + i);
+    const uint32_t v[4] = {static_cast<uint32_t>(js), __float_as_uint(s_nT), __float_as_uint(s_nD),
+                           (js >= 0 && js < L) ? 1u : 0u};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) st_cluster_b32(mapa_shared(smem_u32(&s_draw[q]), threadIdx.x), v[q]);
+  }
+  cluster_barrier();
+  const int32_t js = static_cast<int32_t>(s_draw[0]);
+  if (js < 0) return;  // the same in every CTA of the cluster
   // ---- the next token by inverse CDF: [p - q]_+ at row js, or p at the bonus row ----
   const int64_t c_i = __ldg(a.cu + i);
-  const int32_t L = __ldg(a.cu + i + 1) - static_cast<int32_t>(c_i);
   RowConst rc;
   rc.k = a.k;
-  rc.resid = js < L;
-  rc.nT = s_nT;
-  rc.nD = s_nD;
+  rc.resid = s_draw[3] != 0;
+  rc.nT = __uint_as_float(s_draw[1]);
+  rc.nD = __uint_as_float(s_draw[2]);
   const char *trow = static_cast<const char *>(a.target) + (c_i + i + js) * a.V * E::kSize;
   const char *drow = rc.resid ? static_cast<const char *>(a.draft) + (c_i + js) * a.V * E::kSize : nullptr;
   const float w = philox_uniform(a.seed, static_cast<uint32_t>(i), static_cast<uint32_t>(js), 1u);
-  const int32_t tok = cta_sample<DT, true, kFThreads>(trow, drow, a.V, rc, w, ssm);
-  if (threadIdx.x == 0) a.next_token[i] = tok;
+  const int32_t tok = cluster_sample<DT, true, kFThreads>(trow, drow, a.V, rc, w, ssm, sample_w, CL, rank);
+  if (threadIdx.x == 0 && tok >= 0) a.next_token[i] = tok;
 }
 
+// at T > 0 a cluster of CL CTAs per request (draw_cluster), each with the
+// draw's dynamic shared memory
 template <int DT>
 cudaError_t launch_t(const FusedArgs &a, bool greedy, cudaStream_t st) {
+  cudaError_t e = cudaSuccess;
+  int cl = 1;
+  size_t smem = 0;
+  if (!greedy) {
+    cl = draw_cluster(a.N);
+    smem = sample_dyn_bytes(a.V, cl, kFThreads);
+    e = cudaFuncSetAttribute(fused_finalize<DT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.gridDim = dim3(static_cast<unsigned>(a.N), 1, 1);
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(cl);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(a.N) * static_cast<unsigned>(cl), 1, 1);
   cfg.blockDim = dim3(kFThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = greedy ? 1 : 2;
   void *tm = timer_before("fused_finalize", st);
-  const cudaError_t e = greedy ? cudaLaunchKernelEx(&cfg, fused_finalize<DT, true>, a)
-                               : cudaLaunchKernelEx(&cfg, fused_finalize<DT, false>, a);
+  e = greedy ? cudaLaunchKernelEx(&cfg, fused_finalize<DT, true>, a)
+             : cudaLaunchKernelEx(&cfg, fused_finalize<DT, false>, a);
   timer_after(tm, st);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

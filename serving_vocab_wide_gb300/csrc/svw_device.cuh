@@ -133,10 +133,20 @@ __device__ __forceinline__ bool mbar_try_wait(unsigned long long *bar, uint32_t 
 }
 // bounded wait on an mbarrier phase: false if the clock deadline passed first
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
+// The deadline in force: each translation unit has its own copy, and every
+// copy registers its setter at load time (register_wait_limit, api.cu), so
+// that svw_set_wait_limit reaches all of them.  The registry is a weak
+// reference: a program built from this header alone keeps the default.
+static __constant__ long long c_wait_limit = kWaitCycles;
+__attribute__((weak)) cudaError_t register_wait_limit(cudaError_t (*set)(long long));
+static cudaError_t set_wait_limit_here(long long v) { return cudaMemcpyToSymbol(c_wait_limit, &v, sizeof(v)); }
+[[maybe_unused]] static const cudaError_t wait_limit_registered =
+    register_wait_limit ? register_wait_limit(&set_wait_limit_here) : cudaSuccess;
 __device__ __forceinline__ bool mbar_wait_bounded(unsigned long long *bar, uint32_t parity) {
   const long long t0 = clock64();
+  const long long limit = c_wait_limit;
   while (!mbar_try_wait(bar, parity))
-    if (clock64() - t0 > kWaitCycles) return false;
+    if (clock64() - t0 > limit) return false;
   return true;
 }
 // the accept test u < min(1, p(x)/q(x)) of speculative verification from the
@@ -164,6 +174,24 @@ __device__ __forceinline__ void named_sync(int id, int nt) { asm volatile("bar.s
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// 32-bit store into a peer's shared memory (ordered by the next cluster barrier)
+__device__ __forceinline__ void st_cluster_b32(uint32_t dst, uint32_t v) {
+  asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(dst), "r"(v) : "memory");
+}
+// every thread of every CTA of the cluster (release / acquire)
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
   return r;
 }
 // 16-byte store into a peer's shared memory that completes 16 bytes of the

@@ -72,6 +72,7 @@ struct VerifyArgs {
   int32_t *qnext;                  // cluster path: next record slot to hand out
   int4 *eres;                      // cluster path, per request: {stop position, bad, greedy argmax, 0}
   float4 *erow;                    // cluster path, per request: {m_T, l_T, m_D, l_D} at the stop position
+  int32_t fault;                   // test-only (svw_set_fault): 1 = the stats kernel's CTA 0 issues no copy
 };
 
 cudaError_t launch_verify(const VerifyArgs &a, int dtype, bool vec, bool greedy,
@@ -121,6 +122,8 @@ struct FusedArgs {
   int32_t *next_token;
   int32_t *status;
 };
+int draw_cluster(int N);
+int32_t test_fault();  // the fault set by svw_set_fault (0: none)  // CTAs per request of a finalize grid that draws (T > 0)
 cudaError_t launch_fused_finalize(const FusedArgs &a, int dtype, bool greedy, cudaStream_t stream);
 
 // adaptive length head (lengthhead.cu); 0 on success
@@ -192,6 +195,7 @@ struct OpdArgs {
   int32_t nbonus;
   float4 *bpart;
   int32_t *csr_bad;
+  int32_t fault;  // test-only (svw_set_fault): 1 = cluster 0 of the fast kernel issues no copy
 };
 
 cudaError_t launch_opd(const OpdArgs &a, int dtype, bool bulk, cudaStream_t stream);

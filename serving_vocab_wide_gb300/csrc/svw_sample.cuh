@@ -1,4 +1,5 @@
-// svw_sample.cuh -- inverse-CDF draw of the next token by one CTA.
+// svw_sample.cuh -- inverse-CDF draw of the next token by a thread-block
+// cluster.
 //
 // "DFlash 阅读笔记：并行起草、目标特征与精确验证" §5.2 eq. (7) and Algorithm 1
 // (and "AdaFlash: Taming Variance in Diffusion Speculative Decoding",
@@ -8,18 +9,15 @@
 // inverse CDF in vocabulary order: the smallest v with C_v > w Z, where C is
 // the prefix sum of the weights, Z their total and w the request's uniform.
 //
-// Prefix definition (fp32, reproducible, each level a fixed order of adds):
-//   group  8 consecutive entries           sequential partial sums, total a_g
-//   warp   32 consecutive groups           inclusive shuffle scan E_l, total W
-//   round  the NT / 32 warps of the CTA    sequential prefix Q_w, total R_r
-//   row    rounds                          sequential prefix P_r, total Z
-//   C_v = fl(P_r + fl(Q_w + fl(E_{l-1} + part_k)))
-// A round is one group per thread, so the row streams through the CTA with
-// coalesced 16-byte loads; only the crossing warp's 32 groups are read a
-// second time.  Rounding can leave the lane or entry level without a crossing
-// (or w Z can round up to Z): then the last entry with positive weight in the
-// group (or row) is taken -- such draws are within float rounding of a CDF
-// boundary.  A rejected row whose residual rounds to zero mass is drawn from p.
+// The row is cut into one slice per CTA of the cluster, so a request's row
+// pair streams through several SMs at once (and a batch of requests spreads
+// evenly over the GPU); each CTA keeps its slice's round and warp totals on
+// chip, the slice totals are exchanged, and only the crossing warp's 32
+// groups are read a second time.  Rounding can leave a
+// level without a crossing (or w Z can round up to Z): then the last entry
+// with positive weight of the slice (or row) is taken -- such draws are within
+// float rounding of a CDF boundary.  A rejected row whose residual rounds to
+// zero mass is drawn from p.
 #pragma once
 
 #include <cfloat>
@@ -68,7 +66,8 @@ __device__ __forceinline__ void sample_load_group(const char *row, int64_t g, in
   }
 }
 
-// the 8 weights of group g and their sequential sum a_g (0 beyond the row)
+// the 8 weights of group g and their sequential sum a_g (0 at g >= NG, the
+// end of the row or of the caller's slice)
 template <int DT, bool VEC>
 __device__ __forceinline__ float sample_group(const char *trow, const char *drow, int64_t g, int64_t NG,
                                               int64_t V, const RowConst &c, float (&w)[8]) {
@@ -100,30 +99,54 @@ __device__ __forceinline__ float warp_scan_incl(float x) {
   return x;
 }
 
-// shared memory of cta_sample
+// shared memory of cluster_sample
+constexpr int kMaxSampleCluster = 8;
+// The warp totals of a CTA's slice (round-major, NT / 32 per round) live in
+// dynamic shared memory: sample_dyn_bytes() per CTA.
 template <int NT>
 struct SampleSmem {
-  static constexpr int kW = NT / 32;
   static constexpr int kMaxRounds = ((1 << 20) / 8 + NT - 1) / NT;  // V <= 2^20
-  float W[kMaxRounds * kW];  // warp totals (round-major)
-  float R[kMaxRounds];       // round totals
-  int32_t lastg;             // last group with positive weight
-  int32_t rs, ws, result, degenerate;
+  float R[kMaxRounds];  // round totals of this CTA's slice
+  float Zs[kMaxSampleCluster];    // slice totals of the cluster, one per CTA (pushed by every peer)
+  int32_t lg[kMaxSampleCluster];  // last group with positive weight, per slice (-1: none)
+  int32_t lastg;                  // this CTA's
+  int32_t rs, ws, degenerate, spick;
   float t, Pr, Qw;
 };
 
-// The next token drawn from row trow (and drow when rc.resid) by the whole CTA
-// of NT threads; every thread returns it.  wu: the request's uniform in [0, 1).
+// dynamic shared memory of cluster_sample for rows of V entries cut into CL
+// slices: the warp totals of a slice
+__host__ __device__ inline size_t sample_dyn_bytes(int64_t V, int CL, int NT) {
+  const int64_t NG = (V + 7) / 8, P = (NG + CL - 1) / CL, nR = (P + NT - 1) / NT;
+  return static_cast<size_t>(nR) * (NT / 32) * sizeof(float);
+}
+
+// The next token drawn from row trow (and drow when rc.resid) by the CL CTAs
+// of a thread-block cluster, NT threads each; wu: the request's uniform in
+// [0, 1).  CTA `rank` streams groups [rank P, (rank + 1) P) of the row (P =
+// ceil(NG / CL)); the slice totals are exchanged through distributed shared
+// memory, the crossing slice is found by every CTA alike, and only the CTA
+// that owns it resolves the round, lane and entry levels.  Returns the token
+// in the CTA that drew it, -1 in the others (every thread of a CTA returns
+// the same).  Every CTA of the cluster must call it with the same arguments
+// (but its own rank); it ends with no peer access outstanding.
+//
+// Prefix definition (fp32, each level a fixed order of adds): groups of 8
+// entries (sequential), warps of 32 groups (shuffle scan), rounds of NT / 32
+// warps (sequential), the rounds of a slice (sequential), the CL slices
+// (sequential): C_v = fl(P_s + fl(P_r + fl(Q_w + fl(E_{l-1} + part_k)))).
 template <int DT, bool VEC, int NT>
-__device__ __noinline__ int32_t cta_sample(const char *trow, const char *drow, int64_t V, RowConst rc, float wu,
-                                           SampleSmem<NT> &sm) {
+__device__ __noinline__ int32_t cluster_sample(const char *trow, const char *drow, int64_t V, RowConst rc, float wu,
+                                               SampleSmem<NT> &sm, float *Wt, int CL, int rank) {
   constexpr int NW = NT / 32;
   constexpr int B = (DT == 1) ? 4 : 2;  // rounds whose loads are in flight together
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t NG = (V + 7) / 8;
-  const int nR = static_cast<int>((NG + NT - 1) / NT);
+  const int64_t P = (NG + CL - 1) / CL;
+  const int64_t gs = min(NG, static_cast<int64_t>(rank) * P), ge = min(NG, gs + P);
+  const int nR = static_cast<int>((ge - gs + NT - 1) / NT);
   for (int attempt = 0; attempt < 2; ++attempt) {
-    // ---- one pass: group sums, warp scans, warp totals ----
+    // ---- one pass over the slice: group sums, warp scans, warp totals ----
     if (tid == 0) sm.lastg = -1;
     int32_t lastg = -1;
     for (int r0 = 0; r0 < nR; r0 += B) {
@@ -134,14 +157,14 @@ __device__ __noinline__ int32_t cta_sample(const char *trow, const char *drow, i
         uint4 ry[B], rz[B];
 #pragma unroll
         for (int b = 0; b < B; ++b) {
-          const int64_t g = static_cast<int64_t>(r0 + b) * NT + tid;
-          const bool in = (r0 + b < nR) && g < NG;
+          const int64_t g = gs + static_cast<int64_t>(r0 + b) * NT + tid;
+          const bool in = (r0 + b < nR) && g < ge;
           ry[b] = in ? ld_vec(trow + g * 16) : make_uint4(ninf, ninf, ninf, ninf);
           rz[b] = (in && rc.resid) ? ld_vec(drow + g * 16) : make_uint4(ninf, ninf, ninf, ninf);
         }
 #pragma unroll
         for (int b = 0; b < B; ++b) {
-          const int64_t g = static_cast<int64_t>(r0 + b) * NT + tid;
+          const int64_t g = gs + static_cast<int64_t>(r0 + b) * NT + tid;
           float y[8], z[8];
           Elem<1>::unpack(ry[b], y);
           Elem<1>::unpack(rz[b], z);
@@ -155,15 +178,15 @@ __device__ __noinline__ int32_t cta_sample(const char *trow, const char *drow, i
 #pragma unroll
         for (int b = 0; b < B; ++b) {
           float w[8];
-          const int64_t g = static_cast<int64_t>(r0 + b) * NT + tid;
-          ag[b] = (r0 + b < nR) ? sample_group<DT, VEC>(trow, drow, g, NG, V, rc, w) : 0.f;
+          const int64_t g = gs + static_cast<int64_t>(r0 + b) * NT + tid;
+          ag[b] = (r0 + b < nR) ? sample_group<DT, VEC>(trow, drow, g, ge, V, rc, w) : 0.f;
           if (ag[b] > 0.f) lastg = static_cast<int32_t>(g);
         }
       }
 #pragma unroll
       for (int b = 0; b < B; ++b) {
         const float W = warp_scan_incl(ag[b]);
-        if (lane == 31 && r0 + b < nR) sm.W[(r0 + b) * NW + warp] = W;
+        if (lane == 31 && r0 + b < nR) Wt[(r0 + b) * NW + warp] = W;
       }
     }
 #pragma unroll
@@ -173,34 +196,67 @@ __device__ __noinline__ int32_t cta_sample(const char *trow, const char *drow, i
     // round totals (sequential over warps), one round per thread
     for (int r = tid; r < nR; r += NT) {
       float R = 0.f;
-      for (int w = 0; w < NW; ++w) R = __fadd_rn(R, sm.W[r * NW + w]);
+      for (int w = 0; w < NW; ++w) R = __fadd_rn(R, Wt[r * NW + w]);
       sm.R[r] = R;
     }
     __syncthreads();
+    // the slice total and last positive group, pushed to every CTA of the cluster
+    if (warp == 0) {
+      float Zs = 0.f;
+      if (lane == 0)
+        for (int r = 0; r < nR; ++r) Zs = __fadd_rn(Zs, sm.R[r]);
+      Zs = __shfl_sync(0xffffffffu, Zs, 0);
+      if (lane < CL) {
+        st_cluster_b32(mapa_shared(smem_u32(&sm.Zs[rank]), lane), __float_as_uint(Zs));
+        st_cluster_b32(mapa_shared(smem_u32(&sm.lg[rank]), lane), static_cast<uint32_t>(sm.lastg));
+      }
+    }
+    cluster_barrier();
     if (tid == 0) {
       float Z = 0.f;
-      for (int r = 0; r < nR; ++r) Z = __fadd_rn(Z, sm.R[r]);
+      for (int q = 0; q < CL; ++q) Z = __fadd_rn(Z, sm.Zs[q]);
       sm.degenerate = (rc.resid && !(Z > 0.f)) ? 1 : 0;
       const float t = __fmul_rn(wu, Z);
-      int rs = -1, ws = -1;
-      float Pr = 0.f, Qw = 0.f, P = 0.f;
-      for (int r = 0; r < nR && rs < 0; ++r) {
-        const float P2 = __fadd_rn(P, sm.R[r]);
+      // the crossing slice (the same in every CTA), then, in its owner, the round and warp
+      int ss = -1, rs = -1, ws = -1;
+      float Ps = 0.f, Pr = 0.f, Qw = 0.f, Pacc = 0.f;
+      for (int q = 0; q < CL && ss < 0; ++q) {
+        const float P2 = __fadd_rn(Pacc, sm.Zs[q]);
         if (P2 > t) {
-          rs = r;
-          Pr = P;
+          ss = q;
+          Ps = Pacc;
         }
-        P = P2;
+        Pacc = P2;
       }
-      if (rs >= 0) {
-        float Q = 0.f;
-        for (int w = 0; w < NW && ws < 0; ++w) {
-          const float Q2 = __fadd_rn(Q, sm.W[rs * NW + w]);
-          if (__fadd_rn(Pr, Q2) > t) {
-            ws = w;
-            Qw = Q;
+      int spick = -1;  // the CTA that returns the token
+      if (ss < 0) {
+        // no crossing after rounding (w Z rounded up to Z): the last entry of
+        // the row with positive weight, in the slice that holds it
+        for (int q = 0; q < CL; ++q)
+          if (sm.lg[q] >= 0) spick = q;
+      } else {
+        spick = ss;
+      }
+      if (ss == rank) {
+        float Pq = Ps;
+        for (int r = 0; r < nR && rs < 0; ++r) {
+          const float P2 = __fadd_rn(Pq, sm.R[r]);
+          if (P2 > t) {
+            rs = r;
+            Pr = Pq;
           }
-          Q = Q2;
+          Pq = P2;
+        }
+        if (rs >= 0) {
+          float Q = 0.f;
+          for (int w = 0; w < NW && ws < 0; ++w) {
+            const float Q2 = __fadd_rn(Q, Wt[rs * NW + w]);
+            if (__fadd_rn(Pr, Q2) > t) {
+              ws = w;
+              Qw = Q;
+            }
+            Q = Q2;
+          }
         }
       }
       sm.t = t;
@@ -208,25 +264,27 @@ __device__ __noinline__ int32_t cta_sample(const char *trow, const char *drow, i
       sm.ws = ws;
       sm.Pr = Pr;
       sm.Qw = Qw;
-      sm.result = -1;
+      sm.spick = spick;
     }
     __syncthreads();
     if (sm.degenerate) {
-      // no residual mass after rounding: draw from p at that row instead
+      // no residual mass after rounding: draw from p at that row instead;
+      // every peer has read this CTA's slice totals before they are rewritten
       rc.resid = false;
-      __syncthreads();
+      cluster_barrier();
       continue;
     }
+    if (sm.spick != rank) return -1;
+    int32_t pick = -1;
     if (warp == 0) {
       const int rs = sm.rs, ws = sm.ws;
-      int32_t pick = -1;
       const int64_t glast = sm.lastg;
       if (rs >= 0 && ws >= 0) {
         // lane and entry levels: lane l recomputes group l of the crossing warp
         const float t = sm.t, Pr = sm.Pr, Qw = sm.Qw;
-        const int64_t g = static_cast<int64_t>(rs) * NT + ws * 32 + lane;
+        const int64_t g = gs + static_cast<int64_t>(rs) * NT + ws * 32 + lane;
         float w[8];
-        const float ag = sample_group<DT, VEC>(trow, drow, g, NG, V, rc, w);
+        const float ag = sample_group<DT, VEC>(trow, drow, g, ge, V, rc, w);
         const float E = warp_scan_incl(ag);
         const float Ex = __shfl_up_sync(0xffffffffu, E, 1);
         const float Eprev = (lane == 0) ? 0.f : Ex;
@@ -248,17 +306,16 @@ __device__ __noinline__ int32_t cta_sample(const char *trow, const char *drow, i
         }
       }
       if (pick < 0 && glast >= 0 && lane == 0) {
-        // no crossing after rounding (w Z rounded up to Z, or between two
-        // levels): the last entry of the row with positive weight
+        // no crossing inside the slice after rounding: its last entry with positive weight
         float w[8];
-        sample_group<DT, VEC>(trow, drow, glast, NG, V, rc, w);
+        sample_group<DT, VEC>(trow, drow, glast, ge, V, rc, w);
         for (int e = 0; e < 8; ++e)
           if (w[e] > 0.f) pick = static_cast<int32_t>(glast * 8 + e);
       }
-      if (lane == 0) sm.result = pick;
+      if (lane == 0) sm.rs = pick;
     }
     __syncthreads();
-    return sm.result;
+    return sm.rs;
   }
   return -1;  // not reached: p always has mass
 }

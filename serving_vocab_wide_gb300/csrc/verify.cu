@@ -20,14 +20,15 @@
 //                       arithmetic, and write one Partial per warp.  No block
 //                       barrier in the steady state.  Each CTA also checks a
 //                       share of the CSR offsets.
-//  2. verify_finalize   one CTA per request (two per SM, so every request of
-//                       a large batch is in flight at once): validates the
-//                       request, merges the partials into row log-sum-exps
-//                       (or argmaxes), runs every accept test in one warp
-//                       (ballot + ffs = leftmost rejection), writes
-//                       accept_len, then (T > 0) the whole CTA draws the next
+//  2. verify_finalize   one CTA per request (at T > 0 a cluster of CTAs per
+//                       request, as many as fill the GPU once): CTA 0
+//                       validates the request, merges the partials into row
+//                       log-sum-exps (or argmaxes), runs every accept test in
+//                       one warp (ballot + ffs = leftmost rejection), writes
+//                       accept_len, then (T > 0) the cluster draws the next
 //                       token by inverse CDF over the residual row pair or the
-//                       bonus row (svw_sample.cuh), in one coalesced pass.
+//                       bonus row (svw_sample.cuh), one slice of the row
+//                       per CTA.
 // The finalize kernel is launched as a programmatic dependent of the stats
 // kernel: it is scheduled while the stream drains and reads the draft tokens
 // and their logits before waiting (griddepcontrol.wait) for the partials.
@@ -540,6 +541,9 @@ __global__ void __launch_bounds__(StatsShape<GREEDY, EARLY>::kThreads, 2)
       if (EARLY && a.bytes_read) atomicAdd(a.bytes_read, nbytes);
     };
     int k = 0;
+    // test-only fault (svw_set_fault): CTA 0 issues nothing, so its consumers'
+    // first wait runs out with no copy in flight
+    if (a.fault == 1 && blockIdx.x == 0) return;
     // early exit: the next item's two loads are in flight while this lane
     // waits for its stage
     EarlyPre pre;
@@ -640,166 +644,189 @@ __global__ void __launch_bounds__(kFinThreads) verify_finalize(VerifyArgs a) {
   __shared__ int32_t row_idx[kMaxRows];
   __shared__ int32_t row_bad[kMaxRows];
   __shared__ int32_t s_ok, s_js;
+  __shared__ uint32_t s_draw[4];  // the draw's inputs from CTA 0 of the cluster: js, nT, nD, resid
   __shared__ SampleSmem<kFinThreads> ssm;
-  const int32_t i = blockIdx.x;
+  extern __shared__ float sample_w[];  // T > 0: the draw's warp totals
+  // at T > 0 a cluster of CL CTAs serves request i: CTA 0 merges and tests,
+  // then all of them draw the next token (one slice of the row each)
+  const int CL = GREEDY ? 1 : static_cast<int>(cluster_size());
+  const int rank = GREEDY ? 0 : static_cast<int>(cluster_rank());
+  const int32_t i = blockIdx.x / CL;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   pdl_launch_dependents();
-
-  // ---- inputs only: this part overlaps the end of the stats kernel ----
-  const int64_t c_i = __ldg(a.cu + i), c_e = __ldg(a.cu + i + 1);
-  const bool len_ok = (c_e - c_i >= 1 && c_e - c_i <= a.max_len && c_i >= 0 && c_e <= a.total_rows);
-  const int32_t L = len_ok ? static_cast<int32_t>(c_e - c_i) : 0;
-  const int64_t t0 = c_i + i, d0 = c_i;
-  int32_t x = 0;
-  float yx = 0.f, zx = 0.f, u = 0.f;
-  if (warp == 0) {
-    bool tok_ok = true;
-    if (lane < L) {
-      x = __ldg(a.tokens + d0 + lane);
-      tok_ok = (x >= 0 && static_cast<int64_t>(x) < a.V);
-      if (tok_ok && !GREEDY && MODE == 0) {
-        yx = E::load(a.target, (t0 + lane) * a.V + x);
-        zx = E::load(a.draft, (d0 + lane) * a.V + x);
-        u = philox_uniform(a.seed, static_cast<uint32_t>(i), static_cast<uint32_t>(lane), 0u);
-      }
-    }
-    const bool ok = len_ok && __all_sync(0xffffffffu, tok_ok);
-    if (lane == 0) s_ok = ok ? 1 : 0;
-  }
-  pdl_wait();  // the stats kernel's partials and CSR flags are complete
-
-  int csr_bad = 0;
-  for (int b = tid; b < a.stats_grid; b += kFinThreads) csr_bad |= __ldcg(a.csr_bad + b);
-  csr_bad = __syncthreads_or(csr_bad);
-  auto reject = [&]() {  // one thread: a bad request
-    a.accept_len[i] = -1;
-    a.next_token[i] = -1;
-    if (a.status) atomicOr(a.status, SVW_DEV_BAD_INPUT);
-  };
-  if (!s_ok || csr_bad) {
-    if (tid == 0) reject();
-    return;
-  }
-  const int np = a.C * StatsShape<GREEDY>::kCW;  // partials per row
-  if (MODE == 2) {
+  if (rank == 0) {
+    // ---- inputs only: this part overlaps the end of the stats kernel ----
+    const int64_t c_i = __ldg(a.cu + i), c_e = __ldg(a.cu + i + 1);
+    const bool len_ok = (c_e - c_i >= 1 && c_e - c_i <= a.max_len && c_i >= 0 && c_e <= a.total_rows);
+    const int32_t L = len_ok ? static_cast<int32_t>(c_e - c_i) : 0;
+    const int64_t t0 = c_i + i, d0 = c_i;
+    int32_t x = 0;
+    float yx = 0.f, zx = 0.f, u = 0.f;
     if (warp == 0) {
-      const int4 r = __ldcg(a.eres + i);
-      const float4 f = __ldcg(a.erow + i);
-      const int32_t js = r.x;
-      if (lane == 0) {
-        if (r.y != 0 || js < 0 || js > L) {
-          reject();
-          s_js = -1;
-        } else {
-          a.accept_len[i] = js;
-          if (GREEDY) a.next_token[i] = r.z;
-          row_m[js] = f.x;
-          row_l[js] = f.y;
-          if (js < L) {
-            row_m[L + 1 + js] = f.z;
-            row_l[L + 1 + js] = f.w;
-          }
-          s_js = js;
+      bool tok_ok = true;
+      if (lane < L) {
+        x = __ldg(a.tokens + d0 + lane);
+        tok_ok = (x >= 0 && static_cast<int64_t>(x) < a.V);
+        if (tok_ok && !GREEDY && MODE == 0) {
+          yx = E::load(a.target, (t0 + lane) * a.V + x);
+          zx = E::load(a.draft, (d0 + lane) * a.V + x);
+          u = philox_uniform(a.seed, static_cast<uint32_t>(i), static_cast<uint32_t>(lane), 0u);
         }
       }
+      const bool ok = len_ok && __all_sync(0xffffffffu, tok_ok);
+      if (lane == 0) s_ok = ok ? 1 : 0;
     }
-  } else if (MODE == 1) {
-    // the stats stream ran the accept tests in position order and stopped
-    // reading a request at its first rejection (or bad row): only the rows
-    // at that position are merged here
-    if (warp == 0) {
-      const int32_t r = min(__ldcg(a.rej + i), L);
-      int32_t bad = (__ldcg(a.badpos + i) <= r) ? 1 : 0;
-      int32_t idx = INT32_MAX, b = 0;
-      if (GREEDY) {
-        merge_row_amax(a.part + (t0 + r) * np, np, lane, idx, b);
-        bad |= b;
-      } else {
-        float m, l;
-        merge_row_lse(a.part + (t0 + r) * np, np, a.k, lane, m, l, b);
-        bad |= b;
+    pdl_wait();  // the stats kernel's partials and CSR flags are complete
+
+    int csr_bad = 0;
+    for (int b = tid; b < a.stats_grid; b += kFinThreads) csr_bad |= __ldcg(a.csr_bad + b);
+    csr_bad = __syncthreads_or(csr_bad);
+    auto reject = [&]() {  // one thread: a bad request
+      a.accept_len[i] = -1;
+      a.next_token[i] = -1;
+      if (a.status) atomicOr(a.status, SVW_DEV_BAD_INPUT);
+    };
+    const int np = a.C * StatsShape<GREEDY>::kCW;  // partials per row
+    if (!s_ok || csr_bad) {
+      if (tid == 0) {
+        reject();
+        s_js = -1;
+      }
+    } else if (MODE == 2) {
+      if (warp == 0) {
+        const int4 r = __ldcg(a.eres + i);
+        const float4 f = __ldcg(a.erow + i);
+        const int32_t js = r.x;
         if (lane == 0) {
-          row_m[r] = m;
-          row_l[r] = l;
+          if (r.y != 0 || js < 0 || js > L) {
+            reject();
+            s_js = -1;
+          } else {
+            a.accept_len[i] = js;
+            if (GREEDY) a.next_token[i] = r.z;
+            row_m[js] = f.x;
+            row_l[js] = f.y;
+            if (js < L) {
+              row_m[L + 1 + js] = f.z;
+              row_l[L + 1 + js] = f.w;
+            }
+            s_js = js;
+          }
         }
-        if (r < L) {
-          merge_row_lse(a.part + (a.rows_t + d0 + r) * np, np, a.k, lane, m, l, b);
+      }
+    } else if (MODE == 1) {
+      // the stats stream ran the accept tests in position order and stopped
+      // reading a request at its first rejection (or bad row): only the rows
+      // at that position are merged here
+      if (warp == 0) {
+        const int32_t r = min(__ldcg(a.rej + i), L);
+        int32_t bad = (__ldcg(a.badpos + i) <= r) ? 1 : 0;
+        int32_t idx = INT32_MAX, b = 0;
+        if (GREEDY) {
+          merge_row_amax(a.part + (t0 + r) * np, np, lane, idx, b);
+          bad |= b;
+        } else {
+          float m, l;
+          merge_row_lse(a.part + (t0 + r) * np, np, a.k, lane, m, l, b);
           bad |= b;
           if (lane == 0) {
-            row_m[L + 1 + r] = m;
-            row_l[L + 1 + r] = l;
+            row_m[r] = m;
+            row_l[r] = l;
+          }
+          if (r < L) {
+            merge_row_lse(a.part + (a.rows_t + d0 + r) * np, np, a.k, lane, m, l, b);
+            bad |= b;
+            if (lane == 0) {
+              row_m[L + 1 + r] = m;
+              row_l[L + 1 + r] = l;
+            }
+          }
+        }
+        if (lane == 0) {
+          if (bad) {
+            reject();
+            s_js = -1;
+          } else {
+            a.accept_len[i] = r;
+            if (GREEDY) a.next_token[i] = idx;
+            s_js = r;
           }
         }
       }
-      if (lane == 0) {
-        if (bad) {
-          reject();
-          s_js = -1;
+    } else {
+      const int32_t nrows = GREEDY ? L + 1 : 2 * L + 1;
+      for (int r = warp; r < nrows; r += kFinWarps) {
+        const int64_t prow = (r <= L) ? (t0 + r) : (a.rows_t + d0 + (r - L - 1));
+        const Partial *pp = a.part + prow * np;
+        int32_t b;
+        if (GREEDY) {
+          int32_t idx;
+          merge_row_amax(pp, np, lane, idx, b);
+          if (lane == 0) row_idx[r] = idx;
         } else {
-          a.accept_len[i] = r;
-          if (GREEDY) a.next_token[i] = idx;
-          s_js = r;
+          float m, l;
+          merge_row_lse(pp, np, a.k, lane, m, l, b);
+          if (lane == 0) {
+            row_m[r] = m;
+            row_l[r] = l;
+          }
         }
+        if (lane == 0) row_bad[r] = b;
       }
-    }
-  } else {
-    const int32_t nrows = GREEDY ? L + 1 : 2 * L + 1;
-    for (int r = warp; r < nrows; r += kFinWarps) {
-      const int64_t prow = (r <= L) ? (t0 + r) : (a.rows_t + d0 + (r - L - 1));
-      const Partial *pp = a.part + prow * np;
-      int32_t b;
-      if (GREEDY) {
-        int32_t idx;
-        merge_row_amax(pp, np, lane, idx, b);
-        if (lane == 0) row_idx[r] = idx;
-      } else {
-        float m, l;
-        merge_row_lse(pp, np, a.k, lane, m, l, b);
+      __syncthreads();
+      if (warp == 0) {
+        int bad = 0;
+        for (int r = lane; r < nrows; r += 32) bad |= row_bad[r];
+        bad = __any_sync(0xffffffffu, bad);
+        bool acc = true;
+        if (lane < L)
+          acc = GREEDY ? (x == row_idx[lane])
+                       : accept_token(u, yx, zx, row_m[lane], row_l[lane], row_m[L + 1 + lane],
+                                      row_l[L + 1 + lane], a.k);
+        const unsigned rej = __ballot_sync(0xffffffffu, !acc);
+        const int32_t js = rej ? (__ffs(rej) - 1) : L;
         if (lane == 0) {
-          row_m[r] = m;
-          row_l[r] = l;
+          if (bad) {
+            reject();
+            s_js = -1;
+          } else {
+            a.accept_len[i] = js;
+            if (GREEDY) a.next_token[i] = row_idx[js];
+            s_js = js;
+          }
         }
       }
-      if (lane == 0) row_bad[r] = b;
     }
+    if (GREEDY) return;
     __syncthreads();
-    if (warp == 0) {
-      int bad = 0;
-      for (int r = lane; r < nrows; r += 32) bad |= row_bad[r];
-      bad = __any_sync(0xffffffffu, bad);
-      bool acc = true;
-      if (lane < L)
-        acc = GREEDY ? (x == row_idx[lane])
-                     : accept_token(u, yx, zx, row_m[lane], row_l[lane], row_m[L + 1 + lane], row_l[L + 1 + lane], a.k);
-      const unsigned rej = __ballot_sync(0xffffffffu, !acc);
-      const int32_t js = rej ? (__ffs(rej) - 1) : L;
-      if (lane == 0) {
-        if (bad) {
-          reject();
-          s_js = -1;
-        } else {
-          a.accept_len[i] = js;
-          if (GREEDY) a.next_token[i] = row_idx[js];
-          s_js = js;
-        }
-      }
+    // the draw's inputs to every CTA of the cluster
+    if (tid < CL) {
+      const int32_t js = s_js;
+      const bool resid = js >= 0 && js < L;
+      const float nT = (js >= 0) ? -__fmaf_rn(row_m[js], a.k, row_l[js]) : 0.f;
+      const float nD = resid ? -__fmaf_rn(row_m[L + 1 + js], a.k, row_l[L + 1 + js]) : 0.f;
+      const uint32_t v[4] = {static_cast<uint32_t>(js), __float_as_uint(nT), __float_as_uint(nD), resid ? 1u : 0u};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) st_cluster_b32(mapa_shared(smem_u32(&s_draw[q]), tid), v[q]);
     }
-  }
+  }  // CTA 0
   if (GREEDY) return;
-  __syncthreads();
-  const int32_t js = s_js;
-  if (js < 0) return;
+  cluster_barrier();
+  const int32_t js = static_cast<int32_t>(s_draw[0]);
+  if (js < 0) return;  // the same in every CTA of the cluster
   // ---- the next token: inverse CDF over [p - q]_+ at row js, or p at the bonus row ----
+  const int64_t c_i = __ldg(a.cu + i);
   RowConst rc;
   rc.k = a.k;
-  rc.resid = js < L;
-  rc.nT = -__fmaf_rn(row_m[js], a.k, row_l[js]);
-  rc.nD = rc.resid ? -__fmaf_rn(row_m[L + 1 + js], a.k, row_l[L + 1 + js]) : 0.f;
-  const char *trow = static_cast<const char *>(a.target) + (t0 + js) * a.V * E::kSize;
-  const char *drow = rc.resid ? static_cast<const char *>(a.draft) + (d0 + js) * a.V * E::kSize : nullptr;
+  rc.resid = s_draw[3] != 0;
+  rc.nT = __uint_as_float(s_draw[1]);
+  rc.nD = __uint_as_float(s_draw[2]);
+  const char *trow = static_cast<const char *>(a.target) + (c_i + i + js) * a.V * E::kSize;
+  const char *drow = rc.resid ? static_cast<const char *>(a.draft) + (c_i + js) * a.V * E::kSize : nullptr;
   const float w = philox_uniform(a.seed, static_cast<uint32_t>(i), static_cast<uint32_t>(js), 1u);
-  const int32_t tok = cta_sample<DT, VEC, kFinThreads>(trow, drow, a.V, rc, w, ssm);
-  if (tid == 0) a.next_token[i] = tok;
+  const int32_t tok =
+      cluster_sample<DT, VEC, kFinThreads>(trow, drow, a.V, rc, w, ssm, sample_w, CL, rank);
+  if (tid == 0 && tok >= 0) a.next_token[i] = tok;
 }
 
 // ---------------------------------------------------------------------------
@@ -852,6 +879,39 @@ cudaError_t launch_dependent(const char *name, Kern kern, unsigned grid, unsigne
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+// The finalize grid: one CTA per request, or at T > 0 a cluster of CL CTAs
+// per request that draws the next token together.
+template <bool GREEDY, bool VEC, typename Kern>
+cudaError_t launch_finalize(const char *name, Kern kern, int N, int threads, cudaStream_t st, const VerifyArgs &a) {
+  int cl = 1;
+  size_t smem = 0;  // the draw's warp totals
+  if (!GREEDY) {
+    cl = draw_cluster(N);
+    smem = sample_dyn_bytes(a.V, cl, threads);
+    const cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(cl);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(N) * static_cast<unsigned>(cl), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = GREEDY ? 1 : 2;
+  void *tm = timer_before(name, st);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
+  timer_after(tm, st);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 template <int DT, bool VEC, bool GREEDY, bool EARLY>
 cudaError_t launch_all_t(const VerifyArgs &args, cudaStream_t st) {
   using E = Elem<DT>;
@@ -868,8 +928,8 @@ cudaError_t launch_all_t(const VerifyArgs &args, cudaStream_t st) {
       if (e != cudaSuccess) return e;
       e = launch_early_cluster(a, DT == 1 ? SVW_BF16 : SVW_F32, GREEDY, cp, st);
       if (e != cudaSuccess) return e;
-      return launch_dependent("verify_finalize", verify_finalize<DT, GREEDY, VEC, 2>, static_cast<unsigned>(a.N),
-                              kFinThreads, 0, st, a);
+      return launch_finalize<GREEDY, VEC>("verify_finalize", verify_finalize<DT, GREEDY, VEC, 2>, a.N, kFinThreads, st,
+                                     a);
     }
   }
   const int stage_bytes = VEC ? (args.chunk_len * E::kSize + 127) / 128 * 128 : 0;
@@ -906,8 +966,8 @@ cudaError_t launch_all_t(const VerifyArgs &args, cudaStream_t st) {
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) return e;
-  return launch_dependent("verify_finalize", verify_finalize<DT, GREEDY, VEC, EARLY ? 1 : 0>,
-                          static_cast<unsigned>(a.N), kFinThreads, 0, st, a);
+  return launch_finalize<GREEDY, VEC>("verify_finalize", verify_finalize<DT, GREEDY, VEC, EARLY ? 1 : 0>, a.N,
+                                 kFinThreads, st, a);
 }
 
 template <int DT, bool VEC, bool EARLY>
@@ -916,6 +976,21 @@ cudaError_t launch_all(const VerifyArgs &a, bool greedy, cudaStream_t st) {
 }
 
 }  // namespace
+
+// CTAs per request of a finalize grid that draws at T > 0 (1, 2, 4 or 8): the
+// largest cluster with which the whole grid is resident at once, two CTAs
+// per SM.  Every CTA waits for its request's accept tests before it draws, so
+// a grid in several waves would pay that wait once per wave: a small batch
+// gets its rows split over the GPU, a large one keeps one CTA per request.
+int draw_cluster(int N) {
+  int dev = 0, nsm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    nsm = 1;
+  int cl = 1;
+  while (cl < kMaxSampleCluster && static_cast<int64_t>(N) * cl * 2 <= 2 * static_cast<int64_t>(nsm)) cl *= 2;
+  return cl;
+}
 
 
 ChunkPlan plan_chunks(int64_t V, int esize) {

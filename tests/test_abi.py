@@ -36,6 +36,28 @@ def test_header_symbols_exported(lib):
         assert hasattr(lib, n), f"{n} declared in svw.h but not exported"
 
 
+def test_no_unresolved_internal_symbols(lib):
+    """Every internal function the library calls is defined in it: the library
+    loads with immediate binding (as a loader that resolves everything at
+    load time requires), and no symbol of its own namespace is undefined."""
+    import serving_vocab_wide_gb300 as svw
+    ctypes.CDLL(svw.LIB_PATH, mode=os.RTLD_NOW | os.RTLD_LOCAL)
+    import shutil
+    import subprocess
+    if shutil.which("nm"):
+        out = subprocess.run(["nm", "-D", "--undefined-only", svw.LIB_PATH], capture_output=True, text=True).stdout
+        assert "_ZN3svw" not in out, [l for l in out.splitlines() if "_ZN3svw" in l]
+
+
+def test_test_hooks_validate(lib):
+    """The wait-limit and fault hooks reject bad values on the host."""
+    assert lib.svw_set_wait_limit(0) == 1      # SVW_ERR_INVALID_ARG
+    assert lib.svw_set_wait_limit(-5) == 1
+    assert lib.svw_set_fault(2) == 1
+    assert lib.svw_set_fault(-1) == 1
+    assert lib.svw_set_fault(0) == 0
+
+
 def test_version_and_status_strings(lib):
     assert lib.svw_version() == 100
     for code in range(8):
