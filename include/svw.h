@@ -249,13 +249,14 @@ svw_status spec_verify_filtered(const void *target_logits, const void *draft_log
  *                 a bounded wait on a bulk copy gave up).
  *   workspace     device, 256-byte aligned, >= svw_opd_workspace_size(
  *                 total_draft_rows) bytes (per row: a flag, the row
- *                 constants, 32 chunk partials of the exact fix-up; about
- *                 276 B), contents need not be initialised,
- *                 not preserved; or NULL.  With a workspace, rows whose byte
- *                 pitch is a multiple of 16 take a one-exchange fast pass and
- *                 only rows where some term reaches the clip (or the draft has
- *                 masked entries) are recomputed exactly; the results are the
- *                 same either way (up to float rounding order).
+ *                 constants, 128 partial clamped sums; about 1 KB), contents
+ *                 need not be initialised, not preserved; or NULL.  With a
+ *                 workspace, rows whose byte pitch is a multiple of 16 take
+ *                 a one-exchange fast pass, which also leaves each row's
+ *                 exact clamped sum as partials, and only the gradient of
+ *                 rows where some term reaches the clip (or the draft has
+ *                 masked entries) is written again; the results are the same
+ *                 either way (up to float rounding order).
  */
 size_t svw_opd_workspace_size(int64_t total_draft_rows);
 
@@ -384,7 +385,7 @@ svw_status spec_verify_noalloc(const void *target_logits, const void *draft_logi
  * one-shot timer on the calling host thread: the next launch of the named
  * kernel made from this thread ("early_plan", "verify_stats",
  * "verify_finalize", "verify_early_cluster", "filter_rows", "filtered_finalize",
- * "opd_fast_kernel", "opd_fix_sums", "opd_fix_grad", "opd_exact_kernel",
+ * "opd_fast_kernel", "opd_fix_parts", "opd_fix_grad", "opd_exact_kernel",
  * "fused_finalize", "length_head_mma", "length_head_reduce") records
  * begin_event just before it and end_event just after it on the launch stream (cudaEvent_t handles passed as void*, owned
  * by the caller).  kernel = NULL disarms.  The library records nothing

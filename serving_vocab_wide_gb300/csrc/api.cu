@@ -316,11 +316,11 @@ svw_status spec_verify_early(const void *target_logits, const void *draft_logits
 static size_t opd_flags_bytes(int64_t R) { return static_cast<size_t>((R * 4 + 255) / 256 * 256); }
 static size_t opd_rowc_bytes(int64_t R) { return static_cast<size_t>((R * 16 + 255) / 256 * 256); }
 
-// flags [R] int32 | row constants [R] float4 | fix-up chunk partials [R][kOpdFixChunks] float2
+// flags [R] int32 | row constants [R] float4 | clamped-sum partials [R][kOpdFixParts] float2
 size_t svw_opd_workspace_size(int64_t total_draft_rows) {
   if (total_draft_rows <= 0 || total_draft_rows > (int64_t{1} << 40)) return 0;
   return opd_flags_bytes(total_draft_rows) + opd_rowc_bytes(total_draft_rows) +
-         static_cast<size_t>(total_draft_rows) * svw::kOpdFixChunks * sizeof(float2);
+         static_cast<size_t>(total_draft_rows) * svw::kOpdFixParts * sizeof(float2);
 }
 
 svw_status opd_loss(const void *target_logits, const void *draft_logits, svw_dtype dtype,

@@ -38,9 +38,12 @@
 // recomputation: the flag word is set to the call's tag (never cleared), so
 // flags need no ordering and a stale tag at worst sends a row to the exact
 // fix-up once more.
-// Fix-up.  Rows the fast kernel flagged are redone exactly from the row
-// constants it stored, by two flat grids over (row, vocabulary chunk) items:
-// clamped terms and S per chunk, then the row totals and the gradient.
+// Fix-up.  After the exchange every warp of the fast kernel also leaves its
+// share of the exact clamped sum and of S, in closed form from its pass-1
+// sums where no term of the warp is clipped.
+// Warps that hold a clipped term leave their share to the fix-up: one grid
+// sums those warps' entries term by term, a second adds the partials up for
+// the rows the fast kernel flagged, writes the loss and rewrites the gradient.
 // Exact kernel.  Without a workspace (or for rows that are not 16-byte
 // pitched) every row is done from shared memory in three passes:
 // log-sum-exps; clamped terms, S and the argmax; gradient -- two exchanges.
@@ -777,15 +780,18 @@ __global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) 
     const float c2 = a.clip_c * kLog2e;           // clip bound for t / ln 2
     const int32_t xs = Rw.idx;
     const bool exact = (kl == kl) && fabsf(kl) <= FLT_MAX;
+    // loss = KL + lambda (-lq[x*]),  -lq[x*] = ln2 ((m_z - z_x*) k + log2 S_z)
+    // (every thread: the merged row is the same in every CTA of the cluster)
+    const float loss_r = fmaf(a.lambda_ce * kLn2, fmaf(Rw.mz - Rw.zx, k, lg2(Sz)), kl);
+    const bool small = !(fabsf(loss_r) >= kFastLossFloor);
     if (rank == 0 && tid == 0) {
       float out = __int_as_float(0x7fffffff);
       float4 rc = make_float4(__int_as_float(0x7fffffff), 0.f, 0.f, 0.f);  // NaN: not a row to fix
       if (row_ok && xs != INT32_MAX) {
-        // loss = KL + lambda (-lq[x*]),  -lq[x*] = ln2 ((m_z - z_x*) k + log2 S_z)
-        out = fmaf(a.lambda_ce * kLn2, fmaf(Rw.mz - Rw.zx, k, lg2(Sz)), kl);
+        out = loss_r;
         if (!exact)
           atomicExch(a.flags + r, a.epoch);  // masked entries: the fix-up redoes this row
-        else if (!(fabsf(out) >= kFastLossFloor))
+        else if (small)
           flag_loss_only(a.flags + r, a.epoch);  // a loss this small: the fix-up sums it exactly
         const int64_t t = sm_tr_row;
         rc = make_float4(Ct, dC, __int_as_float(xs),
@@ -859,6 +865,25 @@ __global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) 
       // some term reached the clip: the fix-up kernel redoes the row (every
       // writer stores the same call tag, so no ordering is needed)
       if (row_ok && !(tmax < c2)) atomicExch(a.flags + r, a.epoch);
+      // the fix-up's partial sums over this warp's entries, sum [clamp(t) - q + p]
+      // and S - 1 (nats), in closed form from the warp's pass-1 sums where no
+      // term of the warp is clipped: sum q d2 = 2^(m_z k - Cd) (u + ((m_z -
+      // m_y) k - dC) s_z).  NaN where the warp holds a term at the clip or the
+      // row needs its sums term by term (masked entries, a small loss): the
+      // fix-up sums those warps' entries exactly.
+      if (row_ok) {
+        float rk = 0.f, s1 = 0.f;
+        if (__any_sync(0xffffffffu, !(tmax < c2)) || !exact || small) {
+          rk = s1 = __int_as_float(0x7fffffff);
+        } else if (P.my != -INFINITY && P.mz != -INFINITY) {
+          const float Szw = P.sy + P.w;
+          const float fq = ex2(fmaf(P.mz, k, -Cd)), fp = ex2(fmaf(P.my, k, -Ct));
+          const float qd2 = fq * fmaf(fmaf(P.mz - P.my, k, -dC), Szw, P.u);
+          s1 = kLn2 * qd2;
+          rk = fmaf(fp, P.sy, fmaf(-fq, Szw, s1));
+        }
+        if (lane == 0) a.fixp[r * kOpdFixParts + rank * kWarps + warp] = make_float2(rk, s1);
+      }
     }
   }
   // after a timeout no copy is issued; let the one that timed out land if it can
@@ -868,33 +893,36 @@ __global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) 
 
 // Fix-up of the rows the fast kernel flagged (a term at the clip bound, or
 // masked draft entries; or, loss only, a loss below kFastLossFloor),
-// exactly, from the row constants it stored (Ct, dC, x*, target row).  Two
-// flat grids over (flagged row, vocabulary chunk) items, kOpdFixChunks chunks
-// per row, so every SM streams a share of the flagged rows at once whatever
-// their number:
-//   opd_fix_sums: per chunk, sum [clamp(t) - q + p] and S - 1 (nats,
-//                 fixed-order reduction) into the workspace;
-//   opd_fix_grad: per chunk, the row totals (a fixed butterfly over the
-//                 chunk partials, identical in every warp), the loss (chunk 0)
-//                 and the chunk's gradient (its logits read again; the
-//                 flagged rows of a call are a few tens of MB, so much of
-//                 the re-read can come from the 129 MB L2).
+// exactly, from the row constants it stored (Ct, dC, x*, target row) and the
+// per-warp partial sums sum [clamp(t) - q + p] and S - 1 (nats) it left in
+// the workspace (NaN for a warp that held a clipped term, or for every warp
+// of a row that needs its sums term by term):
+//   opd_fix_parts: one warp per row: for a flagged row, each NaN part's
+//                  entries summed term by term;
+//   opd_fix_grad:  one CTA per (flagged row, vocabulary chunk) item,
+//                  kOpdFixChunks chunks per row: the row totals (a fixed
+//                  order over the partials, identical in every warp), the
+//                  loss (chunk 0) and the chunk's gradient (its logits read
+//                  again).
 // Both walk the flags in batches of kFixBatch rows; a batch's flagged rows
 // are listed in row order by every CTA (a block scan), so the item order is
 // the same everywhere.  No waits on other CTAs: nothing can hang.
 constexpr int kFixBatch = 4096;  // flags scanned per batch
 constexpr int kFixNT = 256;
-constexpr int kFixU = 4;  // 16-byte vectors of each row in flight per thread
+constexpr int kFixU = 5;  // 16-byte vectors of each row in flight per thread (a chunk in one round)
 
 struct FixGeo {
   int32_t CH;   // entries per chunk (a multiple of 8)
   int32_t nch;  // chunks per row (<= kOpdFixChunks)
+  // the fast kernel's layout: its clusters left np = CL * fw partial sums
+  // per row, part q from warp q % fw of CTA q / fw, whose threads held
+  // vectors tid + j fnt (j < vpt) of vocabulary slice [SL (q / fw), SL (q / fw + 1))
+  int32_t np, fw, fnt, vpt, SL;
 };
 
 struct FixList {
   int32_t list[kFixBatch];  // flagged rows of the batch (offsets from its base), in order
   int32_t wcnt[kFixNT / 32];
-  float2 red[kFixNT / 32];
 };
 
 // The flagged rows of batch [base, base + kFixBatch) into fl.list, in row
@@ -952,75 +980,84 @@ __device__ __forceinline__ int64_t fix_target_row(const OpdArgs &a, int64_t r, c
   return (t32 >= 0) ? static_cast<int64_t>(t32) : target_row_of(a, r);
 }
 
+// Exact partial sums, term by term, of the warps the fast kernel left NaN (a
+// clipped term in the warp, or a row that needs its sums exactly): one warp
+// per draft row, no block barrier.  The warp reads the row's flag; for a
+// flagged row lane q checks parts q, q + 32, ... and the warp sums each NaN
+// part's entries (the entries that fast-kernel warp held).  Parts already in
+// closed form are left alone.
 template <int DT>
-__global__ void __launch_bounds__(kFixNT, 4) opd_fix_sums(OpdArgs a, FixGeo fg) {
+__global__ void __launch_bounds__(kFixNT, 3) opd_fix_parts(OpdArgs a, FixGeo fg) {
   using E = Elem<DT>;
   constexpr int EPV = E::kPerVec;
-  constexpr int kWarps = kFixNT / 32;
-  __shared__ FixList fl;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int kW = kFixNT / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t V = a.V;
   const float k = a.k, c2 = a.clip_c * kLog2e;
-  // The gradient grid may be scheduled now: it scans the flags, then waits
-  // for this grid.  This grid itself may start before the kernel launched
-  // ahead of it in the stream ends (the fused finalize kernel, which lets its
-  // dependents go only once the fast kernel's flags and row constants are
-  // complete): it reads only those, and waits for that kernel at its end.
+  // the gradient grid may be scheduled now: it scans the flags, then waits
+  // for this grid.  This grid may start before the kernel ahead of it ends
+  // (see opd_fix_grad): it reads only the fast kernel's output.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  for (int64_t base = 0; base < a.R; base += kFixBatch) {
-    const int m = fix_scan(a, base, fl);
-    const int64_t items = static_cast<int64_t>(m) * fg.nch;
-    for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
-      const int kq = static_cast<int>(item / fg.nch), c = static_cast<int>(item % fg.nch);
-      const int64_t r = base + fl.list[kq];
-      const float4 rc = __ldcg(a.rowc + r);
-      const int64_t t = fix_target_row(a, r, rc);
-      const int64_t lo = static_cast<int64_t>(c) * fg.CH;
-      const int nv = static_cast<int>(min(static_cast<int64_t>(fg.CH), V - lo)) / EPV;
-      // sum_v [clamp(t_v) - q_v + p_v] and S over the chunk, in nats (see psi_series)
-      const float Ct = rc.x, dC = rc.y, Cd = Ct + dC;
-      const float2 kk = make_float2(k, k), neg1 = make_float2(-1.f, -1.f);
-      const float2 nCd = make_float2(-Cd, -Cd), ndC = make_float2(-dC, -dC);
-      float rk1 = 0.f, S1 = 0.f;
-      if (t >= 0) {
+  for (int64_t r = static_cast<int64_t>(blockIdx.x) * kW + warp; r < a.R; r += static_cast<int64_t>(gridDim.x) * kW) {
+    const int32_t fv = __ldcg(a.flags + r);
+    if (fv != a.epoch && fv != (a.epoch ^ kLossOnlyTag)) continue;
+    const float4 rc = __ldcg(a.rowc + r);
+    if (!(rc.x == rc.x)) continue;  // a bad row: not fixed
+    const int64_t t = fix_target_row(a, r, rc);
+    if (t < 0) continue;
+    uint32_t todo = 0;  // bit u: part lane + 32 u is NaN
+#pragma unroll
+    for (int u = 0; u < kOpdFixParts / 32; ++u)
+      if (lane + 32 * u < fg.np) {
+        const float x = __ldcg(&a.fixp[r * kOpdFixParts + lane + 32 * u].x);
+        if (!(x == x)) todo |= 1u << u;
+      }
+    const float Ct = rc.x, dC = rc.y, Cd = Ct + dC;
+    const float2 kk = make_float2(k, k), neg1 = make_float2(-1.f, -1.f);
+    const float2 nCd = make_float2(-Cd, -Cd), ndC = make_float2(-dC, -dC);
+#pragma unroll 1
+    for (int u = 0; u < kOpdFixParts / 32; ++u) {
+      uint32_t ball = __ballot_sync(0xffffffffu, (todo >> u) & 1u);
+      while (ball) {
+        const int q = 32 * u + __ffs(ball) - 1;
+        ball &= ball - 1;
+        const int64_t lo = static_cast<int64_t>(q / fg.fw) * fg.SL;
+        const int nvec =
+            static_cast<int>(max(static_cast<int64_t>(0), min(static_cast<int64_t>(fg.SL), V - lo))) / EPV;
         const char *trow = static_cast<const char *>(a.target) + (t * V + lo) * E::kSize;
         const char *drow = static_cast<const char *>(a.draft) + (r * V + lo) * E::kSize;
-        for (int v0 = tid; v0 < nv; v0 += kFixNT * kFixU) {
+        const int v0 = (q % fg.fw) * 32 + lane;
+        float rk = 0.f, s1 = 0.f;
+        for (int j0 = 0; j0 < fg.vpt; j0 += kFixU) {
+          // kFixU vectors of each row in flight before any arithmetic
           uint4 ty[kFixU], tz[kFixU];
 #pragma unroll
-          for (int u = 0; u < kFixU; ++u) {
-            const int v = v0 + u * kFixNT;
-            if (v < nv) {
-              ty[u] = ld_vec(trow + static_cast<int64_t>(v) * 16);
-              tz[u] = ld_vec(drow + static_cast<int64_t>(v) * 16);
+          for (int w = 0; w < kFixU; ++w) {
+            const int v = v0 + (j0 + w) * fg.fnt;
+            if (j0 + w < fg.vpt && v < nvec) {
+              ty[w] = ld_vec(trow + static_cast<int64_t>(v) * 16);
+              tz[w] = ld_vec(drow + static_cast<int64_t>(v) * 16);
             }
           }
 #pragma unroll
-          for (int u = 0; u < kFixU; ++u)
-            if (v0 + u * kFixNT < nv) {
-              const Pairs<DT> y(ty[u]), z(tz[u]);
+          for (int w = 0; w < kFixU; ++w) {
+            const int v = v0 + (j0 + w) * fg.fnt;
+            if (!(j0 + w < fg.vpt && v < nvec)) continue;
+            const Pairs<DT> y(ty[w]), z(tz[w]);
 #pragma unroll
-              for (int h = 0; h < Pairs<DT>::kN; ++h) {
-                const float2 A = __ffma2_rn(z.p[h], kk, nCd);                              // log2 q
-                const float2 q = make_float2(ex2(A.x), ex2(A.y));
-                const float2 d = __ffma2_rn(__ffma2_rn(y.p[h], neg1, z.p[h]), kk, ndC);  // log2 q - log2 p
-                clamped_term(q.x, d.x, y.p[h].x, k, Ct, c2, a.clip_c, rk1, S1);
-                clamped_term(q.y, d.y, y.p[h].y, k, Ct, c2, a.clip_c, rk1, S1);
-              }
+            for (int h = 0; h < Pairs<DT>::kN; ++h) {
+              const float2 A = __ffma2_rn(z.p[h], kk, nCd);                              // log2 q
+              const float2 qq = make_float2(ex2(A.x), ex2(A.y));
+              const float2 d = __ffma2_rn(__ffma2_rn(y.p[h], neg1, z.p[h]), kk, ndC);  // log2 q - log2 p
+              clamped_term(qq.x, d.x, y.p[h].x, k, Ct, c2, a.clip_c, rk, s1);
+              clamped_term(qq.y, d.y, y.p[h].y, k, Ct, c2, a.clip_c, rk, s1);
             }
+          }
         }
+        rk = warp_sum(rk);
+        s1 = warp_sum(s1);
+        if (lane == 0) a.fixp[r * kOpdFixParts + q] = make_float2(rk, s1);
       }
-      const float2 r2 = make_float2(rk1, 0.f), s2 = make_float2(S1, 0.f);
-      const float rk = warp_sum(r2.x + r2.y), S = warp_sum(s2.x + s2.y);
-      if (lane == 0) fl.red[warp] = make_float2(rk, S);
-      __syncthreads();
-      if (tid == 0) {
-        float2 p = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) p = make_float2(p.x + fl.red[w].x, p.y + fl.red[w].y);
-        a.fixp[r * kOpdFixChunks + c] = p;
-      }
-      __syncthreads();  // fl.red is rewritten by the next item
     }
   }
   // complete only after the kernel ahead of it, so that the stream's order holds
@@ -1028,7 +1065,7 @@ __global__ void __launch_bounds__(kFixNT, 4) opd_fix_sums(OpdArgs a, FixGeo fg) 
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kFixNT, 4) opd_fix_grad(OpdArgs a, FixGeo fg) {
+__global__ void __launch_bounds__(kFixNT, 3) opd_fix_grad(OpdArgs a, FixGeo fg) {
   using E = Elem<DT>;
   constexpr int EPV = E::kPerVec;
   __shared__ FixList fl;
@@ -1036,11 +1073,13 @@ __global__ void __launch_bounds__(kFixNT, 4) opd_fix_grad(OpdArgs a, FixGeo fg) 
   const int64_t V = a.V;
   const float k = a.k, c2 = a.clip_c * kLog2e;
   const float gsT = a.grad_scale * a.invT;
+  // this grid may start while the parts grid ahead of it runs: it scans the
+  // flags (final since the fast kernel ended), then waits for that grid
   bool waited = false;
   for (int64_t base = 0; base < a.R; base += kFixBatch) {
-    const int m = fix_scan(a, base, fl);  // the flags predate the sums grid
+    const int m = fix_scan(a, base, fl);
     if (!waited) {
-      asm volatile("griddepcontrol.wait;" ::: "memory");  // the chunk partials are complete
+      asm volatile("griddepcontrol.wait;" ::: "memory");
       waited = true;
     }
     const int64_t items = static_cast<int64_t>(m) * fg.nch;
@@ -1052,8 +1091,16 @@ __global__ void __launch_bounds__(kFixNT, 4) opd_fix_grad(OpdArgs a, FixGeo fg) 
       if (t < 0) continue;
       const float Ct = rc.x, dC = rc.y, Cd = Ct + dC;
       const int32_t xs = __float_as_int(rc.z);
-      // row totals: a fixed butterfly over the chunk partials, the same in every warp
-      float2 p = (lane < fg.nch) ? __ldcg(a.fixp + r * kOpdFixChunks + lane) : make_float2(0.f, 0.f);
+      // row totals of the fast kernel's partial sums: a fixed order (lane q
+      // adds partials q, q + 32, ..., then a butterfly), the same in every warp
+      float2 p = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int q = 0; q < kOpdFixParts / 32; ++q)
+        if (lane + 32 * q < fg.np) {
+          const float2 v = __ldcg(a.fixp + r * kOpdFixParts + lane + 32 * q);
+          p.x += v.x;
+          p.y += v.y;
+        }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         p.x += __shfl_xor_sync(0xffffffffu, p.x, o);
@@ -1124,8 +1171,13 @@ __global__ void __launch_bounds__(kFixNT, 4) opd_fix_grad(OpdArgs a, FixGeo fg) 
 }
 
 // chunk geometry of the fix-up grids
-FixGeo fix_geo(int64_t V) {
+FixGeo fix_geo(int64_t V, int CL, int NT, int VPT, int SL) {
   FixGeo g;
+  g.fw = NT / 32;
+  g.np = CL * g.fw;
+  g.fnt = NT;
+  g.vpt = VPT;
+  g.SL = SL;
   int64_t CH = (V + kOpdFixChunks - 1) / kOpdFixChunks;
   CH = (CH + 7) / 8 * 8;
   g.CH = static_cast<int32_t>(CH);
@@ -1133,8 +1185,10 @@ FixGeo fix_geo(int64_t V) {
   return g;
 }
 
+// the fix-up grids after the fast kernel (CL CTAs of NT threads, VPT vectors
+// per thread, slices of SL entries)
 template <int DT>
-cudaError_t launch_fix(const OpdArgs &a, cudaStream_t st) {
+cudaError_t launch_fix(const OpdArgs &a, cudaStream_t st, int CL, int NT, int VPT, int SL) {
   static std::atomic<int> nsm_cache[64];  // zero-initialised (static storage)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1144,22 +1198,20 @@ cudaError_t launch_fix(const OpdArgs &a, cudaStream_t st) {
     if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) nsm_cache[dev].store(nsm, std::memory_order_relaxed);
   }
-  const FixGeo fg = fix_geo(a.V);
-  const unsigned grid = static_cast<unsigned>(4 * nsm);
-  // both grids are programmatic launches: the sums grid overlaps the kernel
-  // ahead of it (see opd_fix_sums), the gradient grid the sums grid's tail
+  const FixGeo fg = fix_geo(a.V, CL, NT, VPT, SL);
+  // programmatic launches: each overlaps the tail of the kernel ahead of it
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(3 * nsm), 1, 1);
   cfg.blockDim = dim3(kFixNT, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  void *tm = timer_before("opd_fix_sums", st);
-  e = cudaLaunchKernelEx(&cfg, opd_fix_sums<DT>, a, fg);
+  void *tm = timer_before("opd_fix_parts", st);
+  e = cudaLaunchKernelEx(&cfg, opd_fix_parts<DT>, a, fg);
   timer_after(tm, st);
   if (e != cudaSuccess) return e;
   tm = timer_before("opd_fix_grad", st);
@@ -1275,7 +1327,7 @@ cudaError_t launch_fast(const OpdArgs &a, const OpdPlan &p, cudaStream_t st, boo
     const cudaError_t e = launch_clusters("opd_fast_kernel", opd_fast_kernel<DT, VPT, NT>, NT, a, p, kTable, st, grid);
     if (e != cudaSuccess || !fix) return e;
   }
-  return launch_fix<DT>(a, st);
+  return launch_fix<DT>(a, st, p.CL, NT, VPT, p.SL);
 }
 
 // the fast-path variant for this row geometry; false if the row is too wide

@@ -164,7 +164,8 @@ int filter_group(int32_t top_k);
 size_t filter_smem_bytes(int64_t V, int esize, int32_t top_k);
 cudaError_t launch_filtered(const FilterArgs &a, int dtype, bool vec, cudaStream_t stream);
 
-constexpr int kOpdFixChunks = 32;  // vocabulary chunks per row of the OPD fix-up grids
+constexpr int kOpdFixChunks = 16;  // vocabulary chunks per row of the OPD fix-up grid
+constexpr int kOpdFixParts = 128;  // partial sums per row from the fast kernel (one per warp of the cluster)
 constexpr int kBonusParts = 8;  // bonus-row partial slots per request (the largest OPD cluster)
 
 struct OpdArgs {
@@ -186,7 +187,7 @@ struct OpdArgs {
   // workspace of the fast path (NULL: the exact kernel takes every row)
   int32_t *flags;  // [R] == epoch: rows the fix-up must redo; == epoch ^ 0x40000000: only their loss
   float4 *rowc;    // [R] row constants of the fast kernel: Ct, dC = Cd - Ct, x*, target row (NaN: bad row)
-  float2 *fixp;    // [R][kOpdFixChunks] chunk partials of the fix-up (clamped sum, S - 1; nats)
+  float2 *fixp;    // [R][kOpdFixParts] per-warp partials of the fast kernel (clamped sum, S - 1; nats)
   int32_t epoch;   // this call's tag (never 0)
   // fused verification (spec_verify_opd): after the R draft rows the fast
   // kernel also reduces the N bonus target rows, one partial per CTA of the

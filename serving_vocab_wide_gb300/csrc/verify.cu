@@ -1032,7 +1032,7 @@ FusedLayout fused_layout(int32_t N, int64_t total_rows, int64_t V) {
   l.bpart_off = off;
   off += align256(static_cast<size_t>(N) * kBonusParts * 16);
   l.fixp_off = off;
-  off += align256(R * kOpdFixChunks * sizeof(float2));
+  off += align256(R * kOpdFixParts * sizeof(float2));
   l.csr_bad_off = off;
   off += align256(kMaxStatsGrid * sizeof(int32_t));
   l.total = off;

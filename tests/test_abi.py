@@ -113,9 +113,9 @@ def test_workspace_size(lib):
     assert svw.verify_workspace_size(4, 10, 0, svw.SVW_BF16) == 0
     assert svw.verify_workspace_size(4, 10, 1 << 21, svw.SVW_BF16) == 0
     assert svw.opd_workspace_size(0) == 0
-    # flags and row constants (256-byte aligned), then 32 float2 chunk partials per row
-    assert svw.opd_workspace_size(1) == 512 + 256
-    assert svw.opd_workspace_size(1920) == 7680 + 30720 + 1920 * 256
+    # flags and row constants (256-byte aligned), then 128 float2 partial sums per row
+    assert svw.opd_workspace_size(1) == 512 + 1024
+    assert svw.opd_workspace_size(1920) == 7680 + 30720 + 1920 * 1024
 
 
 def _fake(n):
