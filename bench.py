@@ -54,6 +54,9 @@ def _args():
     p.add_argument("--workload", choices=["mix"], default="mix")
     p.add_argument("--e2e-steps", type=int, default=None)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--only", choices=["verify_T0", "verify_T0.6", "verify_T1+opd", "length_head"], default=None,
+                   help="run warmup + steps iterations of this one call of the step and exit (a small case for "
+                        "profilers: no timing, no end-to-end buffers)")
     return p.parse_args()
 
 
@@ -415,6 +418,16 @@ def run_native(args, ws, rank, local):
             fn()
             if ev is not None:
                 ev[2 * ci + 1].record(stream)
+
+    if args.only is not None:
+        fn = dict(zip(calls, (lambda: verify(0.0), lambda: verify(0.6), verify_opd, head)))[args.only]
+        for _ in range(args.warmup + args.steps):
+            fn()
+        torch.cuda.synchronize()
+        if rank == 0:
+            print(json.dumps({"only": args.only, "iterations": args.warmup + args.steps,
+                              "device_status": int(status.item())}))
+        return
 
     for _ in range(args.warmup):
         step()

@@ -312,7 +312,9 @@ svw_status spec_verify_opd(const void *target_logits, const void *draft_logits, 
  *   h'_p = SiLU(W1 h_i[p] + b1),  hbar = (1/k) sum_p h'_p,
  *   a_hat[i] = sigmoid(w2 . hbar + b2),
  *   k_hat[i] = clamp(floor(gamma a_hat[i] k), 1, k)   (next round's verified length).
- *   hidden     device bf16 [N, k, H] row-major, 16-byte aligned, H % 8 == 0.
+ *   hidden     device bf16 [N, k, H] row-major, 16-byte aligned, H % 8 == 0;
+ *              N k <= 2^20 positions and k <= SVW_MAX_LEN (else
+ *              SVW_ERR_UNSUPPORTED, and a workspace size of 0).
  *   w1         device bf16 [hidden_out, H] row-major (H' = hidden_out < H).
  *   b1, w2     device float [hidden_out];  b2, gamma > 0 on the host.
  *   a_hat      device float [N] out (before the gamma scaling);  k_hat device int32 [N] out.

@@ -18,6 +18,7 @@ bool opd_supported(int64_t V, int esize);
 namespace {
 
 constexpr int64_t kMaxV = 1 << 20;  // sampler span cap (256 threads x 512 groups x 8)
+constexpr int64_t kMaxHeadPositions = 1 << 20;  // length head: N k (32-bit offsets into its partials)
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -496,6 +497,7 @@ svw_status spec_verify_opd(const void *target_logits, const void *draft_logits, 
 
 size_t svw_length_head_workspace_size(int32_t n_requests, int32_t k, int32_t hidden_out) {
   if (n_requests <= 0 || k <= 0 || k > SVW_MAX_LEN || hidden_out <= 0) return 0;
+  if (static_cast<int64_t>(n_requests) * k > kMaxHeadPositions) return 0;
   return svw::length_head_gemm_bytes(n_requests, k, hidden_out);
 }
 
@@ -503,7 +505,7 @@ svw_status length_head(const void *hidden, const void *w1, const float *b1, cons
                        int32_t k, int32_t H, int32_t hidden_out, float gamma, float *a_hat, int32_t *k_hat,
                        void *workspace, size_t workspace_bytes, void *stream) {
   if (N <= 0 || k <= 0 || H <= 0 || hidden_out <= 0) return SVW_ERR_INVALID_ARG;
-  if (k > SVW_MAX_LEN) return SVW_ERR_UNSUPPORTED;
+  if (k > SVW_MAX_LEN || static_cast<int64_t>(N) * k > kMaxHeadPositions) return SVW_ERR_UNSUPPORTED;
   if (!hidden || !w1 || !b1 || !w2 || !a_hat || !k_hat) return SVW_ERR_INVALID_ARG;
   if (!workspace) return SVW_ERR_WORKSPACE;
   if (!(gamma > 0.f) || !std::isfinite(gamma) || !std::isfinite(b2)) return SVW_ERR_INVALID_ARG;

@@ -356,7 +356,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 // are averaged, dotted with w2 (a fixed-order block reduction), and b2,
 // sigmoid, gamma, floor and clamp give a_hat and k_hat.
 constexpr int kReduceThreads = 256;
-__global__ void __launch_bounds__(kReduceThreads) length_head_reduce(const float *part, const float *b1, const float *w2,
+__global__ void __launch_bounds__(kReduceThreads, 2) length_head_reduce(const float *part, const float *b1, const float *w2,
                                                                      float b2, int32_t k, int32_t Hp, int32_t Mpad,
                                                                      int32_t NT, float gamma, float *a_hat,
                                                                      int32_t *k_hat) {
@@ -370,13 +370,25 @@ __global__ void __launch_bounds__(kReduceThreads) length_head_reduce(const float
     const float bn = __ldg(b1 + n);
     const float *blk = part + static_cast<int64_t>(t) * kKSplit * Mpad * NT + c;
     float s = 0.f;
-    for (int p = 0; p < k; ++p) {
-      const int64_t m = static_cast<int64_t>(i) * k + p;
-      float y = 0.f;
+    for (int p0 = 0; p0 < k; p0 += 8) {
+      // the quarters of eight positions in flight before any arithmetic
+      float y[8];
 #pragma unroll
-      for (int q = 0; q < kKSplit; ++q) y += __ldcg(blk + (static_cast<int64_t>(q) * Mpad + m) * NT);
-      const float g = y + bn;
-      s += g / (1.f + expf(-g));  // SiLU
+      for (int u = 0; u < 8; ++u) {
+        // offsets within the partials (M_pad NT floats per quarter) fit 32 bits
+        const int m = i * k + p0 + u;
+        y[u] = 0.f;
+        if (p0 + u < k) {
+#pragma unroll
+          for (int q = 0; q < kKSplit; ++q) y[u] += __ldcg(blk + (q * Mpad + m) * NT);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (p0 + u < k) {
+          const float g = y[u] + bn;
+          s += g / (1.f + expf(-g));  // SiLU
+        }
     }
     acc = fmaf(__ldg(w2 + n), s / static_cast<float>(k), acc);
   }

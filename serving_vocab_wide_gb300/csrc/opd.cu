@@ -39,11 +39,12 @@
 // flags need no ordering and a stale tag at worst sends a row to the exact
 // fix-up once more.
 // Fix-up.  After the exchange every warp of the fast kernel also leaves its
-// share of the exact clamped sum and of S, in closed form from its pass-1
-// sums where no term of the warp is clipped.
-// Warps that hold a clipped term leave their share to the fix-up: one grid
-// sums those warps' entries term by term, a second adds the partials up for
-// the rows the fast kernel flagged, writes the loss and rewrites the gradient.
+// share of the exact clamped sum and of S: in closed form from its pass-1
+// sums, corrected at the few entries that reach the clip.  Rows that need
+// their sums term by term (masked entries, a small loss) leave that to the
+// fix-up: one grid sums those rows' entries, a second adds the partials up
+// for the rows the fast kernel flagged, writes the loss and rewrites the
+// gradient.
 // Exact kernel.  Without a workspace (or for rows that are not 16-byte
 // pitched) every row is done from shared memory in three passes:
 // log-sum-exps; clamped terms, S and the argmax; gradient -- two exchanges.
@@ -866,21 +867,51 @@ __global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) 
       // writer stores the same call tag, so no ordering is needed)
       if (row_ok && !(tmax < c2)) atomicExch(a.flags + r, a.epoch);
       // the fix-up's partial sums over this warp's entries, sum [clamp(t) - q + p]
-      // and S - 1 (nats), in closed form from the warp's pass-1 sums where no
-      // term of the warp is clipped: sum q d2 = 2^(m_z k - Cd) (u + ((m_z -
-      // m_y) k - dC) s_z).  NaN where the warp holds a term at the clip or the
-      // row needs its sums term by term (masked entries, a small loss): the
-      // fix-up sums those warps' entries exactly.
+      // and S - 1 (nats): in closed form from the warp's pass-1 sums as if no
+      // term were clipped, sum q d2 = 2^(m_z k - Cd) (u + ((m_z - m_y) k - dC)
+      // s_z), plus a correction at the entries that reach the clip.  NaN where
+      // the row needs its sums term by term (masked entries, a small loss):
+      // the fix-up sums those rows' entries exactly.
       if (row_ok) {
         float rk = 0.f, s1 = 0.f;
-        if (__any_sync(0xffffffffu, !(tmax < c2)) || !exact || small) {
+        if (!exact || small) {
           rk = s1 = __int_as_float(0x7fffffff);
-        } else if (P.my != -INFINITY && P.mz != -INFINITY) {
-          const float Szw = P.sy + P.w;
-          const float fq = ex2(fmaf(P.mz, k, -Cd)), fp = ex2(fmaf(P.my, k, -Ct));
-          const float qd2 = fq * fmaf(fmaf(P.mz - P.my, k, -dC), Szw, P.u);
-          s1 = kLn2 * qd2;
-          rk = fmaf(fp, P.sy, fmaf(-fq, Szw, s1));
+        } else {
+          if (P.my != -INFINITY && P.mz != -INFINITY) {
+            const float Szw = P.sy + P.w;
+            const float fq = ex2(fmaf(P.mz, k, -Cd)), fp = ex2(fmaf(P.my, k, -Ct));
+            const float qd2 = fq * fmaf(fmaf(P.mz - P.my, k, -dC), Szw, P.u);
+            s1 = kLn2 * qd2;
+            rk = fmaf(fp, P.sy, fmaf(-fq, Szw, s1));
+          }
+          if (__any_sync(0xffffffffu, !(tmax < c2))) {
+            // the warp holds a term at the clip: such an entry contributes
+            // +-c - t instead of nothing more to the clamped sum, and -q(1 + d)
+            // to S - 1 (t = q d, d = ln2 d2)
+            float cr = 0.f, cs = 0.f;
+#pragma unroll
+            for (int j = 0; j < VPT; ++j)
+              if (j < nj) {
+                const Pairs<DT> y(ty[j]), z(tz[j]);
+#pragma unroll
+                for (int h = 0; h < Pairs<DT>::kN; ++h) {
+                  const float2 A = __ffma2_rn(z.p[h], kk, nCd);
+                  const float2 q = make_float2(ex2(A.x), ex2(A.y));
+                  const float2 d = __ffma2_rn(__ffma2_rn(y.p[h], neg1, z.p[h]), kk, ndC);
+                  const float2 t = __fmul2_rn(q, d);
+                  if (!(fabsf(t.x) < c2)) {
+                    cr += fmaf(-kLn2, t.x, (t.x > 0.f) ? a.clip_c : -a.clip_c);
+                    cs -= fmaf(q.x * kLn2, d.x, q.x);
+                  }
+                  if (!(fabsf(t.y) < c2)) {
+                    cr += fmaf(-kLn2, t.y, (t.y > 0.f) ? a.clip_c : -a.clip_c);
+                    cs -= fmaf(q.y * kLn2, d.y, q.y);
+                  }
+                }
+              }
+            rk += warp_sum(cr);
+            s1 += warp_sum(cs);
+          }
         }
         if (lane == 0) a.fixp[r * kOpdFixParts + rank * kWarps + warp] = make_float2(rk, s1);
       }
@@ -895,11 +926,11 @@ __global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) 
 // masked draft entries; or, loss only, a loss below kFastLossFloor),
 // exactly, from the row constants it stored (Ct, dC, x*, target row) and the
 // per-warp partial sums sum [clamp(t) - q + p] and S - 1 (nats) it left in
-// the workspace (NaN for a warp that held a clipped term, or for every warp
-// of a row that needs its sums term by term):
+// the workspace (NaN for every warp of a row that needs its sums term by
+// term):
 //   opd_fix_parts: one warp per row: for a flagged row, each NaN part's
 //                  entries summed term by term;
-//   opd_fix_grad:  one CTA per (flagged row, vocabulary chunk) item,
+//   opd_fix_grad:  one warp per (flagged row, vocabulary chunk) item,
 //                  kOpdFixChunks chunks per row: the row totals (a fixed
 //                  order over the partials, identical in every warp), the
 //                  loss (chunk 0) and the chunk's gradient (its logits read
@@ -908,8 +939,9 @@ __global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) 
 // are listed in row order by every CTA (a block scan), so the item order is
 // the same everywhere.  No waits on other CTAs: nothing can hang.
 constexpr int kFixBatch = 4096;  // flags scanned per batch
+constexpr int32_t kFixFullBit = 1 << 30;  // in a FixList entry: the row's gradient is rewritten
 constexpr int kFixNT = 256;
-constexpr int kFixU = 5;  // 16-byte vectors of each row in flight per thread (a chunk in one round)
+constexpr int kFixU = 5;  // 16-byte vectors of each row in flight per thread
 
 struct FixGeo {
   int32_t CH;   // entries per chunk (a multiple of 8)
@@ -926,7 +958,8 @@ struct FixList {
 };
 
 // The flagged rows of batch [base, base + kFixBatch) into fl.list, in row
-// order; returns their number (in every thread).  Warp w reads rows
+// order (kFixFullBit set for a row flagged for the full recomputation, clear
+// for a loss-only one); returns their number (in every thread).  Warp w reads rows
 // [w 512, (w + 1) 512) of the batch 32 at a time (coalesced) and keeps one
 // ballot per 32.  A flag is this call's tag; a stale tag on a row the fast
 // kernel found bad (NaN row constants) is not.
@@ -936,21 +969,23 @@ __device__ __forceinline__ int fix_scan(const OpdArgs &a, int64_t base, FixList 
   constexpr int kRounds = kPerWarp / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t wb = base + static_cast<int64_t>(warp) * kPerWarp;
-  uint32_t ball[kRounds];
+  uint32_t ball[kRounds], full[kRounds];
   int cnt = 0;
 #pragma unroll
   for (int i = 0; i < kRounds; ++i) {
     const int64_t r = wb + i * 32 + lane;
-    bool f = false;
+    bool f = false, g = false;
     if (r < a.R) {
       const int32_t fv = __ldcg(a.flags + r);
-      f = (fv == a.epoch) || (fv == (a.epoch ^ kLossOnlyTag));
+      g = (fv == a.epoch);
+      f = g || (fv == (a.epoch ^ kLossOnlyTag));
     }
     if (f) {
       const float ct = __ldcg(&a.rowc[r].x);
       f = (ct == ct);
     }
     ball[i] = __ballot_sync(0xffffffffu, f);
+    full[i] = __ballot_sync(0xffffffffu, f && g);
     cnt += __popc(ball[i]);
   }
   if (lane == 0) fl.wcnt[warp] = cnt;
@@ -966,7 +1001,9 @@ __device__ __forceinline__ int fix_scan(const OpdArgs &a, int64_t base, FixList 
   int g = before;
 #pragma unroll
   for (int i = 0; i < kRounds; ++i) {
-    if (ball[i] & (1u << lane)) fl.list[g + __popc(ball[i] & below)] = warp * kPerWarp + i * 32 + lane;
+    if (ball[i] & (1u << lane))
+      fl.list[g + __popc(ball[i] & below)] =
+          (warp * kPerWarp + i * 32 + lane) | ((full[i] & (1u << lane)) ? kFixFullBit : 0);
     g += __popc(ball[i]);
   }
   __syncthreads();  // the list is complete; every thread has read fl.wcnt
@@ -981,8 +1018,8 @@ __device__ __forceinline__ int64_t fix_target_row(const OpdArgs &a, int64_t r, c
 }
 
 // Exact partial sums, term by term, of the warps the fast kernel left NaN (a
-// clipped term in the warp, or a row that needs its sums exactly): one warp
-// per draft row, no block barrier.  The warp reads the row's flag; for a
+// row that needs its sums term by term): one warp per draft row, no block
+// barrier.  The warp reads the row's flag; for a
 // flagged row lane q checks parts q, q + 32, ... and the warp sums each NaN
 // part's entries (the entries that fast-kernel warp held).  Parts already in
 // closed form are left alone.
@@ -1082,37 +1119,44 @@ __global__ void __launch_bounds__(kFixNT, 3) opd_fix_grad(OpdArgs a, FixGeo fg) 
       asm volatile("griddepcontrol.wait;" ::: "memory");
       waited = true;
     }
+    // one warp per (flagged row, chunk) item
     const int64_t items = static_cast<int64_t>(m) * fg.nch;
-    for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
+    for (int64_t item = static_cast<int64_t>(blockIdx.x) * (kFixNT / 32) + (tid >> 5); item < items;
+         item += static_cast<int64_t>(gridDim.x) * (kFixNT / 32)) {
       const int kq = static_cast<int>(item / fg.nch), c = static_cast<int>(item % fg.nch);
-      const int64_t r = base + fl.list[kq];
+      const int32_t ent = fl.list[kq];
+      const int64_t r = base + (ent & ~kFixFullBit);
+      const bool full = (ent & kFixFullBit) != 0;
+      // the row constants and the fast kernel's partial sums in one round of loads
       const float4 rc = __ldcg(a.rowc + r);
+      float2 pv[kOpdFixParts / 32];
+#pragma unroll
+      for (int q = 0; q < kOpdFixParts / 32; ++q)
+        pv[q] = (lane + 32 * q < fg.np) ? __ldcg(a.fixp + r * kOpdFixParts + lane + 32 * q) : make_float2(0.f, 0.f);
       const int64_t t = fix_target_row(a, r, rc);
       if (t < 0) continue;
       const float Ct = rc.x, dC = rc.y, Cd = Ct + dC;
       const int32_t xs = __float_as_int(rc.z);
-      // row totals of the fast kernel's partial sums: a fixed order (lane q
-      // adds partials q, q + 32, ..., then a butterfly), the same in every warp
+      // row totals of the partial sums: a fixed order (lane q adds partials
+      // q, q + 32, ..., then a butterfly), the same in every warp
       float2 p = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int q = 0; q < kOpdFixParts / 32; ++q)
-        if (lane + 32 * q < fg.np) {
-          const float2 v = __ldcg(a.fixp + r * kOpdFixParts + lane + 32 * q);
-          p.x += v.x;
-          p.y += v.y;
-        }
+      for (int q = 0; q < kOpdFixParts / 32; ++q) {
+        p.x += pv[q].x;
+        p.y += pv[q].y;
+      }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         p.x += __shfl_xor_sync(0xffffffffu, p.x, o);
         p.y += __shfl_xor_sync(0xffffffffu, p.y, o);
       }
       const float RKL = p.x, SS = p.y;
-      if (c == 0 && tid == 0) {
+      if (c == 0 && lane == 0) {
         const float zx = E::load(a.draft, r * V + xs);
         a.loss[r] = fmaf(a.lambda_ce * kLn2, Cd - zx * k, RKL);  // -lq[x*] = ln2 (Cd - z_x* k)
       }
       // rows flagged only for the size of their loss keep the fast kernel's gradient
-      if (a.dlogits == nullptr || __ldcg(a.flags + r) != a.epoch) continue;
+      if (a.dlogits == nullptr || !full) continue;
       // gradient: gsT (q a + q (lambda - S)) - gsT lambda [v = x*]  (SS holds S - 1)
       const int64_t lo = static_cast<int64_t>(c) * fg.CH;
       const int nv = static_cast<int>(min(static_cast<int64_t>(fg.CH), V - lo)) / EPV;
@@ -1124,11 +1168,11 @@ __global__ void __launch_bounds__(kFixNT, 3) opd_fix_grad(OpdArgs a, FixGeo fg) 
       const float2 kk = make_float2(k, k), neg1 = make_float2(-1.f, -1.f);
       const float2 nCd = make_float2(-Cd, -Cd), ndC = make_float2(-dC, -dC);
       const float2 gl = make_float2(gsT * kLn2, gsT * kLn2), g1 = make_float2(gL1, gL1);
-      for (int v0 = tid; v0 < nv; v0 += kFixNT * kFixU) {
+      for (int v0 = lane; v0 < nv; v0 += 32 * kFixU) {
         uint4 ty[kFixU], tz[kFixU];
 #pragma unroll
         for (int u = 0; u < kFixU; ++u) {
-          const int v = v0 + u * kFixNT;
+          const int v = v0 + u * 32;
           if (v < nv) {
             ty[u] = ld_vec(trow + static_cast<int64_t>(v) * 16);
             tz[u] = ld_vec(drow + static_cast<int64_t>(v) * 16);
@@ -1136,7 +1180,7 @@ __global__ void __launch_bounds__(kFixNT, 3) opd_fix_grad(OpdArgs a, FixGeo fg) 
         }
 #pragma unroll
         for (int u = 0; u < kFixU; ++u) {
-          const int v = v0 + u * kFixNT;
+          const int v = v0 + u * 32;
           if (v < nv) {
             const Pairs<DT> y(ty[u]), z(tz[u]);
             float g[EPV];

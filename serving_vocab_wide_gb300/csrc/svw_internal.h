@@ -164,7 +164,7 @@ int filter_group(int32_t top_k);
 size_t filter_smem_bytes(int64_t V, int esize, int32_t top_k);
 cudaError_t launch_filtered(const FilterArgs &a, int dtype, bool vec, cudaStream_t stream);
 
-constexpr int kOpdFixChunks = 16;  // vocabulary chunks per row of the OPD fix-up grid
+constexpr int kOpdFixChunks = 64;  // vocabulary chunks per row of the OPD fix-up grid (one warp each)
 constexpr int kOpdFixParts = 128;  // partial sums per row from the fast kernel (one per warp of the cluster)
 constexpr int kBonusParts = 8;  // bonus-row partial slots per request (the largest OPD cluster)
 

@@ -292,6 +292,9 @@ def test_length_head_argument_validation(lib):
     assert lib.svw_length_head_workspace_size(3, 5, 300) == 2 * 4 * 512 * 256 * 4
     assert lib.svw_length_head_workspace_size(5, 16, 40) == 4 * 512 * 64 * 4
     assert lib.svw_length_head_workspace_size(0, 16, 256) == 0
+    # at most 2^20 positions (N k)
+    assert lib.svw_length_head_workspace_size(1 << 15, 32, 256) == 4 * (1 << 20) * 256 * 4
+    assert lib.svw_length_head_workspace_size((1 << 15) + 1, 32, 256) == 0
 
 
 def test_noalloc_argument_checks_come_before_the_size_check(lib):
