@@ -714,7 +714,9 @@ __global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) 
             const float2 az = __ffma2_rn(z.p[h], kk, nz2);  // (z - m_z) k
             const float2 ey = make_float2(ex2(ay.x), ex2(ay.y));
             const float2 ez = make_float2(ex2(az.x), ex2(az.y));
-            const float2 xd = __ffma2_rn(__ffma2_rn(y.p[h], neg1, z.p[h]), kk, nc2);  // (z - y) k - (m_z - m_y) k
+            // (z - y) k - (m_z - m_y) k as the difference of the two scaled entries:
+            // its rounding (~1e-7 of |az|) is weighted by ez, small where |az| is large
+            const float2 xd = __ffma2_rn(ay, neg1, az);
             sy = __fadd2_rn(sy, ey);
             ww = __fadd2_rn(ww, __ffma2_rn(ey, neg1, ez));
             uu = __ffma2_rn(ez, xd, uu);
