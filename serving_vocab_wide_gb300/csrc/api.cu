@@ -489,9 +489,13 @@ svw_status spec_verify_opd(const void *target_logits, const void *draft_logits, 
   f.accept_len = accept_len;
   f.next_token = next_token;
   f.status = status;
+  // the parts grid (tiny) first, so that the gradient fix-up can run beside
+  // the finalize kernel's draw
+  e = svw::launch_opd_fix(o, dtype, svw::kFixParts, st);
+  if (e != cudaSuccess) return SVW_ERR_CUDA;
   e = svw::launch_fused_finalize(f, dtype, greedy, st);
   if (e != cudaSuccess) return SVW_ERR_CUDA;
-  e = svw::launch_opd_fix(o, dtype, st);  // rows with a clipped term, exactly
+  e = svw::launch_opd_fix(o, dtype, svw::kFixGradLast, st);  // rows with a clipped term, exactly
   return e == cudaSuccess ? SVW_OK : SVW_ERR_CUDA;
 }
 

@@ -952,6 +952,11 @@ struct FixGeo {
   // per row, part q from warp q % fw of CTA q / fw, whose threads held
   // vectors tid + j fnt (j < vpt) of vocabulary slice [SL (q / fw), SL (q / fw + 1))
   int32_t np, fw, fnt, vpt, SL;
+  // opd_fix_grad: 0 = wait for the grid ahead (the parts grid) before reading
+  // the partial sums; 1 = read them at once and wait at the end (the grid
+  // ahead is the fused finalize, which lets its dependents go only once it
+  // has waited for the parts grid, itself complete only after the fast kernel)
+  int32_t wait_last;
 };
 
 struct FixList {
@@ -1033,10 +1038,12 @@ __global__ void __launch_bounds__(kFixNT, 3) opd_fix_parts(OpdArgs a, FixGeo fg)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t V = a.V;
   const float k = a.k, c2 = a.clip_c * kLog2e;
-  // the gradient grid may be scheduled now: it scans the flags, then waits
-  // for this grid.  This grid may start before the kernel ahead of it ends
-  // (see opd_fix_grad): it reads only the fast kernel's output.
+  // the grid behind may be scheduled now (the gradient grid scans the flags,
+  // then waits for this one; the fused finalize reads its inputs, then
+  // waits).  The kernel ahead is the fast kernel, which in the fused call
+  // lets this grid start as it begins: wait for its output.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   for (int64_t r = static_cast<int64_t>(blockIdx.x) * kW + warp; r < a.R; r += static_cast<int64_t>(gridDim.x) * kW) {
     const int32_t fv = __ldcg(a.flags + r);
     if (fv != a.epoch && fv != (a.epoch ^ kLossOnlyTag)) continue;
@@ -1099,8 +1106,6 @@ __global__ void __launch_bounds__(kFixNT, 3) opd_fix_parts(OpdArgs a, FixGeo fg)
       }
     }
   }
-  // complete only after the kernel ahead of it, so that the stream's order holds
-  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 template <int DT>
@@ -1112,12 +1117,14 @@ __global__ void __launch_bounds__(kFixNT, 3) opd_fix_grad(OpdArgs a, FixGeo fg) 
   const int64_t V = a.V;
   const float k = a.k, c2 = a.clip_c * kLog2e;
   const float gsT = a.grad_scale * a.invT;
-  // this grid may start while the parts grid ahead of it runs: it scans the
-  // flags (final since the fast kernel ended), then waits for that grid
+  // this grid may start while the grid ahead of it runs: it scans the flags
+  // (final since the fast kernel ended), then, behind the parts grid, waits
+  // for it; behind the fused finalize (fg.wait_last) it works at once, beside
+  // the finalize, and waits only at its end
   bool waited = false;
   for (int64_t base = 0; base < a.R; base += kFixBatch) {
     const int m = fix_scan(a, base, fl);
-    if (!waited) {
+    if (!waited && !fg.wait_last) {
       asm volatile("griddepcontrol.wait;" ::: "memory");
       waited = true;
     }
@@ -1232,9 +1239,11 @@ FixGeo fix_geo(int64_t V, int CL, int NT, int VPT, int SL) {
 }
 
 // the fix-up grids after the fast kernel (CL CTAs of NT threads, VPT vectors
-// per thread, slices of SL entries)
+// per thread, slices of SL entries): which = kFixBoth (parts, then the
+// gradient behind it), kFixParts, or kFixGradLast (the gradient grid behind
+// the fused finalize, see FixGeo::wait_last)
 template <int DT>
-cudaError_t launch_fix(const OpdArgs &a, cudaStream_t st, int CL, int NT, int VPT, int SL) {
+cudaError_t launch_fix(const OpdArgs &a, cudaStream_t st, int CL, int NT, int VPT, int SL, int which) {
   static std::atomic<int> nsm_cache[64];  // zero-initialised (static storage)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1244,7 +1253,8 @@ cudaError_t launch_fix(const OpdArgs &a, cudaStream_t st, int CL, int NT, int VP
     if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) nsm_cache[dev].store(nsm, std::memory_order_relaxed);
   }
-  const FixGeo fg = fix_geo(a.V, CL, NT, VPT, SL);
+  FixGeo fg = fix_geo(a.V, CL, NT, VPT, SL);
+  fg.wait_last = (which == kFixGradLast) ? 1 : 0;
   // programmatic launches: each overlaps the tail of the kernel ahead of it
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -1256,14 +1266,18 @@ cudaError_t launch_fix(const OpdArgs &a, cudaStream_t st, int CL, int NT, int VP
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  void *tm = timer_before("opd_fix_parts", st);
-  e = cudaLaunchKernelEx(&cfg, opd_fix_parts<DT>, a, fg);
-  timer_after(tm, st);
-  if (e != cudaSuccess) return e;
-  tm = timer_before("opd_fix_grad", st);
-  e = cudaLaunchKernelEx(&cfg, opd_fix_grad<DT>, a, fg);
-  timer_after(tm, st);
-  if (e != cudaSuccess) return e;
+  if (which != kFixGradLast) {
+    void *tm = timer_before("opd_fix_parts", st);
+    e = cudaLaunchKernelEx(&cfg, opd_fix_parts<DT>, a, fg);
+    timer_after(tm, st);
+    if (e != cudaSuccess) return e;
+  }
+  if (which != kFixParts) {
+    void *tm = timer_before("opd_fix_grad", st);
+    e = cudaLaunchKernelEx(&cfg, opd_fix_grad<DT>, a, fg);
+    timer_after(tm, st);
+    if (e != cudaSuccess) return e;
+  }
   return cudaGetLastError();
 }
 
@@ -1368,17 +1382,17 @@ cudaError_t launch_clusters(const char *name, Kern kern, int nt, const OpdArgs &
 
 // fast pass and / or fix-up with NT threads and up to VPT vectors per thread
 template <int DT, int VPT, int NT>
-cudaError_t launch_fast(const OpdArgs &a, const OpdPlan &p, cudaStream_t st, bool fast, bool fix, int *grid) {
+cudaError_t launch_fast(const OpdArgs &a, const OpdPlan &p, cudaStream_t st, bool fast, int fix, int *grid) {
   if (fast) {
     const cudaError_t e = launch_clusters("opd_fast_kernel", opd_fast_kernel<DT, VPT, NT>, NT, a, p, kTable, st, grid);
-    if (e != cudaSuccess || !fix) return e;
+    if (e != cudaSuccess || fix == kFixNone) return e;
   }
-  return launch_fix<DT>(a, st, p.CL, NT, VPT, p.SL);
+  return launch_fix<DT>(a, st, p.CL, NT, VPT, p.SL, fix);
 }
 
 // the fast-path variant for this row geometry; false if the row is too wide
 template <int DT>
-cudaError_t launch_fast_any(const OpdArgs &a, const OpdPlan &p, cudaStream_t st, bool fast, bool fix, int *grid,
+cudaError_t launch_fast_any(const OpdArgs &a, const OpdPlan &p, cudaStream_t st, bool fast, int fix, int *grid,
                             bool *ok) {
   const int nvec = static_cast<int>(static_cast<int64_t>(p.SL) * Elem<DT>::kSize / 16);
   *ok = true;
@@ -1394,7 +1408,7 @@ template <int DT, bool BULK>
 cudaError_t launch_opd_cfg(const OpdArgs &a, const OpdPlan &p, cudaStream_t st) {
   if (BULK && a.flags != nullptr) {
     bool ok = false;
-    const cudaError_t e = launch_fast_any<DT>(a, p, st, true, true, nullptr, &ok);
+    const cudaError_t e = launch_fast_any<DT>(a, p, st, true, kFixBoth, nullptr, &ok);
     if (ok) return e;
   }
   return launch_clusters("opd_exact_kernel", opd_exact_kernel<DT, BULK>, 512, a, p, kNone, st);
@@ -1415,17 +1429,17 @@ cudaError_t launch_opd_fused_fast(const OpdArgs &a, int dtype, int *grid, cudaSt
   const int esize = (dtype == SVW_BF16) ? 2 : 4;
   const OpdPlan p = plan_opd(a.V, esize);
   bool ok = false;
-  const cudaError_t e = (dtype == SVW_BF16) ? launch_fast_any<1>(a, p, st, true, false, grid, &ok)
-                                            : launch_fast_any<0>(a, p, st, true, false, grid, &ok);
+  const cudaError_t e = (dtype == SVW_BF16) ? launch_fast_any<1>(a, p, st, true, kFixNone, grid, &ok)
+                                            : launch_fast_any<0>(a, p, st, true, kFixNone, grid, &ok);
   return ok ? e : cudaErrorInvalidValue;
 }
 
-cudaError_t launch_opd_fix(const OpdArgs &a, int dtype, cudaStream_t st) {
+cudaError_t launch_opd_fix(const OpdArgs &a, int dtype, int which, cudaStream_t st) {
   const int esize = (dtype == SVW_BF16) ? 2 : 4;
   const OpdPlan p = plan_opd(a.V, esize);
   bool ok = false;
-  const cudaError_t e = (dtype == SVW_BF16) ? launch_fast_any<1>(a, p, st, false, true, nullptr, &ok)
-                                            : launch_fast_any<0>(a, p, st, false, true, nullptr, &ok);
+  const cudaError_t e = (dtype == SVW_BF16) ? launch_fast_any<1>(a, p, st, false, which, nullptr, &ok)
+                                            : launch_fast_any<0>(a, p, st, false, which, nullptr, &ok);
   return ok ? e : cudaErrorInvalidValue;
 }
 

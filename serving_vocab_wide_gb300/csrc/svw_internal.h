@@ -205,6 +205,8 @@ cudaError_t launch_opd(const OpdArgs &a, int dtype, bool bulk, cudaStream_t stre
 bool opd_fast_supported(int64_t V, int esize);
 int opd_cluster_size(int64_t V, int esize);  // CTAs per row in the OPD kernels
 cudaError_t launch_opd_fused_fast(const OpdArgs &a, int dtype, int *grid, cudaStream_t stream);
-cudaError_t launch_opd_fix(const OpdArgs &a, int dtype, cudaStream_t stream);
+// which fix-up grids launch_opd_fix launches (see opd.cu)
+constexpr int kFixNone = 0, kFixBoth = 1, kFixParts = 2, kFixGradLast = 3;
+cudaError_t launch_opd_fix(const OpdArgs &a, int dtype, int which, cudaStream_t stream);
 
 }  // namespace svw
