@@ -111,7 +111,7 @@ CALL_KERNELS = {
     "spec_verify": "verify_stats + verify_finalize (accept tests and, at T > 0, the inverse-CDF draw)",
     "opd_loss": "opd_fast_kernel + opd_fix_parts + opd_fix_grad",
     "spec_verify_opd": "opd_fast_kernel (draft rows + bonus rows) + fused_finalize (accept tests, draw) + opd_fix_parts + opd_fix_grad",
-    "length_head": "length_head_label + length_head_mma (tcgen05 projection, four K quarters) + length_head_reduce (quarters summed, bias, SiLU, mean, w2 dot, sigmoid, clamp)",
+    "length_head": "length_head_label + length_head_mma (tcgen05 projection, four K quarters summed in the cluster, bias, SiLU, w2 dot per position) + length_head_final (mean, b2, sigmoid, clamp)",
 }
 CALLS = ["verify_T0", "verify_T0.6", "verify_T1+opd", "length_head"]
 # top-k / top-p settings of the filtered-verification measurement: (T, top_k, top_p)

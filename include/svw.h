@@ -319,17 +319,19 @@ svw_status spec_verify_opd(const void *target_logits, const void *draft_logits, 
  *   b1, w2     device float [hidden_out];  b2, gamma > 0 on the host.
  *   a_hat      device float [N] out (before the gamma scaling);  k_hat device int32 [N] out.
  *   workspace  device, 256-byte aligned, >= svw_length_head_workspace_size(N, k,
- *              hidden_out) bytes: the projection's fp32 partial products (four
- *              K quarters of N k positions, rounded up to 512, times H' rounded
- *              up to 32, or to 256-wide tiles above 256); contents need not be
- *              initialised.
+ *              hidden_out) bytes: one fp32 per position and 256-wide column
+ *              tile of W1 (N k ceil(H'/256) floats, rounded up to 256 bytes);
+ *              contents need not be initialised.
  * The projection of the N k positions runs on the tensor cores (tcgen05 MMA,
  * operands staged by TMA, fp32 accumulation in tensor memory) in four K
- * quarters; a second kernel, one CTA per request, sums the quarters and
- * applies bias, SiLU, the mean over positions, the dot with w2, sigmoid,
- * gamma, floor and clamp.  Two kernel launches, no library call; the host
- * only encodes the two TMA descriptors.  If a bounded wait inside the
- * projection gives up, the affected requests get a_hat = NaN.
+ * quarters, one thread-block cluster per 128 positions; the quarters are
+ * summed inside the cluster (distributed shared memory), and the same kernel
+ * applies bias and SiLU and dots each position with w2.  A second, small
+ * kernel adds each request's position dots and applies the mean, b2,
+ * sigmoid, gamma, floor and clamp.  Two kernel launches, each a programmatic
+ * dependent of the one ahead (its set-up overlaps that kernel's tail); no
+ * library call; the host only encodes the two TMA descriptors.  If a bounded
+ * wait inside the projection gives up, the affected requests get a_hat = NaN.
  */
 size_t svw_length_head_workspace_size(int32_t n_requests, int32_t k, int32_t hidden_out);
 
@@ -388,7 +390,7 @@ svw_status spec_verify_noalloc(const void *target_logits, const void *draft_logi
  * kernel made from this thread ("early_plan", "verify_stats",
  * "verify_finalize", "verify_early_cluster", "filter_rows", "filtered_finalize",
  * "opd_fast_kernel", "opd_fix_parts", "opd_fix_grad", "opd_exact_kernel",
- * "fused_finalize", "length_head_mma", "length_head_reduce") records
+ * "fused_finalize", "length_head_mma", "length_head_final") records
  * begin_event just before it and end_event just after it on the launch stream (cudaEvent_t handles passed as void*, owned
  * by the caller).  kernel = NULL disarms.  The library records nothing
  * unless armed.  Lets a benchmark time one kernel of a multi-kernel call with

@@ -15,23 +15,29 @@
 // in tensor memory), both operands K-major, staged by TMA (cp.async.bulk.tensor
 // with the 128-byte swizzle).  A CTA owns a 128-row tile of X and a 256-column
 // tile of W1 (H' <= 256: all of it) over one quarter of K = H, so that 128
-// CTAs share the work at the benchmark's shape; a thread-block cluster holds
-// four row tiles with the same K quarter, which load one quarter each of
-// their common W1 tile and multicast it to all four (W1 is re-read by every
-// row tile: without this it is two thirds of the traffic into the SMs).  X tiles come from DRAM through a seven-stage ring,
-// W1 tiles through a three-stage ring, each fed by its own producer thread;
-// one thread issues the MMAs.  The fp32 partial tile leaves tensor memory
-// through shared memory (a transpose for coalesced stores) into the caller's
-// workspace.  A second kernel, one CTA per request and a programmatic
-// dependent of the first, sums the four K partials of each of the request's
-// positions in a fixed order and finishes the head: bias, SiLU, the mean
-// over positions, the dot with w2, sigmoid, gamma, floor and clamp.
+// CTAs share the work at the benchmark's shape; the four K quarters of a row
+// tile form a thread-block cluster.  X tiles come from DRAM (all of them
+// requested into L2 once the first round is on its way) through a five-stage
+// ring, W1 tiles (2 MB in all, read by every row tile: L2 hits) through a
+// four-stage ring, each fed by its own producer thread; one thread issues the
+// MMAs.  The K quarters are then summed inside the cluster: CTA q
+// of the cluster takes rows [32 q, 32 q + 32) of the tile, and every CTA
+// sends each 32-row block of its fp32 partial tile from tensor memory into
+// the owning CTA's shared memory (distributed shared memory, one slot per
+// quarter).  The owner adds the four quarters in quarter order and finishes
+// each of its rows: bias, SiLU and the dot with w2 over the tile's columns,
+// one float per position and column tile.  Since the mean over positions and
+// the dot with w2 commute, a request only needs the sum of its positions'
+// dots: when its k positions lie in one 32-row block (k divides 32, H' <= 256)
+// the owning CTA adds them and applies b2, sigmoid, gamma, floor and clamp;
+// otherwise a small programmatic-dependent kernel does, from the dots in the
+// workspace (the same order, the same arithmetic).  No partial product
+// leaves the chip.
 //
 // Every mbarrier wait is bounded by a clock deadline; a CTA that gives up
-// stops issuing work, lets the copies it started land (again bounded), writes
+// stops issuing work, lets the copies it started land (again bounded), sends
 // NaN for its rows, still joins every cluster barrier and frees its tensor
 // memory.
-#include <cooperative_groups.h>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -44,8 +50,6 @@
 #include "svw_device.cuh"
 #include "svw_internal.h"
 
-namespace cg = cooperative_groups;
-
 namespace svw {
 
 namespace {
@@ -53,24 +57,22 @@ namespace {
 constexpr int kTM = 128;          // rows of X per CTA (the MMA's M)
 constexpr int kTN = 256;          // columns of W1 rows per CTA (the MMA's N at most)
 constexpr int kBK = 64;           // K per stage: one 128-byte swizzle row of bf16
-constexpr int kStagesA = 7;       // X tiles come from DRAM: the deeper ring
-constexpr int kStagesB = 3;       // W1 tiles mostly hit L2
-constexpr int kKSplit = 4;        // K quarters
-constexpr int kMGroup = 4;        // row tiles per cluster, sharing their W1 tiles
-constexpr int kCluster = kMGroup;
-constexpr int kMmaThreads = 128;  // four warps: TMEM lanes 0-127
+constexpr int kStagesA = 5;       // X tiles (16 KB; requested into L2 ahead)
+constexpr int kStagesB = 4;       // W1 tiles (32 KB; L2 hits): bytes in flight in proportion
+constexpr int kKSplit = 4;        // K quarters: the CTAs of a cluster
+constexpr int kMmaThreads = 256;  // eight warps; warp w reads TMEM lanes [32 (w % 4), 32 (w % 4) + 32)
+constexpr int kWarps = kMmaThreads / 32;
 constexpr int kStageA = kTM * kBK * 2;  // 16 KB
+constexpr int kBlock = kTM / kKSplit;   // rows each CTA of the cluster finishes (32)
 
 // Dynamic shared memory: the two rings, reused after the main loop for the
-// partial tile on its way out (128 rows of NT + 4 floats: rows stay 16-byte
-// aligned, and with 16-byte stores the eight rows of one store phase fall on
-// distinct banks).
+// four K quarters of this CTA's 32-row block (slot q from quarter q, float4
+// entry (c / 4) * 32 + row holding columns c .. c + 3 of that row).
 __host__ __device__ constexpr int ringB_off() { return kStagesA * kStageA; }
 __host__ __device__ constexpr int ring_bytes(int NT) { return kStagesA * kStageA + kStagesB * NT * kBK * 2; }
-__host__ __device__ constexpr int tile_pitch(int NT) { return NT + 4; }
-__host__ __device__ constexpr int tile_bytes(int NT) { return kTM * tile_pitch(NT) * 4; }
+__host__ __device__ constexpr int slot_bytes(int NT) { return kBlock * NT * 4; }
 __host__ __device__ constexpr int head_smem(int NT) {
-  return (ring_bytes(NT) > tile_bytes(NT) ? ring_bytes(NT) : tile_bytes(NT)) + 1024;
+  return (ring_bytes(NT) > kKSplit * slot_bytes(NT) ? ring_bytes(NT) : kKSplit * slot_bytes(NT)) + 1024;
 }
 
 // ---------------------------------------------------------------------------
@@ -82,17 +84,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
       "[%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(mbar)
-      : "memory");
-}
-
-// the same box delivered to every CTA of ctamask (same shared-memory offset,
-// each CTA's own mbarrier at the same offset)
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap *map, int32_t x, int32_t y,
-                                               uint32_t mbar, uint16_t ctamask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, "
-      "{%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(mbar), "h"(ctamask)
       : "memory");
 }
 
@@ -124,18 +115,23 @@ __device__ __forceinline__ void mma_commit(uint32_t mbar) {
                : "memory");
 }
 
-// one arrival on the mbarrier at this offset in every CTA of ctamask once
-// every MMA issued before it is done
-__device__ __forceinline__ void mma_commit_mc(uint32_t mbar, uint16_t ctamask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::
-                   "r"(mbar),
-               "h"(ctamask)
+// the box at (x, y) fetched into L2 ahead of its load (no completion to wait for)
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
                : "memory");
 }
 
-// 32 consecutive fp32 columns of this thread's TMEM lane
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
-  uint32_t r[32];
+// 16 bytes into the shared memory of a CTA of this cluster (address from mapa)
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+// start loading 32 consecutive fp32 columns of this thread's TMEM lane; the
+// registers hold them after tmem_wait_ld()
+__device__ __forceinline__ void tmem_ld32_start(uint32_t taddr, uint32_t *r) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
       "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
@@ -144,10 +140,8 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
         "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
         "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
 }
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor of a K-major operand tile as the TMA's
 // 128-byte swizzle lays it out: rows of 128 bytes (64 bf16 of K), eight-row
@@ -175,12 +169,19 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
 }
 
 struct HeadArgs {
-  float *part;     // [ntiles][kKSplit][Mpad][NT] fp32 partial products (the workspace)
-  int32_t M;       // positions (N k)
-  int32_t Mpad;    // rows per partial block: M rounded up to a cluster's row tiles
-  int32_t nkb;     // 64-wide K blocks of H
-  int32_t kb_per;  // K blocks per K quarter
-  int32_t NT;      // columns of this launch's W1 tiles (a multiple of 16, <= 256)
+  float *s;         // [ntiles][M] per position and column tile: sum_c w2[c] SiLU(y[c] + b1[c])
+  float *a_hat;     // [N] out, when fuse
+  int32_t *k_hat;   // [N] out, when fuse
+  int32_t N, k;     // requests, positions per request
+  float b2, gamma;
+  int32_t fuse;     // 1: each CTA finishes its block's requests (k divides 32, one column tile)
+  const float *b1;  // [Hp]
+  const float *w2;  // [Hp]
+  int32_t M;        // positions (N k)
+  int32_t Hp;       // columns of W1 (H')
+  int32_t nkb;      // 64-wide K blocks of H
+  int32_t kb_per;   // K blocks per K quarter
+  int32_t NT;       // columns of this launch's W1 tiles (a multiple of 32, <= 256)
 };
 
 struct HeadSmem {
@@ -191,7 +192,21 @@ struct HeadSmem {
   int32_t err;
   int32_t consumed;  // K blocks the MMA thread consumed
   int32_t issuedA, issuedB;
+  float red[kWarps][32];            // the row dots of the eight column groups
+  float dot[kBlock];                // the block's position dots (fuse)
+  float b1[kTN], w2[kTN];           // this column tile's bias and output weights
 };
+
+// a_hat and k_hat of request i from the sum z of its position dots
+__device__ __forceinline__ void head_finish(float z, int32_t k, float b2, float gamma, float *a_hat, int32_t *k_hat,
+                                            int32_t i) {
+  z = b2 + z / static_cast<float>(k);
+  const float av = 1.f / (1.f + expf(-z));
+  float kh = floorf(gamma * av * static_cast<float>(k));
+  kh = fminf(fmaxf(kh, 1.f), static_cast<float>(k));
+  a_hat[i] = av;
+  k_hat[i] = (av == av) ? static_cast<int32_t>(kh) : 1;
+}
 
 __global__ void __launch_bounds__(kMmaThreads, 1)
     length_head_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, HeadArgs a) {
@@ -202,19 +217,16 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   unsigned char *ring = dyn_raw + (base - raw);
   const int NT = a.NT;
   const int stageB = NT * kBK * 2;
-  const int shareB = stageB / kMGroup;  // the part of a W1 tile each CTA loads (a multiple of 1024 bytes)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // blockIdx.x = (row group * kKSplit + K quarter) * kMGroup + rank in the cluster
-  const int mh = static_cast<int>(blockIdx.x % kCluster);  // which row tile of the cluster's group
-  const int kr = static_cast<int>((blockIdx.x / kCluster) % kKSplit);  // K quarter
-  const int mtile = static_cast<int>(blockIdx.x / (kCluster * kKSplit)) * kMGroup + mh;
+  // blockIdx.x = row tile * kKSplit + K quarter (the rank in the cluster)
+  const int kr = static_cast<int>(blockIdx.x % kKSplit);
+  const int mtile = static_cast<int>(blockIdx.x / kKSplit);
   const int ntile = static_cast<int>(blockIdx.y);
   const int kb0 = kr * a.kb_per;
   const int kb1 = min(a.nkb, kb0 + a.kb_per);
   const int nkb = max(0, kb1 - kb0);
-  const uint16_t group = static_cast<uint16_t>((1u << kCluster) - 1u);  // the CTAs sharing W1 tiles
 
-  // the reducing kernel may be scheduled now; it waits for this grid
+  // the finishing kernel may be scheduled now; it waits for this grid
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) {
     for (int s = 0; s < kStagesA; ++s) {
@@ -223,7 +235,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     }
     for (int s = 0; s < kStagesB; ++s) {
       mbar_init(&sm.fullB[s], 1);
-      mbar_init(&sm.emptyB[s], kMGroup);  // every CTA of the group must be done with the stage
+      mbar_init(&sm.emptyB[s], 1);
     }
     mbar_init(&sm.acc, 1);
     sm.err = 0;
@@ -239,15 +251,27 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  cg::this_cluster().sync();  // every CTA's barriers exist before a peer multicasts into it
+  __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem;
+  // the set-up above overlaps the kernel ahead; its output (the hidden
+  // states, an updated W1) is read only from here on
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  for (int c = tid; c < NT; c += kMmaThreads) {
+    const int col = ntile * kTN + c;
+    sm.b1[c] = (col < a.Hp) ? __ldg(a.b1 + col) : 0.f;
+    sm.w2[c] = (col < a.Hp) ? __ldg(a.w2 + col) : 0.f;  // padding columns contribute nothing
+  }
 
   if (warp == 0 && lane == 0) {
-    // ---- producer of A: this CTA's X tiles (128 rows x 64 of K) ----
+    // ---- producer of A: this CTA's X tiles (128 rows x 64 of K) through
+    // the ring; once the ring's first round is on its way, the rest are
+    // requested into L2 (DRAM sees the whole projection's reads together) ----
     int i = 0;
     for (; i < nkb; ++i) {
       const int s = i % kStagesA;
+      if (i == kStagesA)
+        for (int j = kStagesA; j < nkb; ++j) tma_prefetch_2d(&tmA, (kb0 + j) * kBK, mtile * kTM);
       if (i >= kStagesA && !mbar_wait_bounded(&sm.emptyA[s], static_cast<uint32_t>((i / kStagesA - 1) & 1))) {
         atomicOr(&sm.err, 1);
         break;
@@ -258,18 +282,20 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     }
     sm.issuedA = i;
   } else if (warp == 2 && lane == 0) {
-    // ---- producer of B: a quarter of each W1 tile (NT / 4 rows x 64 of K),
-    // multicast to the group; the stage's barrier expects the whole tile ----
+    // ---- producer of B: this CTA's W1 tiles (NT rows x 64 of K), the ones
+    // beyond the ring's first round requested into L2 as for A ----
     int i = 0;
     for (; i < nkb; ++i) {
       const int s = i % kStagesB;
+      if (i == kStagesB)
+        for (int j = kStagesB; j < nkb; ++j) tma_prefetch_2d(&tmB, (kb0 + j) * kBK, ntile * kTN);
       if (i >= kStagesB && !mbar_wait_bounded(&sm.emptyB[s], static_cast<uint32_t>((i / kStagesB - 1) & 1))) {
         atomicOr(&sm.err, 1);
         break;
       }
       mbar_arrive_expect_tx(&sm.fullB[s], static_cast<uint32_t>(stageB));
-      tma_load_2d_mc(base + static_cast<uint32_t>(ringB_off() + s * stageB + mh * shareB), &tmB, (kb0 + i) * kBK,
-                     ntile * kTN + mh * (NT / kMGroup), smem_u32(&sm.fullB[s]), group);
+      tma_load_2d(base + static_cast<uint32_t>(ringB_off() + s * stageB), &tmB, (kb0 + i) * kBK, ntile * kTN,
+                  smem_u32(&sm.fullB[s]));
     }
     sm.issuedB = i;
   } else if (warp == 1 && lane == 0) {
@@ -289,8 +315,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
 #pragma unroll
       for (int kk = 0; kk < kBK / 16; ++kk)  // +32 bytes of K per step: +2 in the address field
         mma_bf16(tmem, da + 2 * kk, db + 2 * kk, idesc, (i > 0 || kk > 0) ? 1u : 0u);
-      mma_commit(smem_u32(&sm.emptyA[sa]));          // free once these MMAs are done
-      mma_commit_mc(smem_u32(&sm.emptyB[sb]), group);  // in every CTA of the group
+      mma_commit(smem_u32(&sm.emptyA[sa]));  // free once these MMAs are done
+      mma_commit(smem_u32(&sm.emptyB[sb]));
     }
     sm.consumed = i;
     if (i > 0) mma_commit(smem_u32(&sm.acc));
@@ -309,105 +335,122 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   __syncthreads();
   const bool ok = (sm.err == 0) && (sm.consumed == nkb);
 
-  // ---- the partial tile: TMEM lane = row -> shared memory -> coalesced rows in
-  // the workspace (block (ntile, kr), rows of NT floats) ----
-  float *P = reinterpret_cast<float *>(ring);
-  const int pitch = tile_pitch(NT);
+  // ---- the K quarters summed inside the cluster ----
+  // every CTA of the cluster is past its main loop: its rings may be written
+  cluster_barrier();
   {
-    const int row = warp * 32 + lane;
-    float *prow = P + row * pitch;
-    for (int c = 0; c < NT; c += 64) {
-      float v[64];
-      if (nkb > 0 && ok) {
-        tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + static_cast<uint32_t>(c), v);
-        if (c + 32 < NT) tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + static_cast<uint32_t>(c + 32), v + 32);
+    // warp w holds tile rows [32 q, 32 q + 32), q = w % 4 (its TMEM lanes),
+    // and sends them to CTA q, slot kr: the 32-column chunks of parity w / 4
+    const int q = warp & 3;
+    const uint32_t slot = base + static_cast<uint32_t>(kr * slot_bytes(NT));
+    const uint32_t dst = (q == kr) ? slot : mapa_shared(slot, static_cast<uint32_t>(q));
+    const bool have = (nkb > 0 && ok);
+    // no K block for this quarter: a zero partial; a wait that gave up: NaN
+    const uint32_t fill = (nkb == 0) ? 0u : 0x7fffffffu;
+    // two chunks per round: both TMEM loads in flight, then 16 stores of 16 bytes
+    for (int c = (warp >> 2) * 32; c < NT; c += 128) {
+      const bool two = (c + 64 < NT);
+      uint32_t v[64];
+      if (have) {
+        const uint32_t ta = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(c);
+        tmem_ld32_start(ta, v);
+        if (two) tmem_ld32_start(ta + 64, v + 32);
+        tmem_wait_ld();
       } else {
-        // no K block for this quarter: a zero partial; a wait that gave up: NaN
 #pragma unroll
-        for (int j = 0; j < 64; ++j) v[j] = (nkb == 0) ? 0.f : __int_as_float(0x7fffffff);
+        for (int j = 0; j < 64; ++j) v[j] = fill;
       }
 #pragma unroll
-      for (int j = 0; j < 64; j += 4)
-        if (c + j < NT) *reinterpret_cast<float4 *>(prow + c + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-    }
-  }
-  __syncthreads();
-  {
-    float *G = a.part + ((static_cast<int64_t>(ntile) * kKSplit + kr) * a.Mpad + static_cast<int64_t>(mtile) * kTM) * NT;
-    const int nv = NT / 4;  // 16-byte vectors per row
-    for (int row = warp; row < kTM; row += kMmaThreads / 32) {
-      if (mtile * kTM + row >= a.M) break;
-      const float *prow = P + row * pitch;
-      for (int v = lane; v < nv; v += 32)
-        st_stream(G + static_cast<int64_t>(row) * NT + 4 * v, prow[4 * v], prow[4 * v + 1], prow[4 * v + 2],
-                  prow[4 * v + 3]);
+      for (int j = 0; j < 16; ++j) {
+        const int cc = c + ((j < 8) ? 4 * j : 64 + 4 * (j - 8));  // first column of the 16-byte piece
+        if (j < 8 || two) {
+          const uint32_t off = static_cast<uint32_t>(((cc >> 2) * 32 + lane) * 16);
+          st_cluster_v4(dst + off, __uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                        __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+        }
+      }
     }
   }
   tc_fence_before();
-  cg::this_cluster().sync();  // every commit into a peer's barrier has landed before anyone exits
+  cluster_barrier();  // every quarter of this CTA's rows has landed
+  {
+    // thread (g, r): row r of the block, columns [g NT / 8, (g + 1) NT / 8)
+    const int r = lane, g = warp;
+    const float4 *S = reinterpret_cast<const float4 *>(ring);
+    const int sl = slot_bytes(NT) / 16;  // float4 entries per slot
+    const int q0 = g * (NT / 32), q1 = q0 + NT / 32;
+    float acc = 0.f;
+#pragma unroll 4
+    for (int c4 = q0; c4 < q1; ++c4) {
+      const int e = c4 * 32 + r;
+      float4 y = S[e];
+#pragma unroll
+      for (int q = 1; q < kKSplit; ++q) {  // quarter order
+        const float4 t = S[q * sl + e];
+        y.x += t.x;
+        y.y += t.y;
+        y.z += t.z;
+        y.w += t.w;
+      }
+      const float yv[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float x = yv[j] + sm.b1[c4 * 4 + j];
+        acc = fmaf(sm.w2[c4 * 4 + j], __fdividef(x, 1.f + __expf(-x)), acc);  // w2 SiLU
+      }
+    }
+    sm.red[g][r] = acc;
+    __syncthreads();
+    if (g == 0) {
+      const int64_t m0 = static_cast<int64_t>(mtile) * kTM + kr * kBlock;  // the block's first position
+      float d = sm.red[0][r];
+#pragma unroll
+      for (int w = 1; w < kWarps; ++w) d += sm.red[w][r];  // column-group order
+      if (!a.fuse) {
+        if (m0 + r < a.M) a.s[static_cast<int64_t>(ntile) * a.M + m0 + r] = d;
+      } else {
+        sm.dot[r] = d;
+        __syncwarp();
+        // lane j finishes the block's j-th request (positions in order)
+        const int64_t i = m0 / a.k + r;
+        if (r < kBlock / a.k && i < a.N) {
+          float z = 0.f;
+          for (int p = 0; p < a.k; ++p) z += sm.dot[r * a.k + p];
+          head_finish(z, a.k, a.b2, a.gamma, a.a_hat, a.k_hat, static_cast<int32_t>(i));
+        }
+      }
+    }
+  }
+  __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTN);
   }
 }
 
-// Per request (one CTA): for each of its k positions the four K partials of
-// every column are summed in quarter order, then bias and SiLU; the positions
-// are averaged, dotted with w2 (a fixed-order block reduction), and b2,
-// sigmoid, gamma, floor and clamp give a_hat and k_hat.
-constexpr int kReduceThreads = 256;
-__global__ void __launch_bounds__(kReduceThreads, 2) length_head_reduce(const float *part, const float *b1, const float *w2,
-                                                                     float b2, int32_t k, int32_t Hp, int32_t Mpad,
-                                                                     int32_t NT, float gamma, float *a_hat,
-                                                                     int32_t *k_hat) {
-  __shared__ float red[kReduceThreads / 32];
-  asm volatile("griddepcontrol.wait;" ::: "memory");  // the partials are complete
-  const int32_t i = blockIdx.x;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  float acc = 0.f;
-  for (int n = tid; n < Hp; n += kReduceThreads) {
-    const int t = n / kTN, c = n % kTN;
-    const float bn = __ldg(b1 + n);
-    const float *blk = part + static_cast<int64_t>(t) * kKSplit * Mpad * NT + c;
-    float s = 0.f;
-    for (int p0 = 0; p0 < k; p0 += 8) {
-      // the quarters of eight positions in flight before any arithmetic
-      float y[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        // offsets within the partials (M_pad NT floats per quarter) fit 32 bits
-        const int m = i * k + p0 + u;
-        y[u] = 0.f;
-        if (p0 + u < k) {
-#pragma unroll
-          for (int q = 0; q < kKSplit; ++q) y[u] += __ldcg(blk + (q * Mpad + m) * NT);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        if (p0 + u < k) {
-          const float g = y[u] + bn;
-          s += g / (1.f + expf(-g));  // SiLU
-        }
-    }
-    acc = fmaf(__ldg(w2 + n), s / static_cast<float>(k), acc);
+// Per request: the positions' dots summed over column tiles and positions
+// (fixed order), then the mean, b2, sigmoid, gamma, floor and clamp give
+// a_hat and k_hat.
+__global__ void length_head_final(const float *s, int32_t ntiles, int32_t M, int32_t N, int32_t k, float b2,
+                                  float gamma, float *a_hat, int32_t *k_hat) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the dots are complete
+  const int32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= N) return;
+  float z = 0.f;
+  for (int t = 0; t < ntiles; ++t) {
+    const float *st = s + static_cast<int64_t>(t) * M + static_cast<int64_t>(i) * k;
+#pragma unroll 8
+    for (int p = 0; p < k; ++p) z += __ldcg(st + p);
   }
-  acc = warp_sum(acc);
-  if (lane == 0) red[warp] = acc;
-  __syncthreads();
-  if (tid == 0) {
-    float z = b2;
-    for (int w = 0; w < kReduceThreads / 32; ++w) z += red[w];
-    const float av = 1.f / (1.f + expf(-z));
-    float kh = floorf(gamma * av * static_cast<float>(k));
-    kh = fminf(fmaxf(kh, 1.f), static_cast<float>(k));
-    a_hat[i] = av;
-    k_hat[i] = (av == av) ? static_cast<int32_t>(kh) : 1;
-  }
+  head_finish(z, k, b2, gamma, a_hat, k_hat, i);
 }
 
 __global__ void length_label_kernel(const int32_t *accept_len, const int32_t *cu, const float *a_hat, int32_t N,
                                     float *a_star, float *loss) {
+  // the length head's projection may set up now (it waits for this grid
+  // before it reads anything)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the accepted lengths are complete
   const int32_t i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= N) return;
   const int32_t L = __ldg(cu + i + 1) - __ldg(cu + i);
@@ -455,21 +498,17 @@ bool make_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t H, int bo
 
 }  // namespace
 
-// the partial-product blocks' geometry: column tiles, their width, padded rows
-static void head_geometry(int32_t N, int32_t k, int32_t Hp, int *ntiles, int *NT, int64_t *Mpad) {
+// column tiles of W1 and their width (the MMA's N: a multiple of 16; of 32
+// here, so that the tile's 32-column TMEM loads stay whole)
+static void head_geometry(int32_t Hp, int *ntiles, int *NT) {
   *ntiles = (Hp + kTN - 1) / kTN;
-  // the MMA's N: a multiple of 16; of 32 here, so that each CTA's quarter of a
-  // W1 tile starts on a 1024-byte swizzle atom
   *NT = (*ntiles == 1) ? (Hp + 31) / 32 * 32 : kTN;
-  const int64_t rows = static_cast<int64_t>(kTM) * kMGroup;
-  *Mpad = (static_cast<int64_t>(N) * k + rows - 1) / rows * rows;
 }
 
 size_t length_head_gemm_bytes(int32_t N, int32_t k, int32_t Hp) {
   int ntiles = 0, NT = 0;
-  int64_t Mpad = 0;
-  head_geometry(N, k, Hp, &ntiles, &NT, &Mpad);
-  return (static_cast<size_t>(ntiles) * kKSplit * Mpad * NT * sizeof(float) + 255) / 256 * 256;
+  head_geometry(Hp, &ntiles, &NT);
+  return (static_cast<size_t>(ntiles) * N * k * sizeof(float) + 255) / 256 * 256;
 }
 
 int launch_length_head(const void *hidden, const void *w1, const float *b1, const float *w2, float b2, int32_t N,
@@ -477,18 +516,26 @@ int launch_length_head(const void *hidden, const void *w1, const float *b1, cons
                        void *workspace, size_t workspace_bytes, cudaStream_t st) {
   if (workspace_bytes < length_head_gemm_bytes(N, k, Hp)) return 4;
   int ntiles = 0, NT = 0;
-  int64_t Mpad = 0;
-  head_geometry(N, k, Hp, &ntiles, &NT, &Mpad);
+  head_geometry(Hp, &ntiles, &NT);
   const int64_t M = static_cast<int64_t>(N) * k;
   CUtensorMap mA, mB;
-  if (!make_map(&mA, hidden, M, H, kTM) || !make_map(&mB, w1, Hp, H, NT / kMGroup)) return 2;
+  if (!make_map(&mA, hidden, M, H, kTM) || !make_map(&mB, w1, Hp, H, NT)) return 2;
   HeadArgs a;
-  a.part = static_cast<float *>(workspace);
+  a.s = static_cast<float *>(workspace);
+  a.b1 = b1;
+  a.w2 = w2;
   a.M = static_cast<int32_t>(M);
-  a.Mpad = static_cast<int32_t>(Mpad);
+  a.Hp = Hp;
   a.nkb = (H + kBK - 1) / kBK;
   a.kb_per = (a.nkb + kKSplit - 1) / kKSplit;
   a.NT = NT;
+  a.a_hat = a_hat;
+  a.k_hat = k_hat;
+  a.N = N;
+  a.k = k;
+  a.b2 = b2;
+  a.gamma = gamma;
+  a.fuse = (ntiles == 1 && kBlock % k == 0) ? 1 : 0;
   const size_t smem = static_cast<size_t>(head_smem(NT));
   // the largest launch's shared memory, once per device
   static std::mutex mu;
@@ -504,35 +551,41 @@ int launch_length_head(const void *hidden, const void *w1, const float *b1, cons
       attr_done[dev] = true;
     }
   }
+  // the projection: clusters of the four K quarters of a row tile, a
+  // programmatic dependent of the kernel ahead (its set-up overlaps that
+  // kernel's tail)
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kCluster;
+  attr[0].val.clusterDim.x = kKSplit;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3(static_cast<unsigned>(Mpad / (kTM * kMGroup) * kKSplit * kCluster), static_cast<unsigned>(ntiles), 1);
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>((M + kTM - 1) / kTM * kKSplit), static_cast<unsigned>(ntiles), 1);
   cfg.blockDim = dim3(kMmaThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   void *tm = timer_before("length_head_mma", st);
   cudaError_t e = cudaLaunchKernelEx(&cfg, length_head_mma, mA, mB, a);
   timer_after(tm, st);
   if (e != cudaSuccess) return 1;
-  // the per-request reduction: a programmatic dependent of the projection
+  if (a.fuse) return cudaGetLastError() == cudaSuccess ? 0 : 1;
+  // the per-request finish: a programmatic dependent of the projection
   cudaLaunchConfig_t f = {};
   cudaLaunchAttribute fa[1];
   fa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   fa[0].val.programmaticStreamSerializationAllowed = 1;
-  f.gridDim = dim3(static_cast<unsigned>(N), 1, 1);
-  f.blockDim = dim3(kReduceThreads, 1, 1);
+  f.gridDim = dim3(static_cast<unsigned>((N + 127) / 128), 1, 1);
+  f.blockDim = dim3(128, 1, 1);
   f.stream = st;
   f.attrs = fa;
   f.numAttrs = 1;
-  tm = timer_before("length_head_reduce", st);
-  e = cudaLaunchKernelEx(&f, length_head_reduce, static_cast<const float *>(a.part), b1, w2, b2, k, Hp, a.Mpad, NT,
-                         gamma, a_hat, k_hat);
+  tm = timer_before("length_head_final", st);
+  e = cudaLaunchKernelEx(&f, length_head_final, static_cast<const float *>(a.s), static_cast<int32_t>(ntiles),
+                         a.M, N, k, b2, gamma, a_hat, k_hat);
   timer_after(tm, st);
   if (e != cudaSuccess) return 1;
   return cudaGetLastError() == cudaSuccess ? 0 : 1;
@@ -540,8 +593,19 @@ int launch_length_head(const void *hidden, const void *w1, const float *b1, cons
 
 int launch_length_label(const int32_t *accept_len, const int32_t *cu, const float *a_hat, int32_t N,
                         float *a_star, float *loss, cudaStream_t st) {
-  length_label_kernel<<<(N + 255) / 256, 256, 0, st>>>(accept_len, cu, a_hat, N, a_star, loss);
-  return cudaGetLastError() == cudaSuccess ? 0 : 1;
+  // a programmatic dependent of the kernel ahead (it waits for it first), so
+  // that its launch overlaps that kernel's tail
+  cudaLaunchConfig_t f = {};
+  cudaLaunchAttribute fa[1];
+  fa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  fa[0].val.programmaticStreamSerializationAllowed = 1;
+  f.gridDim = dim3(static_cast<unsigned>((N + 255) / 256), 1, 1);
+  f.blockDim = dim3(256, 1, 1);
+  f.stream = st;
+  f.attrs = fa;
+  f.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&f, length_label_kernel, accept_len, cu, a_hat, N, a_star, loss);
+  return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? 0 : 1;
 }
 
 }  // namespace svw

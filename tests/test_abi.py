@@ -283,17 +283,18 @@ def test_length_head_argument_validation(lib):
     assert call(k=40) == 2                  # above SVW_MAX_LEN
     assert call(h=None) == 1
     assert call(ws=None) == 4
-    assert call(wsb=4096) == 4              # needs 4 x 512 x 32 x 4 bytes
+    assert call(wsb=128) == 4               # needs 64 positions x 4 bytes, rounded up to 256
     assert call(g=0.0) == 1
     assert call(H=60) == 2                  # rows must be 16-byte pitched
     assert call(h=ctypes.c_void_p(p.value + 8)) == 3
-    # fp32 partial products: column tiles x 4 K quarters x positions (rounded up to 256) x tile width
-    assert lib.svw_length_head_workspace_size(256, 16, 256) == 4 * 4096 * 256 * 4
-    assert lib.svw_length_head_workspace_size(3, 5, 300) == 2 * 4 * 512 * 256 * 4
-    assert lib.svw_length_head_workspace_size(5, 16, 40) == 4 * 512 * 64 * 4
+    # one fp32 dot per position and 256-wide column tile of W1, rounded up to 256 bytes
+    assert lib.svw_length_head_workspace_size(256, 16, 256) == 4096 * 4
+    assert lib.svw_length_head_workspace_size(3, 5, 300) == 256
+    assert lib.svw_length_head_workspace_size(5, 16, 40) == 512
+    assert lib.svw_length_head_workspace_size(40, 13, 600) == 6400  # 3 tiles x 520 x 4 = 6240
     assert lib.svw_length_head_workspace_size(0, 16, 256) == 0
     # at most 2^20 positions (N k)
-    assert lib.svw_length_head_workspace_size(1 << 15, 32, 256) == 4 * (1 << 20) * 256 * 4
+    assert lib.svw_length_head_workspace_size(1 << 15, 32, 256) == (1 << 20) * 4
     assert lib.svw_length_head_workspace_size((1 << 15) + 1, 32, 256) == 0
 
 
