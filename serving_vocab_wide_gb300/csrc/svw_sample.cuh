@@ -34,6 +34,13 @@ struct RowConst {
   bool resid;
 };
 
+// [p - q]_+ from log2 p and log2 q (both exp2 evaluated, then a select: the
+// same value as sample_weight's)
+__device__ __forceinline__ float resid_weight(float lp, float lq) {
+  const float d = fmaxf(__fsub_rn(ex2(lp), ex2(lq)), 0.f);
+  return (lq < lp) ? d : 0.f;
+}
+
 // [p - q]_+ (resid) or p
 __device__ __forceinline__ float sample_weight(float y, float z, const RowConst &c) {
   const float lp = __fmaf_rn(y, c.k, c.nT);
@@ -162,15 +169,31 @@ __device__ __noinline__ int32_t cluster_sample(const char *trow, const char *dro
           ry[b] = in ? ld_vec(trow + g * 16) : make_uint4(ninf, ninf, ninf, ninf);
           rz[b] = (in && rc.resid) ? ld_vec(drow + g * 16) : make_uint4(ninf, ninf, ninf, ninf);
         }
+        // log2 p and log2 q two entries at a time (f32x2); the weights and
+        // the group's sum as sample_weight and sample_group form them
+        const float2 k2 = make_float2(rc.k, rc.k), nT2 = make_float2(rc.nT, rc.nT), nD2 = make_float2(rc.nD, rc.nD);
 #pragma unroll
         for (int b = 0; b < B; ++b) {
           const int64_t g = gs + static_cast<int64_t>(r0 + b) * NT + tid;
-          float y[8], z[8];
-          Elem<1>::unpack(ry[b], y);
-          Elem<1>::unpack(rz[b], z);
+          const uint32_t wy[4] = {ry[b].x, ry[b].y, ry[b].z, ry[b].w};
+          const uint32_t wz[4] = {rz[b].x, rz[b].y, rz[b].z, rz[b].w};
           float a = 0.f;
+          if (rc.resid) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) a = __fadd_rn(a, sample_weight(y[e], z[e], rc));
+            for (int h = 0; h < 4; ++h) {
+              const float2 lp = __ffma2_rn(bf16x2_f2(wy[h]), k2, nT2);
+              const float2 lq = __ffma2_rn(bf16x2_f2(wz[h]), k2, nD2);
+              a = __fadd_rn(a, resid_weight(lp.x, lq.x));
+              a = __fadd_rn(a, resid_weight(lp.y, lq.y));
+            }
+          } else {
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const float2 lp = __ffma2_rn(bf16x2_f2(wy[h]), k2, nT2);
+              a = __fadd_rn(a, ex2(lp.x));
+              a = __fadd_rn(a, ex2(lp.y));
+            }
+          }
           ag[b] = a;
           if (a > 0.f) lastg = static_cast<int32_t>(g);
         }
