@@ -463,6 +463,11 @@ struct FastSmem {
   FastPart inbox[2][kMaxCluster];
   FastPart red[16];  // one partial per warp
   FastPart row;      // merged over the cluster
+  // the row's constants, computed once from it (row_ok, any_abort, exact, small in bits)
+  struct {
+    float Ct, dC, kl, loss;
+    int32_t bits;
+  } rk;
   // bonus rows (fused verification) are not exchanged: double-buffered warp
   // partials, merged by the last warp and stored per CTA
   FastPart bred[2][16];
@@ -604,15 +609,25 @@ __global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) 
         for (int o = 16; o > 0; o >>= 1) My = fmaxf(My, __shfl_xor_sync(0xffffffffu, My, o));
         int32_t idx = INT32_MAX;
         if (my == My) {
+          if (DT == 1) {
+            const uint32_t m16 = __float_as_uint(My) >> 16, m2 = m16 | (m16 << 16);
 #pragma unroll
-          for (int j = 0; j < VPT; ++j)
-            if (j < nj && idx == INT32_MAX) {
-              float y[EPV];
-              E::unpack(ty[j], y);
+            for (int j = 0; j < VPT; ++j)
+              if (j < nj && idx == INT32_MAX) {
+                const int e = bf16_vec_find(ty[j], m2);
+                if (e >= 0) idx = static_cast<int32_t>(lo + (tid + j * NT) * EPV + e);
+              }
+          } else {
 #pragma unroll
-              for (int e = EPV - 1; e >= 0; --e)
-                if (y[e] == My) idx = static_cast<int32_t>(lo + (tid + j * NT) * EPV + e);
-            }
+            for (int j = 0; j < VPT; ++j)
+              if (j < nj && idx == INT32_MAX) {
+                float y[EPV];
+                E::unpack(ty[j], y);
+#pragma unroll
+                for (int e = EPV - 1; e >= 0; --e)
+                  if (y[e] == My) idx = static_cast<int32_t>(lo + (tid + j * NT) * EPV + e);
+              }
+          }
         }
         const float nmy = (My == -INFINITY) ? 0.f : -My * k;
         const float2 kk = make_float2(k, k), ny2 = make_float2(nmy, nmy);
@@ -683,19 +698,32 @@ __global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) 
       int32_t idx = INT32_MAX;
       float zx = 0.f;
       if (my == My) {
+        if (DT == 1) {
+          const uint32_t m16 = __float_as_uint(My) >> 16, m2 = m16 | (m16 << 16);  // My is a bf16 value
 #pragma unroll
-        for (int j = 0; j < VPT; ++j)
-          if (j < nj && idx == INT32_MAX) {
-            float y[EPV], z[EPV];
-            E::unpack(ty[j], y);
-            E::unpack(tz[j], z);
-#pragma unroll
-            for (int e = EPV - 1; e >= 0; --e)
-              if (y[e] == My) {
+          for (int j = 0; j < VPT; ++j)
+            if (j < nj && idx == INT32_MAX) {
+              const int e = bf16_vec_find(ty[j], m2);
+              if (e >= 0) {
                 idx = static_cast<int32_t>(lo + (tid + j * NT) * EPV + e);
-                zx = z[e];
+                zx = bf16_vec_get(tz[j], e);
               }
-          }
+            }
+        } else {
+#pragma unroll
+          for (int j = 0; j < VPT; ++j)
+            if (j < nj && idx == INT32_MAX) {
+              float y[EPV], z[EPV];
+              E::unpack(ty[j], y);
+              E::unpack(tz[j], z);
+#pragma unroll
+              for (int e = EPV - 1; e >= 0; --e)
+                if (y[e] == My) {
+                  idx = static_cast<int32_t>(lo + (tid + j * NT) * EPV + e);
+                  zx = z[e];
+                }
+            }
+        }
       }
       const float nmy = (My == -INFINITY) ? 0.f : -My * k;
       const float nmz = (Mz == -INFINITY) ? 0.f : -Mz * k;
@@ -763,30 +791,42 @@ __global__ void __launch_bounds__(NT, 2) opd_fast_kernel(OpdArgs a, OpdGeo geo) 
         Pq.abort = 1;
       }
       const FastPart M = merge_lanes<kMaxCluster>(Pq, k);
-      if (lane == 0) sm.row = M;
+      if (lane == 0) {
+        sm.row = M;
+        // the row's constants, once per CTA (the merged row is the same in
+        // every CTA of the cluster, so these are too)
+        const bool any_abort = M.abort != 0;
+        const float Sz = M.sy + M.w;
+        const bool row_ok = valid && !any_abort && (M.sy > 0.f && M.sy <= FLT_MAX) && (Sz > 0.f && Sz <= FLT_MAX);
+        const float Ct = fmaf(M.my, k, lg2(M.sy));  // log2 p = y k - Ct
+        // log2(S_z / S_y) from the termwise difference w (accurate log1p), and
+        // dC = Cd - Ct: log2 q - log2 p = (z - y) k - dC
+        const float l2r = log1pf(M.w / M.sy) * kLog2e;
+        const float dC = fmaf(M.mz - M.my, k, l2r);
+        // unclipped KL(q||p) = E_q[(z - y) k - (m_z - m_y) k] - log2(S_z / S_y), in nats
+        const float kl = kLn2 * (M.u / Sz - l2r);
+        const bool exact = (kl == kl) && fabsf(kl) <= FLT_MAX;
+        // loss = KL + lambda (-lq[x*]),  -lq[x*] = ln2 ((m_z - z_x*) k + log2 S_z)
+        const float loss_r = fmaf(a.lambda_ce * kLn2, fmaf(M.mz - M.zx, k, lg2(Sz)), kl);
+        const bool small = !(fabsf(loss_r) >= kFastLossFloor);
+        sm.rk.Ct = Ct;
+        sm.rk.dC = dC;
+        sm.rk.kl = kl;
+        sm.rk.loss = loss_r;
+        sm.rk.bits = (row_ok ? 1 : 0) | (any_abort ? 2 : 0) | (exact ? 4 : 0) | (small ? 8 : 0);
+      }
     } else {
       named_arrive(2, NT);
     }
-    __syncthreads();  // the merged row is published
+    __syncthreads();  // the merged row and its constants are published
     const FastPart Rw = sm.row;
-    const bool any_abort = Rw.abort != 0;
-    const float Sz = Rw.sy + Rw.w;
-    const bool row_ok = valid && !any_abort && (Rw.sy > 0.f && Rw.sy <= FLT_MAX) && (Sz > 0.f && Sz <= FLT_MAX);
-    const float Ct = fmaf(Rw.my, k, lg2(Rw.sy));  // log2 p = y k - Ct
-    // log2(S_z / S_y) from the termwise difference w (accurate log1p), and
-    // dC = Cd - Ct: log2 q - log2 p = (z - y) k - dC
-    const float l2r = log1pf(Rw.w / Rw.sy) * kLog2e;
-    const float dC = fmaf(Rw.mz - Rw.my, k, l2r);
+    const int32_t kbits = sm.rk.bits;
+    const bool row_ok = (kbits & 1) != 0, any_abort = (kbits & 2) != 0;
+    const bool exact = (kbits & 4) != 0, small = (kbits & 8) != 0;
+    const float Ct = sm.rk.Ct, dC = sm.rk.dC, kl = sm.rk.kl, loss_r = sm.rk.loss;
     const float Cd = Ct + dC;                     // log2 q = z k - Cd
-    // unclipped KL(q||p) = E_q[(z - y) k - (m_z - m_y) k] - log2(S_z / S_y), in nats
-    const float kl = kLn2 * (Rw.u / Sz - l2r);
     const float c2 = a.clip_c * kLog2e;           // clip bound for t / ln 2
     const int32_t xs = Rw.idx;
-    const bool exact = (kl == kl) && fabsf(kl) <= FLT_MAX;
-    // loss = KL + lambda (-lq[x*]),  -lq[x*] = ln2 ((m_z - z_x*) k + log2 S_z)
-    // (every thread: the merged row is the same in every CTA of the cluster)
-    const float loss_r = fmaf(a.lambda_ce * kLn2, fmaf(Rw.mz - Rw.zx, k, lg2(Sz)), kl);
-    const bool small = !(fabsf(loss_r) >= kFastLossFloor);
     if (rank == 0 && tid == 0) {
       float out = __int_as_float(0x7fffffff);
       float4 rc = make_float4(__int_as_float(0x7fffffff), 0.f, 0.f, 0.f);  // NaN: not a row to fix

@@ -5,6 +5,7 @@
 #pragma once
 #include <cfloat>
 #include <climits>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "svw_device.cuh"
@@ -56,6 +57,27 @@ __device__ __forceinline__ float vec_max(const uint4 &w, float m) {
   }
   return fmaxf(fmaxf(m, fmaxf(__uint_as_float(w.x), __uint_as_float(w.y))),
                fmaxf(__uint_as_float(w.z), __uint_as_float(w.w)));
+}
+
+// The first entry of a 16-byte vector of bf16 values equal to the bf16 value
+// whose bits are m16 in both halves of m2 (float equality: -0 == +0, NaN
+// equals nothing), or -1: four packed compares instead of eight unpacked ones.
+__device__ __forceinline__ int bf16_vec_find(const uint4 &w, uint32_t m2) {
+  const __nv_bfloat162 m = *reinterpret_cast<const __nv_bfloat162 *>(&m2);
+  const uint32_t e0 = __heq2_mask(*reinterpret_cast<const __nv_bfloat162 *>(&w.x), m);
+  const uint32_t e1 = __heq2_mask(*reinterpret_cast<const __nv_bfloat162 *>(&w.y), m);
+  const uint32_t e2 = __heq2_mask(*reinterpret_cast<const __nv_bfloat162 *>(&w.z), m);
+  const uint32_t e3 = __heq2_mask(*reinterpret_cast<const __nv_bfloat162 *>(&w.w), m);
+  if (!(e0 | e1 | e2 | e3)) return -1;
+  const uint32_t f = e0 ? e0 : (e1 ? e1 : (e2 ? e2 : e3));  // the first word with a match
+  const int base = e0 ? 0 : (e1 ? 2 : (e2 ? 4 : 6));
+  return base + ((f & 0xffffu) ? 0 : 1);  // low half: the even entry
+}
+
+// entry e of a 16-byte vector of bf16 values, as a float
+__device__ __forceinline__ float bf16_vec_get(const uint4 &w, int e) {
+  const uint32_t v = (e < 4) ? ((e < 2) ? w.x : w.y) : ((e < 6) ? w.z : w.w);
+  return __uint_as_float((e & 1) ? (v & 0xffff0000u) : (v << 16));
 }
 
 // the elements of a 16-byte vector as float pairs, in index order
