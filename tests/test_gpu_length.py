@@ -110,3 +110,35 @@ def test_label():
     # error is about 2 |a_hat - a*| 2^-24 <= 2.4e-7, absolute
     assert np.all(np.abs(loss[ok] - ref["loss"][ok]) <= 1e-6)
     assert np.all(np.isnan(a_star[~ok])) and np.all(np.isnan(loss[~ok]))
+
+
+@pytest.mark.parametrize("k", [16, 7])
+def test_label_then_head_same_stream(k):
+    """The label of this round reads last round's a_hat while the head that
+    follows it on the same stream (a programmatic launch, which may start
+    before the label ends) writes the new a_hat: the label must see only the
+    old values, whichever finishing path the head takes (k = 16: the
+    projection kernel finishes the requests; k = 7: a second kernel does)."""
+    import torch
+    import serving_vocab_wide_gb300 as svw
+    N, H, Hp = 64, 512, 64
+    h, w1, b1, w2 = _inputs(5 + k, N, k, H, Hp)
+    rng = np.random.default_rng(17 + k)
+    L = rng.integers(1, 17, size=N)
+    cu = np.concatenate([[0], np.cumsum(L)]).astype(np.int32)
+    acc = rng.integers(0, L + 1).astype(np.int32)
+    old = rng.uniform(0, 1, size=N).astype(np.float32)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    hb = t(h.view(np.int16)).view(torch.bfloat16)
+    wb = t(w1.view(np.int16)).view(torch.bfloat16)
+    a_hat = t(old)
+    k_hat = torch.empty(N, dtype=torch.int32, device="cuda")
+    for _ in range(3):  # repeated, so that a late write would show at least once
+        a_hat.copy_(t(old))
+        a_star, loss = svw.length_head_label(t(acc), t(cu), a_hat)
+        svw.length_head(hb, wb, t(b1), t(w2), 0.1, 1.0, a_hat=a_hat, k_hat=k_hat)
+        torch.cuda.synchronize()
+        ref = oracle.length_label(acc, cu, old.astype(np.float64))
+        assert np.all(np.abs(loss.cpu().numpy() - ref["loss"]) <= 1e-6)
+        new = oracle.length_head(h, w1, b1, w2, 0.1, 1.0)
+        assert np.all(np.abs(a_hat.cpu().numpy().astype(np.float64) - new["a_hat"]) <= 1e-4)
