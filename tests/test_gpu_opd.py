@@ -41,7 +41,10 @@ PATHS = pytest.mark.parametrize("exact_only", [False, True], ids=["fast", "exact
 @PATHS
 @pytest.mark.parametrize("V,dtype", [(151936, "bf16"), (1024, "bf16"), (5003, "bf16"),
                                      (1001, "f32"), (4096, "f32"), (8, "bf16"), (151936, "f32"),
-                                     (2048, "bf16"), (129024, "bf16"), (24, "f32")])
+                                     (2048, "bf16"), (129024, "bf16"), (24, "f32"),
+                                     # a 256K vocabulary: wider than the one-pass path, so the
+                                     # exact kernel takes every row on both parametrisations
+                                     (262144, "bf16")])
 def test_paired_rows(V, dtype, exact_only):
     rows = 6
     b = synth.make_batch("opd", seed=V + 1, lengths=np.full(1, rows, np.int32), V=V,

@@ -60,7 +60,9 @@ def test_ragged_wide_vocab_all_requests(T):
 
 
 @pytest.mark.parametrize("V,dtype", [(5003, "bf16"), (1001, "f32"), (8, "bf16"), (1, "f32"),
-                                     (4100, "f32"), (65543, "bf16")])
+                                     (4100, "f32"), (65543, "bf16"),
+                                     # a 256K vocabulary: 15 chunks per row, and the draw's widest rows
+                                     (262144, "bf16")])
 @pytest.mark.parametrize("T", [1.0, 0.0])
 def test_odd_shapes(V, dtype, T):
     lengths = np.array([1, 5, 3, 16], np.int32)
