@@ -16,9 +16,9 @@
 // with the 128-byte swizzle).  A CTA owns a 128-row tile of X and a 256-column
 // tile of W1 (H' <= 256: all of it) over one quarter of K = H, so that 128
 // CTAs share the work at the benchmark's shape; the four K quarters of a row
-// tile form a thread-block cluster.  X tiles come from DRAM (all of them
-// requested into L2 once the first round is on its way) through a five-stage
-// ring, W1 tiles (2 MB in all, read by every row tile: L2 hits) through a
+// tile form a thread-block cluster.  X tiles come from DRAM (the ones beyond
+// the ring's first round requested into L2 once that round is on its way)
+// through a five-stage ring, W1 tiles (2 MB in all, read by every row tile: L2 hits) through a
 // four-stage ring, each fed by its own producer thread; one thread issues the
 // MMAs.  The K quarters are then summed inside the cluster: CTA q
 // of the cluster takes rows [32 q, 32 q + 32) of the tile, and every CTA
